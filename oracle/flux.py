@@ -1,0 +1,364 @@
+"""fp64 CPU oracle of the Flux MMDiT block forward and the rectified-flow loss.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the library imports this module; only
+the tests, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may call it.  It shares no code with
+the CUDA path.  Every function is the plain definition, written in numpy
+float64, in the order the pages give the steps.
+
+Page titles used in citations:
+  * "Flux model API reference" (the API page),
+  * "Flux architecture deep dive" (the architecture page),
+  * "FP8 training for Flux models" (the FP8 page).
+
+Readings taken where the pages are silent or disagree (each is listed in the
+design notes of the repository as well):
+  * RoPE pairs are interleaved ``(x[2j], x[2j+1])`` by default (API page,
+    §Configuration table, ``rotary_interleaved=True``); the half-split pairing
+    ``(x[j], x[j+d/2])`` printed in the architecture page (§3D RoPE
+    mathematics) is available behind ``interleaved=False``.
+  * Frequency index ``i`` runs over ``0 <= i < d_axis/2`` (the printed range
+    ``i = 0..d_axis/2`` has one index too many for a ``d_axis``-wide axis).
+  * QK-RMSNorm is applied per head over ``head_dim`` on q and k, after the QKV
+    bias and before RoPE, with a learned gain and eps 1e-6.
+  * LayerNorm has no affine parameters (the modulation supplies scale/shift),
+    biased variance, eps 1e-6 (API page, §Configuration, layernorm_epsilon).
+  * Every linear has a bias.  The attention output projection is included.
+  * GELU is the exact erf form; the tanh form is behind ``gelu_tanh=True``.
+  * Attention scale is 1/sqrt(head_dim), no mask.
+  * The single block runs attention then MLP in sequence with six modulation
+    chunks, over the whole concatenated sequence, and returns every row.
+  * The output head takes (shift, scale) from a SiLU + linear of ``vec``.
+  * Loss is the mean over all elements.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+LN_EPS = 1e-6
+RMS_EPS = 1e-6
+AXES_DIM = (16, 56, 56)
+THETA = 10000.0
+
+F64 = np.float64
+
+
+def _f64(x):
+    return np.asarray(x, dtype=F64)
+
+
+# ----------------------------------------------------------------------------- 3D RoPE
+def rope_angles(ids, axes_dim=AXES_DIM, theta=THETA):
+    """Per-token rotation angles, ``[..., sum(axes_dim)/2]``.
+
+    Architecture page, §Model components › 2. Position embeddings (3D RoPE)
+    and §Mathematical formulation › 3D RoPE mathematics: for axis ``a`` of
+    width ``d_a`` the frequencies are ``theta^(-2i/d_a)`` for ``i < d_a/2``
+    and the angle is ``pid[a] * theta^(-2i/d_a)``; the three axes' angles are
+    concatenated in axis order.
+    """
+    ids = _f64(ids)
+    parts = []
+    for a, d_a in enumerate(axes_dim):
+        i = np.arange(d_a // 2, dtype=F64)
+        inv_freq = float(theta) ** (-2.0 * i / d_a)
+        parts.append(ids[..., a:a + 1] * inv_freq)
+    return np.concatenate(parts, axis=-1)
+
+
+def rope_cos_sin(ids, axes_dim=AXES_DIM, theta=THETA):
+    ang = rope_angles(ids, axes_dim, theta)
+    return np.cos(ang), np.sin(ang)
+
+
+def apply_rope(x, cos, sin, interleaved=True):
+    """Rotate pairs of ``x[..., d]`` by the angles whose cos/sin are ``[..., d/2]``.
+
+    Interleaved pairs ``(x[2j], x[2j+1])`` (API page, §Configuration,
+    ``rotary_interleaved``); half-split pairs ``(x[j], x[j+d/2])``
+    (architecture page, §3D RoPE mathematics, "RoPE Rotation").  Each pair
+    (a, b) becomes (a cos - b sin, a sin + b cos).
+    """
+    x = _f64(x)
+    d = x.shape[-1]
+    if interleaved:
+        a, b = x[..., 0::2], x[..., 1::2]
+    else:
+        a, b = x[..., : d // 2], x[..., d // 2:]
+    ra = a * cos - b * sin
+    rb = a * sin + b * cos
+    out = np.empty_like(x)
+    if interleaved:
+        out[..., 0::2], out[..., 1::2] = ra, rb
+    else:
+        out[..., : d // 2], out[..., d // 2:] = ra, rb
+    return out
+
+
+# ----------------------------------------------------------------------------- norms, activations
+def layernorm(x, eps=LN_EPS):
+    """LayerNorm over the last axis, biased variance, no affine."""
+    x = _f64(x)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps)
+
+
+def rmsnorm(x, g, eps=RMS_EPS):
+    """API page, §Normalization › RMSNorm: x / sqrt(mean(x^2) + eps) * g."""
+    x = _f64(x)
+    return x / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps) * _f64(g)
+
+
+def silu(x):
+    x = _f64(x)
+    return x / (1.0 + np.exp(-x))
+
+
+_erf = np.vectorize(math.erf, otypes=[F64])
+
+
+def gelu(x, tanh=False):
+    """GELU: x * Phi(x) with the exact normal CDF; or the tanh approximation."""
+    x = _f64(x)
+    if tanh:
+        return 0.5 * x * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (x + 0.044715 * x ** 3)))
+    return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))
+
+
+def linear(x, w, b=None):
+    """y = x W^T + b with W stored [out, in]."""
+    y = _f64(x) @ _f64(w).T
+    return y if b is None else y + _f64(b)
+
+
+# ----------------------------------------------------------------------------- AdaLN
+def modulation(vec, w_mod, b_mod, n_chunks=6):
+    """AdaLN.forward: Linear(SiLU(vec)) split into chunks along the feature axis.
+
+    API page, §Normalization › AdaLN (six chunks named shift, scale, gate,
+    shift_mlp, scale_mlp, gate_mlp, in that order); architecture page,
+    §Implementation details › Adaptive layer normalization.
+    """
+    m = linear(silu(vec), w_mod, b_mod)  # [B, n*D]
+    return np.split(m, n_chunks, axis=-1)
+
+
+def modulate(x, shift, scale, eps=LN_EPS):
+    """AdaLN.modulate: LayerNorm(x) * (1 + scale) + shift, shift/scale per batch row."""
+    return layernorm(x, eps) * (1.0 + _f64(scale)[:, None, :]) + _f64(shift)[:, None, :]
+
+
+def gated_residual(x, gate, y):
+    """AdaLN.scale_add: x + gate * y, gate per batch row."""
+    return _f64(x) + _f64(gate)[:, None, :] * _f64(y)
+
+
+# ----------------------------------------------------------------------------- attention
+def attention(q, k, v):
+    """softmax(q k^T / sqrt(d)) v over the key axis, no mask.  q,k,v: [..., S, d].
+
+    Architecture page, §Implementation details › Attention implementation
+    (no mask) and › Joint Attention Trick (one call over the joint sequence).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    d = q.shape[-1]
+    s = (q @ np.swapaxes(k, -1, -2)) / math.sqrt(d)
+    s = s - s.max(axis=-1, keepdims=True)
+    p = np.exp(s)
+    p = p / p.sum(axis=-1, keepdims=True)
+    return p @ v
+
+
+# ----------------------------------------------------------------------------- block pieces
+def _heads(x, heads):
+    """[B, S, H*d] -> [B, H, S, d] (column h*d + j is head h, element j)."""
+    B, S, HD = x.shape
+    return x.reshape(B, S, heads, HD // heads).transpose(0, 2, 1, 3)
+
+
+def _merge(x):
+    """[B, H, S, d] -> [B, S, H*d]."""
+    B, H, S, d = x.shape
+    return x.transpose(0, 2, 1, 3).reshape(B, S, H * d)
+
+
+def qkv_heads(x, shift, scale, w, heads, ln_eps=LN_EPS, rms_eps=RMS_EPS):
+    """Attention-branch pre-norm and projection of one stream, before RoPE.
+
+    Architecture page, §3. MMDiT layer (double block), steps 1-2:
+    AdaLN-modulated LayerNorm, then the QKV linear (with bias); then per-head
+    RMSNorm of q and k.  Returns q, k, v as [B, H, S, d].
+    """
+    h = modulate(x, shift, scale, ln_eps)
+    qkv = linear(h, w["w_qkv"], w["b_qkv"])
+    q, k, v = np.split(qkv, 3, axis=-1)
+    q = rmsnorm(_heads(q, heads), w["g_q"], rms_eps)
+    k = rmsnorm(_heads(k, heads), w["g_k"], rms_eps)
+    return q, k, _heads(v, heads)
+
+
+def mlp_branch(x, shift, scale, w, gelu_tanh=False, ln_eps=LN_EPS):
+    """Architecture page, §3. MMDiT layer, step 4: AdaLN -> Linear -> GELU -> Linear."""
+    h = modulate(x, shift, scale, ln_eps)
+    return linear(gelu(linear(h, w["w_1"], w["b_1"]), gelu_tanh), w["w_2"], w["b_2"])
+
+
+def double_block(x_img, x_txt, vec, cos, sin, w_img, w_txt, heads,
+                 interleaved=True, gelu_tanh=False, ln_eps=LN_EPS, rms_eps=RMS_EPS):
+    """Double-stream (joint) block forward.
+
+    Architecture page, §Model components › 3. MMDiT layer (double block);
+    API page, §Layer specifications › MMDiTLayer.  ``cos``/``sin`` are
+    ``[B, S_img + S_txt, d/2]`` in the joint order [image; text].
+    Returns (y_img, y_txt).
+    """
+    S_i = np.shape(x_img)[1]
+    mi = modulation(vec, w_img["w_mod"], w_img["b_mod"])
+    mt = modulation(vec, w_txt["w_mod"], w_txt["b_mod"])
+    qi, ki, vi = qkv_heads(x_img, mi[0], mi[1], w_img, heads, ln_eps, rms_eps)
+    qt, kt, vt = qkv_heads(x_txt, mt[0], mt[1], w_txt, heads, ln_eps, rms_eps)
+    q = np.concatenate([qi, qt], axis=2)
+    k = np.concatenate([ki, kt], axis=2)
+    v = np.concatenate([vi, vt], axis=2)
+    c, s = _f64(cos)[:, None], _f64(sin)[:, None]
+    q = apply_rope(q, c, s, interleaved)
+    k = apply_rope(k, c, s, interleaved)
+    o = _merge(attention(q, k, v))
+    o_img, o_txt = o[:, :S_i], o[:, S_i:]
+    x_img = gated_residual(x_img, mi[2], linear(o_img, w_img["w_o"], w_img["b_o"]))
+    x_txt = gated_residual(x_txt, mt[2], linear(o_txt, w_txt["w_o"], w_txt["b_o"]))
+    x_img = gated_residual(x_img, mi[5], mlp_branch(x_img, mi[3], mi[4], w_img, gelu_tanh, ln_eps))
+    x_txt = gated_residual(x_txt, mt[5], mlp_branch(x_txt, mt[3], mt[4], w_txt, gelu_tanh, ln_eps))
+    return x_img, x_txt
+
+
+def single_block(x, vec, cos, sin, w, heads, interleaved=True, gelu_tanh=False,
+                 ln_eps=LN_EPS, rms_eps=RMS_EPS):
+    """Single-stream block forward over the concatenated sequence ``x = [img; txt]``.
+
+    Architecture page, §Model components › 4. Flux single block: AdaLN,
+    QKV, attention, gated residual, AdaLN, MLP, gated residual, all with one
+    weight set.  Returns all rows (the caller keeps the image rows after the
+    last single block).
+    """
+    m = modulation(vec, w["w_mod"], w["b_mod"])
+    q, k, v = qkv_heads(x, m[0], m[1], w, heads, ln_eps, rms_eps)
+    c, s = _f64(cos)[:, None], _f64(sin)[:, None]
+    q = apply_rope(q, c, s, interleaved)
+    k = apply_rope(k, c, s, interleaved)
+    o = _merge(attention(q, k, v))
+    x = gated_residual(x, m[2], linear(o, w["w_o"], w["b_o"]))
+    return gated_residual(x, m[5], mlp_branch(x, m[3], m[4], w, gelu_tanh, ln_eps))
+
+
+# ----------------------------------------------------------------------------- row-sampled blocks
+def _rows_after_attention(x_rows, o_rows, m, w, gelu_tanh, ln_eps):
+    x1 = gated_residual(x_rows, m[2], linear(o_rows, w["w_o"], w["b_o"]))
+    return gated_residual(x1, m[5], mlp_branch(x1, m[3], m[4], w, gelu_tanh, ln_eps))
+
+
+def _attend_rows(q_rows, k, v, c_rows, s_rows, c_all, s_all, interleaved):
+    q = apply_rope(q_rows, c_rows[:, None], s_rows[:, None], interleaved)
+    kk = apply_rope(k, c_all[:, None], s_all[:, None], interleaved)
+    return _merge(attention(q, kk, v))
+
+
+def double_block_rows(x_img, x_txt, vec, cos, sin, w_img, w_txt, heads, rows_img, rows_txt,
+                      interleaved=True, gelu_tanh=False, ln_eps=LN_EPS, rms_eps=RMS_EPS):
+    """The double block's output at selected rows only (same batch rows for every sample).
+
+    Keys and values need every token; queries, attention, the output
+    projection and the MLP are row-wise, so computing them for a subset of
+    rows gives those rows of ``double_block`` exactly.
+    """
+    S_i = np.shape(x_img)[1]
+    mi = modulation(vec, w_img["w_mod"], w_img["b_mod"])
+    mt = modulation(vec, w_txt["w_mod"], w_txt["b_mod"])
+    # keys/values for every token (queries are recomputed only for the chosen rows)
+    _, ki, vi = qkv_heads(x_img, mi[0], mi[1], w_img, heads, ln_eps, rms_eps)
+    _, kt, vt = qkv_heads(x_txt, mt[0], mt[1], w_txt, heads, ln_eps, rms_eps)
+    k = np.concatenate([ki, kt], axis=2)
+    v = np.concatenate([vi, vt], axis=2)
+    cos, sin = _f64(cos), _f64(sin)
+    rows_img = np.asarray(rows_img)
+    rows_txt = np.asarray(rows_txt)
+    qi, _, _ = qkv_heads(_f64(x_img)[:, rows_img], mi[0], mi[1], w_img, heads, ln_eps, rms_eps)
+    qt, _, _ = qkv_heads(_f64(x_txt)[:, rows_txt], mt[0], mt[1], w_txt, heads, ln_eps, rms_eps)
+    jr_i, jr_t = rows_img, S_i + rows_txt
+    oi = _attend_rows(qi, k, v, cos[:, jr_i], sin[:, jr_i], cos, sin, interleaved)
+    ot = _attend_rows(qt, k, v, cos[:, jr_t], sin[:, jr_t], cos, sin, interleaved)
+    yi = _rows_after_attention(_f64(x_img)[:, rows_img], oi, mi, w_img, gelu_tanh, ln_eps)
+    yt = _rows_after_attention(_f64(x_txt)[:, rows_txt], ot, mt, w_txt, gelu_tanh, ln_eps)
+    return yi, yt
+
+
+def single_block_rows(x, vec, cos, sin, w, heads, rows, interleaved=True, gelu_tanh=False,
+                      ln_eps=LN_EPS, rms_eps=RMS_EPS):
+    """The single block's output at selected rows only (see ``double_block_rows``)."""
+    m = modulation(vec, w["w_mod"], w["b_mod"])
+    _, k, v = qkv_heads(x, m[0], m[1], w, heads, ln_eps, rms_eps)
+    rows = np.asarray(rows)
+    q, _, _ = qkv_heads(_f64(x)[:, rows], m[0], m[1], w, heads, ln_eps, rms_eps)
+    cos, sin = _f64(cos), _f64(sin)
+    o = _attend_rows(q, k, v, cos[:, rows], sin[:, rows], cos, sin, interleaved)
+    return _rows_after_attention(_f64(x)[:, rows], o, m, w, gelu_tanh, ln_eps)
+
+
+# ----------------------------------------------------------------------------- embeddings and head
+def patchify(z):
+    """[B, C, H, W] -> [B, H*W, C] with patch size 1 (architecture page, §Memory layout)."""
+    z = _f64(z)
+    B, C, H, W = z.shape
+    return z.reshape(B, C, H * W).transpose(0, 2, 1)
+
+
+def unpatchify(tokens, H, W):
+    """[B, H*W, C] -> [B, C, H, W]."""
+    t = _f64(tokens)
+    B, S, C = t.shape
+    return t.transpose(0, 2, 1).reshape(B, C, H, W)
+
+
+def img_in(z, w, b):
+    """Image path: patchify, then Linear C -> D (architecture page, §1. Input embeddings)."""
+    return linear(patchify(z), w, b)
+
+
+def txt_in(txt, w, b):
+    """Text path: Linear ctx_dim -> D (architecture page, §1. Input embeddings)."""
+    return linear(txt, w, b)
+
+
+def final_layer(x_img, vec, w_ada, b_ada, w_out, b_out, H, W, ln_eps=LN_EPS):
+    """Output head: AdaLNContinuous(vec), Linear D -> C, reshape to [B, C, H, W].
+
+    Architecture page, §Model components › 5. Output processing; API page,
+    §Normalization › AdaLNContinuous.  (shift, scale) = SiLU(vec) W^T + b.
+    """
+    shift, scale = modulation(vec, w_ada, b_ada, 2)
+    y = linear(modulate(x_img, shift, scale, ln_eps), w_out, b_out)
+    return unpatchify(y, H, W)
+
+
+# ----------------------------------------------------------------------------- rectified flow
+def flow_match_noise(z0, z1, t):
+    """z_t = (1 - t) z0 + t z1, t per sample (architecture page, §Flow matching objective;
+    API page, §Noise application › apply_flow_matching_noise)."""
+    z0, z1 = _f64(z0), _f64(z1)
+    tt = _f64(t).reshape((-1,) + (1,) * (z0.ndim - 1))
+    return (1.0 - tt) * z0 + tt * z1
+
+
+def flow_match_target(z0, z1):
+    """Velocity target v* = z1 - z0 (architecture page, §Flow matching objective)."""
+    return _f64(z1) - _f64(z0)
+
+
+def flow_match_loss(pred, z0, z1):
+    """MSE(pred, z1 - z0), mean over all elements (API page, §Loss computation ›
+    compute_flow_matching_loss)."""
+    diff = _f64(pred) - flow_match_target(z0, z1)
+    return float(np.mean(diff * diff))
