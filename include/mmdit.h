@@ -1,0 +1,235 @@
+/*
+ * mmdit.h -- C ABI of the GB300 (sm_103a) Flux MMDiT block-forward library (libmmdit.so).
+ *
+ * The library computes, with hand-written CUDA kernels for sm_103a, the forward pass of the
+ * Flux double-stream (joint) block and single-stream block, their input embeddings and output
+ * head, the 3D RoPE tables, and the rectified-flow noise / velocity target / MSE loss.
+ *
+ * Sources (page title, section):
+ *   [API]  "Flux model API reference"
+ *   [ARCH] "Flux architecture deep dive"
+ *   [FP8]  "FP8 training for Flux models"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is DEVICE memory owned by the caller, except `dims`, the weight-set
+ *    structs and `axes_dim`, which are host memory read during the call.  The library
+ *    allocates no device memory and keeps no device state between calls.
+ *  - Calls are asynchronous: kernels are enqueued on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and the call returns without synchronising.
+ *  - Layouts are row-major.  Activations are token-major [B, S, features].  Linear weights are
+ *    [out, in] (y = x W^T + b).  The QKV weight is [3D, D] as q|k|v blocks, each head-major
+ *    (column h*head_dim + j is head h, element j).
+ *  - Element types: `act` selects fp32 (MMDIT_F32: linears on tf32 tensor cores) or bf16
+ *    (MMDIT_BF16).  Activations, weights, biases, gains and `vec` all use the `act` type.
+ *    RoPE tables, modulation vectors, timesteps and the loss are fp32.
+ *  - Every device pointer must be 16-byte aligned.  Row strides are the dense ones implied by
+ *    the shapes; feature widths must be multiples of 8 elements so that rows fed to the
+ *    tensor-memory-access (TMA) engine start on 16-byte boundaries.
+ *  - Workspaces: entry points that take `workspace` need at least the bytes the matching
+ *    *_workspace_size function returns, 256-byte aligned.  The first 256 bytes hold a device
+ *    status word that the call clears on entry; kernels with bounded waits set bits there if a
+ *    wait gives up (they then return early and the outputs are undefined).  Read it with
+ *    mmdit_workspace_status after the stream has run.
+ *  - Errors: argument problems return MMDIT_ERR_INVALID_ARG, shapes or modes this build does
+ *    not implement return MMDIT_ERR_UNSUPPORTED, a short workspace returns
+ *    MMDIT_ERR_WORKSPACE -- all before anything is enqueued.  A failed CUDA call or launch
+ *    returns MMDIT_ERR_CUDA.  mmdit_last_error() gives a message for the calling thread's last
+ *    failure.
+ *  - Aliasing: outputs must not alias inputs unless an entry point says otherwise.
+ */
+#ifndef MMDIT_H_
+#define MMDIT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mmdit_status {
+  MMDIT_OK = 0,
+  MMDIT_ERR_INVALID_ARG = 1,
+  MMDIT_ERR_UNSUPPORTED = 2,
+  MMDIT_ERR_WORKSPACE = 3,
+  MMDIT_ERR_CUDA = 4,
+  MMDIT_ERR_NONFINITE = 5,
+  MMDIT_ERR_DEVICE = 6 /* a kernel's bounded wait gave up; see mmdit_workspace_status */
+} mmdit_status;
+
+typedef enum mmdit_act_dtype { MMDIT_F32 = 0, MMDIT_BF16 = 1 } mmdit_act_dtype;
+
+/* Linear-layer arithmetic: NATIVE = tf32 for MMDIT_F32, bf16 for MMDIT_BF16.
+ * FP8_E4M3 = E4M3 operands with delayed per-tensor scaling ([FP8] §Configuration). */
+typedef enum mmdit_gemm_mode { MMDIT_GEMM_NATIVE = 0, MMDIT_GEMM_FP8_E4M3 = 1 } mmdit_gemm_mode;
+
+/* Shapes and options of one block call ([API] §Configuration, FluxConfig). */
+typedef struct mmdit_dims {
+  int32_t batch;      /* B */
+  int32_t seq_img;    /* image tokens S_i */
+  int32_t seq_txt;    /* text tokens S_t; the joint sequence is [image; text], S = S_i + S_t */
+  int32_t hidden;     /* D = heads * head_dim; multiple of 256 */
+  int32_t heads;      /* H */
+  int32_t head_dim;   /* d; must be 128 */
+  int32_t mlp_hidden; /* F; multiple of 256 */
+  float ln_eps;       /* LayerNorm eps (1e-6, [API] §Configuration layernorm_epsilon) */
+  float rms_eps;      /* QK-RMSNorm eps (1e-6) */
+  int32_t rope_interleaved; /* 1: pairs (2j, 2j+1) ([API] rotary_interleaved); 0: (j, j+d/2) */
+  int32_t gelu_tanh;  /* 0: exact erf GELU; 1: tanh approximation */
+  int32_t act;        /* mmdit_act_dtype */
+  int32_t gemm;       /* mmdit_gemm_mode */
+} mmdit_dims;
+
+/* One stream's weights ([ARCH] §Model components, 3. MMDiT layer).  All device pointers of
+ * element type `act`.  Shapes: w_mod [6D, D], b_mod [6D] (AdaLN chunks in the order shift,
+ * scale, gate, shift_mlp, scale_mlp, gate_mlp -- [API] §Normalization, AdaLN); w_qkv [3D, D],
+ * b_qkv [3D]; g_q, g_k [d] (per-head QK-RMSNorm gains); w_o [D, D], b_o [D] (attention output
+ * projection); w_1 [F, D], b_1 [F]; w_2 [D, F], b_2 [D] (GELU MLP). */
+typedef struct mmdit_stream_w {
+  const void *w_mod, *b_mod;
+  const void *w_qkv, *b_qkv;
+  const void *g_q, *g_k;
+  const void *w_o, *b_o;
+  const void *w_1, *b_1;
+  const void *w_2, *b_2;
+} mmdit_stream_w;
+
+/* FP8 delayed-scaling state, caller-owned device memory ([FP8] §Configuration: history 1024,
+ * most_recent, margin 0).  Reserved: MMDIT_GEMM_FP8_E4M3 returns MMDIT_ERR_UNSUPPORTED in this
+ * build; pass NULL with MMDIT_GEMM_NATIVE. */
+typedef struct mmdit_fp8_state {
+  float *amax_history; /* [n_tensors, hist_len] */
+  float *scale;        /* [n_tensors] */
+  int32_t hist_len;
+  int32_t n_tensors;
+  int32_t pos;
+} mmdit_fp8_state;
+
+/* Message for the calling thread's most recent non-OK status (never NULL). */
+const char *mmdit_last_error(void);
+
+/* Synchronises `stream`, reads the status word of `workspace` and clears it.  Returns MMDIT_OK,
+ * MMDIT_ERR_DEVICE if a kernel recorded a timed-out wait (bits in *bits_out if non-NULL), or
+ * MMDIT_ERR_CUDA. */
+mmdit_status mmdit_workspace_status(void *workspace, uint32_t *bits_out, void *stream);
+
+/* Number of the library's own kernel launches enqueued by this thread since the last reset
+ * (a diagnostic count used by benchmarks); mmdit_launch_count_reset() sets it to zero. */
+uint64_t mmdit_launch_count(void);
+void mmdit_launch_count_reset(void);
+
+/* ---------------------------------------------------------------------------------------
+ * 3D RoPE tables ([ARCH] §Model components, 2. Position embeddings (3D RoPE), and
+ * §Mathematical formulation, 3D RoPE mathematics; [API] §Position embeddings, EmbedND).
+ * For token ids p = ids[b, s, 0..2] and axis a of width axes_dim[a] (even), pair i < axes_dim[a]/2
+ * gets angle p[a] * theta^(-2i/axes_dim[a]); the axes' angles are concatenated in axis order.
+ *   ids      [batch, seq, 3] fp32 (device)
+ *   axes_dim host int32[3], each even, sum <= 256 (Flux: 16, 56, 56)
+ *   cos_out, sin_out [batch, seq, P] fp32 (device), P = sum(axes_dim)/2
+ * No workspace.  batch*seq == 0 is a no-op. */
+mmdit_status rope3d_freqs(const float *ids, int32_t batch, int32_t seq, const int32_t *axes_dim,
+                          float theta, float *cos_out, float *sin_out, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Rectified flow ([ARCH] §Mathematical formulation, Flow matching objective; [API] §Training
+ * utilities, apply_flow_matching_noise and compute_flow_matching_loss).
+ *   z_t  = (1 - t[b]) * z0 + t[b] * z1                        (written if z_t != NULL)
+ *   loss = mean over all batch*n elements of (pred - (z1 - z0))^2   (written if pred and
+ *          loss are both non-NULL; one fp32 scalar; fixed-order, deterministic reduction)
+ * z0, z1, z_t, pred: [batch, n_per_sample] of type `dtype` (MMDIT_F32 or MMDIT_BF16);
+ * n_per_sample a multiple of 8.  t: [batch] fp32.
+ * workspace >= flow_match_workspace_size(batch, n_per_sample) (per-block partial sums).
+ * z_t may alias z0 or z1 only when no loss is requested. */
+size_t flow_match_workspace_size(int32_t batch, int64_t n_per_sample);
+mmdit_status flow_match_noise_and_loss(int32_t dtype, const void *z0, const void *z1,
+                                       const float *t, int32_t batch, int64_t n_per_sample,
+                                       void *z_t, const void *pred, float *loss,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Plain linear layer y = x W^T + b on the tensor cores (the text embedding txt_in of [ARCH]
+ * §Model components, 1. Input embeddings, and any other projection).
+ *   x [M, K], w [N, K], b [N] (may be NULL), y [M, N]; element type `act`.
+ *   N multiple of 32, K multiple of 8.  workspace >= mmdit_linear_workspace_size(). */
+size_t mmdit_linear_workspace_size(void);
+mmdit_status mmdit_linear_fwd(int32_t act, int32_t M, int32_t N, int32_t K, const void *x,
+                              const void *w, const void *b, void *y, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
+/* Image embedding img_in ([ARCH] §Model components, 1. Input embeddings, and §Implementation
+ * details, Memory layout): patchify latents [B, C, H, W] (fp32, patch size 1, token r*W + c)
+ * into [B, H*W, C] and project with w [D, C], b [D] to out [B, H*W, D] (type `act`).
+ * C multiple of 8. */
+size_t mmdit_img_in_workspace_size(int32_t act, int32_t batch, int32_t channels, int32_t lat_h,
+                                   int32_t lat_w);
+mmdit_status mmdit_img_in_fwd(int32_t act, int32_t batch, int32_t channels, int32_t lat_h,
+                              int32_t lat_w, int32_t hidden, const float *z, const void *w,
+                              const void *b, void *out, void *workspace, size_t workspace_bytes,
+                              void *stream);
+
+/* Output head ([ARCH] §Model components, 5. Output processing; [API] AdaLNContinuous):
+ * (shift, scale) = SiLU(vec) w_ada^T + b_ada (w_ada [2D, D]); y = (LN(x_img) * (1 + scale) +
+ * shift) w_out^T + b_out (w_out [C, D]); pred [B, C, H, W] fp32 with token r*W + c at [.., r, c].
+ * Uses dims->batch, hidden, ln_eps, act; x_img is [B, lat_h*lat_w, D].  C multiple of 32. */
+size_t mmdit_final_layer_workspace_size(const mmdit_dims *dims, int32_t channels);
+mmdit_status mmdit_final_layer_fwd(const mmdit_dims *dims, int32_t channels, int32_t lat_h,
+                                   int32_t lat_w, const void *x_img, const void *vec,
+                                   const void *w_ada, const void *b_ada, const void *w_out,
+                                   const void *b_out, float *pred, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Joint softmax attention ([ARCH] §Implementation details, Attention implementation (no mask)
+ * and Joint Attention Trick).  out[b, s, h*d + j] = sum_t softmax_t(q_s . k_t / sqrt(d)) v_t[j]
+ * for each (b, h), over all S keys.  q, k, v [B, H, S, d] bf16; out [B, S, H*d] of type
+ * `act`.  d must be 128.  workspace >= mmdit_attention_workspace_size(B, H, S). */
+size_t mmdit_attention_workspace_size(int32_t batch, int32_t heads, int32_t seq);
+mmdit_status mmdit_attention_fwd(int32_t act, int32_t batch, int32_t heads, int32_t seq,
+                                 int32_t head_dim, const void *q, const void *k, const void *v,
+                                 void *out, void *workspace, size_t workspace_bytes,
+                                 void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Double-stream (joint) block forward ([ARCH] §Model components, 3. MMDiT layer (double
+ * block); [API] §Layer specifications, MMDiTLayer).  Per stream s in {img, txt}, each with its
+ * own weights:
+ *   (shift1, scale1, gate1, shift2, scale2, gate2) = SiLU(vec) w_mod^T + b_mod;
+ *   h = LN(x_s) * (1 + scale1) + shift1;   q|k|v = h w_qkv^T + b_qkv;
+ *   q, k <- per-head RMSNorm (gains g_q, g_k), then RoPE with the joint-sequence tables;
+ *   O = softmax(Q K^T / sqrt(d)) V over the joint sequence [img; txt];
+ *   x1 = x_s + gate1 * (O_s w_o^T + b_o);
+ *   y_s = x1 + gate2 * (GELU((LN(x1) * (1 + scale2) + shift2) w_1^T + b_1) w_2^T + b_2).
+ * vec [B, D]; rope_cos, rope_sin [B, S_i + S_t, d/2] fp32 (rope3d_freqs of the joint ids);
+ * x_img, y_img [B, S_i, D]; x_txt, y_txt [B, S_t, D]; y may alias x.
+ * fp8: NULL (reserved).  workspace >= mmdit_double_block_workspace_size(dims). */
+size_t mmdit_double_block_workspace_size(const mmdit_dims *dims);
+mmdit_status mmdit_double_block_fwd(const mmdit_dims *dims, const mmdit_stream_w *w_img,
+                                    const mmdit_stream_w *w_txt, const void *vec,
+                                    const float *rope_cos, const float *rope_sin,
+                                    const void *x_img, const void *x_txt, void *y_img,
+                                    void *y_txt, mmdit_fp8_state *fp8, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+/* Single-stream block forward ([ARCH] §Model components, 4. Flux single block; [API]
+ * FluxSingleTransformerBlock): the same chain with one weight set over the whole concatenated
+ * sequence x [B, S, D], S = S_i + S_t; returns all S rows in y (may alias x).
+ * rope_cos, rope_sin [B, S, d/2].  workspace >= mmdit_single_block_workspace_size(dims). */
+size_t mmdit_single_block_workspace_size(const mmdit_dims *dims);
+mmdit_status mmdit_single_block_fwd(const mmdit_dims *dims, const mmdit_stream_w *w,
+                                    const void *vec, const float *rope_cos,
+                                    const float *rope_sin, const void *x, void *y,
+                                    mmdit_fp8_state *fp8, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+/* Byte offsets of named intermediates inside a block workspace, for inspection by tests:
+ * out[0..9] = mod_img, mod_txt, Q, K, Vt, O_img, O_txt, x1_img, x1_txt, u_img (a single block
+ * uses the *_img slots; unused slots are -1).  Q, K are [B, H, S, d] bf16, Vt is [B, H, d,
+ * S_pad] bf16 with S_pad = S rounded up to 8.  Returns the count written or -1 on bad dims. */
+int32_t mmdit_block_workspace_offsets(const mmdit_dims *dims, int32_t single, int64_t *out,
+                                      int32_t n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MMDIT_H_ */
