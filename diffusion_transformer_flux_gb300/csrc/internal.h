@@ -1,0 +1,111 @@
+// internal.h -- interfaces between the library's translation units (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mmdit {
+
+// Epilogues of the tensor-core GEMM  C[M, N] = A[M, K] * W[N, K]^T (fp32 accumulation).
+enum EpiKind : int {
+  kEpiBias = 0,       // out[m, n] = acc + bias[n]
+  kEpiGelu = 1,       // out[m, n] = GELU(acc + bias[n])
+  kEpiGateResid = 2,  // out[m, n] = resid[m, n] + gate[b(m), n] * (acc + bias[n])
+  kEpiQkv = 3,        // bias, per-head RMSNorm of q and k, RoPE, scatter to Q, K, Vt
+  kEpiUnpatchify = 4  // pred[b, n, s] (fp32) = acc + bias[n], m = b * rows_per_batch + s
+};
+
+struct EpiArgs {
+  const void* bias = nullptr;  // [N], activation type, may be null
+  void* out = nullptr;         // [M, N] activation type (fp32 [B, N, rows_per_batch] for unpatchify)
+  const void* resid = nullptr; // [M, N] (gated residual)
+  const float* gate = nullptr; // gate for batch b at gate + b * gate_bstride
+  int64_t gate_bstride = 0;
+  int rows_per_batch = 1;      // m -> (b = m / rows_per_batch, s = m % rows_per_batch)
+  int gelu_tanh = 0;
+  // QKV scatter
+  const void* g_q = nullptr;   // [128] activation type
+  const void* g_k = nullptr;
+  const float* rope_cos = nullptr;  // [B, seq_joint, 64]
+  const float* rope_sin = nullptr;
+  __nv_bfloat16* q = nullptr;  // [B, H, seq_joint, 128]
+  __nv_bfloat16* k = nullptr;
+  __nv_bfloat16* vt = nullptr; // [B, H, 128, seq_pad]
+  int seq_offset = 0;          // joint index of this stream's token 0
+  int seq_joint = 0;
+  int seq_pad = 0;
+  int heads = 0;
+  int hidden = 0;
+  float rms_eps = 1e-6f;
+  int rope_interleaved = 1;
+};
+
+struct GemmProblem {
+  int act = 1;           // 0 = fp32 operands (tf32 MMA), 1 = bf16
+  int epi = kEpiBias;
+  int M = 0, N = 0, K = 0;
+  const void* A = nullptr;  // [M, K]
+  const void* W = nullptr;  // [N, K]
+  EpiArgs ep;
+};
+
+// Device status word layout: the first 4 bytes of every workspace.
+constexpr size_t kStatusBytes = 256;
+
+// Launch accounting for diagnostics.
+void count_launch(int n = 1);
+
+// Number of SMs of the current device.
+int num_sms();
+
+// Tensor-map encoding through the driver entry point (no link-time libcuda dependency).
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle);
+
+// gemm_bf16.cu / gemm_tf32.cu
+cudaError_t launch_gemm_bf16(const GemmProblem& p, uint32_t* status, cudaStream_t stream);
+cudaError_t launch_gemm_tf32(const GemmProblem& p, uint32_t* status, cudaStream_t stream);
+inline cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream) {
+  return p.act == 1 ? launch_gemm_bf16(p, status, stream) : launch_gemm_tf32(p, status, stream);
+}
+
+// attention.cu: O = softmax(Q K^T / sqrt(128)) V per (b, h); rows [0, split) of each batch go
+// to out0 ([B, split, H*128]), rows [split, S) to out1 ([B, S - split, H*128]).
+struct AttnProblem {
+  int act = 1;  // output type: 0 fp32, 1 bf16
+  int batch = 0, heads = 0, seq = 0, seq_pad = 0, split = 0;
+  const __nv_bfloat16* q = nullptr;   // [B, H, S, 128]
+  const __nv_bfloat16* k = nullptr;   // [B, H, S, 128]
+  const __nv_bfloat16* vt = nullptr;  // [B, H, 128, seq_pad]
+  void* out0 = nullptr;
+  void* out1 = nullptr;
+};
+cudaError_t launch_attention(const AttnProblem& p, uint32_t* status, cudaStream_t stream);
+
+// elementwise.cu
+cudaError_t launch_rope3d(const float* ids, int batch, int seq, const int axes[3], float theta,
+                          float* cos_out, float* sin_out, cudaStream_t stream);
+// m[b, n] = sum_k SiLU(vec[b, k]) w[n, k] + bias[n], n < rows, k < dim; m fp32 [B, rows].
+cudaError_t launch_modulation(int act, const void* vec, const void* w, const void* bias, int batch,
+                              int rows, int dim, float* m, cudaStream_t stream);
+// out[r, :] = LN(x[r, :]) * (1 + scale[b]) + shift[b], b = r / rows_per_batch; x, out [R, D].
+cudaError_t launch_ln_modulate(int act, const void* x, const float* shift, const float* scale,
+                               int64_t mod_bstride, int rows, int rows_per_batch, int dim, float eps,
+                               void* out, cudaStream_t stream);
+// z [B, C, HW] fp32 -> tokens [B, HW, C] of the activation type.
+cudaError_t launch_patchify(int act, const float* z, int batch, int channels, int hw, void* out,
+                            cudaStream_t stream);
+// v [B, H, S, 128] -> vt [B, H, 128, seq_pad]
+cudaError_t launch_transpose_v(const __nv_bfloat16* v, int bh, int seq, int seq_pad,
+                               __nv_bfloat16* vt, cudaStream_t stream);
+// Rectified-flow noise and loss.
+int flow_partial_blocks(int64_t n_total);
+cudaError_t launch_flow_match(int dtype, const void* z0, const void* z1, const float* t, int batch,
+                              int64_t n_per_sample, void* z_t, const void* pred, float* loss,
+                              float* partials, int n_partials, cudaStream_t stream);
+
+}  // namespace mmdit
