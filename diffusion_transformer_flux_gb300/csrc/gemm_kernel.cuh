@@ -226,4 +226,201 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t taddr, int m, int n0, int
   }
 }
 
+
+// ----------------------------------------------------------------------------- kernel
+template <int KIND, int BN, int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   int M, int N, int K, EpiArgs ep, uint32_t* status) {
+  using Cfg = GemmCfg<BN>;
+  using T = typename KindTraits<KIND>::T;
+  constexpr int kBK = 128 / KindTraits<KIND>::kEltBytes;     // elements per 128-byte K slice
+  constexpr int kUmmaK = 32 / KindTraits<KIND>::kEltBytes;   // K of one tcgen05.mma
+  constexpr int kKSteps = kBK / kUmmaK;
+  constexpr uint32_t kIdesc = make_idesc<KIND>(kBM, BN);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kStages * Cfg::kStageBytes);
+  uint64_t* empty = full + Cfg::kStages;
+  uint64_t* tfull = empty + Cfg::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = (M + kBM - 1) / kBM;
+  const int num_tiles = num_m * ((N + BN - 1) / BN);
+  const int num_kb = (K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::kStages; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], 1);
+    for (int a = 0; a < 2; ++a) mbar_init(&tfull[a], 1), mbar_init(&tempty[a], 128);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      tma_prefetch_desc(&tm_a);
+      tma_prefetch_desc(&tm_b);
+      int stage = 0;
+      uint32_t phase = 0;
+      int last_parity[Cfg::kStages];
+      for (int s = 0; s < Cfg::kStages; ++s) last_parity[s] = -1;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int mb = tile % num_m, nb = tile / num_m;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, status, kErrGemmWait)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+          tma_load_2d(sa, &tm_a, &full[stage], kb * kBK, mb * kBM);
+          tma_load_2d(sa + Cfg::kABytes, &tm_b, &full[stage], kb * kBK, nb * BN);
+          last_parity[stage] = static_cast<int>(phase);
+          if (++stage == Cfg::kStages) stage = 0, phase ^= 1;
+        }
+      }
+      if (*abort_flag) {
+        // Give the copies already issued a bounded chance to land before the CTA exits.
+        int never = 0;
+        for (int s = 0; s < Cfg::kStages; ++s)
+          if (last_parity[s] >= 0)
+            mbar_wait(&full[s], static_cast<uint32_t>(last_parity[s]), &never, status, 0);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, status, kErrGemmWait)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, status, kErrGemmWait)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_addr(smem + stage * Cfg::kStageBytes);
+          const uint32_t sb = sa + Cfg::kABytes;
+#pragma unroll
+          for (int k = 0; k < kKSteps; ++k)
+            tc_mma<KIND>(d_tmem, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32),
+                         kIdesc, (kb | k) != 0 ? 1u : 0u);
+          tc_commit(&empty[stage]);
+          if (++stage == Cfg::kStages) stage = 0, phase ^= 1;
+        }
+        if (!ok) break;
+        tc_commit(&tfull[acc]);
+        if (++acc == 2) acc = 0, acc_phase ^= 1;
+      }
+      if (*abort_flag) {
+        // Wait (bounded) for every MMA issued so far before TMEM is released.
+        int never = 0;
+        tc_commit(drain);
+        mbar_wait(drain, 0, &never, status, 0);
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5; warp w reads TMEM lanes 32*(w%4) .. +31
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int mb = tile % num_m, nb = tile / num_m;
+      bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status, kErrGemmWait);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
+      gemm_epilogue<T, BN, EPI>(taddr, mb * kBM + row, nb * BN, M, N, ep);
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) acc = 0, acc_phase ^= 1;
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------------------------- host side
+template <int KIND, int BN, int EPI>
+cudaError_t run_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream) {
+  using Cfg = GemmCfg<BN>;
+  constexpr int kElt = KindTraits<KIND>::kEltBytes;
+  constexpr int kBK = 128 / kElt;
+  const CUtensorMapDataType dt =
+      KIND == kKindF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUtensorMap ta, tb;
+  const uint64_t da[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.M)};
+  const uint64_t db[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
+  const uint64_t stride[1] = {static_cast<uint64_t>(p.K) * kElt};
+  const uint32_t box_a[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kBM)};
+  const uint32_t box_b[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(BN)};
+  if (!encode_tmap(&ta, dt, 2, p.A, da, stride, box_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap(&tb, dt, 2, p.W, db, stride, box_b, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  auto kern = gemm_tc_kernel<KIND, BN, EPI>;
+  static int configured_device = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_device != dev) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  kern<<<grid, kGemmThreads, Cfg::kSmemBytes, stream>>>(ta, tb, p.M, p.N, p.K, p.ep, status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// Picks the tile width for N and the epilogue, then launches.
+template <int KIND>
+cudaError_t dispatch_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream) {
+#define MMDIT_GEMM_EPI(BN)                                                          \
+  switch (p.epi) {                                                                  \
+    case kEpiBias: return run_gemm<KIND, BN, kEpiBias>(p, status, stream);          \
+    case kEpiGelu: return run_gemm<KIND, BN, kEpiGelu>(p, status, stream);          \
+    case kEpiGateResid: return run_gemm<KIND, BN, kEpiGateResid>(p, status, stream); \
+    case kEpiUnpatchify: return run_gemm<KIND, BN, kEpiUnpatchify>(p, status, stream); \
+    default: return cudaErrorInvalidValue;                                          \
+  }
+  if (p.epi == kEpiQkv) {
+    if (p.N % 256 == 0 && p.ep.hidden % 256 == 0) return run_gemm<KIND, 256, kEpiQkv>(p, status, stream);
+    return run_gemm<KIND, 128, kEpiQkv>(p, status, stream);
+  }
+  if (p.N % 256 == 0) { MMDIT_GEMM_EPI(256) }
+  if (p.N % 128 == 0) { MMDIT_GEMM_EPI(128) }
+  if (p.N % 64 == 0) { MMDIT_GEMM_EPI(64) }
+  MMDIT_GEMM_EPI(32)
+#undef MMDIT_GEMM_EPI
+}
+
 }  // namespace mmdit
