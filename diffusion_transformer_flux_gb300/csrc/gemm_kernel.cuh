@@ -42,44 +42,6 @@ struct GemmCfg {
   static constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;
 };
 
-// ----------------------------------------------------------------------------- vector I/O
-__device__ __forceinline__ void load32(const __nv_bfloat16* p, float (&v)[32]) {
-  const uint4* q = reinterpret_cast<const uint4*>(p);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint4 u = __ldg(q + i);
-    v[8 * i + 0] = bf16_lo(u.x), v[8 * i + 1] = bf16_hi(u.x);
-    v[8 * i + 2] = bf16_lo(u.y), v[8 * i + 3] = bf16_hi(u.y);
-    v[8 * i + 4] = bf16_lo(u.z), v[8 * i + 5] = bf16_hi(u.z);
-    v[8 * i + 6] = bf16_lo(u.w), v[8 * i + 7] = bf16_hi(u.w);
-  }
-}
-__device__ __forceinline__ void load32(const float* p, float (&v)[32]) {
-  const float4* q = reinterpret_cast<const float4*>(p);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float4 u = __ldg(q + i);
-    v[4 * i] = u.x, v[4 * i + 1] = u.y, v[4 * i + 2] = u.z, v[4 * i + 3] = u.w;
-  }
-}
-__device__ __forceinline__ void store32(__nv_bfloat16* p, const float (&v)[32]) {
-  uint4* q = reinterpret_cast<uint4*>(p);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint4 u;
-    u.x = pack_bf16x2(v[8 * i + 0], v[8 * i + 1]);
-    u.y = pack_bf16x2(v[8 * i + 2], v[8 * i + 3]);
-    u.z = pack_bf16x2(v[8 * i + 4], v[8 * i + 5]);
-    u.w = pack_bf16x2(v[8 * i + 6], v[8 * i + 7]);
-    q[i] = u;
-  }
-}
-__device__ __forceinline__ void store32(float* p, const float (&v)[32]) {
-  float4* q = reinterpret_cast<float4*>(p);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-}
-
 __device__ __forceinline__ float gelu_f(float x, int tanh_form) {
   if (tanh_form) {
     const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
@@ -91,8 +53,7 @@ __device__ __forceinline__ float gelu_f(float x, int tanh_form) {
 // Loads 32 accumulator columns [col, col+32) of this thread's TMEM lane as floats.
 __device__ __forceinline__ void tmem_load_f32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
-  tmem_ld32(taddr, r);
-  tmem_ld_wait();
+  tmem_ld32_wait(taddr, r);
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
