@@ -1,0 +1,265 @@
+// elementwise.cu -- the memory-bound steps of the block: 3D RoPE tables, the AdaLN modulation
+// GEMV, LayerNorm + modulate, latent patchify, V transpose, and the rectified-flow noise/loss.
+// All use 128-bit loads and stores along the contiguous axis.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mmdit {
+namespace {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// 8 consecutive elements <-> floats
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  v[0] = bf16_lo(u.x), v[1] = bf16_hi(u.x), v[2] = bf16_lo(u.y), v[3] = bf16_hi(u.y);
+  v[4] = bf16_lo(u.z), v[5] = bf16_hi(u.z), v[6] = bf16_lo(u.w), v[7] = bf16_hi(u.w);
+}
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
+  uint4 u;
+  u.x = pack_bf16x2(v[0], v[1]), u.y = pack_bf16x2(v[2], v[3]);
+  u.z = pack_bf16x2(v[4], v[5]), u.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// ----------------------------------------------------------------------------- 3D RoPE tables
+struct RopeTable {
+  float inv_freq[128];  // theta^(-2i/d_a) of pair j
+  int axis[128];        // axis of pair j
+  int pairs;
+};
+
+__global__ void rope3d_kernel(const float* __restrict__ ids, int64_t n_tok, RopeTable tab,
+                              float* __restrict__ cos_out, float* __restrict__ sin_out) {
+  const int64_t total = n_tok * tab.pairs;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tok = i / tab.pairs;
+    const int j = static_cast<int>(i - tok * tab.pairs);
+    const double ang = static_cast<double>(ids[tok * 3 + tab.axis[j]]) * tab.inv_freq[j];
+    float s, c;
+    sincosf(static_cast<float>(ang), &s, &c);
+    cos_out[i] = c;
+    sin_out[i] = s;
+  }
+}
+
+// ----------------------------------------------------------------------------- modulation GEMV
+// m[b, r] = sum_k SiLU(vec[b, k]) w[r, k] + bias[r], one warp per weight row; batch <= 8.
+constexpr int kModMaxBatch = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(256) modulation_kernel(const T* __restrict__ vec,
+                                                         const T* __restrict__ w,
+                                                         const T* __restrict__ bias, int batch,
+                                                         int rows, int dim, float* __restrict__ m,
+                                                         int64_t m_bstride) {
+  extern __shared__ float svec[];  // [batch, dim] SiLU(vec)
+  for (int i = threadIdx.x; i < batch * dim; i += blockDim.x) {
+    const float v = to_f32(vec[i]);
+    svec[i] = v / (1.f + expf(-v));
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warps = blockDim.x >> 5;
+  for (int r = blockIdx.x * warps + warp; r < rows; r += gridDim.x * warps) {
+    float acc[kModMaxBatch];
+#pragma unroll
+    for (int b = 0; b < kModMaxBatch; ++b) acc[b] = 0.f;
+    const T* wr = w + static_cast<size_t>(r) * dim;
+#pragma unroll 4
+    for (int k = lane * 8; k < dim; k += 256) {
+      float wv[8];
+      load8(wr + k, wv);
+#pragma unroll
+      for (int b = 0; b < kModMaxBatch; ++b) {
+        if (b < batch) {
+          const float4 s0 = *reinterpret_cast<const float4*>(svec + b * dim + k);
+          const float4 s1 = *reinterpret_cast<const float4*>(svec + b * dim + k + 4);
+          acc[b] += wv[0] * s0.x + wv[1] * s0.y + wv[2] * s0.z + wv[3] * s0.w + wv[4] * s1.x +
+                    wv[5] * s1.y + wv[6] * s1.z + wv[7] * s1.w;
+        }
+      }
+    }
+    const float bb = bias ? to_f32(bias[r]) : 0.f;
+#pragma unroll
+    for (int b = 0; b < kModMaxBatch; ++b) {
+      if (b < batch) {
+        const float s = warp_sum(acc[b]);
+        if (lane == 0) m[b * m_bstride + r] = s + bb;
+      }
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------- LN + modulate
+// One warp per row: mean, biased variance (two passes over the L1-resident row), then
+// out = (x - mean) * rsqrt(var + eps) * (1 + scale[b]) + shift[b].
+template <typename T>
+__global__ void __launch_bounds__(256) ln_modulate_kernel(const T* __restrict__ x,
+                                                          const float* __restrict__ shift,
+                                                          const float* __restrict__ scale,
+                                                          int64_t mod_bstride, int rows, int rpb,
+                                                          int dim, float eps, T* __restrict__ out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (r >= rows) return;
+  const T* xr = x + static_cast<size_t>(r) * dim;
+  float s = 0.f;
+  for (int k = lane * 8; k < dim; k += 256) {
+    float v[8];
+    load8(xr + k, v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) s += v[e];
+  }
+  const float mean = warp_sum(s) / dim;
+  float q = 0.f;
+  for (int k = lane * 8; k < dim; k += 256) {
+    float v[8];
+    load8(xr + k, v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) q = fmaf(v[e] - mean, v[e] - mean, q);
+  }
+  const float rstd = rsqrtf(warp_sum(q) / dim + eps);
+  const int b = r / rpb;
+  const float* sh = shift + b * mod_bstride;
+  const float* sc = scale + b * mod_bstride;
+  T* orow = out + static_cast<size_t>(r) * dim;
+  for (int k = lane * 8; k < dim; k += 256) {
+    float v[8], a[8], c[8];
+    load8(xr + k, v);
+    load8(sh + k, a);
+    load8(sc + k, c);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = fmaf((v[e] - mean) * rstd, 1.f + c[e], a[e]);
+    store8(orow + k, v);
+  }
+}
+
+// ----------------------------------------------------------------------------- transposes
+// z [B, C, HW] fp32 -> out [B, HW, C]
+template <typename T>
+__global__ void patchify_kernel(const float* __restrict__ z, int channels, int hw, T* __restrict__ out) {
+  __shared__ float tile[32][33];
+  const int b = blockIdx.z;
+  const int s0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  const float* zb = z + static_cast<size_t>(b) * channels * hw;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int c = c0 + i, s = s0 + threadIdx.x;
+    tile[i][threadIdx.x] = (c < channels && s < hw) ? zb[static_cast<size_t>(c) * hw + s] : 0.f;
+  }
+  __syncthreads();
+  T* ob = out + static_cast<size_t>(b) * hw * channels;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int s = s0 + i, c = c0 + threadIdx.x;
+    if (s < hw && c < channels) {
+      if constexpr (sizeof(T) == 2)
+        ob[static_cast<size_t>(s) * channels + c] = __float2bfloat16_rn(tile[threadIdx.x][i]);
+      else
+        ob[static_cast<size_t>(s) * channels + c] = tile[threadIdx.x][i];
+    }
+  }
+}
+
+// v [BH, S, 128] -> vt [BH, 128, S_pad]
+__global__ void transpose_v_kernel(const __nv_bfloat16* __restrict__ v, int seq, int seq_pad,
+                                   __nv_bfloat16* __restrict__ vt) {
+  __shared__ __nv_bfloat16 tile[32][34];
+  const size_t bh = blockIdx.z;
+  const int s0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int s = s0 + i;
+    tile[i][threadIdx.x] = s < seq ? v[(bh * seq + s) * 128 + j0 + threadIdx.x] : __float2bfloat16_rn(0.f);
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int s = s0 + threadIdx.x;
+    if (s < seq) vt[(bh * 128 + j0 + i) * seq_pad + s] = tile[threadIdx.x][i];
+  }
+}
+
+// ----------------------------------------------------------------------------- rectified flow
+constexpr int kFlowThreads = 256;
+constexpr int kFlowMaxPartials = 1024;
+
+template <typename T>
+__global__ void __launch_bounds__(kFlowThreads) flow_kernel(const T* __restrict__ z0, const T* __restrict__ z1,
+                                                            const float* __restrict__ t, int64_t n_per,
+                                                            int64_t n_total, T* __restrict__ z_t,
+                                                            const T* __restrict__ pred,
+                                                            float* __restrict__ partials) {
+  float acc = 0.f;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
+  for (int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) * 8; i < n_total;
+       i += step) {
+    float a[8], c[8];
+    load8(z0 + i, a);
+    load8(z1 + i, c);
+    if (z_t) {
+      const float tt = t[i / n_per];
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[e] = fmaf(tt, c[e], (1.f - tt) * a[e]);
+      store8(z_t + i, o);
+    }
+    if (pred) {
+      float p[8];
+      load8(pred + i, p);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float d = p[e] - (c[e] - a[e]);
+        acc = fmaf(d, d, acc);
+      }
+    }
+  }
+  if (!partials) return;
+  __shared__ float red[kFlowThreads / 32];
+  acc = warp_sum(acc);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < kFlowThreads / 32 ? red[threadIdx.x] : 0.f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) partials[blockIdx.x] = v;
+  }
+}
+
+// Sums the partials in a fixed order and writes sum / n_total.
+__global__ void __launch_bounds__(kFlowThreads) flow_finish_kernel(const float* __restrict__ partials,
+                                                                   int n, double inv_total,
+                                                                   float* __restrict__ loss) {
+  __shared__ float red[kFlowThreads / 32];
+  float v = 0.f;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) v += partials[i];
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float w = threadIdx.x < kFlowThreads / 32 ? red[threadIdx.x] : 0.f;
+    w = warp_sum(w);
+    if (threadIdx.x == 0) *loss = static_cast<float>(static_cast<double>(w) * inv_total);
+  }
+}
+
+int blocks_for(int64_t n, int per_block, int cap) {
+  int64_t b = (n + per_block - 1) / per_block;
+  if (b < 1) b = 1;
+  return static_cast<int>(b < cap ? b : cap);
+}
+
+}  // namespace
