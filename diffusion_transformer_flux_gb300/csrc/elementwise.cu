@@ -263,3 +263,121 @@ int blocks_for(int64_t n, int per_block, int cap) {
 }
 
 }  // namespace
+
+// ----------------------------------------------------------------------------- launchers
+cudaError_t launch_rope3d(const float* ids, int batch, int seq, const int axes[3], float theta,
+                          float* cos_out, float* sin_out, cudaStream_t stream) {
+  RopeTable tab{};
+  int j = 0;
+  for (int a = 0; a < 3; ++a)
+    for (int i = 0; i < axes[a] / 2; ++i, ++j) {
+      tab.inv_freq[j] = static_cast<float>(pow(static_cast<double>(theta), -2.0 * i / axes[a]));
+      tab.axis[j] = a;
+    }
+  tab.pairs = j;
+  const int64_t n_tok = static_cast<int64_t>(batch) * seq;
+  if (n_tok == 0 || j == 0) return cudaSuccess;
+  const int grid = blocks_for(n_tok * j, 256, num_sms() * 8);
+  rope3d_kernel<<<grid, 256, 0, stream>>>(ids, n_tok, tab, cos_out, sin_out);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_modulation(int act, const void* vec, const void* w, const void* bias, int batch,
+                              int rows, int dim, float* m, cudaStream_t stream) {
+  const int threads = 256;
+  const int grid = blocks_for(rows, threads / 32, num_sms() * 4);
+  for (int b0 = 0; b0 < batch; b0 += kModMaxBatch) {
+    const int nb = batch - b0 < kModMaxBatch ? batch - b0 : kModMaxBatch;
+    const size_t smem = static_cast<size_t>(nb) * dim * sizeof(float);
+    if (act == 1) {
+      auto k = modulation_kernel<__nv_bfloat16>;
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (e != cudaSuccess) return e;
+      k<<<grid, threads, smem, stream>>>(static_cast<const __nv_bfloat16*>(vec) + static_cast<size_t>(b0) * dim,
+                                         static_cast<const __nv_bfloat16*>(w),
+                                         static_cast<const __nv_bfloat16*>(bias), nb, rows, dim,
+                                         m + static_cast<size_t>(b0) * rows, rows);
+    } else {
+      auto k = modulation_kernel<float>;
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      if (e != cudaSuccess) return e;
+      k<<<grid, threads, smem, stream>>>(static_cast<const float*>(vec) + static_cast<size_t>(b0) * dim,
+                                         static_cast<const float*>(w), static_cast<const float*>(bias),
+                                         nb, rows, dim, m + static_cast<size_t>(b0) * rows, rows);
+    }
+    count_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_ln_modulate(int act, const void* x, const float* shift, const float* scale,
+                               int64_t mod_bstride, int rows, int rows_per_batch, int dim, float eps,
+                               void* out, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  const int grid = (rows + 7) / 8;
+  if (act == 1)
+    ln_modulate_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), shift, scale, mod_bstride, rows, rows_per_batch, dim,
+        eps, static_cast<__nv_bfloat16*>(out));
+  else
+    ln_modulate_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float*>(x), shift, scale,
+                                                        mod_bstride, rows, rows_per_batch, dim, eps,
+                                                        static_cast<float*>(out));
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_patchify(int act, const float* z, int batch, int channels, int hw, void* out,
+                            cudaStream_t stream) {
+  const dim3 grid((hw + 31) / 32, (channels + 31) / 32, batch), block(32, 8);
+  if (act == 1)
+    patchify_kernel<__nv_bfloat16><<<grid, block, 0, stream>>>(z, channels, hw,
+                                                               static_cast<__nv_bfloat16*>(out));
+  else
+    patchify_kernel<float><<<grid, block, 0, stream>>>(z, channels, hw, static_cast<float*>(out));
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_v(const __nv_bfloat16* v, int bh, int seq, int seq_pad,
+                               __nv_bfloat16* vt, cudaStream_t stream) {
+  const dim3 grid((seq + 31) / 32, 4, bh), block(32, 8);
+  transpose_v_kernel<<<grid, block, 0, stream>>>(v, seq, seq_pad, vt);
+  count_launch();
+  return cudaGetLastError();
+}
+
+int flow_partial_blocks(int64_t n_total) {
+  return blocks_for(n_total, kFlowThreads * 8 * 4, kFlowMaxPartials);
+}
+
+cudaError_t launch_flow_match(int dtype, const void* z0, const void* z1, const float* t, int batch,
+                              int64_t n_per_sample, void* z_t, const void* pred, float* loss,
+                              float* partials, int n_partials, cudaStream_t stream) {
+  const int64_t n_total = static_cast<int64_t>(batch) * n_per_sample;
+  if (n_total == 0) return cudaSuccess;
+  const bool want_loss = pred != nullptr && loss != nullptr;
+  const int grid = n_partials;
+  if (dtype == 1)
+    flow_kernel<__nv_bfloat16><<<grid, kFlowThreads, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(z0), static_cast<const __nv_bfloat16*>(z1), t,
+        n_per_sample, n_total, static_cast<__nv_bfloat16*>(z_t),
+        want_loss ? static_cast<const __nv_bfloat16*>(pred) : nullptr, want_loss ? partials : nullptr);
+  else
+    flow_kernel<float><<<grid, kFlowThreads, 0, stream>>>(
+        static_cast<const float*>(z0), static_cast<const float*>(z1), t, n_per_sample, n_total,
+        static_cast<float*>(z_t), want_loss ? static_cast<const float*>(pred) : nullptr,
+        want_loss ? partials : nullptr);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !want_loss) return e;
+  flow_finish_kernel<<<1, kFlowThreads, 0, stream>>>(partials, grid, 1.0 / static_cast<double>(n_total),
+                                                     loss);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace mmdit
