@@ -1,0 +1,440 @@
+// api.cu -- the C ABI of libmmdit.so (declared in include/mmdit.h): argument validation,
+// workspace planning and the launch sequences of each entry point.  No device memory is
+// allocated here; every buffer comes from the caller.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <initializer_list>
+
+#include "../../include/mmdit.h"
+#include "internal.h"
+
+namespace mmdit {
+
+namespace {
+thread_local char g_err[512] = "no error";
+thread_local uint64_t g_launches = 0;
+
+mmdit_status fail(mmdit_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+mmdit_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(MMDIT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+size_t elt_bytes(int act) { return act == MMDIT_BF16 ? 2 : 4; }
+
+// Sequential 256-byte-aligned carving of a workspace.
+struct Carver {
+  size_t off = kStatusBytes;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off = round_up(off + bytes, 256);
+    return o;
+  }
+};
+
+}  // namespace
+
+void count_launch(int n) { g_launches += static_cast<uint64_t>(n); }
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                 CUtensorMapSwizzle swizzle) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) d[i] = dims[i], b[i] = box[i], e[i] = 1;
+  for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
+  return fn(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, e,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ----------------------------------------------------------------------------- block planning
+struct BlockPlan {
+  bool single;
+  int B, Si, St, S, S_pad, D, H, F;
+  size_t elt;
+  size_t mod[2], h[2], q, k, vt, o[2], x1[2], u[2];
+  size_t total;
+};
+
+static bool plan_block(const mmdit_dims* d, bool single, BlockPlan* p) {
+  if (!d) return false;
+  p->single = single;
+  p->B = d->batch, p->Si = d->seq_img, p->St = d->seq_txt;
+  p->S = d->seq_img + d->seq_txt;
+  p->S_pad = static_cast<int>(round_up(static_cast<size_t>(p->S), 8));
+  p->D = d->hidden, p->H = d->heads, p->F = d->mlp_hidden;
+  p->elt = elt_bytes(d->act);
+  Carver c;
+  const size_t B = p->B, D = p->D, F = p->F, S = p->S;
+  const size_t rows[2] = {B * (single ? S : static_cast<size_t>(p->Si)),
+                          single ? 0 : B * static_cast<size_t>(p->St)};
+  const int ns = single ? 1 : 2;
+  for (int s = 0; s < 2; ++s) p->mod[s] = s < ns ? c.take(B * 6 * D * 4) : 0;
+  for (int s = 0; s < 2; ++s) p->h[s] = s < ns ? c.take(rows[s] * D * p->elt) : 0;
+  p->q = c.take(B * D * S * 2);
+  p->k = c.take(B * D * S * 2);
+  p->vt = c.take(B * D * static_cast<size_t>(p->S_pad) * 2);
+  for (int s = 0; s < 2; ++s) p->o[s] = s < ns ? c.take(rows[s] * D * p->elt) : 0;
+  for (int s = 0; s < 2; ++s) p->x1[s] = s < ns ? c.take(rows[s] * D * p->elt) : 0;
+  for (int s = 0; s < 2; ++s) p->u[s] = s < ns ? c.take(rows[s] * F * p->elt) : 0;
+  p->total = c.off;
+  return true;
+}
+
+static mmdit_status check_dims(const mmdit_dims* d) {
+  if (!d) return fail(MMDIT_ERR_INVALID_ARG, "dims is NULL");
+  if (d->batch < 1 || d->seq_img < 0 || d->seq_txt < 0 || d->seq_img + d->seq_txt < 1)
+    return fail(MMDIT_ERR_INVALID_ARG, "bad batch/sequence sizes (B=%d, S_i=%d, S_t=%d)", d->batch,
+                d->seq_img, d->seq_txt);
+  if (d->act != MMDIT_F32 && d->act != MMDIT_BF16)
+    return fail(MMDIT_ERR_INVALID_ARG, "act must be MMDIT_F32 or MMDIT_BF16 (got %d)", d->act);
+  if (d->gemm == MMDIT_GEMM_FP8_E4M3)
+    return fail(MMDIT_ERR_UNSUPPORTED, "FP8 E4M3 linears are not implemented in this build");
+  if (d->gemm != MMDIT_GEMM_NATIVE) return fail(MMDIT_ERR_INVALID_ARG, "unknown gemm mode %d", d->gemm);
+  if (d->head_dim != 128)
+    return fail(MMDIT_ERR_UNSUPPORTED, "head_dim must be 128 (got %d)", d->head_dim);
+  if (d->heads < 1 || d->heads * d->head_dim != d->hidden)
+    return fail(MMDIT_ERR_INVALID_ARG, "heads * head_dim (%d * %d) != hidden (%d)", d->heads,
+                d->head_dim, d->hidden);
+  if (d->mlp_hidden < 64 || d->mlp_hidden % 64 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "mlp_hidden must be a positive multiple of 64 (got %d)",
+                d->mlp_hidden);
+  if (!(d->ln_eps >= 0.f) || !(d->rms_eps >= 0.f))
+    return fail(MMDIT_ERR_INVALID_ARG, "eps must be non-negative");
+  return MMDIT_OK;
+}
+
+static mmdit_status check_ptrs(std::initializer_list<const void*> ptrs, const char* what) {
+  int i = 0;
+  for (const void* p : ptrs) {
+    if (!p) return fail(MMDIT_ERR_INVALID_ARG, "%s: pointer %d is NULL", what, i);
+    if (!aligned16(p)) return fail(MMDIT_ERR_INVALID_ARG, "%s: pointer %d is not 16-byte aligned", what, i);
+    ++i;
+  }
+  return MMDIT_OK;
+}
+
+static mmdit_status check_stream_w(const mmdit_stream_w* w, const char* what) {
+  if (!w) return fail(MMDIT_ERR_INVALID_ARG, "%s: weight set is NULL", what);
+  return check_ptrs({w->w_mod, w->b_mod, w->w_qkv, w->b_qkv, w->g_q, w->g_k, w->w_o, w->b_o, w->w_1,
+                     w->b_1, w->w_2, w->b_2},
+                    what);
+}
+
+static mmdit_status check_workspace(void* ws, size_t have, size_t need) {
+  if (!ws) return fail(MMDIT_ERR_WORKSPACE, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return fail(MMDIT_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+  if (have < need)
+    return fail(MMDIT_ERR_WORKSPACE, "workspace too small: %zu bytes given, %zu needed", have, need);
+  return MMDIT_OK;
+}
+
+#define MMDIT_CUDA(call, what)                       \
+  do {                                               \
+    cudaError_t e_ = (call);                         \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+}  // namespace mmdit
+
+using namespace mmdit;
+
+namespace {
+
+uint32_t* status_word(void* ws) { return static_cast<uint32_t*>(ws); }
+template <typename T = uint8_t>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// Launches the chain of one block over stream s (double block: s = 0 image, 1 text).
+mmdit_status run_stream_qkv(const mmdit_dims* d, const BlockPlan& p, int s, const mmdit_stream_w* w,
+                            const void* vec, const float* cs, const float* sn, const void* x,
+                            void* ws, cudaStream_t st) {
+  const int rows_per_batch = p.single ? p.S : (s == 0 ? p.Si : p.St);
+  const int rows = p.B * rows_per_batch;
+  if (rows == 0) return MMDIT_OK;
+  float* mod = at<float>(ws, p.mod[s]);
+  MMDIT_CUDA(launch_modulation(d->act, vec, w->w_mod, w->b_mod, p.B, 6 * p.D, p.D, mod, st),
+             "modulation");
+  MMDIT_CUDA(launch_ln_modulate(d->act, x, mod, mod + p.D, 6 * p.D, rows, rows_per_batch, p.D,
+                                d->ln_eps, at(ws, p.h[s]), st),
+             "LayerNorm-modulate (attention branch)");
+  GemmProblem g;
+  g.act = d->act, g.epi = kEpiQkv, g.M = rows, g.N = 3 * p.D, g.K = p.D;
+  g.A = at(ws, p.h[s]), g.W = w->w_qkv;
+  g.ep.bias = w->b_qkv, g.ep.g_q = w->g_q, g.ep.g_k = w->g_k;
+  g.ep.rope_cos = cs, g.ep.rope_sin = sn;
+  g.ep.q = at<__nv_bfloat16>(ws, p.q), g.ep.k = at<__nv_bfloat16>(ws, p.k);
+  g.ep.vt = at<__nv_bfloat16>(ws, p.vt);
+  g.ep.rows_per_batch = rows_per_batch;
+  g.ep.seq_offset = (p.single || s == 0) ? 0 : p.Si;
+  g.ep.seq_joint = p.S, g.ep.seq_pad = p.S_pad, g.ep.heads = p.H, g.ep.hidden = p.D;
+  g.ep.rms_eps = d->rms_eps, g.ep.rope_interleaved = d->rope_interleaved ? 1 : 0;
+  MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "QKV projection");
+  return MMDIT_OK;
+}
+
+mmdit_status run_stream_post(const mmdit_dims* d, const BlockPlan& p, int s, const mmdit_stream_w* w,
+                             const void* x, void* y, void* ws, cudaStream_t st) {
+  const int rows_per_batch = p.single ? p.S : (s == 0 ? p.Si : p.St);
+  const int rows = p.B * rows_per_batch;
+  if (rows == 0) return MMDIT_OK;
+  const float* mod = at<float>(ws, p.mod[s]);
+  GemmProblem g;
+  g.act = d->act, g.epi = kEpiGateResid, g.M = rows, g.N = p.D, g.K = p.D;
+  g.A = at(ws, p.o[s]), g.W = w->w_o;
+  g.ep.bias = w->b_o, g.ep.resid = x, g.ep.gate = mod + 2 * p.D, g.ep.gate_bstride = 6 * p.D;
+  g.ep.rows_per_batch = rows_per_batch, g.ep.out = at(ws, p.x1[s]);
+  MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "attention output projection");
+  MMDIT_CUDA(launch_ln_modulate(d->act, at(ws, p.x1[s]), mod + 3 * p.D, mod + 4 * p.D, 6 * p.D, rows,
+                                rows_per_batch, p.D, d->ln_eps, at(ws, p.h[s]), st),
+             "LayerNorm-modulate (MLP branch)");
+  GemmProblem f1;
+  f1.act = d->act, f1.epi = kEpiGelu, f1.M = rows, f1.N = p.F, f1.K = p.D;
+  f1.A = at(ws, p.h[s]), f1.W = w->w_1;
+  f1.ep.bias = w->b_1, f1.ep.gelu_tanh = d->gelu_tanh, f1.ep.out = at(ws, p.u[s]);
+  MMDIT_CUDA(launch_gemm(f1, status_word(ws), st), "MLP fc1 + GELU");
+  GemmProblem f2;
+  f2.act = d->act, f2.epi = kEpiGateResid, f2.M = rows, f2.N = p.D, f2.K = p.F;
+  f2.A = at(ws, p.u[s]), f2.W = w->w_2;
+  f2.ep.bias = w->b_2, f2.ep.resid = at(ws, p.x1[s]), f2.ep.gate = mod + 5 * p.D;
+  f2.ep.gate_bstride = 6 * p.D, f2.ep.rows_per_batch = rows_per_batch, f2.ep.out = y;
+  MMDIT_CUDA(launch_gemm(f2, status_word(ws), st), "MLP fc2 + gated residual");
+  return MMDIT_OK;
+}
+
+mmdit_status run_attention(const BlockPlan& p, int act, void* ws, cudaStream_t st) {
+  AttnProblem a;
+  a.act = act, a.batch = p.B, a.heads = p.H, a.seq = p.S, a.seq_pad = p.S_pad;
+  a.split = p.single ? p.S : p.Si;
+  a.q = at<__nv_bfloat16>(ws, p.q), a.k = at<__nv_bfloat16>(ws, p.k);
+  a.vt = at<__nv_bfloat16>(ws, p.vt);
+  a.out0 = at(ws, p.o[0]);
+  a.out1 = p.single ? nullptr : at(ws, p.o[1]);
+  MMDIT_CUDA(launch_attention(a, status_word(ws), st), "joint attention");
+  return MMDIT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mmdit_last_error(void) { return g_err; }
+
+uint64_t mmdit_launch_count(void) { return g_launches; }
+void mmdit_launch_count_reset(void) { g_launches = 0; }
+
+mmdit_status mmdit_workspace_status(void* workspace, uint32_t* bits_out, void* stream) {
+  if (!workspace) return fail(MMDIT_ERR_INVALID_ARG, "workspace is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t bits = 0;
+  MMDIT_CUDA(cudaStreamSynchronize(st), "stream synchronize");
+  MMDIT_CUDA(cudaMemcpy(&bits, workspace, sizeof(bits), cudaMemcpyDeviceToHost), "status read");
+  MMDIT_CUDA(cudaMemset(workspace, 0, sizeof(bits)), "status clear");
+  if (bits_out) *bits_out = bits;
+  if (bits) return fail(MMDIT_ERR_DEVICE, "a kernel gave up a bounded wait (status bits 0x%x)", bits);
+  return MMDIT_OK;
+}
+
+mmdit_status rope3d_freqs(const float* ids, int32_t batch, int32_t seq, const int32_t* axes_dim,
+                          float theta, float* cos_out, float* sin_out, void* stream) {
+  if (!axes_dim) return fail(MMDIT_ERR_INVALID_ARG, "axes_dim is NULL");
+  if (batch < 0 || seq < 0) return fail(MMDIT_ERR_INVALID_ARG, "negative batch or seq");
+  int sum = 0;
+  for (int a = 0; a < 3; ++a) {
+    if (axes_dim[a] < 0 || axes_dim[a] % 2 != 0)
+      return fail(MMDIT_ERR_INVALID_ARG, "axes_dim[%d] = %d must be even and >= 0", a, axes_dim[a]);
+    sum += axes_dim[a];
+  }
+  if (sum > 256) return fail(MMDIT_ERR_UNSUPPORTED, "sum(axes_dim) = %d exceeds 256", sum);
+  if (!(theta > 0.f)) return fail(MMDIT_ERR_INVALID_ARG, "theta must be positive");
+  if (static_cast<int64_t>(batch) * seq == 0) return MMDIT_OK;
+  if (!ids || !cos_out || !sin_out) return fail(MMDIT_ERR_INVALID_ARG, "NULL ids or output");
+  const int axes[3] = {axes_dim[0], axes_dim[1], axes_dim[2]};
+  MMDIT_CUDA(launch_rope3d(ids, batch, seq, axes, theta, cos_out, sin_out,
+                           static_cast<cudaStream_t>(stream)),
+             "rope3d_freqs");
+  return MMDIT_OK;
+}
+
+size_t flow_match_workspace_size(int32_t batch, int64_t n_per_sample) {
+  const int64_t n = static_cast<int64_t>(batch > 0 ? batch : 0) * (n_per_sample > 0 ? n_per_sample : 0);
+  return kStatusBytes + round_up(static_cast<size_t>(flow_partial_blocks(n)) * sizeof(float), 256);
+}
+
+mmdit_status flow_match_noise_and_loss(int32_t dtype, const void* z0, const void* z1, const float* t,
+                                       int32_t batch, int64_t n_per_sample, void* z_t,
+                                       const void* pred, float* loss, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+  if (dtype != MMDIT_F32 && dtype != MMDIT_BF16)
+    return fail(MMDIT_ERR_INVALID_ARG, "dtype must be MMDIT_F32 or MMDIT_BF16");
+  if (batch < 0 || n_per_sample < 0) return fail(MMDIT_ERR_INVALID_ARG, "negative size");
+  if (n_per_sample % 8 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "n_per_sample must be a multiple of 8 (got %lld)",
+                static_cast<long long>(n_per_sample));
+  if ((pred == nullptr) != (loss == nullptr))
+    return fail(MMDIT_ERR_INVALID_ARG, "pred and loss must both be given or both be NULL");
+  mmdit_status s = check_ptrs({z0, z1}, "flow_match latents");
+  if (s != MMDIT_OK) return s;
+  if (z_t && (s = check_ptrs({z_t, t}, "flow_match z_t/t")) != MMDIT_OK) return s;
+  if (pred && (s = check_ptrs({pred, loss}, "flow_match pred/loss")) != MMDIT_OK) return s;
+  if (pred && z_t && (z_t == z0 || z_t == z1))
+    return fail(MMDIT_ERR_INVALID_ARG, "z_t may not alias z0/z1 when the loss is requested");
+  if ((s = check_workspace(workspace, workspace_bytes,
+                           flow_match_workspace_size(batch, n_per_sample))) != MMDIT_OK)
+    return s;
+  const int64_t n = static_cast<int64_t>(batch) * n_per_sample;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  MMDIT_CUDA(launch_flow_match(dtype, z0, z1, t, batch, n_per_sample, z_t, pred, loss,
+                               at<float>(workspace, kStatusBytes), flow_partial_blocks(n), st),
+             "flow_match_noise_and_loss");
+  return MMDIT_OK;
+}
+
+size_t mmdit_linear_workspace_size(void) { return kStatusBytes; }
+
+mmdit_status mmdit_linear_fwd(int32_t act, int32_t M, int32_t N, int32_t K, const void* x,
+                              const void* w, const void* b, void* y, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (act != MMDIT_F32 && act != MMDIT_BF16) return fail(MMDIT_ERR_INVALID_ARG, "bad act %d", act);
+  if (M < 0 || N <= 0 || K <= 0) return fail(MMDIT_ERR_INVALID_ARG, "bad shape M=%d N=%d K=%d", M, N, K);
+  if (N % 32 != 0 || K % 8 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "N must be a multiple of 32 and K of 8 (N=%d, K=%d)", N, K);
+  mmdit_status s = check_ptrs({x, w, y}, "linear");
+  if (s != MMDIT_OK) return s;
+  if (b && !aligned16(b)) return fail(MMDIT_ERR_INVALID_ARG, "linear: bias not 16-byte aligned");
+  if ((s = check_workspace(workspace, workspace_bytes, mmdit_linear_workspace_size())) != MMDIT_OK)
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  if (M == 0) return MMDIT_OK;
+  GemmProblem g;
+  g.act = act, g.epi = kEpiBias, g.M = M, g.N = N, g.K = K, g.A = x, g.W = w;
+  g.ep.bias = b, g.ep.out = y;
+  MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "linear");
+  return MMDIT_OK;
+}
+
+size_t mmdit_img_in_workspace_size(int32_t act, int32_t batch, int32_t channels, int32_t lat_h,
+                                   int32_t lat_w) {
+  Carver c;
+  c.take(static_cast<size_t>(batch > 0 ? batch : 0) * (lat_h > 0 ? lat_h : 0) *
+         (lat_w > 0 ? lat_w : 0) * (channels > 0 ? channels : 0) * elt_bytes(act));
+  return c.off;
+}
+
+mmdit_status mmdit_img_in_fwd(int32_t act, int32_t batch, int32_t channels, int32_t lat_h,
+                              int32_t lat_w, int32_t hidden, const float* z, const void* w,
+                              const void* b, void* out, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (act != MMDIT_F32 && act != MMDIT_BF16) return fail(MMDIT_ERR_INVALID_ARG, "bad act %d", act);
+  if (batch < 1 || channels < 1 || lat_h < 1 || lat_w < 1 || hidden < 1)
+    return fail(MMDIT_ERR_INVALID_ARG, "bad img_in shape");
+  if (channels % 8 != 0 || hidden % 32 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "channels must be a multiple of 8 and hidden of 32");
+  mmdit_status s = check_ptrs({z, w, b, out}, "img_in");
+  if (s != MMDIT_OK) return s;
+  if ((s = check_workspace(workspace, workspace_bytes,
+                           mmdit_img_in_workspace_size(act, batch, channels, lat_h, lat_w))) != MMDIT_OK)
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  void* tokens = at(workspace, kStatusBytes);
+  const int hw = lat_h * lat_w;
+  MMDIT_CUDA(launch_patchify(act, z, batch, channels, hw, tokens, st), "patchify");
+  GemmProblem g;
+  g.act = act, g.epi = kEpiBias, g.M = batch * hw, g.N = hidden, g.K = channels;
+  g.A = tokens, g.W = w, g.ep.bias = b, g.ep.out = out;
+  MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "img_in linear");
+  return MMDIT_OK;
+}
+
+size_t mmdit_final_layer_workspace_size(const mmdit_dims* d, int32_t channels) {
+  (void)channels;
+  if (!d || d->batch < 1 || d->hidden < 1 || d->seq_img < 0) return 0;
+  Carver c;
+  c.take(static_cast<size_t>(d->batch) * 2 * d->hidden * 4);
+  c.take(static_cast<size_t>(d->batch) * d->seq_img * d->hidden * elt_bytes(d->act));
+  return c.off;
+}
+
+mmdit_status mmdit_final_layer_fwd(const mmdit_dims* d, int32_t channels, int32_t lat_h,
+                                   int32_t lat_w, const void* x_img, const void* vec,
+                                   const void* w_ada, const void* b_ada, const void* w_out,
+                                   const void* b_out, float* pred, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  if (!d) return fail(MMDIT_ERR_INVALID_ARG, "dims is NULL");
+  if (d->act != MMDIT_F32 && d->act != MMDIT_BF16) return fail(MMDIT_ERR_INVALID_ARG, "bad act");
+  if (d->batch < 1 || lat_h < 1 || lat_w < 1 || d->seq_img != lat_h * lat_w)
+    return fail(MMDIT_ERR_INVALID_ARG, "final layer: seq_img must equal lat_h * lat_w");
+  if (channels < 32 || channels % 32 != 0 || d->hidden % 256 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "final layer: channels multiple of 32, hidden of 256");
+  mmdit_status s = check_ptrs({x_img, vec, w_ada, b_ada, w_out, b_out, pred}, "final layer");
+  if (s != MMDIT_OK) return s;
+  if ((s = check_workspace(workspace, workspace_bytes, mmdit_final_layer_workspace_size(d, channels))) !=
+      MMDIT_OK)
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  Carver c;
+  float* mod = at<float>(workspace, c.take(static_cast<size_t>(d->batch) * 2 * d->hidden * 4));
+  void* h = at(workspace, c.take(static_cast<size_t>(d->batch) * d->seq_img * d->hidden * elt_bytes(d->act)));
+  const int D = d->hidden, rows = d->batch * d->seq_img;
+  MMDIT_CUDA(launch_modulation(d->act, vec, w_ada, b_ada, d->batch, 2 * D, D, mod, st), "final modulation");
+  MMDIT_CUDA(launch_ln_modulate(d->act, x_img, mod, mod + D, 2 * D, rows, d->seq_img, D, d->ln_eps, h, st),
+             "final LayerNorm-modulate");
+  GemmProblem g;
+  g.act = d->act, g.epi = kEpiUnpatchify, g.M = rows, g.N = channels, g.K = D;
+  g.A = h, g.W = w_out, g.ep.bias = b_out, g.ep.out = pred, g.ep.rows_per_batch = d->seq_img;
+  MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "final projection");
+  return MMDIT_OK;
+}
+
+}  // extern "C"
