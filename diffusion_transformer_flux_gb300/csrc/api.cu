@@ -437,4 +437,118 @@ mmdit_status mmdit_final_layer_fwd(const mmdit_dims* d, int32_t channels, int32_
   return MMDIT_OK;
 }
 
+
+size_t mmdit_attention_workspace_size(int32_t batch, int32_t heads, int32_t seq) {
+  if (batch < 1 || heads < 1 || seq < 1) return kStatusBytes;
+  Carver c;
+  c.take(static_cast<size_t>(batch) * heads * 128 * round_up(static_cast<size_t>(seq), 8) * 2);
+  return c.off;
+}
+
+mmdit_status mmdit_attention_fwd(int32_t act, int32_t batch, int32_t heads, int32_t seq,
+                                 int32_t head_dim, const void* q, const void* k, const void* v,
+                                 void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (act != MMDIT_F32 && act != MMDIT_BF16) return fail(MMDIT_ERR_INVALID_ARG, "bad act %d", act);
+  if (head_dim != 128) return fail(MMDIT_ERR_UNSUPPORTED, "head_dim must be 128");
+  if (batch < 1 || heads < 1 || seq < 1) return fail(MMDIT_ERR_INVALID_ARG, "bad attention shape");
+  if (static_cast<int64_t>(batch) * heads > 65535)
+    return fail(MMDIT_ERR_UNSUPPORTED, "batch * heads must be <= 65535");
+  mmdit_status s = check_ptrs({q, k, v, out}, "attention");
+  if (s != MMDIT_OK) return s;
+  if ((s = check_workspace(workspace, workspace_bytes,
+                           mmdit_attention_workspace_size(batch, heads, seq))) != MMDIT_OK)
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  const int seq_pad = static_cast<int>(round_up(static_cast<size_t>(seq), 8));
+  __nv_bfloat16* vt = at<__nv_bfloat16>(workspace, kStatusBytes);
+  MMDIT_CUDA(launch_transpose_v(static_cast<const __nv_bfloat16*>(v), batch * heads, seq, seq_pad, vt, st),
+             "V transpose");
+  AttnProblem a;
+  a.act = act, a.batch = batch, a.heads = heads, a.seq = seq, a.seq_pad = seq_pad, a.split = seq;
+  a.q = static_cast<const __nv_bfloat16*>(q), a.k = static_cast<const __nv_bfloat16*>(k), a.vt = vt;
+  a.out0 = out, a.out1 = nullptr;
+  MMDIT_CUDA(launch_attention(a, status_word(workspace), st), "attention");
+  return MMDIT_OK;
+}
+
+size_t mmdit_double_block_workspace_size(const mmdit_dims* d) {
+  BlockPlan p;
+  if (check_dims(d) != MMDIT_OK || !plan_block(d, false, &p)) return 0;
+  return p.total;
+}
+
+size_t mmdit_single_block_workspace_size(const mmdit_dims* d) {
+  BlockPlan p;
+  if (check_dims(d) != MMDIT_OK || !plan_block(d, true, &p)) return 0;
+  return p.total;
+}
+
+int32_t mmdit_block_workspace_offsets(const mmdit_dims* d, int32_t single, int64_t* out, int32_t n) {
+  BlockPlan p;
+  if (!out || check_dims(d) != MMDIT_OK || !plan_block(d, single != 0, &p)) return -1;
+  const int64_t none = -1;
+  const int64_t v[10] = {static_cast<int64_t>(p.mod[0]), single ? none : static_cast<int64_t>(p.mod[1]),
+                         static_cast<int64_t>(p.q), static_cast<int64_t>(p.k), static_cast<int64_t>(p.vt),
+                         static_cast<int64_t>(p.o[0]), single ? none : static_cast<int64_t>(p.o[1]),
+                         static_cast<int64_t>(p.x1[0]), single ? none : static_cast<int64_t>(p.x1[1]),
+                         static_cast<int64_t>(p.u[0])};
+  const int m = n < 10 ? n : 10;
+  for (int i = 0; i < m; ++i) out[i] = v[i];
+  return m;
+}
+
+mmdit_status mmdit_double_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w_img,
+                                    const mmdit_stream_w* w_txt, const void* vec,
+                                    const float* rope_cos, const float* rope_sin, const void* x_img,
+                                    const void* x_txt, void* y_img, void* y_txt, mmdit_fp8_state* fp8,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  mmdit_status s = check_dims(d);
+  if (s != MMDIT_OK) return s;
+  if (fp8) return fail(MMDIT_ERR_UNSUPPORTED, "fp8 state given but FP8 linears are not implemented");
+  if ((s = check_stream_w(w_img, "image weights")) != MMDIT_OK) return s;
+  if ((s = check_stream_w(w_txt, "text weights")) != MMDIT_OK) return s;
+  if ((s = check_ptrs({vec, rope_cos, rope_sin}, "double block conditioning")) != MMDIT_OK) return s;
+  if (d->seq_img > 0 && (s = check_ptrs({x_img, y_img}, "image stream")) != MMDIT_OK) return s;
+  if (d->seq_txt > 0 && (s = check_ptrs({x_txt, y_txt}, "text stream")) != MMDIT_OK) return s;
+  if (static_cast<int64_t>(d->batch) * d->heads > 65535)
+    return fail(MMDIT_ERR_UNSUPPORTED, "batch * heads must be <= 65535");
+  BlockPlan p;
+  plan_block(d, false, &p);
+  if ((s = check_workspace(workspace, workspace_bytes, p.total)) != MMDIT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  const mmdit_stream_w* ws_[2] = {w_img, w_txt};
+  const void* xs[2] = {x_img, x_txt};
+  void* ys[2] = {y_img, y_txt};
+  for (int i = 0; i < 2; ++i)
+    if ((s = run_stream_qkv(d, p, i, ws_[i], vec, rope_cos, rope_sin, xs[i], workspace, st)) != MMDIT_OK)
+      return s;
+  if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
+  for (int i = 0; i < 2; ++i)
+    if ((s = run_stream_post(d, p, i, ws_[i], xs[i], ys[i], workspace, st)) != MMDIT_OK) return s;
+  return MMDIT_OK;
+}
+
+mmdit_status mmdit_single_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w, const void* vec,
+                                    const float* rope_cos, const float* rope_sin, const void* x,
+                                    void* y, mmdit_fp8_state* fp8, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  mmdit_status s = check_dims(d);
+  if (s != MMDIT_OK) return s;
+  if (fp8) return fail(MMDIT_ERR_UNSUPPORTED, "fp8 state given but FP8 linears are not implemented");
+  if ((s = check_stream_w(w, "single-block weights")) != MMDIT_OK) return s;
+  if ((s = check_ptrs({vec, rope_cos, rope_sin, x, y}, "single block")) != MMDIT_OK) return s;
+  if (static_cast<int64_t>(d->batch) * d->heads > 65535)
+    return fail(MMDIT_ERR_UNSUPPORTED, "batch * heads must be <= 65535");
+  BlockPlan p;
+  plan_block(d, true, &p);
+  if ((s = check_workspace(workspace, workspace_bytes, p.total)) != MMDIT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  if ((s = run_stream_qkv(d, p, 0, w, vec, rope_cos, rope_sin, x, workspace, st)) != MMDIT_OK) return s;
+  if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
+  return run_stream_post(d, p, 0, w, x, y, workspace, st);
+}
+
 }  // extern "C"
