@@ -1,0 +1,278 @@
+"""ctypes binding of libmmdit.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls and forwards torch tensors as
+raw device pointers together with torch's current CUDA stream.  No computation happens in
+Python; when the library is missing, loading fails with an error (there is no fallback).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+from . import build_ext
+
+MMDIT_OK = 0
+MMDIT_F32 = 0
+MMDIT_BF16 = 1
+STATUS_NAMES = {0: "MMDIT_OK", 1: "MMDIT_ERR_INVALID_ARG", 2: "MMDIT_ERR_UNSUPPORTED",
+                3: "MMDIT_ERR_WORKSPACE", 4: "MMDIT_ERR_CUDA", 5: "MMDIT_ERR_NONFINITE",
+                6: "MMDIT_ERR_DEVICE"}
+
+# Names exported by the library, in include/mmdit.h order.
+EXPORTED = [
+    "mmdit_last_error", "mmdit_workspace_status", "mmdit_launch_count", "mmdit_launch_count_reset",
+    "rope3d_freqs", "flow_match_workspace_size", "flow_match_noise_and_loss",
+    "mmdit_linear_workspace_size", "mmdit_linear_fwd", "mmdit_img_in_workspace_size",
+    "mmdit_img_in_fwd", "mmdit_final_layer_workspace_size", "mmdit_final_layer_fwd",
+    "mmdit_attention_workspace_size", "mmdit_attention_fwd", "mmdit_double_block_workspace_size",
+    "mmdit_double_block_fwd", "mmdit_single_block_workspace_size", "mmdit_single_block_fwd",
+    "mmdit_block_workspace_offsets",
+]
+
+
+class MMDitError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class Dims(C.Structure):
+    _fields_ = [("batch", C.c_int32), ("seq_img", C.c_int32), ("seq_txt", C.c_int32),
+                ("hidden", C.c_int32), ("heads", C.c_int32), ("head_dim", C.c_int32),
+                ("mlp_hidden", C.c_int32), ("ln_eps", C.c_float), ("rms_eps", C.c_float),
+                ("rope_interleaved", C.c_int32), ("gelu_tanh", C.c_int32), ("act", C.c_int32),
+                ("gemm", C.c_int32)]
+
+
+STREAM_W_FIELDS = ["w_mod", "b_mod", "w_qkv", "b_qkv", "g_q", "g_k", "w_o", "b_o", "w_1", "b_1",
+                   "w_2", "b_2"]
+
+
+class StreamW(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in STREAM_W_FIELDS]
+
+
+VP, SZ, I32, I64, F32 = C.c_void_p, C.c_size_t, C.c_int32, C.c_int64, C.c_float
+PDIMS, PW = C.POINTER(Dims), C.POINTER(StreamW)
+
+_SIGS = {
+    "mmdit_last_error": (C.c_char_p, []),
+    "mmdit_workspace_status": (C.c_int, [VP, C.POINTER(C.c_uint32), VP]),
+    "mmdit_launch_count": (C.c_uint64, []),
+    "mmdit_launch_count_reset": (None, []),
+    "rope3d_freqs": (C.c_int, [VP, I32, I32, C.POINTER(I32), F32, VP, VP, VP]),
+    "flow_match_workspace_size": (SZ, [I32, I64]),
+    "flow_match_noise_and_loss": (C.c_int, [I32, VP, VP, VP, I32, I64, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_linear_workspace_size": (SZ, []),
+    "mmdit_linear_fwd": (C.c_int, [I32, I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_img_in_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
+    "mmdit_img_in_fwd": (C.c_int, [I32, I32, I32, I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_final_layer_workspace_size": (SZ, [PDIMS, I32]),
+    "mmdit_final_layer_fwd": (C.c_int, [PDIMS, I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_attention_workspace_size": (SZ, [I32, I32, I32]),
+    "mmdit_attention_fwd": (C.c_int, [I32, I32, I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_double_block_workspace_size": (SZ, [PDIMS]),
+    "mmdit_double_block_fwd": (C.c_int, [PDIMS, PW, PW, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_single_block_workspace_size": (SZ, [PDIMS]),
+    "mmdit_single_block_fwd": (C.c_int, [PDIMS, PW, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_block_workspace_offsets": (I32, [PDIMS, I32, C.POINTER(I64), I32]),
+}
+
+_lib = None
+
+
+def library_path() -> str:
+    return build_ext.LIB
+
+
+def load() -> C.CDLL:
+    """Load libmmdit.so (built by ``build_ext.build()``); raises if it is missing."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with diffusion_transformer_flux_gb300."
+                               "build_ext.build() (there is no CPU fallback)")
+        lib = C.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype, fn.argtypes = res, args
+        _lib = lib
+    return _lib
+
+
+def last_error() -> str:
+    return load().mmdit_last_error().decode()
+
+
+def _check(status: int):
+    if status != MMDIT_OK:
+        raise MMDitError(status, last_error())
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def act_of(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return MMDIT_BF16
+    if t.dtype == torch.float32:
+        return MMDIT_F32
+    raise TypeError(f"unsupported activation dtype {t.dtype}")
+
+
+def make_dims(batch, seq_img, seq_txt, hidden, heads, mlp_hidden, act, head_dim=128, ln_eps=1e-6,
+              rms_eps=1e-6, rope_interleaved=True, gelu_tanh=False, gemm=0) -> Dims:
+    return Dims(batch, seq_img, seq_txt, hidden, heads, head_dim, mlp_hidden, ln_eps, rms_eps,
+                int(rope_interleaved), int(gelu_tanh), act, gemm)
+
+
+def make_stream_w(w: dict) -> StreamW:
+    return StreamW(*[_ptr(w[n]) for n in STREAM_W_FIELDS])
+
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A caller-owned workspace: a zeroed uint8 device tensor (256-byte aligned by torch)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ----------------------------------------------------------------------------- entry points
+def mmdit_workspace_status(ws, stream=None) -> int:
+    bits = C.c_uint32(0)
+    st = load().mmdit_workspace_status(_ptr(ws), C.byref(bits), _stream(stream))
+    if st not in (MMDIT_OK, 6):
+        _check(st)
+    return bits.value
+
+
+def mmdit_launch_count() -> int:
+    return load().mmdit_launch_count()
+
+
+def mmdit_launch_count_reset():
+    load().mmdit_launch_count_reset()
+
+
+def rope3d_freqs(ids, axes_dim, theta, cos_out, sin_out, stream=None):
+    B, S, _ = ids.shape
+    axes = (I32 * 3)(*axes_dim)
+    _check(load().rope3d_freqs(_ptr(ids), B, S, axes, float(theta), _ptr(cos_out), _ptr(sin_out),
+                               _stream(stream)))
+
+
+def flow_match_workspace_size(batch, n_per_sample) -> int:
+    return load().flow_match_workspace_size(batch, n_per_sample)
+
+
+def flow_match_noise_and_loss(z0, z1, t, z_t=None, pred=None, loss=None, ws=None, stream=None):
+    B = z0.shape[0]
+    n = z0.numel() // B
+    if ws is None:
+        ws = workspace(flow_match_workspace_size(B, n), z0.device)
+    _check(load().flow_match_noise_and_loss(act_of(z0), _ptr(z0), _ptr(z1), _ptr(t), B, n, _ptr(z_t),
+                                            _ptr(pred), _ptr(loss), _ptr(ws), ws.numel(),
+                                            _stream(stream)))
+    return ws
+
+
+def mmdit_linear_fwd(x, w, b, y, ws=None, stream=None):
+    M, K = x.reshape(-1, x.shape[-1]).shape
+    N = w.shape[0]
+    if ws is None:
+        ws = workspace(load().mmdit_linear_workspace_size(), x.device)
+    _check(load().mmdit_linear_fwd(act_of(x), M, N, K, _ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(ws),
+                                   ws.numel(), _stream(stream)))
+    return ws
+
+
+def mmdit_img_in_workspace_size(act, batch, channels, lat_h, lat_w) -> int:
+    return load().mmdit_img_in_workspace_size(act, batch, channels, lat_h, lat_w)
+
+
+def mmdit_img_in_fwd(z, w, b, out, ws=None, stream=None):
+    B, Cc, H, W = z.shape
+    act = act_of(w)
+    if ws is None:
+        ws = workspace(mmdit_img_in_workspace_size(act, B, Cc, H, W), z.device)
+    _check(load().mmdit_img_in_fwd(act, B, Cc, H, W, w.shape[0], _ptr(z), _ptr(w), _ptr(b), _ptr(out),
+                                   _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+def mmdit_final_layer_workspace_size(dims: Dims, channels: int) -> int:
+    return load().mmdit_final_layer_workspace_size(C.byref(dims), channels)
+
+
+def mmdit_final_layer_fwd(dims: Dims, lat_h, lat_w, x_img, vec, w_ada, b_ada, w_out, b_out, pred,
+                          ws=None, stream=None):
+    channels = w_out.shape[0]
+    if ws is None:
+        ws = workspace(mmdit_final_layer_workspace_size(dims, channels), x_img.device)
+    _check(load().mmdit_final_layer_fwd(C.byref(dims), channels, lat_h, lat_w, _ptr(x_img), _ptr(vec),
+                                        _ptr(w_ada), _ptr(b_ada), _ptr(w_out), _ptr(b_out), _ptr(pred),
+                                        _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+def mmdit_attention_workspace_size(batch, heads, seq) -> int:
+    return load().mmdit_attention_workspace_size(batch, heads, seq)
+
+
+def mmdit_attention_fwd(q, k, v, out, ws=None, stream=None):
+    B, H, S, d = q.shape
+    if ws is None:
+        ws = workspace(mmdit_attention_workspace_size(B, H, S), q.device)
+    _check(load().mmdit_attention_fwd(act_of(out), B, H, S, d, _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                      _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+def mmdit_double_block_workspace_size(dims: Dims) -> int:
+    return load().mmdit_double_block_workspace_size(C.byref(dims))
+
+
+def mmdit_single_block_workspace_size(dims: Dims) -> int:
+    return load().mmdit_single_block_workspace_size(C.byref(dims))
+
+
+def mmdit_block_workspace_offsets(dims: Dims, single: bool) -> list:
+    out = (I64 * 10)()
+    n = load().mmdit_block_workspace_offsets(C.byref(dims), int(single), out, 10)
+    if n < 0:
+        raise MMDitError(1, "bad dims")
+    return list(out)[:n]
+
+
+def mmdit_double_block_fwd(dims: Dims, w_img: dict, w_txt: dict, vec, rope_cos, rope_sin, x_img,
+                           x_txt, y_img, y_txt, ws=None, stream=None):
+    if ws is None:
+        ws = workspace(mmdit_double_block_workspace_size(dims), vec.device)
+    wi, wt = make_stream_w(w_img), make_stream_w(w_txt)
+    _check(load().mmdit_double_block_fwd(C.byref(dims), C.byref(wi), C.byref(wt), _ptr(vec),
+                                         _ptr(rope_cos), _ptr(rope_sin), _ptr(x_img), _ptr(x_txt),
+                                         _ptr(y_img), _ptr(y_txt), None, _ptr(ws), ws.numel(),
+                                         _stream(stream)))
+    return ws
+
+
+def mmdit_single_block_fwd(dims: Dims, w: dict, vec, rope_cos, rope_sin, x, y, ws=None, stream=None):
+    if ws is None:
+        ws = workspace(mmdit_single_block_workspace_size(dims), vec.device)
+    ww = make_stream_w(w)
+    _check(load().mmdit_single_block_fwd(C.byref(dims), C.byref(ww), _ptr(vec), _ptr(rope_cos),
+                                         _ptr(rope_sin), _ptr(x), _ptr(y), None, _ptr(ws), ws.numel(),
+                                         _stream(stream)))
+    return ws

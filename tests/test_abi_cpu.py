@@ -1,0 +1,113 @@
+"""The C ABI without a GPU: the library builds and loads, exports every function that
+include/mmdit.h declares, sizes workspaces, and rejects bad arguments before touching CUDA."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from diffusion_transformer_flux_gb300 import _lib as L
+from diffusion_transformer_flux_gb300 import build_ext
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_ext.build()
+    return L.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "mmdit.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\([^;{]*\)\s*;", src)
+    return sorted(set(n for n in names if not n.startswith("typedef")))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("mmdit_double_block_fwd", "mmdit_single_block_fwd", "rope3d_freqs",
+              "flow_match_noise_and_loss"):
+        assert n in names
+    assert sorted(L.EXPORTED) == names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), n
+
+
+def _dims(**kw):
+    base = dict(batch=1, seq_img=4096, seq_txt=512, hidden=3072, heads=24, mlp_hidden=12288,
+                act=L.MMDIT_BF16)
+    base.update(kw)
+    return L.make_dims(**base)
+
+
+def test_workspace_sizes(lib):
+    d = _dims()
+    ws = L.mmdit_double_block_workspace_size(d)
+    B, S, Si, St, D, F = 1, 4608, 4096, 512, 3072, 12288
+    # at least: modulation, LN outputs, Q, K, V^T, attention outputs, x1, MLP hidden
+    floor = 2 * 6 * D * 4 + S * D * 2 * (1 + 3 + 1 + 1) + S * F * 2
+    assert ws >= floor
+    assert ws < floor * 1.01 + 64 * 1024
+    single = L.mmdit_single_block_workspace_size(d)
+    assert single >= S * D * 2 * 6 + S * F * 2
+    assert L.mmdit_double_block_workspace_size(_dims(head_dim=64)) == 0
+    offs = L.mmdit_block_workspace_offsets(d, False)
+    assert len(offs) == 10 and offs[0] == 256
+    assert all(o % 256 == 0 for o in offs)
+    assert sorted(offs) == offs  # carved in order
+    so = L.mmdit_block_workspace_offsets(d, True)
+    assert so[1] == -1 and so[6] == -1 and so[8] == -1
+    assert L.flow_match_workspace_size(4, 64 * 32 * 32) >= 256 + 4
+    assert lib.mmdit_linear_workspace_size() == 256
+
+
+def test_validation_errors_before_any_launch(lib):
+    d = _dims()
+    w = L.StreamW()
+    st = lib.mmdit_double_block_fwd(C.byref(d), C.byref(w), C.byref(w), None, None, None, None, None,
+                                    None, None, None, None, 0, None)
+    assert st == 1 and "NULL" in L.last_error()
+    bad = _dims(head_dim=64)
+    assert lib.mmdit_single_block_fwd(C.byref(bad), C.byref(w), None, None, None, None, None, None,
+                                      None, 0, None) == 2
+    fp8 = _dims(gemm=1)
+    assert lib.mmdit_double_block_fwd(C.byref(fp8), C.byref(w), C.byref(w), None, None, None, None,
+                                      None, None, None, None, None, 0, None) == 2
+    assert "FP8" in L.last_error()
+    mism = _dims(heads=23)
+    assert lib.mmdit_double_block_fwd(C.byref(mism), C.byref(w), C.byref(w), None, None, None, None,
+                                      None, None, None, None, None, 0, None) == 1
+    # odd axes_dim and oversize tables
+    axes = (C.c_int32 * 3)(16, 55, 56)
+    assert lib.rope3d_freqs(None, 1, 4, axes, 1e4, None, None, None) == 1
+    axes = (C.c_int32 * 3)(128, 128, 2)
+    assert lib.rope3d_freqs(None, 1, 4, axes, 1e4, None, None, None) == 2
+    # empty RoPE call is a no-op
+    axes = (C.c_int32 * 3)(16, 56, 56)
+    assert lib.rope3d_freqs(None, 0, 4, axes, 1e4, None, None, None) == 0
+    # misaligned pointer
+    assert lib.mmdit_linear_fwd(1, 8, 32, 8, 0x1001, 0x2000, None, 0x3000, 0x4000, 256, None) == 1
+    # shape the tensor-core path does not take
+    assert lib.mmdit_linear_fwd(1, 8, 33, 8, 0x1000, 0x2000, None, 0x3000, 0x4000, 256, None) == 2
+    # workspace too small / misaligned
+    assert lib.mmdit_linear_fwd(1, 8, 32, 8, 0x1000, 0x2000, None, 0x3000, 0x4000, 16, None) == 3
+    assert lib.mmdit_linear_fwd(1, 8, 32, 8, 0x1000, 0x2000, None, 0x3000, 0x4010, 4096, None) == 3
+    # flow matching: loss needs both pred and loss, n multiple of 8
+    assert lib.flow_match_noise_and_loss(0, 0x1000, 0x2000, 0x3000, 1, 12, None, None, None, 0x4000,
+                                         4096, None) == 2
+    assert lib.flow_match_noise_and_loss(0, 0x1000, 0x2000, 0x3000, 1, 16, None, 0x5000, None,
+                                         0x4000, 4096, None) == 1
+    assert lib.mmdit_attention_fwd(1, 1, 1, 16, 64, 0x1000, 0x1000, 0x1000, 0x1000, 0x4000, 1 << 20,
+                                   None) == 2
+
+
+def test_library_does_not_fall_back(tmp_path, monkeypatch):
+    monkeypatch.setattr(build_ext, "LIB", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(L, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        L.load()
