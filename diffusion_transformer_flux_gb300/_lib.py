@@ -23,6 +23,7 @@ STATUS_NAMES = {0: "MMDIT_OK", 1: "MMDIT_ERR_INVALID_ARG", 2: "MMDIT_ERR_UNSUPPO
 # Names exported by the library, in include/mmdit.h order.
 EXPORTED = [
     "mmdit_last_error", "mmdit_workspace_status", "mmdit_launch_count", "mmdit_launch_count_reset",
+    "mmdit_profile_enable", "mmdit_profile_collect",
     "rope3d_freqs", "flow_match_workspace_size", "flow_match_noise_and_loss",
     "mmdit_linear_workspace_size", "mmdit_linear_fwd", "mmdit_img_in_workspace_size",
     "mmdit_img_in_fwd", "mmdit_final_layer_workspace_size", "mmdit_final_layer_fwd",
@@ -62,6 +63,8 @@ _SIGS = {
     "mmdit_workspace_status": (C.c_int, [VP, C.POINTER(C.c_uint32), VP]),
     "mmdit_launch_count": (C.c_uint64, []),
     "mmdit_launch_count_reset": (None, []),
+    "mmdit_profile_enable": (None, [I32]),
+    "mmdit_profile_collect": (I32, [VP, C.c_char_p, SZ, C.POINTER(F32), I32]),
     "rope3d_freqs": (C.c_int, [VP, I32, I32, C.POINTER(I32), F32, VP, VP, VP]),
     "flow_match_workspace_size": (SZ, [I32, I64]),
     "flow_match_noise_and_loss": (C.c_int, [I32, VP, VP, VP, I32, I64, VP, VP, VP, VP, SZ, VP]),
@@ -164,6 +167,21 @@ def mmdit_launch_count() -> int:
 
 def mmdit_launch_count_reset():
     load().mmdit_launch_count_reset()
+
+
+def mmdit_profile_enable(on: bool):
+    load().mmdit_profile_enable(int(bool(on)))
+
+
+def mmdit_profile_collect(stream=None, max_entries=1 << 16) -> list:
+    """[(step name, milliseconds), ...] recorded since the last collect (synchronises)."""
+    names = C.create_string_buffer(max_entries * 32)
+    ms = (F32 * max_entries)()
+    n = load().mmdit_profile_collect(_stream(stream), names, len(names), ms, max_entries)
+    if n < 0:
+        raise MMDitError(4, "profile collection failed")
+    labels = names.raw.split(b"\0")[:n]
+    return [(labels[i].decode(), float(ms[i])) for i in range(n)]
 
 
 def rope3d_freqs(ids, axes_dim, theta, cos_out, sin_out, stream=None):

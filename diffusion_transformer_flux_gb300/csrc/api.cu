@@ -3,6 +3,7 @@
 // allocated here; every buffer comes from the caller.
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <initializer_list>
@@ -63,6 +64,44 @@ struct Carver {
 }  // namespace
 
 void count_launch(int n) { g_launches += static_cast<uint64_t>(n); }
+
+// ----------------------------------------------------------------------------- step timing
+namespace {
+struct ProfRecord {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+thread_local bool g_prof_on = false;
+thread_local ProfRecord* g_prof = nullptr;
+thread_local int g_prof_n = 0, g_prof_cap = 0;
+
+// Brackets one library step with events on `stream` when profiling is enabled.
+struct ProfScope {
+  ProfRecord* rec = nullptr;
+  cudaStream_t stream;
+  ProfScope(const char* name, cudaStream_t s) : stream(s) {
+    if (!g_prof_on) return;
+    if (g_prof_n == g_prof_cap) {
+      const int cap = g_prof_cap ? 2 * g_prof_cap : 256;
+      ProfRecord* n = static_cast<ProfRecord*>(realloc(g_prof, cap * sizeof(ProfRecord)));
+      if (!n) return;
+      g_prof = n, g_prof_cap = cap;
+    }
+    ProfRecord r{name, nullptr, nullptr};
+    if (cudaEventCreate(&r.start) != cudaSuccess) return;
+    if (cudaEventCreate(&r.stop) != cudaSuccess) {
+      cudaEventDestroy(r.start);
+      return;
+    }
+    g_prof[g_prof_n] = r;
+    rec = &g_prof[g_prof_n++];
+    cudaEventRecord(rec->start, stream);
+  }
+  ~ProfScope() {
+    if (rec) cudaEventRecord(rec->stop, stream);
+  }
+};
+}  // namespace
 
 int num_sms() {
   static int cached[64] = {0};
@@ -200,11 +239,13 @@ mmdit_status run_stream_qkv(const mmdit_dims* d, const BlockPlan& p, int s, cons
   const int rows = p.B * rows_per_batch;
   if (rows == 0) return MMDIT_OK;
   float* mod = at<float>(ws, p.mod[s]);
+  { ProfScope ps_(p.single ? "single.modulation" : (s == 0 ? "double.modulation.img" : "double.modulation.txt"), st);
   MMDIT_CUDA(launch_modulation(d->act, vec, w->w_mod, w->b_mod, p.B, 6 * p.D, p.D, mod, st),
-             "modulation");
+             "modulation"); }
+  { ProfScope ps_(p.single ? "single.ln1" : (s == 0 ? "double.ln1.img" : "double.ln1.txt"), st);
   MMDIT_CUDA(launch_ln_modulate(d->act, x, mod, mod + p.D, 6 * p.D, rows, rows_per_batch, p.D,
                                 d->ln_eps, at(ws, p.h[s]), st),
-             "LayerNorm-modulate (attention branch)");
+             "LayerNorm-modulate (attention branch)"); }
   GemmProblem g;
   g.act = d->act, g.epi = kEpiQkv, g.M = rows, g.N = 3 * p.D, g.K = p.D;
   g.A = at(ws, p.h[s]), g.W = w->w_qkv;
@@ -216,7 +257,8 @@ mmdit_status run_stream_qkv(const mmdit_dims* d, const BlockPlan& p, int s, cons
   g.ep.seq_offset = (p.single || s == 0) ? 0 : p.Si;
   g.ep.seq_joint = p.S, g.ep.seq_pad = p.S_pad, g.ep.heads = p.H, g.ep.hidden = p.D;
   g.ep.rms_eps = d->rms_eps, g.ep.rope_interleaved = d->rope_interleaved ? 1 : 0;
-  MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "QKV projection");
+  { ProfScope ps_(p.single ? "single.qkv" : (s == 0 ? "double.qkv.img" : "double.qkv.txt"), st);
+  MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "QKV projection"); }
   return MMDIT_OK;
 }
 
@@ -231,21 +273,25 @@ mmdit_status run_stream_post(const mmdit_dims* d, const BlockPlan& p, int s, con
   g.A = at(ws, p.o[s]), g.W = w->w_o;
   g.ep.bias = w->b_o, g.ep.resid = x, g.ep.gate = mod + 2 * p.D, g.ep.gate_bstride = 6 * p.D;
   g.ep.rows_per_batch = rows_per_batch, g.ep.out = at(ws, p.x1[s]);
-  MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "attention output projection");
+  { ProfScope ps_(p.single ? "single.out" : (s == 0 ? "double.out.img" : "double.out.txt"), st);
+  MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "attention output projection"); }
+  { ProfScope ps_(p.single ? "single.ln2" : (s == 0 ? "double.ln2.img" : "double.ln2.txt"), st);
   MMDIT_CUDA(launch_ln_modulate(d->act, at(ws, p.x1[s]), mod + 3 * p.D, mod + 4 * p.D, 6 * p.D, rows,
                                 rows_per_batch, p.D, d->ln_eps, at(ws, p.h[s]), st),
-             "LayerNorm-modulate (MLP branch)");
+             "LayerNorm-modulate (MLP branch)"); }
   GemmProblem f1;
   f1.act = d->act, f1.epi = kEpiGelu, f1.M = rows, f1.N = p.F, f1.K = p.D;
   f1.A = at(ws, p.h[s]), f1.W = w->w_1;
   f1.ep.bias = w->b_1, f1.ep.gelu_tanh = d->gelu_tanh, f1.ep.out = at(ws, p.u[s]);
-  MMDIT_CUDA(launch_gemm(f1, status_word(ws), st), "MLP fc1 + GELU");
+  { ProfScope ps_(p.single ? "single.fc1" : (s == 0 ? "double.fc1.img" : "double.fc1.txt"), st);
+  MMDIT_CUDA(launch_gemm(f1, status_word(ws), st), "MLP fc1 + GELU"); }
   GemmProblem f2;
   f2.act = d->act, f2.epi = kEpiGateResid, f2.M = rows, f2.N = p.D, f2.K = p.F;
   f2.A = at(ws, p.u[s]), f2.W = w->w_2;
   f2.ep.bias = w->b_2, f2.ep.resid = at(ws, p.x1[s]), f2.ep.gate = mod + 5 * p.D;
   f2.ep.gate_bstride = 6 * p.D, f2.ep.rows_per_batch = rows_per_batch, f2.ep.out = y;
-  MMDIT_CUDA(launch_gemm(f2, status_word(ws), st), "MLP fc2 + gated residual");
+  { ProfScope ps_(p.single ? "single.fc2" : (s == 0 ? "double.fc2.img" : "double.fc2.txt"), st);
+  MMDIT_CUDA(launch_gemm(f2, status_word(ws), st), "MLP fc2 + gated residual"); }
   return MMDIT_OK;
 }
 
@@ -257,7 +303,8 @@ mmdit_status run_attention(const BlockPlan& p, int act, void* ws, cudaStream_t s
   a.vt = at<__nv_bfloat16>(ws, p.vt);
   a.out0 = at(ws, p.o[0]);
   a.out1 = p.single ? nullptr : at(ws, p.o[1]);
-  MMDIT_CUDA(launch_attention(a, status_word(ws), st), "joint attention");
+  { ProfScope ps_(p.single ? "single.attention" : "double.attention", st);
+  MMDIT_CUDA(launch_attention(a, status_word(ws), st), "joint attention"); }
   return MMDIT_OK;
 }
 
@@ -269,6 +316,30 @@ const char* mmdit_last_error(void) { return g_err; }
 
 uint64_t mmdit_launch_count(void) { return g_launches; }
 void mmdit_launch_count_reset(void) { g_launches = 0; }
+
+void mmdit_profile_enable(int32_t on) { g_prof_on = on != 0; }
+
+int32_t mmdit_profile_collect(void* stream, char* names_out, size_t names_len, float* ms_out,
+                              int32_t max_entries) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
+  int32_t n = 0;
+  size_t used = 0;
+  bool ok = true;
+  for (int i = 0; i < g_prof_n; ++i) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_prof[i].start, g_prof[i].stop) != cudaSuccess) ok = false;
+    const size_t len = strlen(g_prof[i].name) + 1;
+    if (n < max_entries && ms_out && names_out && used + len <= names_len) {
+      memcpy(names_out + used, g_prof[i].name, len);
+      used += len;
+      ms_out[n++] = ms;
+    }
+    cudaEventDestroy(g_prof[i].start);
+    cudaEventDestroy(g_prof[i].stop);
+  }
+  g_prof_n = 0;
+  return ok ? n : -1;
+}
 
 mmdit_status mmdit_workspace_status(void* workspace, uint32_t* bits_out, void* stream) {
   if (!workspace) return fail(MMDIT_ERR_INVALID_ARG, "workspace is NULL");
@@ -297,6 +368,7 @@ mmdit_status rope3d_freqs(const float* ids, int32_t batch, int32_t seq, const in
   if (static_cast<int64_t>(batch) * seq == 0) return MMDIT_OK;
   if (!ids || !cos_out || !sin_out) return fail(MMDIT_ERR_INVALID_ARG, "NULL ids or output");
   const int axes[3] = {axes_dim[0], axes_dim[1], axes_dim[2]};
+  ProfScope ps_("rope3d_freqs", static_cast<cudaStream_t>(stream));
   MMDIT_CUDA(launch_rope3d(ids, batch, seq, axes, theta, cos_out, sin_out,
                            static_cast<cudaStream_t>(stream)),
              "rope3d_freqs");
@@ -332,6 +404,7 @@ mmdit_status flow_match_noise_and_loss(int32_t dtype, const void* z0, const void
   const int64_t n = static_cast<int64_t>(batch) * n_per_sample;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  ProfScope ps_(pred ? (z_t ? "flow_match.noise_loss" : "flow_match.loss") : "flow_match.noise", st);
   MMDIT_CUDA(launch_flow_match(dtype, z0, z1, t, batch, n_per_sample, z_t, pred, loss,
                                at<float>(workspace, kStatusBytes), flow_partial_blocks(n), st),
              "flow_match_noise_and_loss");
@@ -358,6 +431,7 @@ mmdit_status mmdit_linear_fwd(int32_t act, int32_t M, int32_t N, int32_t K, cons
   GemmProblem g;
   g.act = act, g.epi = kEpiBias, g.M = M, g.N = N, g.K = K, g.A = x, g.W = w;
   g.ep.bias = b, g.ep.out = y;
+  ProfScope ps_("linear", st);
   MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "linear");
   return MMDIT_OK;
 }
@@ -388,6 +462,7 @@ mmdit_status mmdit_img_in_fwd(int32_t act, int32_t batch, int32_t channels, int3
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
   void* tokens = at(workspace, kStatusBytes);
   const int hw = lat_h * lat_w;
+  ProfScope ps_("img_in", st);
   MMDIT_CUDA(launch_patchify(act, z, batch, channels, hw, tokens, st), "patchify");
   GemmProblem g;
   g.act = act, g.epi = kEpiBias, g.M = batch * hw, g.N = hidden, g.K = channels;
@@ -427,6 +502,7 @@ mmdit_status mmdit_final_layer_fwd(const mmdit_dims* d, int32_t channels, int32_
   float* mod = at<float>(workspace, c.take(static_cast<size_t>(d->batch) * 2 * d->hidden * 4));
   void* h = at(workspace, c.take(static_cast<size_t>(d->batch) * d->seq_img * d->hidden * elt_bytes(d->act)));
   const int D = d->hidden, rows = d->batch * d->seq_img;
+  ProfScope ps_("final_layer", st);
   MMDIT_CUDA(launch_modulation(d->act, vec, w_ada, b_ada, d->batch, 2 * D, D, mod, st), "final modulation");
   MMDIT_CUDA(launch_ln_modulate(d->act, x_img, mod, mod + D, 2 * D, rows, d->seq_img, D, d->ln_eps, h, st),
              "final LayerNorm-modulate");
@@ -462,6 +538,7 @@ mmdit_status mmdit_attention_fwd(int32_t act, int32_t batch, int32_t heads, int3
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
   const int seq_pad = static_cast<int>(round_up(static_cast<size_t>(seq), 8));
   __nv_bfloat16* vt = at<__nv_bfloat16>(workspace, kStatusBytes);
+  ProfScope ps_("attention", st);
   MMDIT_CUDA(launch_transpose_v(static_cast<const __nv_bfloat16*>(v), batch * heads, seq, seq_pad, vt, st),
              "V transpose");
   AttnProblem a;

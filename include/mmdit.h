@@ -119,6 +119,17 @@ mmdit_status mmdit_workspace_status(void *workspace, uint32_t *bits_out, void *s
 uint64_t mmdit_launch_count(void);
 void mmdit_launch_count_reset(void);
 
+/* Per-step timing for diagnostics.  While enabled (on != 0) on the calling thread, every
+ * library step (one named kernel, or a short fixed group such as the modulation GEMV) is
+ * bracketed by two CUDA events recorded on the caller's stream.  mmdit_profile_collect
+ * synchronises `stream`, writes up to max_entries records -- the step name (NUL-separated in
+ * names_out, at most names_len bytes in total) and its duration in milliseconds (ms_out) --
+ * clears the record and returns the number of records (or -1 on a CUDA error).  Enabling and
+ * collecting must not overlap a stream capture. */
+void mmdit_profile_enable(int32_t on);
+int32_t mmdit_profile_collect(void *stream, char *names_out, size_t names_len, float *ms_out,
+                              int32_t max_entries);
+
 /* ---------------------------------------------------------------------------------------
  * 3D RoPE tables ([ARCH] §Model components, 2. Position embeddings (3D RoPE), and
  * §Mathematical formulation, 3D RoPE mathematics; [API] §Position embeddings, EmbedND).
