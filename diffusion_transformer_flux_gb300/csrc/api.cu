@@ -158,7 +158,8 @@ static bool plan_block(const mmdit_dims* d, bool single, BlockPlan* p) {
   p->k = c.take(B * D * S * 2);
   p->vt = c.take(B * D * static_cast<size_t>(p->S_pad) * 2);
   for (int s = 0; s < 2; ++s) p->o[s] = s < ns ? c.take(rows[s] * D * p->elt) : 0;
-  for (int s = 0; s < 2; ++s) p->x1[s] = s < ns ? c.take(rows[s] * D * p->elt) : 0;
+  // the in-block residual x1 stays fp32 so the output is rounded to the activation type once
+  for (int s = 0; s < 2; ++s) p->x1[s] = s < ns ? c.take(rows[s] * D * 4) : 0;
   for (int s = 0; s < 2; ++s) p->u[s] = s < ns ? c.take(rows[s] * F * p->elt) : 0;
   p->total = c.off;
   return true;
@@ -243,7 +244,7 @@ mmdit_status run_stream_qkv(const mmdit_dims* d, const BlockPlan& p, int s, cons
   MMDIT_CUDA(launch_modulation(d->act, vec, w->w_mod, w->b_mod, p.B, 6 * p.D, p.D, mod, st),
              "modulation"); }
   { ProfScope ps_(p.single ? "single.ln1" : (s == 0 ? "double.ln1.img" : "double.ln1.txt"), st);
-  MMDIT_CUDA(launch_ln_modulate(d->act, x, mod, mod + p.D, 6 * p.D, rows, rows_per_batch, p.D,
+  MMDIT_CUDA(launch_ln_modulate(d->act, d->act == MMDIT_F32, x, mod, mod + p.D, 6 * p.D, rows, rows_per_batch, p.D,
                                 d->ln_eps, at(ws, p.h[s]), st),
              "LayerNorm-modulate (attention branch)"); }
   GemmProblem g;
@@ -272,11 +273,11 @@ mmdit_status run_stream_post(const mmdit_dims* d, const BlockPlan& p, int s, con
   g.act = d->act, g.epi = kEpiGateResid, g.M = rows, g.N = p.D, g.K = p.D;
   g.A = at(ws, p.o[s]), g.W = w->w_o;
   g.ep.bias = w->b_o, g.ep.resid = x, g.ep.gate = mod + 2 * p.D, g.ep.gate_bstride = 6 * p.D;
-  g.ep.rows_per_batch = rows_per_batch, g.ep.out = at(ws, p.x1[s]);
+  g.ep.rows_per_batch = rows_per_batch, g.ep.out = at(ws, p.x1[s]), g.ep.out_f32 = 1;
   { ProfScope ps_(p.single ? "single.out" : (s == 0 ? "double.out.img" : "double.out.txt"), st);
   MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "attention output projection"); }
   { ProfScope ps_(p.single ? "single.ln2" : (s == 0 ? "double.ln2.img" : "double.ln2.txt"), st);
-  MMDIT_CUDA(launch_ln_modulate(d->act, at(ws, p.x1[s]), mod + 3 * p.D, mod + 4 * p.D, 6 * p.D, rows,
+  MMDIT_CUDA(launch_ln_modulate(d->act, 1, at(ws, p.x1[s]), mod + 3 * p.D, mod + 4 * p.D, 6 * p.D, rows,
                                 rows_per_batch, p.D, d->ln_eps, at(ws, p.h[s]), st),
              "LayerNorm-modulate (MLP branch)"); }
   GemmProblem f1;
@@ -288,7 +289,7 @@ mmdit_status run_stream_post(const mmdit_dims* d, const BlockPlan& p, int s, con
   GemmProblem f2;
   f2.act = d->act, f2.epi = kEpiGateResid, f2.M = rows, f2.N = p.D, f2.K = p.F;
   f2.A = at(ws, p.u[s]), f2.W = w->w_2;
-  f2.ep.bias = w->b_2, f2.ep.resid = at(ws, p.x1[s]), f2.ep.gate = mod + 5 * p.D;
+  f2.ep.bias = w->b_2, f2.ep.resid = at(ws, p.x1[s]), f2.ep.resid_f32 = 1, f2.ep.gate = mod + 5 * p.D;
   f2.ep.gate_bstride = 6 * p.D, f2.ep.rows_per_batch = rows_per_batch, f2.ep.out = y;
   { ProfScope ps_(p.single ? "single.fc2" : (s == 0 ? "double.fc2.img" : "double.fc2.txt"), st);
   MMDIT_CUDA(launch_gemm(f2, status_word(ws), st), "MLP fc2 + gated residual"); }
@@ -504,7 +505,7 @@ mmdit_status mmdit_final_layer_fwd(const mmdit_dims* d, int32_t channels, int32_
   const int D = d->hidden, rows = d->batch * d->seq_img;
   ProfScope ps_("final_layer", st);
   MMDIT_CUDA(launch_modulation(d->act, vec, w_ada, b_ada, d->batch, 2 * D, D, mod, st), "final modulation");
-  MMDIT_CUDA(launch_ln_modulate(d->act, x_img, mod, mod + D, 2 * D, rows, d->seq_img, D, d->ln_eps, h, st),
+  MMDIT_CUDA(launch_ln_modulate(d->act, d->act == MMDIT_F32, x_img, mod, mod + D, 2 * D, rows, d->seq_img, D, d->ln_eps, h, st),
              "final LayerNorm-modulate");
   GemmProblem g;
   g.act = d->act, g.epi = kEpiUnpatchify, g.M = rows, g.N = channels, g.K = D;

@@ -110,8 +110,9 @@ __device__ __forceinline__ void softmax_role(AttnSmem* sb, uint8_t* s_p, uint32_
     for (int i = 0; i < 64; ++i) {
       const float p0 = fast_exp2(fmaf(s[2 * i], kScaleLog2, -m_run));
       const float p1 = fast_exp2(fmaf(s[2 * i + 1], kScaleLog2, -m_run));
-      sum += p0 + p1;
       pk[i] = pack_bf16x2(p0, p1);
+      // normalise by the sum of the rounded weights that the PV product actually uses
+      sum += bf16_lo(pk[i]) + bf16_hi(pk[i]);
     }
     // P_j goes to buffer j&1 once PV_{j-2} has finished reading it.
     w = mbar_wait(&sb->p_free[buf], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag, status,

@@ -110,8 +110,8 @@ __global__ void __launch_bounds__(256) modulation_kernel(const T* __restrict__ v
 // ----------------------------------------------------------------------------- LN + modulate
 // One warp per row: mean, biased variance (two passes over the L1-resident row), then
 // out = (x - mean) * rsqrt(var + eps) * (1 + scale[b]) + shift[b].
-template <typename T>
-__global__ void __launch_bounds__(256) ln_modulate_kernel(const T* __restrict__ x,
+template <typename TI, typename T>
+__global__ void __launch_bounds__(256) ln_modulate_kernel(const TI* __restrict__ x,
                                                           const float* __restrict__ shift,
                                                           const float* __restrict__ scale,
                                                           int64_t mod_bstride, int rows, int rpb,
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(256) ln_modulate_kernel(const T* __restrict__ 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * (blockDim.x >> 5) + warp;
   if (r >= rows) return;
-  const T* xr = x + static_cast<size_t>(r) * dim;
+  const TI* xr = x + static_cast<size_t>(r) * dim;
   float s = 0.f;
   for (int k = lane * 8; k < dim; k += 256) {
     float v[8];
@@ -313,19 +313,23 @@ cudaError_t launch_modulation(int act, const void* vec, const void* w, const voi
   return cudaSuccess;
 }
 
-cudaError_t launch_ln_modulate(int act, const void* x, const float* shift, const float* scale,
+cudaError_t launch_ln_modulate(int act, int x_f32, const void* x, const float* shift, const float* scale,
                                int64_t mod_bstride, int rows, int rows_per_batch, int dim, float eps,
                                void* out, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   const int grid = (rows + 7) / 8;
-  if (act == 1)
-    ln_modulate_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+  if (act == 1 && x_f32)
+    ln_modulate_kernel<float, __nv_bfloat16><<<grid, 256, 0, stream>>>(
+        static_cast<const float*>(x), shift, scale, mod_bstride, rows, rows_per_batch, dim, eps,
+        static_cast<__nv_bfloat16*>(out));
+  else if (act == 1)
+    ln_modulate_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(x), shift, scale, mod_bstride, rows, rows_per_batch, dim,
         eps, static_cast<__nv_bfloat16*>(out));
   else
-    ln_modulate_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float*>(x), shift, scale,
-                                                        mod_bstride, rows, rows_per_batch, dim, eps,
-                                                        static_cast<float*>(out));
+    ln_modulate_kernel<float, float><<<grid, 256, 0, stream>>>(
+        static_cast<const float*>(x), shift, scale, mod_bstride, rows, rows_per_batch, dim, eps,
+        static_cast<float*>(out));
   count_launch();
   return cudaGetLastError();
 }

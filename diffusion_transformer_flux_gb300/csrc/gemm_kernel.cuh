@@ -170,7 +170,10 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t taddr, int m, int n0, int
         const int b = m / ep.rows_per_batch;
         float g[32], x[32];
         load32(ep.gate + static_cast<size_t>(b) * ep.gate_bstride + n, g);
-        load32(reinterpret_cast<const T*>(ep.resid) + static_cast<size_t>(m) * N + n, x);
+        if (ep.resid_f32)
+          load32(reinterpret_cast<const float*>(ep.resid) + static_cast<size_t>(m) * N + n, x);
+        else
+          load32(reinterpret_cast<const T*>(ep.resid) + static_cast<size_t>(m) * N + n, x);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = fmaf(g[i], v[i], x[i]);
       }
@@ -180,6 +183,8 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t taddr, int m, int n0, int
                      (static_cast<size_t>(b) * N + n) * ep.rows_per_batch + s;
 #pragma unroll
         for (int i = 0; i < 32; ++i) dst[static_cast<size_t>(i) * ep.rows_per_batch] = v[i];
+      } else if (ep.out_f32) {
+        store32(reinterpret_cast<float*>(ep.out) + static_cast<size_t>(m) * N + n, v);
       } else {
         store32(reinterpret_cast<T*>(ep.out) + static_cast<size_t>(m) * N + n, v);
       }

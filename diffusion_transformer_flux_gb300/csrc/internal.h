@@ -21,7 +21,9 @@ enum EpiKind : int {
 struct EpiArgs {
   const void* bias = nullptr;  // [N], activation type, may be null
   void* out = nullptr;         // [M, N] activation type (fp32 [B, N, rows_per_batch] for unpatchify)
+  int out_f32 = 0;             // store `out` as fp32 whatever the operand type
   const void* resid = nullptr; // [M, N] (gated residual)
+  int resid_f32 = 0;           // `resid` is fp32 whatever the operand type
   const float* gate = nullptr; // gate for batch b at gate + b * gate_bstride
   int64_t gate_bstride = 0;
   int rows_per_batch = 1;      // m -> (b = m / rows_per_batch, s = m % rows_per_batch)
@@ -93,7 +95,8 @@ cudaError_t launch_rope3d(const float* ids, int batch, int seq, const int axes[3
 cudaError_t launch_modulation(int act, const void* vec, const void* w, const void* bias, int batch,
                               int rows, int dim, float* m, cudaStream_t stream);
 // out[r, :] = LN(x[r, :]) * (1 + scale[b]) + shift[b], b = r / rows_per_batch; x, out [R, D].
-cudaError_t launch_ln_modulate(int act, const void* x, const float* shift, const float* scale,
+// x is fp32 when x_f32 != 0, else of the activation type; out is of the activation type.
+cudaError_t launch_ln_modulate(int act, int x_f32, const void* x, const float* shift, const float* scale,
                                int64_t mod_bstride, int rows, int rows_per_batch, int dim, float eps,
                                void* out, cudaStream_t stream);
 // z [B, C, HW] fp32 -> tokens [B, HW, C] of the activation type.
