@@ -30,6 +30,11 @@ design notes of the repository as well):
     chunks, over the whole concatenated sequence, and returns every row.
   * The output head takes (shift, scale) from a SiLU + linear of ``vec``.
   * Loss is the mean over all elements.
+  * Precision: by default every step runs in float64.  ``mm_cast=round_bf16`` evaluates the
+    method at the precision the pages fix for training, bf16 autocast (architecture page,
+    §Performance optimizations › 5. Mixed precision; API page, §Optimization tips): the
+    operands of every matrix product (each linear layer and both attention products) are
+    rounded to bf16; everything else stays float64.
 """
 from __future__ import annotations
 
@@ -47,6 +52,25 @@ F64 = np.float64
 
 def _f64(x):
     return np.asarray(x, dtype=F64)
+
+
+def round_bf16(x):
+    """Nearest bfloat16 value (8 significant bits, exponent range of float32, ties to even).
+
+    bfloat16 keeps the sign and 8-bit exponent of IEEE binary32 and 7 stored fraction bits, so
+    a normal value with leading bit 2^e is rounded to a multiple of 2^(e-7); below the float32
+    normal range the quantum stays 2^-133.  Computed directly from float64 (no double rounding).
+    """
+    x = _f64(x)
+    mag = np.abs(x)
+    _, E = np.frexp(np.where(mag > 0, mag, 1.0))  # mag = m * 2^E, m in [0.5, 1)
+    lead = np.maximum(E - 1, -126)
+    quantum = np.ldexp(1.0, lead - 7)
+    return np.where(mag > 0, np.rint(x / quantum) * quantum, x)
+
+
+def _cast(x, mm_cast):
+    return _f64(x) if mm_cast is None else mm_cast(_f64(x))
 
 
 # ----------------------------------------------------------------------------- 3D RoPE
@@ -128,21 +152,21 @@ def gelu(x, tanh=False):
     return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))
 
 
-def linear(x, w, b=None):
-    """y = x W^T + b with W stored [out, in]."""
-    y = _f64(x) @ _f64(w).T
+def linear(x, w, b=None, mm_cast=None):
+    """y = x W^T + b with W stored [out, in]; ``mm_cast`` rounds the two matmul operands."""
+    y = _cast(x, mm_cast) @ _cast(w, mm_cast).T
     return y if b is None else y + _f64(b)
 
 
 # ----------------------------------------------------------------------------- AdaLN
-def modulation(vec, w_mod, b_mod, n_chunks=6):
+def modulation(vec, w_mod, b_mod, n_chunks=6, mm_cast=None):
     """AdaLN.forward: Linear(SiLU(vec)) split into chunks along the feature axis.
 
     API page, §Normalization › AdaLN (six chunks named shift, scale, gate,
     shift_mlp, scale_mlp, gate_mlp, in that order); architecture page,
     §Implementation details › Adaptive layer normalization.
     """
-    m = linear(silu(vec), w_mod, b_mod)  # [B, n*D]
+    m = linear(silu(vec), w_mod, b_mod, mm_cast)  # [B, n*D]
     return np.split(m, n_chunks, axis=-1)
 
 
@@ -157,19 +181,20 @@ def gated_residual(x, gate, y):
 
 
 # ----------------------------------------------------------------------------- attention
-def attention(q, k, v):
+def attention(q, k, v, mm_cast=None):
     """softmax(q k^T / sqrt(d)) v over the key axis, no mask.  q,k,v: [..., S, d].
 
     Architecture page, §Implementation details › Attention implementation
     (no mask) and › Joint Attention Trick (one call over the joint sequence).
+    ``mm_cast`` rounds the operands of both products (q, k; the probabilities and v).
     """
-    q, k, v = _f64(q), _f64(k), _f64(v)
+    q, k, v = _cast(q, mm_cast), _cast(k, mm_cast), _cast(v, mm_cast)
     d = q.shape[-1]
     s = (q @ np.swapaxes(k, -1, -2)) / math.sqrt(d)
     s = s - s.max(axis=-1, keepdims=True)
     p = np.exp(s)
     p = p / p.sum(axis=-1, keepdims=True)
-    return p @ v
+    return _cast(p, mm_cast) @ v
 
 
 # ----------------------------------------------------------------------------- block pieces
@@ -185,7 +210,7 @@ def _merge(x):
     return x.transpose(0, 2, 1, 3).reshape(B, S, H * d)
 
 
-def qkv_heads(x, shift, scale, w, heads, ln_eps=LN_EPS, rms_eps=RMS_EPS):
+def qkv_heads(x, shift, scale, w, heads, ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast=None):
     """Attention-branch pre-norm and projection of one stream, before RoPE.
 
     Architecture page, §3. MMDiT layer (double block), steps 1-2:
@@ -193,21 +218,22 @@ def qkv_heads(x, shift, scale, w, heads, ln_eps=LN_EPS, rms_eps=RMS_EPS):
     RMSNorm of q and k.  Returns q, k, v as [B, H, S, d].
     """
     h = modulate(x, shift, scale, ln_eps)
-    qkv = linear(h, w["w_qkv"], w["b_qkv"])
+    qkv = linear(h, w["w_qkv"], w["b_qkv"], mm_cast)
     q, k, v = np.split(qkv, 3, axis=-1)
     q = rmsnorm(_heads(q, heads), w["g_q"], rms_eps)
     k = rmsnorm(_heads(k, heads), w["g_k"], rms_eps)
     return q, k, _heads(v, heads)
 
 
-def mlp_branch(x, shift, scale, w, gelu_tanh=False, ln_eps=LN_EPS):
+def mlp_branch(x, shift, scale, w, gelu_tanh=False, ln_eps=LN_EPS, mm_cast=None):
     """Architecture page, §3. MMDiT layer, step 4: AdaLN -> Linear -> GELU -> Linear."""
     h = modulate(x, shift, scale, ln_eps)
-    return linear(gelu(linear(h, w["w_1"], w["b_1"]), gelu_tanh), w["w_2"], w["b_2"])
+    u = gelu(linear(h, w["w_1"], w["b_1"], mm_cast), gelu_tanh)
+    return linear(u, w["w_2"], w["b_2"], mm_cast)
 
 
 def double_block(x_img, x_txt, vec, cos, sin, w_img, w_txt, heads,
-                 interleaved=True, gelu_tanh=False, ln_eps=LN_EPS, rms_eps=RMS_EPS):
+                 interleaved=True, gelu_tanh=False, ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast=None):
     """Double-stream (joint) block forward.
 
     Architecture page, §Model components › 3. MMDiT layer (double block);
@@ -215,28 +241,29 @@ def double_block(x_img, x_txt, vec, cos, sin, w_img, w_txt, heads,
     ``[B, S_img + S_txt, d/2]`` in the joint order [image; text].
     Returns (y_img, y_txt).
     """
+    c = mm_cast
     S_i = np.shape(x_img)[1]
-    mi = modulation(vec, w_img["w_mod"], w_img["b_mod"])
-    mt = modulation(vec, w_txt["w_mod"], w_txt["b_mod"])
-    qi, ki, vi = qkv_heads(x_img, mi[0], mi[1], w_img, heads, ln_eps, rms_eps)
-    qt, kt, vt = qkv_heads(x_txt, mt[0], mt[1], w_txt, heads, ln_eps, rms_eps)
+    mi = modulation(vec, w_img["w_mod"], w_img["b_mod"], mm_cast=c)
+    mt = modulation(vec, w_txt["w_mod"], w_txt["b_mod"], mm_cast=c)
+    qi, ki, vi = qkv_heads(x_img, mi[0], mi[1], w_img, heads, ln_eps, rms_eps, c)
+    qt, kt, vt = qkv_heads(x_txt, mt[0], mt[1], w_txt, heads, ln_eps, rms_eps, c)
     q = np.concatenate([qi, qt], axis=2)
     k = np.concatenate([ki, kt], axis=2)
     v = np.concatenate([vi, vt], axis=2)
-    c, s = _f64(cos)[:, None], _f64(sin)[:, None]
-    q = apply_rope(q, c, s, interleaved)
-    k = apply_rope(k, c, s, interleaved)
-    o = _merge(attention(q, k, v))
+    cs, sn = _f64(cos)[:, None], _f64(sin)[:, None]
+    q = apply_rope(q, cs, sn, interleaved)
+    k = apply_rope(k, cs, sn, interleaved)
+    o = _merge(attention(q, k, v, c))
     o_img, o_txt = o[:, :S_i], o[:, S_i:]
-    x_img = gated_residual(x_img, mi[2], linear(o_img, w_img["w_o"], w_img["b_o"]))
-    x_txt = gated_residual(x_txt, mt[2], linear(o_txt, w_txt["w_o"], w_txt["b_o"]))
-    x_img = gated_residual(x_img, mi[5], mlp_branch(x_img, mi[3], mi[4], w_img, gelu_tanh, ln_eps))
-    x_txt = gated_residual(x_txt, mt[5], mlp_branch(x_txt, mt[3], mt[4], w_txt, gelu_tanh, ln_eps))
+    x_img = gated_residual(x_img, mi[2], linear(o_img, w_img["w_o"], w_img["b_o"], c))
+    x_txt = gated_residual(x_txt, mt[2], linear(o_txt, w_txt["w_o"], w_txt["b_o"], c))
+    x_img = gated_residual(x_img, mi[5], mlp_branch(x_img, mi[3], mi[4], w_img, gelu_tanh, ln_eps, c))
+    x_txt = gated_residual(x_txt, mt[5], mlp_branch(x_txt, mt[3], mt[4], w_txt, gelu_tanh, ln_eps, c))
     return x_img, x_txt
 
 
 def single_block(x, vec, cos, sin, w, heads, interleaved=True, gelu_tanh=False,
-                 ln_eps=LN_EPS, rms_eps=RMS_EPS):
+                 ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast=None):
     """Single-stream block forward over the concatenated sequence ``x = [img; txt]``.
 
     Architecture page, §Model components › 4. Flux single block: AdaLN,
@@ -244,67 +271,71 @@ def single_block(x, vec, cos, sin, w, heads, interleaved=True, gelu_tanh=False,
     weight set.  Returns all rows (the caller keeps the image rows after the
     last single block).
     """
-    m = modulation(vec, w["w_mod"], w["b_mod"])
-    q, k, v = qkv_heads(x, m[0], m[1], w, heads, ln_eps, rms_eps)
-    c, s = _f64(cos)[:, None], _f64(sin)[:, None]
-    q = apply_rope(q, c, s, interleaved)
-    k = apply_rope(k, c, s, interleaved)
-    o = _merge(attention(q, k, v))
-    x = gated_residual(x, m[2], linear(o, w["w_o"], w["b_o"]))
-    return gated_residual(x, m[5], mlp_branch(x, m[3], m[4], w, gelu_tanh, ln_eps))
+    c = mm_cast
+    m = modulation(vec, w["w_mod"], w["b_mod"], mm_cast=c)
+    q, k, v = qkv_heads(x, m[0], m[1], w, heads, ln_eps, rms_eps, c)
+    cs, sn = _f64(cos)[:, None], _f64(sin)[:, None]
+    q = apply_rope(q, cs, sn, interleaved)
+    k = apply_rope(k, cs, sn, interleaved)
+    o = _merge(attention(q, k, v, c))
+    x = gated_residual(x, m[2], linear(o, w["w_o"], w["b_o"], c))
+    return gated_residual(x, m[5], mlp_branch(x, m[3], m[4], w, gelu_tanh, ln_eps, c))
 
 
 # ----------------------------------------------------------------------------- row-sampled blocks
-def _rows_after_attention(x_rows, o_rows, m, w, gelu_tanh, ln_eps):
-    x1 = gated_residual(x_rows, m[2], linear(o_rows, w["w_o"], w["b_o"]))
-    return gated_residual(x1, m[5], mlp_branch(x1, m[3], m[4], w, gelu_tanh, ln_eps))
+def _rows_after_attention(x_rows, o_rows, m, w, gelu_tanh, ln_eps, mm_cast):
+    x1 = gated_residual(x_rows, m[2], linear(o_rows, w["w_o"], w["b_o"], mm_cast))
+    return gated_residual(x1, m[5], mlp_branch(x1, m[3], m[4], w, gelu_tanh, ln_eps, mm_cast))
 
 
-def _attend_rows(q_rows, k, v, c_rows, s_rows, c_all, s_all, interleaved):
+def _attend_rows(q_rows, k, v, c_rows, s_rows, c_all, s_all, interleaved, mm_cast):
     q = apply_rope(q_rows, c_rows[:, None], s_rows[:, None], interleaved)
     kk = apply_rope(k, c_all[:, None], s_all[:, None], interleaved)
-    return _merge(attention(q, kk, v))
+    return _merge(attention(q, kk, v, mm_cast))
 
 
 def double_block_rows(x_img, x_txt, vec, cos, sin, w_img, w_txt, heads, rows_img, rows_txt,
-                      interleaved=True, gelu_tanh=False, ln_eps=LN_EPS, rms_eps=RMS_EPS):
+                      interleaved=True, gelu_tanh=False, ln_eps=LN_EPS, rms_eps=RMS_EPS,
+                      mm_cast=None):
     """The double block's output at selected rows only (same batch rows for every sample).
 
     Keys and values need every token; queries, attention, the output
     projection and the MLP are row-wise, so computing them for a subset of
     rows gives those rows of ``double_block`` exactly.
     """
+    c = mm_cast
     S_i = np.shape(x_img)[1]
-    mi = modulation(vec, w_img["w_mod"], w_img["b_mod"])
-    mt = modulation(vec, w_txt["w_mod"], w_txt["b_mod"])
+    mi = modulation(vec, w_img["w_mod"], w_img["b_mod"], mm_cast=c)
+    mt = modulation(vec, w_txt["w_mod"], w_txt["b_mod"], mm_cast=c)
     # keys/values for every token (queries are recomputed only for the chosen rows)
-    _, ki, vi = qkv_heads(x_img, mi[0], mi[1], w_img, heads, ln_eps, rms_eps)
-    _, kt, vt = qkv_heads(x_txt, mt[0], mt[1], w_txt, heads, ln_eps, rms_eps)
+    _, ki, vi = qkv_heads(x_img, mi[0], mi[1], w_img, heads, ln_eps, rms_eps, c)
+    _, kt, vt = qkv_heads(x_txt, mt[0], mt[1], w_txt, heads, ln_eps, rms_eps, c)
     k = np.concatenate([ki, kt], axis=2)
     v = np.concatenate([vi, vt], axis=2)
     cos, sin = _f64(cos), _f64(sin)
     rows_img = np.asarray(rows_img)
     rows_txt = np.asarray(rows_txt)
-    qi, _, _ = qkv_heads(_f64(x_img)[:, rows_img], mi[0], mi[1], w_img, heads, ln_eps, rms_eps)
-    qt, _, _ = qkv_heads(_f64(x_txt)[:, rows_txt], mt[0], mt[1], w_txt, heads, ln_eps, rms_eps)
+    qi, _, _ = qkv_heads(_f64(x_img)[:, rows_img], mi[0], mi[1], w_img, heads, ln_eps, rms_eps, c)
+    qt, _, _ = qkv_heads(_f64(x_txt)[:, rows_txt], mt[0], mt[1], w_txt, heads, ln_eps, rms_eps, c)
     jr_i, jr_t = rows_img, S_i + rows_txt
-    oi = _attend_rows(qi, k, v, cos[:, jr_i], sin[:, jr_i], cos, sin, interleaved)
-    ot = _attend_rows(qt, k, v, cos[:, jr_t], sin[:, jr_t], cos, sin, interleaved)
-    yi = _rows_after_attention(_f64(x_img)[:, rows_img], oi, mi, w_img, gelu_tanh, ln_eps)
-    yt = _rows_after_attention(_f64(x_txt)[:, rows_txt], ot, mt, w_txt, gelu_tanh, ln_eps)
+    oi = _attend_rows(qi, k, v, cos[:, jr_i], sin[:, jr_i], cos, sin, interleaved, c)
+    ot = _attend_rows(qt, k, v, cos[:, jr_t], sin[:, jr_t], cos, sin, interleaved, c)
+    yi = _rows_after_attention(_f64(x_img)[:, rows_img], oi, mi, w_img, gelu_tanh, ln_eps, c)
+    yt = _rows_after_attention(_f64(x_txt)[:, rows_txt], ot, mt, w_txt, gelu_tanh, ln_eps, c)
     return yi, yt
 
 
 def single_block_rows(x, vec, cos, sin, w, heads, rows, interleaved=True, gelu_tanh=False,
-                      ln_eps=LN_EPS, rms_eps=RMS_EPS):
+                      ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast=None):
     """The single block's output at selected rows only (see ``double_block_rows``)."""
-    m = modulation(vec, w["w_mod"], w["b_mod"])
-    _, k, v = qkv_heads(x, m[0], m[1], w, heads, ln_eps, rms_eps)
+    c = mm_cast
+    m = modulation(vec, w["w_mod"], w["b_mod"], mm_cast=c)
+    _, k, v = qkv_heads(x, m[0], m[1], w, heads, ln_eps, rms_eps, c)
     rows = np.asarray(rows)
-    q, _, _ = qkv_heads(_f64(x)[:, rows], m[0], m[1], w, heads, ln_eps, rms_eps)
+    q, _, _ = qkv_heads(_f64(x)[:, rows], m[0], m[1], w, heads, ln_eps, rms_eps, c)
     cos, sin = _f64(cos), _f64(sin)
-    o = _attend_rows(q, k, v, cos[:, rows], sin[:, rows], cos, sin, interleaved)
-    return _rows_after_attention(_f64(x)[:, rows], o, m, w, gelu_tanh, ln_eps)
+    o = _attend_rows(q, k, v, cos[:, rows], sin[:, rows], cos, sin, interleaved, c)
+    return _rows_after_attention(_f64(x)[:, rows], o, m, w, gelu_tanh, ln_eps, c)
 
 
 # ----------------------------------------------------------------------------- embeddings and head
@@ -322,24 +353,24 @@ def unpatchify(tokens, H, W):
     return t.transpose(0, 2, 1).reshape(B, C, H, W)
 
 
-def img_in(z, w, b):
+def img_in(z, w, b, mm_cast=None):
     """Image path: patchify, then Linear C -> D (architecture page, §1. Input embeddings)."""
-    return linear(patchify(z), w, b)
+    return linear(patchify(z), w, b, mm_cast)
 
 
-def txt_in(txt, w, b):
+def txt_in(txt, w, b, mm_cast=None):
     """Text path: Linear ctx_dim -> D (architecture page, §1. Input embeddings)."""
-    return linear(txt, w, b)
+    return linear(txt, w, b, mm_cast)
 
 
-def final_layer(x_img, vec, w_ada, b_ada, w_out, b_out, H, W, ln_eps=LN_EPS):
+def final_layer(x_img, vec, w_ada, b_ada, w_out, b_out, H, W, ln_eps=LN_EPS, mm_cast=None):
     """Output head: AdaLNContinuous(vec), Linear D -> C, reshape to [B, C, H, W].
 
     Architecture page, §Model components › 5. Output processing; API page,
     §Normalization › AdaLNContinuous.  (shift, scale) = SiLU(vec) W^T + b.
     """
-    shift, scale = modulation(vec, w_ada, b_ada, 2)
-    y = linear(modulate(x_img, shift, scale, ln_eps), w_out, b_out)
+    shift, scale = modulation(vec, w_ada, b_ada, 2, mm_cast)
+    y = linear(modulate(x_img, shift, scale, ln_eps), w_out, b_out, mm_cast)
     return unpatchify(y, H, W)
 
 
