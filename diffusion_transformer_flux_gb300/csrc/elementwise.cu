@@ -69,10 +69,14 @@ __global__ void __launch_bounds__(256) modulation_kernel(const T* __restrict__ v
                                                          const T* __restrict__ bias, int batch,
                                                          int rows, int dim, float* __restrict__ m,
                                                          int64_t m_bstride) {
-  extern __shared__ float svec[];  // [batch, dim] SiLU(vec)
+  extern __shared__ float svec[];  // [batch, dim] SiLU(vec), a bf16 operand in bf16 mode
   for (int i = threadIdx.x; i < batch * dim; i += blockDim.x) {
     const float v = to_f32(vec[i]);
-    svec[i] = v / (1.f + expf(-v));
+    const float sv = v / (1.f + expf(-v));
+    if constexpr (sizeof(T) == 2)
+      svec[i] = __bfloat162float(__float2bfloat16_rn(sv));
+    else
+      svec[i] = sv;
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -1,8 +1,15 @@
 """GPU parity of the double- and single-block forward against the fp64 oracle.
 
-Small shapes (several tiles, ragged tails) are compared element by element on every output,
+The bar (max |err| <= 2e-2 x output RMS) is checked against the oracle at the precision the
+pages fix for training, bf16 autocast (every matrix-product operand rounded to bf16, all other
+arithmetic in float64), allowing in addition half a bf16 ulp per element because the block's
+output is itself stored in bf16.  The distance to the pure float64 oracle is checked too, at
+the looser bound that bf16 operands allow (TOL_VS_FP64).  fp32 workloads (tf32 linears) are
+held to the bar against the pure float64 oracle.
+
+Small shapes (several tiles, ragged tails) are compared element by element on every output
 and on the intermediates the workspace exposes (Q, K, V^T after RMSNorm/RoPE, the attention
-output) so a failure names the step.  The Flux-sized workloads run in the launch
+output), so a failure names the step.  The Flux-sized workloads run in the launch
 configuration the benchmark times and are compared on seeded samples of rows, which the
 oracle computes exactly (every step after attention is row-wise).
 """
@@ -13,7 +20,7 @@ import torch
 from diffusion_transformer_flux_gb300 import _lib as L
 from oracle import flux as O
 
-from gpu_util import BlockCase, assert_parity, host, workspace_view
+from gpu_util import TOL_VS_FP64, BlockCase, assert_parity, host, workspace_view
 
 pytestmark = pytest.mark.gpu
 
@@ -26,53 +33,66 @@ def _lib_loaded():
 
 
 def _check_intermediates(case: BlockCase, ws):
-    """Q, K (normalised and rotated), V^T and the attention output against the oracle.
-
-    These are stored in bf16, so the bound is one bf16 half-ulp at the largest values (about
-    4.5 RMS x 2^-8 ~ 1.8e-2 RMS) plus the arithmetic before the rounding."""
+    """Q, K (normalised and rotated), V^T and the attention output against the oracle at the
+    case's precision; all four are stored in bf16 (half-ulp allowance)."""
+    c = case.mm_cast
     offs = L.mmdit_block_workspace_offsets(case.dims, case.single)
     B, H, S, D = case.B, case.H, case.S, case.D
     S_pad = (S + 7) // 8 * 8
     qs, ks, vs = [], [], []
-    streams = [("img", case.w_img, case.x_joint() if case.single else case.x_img)]
+    streams = [(case.w_img, case.x_joint() if case.single else case.x_img)]
     if not case.single:
-        streams.append(("txt", case.w_txt, case.x_txt))
-    for _, w, x in streams:
-        m = O.modulation(case.vec, w["w_mod"], w["b_mod"])
-        q, k, v = O.qkv_heads(x, m[0], m[1], w, H)
+        streams.append((case.w_txt, case.x_txt))
+    for w, x in streams:
+        m = O.modulation(case.vec, w["w_mod"], w["b_mod"], mm_cast=c)
+        q, k, v = O.qkv_heads(x, m[0], m[1], w, H, mm_cast=c)
         qs.append(q), ks.append(k), vs.append(v)
     q, k, v = (np.concatenate(a, axis=2) for a in (qs, ks, vs))
-    c, s = case.cos[:, None], case.sin[:, None]
-    q = O.apply_rope(q, c, s, case.interleaved)
-    k = O.apply_rope(k, c, s, case.interleaved)
+    cs, sn = case.cos[:, None], case.sin[:, None]
+    q = O.apply_rope(q, cs, sn, case.interleaved)
+    k = O.apply_rope(k, cs, sn, case.interleaved)
     gq = host(workspace_view(ws, offs[2], (B, H, S, 128), torch.bfloat16))
     gk = host(workspace_view(ws, offs[3], (B, H, S, 128), torch.bfloat16))
     gvt = host(workspace_view(ws, offs[4], (B, H, 128, S_pad), torch.bfloat16))[..., :S]
-    assert_parity(gq, q, 2.5e-2, "Q after RMSNorm + RoPE")
-    assert_parity(gk, k, 2.5e-2, "K after RMSNorm + RoPE")
-    assert_parity(gvt, np.swapaxes(v, -1, -2), 2.5e-2, "V^T")
-    o = O.attention(q, k, v).transpose(0, 2, 1, 3).reshape(B, S, D)
+    assert_parity(gq, q, 2e-2, "Q after RMSNorm + RoPE", out_bf16=True)
+    assert_parity(gk, k, 2e-2, "K after RMSNorm + RoPE", out_bf16=True)
+    assert_parity(gvt, np.swapaxes(v, -1, -2), 2e-2, "V^T", out_bf16=True)
+    o = O.attention(q, k, v, c).transpose(0, 2, 1, 3).reshape(B, S, D)
     t = torch.float32 if case.act == "f32" else torch.bfloat16
+    ob = case.act != "f32"
     rows_i = B * (S if case.single else case.S_i)
     go = host(workspace_view(ws, offs[5], (rows_i, D), t)).reshape(B, -1, D)
     if case.single:
-        assert_parity(go, o, 2e-2, "attention output")
+        assert_parity(go, o, 2e-2, "attention output", out_bf16=ob)
     else:
-        assert_parity(go, o[:, :case.S_i], 2e-2, "attention output (image rows)")
+        assert_parity(go, o[:, :case.S_i], 2e-2, "attention output (image rows)", out_bf16=ob)
         if case.S_t:
             got = host(workspace_view(ws, offs[6], (B * case.S_t, D), t)).reshape(B, -1, D)
-            assert_parity(got, o[:, case.S_i:], 2e-2, "attention output (text rows)")
+            assert_parity(got, o[:, case.S_i:], 2e-2, "attention output (text rows)", out_bf16=ob)
 
 
-def _check_outputs(case: BlockCase, got, ref, tol=2e-2):
+def _check_outputs(case: BlockCase, got, rows=None):
+    """The bar on every output, then the distance to the pure float64 oracle."""
     names = ["y"] if case.single else ["y_img", "y_txt"]
     xs = [case.x_joint()] if case.single else [case.x_img, case.x_txt]
-    for n, g, r, x in zip(names, got, ref, xs):
+    bf = case.act != "f32"
+    if rows is None:
+        ref, ref64 = case.oracle(case.mm_cast), case.oracle(None) if bf else None
+        sel = [slice(None)] * len(names)
+    else:
+        ref = case.oracle_rows(*rows, mm_cast=case.mm_cast)
+        ref64 = case.oracle_rows(*rows, mm_cast=None) if bf else None
+        sel = list(rows)
+    for i, (n, g, x) in enumerate(zip(names, got, xs)):
+        r = ref[i]
         if r.size == 0:
             continue
-        assert_parity(g, r, tol, n)
+        g, x = g[:, sel[i]], x[:, sel[i]]
+        assert_parity(g, r, 2e-2, n, out_bf16=bf)
         # the residual dominates the output; the branch alone must also be close
-        assert_parity(g - x, r - x, 0.1, n + " branch (y - x)")
+        assert_parity(g - x, r - x, 0.1, n + " branch (y - x)", out_bf16=bf)
+        if bf:
+            assert_parity(g, ref64[i], TOL_VS_FP64, n + " vs float64 oracle")
 
 
 # ----------------------------------------------------------------------------- small shapes
@@ -90,7 +110,7 @@ def test_double_block_small(B, S_i, S_t, D, H, F, act, inter, tanh):
     case = BlockCase(B, S_i, S_t, D, H, F, act, seed=S_i + D, std=0.05, interleaved=inter,
                      gelu_tanh=tanh)
     got, ws, _ = case.run_gpu()
-    _check_outputs(case, got, case.oracle())
+    _check_outputs(case, got)
     _check_intermediates(case, ws)
 
 
@@ -99,7 +119,7 @@ def test_single_block_small(B, S_i, S_t, D, H, F, act, inter, tanh):
     case = BlockCase(B, S_i, S_t, D, H, F, act, seed=7 + S_i, std=0.05, single=True,
                      interleaved=inter, gelu_tanh=tanh)
     got, ws, _ = case.run_gpu()
-    _check_outputs(case, got, case.oracle())
+    _check_outputs(case, got)
     _check_intermediates(case, ws)
 
 
@@ -114,7 +134,7 @@ def test_tiny_workload_with_flux_init():
 
 def test_block_output_may_alias_input():
     case = BlockCase(2, 130, 40, 256, 2, 1024, "bf16", seed=3, std=0.05)
-    ref = case.oracle()
+    ref = case.oracle(case.mm_cast)
     t = torch.bfloat16
     from gpu_util import dev, upload_weights
     ids = torch.from_numpy(case.ids).cuda()
@@ -126,8 +146,8 @@ def test_block_output_may_alias_input():
                              upload_weights(case.w_txt, "bf16"), dev(case.vec, t), cos, sin, xi, xt,
                              xi, xt)
     torch.cuda.synchronize()
-    assert_parity(host(xi), ref[0], 2e-2, "aliased y_img")
-    assert_parity(host(xt), ref[1], 2e-2, "aliased y_txt")
+    assert_parity(host(xi), ref[0], 2e-2, "aliased y_img", out_bf16=True)
+    assert_parity(host(xt), ref[1], 2e-2, "aliased y_txt", out_bf16=True)
 
 
 # ----------------------------------------------------------------------------- Flux-sized workloads
@@ -143,18 +163,11 @@ def test_double_block_flux_sized_sampled_rows(B, lat, S_t):
     case = BlockCase(B, lat * lat, S_t, 3072, 24, 12288, "bf16", seed=1001 + B, std=0.02,
                      gain_jitter=0.0, lat_hw=(lat, lat))
     got, _, _ = case.run_gpu()
-    ri, rt = _sample(case.S_i, 96, 1), _sample(S_t, 32, 2)
-    yi, yt = case.oracle_rows(ri, rt)
-    assert_parity(got[0][:, ri], yi, 2e-2, "y_img (sampled rows)")
-    assert_parity(got[1][:, rt], yt, 2e-2, "y_txt (sampled rows)")
-    # the residual dominates; a gross error in a branch would still show here
-    assert_parity(got[0][:, ri] - case.x_img[:, ri], yi - case.x_img[:, ri], 0.25, "y_img branch")
+    _check_outputs(case, got, rows=(_sample(case.S_i, 96, 1), _sample(S_t, 32, 2)))
 
 
 def test_single_block_flux_sized_sampled_rows():
     case = BlockCase(1, 4096, 512, 3072, 24, 12288, "bf16", seed=1011, std=0.02, gain_jitter=0.0,
                      lat_hw=(64, 64), single=True)
     got, _, _ = case.run_gpu()
-    rows = _sample(case.S, 128, 3)
-    (y,) = case.oracle_rows(rows)
-    assert_parity(got[0][:, rows], y, 2e-2, "single block y (sampled rows)")
+    _check_outputs(case, got, rows=(_sample(case.S, 128, 3),))

@@ -103,7 +103,7 @@ def test_linear_matches_oracle(act, M, N, K):
     torch.cuda.synchronize()
     assert L.mmdit_workspace_status(ws) == 0
     tol = 2e-2 if act == "bf16" else 5e-3
-    assert_parity(host(y), O.linear(x, w, b), tol, f"linear {act} {M}x{N}x{K}")
+    assert_parity(host(y), O.linear(x, w, b), tol, f"linear {act} {M}x{N}x{K}", out_bf16=act == "bf16")
 
 
 # ----------------------------------------------------------------------------- attention
@@ -122,14 +122,13 @@ def test_attention_matches_oracle(B, H, S, qscale, act):
     ws = L.mmdit_attention_fwd(dev(q), dev(k), dev(v), out)
     torch.cuda.synchronize()
     assert L.mmdit_workspace_status(ws) == 0
-    if S > 1000:
-        rows = np.random.default_rng(0).choice(S, 200, replace=False)
-        ref = O.attention(q[:, :, rows], k, v).transpose(0, 2, 1, 3).reshape(B, len(rows), H * 128)
-        got = host(out)[:, rows]
-    else:
-        ref = O.attention(q, k, v).transpose(0, 2, 1, 3).reshape(B, S, H * 128)
-        got = host(out)
-    assert_parity(got, ref, 2e-2, f"attention B={B} H={H} S={S}")
+    # q, k, v are bf16 already; at the bf16-autocast precision the probabilities are bf16 too
+    rows = np.random.default_rng(0).choice(S, 200, replace=False) if S > 1000 else np.arange(S)
+    ref = O.attention(q[:, :, rows], k, v, O.round_bf16).transpose(0, 2, 1, 3).reshape(B, len(rows), H * 128)
+    ref64 = O.attention(q[:, :, rows], k, v).transpose(0, 2, 1, 3).reshape(B, len(rows), H * 128)
+    got = host(out)[:, rows]
+    assert_parity(got, ref, 2e-2, f"attention B={B} H={H} S={S}", out_bf16=act == "bf16")
+    assert_parity(got, ref64, 5e-2, f"attention B={B} H={H} S={S} vs float64")
 
 
 # ----------------------------------------------------------------------------- embeddings / head
@@ -146,7 +145,7 @@ def test_img_in_matches_oracle(act):
     torch.cuda.synchronize()
     assert L.mmdit_workspace_status(ws) == 0
     zr = synth.bf16_round(z) if act == "bf16" else z  # tokens are held in the activation type
-    assert_parity(host(out), O.img_in(zr, e["w"], e["b"]), 2e-2, "img_in")
+    assert_parity(host(out), O.img_in(zr, e["w"], e["b"]), 2e-2, "img_in", out_bf16=act == "bf16")
 
 
 @pytest.mark.parametrize("act", ["bf16", "f32"])
@@ -165,5 +164,6 @@ def test_final_layer_matches_oracle(act):
                                  dev(f["b_ada"], t), dev(f["w_out"], t), dev(f["b_out"], t), pred)
     torch.cuda.synchronize()
     assert L.mmdit_workspace_status(ws) == 0
-    ref = O.final_layer(x, vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], Hh, Ww)
+    cast = O.round_bf16 if act == "bf16" else None
+    ref = O.final_layer(x, vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], Hh, Ww, mm_cast=cast)
     assert_parity(host(pred), ref, 2e-2, "final layer")
