@@ -1,0 +1,381 @@
+#!/usr/bin/env python3
+"""Benchmark of the Flux MMDiT block forward hot path on GB300 (one process per GPU).
+
+One step is one pass of the whole hot path on the 535M-shaped Flux workload (hidden 3072,
+24 heads x 128, MLP 12288, 4096 image tokens from 64x64x64 latents + 512 text tokens from a
+[1, 512, 4096] text embedding, batch 1):
+
+    rope3d_freqs -> flow-matching noise z_t -> img_in -> txt_in -> double block
+    -> single block -> output head -> flow-matching loss
+
+all through the C ABI of libmmdit.so, with inputs resident in HBM when the timed region
+starts (``value``) or copied from pinned host memory inside it (``e2e``).  The metric is the
+dense-contraction throughput of the two blocks (2 * B * S * D * (3D + D + 2F) + 4 * B * S^2 *
+d * H floating-point operations per block) divided by the time of the whole step, reported
+in TFLOP/s and as a fraction of the measured bf16 tensor peak.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs an independent replica (the forward has no exchange step);
+``value`` is the work of all ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MMDiT block fwd TFLOP/s & % of GB300 bf16 tensor peak at 4096+512 tokens"
+WORKLOAD = "flux535m_bf16"
+AXES = (16, 56, 56)
+THETA = 10000.0
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="minimum CPU time of the oracle baseline sample")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    return args
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured (MEASURED_PEAKS.json)"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- workload
+def block_flops(B, S, D, F, H, d=128):
+    return 2 * B * S * D * (3 * D + D + 2 * F) + 4 * B * S * S * d * H
+
+
+class HostWorkload:
+    """Seeded host-side inputs and weights (float32 arrays holding bf16-rounded values)."""
+
+    def __init__(self, wl):
+        from diffusion_transformer_flux_gb300 import synth
+        self.wl = wl
+        B, D, H, F = wl.batch, wl.hidden, wl.heads, wl.mlp_hidden
+        rng_in = np.random.Generator(np.random.PCG64(1000 + wl.index))
+        rng_w = np.random.Generator(np.random.PCG64(2000 + wl.index))
+        self.z0, self.z1 = synth.latent_pair(rng_in, B, wl.channels, wl.lat_h, wl.lat_w)
+        self.t = synth.timesteps(rng_in, B, wl.t_dist)
+        self.txt = synth.bf16_round(rng_in.standard_normal((B, wl.seq_txt, wl.ctx_dim), dtype=np.float32))
+        self.vec = synth.bf16_round(rng_in.standard_normal((B, D), dtype=np.float32))
+        self.ids = synth.position_ids(B, wl.lat_h, wl.lat_w, wl.seq_txt)
+        self.img_in = synth.embed_weights(rng_w, wl.channels, D, "bf16")
+        self.txt_in = synth.embed_weights(rng_w, wl.ctx_dim, D, "bf16")
+        self.w_dimg = synth.stream_weights(rng_w, D, H, 128, F, "bf16")
+        self.w_dtxt = synth.stream_weights(rng_w, D, H, 128, F, "bf16")
+        self.w_single = synth.stream_weights(rng_w, D, H, 128, F, "bf16")
+        self.final = synth.final_layer_weights(rng_w, D, wl.channels, "bf16")
+
+
+class DeviceStep:
+    """Device buffers, weights and workspaces of one replica, and the step itself."""
+
+    def __init__(self, hw: HostWorkload, device):
+        import torch
+        from diffusion_transformer_flux_gb300 import _lib as L
+        self.L, self.torch = L, torch
+        wl = hw.wl
+        self.wl = wl
+        B, D, H, F, S_i, S_t = wl.batch, wl.hidden, wl.heads, wl.mlp_hidden, wl.seq_img, wl.seq_txt
+        assert B == 1, "the concatenated-sequence views below assume batch 1"
+        S = S_i + S_t
+        bf = torch.bfloat16
+
+        def dev(a, dt=bf):
+            return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device).to(dt)
+
+        def devw(w):
+            return {k: dev(v) for k, v in w.items()}
+
+        self.z0, self.z1 = dev(hw.z0, torch.float32), dev(hw.z1, torch.float32)
+        self.t = dev(hw.t, torch.float32)
+        self.txt, self.vec = dev(hw.txt), dev(hw.vec)
+        self.ids = dev(hw.ids, torch.float32)
+        self.img_in, self.txt_in = devw(hw.img_in), devw(hw.txt_in)
+        self.w_dimg, self.w_dtxt, self.w_single = devw(hw.w_dimg), devw(hw.w_dtxt), devw(hw.w_single)
+        self.final = devw(hw.final)
+        self.sw_dimg, self.sw_dtxt = L.make_stream_w(self.w_dimg), L.make_stream_w(self.w_dtxt)
+        self.sw_single = L.make_stream_w(self.w_single)
+        self.cos = torch.empty(B, S, 64, device=device)
+        self.sin = torch.empty_like(self.cos)
+        self.zt = torch.empty_like(self.z0)
+        self.X = torch.empty(B, S, D, device=device, dtype=bf)   # embeddings [img; txt]
+        self.Y = torch.empty_like(self.X)                        # double-block output
+        self.Z = torch.empty_like(self.X)                        # single-block output
+        self.pred = torch.empty_like(self.z0)
+        self.loss = torch.zeros(1, device=device)
+        self.dims = L.make_dims(B, S_i, S_t, D, H, F, L.MMDIT_BF16)
+        self.dims_final = L.make_dims(B, S_i, 0, D, H, F, L.MMDIT_BF16)
+        ws_block = max(L.mmdit_double_block_workspace_size(self.dims),
+                       L.mmdit_single_block_workspace_size(self.dims))
+        self.ws_block = L.workspace(ws_block, device)
+        self.ws_flow = L.workspace(L.flow_match_workspace_size(B, self.z0[0].numel()), device)
+        self.ws_lin = L.workspace(256, device)
+        self.ws_img = L.workspace(L.mmdit_img_in_workspace_size(L.MMDIT_BF16, B, wl.channels, wl.lat_h,
+                                                                wl.lat_w), device)
+        self.ws_final = L.workspace(L.mmdit_final_layer_workspace_size(self.dims_final, wl.channels), device)
+        self.S, self.S_i = S, S_i
+        self.flops_blocks = 2 * block_flops(B, S, D, F, H)
+        self.flops_dense = (self.flops_blocks + 2 * B * S_i * wl.channels * D
+                            + 2 * B * S_t * wl.ctx_dim * D + 2 * B * S_i * D * wl.channels)
+
+    def step(self):
+        """One pass of the hot path; every computation runs in libmmdit.so kernels."""
+        L, wl = self.L, self.wl
+        S_i = self.S_i
+        L.rope3d_freqs(self.ids, AXES, THETA, self.cos, self.sin)
+        L.flow_match_noise_and_loss(self.z0, self.z1, self.t, z_t=self.zt, ws=self.ws_flow)
+        L.mmdit_img_in_fwd(self.zt, self.img_in["w"], self.img_in["b"], self.X[:, :S_i], ws=self.ws_img)
+        L.mmdit_linear_fwd(self.txt, self.txt_in["w"], self.txt_in["b"], self.X[:, S_i:], ws=self.ws_lin)
+        L.mmdit_double_block_fwd(self.dims, self.w_dimg, self.w_dtxt, self.vec, self.cos, self.sin,
+                                 self.X[:, :S_i], self.X[:, S_i:], self.Y[:, :S_i], self.Y[:, S_i:],
+                                 ws=self.ws_block)
+        L.mmdit_single_block_fwd(self.dims, self.w_single, self.vec, self.cos, self.sin, self.Y, self.Z,
+                                 ws=self.ws_block)
+        L.mmdit_final_layer_fwd(self.dims_final, wl.lat_h, wl.lat_w, self.Z[:, :S_i], self.vec,
+                                self.final["w_ada"], self.final["b_ada"], self.final["w_out"],
+                                self.final["b_out"], self.pred, ws=self.ws_final)
+        L.flow_match_noise_and_loss(self.z0, self.z1, self.t, pred=self.pred, loss=self.loss,
+                                    ws=self.ws_flow)
+
+    def step_from_host(self, pinned: dict, loss_host):
+        """The same step with this step's inputs copied from pinned host memory and the loss
+        read back, all on the current stream."""
+        for name, src in pinned.items():
+            getattr(self, name).copy_(src, non_blocking=True)
+        self.step()
+        loss_host.copy_(self.loss, non_blocking=True)
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clock, power and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None, period_ms=20):
+        self.uuid = uuid
+        self.proc = None
+        self.period_ms = period_ms
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.1)
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        rows = [[c.strip() for c in ln.split(",")] for ln in getattr(self, "lines", [])]
+        if self.uuid:
+            mine = [r for r in rows if r and self.uuid in r[0]]
+            rows = mine or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, smax, reasons, power = [], [], set(), []
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        busy = [s for s, p in zip(sm, power) if p > 0.25 * max(power)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+# ----------------------------------------------------------------------------- per-kernel roofline
+def kernel_work(label: str, wl):
+    """(bound, algorithmic amount per launch, unit) of one library step, from the workload shapes."""
+    B, D, F, H = wl.batch, wl.hidden, wl.mlp_hidden, wl.heads
+    S_i, S_t = wl.seq_img, wl.seq_txt
+    S = S_i + S_t
+    rows = {"img": B * S_i, "txt": B * S_t}
+    parts = label.split(".")
+    if parts[0] in ("double", "single"):
+        r = B * S if parts[0] == "single" else rows[parts[-1]] if parts[-1] in rows else B * S
+        op = parts[1]
+        if op == "qkv":
+            return "tensor", 2.0 * r * D * 3 * D, "FLOP"
+        if op == "out":
+            return "tensor", 2.0 * r * D * D, "FLOP"
+        if op in ("fc1", "fc2"):
+            return "tensor", 2.0 * r * D * F, "FLOP"
+        if op == "attention":
+            return "tensor", 4.0 * B * S * S * 128 * H, "FLOP"
+        if op == "modulation":
+            return "hbm", 6.0 * D * D * 2 + B * D * 2 + B * 6 * D * 4, "B"
+        if op == "ln1":
+            return "hbm", 2.0 * r * D * 2, "B"
+        if op == "ln2":
+            return "hbm", r * D * 4 + r * D * 2, "B"
+    n_lat = B * wl.channels * S_i
+    if label == "rope3d_freqs":
+        return "hbm", B * S * 3 * 4 + 2.0 * B * S * 64 * 4, "B"
+    if label in ("flow_match.noise", "flow_match.loss"):
+        return "hbm", 3.0 * n_lat * 4, "B"
+    if label == "img_in":
+        return "tensor", 2.0 * B * S_i * wl.channels * D, "FLOP"
+    if label == "linear":
+        return "tensor", 2.0 * B * S_t * wl.ctx_dim * D, "FLOP"
+    if label == "final_layer":
+        return "tensor", 2.0 * B * S_i * D * wl.channels, "FLOP"
+    return "unknown", 0.0, ""
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "diffusion_transformer_flux_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(label: str):
+    """DRAM bytes per launch of `label` from the committed ncu summary, if it was taken on the
+    current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("source_digest") != source_digest():
+        return None
+    v = t.get("bytes_per_launch", {}).get(label)
+    return float(v) if v is not None else None
+
+
+# ----------------------------------------------------------------------------- oracle baseline
+def oracle_sample(hw: HostWorkload, n_img_rows: int, n_txt_rows: int, seed: int):
+    """One bounded sample of the workload computed by the fp64 oracle: the image and text
+    embeddings, then the double block's output at seeded rows (its keys and values need every
+    token).  Returns the dense floating-point operations the oracle executed."""
+    from oracle import flux as O
+    wl = hw.wl
+    B, D, H, F, S_i, S_t = wl.batch, wl.hidden, wl.heads, wl.mlp_hidden, wl.seq_img, wl.seq_txt
+    S = S_i + S_t
+    rng = np.random.default_rng(seed)
+    ri = rng.choice(S_i, n_img_rows, replace=False)
+    rt = rng.choice(S_t, n_txt_rows, replace=False)
+    zt = O.flow_match_noise(hw.z0, hw.z1, hw.t)
+    x_img = O.img_in(zt, hw.img_in["w"], hw.img_in["b"])
+    x_txt = O.txt_in(hw.txt, hw.txt_in["w"], hw.txt_in["b"])
+    cos, sin = O.rope_cos_sin(hw.ids)
+    O.double_block_rows(x_img, x_txt, hw.vec, cos, sin, hw.w_dimg, hw.w_dtxt, H, ri, rt)
+    nr = B * (n_img_rows + n_txt_rows)
+    return (2.0 * B * S_i * wl.channels * D + 2.0 * B * S_t * wl.ctx_dim * D
+            + 2 * 2.0 * B * D * 6 * D                       # two modulation linears
+            + 2.0 * B * S * D * 3 * D + 2.0 * nr * D * 3 * D  # K/V for all tokens, Q for the rows
+            + 4.0 * nr * S * 128 * H + 2.0 * nr * D * D + 4.0 * nr * D * F)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_cpu_baseline(hw: HostWorkload, min_seconds: float, rows=(32, 8)):
+    flops, n, t0 = 0.0, 0, time.perf_counter()
+    while True:
+        flops += oracle_sample(hw, rows[0], rows[1], seed=n)
+        n += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": (f"{n} x (fp64 oracle: flow-matching noise, img_in, txt_in, then the "
+                       f"{wl_desc(hw.wl)} double block at {rows[0]} image + {rows[1]} text rows with "
+                       "keys/values for all tokens)"), "seconds": round(dt, 2)}
+
+
+def wl_desc(wl):
+    return f"{wl.seq_img}+{wl.seq_txt}-token D{wl.hidden} F{wl.mlp_hidden}"
+
+
+def run_reference(args):
+    """The oracle on the host cores, on this workload, one bounded sample per step."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from diffusion_transformer_flux_gb300 import synth
+    wl = synth.WORKLOADS[WORKLOAD]
+    hw = HostWorkload(wl)
+    rows = (8, 2)
+    for i in range(args.warmup):
+        oracle_sample(hw, *rows, seed=i)
+    flops, t0 = 0.0, time.perf_counter()
+    for i in range(args.steps):
+        flops += oracle_sample(hw, *rows, seed=1000 + i)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    sample = (f"per step: fp64 oracle flow-matching noise, img_in, txt_in and the {wl_desc(wl)} "
+              f"double block at {rows[0]} image + {rows[1]} text rows (keys/values for all tokens)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded PCG64; N(0,0.02) weights, N(0,1) activations and latents)",
+            "config": {"workload": WORKLOAD, "global_batch": wl.batch, "seq_len": wl.seq,
+                       "tokens": f"{wl.seq_img} image + {wl.seq_txt} text", "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)

@@ -92,7 +92,7 @@ def _check_outputs(case: BlockCase, got, rows=None):
         # the residual dominates the output; the branch alone must also be close
         assert_parity(g - x, r - x, 0.1, n + " branch (y - x)", out_bf16=bf)
         if bf:
-            assert_parity(g, ref64[i], TOL_VS_FP64, n + " vs float64 oracle")
+            assert_parity(g, ref64[i], TOL_VS_FP64, n + " vs float64 oracle", out_bf16=True)
 
 
 # ----------------------------------------------------------------------------- small shapes
