@@ -379,3 +379,165 @@ def run_reference(args):
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    rank, world, local = dist_env()
+    import torch
+    from diffusion_transformer_flux_gb300 import _lib as L
+    from diffusion_transformer_flux_gb300 import synth
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    L.load()
+    wl = synth.WORKLOADS[WORKLOAD]
+    hw = HostWorkload(wl)
+    st = DeviceStep(hw, device)
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # > 129 MB of L2
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if dist is None:
+            return x
+        t = torch.tensor([x], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def timed(fn, k):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(k)]
+        barrier()
+        torch.cuda.synchronize()
+        L.mmdit_launch_count_reset()
+        for i in range(k):
+            flush.zero_()
+            evs[i][0].record(stream)
+            fn()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        launches = L.mmdit_launch_count()
+        barrier()
+        return [a.elapsed_time(b) for a, b in evs], launches
+
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+    for ws in (st.ws_block, st.ws_flow, st.ws_lin, st.ws_img, st.ws_final):
+        if L.mmdit_workspace_status(ws) != 0:
+            raise RuntimeError("a kernel gave up a bounded wait during warm-up")
+
+    props = torch.cuda.get_device_properties(device)
+    uuid = str(getattr(props, "uuid", "") or "") or None
+    with ClockSampler(uuid) as clk:
+        ms, launches = timed(st.step, args.steps)
+    clocks = clk.summary()
+    if not np.isfinite(st.loss.item()):
+        raise RuntimeError("non-finite loss")
+    total_s = max_over_ranks(sum(ms) / 1e3)
+    value = world * st.flops_blocks * args.steps / total_s / 1e12
+
+    # end to end: this step's inputs from pinned host memory, the loss back to the host
+    pinned = {n: getattr(st, n).detach().cpu().pin_memory() for n in ("z0", "z1", "t", "txt", "vec", "ids")}
+    loss_host = torch.zeros(1, pin_memory=True)
+    for _ in range(2):
+        st.step_from_host(pinned, loss_host)
+    ms_e2e, _ = timed(lambda: st.step_from_host(pinned, loss_host), args.steps)
+    e2e_s = max_over_ranks(sum(ms_e2e) / 1e3)
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+
+    # per-kernel durations from CUDA events the library records around each of its steps
+    L.mmdit_profile_enable(True)
+    for _ in range(args.profile_steps):
+        flush.zero_()
+        st.step()
+    recs = L.mmdit_profile_collect()
+    L.mmdit_profile_enable(False)
+    agg = {}
+    for name, t in recs:
+        a = agg.setdefault(name, [0, 0.0])
+        a[0] += 1
+        a[1] += t
+    prof_total = sum(v[1] for v in agg.values()) or 1.0
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    per_kernel = []
+    for name, (n, t) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
+        bound, amount, unit = kernel_work(name, wl)
+        avg_s = t / n / 1e3
+        row = {"kernel": name, "launches": n, "avg_us": round(avg_s * 1e6, 2), "share": round(t / prof_total, 4),
+               "bound": bound}
+        if bound == "tensor":
+            row["achieved_tflops"] = round(amount / avg_s / 1e12, 1)
+            row["frac"] = round(amount / avg_s / 1e12 / bf16_peak, 4)
+        elif bound == "hbm":
+            row["achieved_gbs"] = round(amount / avg_s / 1e9, 1)
+            row["frac"] = round(amount / avg_s / 1e9 / hbm_peak, 4)
+        per_kernel.append(row)
+    dom = per_kernel[0]
+    bound, amount, unit = kernel_work(dom["kernel"], wl)
+    dom_s = dom["avg_us"] / 1e6
+    if bound == "tensor":
+        ach, peak, runit = amount / dom_s / 1e12, bf16_peak, "TFLOP/s"
+    else:
+        ach, peak, runit = amount / dom_s / 1e9, hbm_peak, "GB/s"
+    roofline = {"kernel": dom["kernel"], "bound": bound, "achieved": round(ach, 2), "peak": peak,
+                "unit": runit, "frac": round(ach / peak, 4), "traffic": committed_traffic(dom["kernel"]),
+                "algorithmic_per_launch": amount, "algorithmic_unit": unit,
+                "peak_source": f"{peak_src}: {'bf16_tflops (burst)' if bound == 'tensor' else 'hbm_gbs'}"}
+    if bound == "tensor" and "bf16_tflops_sustained" in peaks:
+        roofline["frac_of_sustained"] = round(ach / float(peaks["bf16_tflops_sustained"]), 4)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(hw, args.cpu_seconds)
+
+    if rank == 0:
+        S = wl.seq
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded PCG64; N(0,0.02) weights, N(0,1) activations, text embeddings "
+                    "and latents; no dataset or trained weights)",
+            "config": {"workload": WORKLOAD, "global_batch": world * wl.batch, "seq_len": S,
+                       "tokens": f"{wl.seq_img} image + {wl.seq_txt} text", "hidden": wl.hidden,
+                       "heads": wl.heads, "head_dim": 128, "mlp_hidden": wl.mlp_hidden,
+                       "parallelism": f"{world} independent replica(s), no exchange",
+                       "l2": "flushed before every timed step (256 MB write outside the events)",
+                       "step": "rope3d_freqs, flow-matching noise, img_in, txt_in, double block, "
+                               "single block, output head, flow-matching loss",
+                       "flops_counted_per_step": st.flops_blocks,
+                       "dense_flops_per_step_incl_embeds_and_head": st.flops_dense},
+            "pct_of_bf16_peak": round(100 * value / world / bf16_peak, 2),
+            "tokens_per_s": round(world * wl.batch * S * args.steps / total_s, 1),
+            "clocks": clocks,
+            "e2e": {"value": round(world * st.flops_blocks * args.steps / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4,
+                    "ms_per_step": round(e2e_s / args.steps * 1e3, 4)},
+            "gpu_launches": launches,
+            "roofline": roofline,
+            "per_kernel": per_kernel,
+            "cpu_baseline": cpu,
+            "peaks": {"bf16_tflops": bf16_peak, "hbm_gbs": hbm_peak, "source": peak_src},
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
