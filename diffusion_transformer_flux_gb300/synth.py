@@ -81,13 +81,18 @@ WORKLOADS = {
 
 # --------------------------------------------------------------------------- bf16 rounding
 def bf16_bits(x) -> np.ndarray:
-    """Round float32 values to bf16 (nearest, ties to even); return the uint16 bit patterns."""
+    """Round float32 values to bf16 (nearest, ties to even); return the uint16 bit patterns.
+
+    Works in uint32: for every non-NaN pattern u, u + 0x7FFF + 1 stays below 2^32."""
     f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
-    u = f.view(np.uint32).astype(np.uint64)
+    u = f.view(np.uint32)
+    r = (u >> np.uint32(16)) & np.uint32(1)
+    r += u
+    r += np.uint32(0x7FFF)
+    r >>= np.uint32(16)
     nan = np.isnan(f)
-    lsb = (u >> np.uint64(16)) & np.uint64(1)
-    r = (u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)
-    r = np.where(nan, np.uint64(0x7FC0), r)
+    if nan.any():
+        r[nan] = 0x7FC0
     return r.astype(np.uint16)
 
 
@@ -108,7 +113,10 @@ def _cast(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def _normal(rng, shape, std=1.0):
-    return (rng.standard_normal(size=shape, dtype=np.float32) * np.float32(std)).astype(np.float32)
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return x
 
 
 # --------------------------------------------------------------------------- weights
