@@ -25,6 +25,7 @@ EXPORTED = [
     "mmdit_last_error", "mmdit_workspace_status", "mmdit_launch_count", "mmdit_launch_count_reset",
     "mmdit_profile_enable", "mmdit_profile_collect",
     "rope3d_freqs", "flow_match_workspace_size", "flow_match_noise_and_loss",
+    "flow_match_noise_and_loss_noalloc",
     "mmdit_linear_workspace_size", "mmdit_linear_fwd", "mmdit_img_in_workspace_size",
     "mmdit_img_in_fwd", "mmdit_final_layer_workspace_size", "mmdit_final_layer_fwd",
     "mmdit_attention_workspace_size", "mmdit_attention_fwd", "mmdit_double_block_workspace_size",
@@ -68,6 +69,7 @@ _SIGS = {
     "rope3d_freqs": (C.c_int, [VP, I32, I32, C.POINTER(I32), F32, VP, VP, VP]),
     "flow_match_workspace_size": (SZ, [I32, I64]),
     "flow_match_noise_and_loss": (C.c_int, [I32, VP, VP, VP, I32, I64, VP, VP, VP, VP, SZ, VP]),
+    "flow_match_noise_and_loss_noalloc": (C.c_int, [I32, VP, VP, VP, I32, I64, VP, VP, VP, VP]),
     "mmdit_linear_workspace_size": (SZ, []),
     "mmdit_linear_fwd": (C.c_int, [I32, I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_img_in_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
@@ -204,6 +206,15 @@ def flow_match_noise_and_loss(z0, z1, t, z_t=None, pred=None, loss=None, ws=None
                                             _ptr(pred), _ptr(loss), _ptr(ws), ws.numel(),
                                             _stream(stream)))
     return ws
+
+
+def flow_match_noise_and_loss_noalloc(z0, z1, t, z_t=None, pred=None, loss=None, stream=None):
+    """flow_match_noise_and_loss without a workspace (see include/mmdit.h)."""
+    B = z0.shape[0]
+    n = z0.numel() // B
+    _check(load().flow_match_noise_and_loss_noalloc(act_of(z0), _ptr(z0), _ptr(z1), _ptr(t), B, n,
+                                                    _ptr(z_t), _ptr(pred), _ptr(loss),
+                                                    _stream(stream)))
 
 
 def mmdit_linear_fwd(x, w, b, y, ws=None, stream=None):

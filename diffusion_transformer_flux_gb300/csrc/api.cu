@@ -65,6 +65,10 @@ struct Carver {
 
 void count_launch(int n) { g_launches += static_cast<uint64_t>(n); }
 
+int set_last_error(int status, const char* msg) {
+  return static_cast<int>(fail(static_cast<mmdit_status>(status), "%s", msg));
+}
+
 // ----------------------------------------------------------------------------- step timing
 namespace {
 struct ProfRecord {

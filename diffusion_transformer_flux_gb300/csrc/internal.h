@@ -60,6 +60,10 @@ constexpr size_t kStatusBytes = 256;
 // Launch accounting for diagnostics.
 void count_launch(int n = 1);
 
+// Records `msg` as the calling thread's last error (returned by mmdit_last_error) and returns
+// `status`; for translation units other than the one holding the C ABI's bookkeeping.
+int set_last_error(int status, const char* msg);
+
 // Number of SMs of the current device.
 int num_sms();
 

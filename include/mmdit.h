@@ -158,6 +158,21 @@ mmdit_status flow_match_noise_and_loss(int32_t dtype, const void *z0, const void
                                        void *z_t, const void *pred, float *loss,
                                        void *workspace, size_t workspace_bytes, void *stream);
 
+/* flow_match_noise_and_loss without a workspace, for callers that cannot allocate device
+ * memory (code running under another framework's allocator or inside a stream capture whose
+ * pool it does not own, or a host whose memory is fixed at start-up).  The pages have no
+ * counterpart; this is a packaging variant of the entry point above with the same results.
+ * The partial sums of the loss live in a static device array of 256 floats (1 KiB) that every
+ * GPU loading the library keeps until the process exits, so batch * n_per_sample may be at
+ * most 2,097,152; larger calls return MMDIT_ERR_UNSUPPORTED.  Nothing is allocated.  The
+ * first call on each device looks up the array's address (cudaGetSymbolAddress) and should
+ * precede any stream capture.  All calls share the array: calls whose kernels overlap on the
+ * GPU race, so order them on one stream. */
+mmdit_status flow_match_noise_and_loss_noalloc(int32_t dtype, const void *z0, const void *z1,
+                                               const float *t, int32_t batch,
+                                               int64_t n_per_sample, void *z_t,
+                                               const void *pred, float *loss, void *stream);
+
 /* ---------------------------------------------------------------------------------------
  * Plain linear layer y = x W^T + b on the tensor cores (the text embedding txt_in of [ARCH]
  * §Model components, 1. Input embeddings, and any other projection).
