@@ -259,7 +259,8 @@ def kernel_work(label: str, wl):
         if op == "attention":
             return "tensor", 4.0 * B * S * S * 128 * H, "FLOP"
         if op == "modulation":
-            return "hbm", 6.0 * D * D * 2 + B * D * 2 + B * 6 * D * 4, "B"
+            sets = 2 if label == "double.modulation" else 1
+            return "hbm", sets * (6.0 * D * D * 2 + B * 6 * D * 4) + B * D * 2, "B"
         if op == "ln1":
             return "hbm", 2.0 * r * D * 2, "B"
         if op == "ln2":

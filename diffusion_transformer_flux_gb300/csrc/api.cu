@@ -239,14 +239,16 @@ T* at(void* ws, size_t off) {
 // Launches the chain of one block over stream s (double block: s = 0 image, 1 text).
 mmdit_status run_stream_qkv(const mmdit_dims* d, const BlockPlan& p, int s, const mmdit_stream_w* w,
                             const void* vec, const float* cs, const float* sn, const void* x,
-                            void* ws, cudaStream_t st) {
+                            void* ws, cudaStream_t st, bool do_mod) {
   const int rows_per_batch = p.single ? p.S : (s == 0 ? p.Si : p.St);
   const int rows = p.B * rows_per_batch;
-  if (rows == 0) return MMDIT_OK;
   float* mod = at<float>(ws, p.mod[s]);
-  { ProfScope ps_(p.single ? "single.modulation" : (s == 0 ? "double.modulation.img" : "double.modulation.txt"), st);
-  MMDIT_CUDA(launch_modulation(d->act, vec, w->w_mod, w->b_mod, p.B, 6 * p.D, p.D, mod, st),
-             "modulation"); }
+  if (do_mod) {
+    ProfScope ps_(p.single ? "single.modulation" : (s == 0 ? "double.modulation.img" : "double.modulation.txt"), st);
+    MMDIT_CUDA(launch_modulation(d->act, vec, w->w_mod, w->b_mod, p.B, 6 * p.D, p.D, mod, st),
+               "modulation");
+  }
+  if (rows == 0) return MMDIT_OK;
   { ProfScope ps_(p.single ? "single.ln1" : (s == 0 ? "double.ln1.img" : "double.ln1.txt"), st);
   MMDIT_CUDA(launch_ln_modulate(d->act, d->act == MMDIT_F32, x, mod, mod + p.D, 6 * p.D, rows, rows_per_batch, p.D,
                                 d->ln_eps, at(ws, p.h[s]), st),
@@ -603,8 +605,15 @@ mmdit_status mmdit_double_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
   const mmdit_stream_w* ws_[2] = {w_img, w_txt};
   const void* xs[2] = {x_img, x_txt};
   void* ys[2] = {y_img, y_txt};
+  {
+    // both streams' AdaLN modulation in one launch (they share vec)
+    ProfScope ps_("double.modulation", st);
+    const ModulationJob jobs[2] = {{w_img->w_mod, w_img->b_mod, at<float>(workspace, p.mod[0]), 6 * p.D},
+                                   {w_txt->w_mod, w_txt->b_mod, at<float>(workspace, p.mod[1]), 6 * p.D}};
+    MMDIT_CUDA(launch_modulation2(d->act, vec, jobs, 2, p.B, p.D, st), "modulation");
+  }
   for (int i = 0; i < 2; ++i)
-    if ((s = run_stream_qkv(d, p, i, ws_[i], vec, rope_cos, rope_sin, xs[i], workspace, st)) != MMDIT_OK)
+    if ((s = run_stream_qkv(d, p, i, ws_[i], vec, rope_cos, rope_sin, xs[i], workspace, st, false)) != MMDIT_OK)
       return s;
   if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
   for (int i = 0; i < 2; ++i)
@@ -628,7 +637,7 @@ mmdit_status mmdit_single_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
   if ((s = check_workspace(workspace, workspace_bytes, p.total)) != MMDIT_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
-  if ((s = run_stream_qkv(d, p, 0, w, vec, rope_cos, rope_sin, x, workspace, st)) != MMDIT_OK) return s;
+  if ((s = run_stream_qkv(d, p, 0, w, vec, rope_cos, rope_sin, x, workspace, st, true)) != MMDIT_OK) return s;
   if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
   return run_stream_post(d, p, 0, w, x, y, workspace, st);
 }

@@ -60,15 +60,47 @@ __global__ void rope3d_kernel(const float* __restrict__ ids, int64_t n_tok, Rope
 }
 
 // ----------------------------------------------------------------------------- modulation GEMV
-// m[b, r] = sum_k SiLU(vec[b, k]) w[r, k] + bias[r], one warp per weight row; batch <= 8.
+// m[b, r] = sum_k SiLU(vec[b, k]) w[r, k] + bias[r], one warp per weight row, batch <= 8 per
+// launch.  Up to two weight sets (the image and text streams of a double block) share a launch.
+// Each warp issues kModLoads 16-byte loads per lane before using any of them, so a row of
+// D = 3072 bf16 weights is two rounds of loads.
 constexpr int kModMaxBatch = 8;
+constexpr int kModLoads = 8;
+constexpr int kModThreads = 128;
+
+struct ModJob {
+  const void* w;
+  const void* bias;
+  float* m;  // [batch, rows]
+  int rows;
+};
 
 template <typename T>
-__global__ void __launch_bounds__(256) modulation_kernel(const T* __restrict__ vec,
-                                                         const T* __restrict__ w,
-                                                         const T* __restrict__ bias, int batch,
-                                                         int rows, int dim, float* __restrict__ m,
-                                                         int64_t m_bstride) {
+struct Raw8;  // 8 consecutive elements as loaded
+template <>
+struct Raw8<__nv_bfloat16> {
+  uint4 u;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { u = __ldg(reinterpret_cast<const uint4*>(p)); }
+  __device__ __forceinline__ void to_f32(float (&v)[8]) const {
+    v[0] = bf16_lo(u.x), v[1] = bf16_hi(u.x), v[2] = bf16_lo(u.y), v[3] = bf16_hi(u.y);
+    v[4] = bf16_lo(u.z), v[5] = bf16_hi(u.z), v[6] = bf16_lo(u.w), v[7] = bf16_hi(u.w);
+  }
+};
+template <>
+struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = __ldg(reinterpret_cast<const float4*>(p));
+    b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  }
+  __device__ __forceinline__ void to_f32(float (&v)[8]) const {
+    v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+  }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __restrict__ vec, ModJob j0,
+                                                                 ModJob j1, int batch, int dim) {
   extern __shared__ float svec[];  // [batch, dim] SiLU(vec), a bf16 operand in bf16 mode
   for (int i = threadIdx.x; i < batch * dim; i += blockDim.x) {
     const float v = to_f32(vec[i]);
@@ -81,31 +113,46 @@ __global__ void __launch_bounds__(256) modulation_kernel(const T* __restrict__ v
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
-  for (int r = blockIdx.x * warps + warp; r < rows; r += gridDim.x * warps) {
+  const int total = j0.rows + j1.rows;
+  for (int g = blockIdx.x * warps + warp; g < total; g += gridDim.x * warps) {
+    const bool second = g >= j0.rows;
+    const ModJob& job = second ? j1 : j0;
+    const int r = second ? g - j0.rows : g;
+    const T* wr = reinterpret_cast<const T*>(job.w) + static_cast<size_t>(r) * dim;
     float acc[kModMaxBatch];
 #pragma unroll
     for (int b = 0; b < kModMaxBatch; ++b) acc[b] = 0.f;
-    const T* wr = w + static_cast<size_t>(r) * dim;
-#pragma unroll 4
-    for (int k = lane * 8; k < dim; k += 256) {
-      float wv[8];
-      load8(wr + k, wv);
+    for (int k0 = 0; k0 < dim; k0 += kModLoads * 256) {
+      Raw8<T> raw[kModLoads];
 #pragma unroll
-      for (int b = 0; b < kModMaxBatch; ++b) {
-        if (b < batch) {
-          const float4 s0 = *reinterpret_cast<const float4*>(svec + b * dim + k);
-          const float4 s1 = *reinterpret_cast<const float4*>(svec + b * dim + k + 4);
-          acc[b] += wv[0] * s0.x + wv[1] * s0.y + wv[2] * s0.z + wv[3] * s0.w + wv[4] * s1.x +
-                    wv[5] * s1.y + wv[6] * s1.z + wv[7] * s1.w;
+      for (int u = 0; u < kModLoads; ++u) {
+        const int k = k0 + u * 256 + lane * 8;
+        if (k < dim) raw[u].load(wr + k);
+      }
+#pragma unroll
+      for (int u = 0; u < kModLoads; ++u) {
+        const int k = k0 + u * 256 + lane * 8;
+        if (k < dim) {
+          float wv[8];
+          raw[u].to_f32(wv);
+#pragma unroll
+          for (int b = 0; b < kModMaxBatch; ++b) {
+            if (b < batch) {
+              const float4 s0 = *reinterpret_cast<const float4*>(svec + b * dim + k);
+              const float4 s1 = *reinterpret_cast<const float4*>(svec + b * dim + k + 4);
+              acc[b] += wv[0] * s0.x + wv[1] * s0.y + wv[2] * s0.z + wv[3] * s0.w + wv[4] * s1.x +
+                        wv[5] * s1.y + wv[6] * s1.z + wv[7] * s1.w;
+            }
+          }
         }
       }
     }
-    const float bb = bias ? to_f32(bias[r]) : 0.f;
+    const float bb = job.bias ? to_f32(reinterpret_cast<const T*>(job.bias)[r]) : 0.f;
 #pragma unroll
     for (int b = 0; b < kModMaxBatch; ++b) {
       if (b < batch) {
-        const float s = warp_sum(acc[b]);
-        if (lane == 0) m[b * m_bstride + r] = s + bb;
+        const float sum = warp_sum(acc[b]);
+        if (lane == 0) job.m[static_cast<size_t>(b) * job.rows + r] = sum + bb;
       }
     }
   }
@@ -287,34 +334,49 @@ cudaError_t launch_rope3d(const float* ids, int batch, int seq, const int axes[3
   return cudaGetLastError();
 }
 
-cudaError_t launch_modulation(int act, const void* vec, const void* w, const void* bias, int batch,
-                              int rows, int dim, float* m, cudaStream_t stream) {
-  const int threads = 256;
-  const int grid = blocks_for(rows, threads / 32, num_sms() * 4);
+cudaError_t launch_modulation2(int act, const void* vec, const ModulationJob* jobs, int njobs,
+                               int batch, int dim, cudaStream_t stream) {
+  int total = 0;
+  for (int i = 0; i < njobs; ++i) total += jobs[i].rows;
+  const int warps = kModThreads / 32;
+  const int grid = blocks_for(total, warps, num_sms() * 6);
+  static int configured = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured != dev) {
+    cudaError_t e = cudaFuncSetAttribute(modulation_kernel<__nv_bfloat16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(modulation_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               200 * 1024);
+    if (e != cudaSuccess) return e;
+    configured = dev;
+  }
+  const size_t elt = act == 1 ? 2 : 4;
   for (int b0 = 0; b0 < batch; b0 += kModMaxBatch) {
     const int nb = batch - b0 < kModMaxBatch ? batch - b0 : kModMaxBatch;
     const size_t smem = static_cast<size_t>(nb) * dim * sizeof(float);
-    if (act == 1) {
-      auto k = modulation_kernel<__nv_bfloat16>;
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-      if (e != cudaSuccess) return e;
-      k<<<grid, threads, smem, stream>>>(static_cast<const __nv_bfloat16*>(vec) + static_cast<size_t>(b0) * dim,
-                                         static_cast<const __nv_bfloat16*>(w),
-                                         static_cast<const __nv_bfloat16*>(bias), nb, rows, dim,
-                                         m + static_cast<size_t>(b0) * rows, rows);
-    } else {
-      auto k = modulation_kernel<float>;
-      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-      if (e != cudaSuccess) return e;
-      k<<<grid, threads, smem, stream>>>(static_cast<const float*>(vec) + static_cast<size_t>(b0) * dim,
-                                         static_cast<const float*>(w), static_cast<const float*>(bias),
-                                         nb, rows, dim, m + static_cast<size_t>(b0) * rows, rows);
-    }
+    ModJob j[2] = {{nullptr, nullptr, nullptr, 0}, {nullptr, nullptr, nullptr, 0}};
+    for (int i = 0; i < njobs && i < 2; ++i)
+      j[i] = {jobs[i].w, jobs[i].bias, jobs[i].m + static_cast<size_t>(b0) * jobs[i].rows, jobs[i].rows};
+    const void* vb = static_cast<const uint8_t*>(vec) + static_cast<size_t>(b0) * dim * elt;
+    if (act == 1)
+      modulation_kernel<__nv_bfloat16><<<grid, kModThreads, smem, stream>>>(
+          static_cast<const __nv_bfloat16*>(vb), j[0], j[1], nb, dim);
+    else
+      modulation_kernel<float><<<grid, kModThreads, smem, stream>>>(static_cast<const float*>(vb), j[0],
+                                                                    j[1], nb, dim);
     count_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_modulation(int act, const void* vec, const void* w, const void* bias, int batch,
+                              int rows, int dim, float* m, cudaStream_t stream) {
+  ModulationJob job{w, bias, m, rows};
+  return launch_modulation2(act, vec, &job, 1, batch, dim, stream);
 }
 
 cudaError_t launch_ln_modulate(int act, int x_f32, const void* x, const float* shift, const float* scale,

@@ -98,6 +98,15 @@ cudaError_t launch_rope3d(const float* ids, int batch, int seq, const int axes[3
 // m[b, n] = sum_k SiLU(vec[b, k]) w[n, k] + bias[n], n < rows, k < dim; m fp32 [B, rows].
 cudaError_t launch_modulation(int act, const void* vec, const void* w, const void* bias, int batch,
                               int rows, int dim, float* m, cudaStream_t stream);
+// The same for up to two weight sets sharing `vec`, in one launch.
+struct ModulationJob {
+  const void* w;
+  const void* bias;
+  float* m;
+  int rows;
+};
+cudaError_t launch_modulation2(int act, const void* vec, const ModulationJob* jobs, int njobs,
+                               int batch, int dim, cudaStream_t stream);
 // out[r, :] = LN(x[r, :]) * (1 + scale[b]) + shift[b], b = r / rows_per_batch; x, out [R, D].
 // x is fp32 when x_f32 != 0, else of the activation type; out is of the activation type.
 cudaError_t launch_ln_modulate(int act, int x_f32, const void* x, const float* shift, const float* scale,
