@@ -4,96 +4,91 @@
 // attention of "Flux architecture deep dive", §Implementation details (Attention implementation,
 // Joint Attention Trick): one call over the concatenated [image; text] sequence.
 //
-// One CTA owns 128 query rows of one head and streams the keys in tiles of 128:
-//   warp 0      TMA producer: Q once, then K and V^T tiles into a two-stage ring;
-//   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM score buffers, then
-//               O += P_{j-1} V_{j-1} into a TMEM accumulator, so QK^T of tile j runs while the
-//               softmax warps work on tile j-1;
-//   warps 2..5  softmax: one query row per thread (its TMEM lane), exp2 with the 1/sqrt(d)
-//               scale folded in, P written to shared memory in the tensor core's swizzled
-//               layout, and the running-max correction of O applied in TMEM only when the
-//               row maximum grows by more than 2^8 (otherwise the stale maximum is kept; the
-//               final division by the row sum makes the result exact either way).
-// V arrives transposed ([B, H, 128, S_pad]) so both products read K-major operands.
+// One CTA owns two tiles of 128 query rows (A and B) of one head and streams the keys in tiles
+// of 128.  Twelve warps:
+//   warp 0       TMA producer: both Q tiles once, then K and V^T tiles into a two-stage ring
+//                (K and V of a stage have separate arrival barriers);
+//   warp 1       MMA issuer, in the order S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
+//                so that the tensor core works on one query tile while the other's softmax runs;
+//   warps 4..7   softmax of tile A, warps 8..11 softmax of tile B: one query row per thread (its
+//                TMEM lane).  A first pass over the scores in TMEM takes the row maximum; a second
+//                pass writes P = exp2(S * log2(e)/sqrt(d) - m) as packed bf16 back over the score
+//                columns, where the PV product reads it as its A operand straight from TMEM.  The
+//                running maximum is only moved (and O rescaled in TMEM) when a row's maximum grows
+//                by more than 2^8; the final division by the row sum of the rounded P makes the
+//                result exact either way.
+// TMEM columns: S/P of A [0,128), S/P of B [128,256), O of A [256,384), O of B [384,512).
+// V arrives transposed ([B, H, 128, S_pad]) so the PV product reads a K-major operand.
 #include "common.cuh"
 #include "internal.h"
 
 namespace mmdit {
 namespace {
 
-constexpr int kAttnThreads = 192;
+constexpr int kAttnThreads = 384;
 constexpr int kQTile = 128;
 constexpr int kKvTile = 128;
 constexpr int kKvStages = 2;
-constexpr int kHalfTile = 128 * 128;                      // one 128-row x 64-element bf16 atom block
-constexpr int kQBytes = 2 * kHalfTile;                    // 32 KB
-constexpr int kKBytes = 2 * kHalfTile;
-constexpr int kVBytes = 2 * kHalfTile;
-constexpr int kPBytes = 2 * kHalfTile;
-constexpr int kStageBytes = kKBytes + kVBytes;            // 64 KB
-constexpr int kSmemData = kQBytes + kKvStages * kStageBytes + 2 * kPBytes;  // 224 KB
+constexpr int kHalfTile = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle column block)
+constexpr int kTileBytes = 2 * kHalfTile;  // 128 rows x 128 bf16 = 32 KB
+constexpr int kSmemData = 2 * kTileBytes + kKvStages * 2 * kTileBytes;  // Q_A Q_B | K,V x2 = 192 KB
 constexpr int kAttnSmem = kSmemData + 256 + 1024;
-constexpr uint32_t kTmemCols = 512;                       // S0 | S1 | O | (unused)
-constexpr uint32_t kIdescQK = make_idesc<kKindF16>(128, 128);
-constexpr float kScaleLog2 = 0.12751743074380043f;        // log2(e) / sqrt(128)
-constexpr float kRescaleThreshold = 8.0f;                 // in log2 units
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdesc = make_idesc<kKindF16>(128, 128);
+constexpr float kScaleLog2 = 0.12751743074380043f;  // log2(e) / sqrt(128)
+constexpr float kRescaleThreshold = 8.0f;           // in log2 units
 
-struct AttnSmem {
+struct AttnBarriers {
   uint64_t q_full;
-  uint64_t kv_full[kKvStages];
+  uint64_t k_full[kKvStages];
+  uint64_t v_full[kKvStages];
   uint64_t kv_empty[kKvStages];
   uint64_t s_full[2];
-  uint64_t s_free[2];
   uint64_t p_full[2];
-  uint64_t p_free[2];
-  uint64_t pv_done;
   uint64_t o_full;
   uint64_t drain;
   uint32_t tmem_slot;
   int abort_flag;
 };
 
-// Softmax / correction / output role: warps 2..5, one query row per thread.
+__device__ __forceinline__ uint8_t* q_tile(uint8_t* smem, int x) { return smem + x * kTileBytes; }
+__device__ __forceinline__ uint8_t* k_tile(uint8_t* smem, int st) {
+  return smem + 2 * kTileBytes + st * 2 * kTileBytes;
+}
+__device__ __forceinline__ uint8_t* v_tile(uint8_t* smem, int st) { return k_tile(smem, st) + kTileBytes; }
+
+// Softmax, correction and output of query tile X (warps 4+4X .. 7+4X).
 template <typename OutT>
-__device__ __forceinline__ void softmax_role(AttnSmem* sb, uint8_t* s_p, uint32_t tmem,
-                                             uint32_t tmem_o, int q0, int bh, int heads, int seq,
-                                             int split, int n_kv, OutT* out0, OutT* out1,
-                                             uint32_t* status) {
+__device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t tmem, int q0, int bh,
+                                             int heads, int seq, int split, int n_kv, OutT* out0,
+                                             OutT* out1, uint32_t* status) {
   volatile int* abort_flag = &sb->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+  const uint32_t s_cols = tmem + static_cast<uint32_t>(X * 128) + lane_off;
+  const uint32_t o_cols = tmem + 256u + static_cast<uint32_t>(X * 128) + lane_off;
   float m_run = -INFINITY, l_run = 0.f;
-  bool ok = true;
   for (int j = 0; j < n_kv; ++j) {
-    const int buf = j & 1;
-    bool w = mbar_wait(&sb->s_full[buf], static_cast<uint32_t>(j >> 1) & 1u, abort_flag, status,
-                       kErrAttnWait);
-    if (!__all_sync(0xffffffffu, w)) {
-      ok = false;
-      break;
-    }
+    const bool w = mbar_wait(&sb->s_full[X], static_cast<uint32_t>(j) & 1u, abort_flag, status,
+                             kErrAttnWait);
+    if (!__all_sync(0xffffffffu, w)) return;
     tc_fence_after();
-    float s[128];
+    const int kv0 = j * kKvTile;
+    const bool tail = kv0 + kKvTile > seq;
+    // pass 1: the row maximum of the valid keys
+    float mx = -INFINITY;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       uint32_t r[32];
-      tmem_ld32_wait(tmem + static_cast<uint32_t>(buf * 128 + c * 32) + lane_off, r);
+      tmem_ld32_wait(s_cols + c * 32, r);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]);
+      for (int i = 0; i < 32; ++i) {
+        const float v = (tail && kv0 + c * 32 + i >= seq) ? -INFINITY : __uint_as_float(r[i]);
+        mx = fmaxf(mx, v);
+      }
     }
-    tc_fence_before();
-    mbar_arrive(&sb->s_free[buf]);  // scores are in registers; the buffer may be reused
-    const int kv0 = j * kKvTile;
-    if (kv0 + kKvTile > seq) {
-#pragma unroll
-      for (int i = 0; i < 128; ++i)
-        if (kv0 + i >= seq) s[i] = -INFINITY;
-    }
-    float mx = s[0];
-#pragma unroll
-    for (int i = 1; i < 128; ++i) mx = fmaxf(mx, s[i]);
     mx *= kScaleLog2;
     float alpha = 1.f;
     bool rescale = false;
@@ -104,80 +99,76 @@ __device__ __forceinline__ void softmax_role(AttnSmem* sb, uint8_t* s_p, uint32_
       m_run = mx;
       rescale = true;
     }
-    uint32_t pk[64];
-    float sum = 0.f;
-#pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      const float p0 = fast_exp2(fmaf(s[2 * i], kScaleLog2, -m_run));
-      const float p1 = fast_exp2(fmaf(s[2 * i + 1], kScaleLog2, -m_run));
-      pk[i] = pack_bf16x2(p0, p1);
-      // normalise by the sum of the rounded weights that the PV product actually uses
-      sum += bf16_lo(pk[i]) + bf16_hi(pk[i]);
-    }
-    // P_j goes to buffer j&1 once PV_{j-2} has finished reading it.
-    w = mbar_wait(&sb->p_free[buf], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag, status,
-                  kErrAttnWait);
-    if (!__all_sync(0xffffffffu, w)) {
-      ok = false;
-      break;
-    }
-    // Row `row` of a 128-byte-swizzled K-major tile: 16-byte chunk c sits at c ^ (row % 8).
-    uint8_t* prow = s_p + buf * kPBytes + row * 128;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const int atom = c >> 3, cc = c & 7;
-      uint4 u = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      *reinterpret_cast<uint4*>(prow + atom * kHalfTile + ((cc ^ (row & 7)) << 4)) = u;
-    }
-    fence_proxy_async_smem();
+    // O holds sum_{t<j} P_t V_t: PV(j-1) was issued before S(j), whose completion we saw.
     if (__any_sync(0xffffffffu, rescale)) {
-      // O holds sum_{t<j} P_t V_t only after PV_{j-1} completes.
-      w = mbar_wait(&sb->pv_done, static_cast<uint32_t>(j - 1) & 1u, abort_flag, status,
-                    kErrAttnWait);
-      if (!__all_sync(0xffffffffu, w)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
-        const uint32_t ta = tmem_o + static_cast<uint32_t>(c * 32) + lane_off;
-        tmem_ld32_wait(ta, r);
+        tmem_ld32_wait(o_cols + c * 32, r);
 #pragma unroll
         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-        tmem_st32(ta, r);
+        tmem_st32(o_cols + c * 32, r);
       }
-      tmem_st_wait();
     }
+    // pass 2: P = exp2(s * scale - m) as bf16 pairs over the score columns (keys 2k, 2k+1 in
+    // column k); the packed columns of keys [64h, 64h+64) land in columns [32h, 32h+32), which
+    // hold scores already read.
+    float sum = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t r0[32], r1[32], pk[32];
+      tmem_ld32_wait(s_cols + h * 64, r0);
+      tmem_ld32_wait(s_cols + h * 64 + 32, r1);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        // keys kv0 + 64h + {2i, 2i+1} (from r0) and kv0 + 64h + 32 + {2i, 2i+1} (from r1)
+        float e0 = fast_exp2(fmaf(__uint_as_float(r0[2 * i]), kScaleLog2, -m_run));
+        float e1 = fast_exp2(fmaf(__uint_as_float(r0[2 * i + 1]), kScaleLog2, -m_run));
+        float e2 = fast_exp2(fmaf(__uint_as_float(r1[2 * i]), kScaleLog2, -m_run));
+        float e3 = fast_exp2(fmaf(__uint_as_float(r1[2 * i + 1]), kScaleLog2, -m_run));
+        if (tail) {
+          const int k = kv0 + h * 64 + 2 * i;
+          if (k >= seq) e0 = 0.f;
+          if (k + 1 >= seq) e1 = 0.f;
+          if (k + 32 >= seq) e2 = 0.f;
+          if (k + 33 >= seq) e3 = 0.f;
+        }
+        pk[i] = pack_bf16x2(e0, e1);
+        pk[16 + i] = pack_bf16x2(e2, e3);
+        // normalise by the sum of the rounded weights the PV product actually uses
+        sum += (bf16_lo(pk[i]) + bf16_hi(pk[i])) + (bf16_lo(pk[16 + i]) + bf16_hi(pk[16 + i]));
+      }
+      tmem_st32(s_cols + h * 32, pk);
+    }
+    tmem_st_wait();
     l_run = l_run * alpha + sum;
     tc_fence_before();
-    mbar_arrive(&sb->p_full[buf]);
+    mbar_arrive(&sb->p_full[X]);
   }
-  if (!ok) return;
-  bool w = mbar_wait(&sb->o_full, 0, abort_flag, status, kErrAttnWait);
+  const bool w = mbar_wait(&sb->o_full, 0, abort_flag, status, kErrAttnWait);
   if (!__all_sync(0xffffffffu, w)) return;
   tc_fence_after();
-  const int s_row = q0 + row;
+  const int s_row = q0 + X * kQTile + row;
   const float inv_l = 1.f / l_run;
   OutT* dst = nullptr;
   if (s_row < seq) {
-    const int b = bh / heads, h = bh % heads;
+    const int b = bh / heads, hh = bh % heads;
     if (s_row < split)
-      dst = out0 + ((static_cast<size_t>(b) * split + s_row) * heads + h) * 128;
+      dst = out0 + ((static_cast<size_t>(b) * split + s_row) * heads + hh) * 128;
     else
-      dst = out1 + ((static_cast<size_t>(b) * (seq - split) + (s_row - split)) * heads + h) * 128;
+      dst = out1 + ((static_cast<size_t>(b) * (seq - split) + (s_row - split)) * heads + hh) * 128;
   }
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t r[32];
-    tmem_ld32_wait(tmem_o + static_cast<uint32_t>(c * 32) + lane_off, r);
+    tmem_ld32_wait(o_cols + c * 32, r);
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * inv_l;
     if (dst) store32(dst + c * 32, v);
   }
 }
+
 
 template <typename OutT>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -187,27 +178,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* s_q = smem;
-  uint8_t* s_kv = smem + kQBytes;
-  uint8_t* s_p = s_kv + kKvStages * kStageBytes;
-  AttnSmem* sb = reinterpret_cast<AttnSmem*>(smem + kSmemData);
+  AttnBarriers* sb = reinterpret_cast<AttnBarriers*>(smem + kSmemData);
   volatile int* abort_flag = &sb->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int q0 = blockIdx.x * kQTile;
+  const int q0 = blockIdx.x * 2 * kQTile;
   const int bh = blockIdx.y;
   const int n_kv = (seq + kKvTile - 1) / kKvTile;
 
   if (threadIdx.x == 0) {
     mbar_init(&sb->q_full, 1);
-    for (int s = 0; s < kKvStages; ++s) mbar_init(&sb->kv_full[s], 1), mbar_init(&sb->kv_empty[s], 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&sb->s_full[i], 1);
-      mbar_init(&sb->s_free[i], 128);
-      mbar_init(&sb->p_full[i], 128);
-      mbar_init(&sb->p_free[i], 1);
+    for (int s = 0; s < kKvStages; ++s) {
+      mbar_init(&sb->k_full[s], 1);
+      mbar_init(&sb->v_full[s], 1);
+      mbar_init(&sb->kv_empty[s], 1);
     }
-    mbar_init(&sb->pv_done, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sb->s_full[x], 1);
+      mbar_init(&sb->p_full[x], 128);
+    }
     mbar_init(&sb->o_full, 1);
     mbar_init(&sb->drain, 1);
     sb->abort_flag = 0;
@@ -221,7 +210,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sb->tmem_slot;
-  const uint32_t tmem_o = tmem + 256;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -229,86 +217,95 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_vt);
-      mbar_arrive_expect_tx(&sb->q_full, kQBytes);
-      tma_load_3d(s_q, &tm_q, &sb->q_full, 0, q0, bh);
-      tma_load_3d(s_q + kHalfTile, &tm_q, &sb->q_full, 64, q0, bh);
+      mbar_arrive_expect_tx(&sb->q_full, 2 * kTileBytes);
+      for (int x = 0; x < 2; ++x) {
+        tma_load_3d(q_tile(smem, x), &tm_q, &sb->q_full, 0, q0 + x * kQTile, bh);
+        tma_load_3d(q_tile(smem, x) + kHalfTile, &tm_q, &sb->q_full, 64, q0 + x * kQTile, bh);
+      }
       int last_parity[kKvStages] = {-1, -1};
       for (int j = 0; j < n_kv; ++j) {
         const int st = j % kKvStages;
         const uint32_t ph = static_cast<uint32_t>(j / kKvStages) & 1u;
         if (!mbar_wait(&sb->kv_empty[st], ph ^ 1u, abort_flag, status, kErrAttnWait)) break;
-        uint8_t* sk = s_kv + st * kStageBytes;
-        uint8_t* sv = sk + kKBytes;
         const int kv0 = j * kKvTile;
-        mbar_arrive_expect_tx(&sb->kv_full[st], kStageBytes);
-        tma_load_3d(sk, &tm_k, &sb->kv_full[st], 0, kv0, bh);
-        tma_load_3d(sk + kHalfTile, &tm_k, &sb->kv_full[st], 64, kv0, bh);
-        tma_load_3d(sv, &tm_vt, &sb->kv_full[st], kv0, 0, bh);
-        tma_load_3d(sv + kHalfTile, &tm_vt, &sb->kv_full[st], kv0 + 64, 0, bh);
+        mbar_arrive_expect_tx(&sb->k_full[st], kTileBytes);
+        tma_load_3d(k_tile(smem, st), &tm_k, &sb->k_full[st], 0, kv0, bh);
+        tma_load_3d(k_tile(smem, st) + kHalfTile, &tm_k, &sb->k_full[st], 64, kv0, bh);
+        mbar_arrive_expect_tx(&sb->v_full[st], kTileBytes);
+        tma_load_3d(v_tile(smem, st), &tm_vt, &sb->v_full[st], kv0, 0, bh);
+        tma_load_3d(v_tile(smem, st) + kHalfTile, &tm_vt, &sb->v_full[st], kv0 + 64, 0, bh);
         last_parity[st] = static_cast<int>(ph);
       }
       if (*abort_flag) {
+        // give the copies already issued a bounded chance to land before the CTA exits
         int never = 0;
         mbar_wait(&sb->q_full, 0, &never, status, 0);
         for (int s = 0; s < kKvStages; ++s)
-          if (last_parity[s] >= 0)
-            mbar_wait(&sb->kv_full[s], static_cast<uint32_t>(last_parity[s]), &never, status, 0);
+          if (last_parity[s] >= 0) {
+            mbar_wait(&sb->k_full[s], static_cast<uint32_t>(last_parity[s]), &never, status, 0);
+            mbar_wait(&sb->v_full[s], static_cast<uint32_t>(last_parity[s]), &never, status, 0);
+          }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      const uint32_t aq = smem_addr(s_q);
-      const uint32_t ap = smem_addr(s_p);
-      auto issue_pv = [&](int i) -> bool {
-        if (!mbar_wait(&sb->p_full[i & 1], static_cast<uint32_t>(i >> 1) & 1u, abort_flag, status,
-                       kErrAttnWait))
+      auto issue_s = [&](int x, int j) -> bool {
+        const int st = j % kKvStages;
+        if (!mbar_wait(&sb->k_full[st], static_cast<uint32_t>(j / kKvStages) & 1u, abort_flag,
+                       status, kErrAttnWait))
           return false;
         tc_fence_after();
-        const uint32_t pa = ap + static_cast<uint32_t>((i & 1) * kPBytes);
-        const uint32_t vb = smem_addr(s_kv + (i % kKvStages) * kStageBytes + kKBytes);
+        const uint32_t qa = smem_addr(q_tile(smem, x));
+        const uint32_t kb = smem_addr(k_tile(smem, st));
+        const uint32_t d_s = tmem + static_cast<uint32_t>(x * 128);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = static_cast<uint32_t>((k >> 2) * kHalfTile + (k & 3) * 32);
-          tc_mma<kKindF16>(tmem_o, sdesc_kmajor_sw128(pa + off), sdesc_kmajor_sw128(vb + off),
-                           kIdescQK, (i > 0 || k > 0) ? 1u : 0u);
+          tc_mma<kKindF16>(d_s, sdesc_kmajor_sw128(qa + off), sdesc_kmajor_sw128(kb + off), kIdesc,
+                           k > 0 ? 1u : 0u);
         }
-        tc_commit(&sb->pv_done);
-        tc_commit(&sb->p_free[i & 1]);
-        tc_commit(&sb->kv_empty[i % kKvStages]);
+        tc_commit(&sb->s_full[x]);
         return true;
       };
-      bool ok = mbar_wait(&sb->q_full, 0, abort_flag, status, kErrAttnWait);
-      for (int j = 0; ok && j < n_kv; ++j) {
+      auto issue_pv = [&](int x, int j) -> bool {
         const int st = j % kKvStages;
-        if (!mbar_wait(&sb->kv_full[st], static_cast<uint32_t>(j / kKvStages) & 1u, abort_flag,
-                       status, kErrAttnWait) ||
-            !mbar_wait(&sb->s_free[j & 1], (static_cast<uint32_t>(j >> 1) & 1u) ^ 1u, abort_flag,
-                       status, kErrAttnWait)) {
-          ok = false;
-          break;
-        }
+        if (!mbar_wait(&sb->p_full[x], static_cast<uint32_t>(j) & 1u, abort_flag, status,
+                       kErrAttnWait) ||
+            !mbar_wait(&sb->v_full[st], static_cast<uint32_t>(j / kKvStages) & 1u, abort_flag,
+                       status, kErrAttnWait))
+          return false;
         tc_fence_after();
-        const uint32_t kb = smem_addr(s_kv + st * kStageBytes);
-        const uint32_t d_s = tmem + static_cast<uint32_t>((j & 1) * 128);
+        const uint32_t vb = smem_addr(v_tile(smem, st));
+        const uint32_t p_cols = tmem + static_cast<uint32_t>(x * 128);  // P: 16 keys per 8 columns
+        const uint32_t d_o = tmem + 256u + static_cast<uint32_t>(x * 128);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = static_cast<uint32_t>((k >> 2) * kHalfTile + (k & 3) * 32);
-          tc_mma<kKindF16>(d_s, sdesc_kmajor_sw128(aq + off), sdesc_kmajor_sw128(kb + off),
-                           kIdescQK, k > 0 ? 1u : 0u);
+          tc_mma_ts_f16(d_o, p_cols + static_cast<uint32_t>(k * 8), sdesc_kmajor_sw128(vb + off),
+                        kIdesc, (j > 0 || k > 0) ? 1u : 0u);
         }
-        tc_commit(&sb->s_full[j & 1]);
-        if (j >= 1 && !issue_pv(j - 1)) ok = false;
+        return true;
+      };
+      bool ok = mbar_wait(&sb->q_full, 0, abort_flag, status, kErrAttnWait) && issue_s(0, 0) &&
+                issue_s(1, 0);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const bool more = j + 1 < n_kv;
+        ok = issue_pv(0, j) && (!more || issue_s(0, j + 1)) && issue_pv(1, j);
+        if (!ok) break;
+        tc_commit(&sb->kv_empty[j % kKvStages]);
+        if (more && !issue_s(1, j + 1)) ok = false;
       }
-      if (ok && issue_pv(n_kv - 1)) tc_commit(&sb->o_full);
+      if (ok) tc_commit(&sb->o_full);
       if (*abort_flag) {
+        // wait (bounded) for every MMA issued so far before TMEM is released
         int never = 0;
         tc_commit(&sb->drain);
         mbar_wait(&sb->drain, 0, &never, status, 0);
       }
     }
-  } else {
-    softmax_role<OutT>(sb, s_p, tmem, tmem_o, q0, bh, heads, seq, split, n_kv, out0, out1, status);
+  } else if (warp >= 4) {
+    softmax_role<OutT>(sb, (warp - 4) >> 2, tmem, q0, bh, heads, seq, split, n_kv, out0, out1, status);
   }
 
   __syncthreads();
@@ -336,32 +333,27 @@ cudaError_t launch_attention(const AttnProblem& p, uint32_t* status, cudaStream_
       !encode_tmap(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.vt, dv, sv, box,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  const dim3 grid((p.seq + kQTile - 1) / kQTile, static_cast<unsigned>(bh));
+  const dim3 grid((p.seq + 2 * kQTile - 1) / (2 * kQTile), static_cast<unsigned>(bh));
   int dev = 0;
   cudaGetDevice(&dev);
-  if (p.act == 1) {
-    static int configured = -1;
-    if (configured != dev) {
-      cudaError_t e = cudaFuncSetAttribute(attention_kernel<__nv_bfloat16>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-      if (e != cudaSuccess) return e;
-      configured = dev;
-    }
+  static int configured = -1;
+  if (configured != dev) {
+    cudaError_t e = cudaFuncSetAttribute(attention_kernel<__nv_bfloat16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attention_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kAttnSmem);
+    if (e != cudaSuccess) return e;
+    configured = dev;
+  }
+  if (p.act == 1)
     attention_kernel<__nv_bfloat16><<<grid, kAttnThreads, kAttnSmem, stream>>>(
         tq, tk, tv, p.heads, p.seq, p.split, static_cast<__nv_bfloat16*>(p.out0),
         static_cast<__nv_bfloat16*>(p.out1), status);
-  } else {
-    static int configured = -1;
-    if (configured != dev) {
-      cudaError_t e = cudaFuncSetAttribute(attention_kernel<float>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-      if (e != cudaSuccess) return e;
-      configured = dev;
-    }
+  else
     attention_kernel<float><<<grid, kAttnThreads, kAttnSmem, stream>>>(
-        tq, tk, tv, p.heads, p.seq, p.split, static_cast<float*>(p.out0),
-        static_cast<float*>(p.out1), status);
-  }
+        tq, tk, tv, p.heads, p.seq, p.split, static_cast<float*>(p.out0), static_cast<float*>(p.out1),
+        status);
   count_launch();
   return cudaGetLastError();
 }

@@ -165,6 +165,17 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
   }
 }
 
+// D(tmem) (+)= A(tmem) * B(smem)^T for kind::f16: A is read from tensor memory (row i in lane i,
+// two 16-bit elements per 32-bit column, the lower half first).
+__device__ __forceinline__ void tc_mma_ts_f16(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor for a K-major operand stored with the 128-byte swizzle:
 // rows of 128 bytes, 8-row groups (1024-byte swizzle atoms) stacked at 1024-byte stride.
 // Fields: start address >> 4 (bits 0-13), leading offset >> 4 (16-29, unused for this
