@@ -237,68 +237,103 @@ T* at(void* ws, size_t off) {
 }
 
 // Launches the chain of one block over stream s (double block: s = 0 image, 1 text).
-mmdit_status run_stream_qkv(const mmdit_dims* d, const BlockPlan& p, int s, const mmdit_stream_w* w,
-                            const void* vec, const float* cs, const float* sn, const void* x,
-                            void* ws, cudaStream_t st, bool do_mod) {
-  const int rows_per_batch = p.single ? p.S : (s == 0 ? p.Si : p.St);
-  const int rows = p.B * rows_per_batch;
-  float* mod = at<float>(ws, p.mod[s]);
-  if (do_mod) {
-    ProfScope ps_(p.single ? "single.modulation" : (s == 0 ? "double.modulation.img" : "double.modulation.txt"), st);
-    MMDIT_CUDA(launch_modulation(d->act, vec, w->w_mod, w->b_mod, p.B, 6 * p.D, p.D, mod, st),
-               "modulation");
+// The streams a block call runs: the image and text streams of a double block (each only if
+// it has rows), or the single block's one stream over the joint sequence.  Each GEMM of the
+// block is one launch over all of them (equal N and K, per-stream operands and epilogues).
+struct Streams {
+  int n = 0;
+  int s[2] = {0, 0};  // plan slot: 0 image / single, 1 text
+  const mmdit_stream_w* w[2] = {nullptr, nullptr};
+  const void* x[2] = {nullptr, nullptr};
+  void* y[2] = {nullptr, nullptr};
+  int rpb[2] = {0, 0};  // rows per batch element
+};
+
+void add_problem(GemmProblem& g, int i, int M, const void* A, const void* W, const EpiArgs& ep) {
+  if (i == 0)
+    g.M = M, g.A = A, g.W = W, g.ep = ep;
+  else
+    g.M1 = M, g.A1 = A, g.W1 = W, g.ep1 = ep;
+}
+
+mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss, const float* cs,
+                     const float* sn, void* ws, cudaStream_t st) {
+  {
+    ProfScope ps_(p.single ? "single.ln1" : "double.ln1", st);
+    for (int i = 0; i < ss.n; ++i) {
+      const float* mod = at<float>(ws, p.mod[ss.s[i]]);
+      MMDIT_CUDA(launch_ln_modulate(d->act, d->act == MMDIT_F32, ss.x[i], mod, mod + p.D, 6 * p.D,
+                                    p.B * ss.rpb[i], ss.rpb[i], p.D, d->ln_eps, at(ws, p.h[ss.s[i]]), st),
+                 "LayerNorm-modulate (attention branch)");
+    }
   }
-  if (rows == 0) return MMDIT_OK;
-  { ProfScope ps_(p.single ? "single.ln1" : (s == 0 ? "double.ln1.img" : "double.ln1.txt"), st);
-  MMDIT_CUDA(launch_ln_modulate(d->act, d->act == MMDIT_F32, x, mod, mod + p.D, 6 * p.D, rows, rows_per_batch, p.D,
-                                d->ln_eps, at(ws, p.h[s]), st),
-             "LayerNorm-modulate (attention branch)"); }
   GemmProblem g;
-  g.act = d->act, g.epi = kEpiQkv, g.M = rows, g.N = 3 * p.D, g.K = p.D;
-  g.A = at(ws, p.h[s]), g.W = w->w_qkv;
-  g.ep.bias = w->b_qkv, g.ep.g_q = w->g_q, g.ep.g_k = w->g_k;
-  g.ep.rope_cos = cs, g.ep.rope_sin = sn;
-  g.ep.q = at<__nv_bfloat16>(ws, p.q), g.ep.k = at<__nv_bfloat16>(ws, p.k);
-  g.ep.vt = at<__nv_bfloat16>(ws, p.vt);
-  g.ep.rows_per_batch = rows_per_batch;
-  g.ep.seq_offset = (p.single || s == 0) ? 0 : p.Si;
-  g.ep.seq_joint = p.S, g.ep.seq_pad = p.S_pad, g.ep.heads = p.H, g.ep.hidden = p.D;
-  g.ep.rms_eps = d->rms_eps, g.ep.rope_interleaved = d->rope_interleaved ? 1 : 0;
-  { ProfScope ps_(p.single ? "single.qkv" : (s == 0 ? "double.qkv.img" : "double.qkv.txt"), st);
-  MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "QKV projection"); }
+  g.act = d->act, g.epi = kEpiQkv, g.N = 3 * p.D, g.K = p.D;
+  for (int i = 0; i < ss.n; ++i) {
+    const mmdit_stream_w* w = ss.w[i];
+    EpiArgs e;
+    e.bias = w->b_qkv, e.g_q = w->g_q, e.g_k = w->g_k;
+    e.rope_cos = cs, e.rope_sin = sn;
+    e.q = at<__nv_bfloat16>(ws, p.q), e.k = at<__nv_bfloat16>(ws, p.k);
+    e.vt = at<__nv_bfloat16>(ws, p.vt);
+    e.rows_per_batch = ss.rpb[i];
+    e.seq_offset = ss.s[i] == 0 ? 0 : p.Si;
+    e.seq_joint = p.S, e.seq_pad = p.S_pad, e.heads = p.H, e.hidden = p.D;
+    e.rms_eps = d->rms_eps, e.rope_interleaved = d->rope_interleaved ? 1 : 0;
+    add_problem(g, i, p.B * ss.rpb[i], at(ws, p.h[ss.s[i]]), w->w_qkv, e);
+  }
+  ProfScope ps_(p.single ? "single.qkv" : "double.qkv", st);
+  MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "QKV projection");
   return MMDIT_OK;
 }
 
-mmdit_status run_stream_post(const mmdit_dims* d, const BlockPlan& p, int s, const mmdit_stream_w* w,
-                             const void* x, void* y, void* ws, cudaStream_t st) {
-  const int rows_per_batch = p.single ? p.S : (s == 0 ? p.Si : p.St);
-  const int rows = p.B * rows_per_batch;
-  if (rows == 0) return MMDIT_OK;
-  const float* mod = at<float>(ws, p.mod[s]);
+mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss, void* ws,
+                      cudaStream_t st) {
   GemmProblem g;
-  g.act = d->act, g.epi = kEpiGateResid, g.M = rows, g.N = p.D, g.K = p.D;
-  g.A = at(ws, p.o[s]), g.W = w->w_o;
-  g.ep.bias = w->b_o, g.ep.resid = x, g.ep.gate = mod + 2 * p.D, g.ep.gate_bstride = 6 * p.D;
-  g.ep.rows_per_batch = rows_per_batch, g.ep.out = at(ws, p.x1[s]), g.ep.out_f32 = 1;
-  { ProfScope ps_(p.single ? "single.out" : (s == 0 ? "double.out.img" : "double.out.txt"), st);
-  MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "attention output projection"); }
-  { ProfScope ps_(p.single ? "single.ln2" : (s == 0 ? "double.ln2.img" : "double.ln2.txt"), st);
-  MMDIT_CUDA(launch_ln_modulate(d->act, 1, at(ws, p.x1[s]), mod + 3 * p.D, mod + 4 * p.D, 6 * p.D, rows,
-                                rows_per_batch, p.D, d->ln_eps, at(ws, p.h[s]), st),
-             "LayerNorm-modulate (MLP branch)"); }
+  g.act = d->act, g.epi = kEpiGateResid, g.N = p.D, g.K = p.D;
+  for (int i = 0; i < ss.n; ++i) {
+    const float* mod = at<float>(ws, p.mod[ss.s[i]]);
+    EpiArgs e;
+    e.bias = ss.w[i]->b_o, e.resid = ss.x[i], e.gate = mod + 2 * p.D, e.gate_bstride = 6 * p.D;
+    e.rows_per_batch = ss.rpb[i], e.out = at(ws, p.x1[ss.s[i]]), e.out_f32 = 1;
+    add_problem(g, i, p.B * ss.rpb[i], at(ws, p.o[ss.s[i]]), ss.w[i]->w_o, e);
+  }
+  {
+    ProfScope ps_(p.single ? "single.out" : "double.out", st);
+    MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "attention output projection");
+  }
+  {
+    ProfScope ps_(p.single ? "single.ln2" : "double.ln2", st);
+    for (int i = 0; i < ss.n; ++i) {
+      const float* mod = at<float>(ws, p.mod[ss.s[i]]);
+      MMDIT_CUDA(launch_ln_modulate(d->act, 1, at(ws, p.x1[ss.s[i]]), mod + 3 * p.D, mod + 4 * p.D,
+                                    6 * p.D, p.B * ss.rpb[i], ss.rpb[i], p.D, d->ln_eps,
+                                    at(ws, p.h[ss.s[i]]), st),
+                 "LayerNorm-modulate (MLP branch)");
+    }
+  }
   GemmProblem f1;
-  f1.act = d->act, f1.epi = kEpiGelu, f1.M = rows, f1.N = p.F, f1.K = p.D;
-  f1.A = at(ws, p.h[s]), f1.W = w->w_1;
-  f1.ep.bias = w->b_1, f1.ep.gelu_tanh = d->gelu_tanh, f1.ep.out = at(ws, p.u[s]);
-  { ProfScope ps_(p.single ? "single.fc1" : (s == 0 ? "double.fc1.img" : "double.fc1.txt"), st);
-  MMDIT_CUDA(launch_gemm(f1, status_word(ws), st), "MLP fc1 + GELU"); }
+  f1.act = d->act, f1.epi = kEpiGelu, f1.N = p.F, f1.K = p.D;
+  for (int i = 0; i < ss.n; ++i) {
+    EpiArgs e;
+    e.bias = ss.w[i]->b_1, e.gelu_tanh = d->gelu_tanh, e.out = at(ws, p.u[ss.s[i]]);
+    add_problem(f1, i, p.B * ss.rpb[i], at(ws, p.h[ss.s[i]]), ss.w[i]->w_1, e);
+  }
+  {
+    ProfScope ps_(p.single ? "single.fc1" : "double.fc1", st);
+    MMDIT_CUDA(launch_gemm(f1, status_word(ws), st), "MLP fc1 + GELU");
+  }
   GemmProblem f2;
-  f2.act = d->act, f2.epi = kEpiGateResid, f2.M = rows, f2.N = p.D, f2.K = p.F;
-  f2.A = at(ws, p.u[s]), f2.W = w->w_2;
-  f2.ep.bias = w->b_2, f2.ep.resid = at(ws, p.x1[s]), f2.ep.resid_f32 = 1, f2.ep.gate = mod + 5 * p.D;
-  f2.ep.gate_bstride = 6 * p.D, f2.ep.rows_per_batch = rows_per_batch, f2.ep.out = y;
-  { ProfScope ps_(p.single ? "single.fc2" : (s == 0 ? "double.fc2.img" : "double.fc2.txt"), st);
-  MMDIT_CUDA(launch_gemm(f2, status_word(ws), st), "MLP fc2 + gated residual"); }
+  f2.act = d->act, f2.epi = kEpiGateResid, f2.N = p.D, f2.K = p.F;
+  for (int i = 0; i < ss.n; ++i) {
+    const float* mod = at<float>(ws, p.mod[ss.s[i]]);
+    EpiArgs e;
+    e.bias = ss.w[i]->b_2, e.resid = at(ws, p.x1[ss.s[i]]), e.resid_f32 = 1, e.gate = mod + 5 * p.D;
+    e.gate_bstride = 6 * p.D, e.rows_per_batch = ss.rpb[i], e.out = ss.y[i];
+    add_problem(f2, i, p.B * ss.rpb[i], at(ws, p.u[ss.s[i]]), ss.w[i]->w_2, e);
+  }
+  ProfScope ps_(p.single ? "single.fc2" : "double.fc2", st);
+  MMDIT_CUDA(launch_gemm(f2, status_word(ws), st), "MLP fc2 + gated residual");
   return MMDIT_OK;
 }
 
@@ -602,9 +637,6 @@ mmdit_status mmdit_double_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
   if ((s = check_workspace(workspace, workspace_bytes, p.total)) != MMDIT_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
-  const mmdit_stream_w* ws_[2] = {w_img, w_txt};
-  const void* xs[2] = {x_img, x_txt};
-  void* ys[2] = {y_img, y_txt};
   {
     // both streams' AdaLN modulation in one launch (they share vec)
     ProfScope ps_("double.modulation", st);
@@ -612,13 +644,20 @@ mmdit_status mmdit_double_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
                                    {w_txt->w_mod, w_txt->b_mod, at<float>(workspace, p.mod[1]), 6 * p.D}};
     MMDIT_CUDA(launch_modulation2(d->act, vec, jobs, 2, p.B, p.D, st), "modulation");
   }
+  Streams ss;
+  const mmdit_stream_w* wsets[2] = {w_img, w_txt};
+  const void* xs[2] = {x_img, x_txt};
+  void* ys[2] = {y_img, y_txt};
+  const int rpb[2] = {p.Si, p.St};
   for (int i = 0; i < 2; ++i)
-    if ((s = run_stream_qkv(d, p, i, ws_[i], vec, rope_cos, rope_sin, xs[i], workspace, st, false)) != MMDIT_OK)
-      return s;
+    if (rpb[i] > 0) {
+      ss.s[ss.n] = i, ss.w[ss.n] = wsets[i], ss.x[ss.n] = xs[i], ss.y[ss.n] = ys[i];
+      ss.rpb[ss.n] = rpb[i];
+      ++ss.n;
+    }
+  if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
-  for (int i = 0; i < 2; ++i)
-    if ((s = run_stream_post(d, p, i, ws_[i], xs[i], ys[i], workspace, st)) != MMDIT_OK) return s;
-  return MMDIT_OK;
+  return run_post(d, p, ss, workspace, st);
 }
 
 mmdit_status mmdit_single_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w, const void* vec,
@@ -637,9 +676,17 @@ mmdit_status mmdit_single_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
   if ((s = check_workspace(workspace, workspace_bytes, p.total)) != MMDIT_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
-  if ((s = run_stream_qkv(d, p, 0, w, vec, rope_cos, rope_sin, x, workspace, st, true)) != MMDIT_OK) return s;
+  {
+    ProfScope ps_("single.modulation", st);
+    MMDIT_CUDA(launch_modulation(d->act, vec, w->w_mod, w->b_mod, p.B, 6 * p.D, p.D,
+                                 at<float>(workspace, p.mod[0]), st),
+               "modulation");
+  }
+  Streams ss;
+  ss.n = 1, ss.s[0] = 0, ss.w[0] = w, ss.x[0] = x, ss.y[0] = y, ss.rpb[0] = p.S;
+  if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
-  return run_stream_post(d, p, 0, w, x, y, workspace, st);
+  return run_post(d, p, ss, workspace, st);
 }
 
 }  // extern "C"

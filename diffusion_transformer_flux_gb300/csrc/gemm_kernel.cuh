@@ -196,8 +196,10 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t taddr, int m, int n0, int
 // ----------------------------------------------------------------------------- kernel
 template <int KIND, int BN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   int M, int N, int K, EpiArgs ep, uint32_t* status) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_b0,
+                   const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b1,
+                   int M0, int M1, int N, int K, const __grid_constant__ EpiArgs ep0,
+                   const __grid_constant__ EpiArgs ep1, uint32_t* status) {
   using Cfg = GemmCfg<BN>;
   using T = typename KindTraits<KIND>::T;
   constexpr int kBK = 128 / KindTraits<KIND>::kEltBytes;     // elements per 128-byte K slice
@@ -217,8 +219,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_m = (M + kBM - 1) / kBM;
-  const int num_tiles = num_m * ((N + BN - 1) / BN);
+  // Two problems of equal N and K share the launch (e.g. the image and text streams); the tile
+  // list holds problem 0's tiles, M fastest, then problem 1's.
+  const int num_n = (N + BN - 1) / BN;
+  const int num_m0 = (M0 + kBM - 1) / kBM, num_m1 = (M1 + kBM - 1) / kBM;
+  const int tiles0 = num_m0 * num_n;
+  const int num_tiles = tiles0 + num_m1 * num_n;
+  auto decode = [&](int tile, int& prob, int& mb, int& nb) {
+    prob = tile >= tiles0;
+    const int t = prob ? tile - tiles0 : tile;
+    const int nm = prob ? num_m1 : num_m0;
+    mb = t % nm, nb = t / nm;
+  };
   const int num_kb = (K + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
@@ -240,15 +252,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
-      tma_prefetch_desc(&tm_a);
-      tma_prefetch_desc(&tm_b);
+      tma_prefetch_desc(&tm_a0);
+      tma_prefetch_desc(&tm_b0);
+      if (M1 > 0) tma_prefetch_desc(&tm_a1), tma_prefetch_desc(&tm_b1);
       int stage = 0;
       uint32_t phase = 0;
       int last_parity[Cfg::kStages];
       for (int s = 0; s < Cfg::kStages; ++s) last_parity[s] = -1;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int mb = tile % num_m, nb = tile / num_m;
+        int prob, mb, nb;
+        decode(tile, prob, mb, nb);
+        const CUtensorMap* ma = prob ? &tm_a1 : &tm_a0;
+        const CUtensorMap* mw = prob ? &tm_b1 : &tm_b0;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, status, kErrGemmWait)) {
             ok = false;
@@ -256,8 +272,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           uint8_t* sa = smem + stage * Cfg::kStageBytes;
           mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
-          tma_load_2d(sa, &tm_a, &full[stage], kb * kBK, mb * kBM);
-          tma_load_2d(sa + Cfg::kABytes, &tm_b, &full[stage], kb * kBK, nb * BN);
+          tma_load_2d(sa, ma, &full[stage], kb * kBK, mb * kBM);
+          tma_load_2d(sa + Cfg::kABytes, mw, &full[stage], kb * kBK, nb * BN);
           last_parity[stage] = static_cast<int>(phase);
           if (++stage == Cfg::kStages) stage = 0, phase ^= 1;
         }
@@ -313,13 +329,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int mb = tile % num_m, nb = tile / num_m;
+      int prob, mb, nb;
+      decode(tile, prob, mb, nb);
       bool ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, status, kErrGemmWait);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      gemm_epilogue<T, BN, EPI>(taddr, mb * kBM + row, nb * BN, M, N, ep);
+      gemm_epilogue<T, BN, EPI>(taddr, mb * kBM + row, nb * BN, prob ? M1 : M0, N, prob ? ep1 : ep0);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       if (++acc == 2) acc = 0, acc_phase ^= 1;
@@ -341,14 +358,18 @@ cudaError_t run_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream
   constexpr int kBK = 128 / kElt;
   const CUtensorMapDataType dt =
       KIND == kKindF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  CUtensorMap ta, tb;
-  const uint64_t da[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.M)};
-  const uint64_t db[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
+  const bool two = p.M1 > 0;
+  CUtensorMap ta0, tb0, ta1, tb1;
   const uint64_t stride[1] = {static_cast<uint64_t>(p.K) * kElt};
   const uint32_t box_a[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kBM)};
   const uint32_t box_b[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(BN)};
-  if (!encode_tmap(&ta, dt, 2, p.A, da, stride, box_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap(&tb, dt, 2, p.W, db, stride, box_b, CU_TENSOR_MAP_SWIZZLE_128B))
+  const uint64_t da0[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.M)};
+  const uint64_t db[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
+  const uint64_t da1[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(two ? p.M1 : p.M)};
+  if (!encode_tmap(&ta0, dt, 2, p.A, da0, stride, box_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap(&tb0, dt, 2, p.W, db, stride, box_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap(&ta1, dt, 2, two ? p.A1 : p.A, da1, stride, box_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap(&tb1, dt, 2, two ? p.W1 : p.W, db, stride, box_b, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   auto kern = gemm_tc_kernel<KIND, BN, EPI>;
   static int configured_device = -1;
@@ -360,9 +381,12 @@ cudaError_t run_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const int tiles = ((p.M + kBM - 1) / kBM) * ((p.N + BN - 1) / BN);
+  const int num_n = (p.N + BN - 1) / BN;
+  const int tiles = ((p.M + kBM - 1) / kBM + (two ? (p.M1 + kBM - 1) / kBM : 0)) * num_n;
+  if (tiles == 0) return cudaSuccess;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, kGemmThreads, Cfg::kSmemBytes, stream>>>(ta, tb, p.M, p.N, p.K, p.ep, status);
+  kern<<<grid, kGemmThreads, Cfg::kSmemBytes, stream>>>(ta0, tb0, ta1, tb1, p.M, two ? p.M1 : 0, p.N,
+                                                        p.K, p.ep, two ? p.ep1 : p.ep, status);
   count_launch();
   return cudaGetLastError();
 }

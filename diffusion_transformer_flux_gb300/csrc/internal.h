@@ -52,6 +52,11 @@ struct GemmProblem {
   const void* A = nullptr;  // [M, K]
   const void* W = nullptr;  // [N, K]
   EpiArgs ep;
+  // optional second problem with the same N, K and epilogue kind, run in the same launch
+  int M1 = 0;
+  const void* A1 = nullptr;  // [M1, K]
+  const void* W1 = nullptr;  // [N, K]
+  EpiArgs ep1;
 };
 
 // Device status word layout: the first 4 bytes of every workspace.
