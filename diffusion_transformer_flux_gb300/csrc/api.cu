@@ -260,12 +260,13 @@ mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss,
                      const float* sn, void* ws, cudaStream_t st) {
   {
     ProfScope ps_(p.single ? "single.ln1" : "double.ln1", st);
+    LnModJob jobs[2];
     for (int i = 0; i < ss.n; ++i) {
       const float* mod = at<float>(ws, p.mod[ss.s[i]]);
-      MMDIT_CUDA(launch_ln_modulate(d->act, d->act == MMDIT_F32, ss.x[i], mod, mod + p.D, 6 * p.D,
-                                    p.B * ss.rpb[i], ss.rpb[i], p.D, d->ln_eps, at(ws, p.h[ss.s[i]]), st),
-                 "LayerNorm-modulate (attention branch)");
+      jobs[i] = {ss.x[i], mod, mod + p.D, 6 * p.D, at(ws, p.h[ss.s[i]]), p.B * ss.rpb[i], ss.rpb[i]};
     }
+    MMDIT_CUDA(launch_ln_modulate2(d->act, d->act == MMDIT_F32, jobs, ss.n, p.D, d->ln_eps, st),
+               "LayerNorm-modulate (attention branch)");
   }
   GemmProblem g;
   g.act = d->act, g.epi = kEpiQkv, g.N = 3 * p.D, g.K = p.D;
@@ -304,13 +305,14 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
   }
   {
     ProfScope ps_(p.single ? "single.ln2" : "double.ln2", st);
+    LnModJob jobs[2];
     for (int i = 0; i < ss.n; ++i) {
       const float* mod = at<float>(ws, p.mod[ss.s[i]]);
-      MMDIT_CUDA(launch_ln_modulate(d->act, 1, at(ws, p.x1[ss.s[i]]), mod + 3 * p.D, mod + 4 * p.D,
-                                    6 * p.D, p.B * ss.rpb[i], ss.rpb[i], p.D, d->ln_eps,
-                                    at(ws, p.h[ss.s[i]]), st),
-                 "LayerNorm-modulate (MLP branch)");
+      jobs[i] = {at(ws, p.x1[ss.s[i]]), mod + 3 * p.D, mod + 4 * p.D, 6 * p.D, at(ws, p.h[ss.s[i]]),
+                 p.B * ss.rpb[i], ss.rpb[i]};
     }
+    MMDIT_CUDA(launch_ln_modulate2(d->act, 1, jobs, ss.n, p.D, d->ln_eps, st),
+               "LayerNorm-modulate (MLP branch)");
   }
   GemmProblem f1;
   f1.act = d->act, f1.epi = kEpiGelu, f1.N = p.F, f1.K = p.D;

@@ -3,6 +3,8 @@
 // All use 128-bit loads and stores along the contiguous axis.
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -159,18 +161,71 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __rest
 }
 
 // ----------------------------------------------------------------------------- LN + modulate
-// One warp per row: mean, biased variance (two passes over the L1-resident row), then
-// out = (x - mean) * rsqrt(var + eps) * (1 + scale[b]) + shift[b].
+// One warp per row: mean, biased variance, then out = (x - mean) * rsqrt(var + eps) * (1 + scale[b])
+// + shift[b].  Rows of up to kLnMaxChunks * 256 elements are held in registers (one load round
+// trip, exact two-pass statistics); longer rows stream through L1 in three passes.  Up to two
+// row sets (the image and text streams) share a launch.
+constexpr int kLnMaxChunks = 16;
+
+struct LnJob {
+  const void* x;
+  const float* shift;
+  const float* scale;
+  int64_t mod_bstride;
+  void* out;
+  int rows;
+  int rpb;
+};
+
+template <typename TI, typename T, int NC>
+__device__ __forceinline__ void ln_row_regs(const TI* xr, const float* sh, const float* sc, T* orow,
+                                            int dim, float eps, int lane) {
+  Raw8<TI> raw[NC];
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const int k = c * 256 + lane * 8;
+    if (k < dim) raw[c].load(xr + k);
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    if (c * 256 + lane * 8 < dim) {
+      float v[8];
+      raw[c].to_f32(v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s += v[e];
+    }
+  }
+  const float mean = warp_sum(s) / dim;
+  float q = 0.f;
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    if (c * 256 + lane * 8 < dim) {
+      float v[8];
+      raw[c].to_f32(v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q = fmaf(v[e] - mean, v[e] - mean, q);
+    }
+  }
+  const float rstd = rsqrtf(warp_sum(q) / dim + eps);
+#pragma unroll
+  for (int c = 0; c < NC; ++c) {
+    const int k = c * 256 + lane * 8;
+    if (k < dim) {
+      float v[8], a[8], b[8];
+      raw[c].to_f32(v);
+      load8(sh + k, a);
+      load8(sc + k, b);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = fmaf((v[e] - mean) * rstd, 1.f + b[e], a[e]);
+      store8(orow + k, v);
+    }
+  }
+}
+
 template <typename TI, typename T>
-__global__ void __launch_bounds__(256) ln_modulate_kernel(const TI* __restrict__ x,
-                                                          const float* __restrict__ shift,
-                                                          const float* __restrict__ scale,
-                                                          int64_t mod_bstride, int rows, int rpb,
-                                                          int dim, float eps, T* __restrict__ out) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (r >= rows) return;
-  const TI* xr = x + static_cast<size_t>(r) * dim;
+__device__ __forceinline__ void ln_row_stream(const TI* xr, const float* sh, const float* sc, T* orow,
+                                              int dim, float eps, int lane) {
   float s = 0.f;
   for (int k = lane * 8; k < dim; k += 256) {
     float v[8];
@@ -187,10 +242,6 @@ __global__ void __launch_bounds__(256) ln_modulate_kernel(const TI* __restrict__
     for (int e = 0; e < 8; ++e) q = fmaf(v[e] - mean, v[e] - mean, q);
   }
   const float rstd = rsqrtf(warp_sum(q) / dim + eps);
-  const int b = r / rpb;
-  const float* sh = shift + b * mod_bstride;
-  const float* sc = scale + b * mod_bstride;
-  T* orow = out + static_cast<size_t>(r) * dim;
   for (int k = lane * 8; k < dim; k += 256) {
     float v[8], a[8], c[8];
     load8(xr + k, v);
@@ -200,6 +251,25 @@ __global__ void __launch_bounds__(256) ln_modulate_kernel(const TI* __restrict__
     for (int e = 0; e < 8; ++e) v[e] = fmaf((v[e] - mean) * rstd, 1.f + c[e], a[e]);
     store8(orow + k, v);
   }
+}
+
+template <typename TI, typename T, int NC>
+__global__ void __launch_bounds__(256) ln_modulate_kernel(LnJob j0, LnJob j1, int dim, float eps) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (g >= j0.rows + j1.rows) return;
+  const bool second = g >= j0.rows;
+  const LnJob& job = second ? j1 : j0;
+  const int r = second ? g - j0.rows : g;
+  const TI* xr = static_cast<const TI*>(job.x) + static_cast<size_t>(r) * dim;
+  const int b = r / job.rpb;
+  const float* sh = job.shift + b * job.mod_bstride;
+  const float* sc = job.scale + b * job.mod_bstride;
+  T* orow = static_cast<T*>(job.out) + static_cast<size_t>(r) * dim;
+  if constexpr (NC > 0)
+    ln_row_regs<TI, T, NC>(xr, sh, sc, orow, dim, eps, lane);
+  else
+    ln_row_stream<TI, T>(xr, sh, sc, orow, dim, eps, lane);
 }
 
 // ----------------------------------------------------------------------------- transposes
@@ -379,25 +449,46 @@ cudaError_t launch_modulation(int act, const void* vec, const void* w, const voi
   return launch_modulation2(act, vec, &job, 1, batch, dim, stream);
 }
 
+cudaError_t launch_ln_modulate2(int act, int x_f32, const LnModJob* jobs, int njobs, int dim,
+                                float eps, cudaStream_t stream) {
+  LnJob j[2] = {{nullptr, nullptr, nullptr, 0, nullptr, 0, 1}, {nullptr, nullptr, nullptr, 0, nullptr, 0, 1}};
+  int rows = 0;
+  for (int i = 0; i < njobs && i < 2; ++i) {
+    j[i] = {jobs[i].x, jobs[i].shift, jobs[i].scale, jobs[i].mod_bstride, jobs[i].out, jobs[i].rows,
+            jobs[i].rows_per_batch};
+    rows += jobs[i].rows;
+  }
+  if (rows == 0) return cudaSuccess;
+  const int grid = (rows + 7) / 8;
+  const int chunks = (dim + 255) / 256;
+  auto go = [&](auto nc_tag) {
+    constexpr int NC = decltype(nc_tag)::value;
+    if (act == 1 && x_f32)
+      ln_modulate_kernel<float, __nv_bfloat16, NC><<<grid, 256, 0, stream>>>(j[0], j[1], dim, eps);
+    else if (act == 1)
+      ln_modulate_kernel<__nv_bfloat16, __nv_bfloat16, NC><<<grid, 256, 0, stream>>>(j[0], j[1], dim, eps);
+    else
+      ln_modulate_kernel<float, float, NC><<<grid, 256, 0, stream>>>(j[0], j[1], dim, eps);
+  };
+  if (chunks <= 4)
+    go(std::integral_constant<int, 4>());
+  else if (chunks <= 8)
+    go(std::integral_constant<int, 8>());
+  else if (chunks <= 12)
+    go(std::integral_constant<int, 12>());
+  else if (chunks <= kLnMaxChunks)
+    go(std::integral_constant<int, kLnMaxChunks>());
+  else
+    go(std::integral_constant<int, 0>());
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_ln_modulate(int act, int x_f32, const void* x, const float* shift, const float* scale,
                                int64_t mod_bstride, int rows, int rows_per_batch, int dim, float eps,
                                void* out, cudaStream_t stream) {
-  if (rows == 0) return cudaSuccess;
-  const int grid = (rows + 7) / 8;
-  if (act == 1 && x_f32)
-    ln_modulate_kernel<float, __nv_bfloat16><<<grid, 256, 0, stream>>>(
-        static_cast<const float*>(x), shift, scale, mod_bstride, rows, rows_per_batch, dim, eps,
-        static_cast<__nv_bfloat16*>(out));
-  else if (act == 1)
-    ln_modulate_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), shift, scale, mod_bstride, rows, rows_per_batch, dim,
-        eps, static_cast<__nv_bfloat16*>(out));
-  else
-    ln_modulate_kernel<float, float><<<grid, 256, 0, stream>>>(
-        static_cast<const float*>(x), shift, scale, mod_bstride, rows, rows_per_batch, dim, eps,
-        static_cast<float*>(out));
-  count_launch();
-  return cudaGetLastError();
+  const LnModJob job{x, shift, scale, mod_bstride, out, rows, rows_per_batch};
+  return launch_ln_modulate2(act, x_f32, &job, 1, dim, eps, stream);
 }
 
 cudaError_t launch_patchify(int act, const float* z, int batch, int channels, int hw, void* out,

@@ -336,7 +336,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      gemm_epilogue<T, BN, EPI>(taddr, mb * kBM + row, nb * BN, prob ? M1 : M0, N, prob ? ep1 : ep0);
+      // a private copy, so the epilogue's arguments live in registers rather than being
+      // re-read from parameter space around every store
+      const EpiArgs ep = prob ? ep1 : ep0;
+      gemm_epilogue<T, BN, EPI>(taddr, mb * kBM + row, nb * BN, prob ? M1 : M0, N, ep);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       if (++acc == 2) acc = 0, acc_phase ^= 1;

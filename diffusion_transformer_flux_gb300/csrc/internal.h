@@ -117,6 +117,18 @@ cudaError_t launch_modulation2(int act, const void* vec, const ModulationJob* jo
 cudaError_t launch_ln_modulate(int act, int x_f32, const void* x, const float* shift, const float* scale,
                                int64_t mod_bstride, int rows, int rows_per_batch, int dim, float eps,
                                void* out, cudaStream_t stream);
+// The same for up to two row sets in one launch.
+struct LnModJob {
+  const void* x;
+  const float* shift;
+  const float* scale;
+  int64_t mod_bstride;
+  void* out;
+  int rows;
+  int rows_per_batch;
+};
+cudaError_t launch_ln_modulate2(int act, int x_f32, const LnModJob* jobs, int njobs, int dim, float eps,
+                                cudaStream_t stream);
 // z [B, C, HW] fp32 -> tokens [B, HW, C] of the activation type.
 cudaError_t launch_patchify(int act, const float* z, int batch, int channels, int hw, void* out,
                             cudaStream_t stream);
