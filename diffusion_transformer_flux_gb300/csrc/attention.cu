@@ -77,16 +77,17 @@ __device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t t
     tc_fence_after();
     const int kv0 = j * kKvTile;
     const bool tail = kv0 + kKvTile > seq;
-    // pass 1: the row maximum of the valid keys
+    // pass 1: the row maximum of the valid keys (two TMEM round trips of 64 columns)
     float mx = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t r[32];
-      tmem_ld32_wait(s_cols + c * 32, r);
+    for (int h = 0; h < 2; ++h) {
+      uint32_t ra[32], rb[32];
+      tmem_ld64_wait(s_cols + h * 64, ra, rb);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float v = (tail && kv0 + c * 32 + i >= seq) ? -INFINITY : __uint_as_float(r[i]);
-        mx = fmaxf(mx, v);
+        const float va = (tail && kv0 + h * 64 + i >= seq) ? -INFINITY : __uint_as_float(ra[i]);
+        const float vb = (tail && kv0 + h * 64 + 32 + i >= seq) ? -INFINITY : __uint_as_float(rb[i]);
+        mx = fmaxf(mx, fmaxf(va, vb));
       }
     }
     mx *= kScaleLog2;
@@ -117,8 +118,7 @@ __device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t t
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       uint32_t r0[32], r1[32], pk[32];
-      tmem_ld32_wait(s_cols + h * 64, r0);
-      tmem_ld32_wait(s_cols + h * 64 + 32, r1);
+      tmem_ld64_wait(s_cols + h * 64, r0, r1);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         // keys kv0 + 64h + {2i, 2i+1} (from r0) and kv0 + 64h + 32 + {2i, 2i+1} (from r1)
