@@ -6,7 +6,8 @@
 //               memory stages (128-byte swizzle, the layout the tensor core reads directly);
 //   warp 1      MMA issuer (one thread): tcgen05.mma into a double-buffered fp32 accumulator in
 //               tensor memory (TMEM), so the epilogue of tile i overlaps the main loop of i+1;
-//   warps 2..5  epilogue: tcgen05.ld of one accumulator row per thread, fused math, stores.
+//   warps 2..9  epilogue: two warps per TMEM lane quarter, each taking half of the tile's
+//               columns; tcgen05.ld of one accumulator row per thread, fused math, stores.
 // Every wait is bounded (common.cuh); on a give-up the CTA drains what it started and exits.
 #pragma once
 
@@ -16,7 +17,8 @@
 namespace mmdit {
 
 constexpr int kBM = 128;
-constexpr int kGemmThreads = 192;
+constexpr int kGemmThreads = 320;
+constexpr int kEpiGroups = 2;  // epilogue warp groups splitting the tile columns
 
 template <int KIND>
 struct KindTraits;
@@ -61,8 +63,9 @@ __device__ __forceinline__ void tmem_load_f32(uint32_t taddr, float (&v)[32]) {
 // ----------------------------------------------------------------------------- epilogues
 // Row-wise epilogue of one 128 x BN accumulator tile.  `m` is this thread's output row, `n0`
 // the tile's first column.  All 32 lanes of the warp must call this (tcgen05.ld is collective).
+// `group` (0 or 1) selects which half of the tile's columns (or heads) this warp handles.
 template <typename T, int BN, int EPI>
-__device__ __forceinline__ void gemm_epilogue(uint32_t taddr, int m, int n0, int M, int N,
+__device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, int n0, int M, int N,
                                               const EpiArgs& ep) {
   const bool row_ok = m < M;
   if constexpr (EPI == kEpiQkv) {
@@ -70,7 +73,7 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t taddr, int m, int n0, int
     const int b = row_ok ? m / ep.rows_per_batch : 0;
     const int sj = (row_ok ? m % ep.rows_per_batch : 0) + ep.seq_offset;
 #pragma unroll 1
-    for (int hh = 0; hh < BN / 128; ++hh) {
+    for (int hh = group; hh < BN / 128; hh += kEpiGroups) {
       const int nh = n0 + hh * 128;
       if (nh >= N) break;
       const int which = nh / ep.hidden;
@@ -150,7 +153,9 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t taddr, int m, int n0, int
     }
   } else {
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
+    constexpr int kChunks = BN / 32;
+    constexpr int kPer = (kChunks + kEpiGroups - 1) / kEpiGroups;
+    for (int c = group * kPer; c < (group + 1) * kPer && c < kChunks; ++c) {
       const int n = n0 + c * 32;
       if (n >= N) break;  // uniform across the warp
       float v[32];
@@ -164,7 +169,14 @@ __device__ __forceinline__ void gemm_epilogue(uint32_t taddr, int m, int n0, int
       }
       if constexpr (EPI == kEpiGelu) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i], ep.gelu_tanh);
+        // the variant is chosen once per chunk so the 32 evaluations interleave
+        if (ep.gelu_tanh) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i], 1);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i], 0);
+        }
       }
       if constexpr (EPI == kEpiGateResid) {
         const int b = m / ep.rows_per_batch;
@@ -235,7 +247,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], 1);
-    for (int a = 0; a < 2; ++a) mbar_init(&tfull[a], 1), mbar_init(&tempty[a], 128);
+    for (int a = 0; a < 2; ++a) mbar_init(&tfull[a], 1), mbar_init(&tempty[a], 32 * 4 * kEpiGroups);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -323,8 +335,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue warps 2..5; warp w reads TMEM lanes 32*(w%4) .. +31
+    // ---------------- epilogue warps 2..9; warp w reads TMEM lanes 32*(w%4) .. +31 and takes
+    // the half of the columns given by its group (warps 2..5: group 0, 6..9: group 1)
     const int quarter = warp & 3;
+    const int group = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -339,7 +353,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // a private copy, so the epilogue's arguments live in registers rather than being
       // re-read from parameter space around every store
       const EpiArgs ep = prob ? ep1 : ep0;
-      gemm_epilogue<T, BN, EPI>(taddr, mb * kBM + row, nb * BN, prob ? M1 : M0, N, ep);
+      gemm_epilogue<T, BN, EPI>(group, taddr, mb * kBM + row, nb * BN, prob ? M1 : M0, N, ep);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       if (++acc == 2) acc = 0, acc_phase ^= 1;
