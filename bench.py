@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-steps", type=int, default=5)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time plain per-call launches instead of a CUDA-graph replay of the step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time of the oracle baseline sample")
     args = ap.parse_args()
@@ -441,10 +443,34 @@ def main():
         if L.mmdit_workspace_status(ws) != 0:
             raise RuntimeError("a kernel gave up a bounded wait during warm-up")
 
+    # library launches of one step, counted on a plain (uncaptured) step
+    L.mmdit_launch_count_reset()
+    st.step()
+    torch.cuda.synchronize()
+    launches_per_step = L.mmdit_launch_count()
+    step_fn = st.step
+    if not args.no_graph:
+        # the whole step as one CUDA graph (captured on a side stream after warm-up there)
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=device)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                st.step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph):
+            st.step()
+        torch.cuda.synchronize()
+        step_fn = graph.replay
+        for _ in range(args.warmup):
+            step_fn()
+        torch.cuda.synchronize()
     props = torch.cuda.get_device_properties(device)
     uuid = str(getattr(props, "uuid", "") or "") or None
     with ClockSampler(uuid) as clk:
-        ms, launches = timed(st.step, args.steps)
+        ms, _ = timed(step_fn, args.steps)
+    launches = launches_per_step * args.steps
     clocks = clk.summary()
     if not np.isfinite(st.loss.item()):
         raise RuntimeError("non-finite loss")
@@ -519,6 +545,8 @@ def main():
                        "heads": wl.heads, "head_dim": 128, "mlp_hidden": wl.mlp_hidden,
                        "parallelism": f"{world} independent replica(s), no exchange",
                        "l2": "flushed before every timed step (256 MB write outside the events)",
+                       "launch": "plain calls" if args.no_graph else
+                                 "CUDA-graph replay of the step (e2e: plain calls)",
                        "step": "rope3d_freqs, flow-matching noise, img_in, txt_in, double block, "
                                "single block, output head, flow-matching loss",
                        "flops_counted_per_step": st.flops_blocks,

@@ -120,18 +120,55 @@ int num_sms() {
   return cached[dev];
 }
 
+namespace {
+// Per-thread cache of encoded tensor maps.  A map depends only on the arguments below, so a
+// cached copy stays valid for as long as the same (address, shape) pair is passed again.
+struct TmapKey {
+  int32_t dtype, rank, swizzle, pad;
+  const void* base;
+  uint64_t dims[5];
+  uint64_t strides[4];
+  uint32_t box[5];
+  uint32_t pad2;
+};
+struct TmapEntry {
+  TmapKey key;
+  CUtensorMap map;
+  bool used;
+};
+constexpr int kTmapCache = 128;
+thread_local TmapEntry g_tmap_cache[kTmapCache];
+thread_local int g_tmap_next = 0;
+}  // namespace
+
 bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                  CUtensorMapSwizzle swizzle) {
+  TmapKey key;
+  memset(&key, 0, sizeof(key));
+  key.dtype = static_cast<int32_t>(dtype), key.rank = rank, key.swizzle = static_cast<int32_t>(swizzle);
+  key.base = base;
+  for (int i = 0; i < rank && i < 5; ++i) key.dims[i] = dims[i], key.box[i] = box[i];
+  for (int i = 0; i < rank - 1 && i < 4; ++i) key.strides[i] = strides_bytes[i];
+  for (int i = 0; i < kTmapCache; ++i)
+    if (g_tmap_cache[i].used && memcmp(&g_tmap_cache[i].key, &key, sizeof(key)) == 0) {
+      *map = g_tmap_cache[i].map;
+      return true;
+    }
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t d[5], s[4];
   cuuint32_t b[5], e[5];
   for (int i = 0; i < rank; ++i) d[i] = dims[i], b[i] = box[i], e[i] = 1;
   for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
-  return fn(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, e,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (fn(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, s, b, e,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  TmapEntry& slot = g_tmap_cache[g_tmap_next];
+  g_tmap_next = (g_tmap_next + 1) % kTmapCache;
+  slot.key = key, slot.map = *map, slot.used = true;
+  return true;
 }
 
 // ----------------------------------------------------------------------------- block planning

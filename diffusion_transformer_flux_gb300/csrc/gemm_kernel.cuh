@@ -6,8 +6,9 @@
 //               memory stages (128-byte swizzle, the layout the tensor core reads directly);
 //   warp 1      MMA issuer (one thread): tcgen05.mma into a double-buffered fp32 accumulator in
 //               tensor memory (TMEM), so the epilogue of tile i overlaps the main loop of i+1;
-//   warps 2..9  epilogue: two warps per TMEM lane quarter, each taking half of the tile's
-//               columns; tcgen05.ld of one accumulator row per thread, fused math, stores.
+//   warps 2..   epilogue: one or two warps per TMEM lane quarter (two split the tile's columns
+//               for the GELU epilogue); tcgen05.ld of one accumulator row per thread, fused
+//               math, stores.
 // Every wait is bounded (common.cuh); on a give-up the CTA drains what it started and exits.
 #pragma once
 
@@ -17,8 +18,16 @@
 namespace mmdit {
 
 constexpr int kBM = 128;
-constexpr int kGemmThreads = 320;
-constexpr int kEpiGroups = 2;  // epilogue warp groups splitting the tile columns
+// Epilogue warp groups splitting the tile columns: two for the arithmetic-heavy GELU epilogue,
+// one for the others (whose epilogues hide under the main loop already).
+template <int EPI>
+struct EpiGroups {
+  static constexpr int value = EPI == kEpiGelu ? 2 : 1;
+};
+template <int EPI>
+constexpr int gemm_threads() {
+  return 64 + 128 * EpiGroups<EPI>::value;
+}
 
 template <int KIND>
 struct KindTraits;
@@ -63,7 +72,7 @@ __device__ __forceinline__ void tmem_load_f32(uint32_t taddr, float (&v)[32]) {
 // ----------------------------------------------------------------------------- epilogues
 // Row-wise epilogue of one 128 x BN accumulator tile.  `m` is this thread's output row, `n0`
 // the tile's first column.  All 32 lanes of the warp must call this (tcgen05.ld is collective).
-// `group` (0 or 1) selects which half of the tile's columns (or heads) this warp handles.
+// `group` selects which part of the tile's columns (or heads) this warp handles.
 template <typename T, int BN, int EPI>
 __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, int n0, int M, int N,
                                               const EpiArgs& ep) {
@@ -73,7 +82,7 @@ __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, 
     const int b = row_ok ? m / ep.rows_per_batch : 0;
     const int sj = (row_ok ? m % ep.rows_per_batch : 0) + ep.seq_offset;
 #pragma unroll 1
-    for (int hh = group; hh < BN / 128; hh += kEpiGroups) {
+    for (int hh = group; hh < BN / 128; hh += EpiGroups<EPI>::value) {
       const int nh = n0 + hh * 128;
       if (nh >= N) break;
       const int which = nh / ep.hidden;
@@ -154,7 +163,7 @@ __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, 
   } else {
 #pragma unroll 1
     constexpr int kChunks = BN / 32;
-    constexpr int kPer = (kChunks + kEpiGroups - 1) / kEpiGroups;
+    constexpr int kPer = (kChunks + EpiGroups<EPI>::value - 1) / EpiGroups<EPI>::value;
     for (int c = group * kPer; c < (group + 1) * kPer && c < kChunks; ++c) {
       const int n = n0 + c * 32;
       if (n >= N) break;  // uniform across the warp
@@ -207,7 +216,7 @@ __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, 
 
 // ----------------------------------------------------------------------------- kernel
 template <int KIND, int BN, int EPI>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_b0,
                    const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b1,
                    int M0, int M1, int N, int K, const __grid_constant__ EpiArgs ep0,
@@ -247,7 +256,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], 1);
-    for (int a = 0; a < 2; ++a) mbar_init(&tfull[a], 1), mbar_init(&tempty[a], 32 * 4 * kEpiGroups);
+    for (int a = 0; a < 2; ++a) mbar_init(&tfull[a], 1), mbar_init(&tempty[a], 32 * 4 * EpiGroups<EPI>::value);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -335,8 +344,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue warps 2..9; warp w reads TMEM lanes 32*(w%4) .. +31 and takes
-    // the half of the columns given by its group (warps 2..5: group 0, 6..9: group 1)
+    // ---------------- epilogue warps 2..; warp w reads TMEM lanes 32*(w%4) .. +31 and takes
+    // the part of the columns given by its group (warps 2..5: group 0, 6..9: group 1)
     const int quarter = warp & 3;
     const int group = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
@@ -402,7 +411,7 @@ cudaError_t run_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream
   const int tiles = ((p.M + kBM - 1) / kBM + (two ? (p.M1 + kBM - 1) / kBM : 0)) * num_n;
   if (tiles == 0) return cudaSuccess;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, kGemmThreads, Cfg::kSmemBytes, stream>>>(ta0, tb0, ta1, tb1, p.M, two ? p.M1 : 0, p.N,
+  kern<<<grid, gemm_threads<EPI>(), Cfg::kSmemBytes, stream>>>(ta0, tb0, ta1, tb1, p.M, two ? p.M1 : 0, p.N,
                                                         p.K, p.ep, two ? p.ep1 : p.ep, status);
   count_launch();
   return cudaGetLastError();
