@@ -143,7 +143,7 @@ class DeviceStep:
                        L.mmdit_single_block_workspace_size(self.dims))
         self.ws_block = L.workspace(ws_block, device)
         self.ws_flow = L.workspace(L.flow_match_workspace_size(B, self.z0[0].numel()), device)
-        self.ws_lin = L.workspace(256, device)
+        self.ws_lin = L.workspace(L.mmdit_linear_workspace_size(L.MMDIT_BF16, B * S_t, D, wl.ctx_dim), device)
         self.ws_img = L.workspace(L.mmdit_img_in_workspace_size(L.MMDIT_BF16, B, wl.channels, wl.lat_h,
                                                                 wl.lat_w), device)
         self.ws_final = L.workspace(L.mmdit_final_layer_workspace_size(self.dims_final, wl.channels), device)

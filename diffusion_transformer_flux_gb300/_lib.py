@@ -70,7 +70,7 @@ _SIGS = {
     "flow_match_workspace_size": (SZ, [I32, I64]),
     "flow_match_noise_and_loss": (C.c_int, [I32, VP, VP, VP, I32, I64, VP, VP, VP, VP, SZ, VP]),
     "flow_match_noise_and_loss_noalloc": (C.c_int, [I32, VP, VP, VP, I32, I64, VP, VP, VP, VP]),
-    "mmdit_linear_workspace_size": (SZ, []),
+    "mmdit_linear_workspace_size": (SZ, [I32, I32, I32, I32]),
     "mmdit_linear_fwd": (C.c_int, [I32, I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_img_in_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
     "mmdit_img_in_fwd": (C.c_int, [I32, I32, I32, I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
@@ -217,11 +217,15 @@ def flow_match_noise_and_loss_noalloc(z0, z1, t, z_t=None, pred=None, loss=None,
                                                     _stream(stream)))
 
 
+def mmdit_linear_workspace_size(act, M, N, K) -> int:
+    return load().mmdit_linear_workspace_size(act, M, N, K)
+
+
 def mmdit_linear_fwd(x, w, b, y, ws=None, stream=None):
     M, K = x.reshape(-1, x.shape[-1]).shape
     N = w.shape[0]
     if ws is None:
-        ws = workspace(load().mmdit_linear_workspace_size(), x.device)
+        ws = workspace(mmdit_linear_workspace_size(act_of(x), M, N, K), x.device)
     _check(load().mmdit_linear_fwd(act_of(x), M, N, K, _ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(ws),
                                    ws.numel(), _stream(stream)))
     return ws

@@ -107,15 +107,24 @@ struct ProfScope {
 };
 }  // namespace
 
+// SM count of the current device; without a device (size queries on a host-only machine) the
+// GB300 count, so that workspace sizes do not depend on whether a GPU is visible.
+constexpr int kDefaultSms = 152;
 int num_sms() {
   static int cached[64] = {0};
   int dev = 0;
-  cudaGetDevice(&dev);
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return kDefaultSms;
+  }
   if (dev < 0 || dev >= 64) dev = 0;
   if (cached[dev] == 0) {
     int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return kDefaultSms;
+    }
+    cached[dev] = n > 0 ? n : kDefaultSms;
   }
   return cached[dev];
 }
@@ -260,6 +269,21 @@ static mmdit_status check_workspace(void* ws, size_t have, size_t need) {
     cudaError_t e_ = (call);                         \
     if (e_ != cudaSuccess) return cuda_fail(e_, what); \
   } while (0)
+
+// Split-K factor for a narrow GEMM (few output tiles, long K): enough work items to cover the
+// SMs, at least 4 K slices per item, never an empty split.
+static int choose_splits(int M, int N, int K, int elt_bytes) {
+  const int bn = N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : (N % 64 == 0 ? 64 : 32));
+  const int tiles = ((M + 127) / 128) * ((N + bn - 1) / bn);
+  const int kb = (K * elt_bytes + 127) / 128;
+  if (tiles * 2 > num_sms() || kb < 8) return 1;
+  int s = num_sms() / tiles;
+  if (s > kb / 4) s = kb / 4;
+  if (s > 8) s = 8;
+  if (s < 2) return 1;
+  const int per = (kb + s - 1) / s;
+  return (kb + per - 1) / per;  // every split gets at least one K slice
+}
 
 }  // namespace mmdit
 
@@ -492,7 +516,14 @@ mmdit_status flow_match_noise_and_loss(int32_t dtype, const void* z0, const void
   return MMDIT_OK;
 }
 
-size_t mmdit_linear_workspace_size(void) { return kStatusBytes; }
+size_t mmdit_linear_workspace_size(int32_t act, int32_t M, int32_t N, int32_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return kStatusBytes;
+  const int splits = choose_splits(M, N, K, static_cast<int>(elt_bytes(act)));
+  if (splits <= 1) return kStatusBytes;
+  Carver c;
+  c.take(static_cast<size_t>(splits) * M * N * sizeof(float));
+  return c.off;
+}
 
 mmdit_status mmdit_linear_fwd(int32_t act, int32_t M, int32_t N, int32_t K, const void* x,
                               const void* w, const void* b, void* y, void* workspace,
@@ -504,16 +535,26 @@ mmdit_status mmdit_linear_fwd(int32_t act, int32_t M, int32_t N, int32_t K, cons
   mmdit_status s = check_ptrs({x, w, y}, "linear");
   if (s != MMDIT_OK) return s;
   if (b && !aligned16(b)) return fail(MMDIT_ERR_INVALID_ARG, "linear: bias not 16-byte aligned");
-  if ((s = check_workspace(workspace, workspace_bytes, mmdit_linear_workspace_size())) != MMDIT_OK)
+  if ((s = check_workspace(workspace, workspace_bytes, mmdit_linear_workspace_size(act, M, N, K))) !=
+      MMDIT_OK)
     return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
   if (M == 0) return MMDIT_OK;
+  const int splits = choose_splits(M, N, K, static_cast<int>(elt_bytes(act)));
   GemmProblem g;
-  g.act = act, g.epi = kEpiBias, g.M = M, g.N = N, g.K = K, g.A = x, g.W = w;
-  g.ep.bias = b, g.ep.out = y;
+  g.act = act, g.M = M, g.N = N, g.K = K, g.A = x, g.W = w;
   ProfScope ps_("linear", st);
-  MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "linear");
+  if (splits > 1) {
+    // narrow GEMM: K split across work items, fp32 partials, then a fixed-order finish
+    float* partials = at<float>(workspace, kStatusBytes);
+    g.epi = kEpiPartial, g.splits = splits, g.ep.out = partials;
+    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "linear (split K)");
+    MMDIT_CUDA(launch_splitk_reduce(act, partials, splits, M, N, b, y, 0, st), "linear (split-K sum)");
+  } else {
+    g.epi = kEpiBias, g.ep.bias = b, g.ep.out = y;
+    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "linear");
+  }
   return MMDIT_OK;
 }
 
@@ -553,11 +594,13 @@ mmdit_status mmdit_img_in_fwd(int32_t act, int32_t batch, int32_t channels, int3
 }
 
 size_t mmdit_final_layer_workspace_size(const mmdit_dims* d, int32_t channels) {
-  (void)channels;
-  if (!d || d->batch < 1 || d->hidden < 1 || d->seq_img < 0) return 0;
+  if (!d || d->batch < 1 || d->hidden < 1 || d->seq_img < 0 || channels < 1) return 0;
   Carver c;
   c.take(static_cast<size_t>(d->batch) * 2 * d->hidden * 4);
   c.take(static_cast<size_t>(d->batch) * d->seq_img * d->hidden * elt_bytes(d->act));
+  const int M = d->batch * d->seq_img;
+  const int splits = choose_splits(M, channels, d->hidden, static_cast<int>(elt_bytes(d->act)));
+  if (splits > 1) c.take(static_cast<size_t>(splits) * M * channels * sizeof(float));
   return c.off;
 }
 
@@ -588,9 +631,19 @@ mmdit_status mmdit_final_layer_fwd(const mmdit_dims* d, int32_t channels, int32_
   MMDIT_CUDA(launch_ln_modulate(d->act, d->act == MMDIT_F32, x_img, mod, mod + D, 2 * D, rows, d->seq_img, D, d->ln_eps, h, st),
              "final LayerNorm-modulate");
   GemmProblem g;
-  g.act = d->act, g.epi = kEpiUnpatchify, g.M = rows, g.N = channels, g.K = D;
-  g.A = h, g.W = w_out, g.ep.bias = b_out, g.ep.out = pred, g.ep.rows_per_batch = d->seq_img;
-  MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "final projection");
+  g.act = d->act, g.M = rows, g.N = channels, g.K = D, g.A = h, g.W = w_out;
+  const int splits = choose_splits(rows, channels, D, static_cast<int>(elt_bytes(d->act)));
+  if (splits > 1) {
+    float* partials = at<float>(workspace, c.take(static_cast<size_t>(splits) * rows * channels * 4));
+    g.epi = kEpiPartial, g.splits = splits, g.ep.out = partials;
+    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "final projection (split K)");
+    MMDIT_CUDA(launch_splitk_reduce(d->act, partials, splits, rows, channels, b_out, pred,
+                                    d->seq_img, st),
+               "final projection (split-K sum)");
+  } else {
+    g.epi = kEpiUnpatchify, g.ep.bias = b_out, g.ep.out = pred, g.ep.rows_per_batch = d->seq_img;
+    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "final projection");
+  }
   return MMDIT_OK;
 }
 

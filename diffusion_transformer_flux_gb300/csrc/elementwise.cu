@@ -64,10 +64,8 @@ __global__ void rope3d_kernel(const float* __restrict__ ids, int64_t n_tok, Rope
 // ----------------------------------------------------------------------------- modulation GEMV
 // m[b, r] = sum_k SiLU(vec[b, k]) w[r, k] + bias[r], one warp per weight row, batch <= 8 per
 // launch.  Up to two weight sets (the image and text streams of a double block) share a launch.
-// Each warp issues kModLoads 16-byte loads per lane before using any of them, so a row of
-// D = 3072 bf16 weights is two rounds of loads.
+// Each warp issues all of a row's 16-byte loads (NC per lane) before using any of them.
 constexpr int kModMaxBatch = 8;
-constexpr int kModLoads = 8;
 constexpr int kModThreads = 128;
 
 struct ModJob {
@@ -100,7 +98,7 @@ struct Raw8<float> {
   }
 };
 
-template <typename T>
+template <typename T, int NC>
 __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __restrict__ vec, ModJob j0,
                                                                  ModJob j1, int batch, int dim) {
   extern __shared__ float svec[];  // [batch, dim] SiLU(vec), a bf16 operand in bf16 mode
@@ -121,30 +119,29 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __rest
     const ModJob& job = second ? j1 : j0;
     const int r = second ? g - j0.rows : g;
     const T* wr = reinterpret_cast<const T*>(job.w) + static_cast<size_t>(r) * dim;
+    // the whole row in one round of 16-byte loads (NC per lane)
+    Raw8<T> raw[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const int k = c * 256 + lane * 8;
+      if (k < dim) raw[c].load(wr + k);
+    }
     float acc[kModMaxBatch];
 #pragma unroll
     for (int b = 0; b < kModMaxBatch; ++b) acc[b] = 0.f;
-    for (int k0 = 0; k0 < dim; k0 += kModLoads * 256) {
-      Raw8<T> raw[kModLoads];
 #pragma unroll
-      for (int u = 0; u < kModLoads; ++u) {
-        const int k = k0 + u * 256 + lane * 8;
-        if (k < dim) raw[u].load(wr + k);
-      }
+    for (int c = 0; c < NC; ++c) {
+      const int k = c * 256 + lane * 8;
+      if (k < dim) {
+        float wv[8];
+        raw[c].to_f32(wv);
 #pragma unroll
-      for (int u = 0; u < kModLoads; ++u) {
-        const int k = k0 + u * 256 + lane * 8;
-        if (k < dim) {
-          float wv[8];
-          raw[u].to_f32(wv);
-#pragma unroll
-          for (int b = 0; b < kModMaxBatch; ++b) {
-            if (b < batch) {
-              const float4 s0 = *reinterpret_cast<const float4*>(svec + b * dim + k);
-              const float4 s1 = *reinterpret_cast<const float4*>(svec + b * dim + k + 4);
-              acc[b] += wv[0] * s0.x + wv[1] * s0.y + wv[2] * s0.z + wv[3] * s0.w + wv[4] * s1.x +
-                        wv[5] * s1.y + wv[6] * s1.z + wv[7] * s1.w;
-            }
+        for (int b = 0; b < kModMaxBatch; ++b) {
+          if (b < batch) {
+            const float4 s0 = *reinterpret_cast<const float4*>(svec + b * dim + k);
+            const float4 s1 = *reinterpret_cast<const float4*>(svec + b * dim + k + 4);
+            acc[b] += wv[0] * s0.x + wv[1] * s0.y + wv[2] * s0.z + wv[3] * s0.w + wv[4] * s1.x +
+                      wv[5] * s1.y + wv[6] * s1.z + wv[7] * s1.w;
           }
         }
       }
@@ -254,22 +251,48 @@ __device__ __forceinline__ void ln_row_stream(const TI* xr, const float* sh, con
 }
 
 template <typename TI, typename T, int NC>
-__global__ void __launch_bounds__(256) ln_modulate_kernel(LnJob j0, LnJob j1, int dim, float eps) {
+__global__ void __launch_bounds__(256) ln_modulate_kernel(LnJob j0, LnJob j1, int dim, float eps,
+                                                          int stage_mod) {
+  // shift/scale of one (job, batch element) staged in shared memory when the row width allows;
+  // rows of another batch element read them from global memory
+  extern __shared__ float smod[];  // [2, dim]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (g >= j0.rows + j1.rows) return;
-  const bool second = g >= j0.rows;
-  const LnJob& job = second ? j1 : j0;
-  const int r = second ? g - j0.rows : g;
-  const TI* xr = static_cast<const TI*>(job.x) + static_cast<size_t>(r) * dim;
-  const int b = r / job.rpb;
-  const float* sh = job.shift + b * job.mod_bstride;
-  const float* sc = job.scale + b * job.mod_bstride;
-  T* orow = static_cast<T*>(job.out) + static_cast<size_t>(r) * dim;
-  if constexpr (NC > 0)
-    ln_row_regs<TI, T, NC>(xr, sh, sc, orow, dim, eps, lane);
-  else
-    ln_row_stream<TI, T>(xr, sh, sc, orow, dim, eps, lane);
+  const int warps = blockDim.x >> 5;
+  const int total = j0.rows + j1.rows;
+  int staged_key = -1;
+  for (int base = blockIdx.x * warps; base < total; base += gridDim.x * warps) {
+    const int g = base + warp;
+    // the block stages the (job, batch) of its first row of this round
+    if (stage_mod) {
+      const bool s2 = base >= j0.rows;
+      const LnJob& sj = s2 ? j1 : j0;
+      const int sb = (s2 ? base - j0.rows : base) / sj.rpb;
+      const int key = (s2 ? 1 << 30 : 0) + sb;
+      if (key != staged_key) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < dim; i += blockDim.x) {
+          smod[i] = sj.shift[sb * sj.mod_bstride + i];
+          smod[dim + i] = sj.scale[sb * sj.mod_bstride + i];
+        }
+        __syncthreads();
+        staged_key = key;
+      }
+    }
+    if (g >= total) continue;
+    const bool second = g >= j0.rows;
+    const LnJob& job = second ? j1 : j0;
+    const int r = second ? g - j0.rows : g;
+    const TI* xr = static_cast<const TI*>(job.x) + static_cast<size_t>(r) * dim;
+    const int b = r / job.rpb;
+    const bool from_smem = stage_mod && ((second ? 1 << 30 : 0) + b) == staged_key;
+    const float* sh = from_smem ? smod : job.shift + b * job.mod_bstride;
+    const float* sc = from_smem ? smod + dim : job.scale + b * job.mod_bstride;
+    T* orow = static_cast<T*>(job.out) + static_cast<size_t>(r) * dim;
+    if constexpr (NC > 0)
+      ln_row_regs<TI, T, NC>(xr, sh, sc, orow, dim, eps, lane);
+    else
+      ln_row_stream<TI, T>(xr, sh, sc, orow, dim, eps, lane);
+  }
 }
 
 // ----------------------------------------------------------------------------- transposes
@@ -311,6 +334,43 @@ __global__ void transpose_v_kernel(const __nv_bfloat16* __restrict__ v, int seq,
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int s = s0 + threadIdx.x;
     if (s < seq) vt[(bh * 128 + j0 + i) * seq_pad + s] = tile[threadIdx.x][i];
+  }
+}
+
+// ----------------------------------------------------------------------------- split-K finish
+// out[m, n] = sum_s partial[s][m][n] + bias[n], summed in split order (deterministic); 8
+// consecutive columns per thread.  unpatchify_rows > 0 writes pred[b, n, r] (fp32) instead.
+template <typename T>
+__global__ void splitk_reduce_kernel(const float* __restrict__ partials, int splits, int M, int N,
+                                     const T* __restrict__ bias, void* __restrict__ out,
+                                     int unpatchify_rows) {
+  const int64_t total = static_cast<int64_t>(M) * N / 8;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i * 8;
+    const int m = static_cast<int>(e / N), n = static_cast<int>(e % N);
+    float v[8];
+    load8(partials + e, v);
+    for (int sp = 1; sp < splits; ++sp) {
+      float w[8];
+      load8(partials + static_cast<size_t>(sp) * M * N + e, w);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] += w[q];
+    }
+    if (bias) {
+      float b[8];
+      load8(bias + n, b);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] += b[q];
+    }
+    if (unpatchify_rows > 0) {
+      const int bb = m / unpatchify_rows, r = m % unpatchify_rows;
+      float* dst = static_cast<float*>(out) + (static_cast<size_t>(bb) * N + n) * unpatchify_rows + r;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) dst[static_cast<size_t>(q) * unpatchify_rows] = v[q];
+    } else {
+      store8(static_cast<T*>(out) + e, v);
+    }
   }
 }
 
@@ -404,25 +464,32 @@ cudaError_t launch_rope3d(const float* ids, int batch, int seq, const int axes[3
   return cudaGetLastError();
 }
 
-cudaError_t launch_modulation2(int act, const void* vec, const ModulationJob* jobs, int njobs,
-                               int batch, int dim, cudaStream_t stream) {
-  int total = 0;
-  for (int i = 0; i < njobs; ++i) total += jobs[i].rows;
-  const int warps = kModThreads / 32;
-  const int grid = blocks_for(total, warps, num_sms() * 6);
+template <typename T, int NC>
+cudaError_t launch_mod_nc(const void* vec, const ModJob& j0, const ModJob& j1, int nb, int dim,
+                          size_t smem, cudaStream_t stream) {
+  auto kern = modulation_kernel<T, NC>;
   static int configured = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured != dev) {
-    cudaError_t e = cudaFuncSetAttribute(modulation_kernel<__nv_bfloat16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(modulation_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               200 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     if (e != cudaSuccess) return e;
     configured = dev;
   }
+  int per_sm = 0;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kModThreads, smem);
+  if (per_sm < 1) per_sm = 1;
+  const int rows = j0.rows + j1.rows;
+  const int grid = blocks_for(rows, kModThreads / 32, num_sms() * per_sm);
+  kern<<<grid, kModThreads, smem, stream>>>(static_cast<const T*>(vec), j0, j1, nb, dim);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_modulation2(int act, const void* vec, const ModulationJob* jobs, int njobs,
+                               int batch, int dim, cudaStream_t stream) {
   const size_t elt = act == 1 ? 2 : 4;
+  const int chunks = (dim + 255) / 256;
   for (int b0 = 0; b0 < batch; b0 += kModMaxBatch) {
     const int nb = batch - b0 < kModMaxBatch ? batch - b0 : kModMaxBatch;
     const size_t smem = static_cast<size_t>(nb) * dim * sizeof(float);
@@ -430,14 +497,17 @@ cudaError_t launch_modulation2(int act, const void* vec, const ModulationJob* jo
     for (int i = 0; i < njobs && i < 2; ++i)
       j[i] = {jobs[i].w, jobs[i].bias, jobs[i].m + static_cast<size_t>(b0) * jobs[i].rows, jobs[i].rows};
     const void* vb = static_cast<const uint8_t*>(vec) + static_cast<size_t>(b0) * dim * elt;
-    if (act == 1)
-      modulation_kernel<__nv_bfloat16><<<grid, kModThreads, smem, stream>>>(
-          static_cast<const __nv_bfloat16*>(vb), j[0], j[1], nb, dim);
-    else
-      modulation_kernel<float><<<grid, kModThreads, smem, stream>>>(static_cast<const float*>(vb), j[0],
-                                                                    j[1], nb, dim);
-    count_launch();
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (act == 1) {
+      if (chunks <= 4) e = launch_mod_nc<__nv_bfloat16, 4>(vb, j[0], j[1], nb, dim, smem, stream);
+      else if (chunks <= 8) e = launch_mod_nc<__nv_bfloat16, 8>(vb, j[0], j[1], nb, dim, smem, stream);
+      else if (chunks <= 12) e = launch_mod_nc<__nv_bfloat16, 12>(vb, j[0], j[1], nb, dim, smem, stream);
+      else e = launch_mod_nc<__nv_bfloat16, 24>(vb, j[0], j[1], nb, dim, smem, stream);
+    } else {
+      if (chunks <= 4) e = launch_mod_nc<float, 4>(vb, j[0], j[1], nb, dim, smem, stream);
+      else if (chunks <= 8) e = launch_mod_nc<float, 8>(vb, j[0], j[1], nb, dim, smem, stream);
+      else e = launch_mod_nc<float, 16>(vb, j[0], j[1], nb, dim, smem, stream);
+    }
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -459,27 +529,43 @@ cudaError_t launch_ln_modulate2(int act, int x_f32, const LnModJob* jobs, int nj
     rows += jobs[i].rows;
   }
   if (rows == 0) return cudaSuccess;
-  const int grid = (rows + 7) / 8;
   const int chunks = (dim + 255) / 256;
-  auto go = [&](auto nc_tag) {
+  const int stage = dim <= 8192 ? 1 : 0;
+  const size_t smem = stage ? 2 * static_cast<size_t>(dim) * sizeof(float) : 0;
+  auto go = [&](auto nc_tag) -> cudaError_t {
     constexpr int NC = decltype(nc_tag)::value;
-    if (act == 1 && x_f32)
-      ln_modulate_kernel<float, __nv_bfloat16, NC><<<grid, 256, 0, stream>>>(j[0], j[1], dim, eps);
-    else if (act == 1)
-      ln_modulate_kernel<__nv_bfloat16, __nv_bfloat16, NC><<<grid, 256, 0, stream>>>(j[0], j[1], dim, eps);
-    else
-      ln_modulate_kernel<float, float, NC><<<grid, 256, 0, stream>>>(j[0], j[1], dim, eps);
+    auto launch = [&](auto kern) -> cudaError_t {
+      static int configured = -1;
+      int dev = 0;
+      cudaGetDevice(&dev);
+      if (configured != dev) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+        if (e != cudaSuccess) return e;
+        configured = dev;
+      }
+      int per_sm = 0;
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem);
+      if (per_sm < 1) per_sm = 1;
+      const int grid = blocks_for(rows, 8, num_sms() * per_sm);
+      kern<<<grid, 256, smem, stream>>>(j[0], j[1], dim, eps, stage);
+      return cudaSuccess;
+    };
+    if (act == 1 && x_f32) return launch(ln_modulate_kernel<float, __nv_bfloat16, NC>);
+    if (act == 1) return launch(ln_modulate_kernel<__nv_bfloat16, __nv_bfloat16, NC>);
+    return launch(ln_modulate_kernel<float, float, NC>);
   };
+  cudaError_t e;
   if (chunks <= 4)
-    go(std::integral_constant<int, 4>());
+    e = go(std::integral_constant<int, 4>());
   else if (chunks <= 8)
-    go(std::integral_constant<int, 8>());
+    e = go(std::integral_constant<int, 8>());
   else if (chunks <= 12)
-    go(std::integral_constant<int, 12>());
+    e = go(std::integral_constant<int, 12>());
   else if (chunks <= kLnMaxChunks)
-    go(std::integral_constant<int, kLnMaxChunks>());
+    e = go(std::integral_constant<int, kLnMaxChunks>());
   else
-    go(std::integral_constant<int, 0>());
+    e = go(std::integral_constant<int, 0>());
+  if (e != cudaSuccess) return e;
   count_launch();
   return cudaGetLastError();
 }
@@ -507,6 +593,23 @@ cudaError_t launch_transpose_v(const __nv_bfloat16* v, int bh, int seq, int seq_
                                __nv_bfloat16* vt, cudaStream_t stream) {
   const dim3 grid((seq + 31) / 32, 4, bh), block(32, 8);
   transpose_v_kernel<<<grid, block, 0, stream>>>(v, seq, seq_pad, vt);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(int act, const float* partials, int splits, int M, int N,
+                                 const void* bias, void* out, int unpatchify_rows,
+                                 cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(M) * N / 8;
+  if (total == 0) return cudaSuccess;
+  const int grid = blocks_for(total, 256, num_sms() * 8);
+  if (act == 1)
+    splitk_reduce_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+        partials, splits, M, N, static_cast<const __nv_bfloat16*>(bias), out, unpatchify_rows);
+  else
+    splitk_reduce_kernel<float><<<grid, 256, 0, stream>>>(partials, splits, M, N,
+                                                          static_cast<const float*>(bias), out,
+                                                          unpatchify_rows);
   count_launch();
   return cudaGetLastError();
 }

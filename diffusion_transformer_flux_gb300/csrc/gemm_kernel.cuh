@@ -170,6 +170,10 @@ __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, 
       float v[32];
       tmem_load_f32(taddr + c * 32, v);
       if (!row_ok) continue;
+      if constexpr (EPI == kEpiPartial) {
+        store32(reinterpret_cast<float*>(ep.out) + static_cast<size_t>(m) * N + n, v);
+        continue;
+      }
       if (ep.bias) {
         float bb[32];
         load32(reinterpret_cast<const T*>(ep.bias) + n, bb);
@@ -219,7 +223,7 @@ template <int KIND, int BN, int EPI>
 __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_b0,
                    const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b1,
-                   int M0, int M1, int N, int K, const __grid_constant__ EpiArgs ep0,
+                   int M0, int M1, int N, int K, int splits, const __grid_constant__ EpiArgs ep0,
                    const __grid_constant__ EpiArgs ep1, uint32_t* status) {
   using Cfg = GemmCfg<BN>;
   using T = typename KindTraits<KIND>::T;
@@ -240,19 +244,28 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_kb = (K + kBK - 1) / kBK;
   // Two problems of equal N and K share the launch (e.g. the image and text streams); the tile
   // list holds problem 0's tiles, M fastest, then problem 1's.
   const int num_n = (N + BN - 1) / BN;
   const int num_m0 = (M0 + kBM - 1) / kBM, num_m1 = (M1 + kBM - 1) / kBM;
   const int tiles0 = num_m0 * num_n;
-  const int num_tiles = tiles0 + num_m1 * num_n;
-  auto decode = [&](int tile, int& prob, int& mb, int& nb) {
+  const int tiles = tiles0 + num_m1 * num_n;
+  // split-K: work item w covers tile w % tiles over the split's range of K slices
+  const int num_tiles = tiles * splits;
+  const int kb_per_split = (num_kb + splits - 1) / splits;
+  auto decode = [&](int item, int& prob, int& mb, int& nb) {
+    const int tile = item % tiles;
     prob = tile >= tiles0;
     const int t = prob ? tile - tiles0 : tile;
     const int nm = prob ? num_m1 : num_m0;
     mb = t % nm, nb = t / nm;
   };
-  const int num_kb = (K + kBK - 1) / kBK;
+  auto k_range = [&](int item, int& kb0, int& kb1) {
+    const int split = item / tiles;
+    kb0 = split * kb_per_split;
+    kb1 = kb0 + kb_per_split < num_kb ? kb0 + kb_per_split : num_kb;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) mbar_init(&full[s], 1), mbar_init(&empty[s], 1);
@@ -286,7 +299,9 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
         decode(tile, prob, mb, nb);
         const CUtensorMap* ma = prob ? &tm_a1 : &tm_a0;
         const CUtensorMap* mw = prob ? &tm_b1 : &tm_b0;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        int kb0, kb1;
+        k_range(tile, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, status, kErrGemmWait)) {
             ok = false;
             break;
@@ -317,7 +332,9 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, status, kErrGemmWait)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        int kb0, kb1;
+        k_range(tile, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, status, kErrGemmWait)) {
             ok = false;
             break;
@@ -328,7 +345,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
 #pragma unroll
           for (int k = 0; k < kKSteps; ++k)
             tc_mma<KIND>(d_tmem, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32),
-                         kIdesc, (kb | k) != 0 ? 1u : 0u);
+                         kIdesc, (kb != kb0 || k != 0) ? 1u : 0u);
           tc_commit(&empty[stage]);
           if (++stage == Cfg::kStages) stage = 0, phase ^= 1;
         }
@@ -361,7 +378,10 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
           tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
       // a private copy, so the epilogue's arguments live in registers rather than being
       // re-read from parameter space around every store
-      const EpiArgs ep = prob ? ep1 : ep0;
+      EpiArgs ep = prob ? ep1 : ep0;
+      if constexpr (EPI == kEpiPartial)
+        ep.out = reinterpret_cast<float*>(ep.out) +
+                 static_cast<size_t>(tile / tiles) * static_cast<size_t>(prob ? M1 : M0) * N;
       gemm_epilogue<T, BN, EPI>(group, taddr, mb * kBM + row, nb * BN, prob ? M1 : M0, N, ep);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
@@ -408,11 +428,12 @@ cudaError_t run_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream
     configured_device = dev;
   }
   const int num_n = (p.N + BN - 1) / BN;
-  const int tiles = ((p.M + kBM - 1) / kBM + (two ? (p.M1 + kBM - 1) / kBM : 0)) * num_n;
+  const int splits = EPI == kEpiPartial ? (p.splits > 1 ? p.splits : 1) : 1;
+  const int tiles = ((p.M + kBM - 1) / kBM + (two ? (p.M1 + kBM - 1) / kBM : 0)) * num_n * splits;
   if (tiles == 0) return cudaSuccess;
   const int grid = tiles < num_sms() ? tiles : num_sms();
   kern<<<grid, gemm_threads<EPI>(), Cfg::kSmemBytes, stream>>>(ta0, tb0, ta1, tb1, p.M, two ? p.M1 : 0, p.N,
-                                                        p.K, p.ep, two ? p.ep1 : p.ep, status);
+                                                        p.K, splits, p.ep, two ? p.ep1 : p.ep, status);
   count_launch();
   return cudaGetLastError();
 }
@@ -426,6 +447,7 @@ cudaError_t dispatch_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t s
     case kEpiGelu: return run_gemm<KIND, BN, kEpiGelu>(p, status, stream);          \
     case kEpiGateResid: return run_gemm<KIND, BN, kEpiGateResid>(p, status, stream); \
     case kEpiUnpatchify: return run_gemm<KIND, BN, kEpiUnpatchify>(p, status, stream); \
+    case kEpiPartial: return run_gemm<KIND, BN, kEpiPartial>(p, status, stream);       \
     default: return cudaErrorInvalidValue;                                          \
   }
   if (p.epi == kEpiQkv) {

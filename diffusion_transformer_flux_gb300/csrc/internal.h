@@ -15,7 +15,8 @@ enum EpiKind : int {
   kEpiGelu = 1,       // out[m, n] = GELU(acc + bias[n])
   kEpiGateResid = 2,  // out[m, n] = resid[m, n] + gate[b(m), n] * (acc + bias[n])
   kEpiQkv = 3,        // bias, per-head RMSNorm of q and k, RoPE, scatter to Q, K, Vt
-  kEpiUnpatchify = 4  // pred[b, n, s] (fp32) = acc + bias[n], m = b * rows_per_batch + s
+  kEpiUnpatchify = 4, // pred[b, n, s] (fp32) = acc + bias[n], m = b * rows_per_batch + s
+  kEpiPartial = 5     // split-K: partial[split][m][n] (fp32) = acc over the split's K range
 };
 
 struct EpiArgs {
@@ -52,6 +53,7 @@ struct GemmProblem {
   const void* A = nullptr;  // [M, K]
   const void* W = nullptr;  // [N, K]
   EpiArgs ep;
+  int splits = 1;  // K split into this many ranges (kEpiPartial only), one work item each
   // optional second problem with the same N, K and epilogue kind, run in the same launch
   int M1 = 0;
   const void* A1 = nullptr;  // [M1, K]
@@ -135,6 +137,11 @@ cudaError_t launch_patchify(int act, const float* z, int batch, int channels, in
 // v [B, H, S, 128] -> vt [B, H, 128, seq_pad]
 cudaError_t launch_transpose_v(const __nv_bfloat16* v, int bh, int seq, int seq_pad,
                                __nv_bfloat16* vt, cudaStream_t stream);
+// Split-K finish: out[m, n] = sum_s partials[s][m][n] + bias[n] in the activation type, or, when
+// unpatchify_rows > 0, pred[b, n, r] (fp32) with m = b * unpatchify_rows + r.
+cudaError_t launch_splitk_reduce(int act, const float* partials, int splits, int M, int N,
+                                 const void* bias, void* out, int unpatchify_rows,
+                                 cudaStream_t stream);
 // Rectified-flow noise and loss.
 int flow_partial_blocks(int64_t n_total);
 cudaError_t launch_flow_match(int dtype, const void* z0, const void* z1, const float* t, int batch,

@@ -177,8 +177,9 @@ mmdit_status flow_match_noise_and_loss_noalloc(int32_t dtype, const void *z0, co
  * Plain linear layer y = x W^T + b on the tensor cores (the text embedding txt_in of [ARCH]
  * §Model components, 1. Input embeddings, and any other projection).
  *   x [M, K], w [N, K], b [N] (may be NULL), y [M, N]; element type `act`.
- *   N multiple of 32, K multiple of 8.  workspace >= mmdit_linear_workspace_size(). */
-size_t mmdit_linear_workspace_size(void);
+ *   N multiple of 32, K multiple of 8.  workspace >= mmdit_linear_workspace_size(act, M, N, K)
+ *   (a narrow output with a long K is split along K; the fp32 partial sums live there). */
+size_t mmdit_linear_workspace_size(int32_t act, int32_t M, int32_t N, int32_t K);
 mmdit_status mmdit_linear_fwd(int32_t act, int32_t M, int32_t N, int32_t K, const void *x,
                               const void *w, const void *b, void *y, void *workspace,
                               size_t workspace_bytes, void *stream);

@@ -63,7 +63,8 @@ def test_workspace_sizes(lib):
     so = L.mmdit_block_workspace_offsets(d, True)
     assert so[1] == -1 and so[6] == -1 and so[8] == -1
     assert L.flow_match_workspace_size(4, 64 * 32 * 32) >= 256 + 4
-    assert lib.mmdit_linear_workspace_size() == 256
+    assert lib.mmdit_linear_workspace_size(1, 4096, 3072, 3072) == 256  # wide: no split
+    assert lib.mmdit_linear_workspace_size(1, 512, 3072, 4096) > 512 * 3072 * 4  # narrow: split K
 
 
 def test_validation_errors_before_any_launch(lib):

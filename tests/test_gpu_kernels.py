@@ -149,9 +149,10 @@ def test_img_in_matches_oracle(act):
 
 
 @pytest.mark.parametrize("act", ["bf16", "f32"])
-def test_final_layer_matches_oracle(act):
+@pytest.mark.parametrize("B,Hh,Ww,D", [(2, 10, 12, 256), (1, 32, 32, 1024)])  # the second splits K
+def test_final_layer_matches_oracle(act, B, Hh, Ww, D):
     rng = np.random.default_rng(9)
-    B, Hh, Ww, D, Cc = 2, 10, 12, 256, 64
+    Cc = 64
     cast = "bf16" if act == "bf16" else "f32"
     rnd = synth.bf16_round if act == "bf16" else (lambda a: a)
     x = rnd(rng.standard_normal((B, Hh * Ww, D)).astype(np.float32))
