@@ -227,6 +227,8 @@ static mmdit_status check_dims(const mmdit_dims* d) {
   if (d->gemm != MMDIT_GEMM_NATIVE) return fail(MMDIT_ERR_INVALID_ARG, "unknown gemm mode %d", d->gemm);
   if (d->head_dim != 128)
     return fail(MMDIT_ERR_UNSUPPORTED, "head_dim must be 128 (got %d)", d->head_dim);
+  if (d->hidden > 6144)
+    return fail(MMDIT_ERR_UNSUPPORTED, "hidden must be at most 6144 (got %d)", d->hidden);
   if (d->heads < 1 || d->heads * d->head_dim != d->hidden)
     return fail(MMDIT_ERR_INVALID_ARG, "heads * head_dim (%d * %d) != hidden (%d)", d->heads,
                 d->head_dim, d->hidden);

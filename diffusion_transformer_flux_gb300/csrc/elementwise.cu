@@ -98,9 +98,10 @@ struct Raw8<float> {
   }
 };
 
-template <typename T, int NC>
+template <typename T, int NC, int NB>
 __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __restrict__ vec, ModJob j0,
-                                                                 ModJob j1, int batch, int dim) {
+                                                                 ModJob j1, int dim) {
+  constexpr int batch = NB;  // batch rows handled by this launch (compile time: no idle lanes)
   extern __shared__ float svec[];  // [batch, dim] SiLU(vec), a bf16 operand in bf16 mode
   for (int i = threadIdx.x; i < batch * dim; i += blockDim.x) {
     const float v = to_f32(vec[i]);
@@ -126,9 +127,9 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __rest
       const int k = c * 256 + lane * 8;
       if (k < dim) raw[c].load(wr + k);
     }
-    float acc[kModMaxBatch];
+    float acc[NB];
 #pragma unroll
-    for (int b = 0; b < kModMaxBatch; ++b) acc[b] = 0.f;
+    for (int b = 0; b < NB; ++b) acc[b] = 0.f;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       const int k = c * 256 + lane * 8;
@@ -136,33 +137,30 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __rest
         float wv[8];
         raw[c].to_f32(wv);
 #pragma unroll
-        for (int b = 0; b < kModMaxBatch; ++b) {
-          if (b < batch) {
-            const float4 s0 = *reinterpret_cast<const float4*>(svec + b * dim + k);
-            const float4 s1 = *reinterpret_cast<const float4*>(svec + b * dim + k + 4);
-            acc[b] += wv[0] * s0.x + wv[1] * s0.y + wv[2] * s0.z + wv[3] * s0.w + wv[4] * s1.x +
-                      wv[5] * s1.y + wv[6] * s1.z + wv[7] * s1.w;
-          }
+        for (int b = 0; b < NB; ++b) {
+          const float4 s0 = *reinterpret_cast<const float4*>(svec + b * dim + k);
+          const float4 s1 = *reinterpret_cast<const float4*>(svec + b * dim + k + 4);
+          acc[b] += wv[0] * s0.x + wv[1] * s0.y + wv[2] * s0.z + wv[3] * s0.w + wv[4] * s1.x +
+                    wv[5] * s1.y + wv[6] * s1.z + wv[7] * s1.w;
         }
       }
     }
     const float bb = job.bias ? to_f32(reinterpret_cast<const T*>(job.bias)[r]) : 0.f;
 #pragma unroll
-    for (int b = 0; b < kModMaxBatch; ++b) {
-      if (b < batch) {
-        const float sum = warp_sum(acc[b]);
-        if (lane == 0) job.m[static_cast<size_t>(b) * job.rows + r] = sum + bb;
-      }
+    for (int b = 0; b < NB; ++b) {
+      const float sum = warp_sum(acc[b]);
+      if (lane == 0) job.m[static_cast<size_t>(b) * job.rows + r] = sum + bb;
     }
   }
 }
 
 // ----------------------------------------------------------------------------- LN + modulate
-// One warp per row: mean, biased variance, then out = (x - mean) * rsqrt(var + eps) * (1 + scale[b])
-// + shift[b].  Rows of up to kLnMaxChunks * 256 elements are held in registers (one load round
-// trip, exact two-pass statistics); longer rows stream through L1 in three passes.  Up to two
-// row sets (the image and text streams) share a launch.
-constexpr int kLnMaxChunks = 16;
+// One 128-thread block per row: each thread holds NCT chunks of 8 consecutive elements (one
+// load round trip), the mean and the biased variance are exact two-pass block reductions over
+// the register-resident row, then out = (x - mean) * rsqrt(var + eps) * (1 + scale[b]) + shift[b].
+// Up to two row sets (the image and text streams) share a launch.
+constexpr int kLnThreads = 128;
+constexpr int kLnMaxChunks = 8;  // rows of up to 128 * 8 * 8 = 8192 elements
 
 struct LnJob {
   const void* x;
@@ -174,124 +172,70 @@ struct LnJob {
   int rpb;
 };
 
-template <typename TI, typename T, int NC>
-__device__ __forceinline__ void ln_row_regs(const TI* xr, const float* sh, const float* sc, T* orow,
-                                            int dim, float eps, int lane) {
-  Raw8<TI> raw[NC];
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();  // red[] may still be read by the previous reduction
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
 #pragma unroll
-  for (int c = 0; c < NC; ++c) {
-    const int k = c * 256 + lane * 8;
+  for (int w = 0; w < kLnThreads / 32; ++w) t += red[w];
+  return t;
+}
+
+template <typename TI, typename T, int NCT>
+__global__ void __launch_bounds__(kLnThreads) ln_modulate_kernel(LnJob j0, LnJob j1, int dim, float eps) {
+  __shared__ float red[kLnThreads / 32];
+  const int g = blockIdx.x;
+  const bool second = g >= j0.rows;
+  const LnJob& job = second ? j1 : j0;
+  const int r = second ? g - j0.rows : g;
+  const TI* xr = static_cast<const TI*>(job.x) + static_cast<size_t>(r) * dim;
+  Raw8<TI> raw[NCT];
+#pragma unroll
+  for (int c = 0; c < NCT; ++c) {
+    const int k = (c * kLnThreads + threadIdx.x) * 8;
     if (k < dim) raw[c].load(xr + k);
   }
   float s = 0.f;
 #pragma unroll
-  for (int c = 0; c < NC; ++c) {
-    if (c * 256 + lane * 8 < dim) {
+  for (int c = 0; c < NCT; ++c) {
+    if ((c * kLnThreads + threadIdx.x) * 8 < dim) {
       float v[8];
       raw[c].to_f32(v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) s += v[e];
     }
   }
-  const float mean = warp_sum(s) / dim;
+  const float mean = block_sum(s, red) / dim;
   float q = 0.f;
 #pragma unroll
-  for (int c = 0; c < NC; ++c) {
-    if (c * 256 + lane * 8 < dim) {
+  for (int c = 0; c < NCT; ++c) {
+    if ((c * kLnThreads + threadIdx.x) * 8 < dim) {
       float v[8];
       raw[c].to_f32(v);
 #pragma unroll
       for (int e = 0; e < 8; ++e) q = fmaf(v[e] - mean, v[e] - mean, q);
     }
   }
-  const float rstd = rsqrtf(warp_sum(q) / dim + eps);
+  const float rstd = rsqrtf(block_sum(q, red) / dim + eps);
+  const int b = r / job.rpb;
+  const float* sh = job.shift + b * job.mod_bstride;
+  const float* sc = job.scale + b * job.mod_bstride;
+  T* orow = static_cast<T*>(job.out) + static_cast<size_t>(r) * dim;
 #pragma unroll
-  for (int c = 0; c < NC; ++c) {
-    const int k = c * 256 + lane * 8;
+  for (int c = 0; c < NCT; ++c) {
+    const int k = (c * kLnThreads + threadIdx.x) * 8;
     if (k < dim) {
-      float v[8], a[8], b[8];
+      float v[8], a[8], m[8];
       raw[c].to_f32(v);
       load8(sh + k, a);
-      load8(sc + k, b);
+      load8(sc + k, m);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) v[e] = fmaf((v[e] - mean) * rstd, 1.f + b[e], a[e]);
+      for (int e = 0; e < 8; ++e) v[e] = fmaf((v[e] - mean) * rstd, 1.f + m[e], a[e]);
       store8(orow + k, v);
     }
-  }
-}
-
-template <typename TI, typename T>
-__device__ __forceinline__ void ln_row_stream(const TI* xr, const float* sh, const float* sc, T* orow,
-                                              int dim, float eps, int lane) {
-  float s = 0.f;
-  for (int k = lane * 8; k < dim; k += 256) {
-    float v[8];
-    load8(xr + k, v);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) s += v[e];
-  }
-  const float mean = warp_sum(s) / dim;
-  float q = 0.f;
-  for (int k = lane * 8; k < dim; k += 256) {
-    float v[8];
-    load8(xr + k, v);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) q = fmaf(v[e] - mean, v[e] - mean, q);
-  }
-  const float rstd = rsqrtf(warp_sum(q) / dim + eps);
-  for (int k = lane * 8; k < dim; k += 256) {
-    float v[8], a[8], c[8];
-    load8(xr + k, v);
-    load8(sh + k, a);
-    load8(sc + k, c);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = fmaf((v[e] - mean) * rstd, 1.f + c[e], a[e]);
-    store8(orow + k, v);
-  }
-}
-
-template <typename TI, typename T, int NC>
-__global__ void __launch_bounds__(256) ln_modulate_kernel(LnJob j0, LnJob j1, int dim, float eps,
-                                                          int stage_mod) {
-  // shift/scale of one (job, batch element) staged in shared memory when the row width allows;
-  // rows of another batch element read them from global memory
-  extern __shared__ float smod[];  // [2, dim]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int warps = blockDim.x >> 5;
-  const int total = j0.rows + j1.rows;
-  int staged_key = -1;
-  for (int base = blockIdx.x * warps; base < total; base += gridDim.x * warps) {
-    const int g = base + warp;
-    // the block stages the (job, batch) of its first row of this round
-    if (stage_mod) {
-      const bool s2 = base >= j0.rows;
-      const LnJob& sj = s2 ? j1 : j0;
-      const int sb = (s2 ? base - j0.rows : base) / sj.rpb;
-      const int key = (s2 ? 1 << 30 : 0) + sb;
-      if (key != staged_key) {
-        __syncthreads();
-        for (int i = threadIdx.x; i < dim; i += blockDim.x) {
-          smod[i] = sj.shift[sb * sj.mod_bstride + i];
-          smod[dim + i] = sj.scale[sb * sj.mod_bstride + i];
-        }
-        __syncthreads();
-        staged_key = key;
-      }
-    }
-    if (g >= total) continue;
-    const bool second = g >= j0.rows;
-    const LnJob& job = second ? j1 : j0;
-    const int r = second ? g - j0.rows : g;
-    const TI* xr = static_cast<const TI*>(job.x) + static_cast<size_t>(r) * dim;
-    const int b = r / job.rpb;
-    const bool from_smem = stage_mod && ((second ? 1 << 30 : 0) + b) == staged_key;
-    const float* sh = from_smem ? smod : job.shift + b * job.mod_bstride;
-    const float* sc = from_smem ? smod + dim : job.scale + b * job.mod_bstride;
-    T* orow = static_cast<T*>(job.out) + static_cast<size_t>(r) * dim;
-    if constexpr (NC > 0)
-      ln_row_regs<TI, T, NC>(xr, sh, sc, orow, dim, eps, lane);
-    else
-      ln_row_stream<TI, T>(xr, sh, sc, orow, dim, eps, lane);
   }
 }
 
@@ -464,10 +408,10 @@ cudaError_t launch_rope3d(const float* ids, int batch, int seq, const int axes[3
   return cudaGetLastError();
 }
 
-template <typename T, int NC>
-cudaError_t launch_mod_nc(const void* vec, const ModJob& j0, const ModJob& j1, int nb, int dim,
-                          size_t smem, cudaStream_t stream) {
-  auto kern = modulation_kernel<T, NC>;
+template <typename T, int NC, int NB>
+cudaError_t launch_mod(const void* vec, const ModJob& j0, const ModJob& j1, int dim, size_t smem,
+                       cudaStream_t stream) {
+  auto kern = modulation_kernel<T, NC, NB>;
   static int configured = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -481,9 +425,24 @@ cudaError_t launch_mod_nc(const void* vec, const ModJob& j0, const ModJob& j1, i
   if (per_sm < 1) per_sm = 1;
   const int rows = j0.rows + j1.rows;
   const int grid = blocks_for(rows, kModThreads / 32, num_sms() * per_sm);
-  kern<<<grid, kModThreads, smem, stream>>>(static_cast<const T*>(vec), j0, j1, nb, dim);
+  kern<<<grid, kModThreads, smem, stream>>>(static_cast<const T*>(vec), j0, j1, dim);
   count_launch();
   return cudaGetLastError();
+}
+
+template <typename T, int NC>
+cudaError_t launch_mod_nb(const void* vec, const ModJob& j0, const ModJob& j1, int nb, int dim,
+                          size_t smem, cudaStream_t stream) {
+  switch (nb) {
+    case 1: return launch_mod<T, NC, 1>(vec, j0, j1, dim, smem, stream);
+    case 2: return launch_mod<T, NC, 2>(vec, j0, j1, dim, smem, stream);
+    case 3: return launch_mod<T, NC, 3>(vec, j0, j1, dim, smem, stream);
+    case 4: return launch_mod<T, NC, 4>(vec, j0, j1, dim, smem, stream);
+    case 5: return launch_mod<T, NC, 5>(vec, j0, j1, dim, smem, stream);
+    case 6: return launch_mod<T, NC, 6>(vec, j0, j1, dim, smem, stream);
+    case 7: return launch_mod<T, NC, 7>(vec, j0, j1, dim, smem, stream);
+    default: return launch_mod<T, NC, 8>(vec, j0, j1, dim, smem, stream);
+  }
 }
 
 cudaError_t launch_modulation2(int act, const void* vec, const ModulationJob* jobs, int njobs,
@@ -499,14 +458,14 @@ cudaError_t launch_modulation2(int act, const void* vec, const ModulationJob* jo
     const void* vb = static_cast<const uint8_t*>(vec) + static_cast<size_t>(b0) * dim * elt;
     cudaError_t e;
     if (act == 1) {
-      if (chunks <= 4) e = launch_mod_nc<__nv_bfloat16, 4>(vb, j[0], j[1], nb, dim, smem, stream);
-      else if (chunks <= 8) e = launch_mod_nc<__nv_bfloat16, 8>(vb, j[0], j[1], nb, dim, smem, stream);
-      else if (chunks <= 12) e = launch_mod_nc<__nv_bfloat16, 12>(vb, j[0], j[1], nb, dim, smem, stream);
-      else e = launch_mod_nc<__nv_bfloat16, 24>(vb, j[0], j[1], nb, dim, smem, stream);
+      if (chunks <= 4) e = launch_mod_nb<__nv_bfloat16, 4>(vb, j[0], j[1], nb, dim, smem, stream);
+      else if (chunks <= 8) e = launch_mod_nb<__nv_bfloat16, 8>(vb, j[0], j[1], nb, dim, smem, stream);
+      else if (chunks <= 12) e = launch_mod_nb<__nv_bfloat16, 12>(vb, j[0], j[1], nb, dim, smem, stream);
+      else e = launch_mod_nb<__nv_bfloat16, 24>(vb, j[0], j[1], nb, dim, smem, stream);
     } else {
-      if (chunks <= 4) e = launch_mod_nc<float, 4>(vb, j[0], j[1], nb, dim, smem, stream);
-      else if (chunks <= 8) e = launch_mod_nc<float, 8>(vb, j[0], j[1], nb, dim, smem, stream);
-      else e = launch_mod_nc<float, 16>(vb, j[0], j[1], nb, dim, smem, stream);
+      if (chunks <= 4) e = launch_mod_nb<float, 4>(vb, j[0], j[1], nb, dim, smem, stream);
+      else if (chunks <= 8) e = launch_mod_nb<float, 8>(vb, j[0], j[1], nb, dim, smem, stream);
+      else e = launch_mod_nb<float, 16>(vb, j[0], j[1], nb, dim, smem, stream);
     }
     if (e != cudaSuccess) return e;
   }
@@ -529,43 +488,27 @@ cudaError_t launch_ln_modulate2(int act, int x_f32, const LnModJob* jobs, int nj
     rows += jobs[i].rows;
   }
   if (rows == 0) return cudaSuccess;
-  const int chunks = (dim + 255) / 256;
-  const int stage = dim <= 8192 ? 1 : 0;
-  const size_t smem = stage ? 2 * static_cast<size_t>(dim) * sizeof(float) : 0;
-  auto go = [&](auto nc_tag) -> cudaError_t {
-    constexpr int NC = decltype(nc_tag)::value;
-    auto launch = [&](auto kern) -> cudaError_t {
-      static int configured = -1;
-      int dev = 0;
-      cudaGetDevice(&dev);
-      if (configured != dev) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-        if (e != cudaSuccess) return e;
-        configured = dev;
-      }
-      int per_sm = 0;
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem);
-      if (per_sm < 1) per_sm = 1;
-      const int grid = blocks_for(rows, 8, num_sms() * per_sm);
-      kern<<<grid, 256, smem, stream>>>(j[0], j[1], dim, eps, stage);
-      return cudaSuccess;
-    };
-    if (act == 1 && x_f32) return launch(ln_modulate_kernel<float, __nv_bfloat16, NC>);
-    if (act == 1) return launch(ln_modulate_kernel<__nv_bfloat16, __nv_bfloat16, NC>);
-    return launch(ln_modulate_kernel<float, float, NC>);
+  const int chunks = (dim + kLnThreads * 8 - 1) / (kLnThreads * 8);
+  if (chunks > kLnMaxChunks) return cudaErrorInvalidValue;
+  auto go = [&](auto nct_tag) {
+    constexpr int NCT = decltype(nct_tag)::value;
+    if (act == 1 && x_f32)
+      ln_modulate_kernel<float, __nv_bfloat16, NCT><<<rows, kLnThreads, 0, stream>>>(j[0], j[1], dim, eps);
+    else if (act == 1)
+      ln_modulate_kernel<__nv_bfloat16, __nv_bfloat16, NCT><<<rows, kLnThreads, 0, stream>>>(j[0], j[1], dim, eps);
+    else
+      ln_modulate_kernel<float, float, NCT><<<rows, kLnThreads, 0, stream>>>(j[0], j[1], dim, eps);
   };
-  cudaError_t e;
-  if (chunks <= 4)
-    e = go(std::integral_constant<int, 4>());
-  else if (chunks <= 8)
-    e = go(std::integral_constant<int, 8>());
-  else if (chunks <= 12)
-    e = go(std::integral_constant<int, 12>());
-  else if (chunks <= kLnMaxChunks)
-    e = go(std::integral_constant<int, kLnMaxChunks>());
+  if (chunks <= 1)
+    go(std::integral_constant<int, 1>());
+  else if (chunks <= 2)
+    go(std::integral_constant<int, 2>());
+  else if (chunks <= 3)
+    go(std::integral_constant<int, 3>());
+  else if (chunks <= 4)
+    go(std::integral_constant<int, 4>());
   else
-    e = go(std::integral_constant<int, 0>());
-  if (e != cudaSuccess) return e;
+    go(std::integral_constant<int, kLnMaxChunks>());
   count_launch();
   return cudaGetLastError();
 }

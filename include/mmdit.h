@@ -69,10 +69,10 @@ typedef struct mmdit_dims {
   int32_t batch;      /* B */
   int32_t seq_img;    /* image tokens S_i */
   int32_t seq_txt;    /* text tokens S_t; the joint sequence is [image; text], S = S_i + S_t */
-  int32_t hidden;     /* D = heads * head_dim; multiple of 256 */
+  int32_t hidden;     /* D = heads * head_dim; multiple of 128, at most 6144 */
   int32_t heads;      /* H */
   int32_t head_dim;   /* d; must be 128 */
-  int32_t mlp_hidden; /* F; multiple of 256 */
+  int32_t mlp_hidden; /* F; multiple of 64 */
   float ln_eps;       /* LayerNorm eps (1e-6, [API] §Configuration layernorm_epsilon) */
   float rms_eps;      /* QK-RMSNorm eps (1e-6) */
   int32_t rope_interleaved; /* 1: pairs (2j, 2j+1) ([API] rotary_interleaved); 0: (j, j+d/2) */
