@@ -33,8 +33,8 @@ design notes of the repository as well):
   * Precision: by default every step runs in float64.  ``mm_cast=round_bf16`` evaluates the
     method at the precision the pages fix for training, bf16 autocast (architecture page,
     §Performance optimizations › 5. Mixed precision; API page, §Optimization tips): the
-    operands of every matrix product (each linear layer and both attention products) are
-    rounded to bf16; everything else stays float64.
+    operands of every linear layer and the attention's inputs q, k, v are rounded to bf16;
+    everything else (including the softmax weights inside the fused attention) stays float64.
 """
 from __future__ import annotations
 
@@ -186,7 +186,10 @@ def attention(q, k, v, mm_cast=None):
 
     Architecture page, §Implementation details › Attention implementation
     (no mask) and › Joint Attention Trick (one call over the joint sequence).
-    ``mm_cast`` rounds the operands of both products (q, k; the probabilities and v).
+    ``mm_cast`` rounds the attention's inputs q, k, v.  The softmax weights are kept
+    exact: the pages run attention as one fused kernel (architecture page, §Performance
+    optimizations › 2. Flash attention), whose inputs are the autocast operands; its
+    internal probabilities are not.
     """
     q, k, v = _cast(q, mm_cast), _cast(k, mm_cast), _cast(v, mm_cast)
     d = q.shape[-1]
@@ -194,7 +197,7 @@ def attention(q, k, v, mm_cast=None):
     s = s - s.max(axis=-1, keepdims=True)
     p = np.exp(s)
     p = p / p.sum(axis=-1, keepdims=True)
-    return _cast(p, mm_cast) @ v
+    return p @ v
 
 
 # ----------------------------------------------------------------------------- block pieces

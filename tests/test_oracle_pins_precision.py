@@ -45,14 +45,18 @@ def test_cast_mode_is_exact_on_grid_operands():
 
 
 def test_cast_mode_attention_closed_forms():
-    v = RNG.standard_normal((8, 16))
-    k = RNG.standard_normal((8, 4))
-    # q = 0 over 8 keys: every probability is 1/8, exact in bf16 -> mean of the rounded values
+    v = RNG.standard_normal((7, 16))
+    k = RNG.standard_normal((7, 4))
+    # q = 0: uniform weights (kept exact) -> mean of the rounded values, for any key count
     out = O.attention(np.zeros((2, 4)), k, v, O.round_bf16)
-    np.testing.assert_allclose(out, np.repeat(O.round_bf16(v).mean(0, keepdims=True), 2, 0), rtol=1e-15)
-    # a single key: probability 1 -> the rounded value exactly
+    np.testing.assert_allclose(out, np.repeat(O.round_bf16(v).mean(0, keepdims=True), 2, 0), rtol=1e-14)
+    # a single key: weight 1 -> the rounded value exactly
     out = O.attention(RNG.standard_normal((3, 4)), k[:1], v[:1], O.round_bf16)
     np.testing.assert_array_equal(out, np.repeat(O.round_bf16(v[:1]), 3, 0))
+    # the cast mode is the exact attention of the rounded inputs
+    q = RNG.standard_normal((5, 4))
+    np.testing.assert_allclose(O.attention(q, k, v, O.round_bf16),
+                               O.attention(O.round_bf16(q), O.round_bf16(k), O.round_bf16(v)), rtol=1e-15)
 
 
 def test_cast_mode_block_stays_close_to_exact_block():
