@@ -339,7 +339,7 @@ mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss,
     e.bias = w->b_qkv, e.g_q = w->g_q, e.g_k = w->g_k;
     e.rope_cos = cs, e.rope_sin = sn;
     e.q = at<__nv_bfloat16>(ws, p.q), e.k = at<__nv_bfloat16>(ws, p.k);
-    e.vt = at<__nv_bfloat16>(ws, p.vt);
+    e.vt = at<__half>(ws, p.vt);
     e.rows_per_batch = ss.rpb[i];
     e.seq_offset = ss.s[i] == 0 ? 0 : p.Si;
     e.seq_joint = p.S, e.seq_pad = p.S_pad, e.heads = p.H, e.hidden = p.D;
@@ -407,7 +407,7 @@ mmdit_status run_attention(const BlockPlan& p, int act, void* ws, cudaStream_t s
   a.act = act, a.batch = p.B, a.heads = p.H, a.seq = p.S, a.seq_pad = p.S_pad;
   a.split = p.single ? p.S : p.Si;
   a.q = at<__nv_bfloat16>(ws, p.q), a.k = at<__nv_bfloat16>(ws, p.k);
-  a.vt = at<__nv_bfloat16>(ws, p.vt);
+  a.vt = at<__half>(ws, p.vt);
   a.out0 = at(ws, p.o[0]);
   a.out1 = p.single ? nullptr : at(ws, p.o[1]);
   { ProfScope ps_(p.single ? "single.attention" : "double.attention", st);
@@ -673,7 +673,7 @@ mmdit_status mmdit_attention_fwd(int32_t act, int32_t batch, int32_t heads, int3
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
   const int seq_pad = static_cast<int>(round_up(static_cast<size_t>(seq), 8));
-  __nv_bfloat16* vt = at<__nv_bfloat16>(workspace, kStatusBytes);
+  __half* vt = at<__half>(workspace, kStatusBytes);
   ProfScope ps_("attention", st);
   MMDIT_CUDA(launch_transpose_v(static_cast<const __nv_bfloat16*>(v), batch * heads, seq, seq_pad, vt, st),
              "V transpose");

@@ -12,13 +12,15 @@
 //                so that the tensor core works on one query tile while the other's softmax runs;
 //   warps 4..7   softmax of tile A, warps 8..11 softmax of tile B: one query row per thread (its
 //                TMEM lane).  A first pass over the scores in TMEM takes the row maximum; a second
-//                pass writes P = exp2(S * log2(e)/sqrt(d) - m) as packed bf16 back over the score
-//                columns, where the PV product reads it as its A operand straight from TMEM.  The
+//                pass writes P = exp2(S * log2(e)/sqrt(d) - m) as packed fp16 back over the score
+//                columns, where the PV product (fp16 P and V) reads it as its A operand straight
+//                from TMEM.  The
 //                running maximum is only moved (and O rescaled in TMEM) when a row's maximum grows
 //                by more than 2^8; the final division by the row sum of the rounded P makes the
 //                result exact either way.
 // TMEM columns: S/P of A [0,128), S/P of B [128,256), O of A [256,384), O of B [384,512).
-// V arrives transposed ([B, H, 128, S_pad]) so the PV product reads a K-major operand.
+// V arrives transposed ([B, H, 128, S_pad], fp16 holding the bf16 values) so the PV product
+// reads a K-major operand.
 #include "common.cuh"
 #include "internal.h"
 
@@ -34,7 +36,8 @@ constexpr int kTileBytes = 2 * kHalfTile;  // 128 rows x 128 bf16 = 32 KB
 constexpr int kSmemData = 2 * kTileBytes + kKvStages * 2 * kTileBytes;  // Q_A Q_B | K,V x2 = 192 KB
 constexpr int kAttnSmem = kSmemData + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kIdesc = make_idesc<kKindF16>(128, 128);
+constexpr uint32_t kIdesc = make_idesc<kKindF16>(128, 128);      // S = Q K^T, bf16 operands
+constexpr uint32_t kIdescPV = make_idesc_fp16(128, 128);          // O += P V, fp16 operands
 constexpr float kScaleLog2 = 0.12751743074380043f;  // log2(e) / sqrt(128)
 constexpr float kRescaleThreshold = 8.0f;           // in log2 units
 
@@ -133,10 +136,12 @@ __device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t t
           if (k + 32 >= seq) e2 = 0.f;
           if (k + 33 >= seq) e3 = 0.f;
         }
-        pk[i] = pack_bf16x2(e0, e1);
-        pk[16 + i] = pack_bf16x2(e2, e3);
+        pk[i] = pack_half2(e0, e1);
+        pk[16 + i] = pack_half2(e2, e3);
         // normalise by the sum of the rounded weights the PV product actually uses
-        sum += (bf16_lo(pk[i]) + bf16_hi(pk[i])) + (bf16_lo(pk[16 + i]) + bf16_hi(pk[16 + i]));
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pk[16 + i]));
+        sum += (f0.x + f0.y) + (f1.x + f1.y);
       }
       tmem_st32(s_cols + h * 32, pk);
     }
@@ -283,7 +288,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = static_cast<uint32_t>((k >> 2) * kHalfTile + (k & 3) * 32);
           tc_mma_ts_f16(d_o, p_cols + static_cast<uint32_t>(k * 8), sdesc_kmajor_sw128(vb + off),
-                        kIdesc, (j > 0 || k > 0) ? 1u : 0u);
+                        kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
         }
         return true;
       };
@@ -330,7 +335,7 @@ cudaError_t launch_attention(const AttnProblem& p, uint32_t* status, cudaStream_
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_tmap(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.k, dqk, sqk, box,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.vt, dv, sv, box,
+      !encode_tmap(&tv, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, p.vt, dv, sv, box,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   const dim3 grid((p.seq + 2 * kQTile - 1) / (2 * kQTile), static_cast<unsigned>(bh));

@@ -264,9 +264,9 @@ __global__ void patchify_kernel(const float* __restrict__ z, int channels, int h
   }
 }
 
-// v [BH, S, 128] -> vt [BH, 128, S_pad]
+// v [BH, S, 128] bf16 -> vt [BH, 128, S_pad] fp16
 __global__ void transpose_v_kernel(const __nv_bfloat16* __restrict__ v, int seq, int seq_pad,
-                                   __nv_bfloat16* __restrict__ vt) {
+                                   __half* __restrict__ vt) {
   __shared__ __nv_bfloat16 tile[32][34];
   const size_t bh = blockIdx.z;
   const int s0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
@@ -277,7 +277,7 @@ __global__ void transpose_v_kernel(const __nv_bfloat16* __restrict__ v, int seq,
   __syncthreads();
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int s = s0 + threadIdx.x;
-    if (s < seq) vt[(bh * 128 + j0 + i) * seq_pad + s] = tile[threadIdx.x][i];
+    if (s < seq) vt[(bh * 128 + j0 + i) * seq_pad + s] = __float2half_rn(__bfloat162float(tile[threadIdx.x][i]));
   }
 }
 
@@ -532,8 +532,8 @@ cudaError_t launch_patchify(int act, const float* z, int batch, int channels, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_transpose_v(const __nv_bfloat16* v, int bh, int seq, int seq_pad,
-                               __nv_bfloat16* vt, cudaStream_t stream) {
+cudaError_t launch_transpose_v(const __nv_bfloat16* v, int bh, int seq, int seq_pad, __half* vt,
+                               cudaStream_t stream) {
   const dim3 grid((seq + 31) / 32, 4, bh), block(32, 8);
   transpose_v_kernel<<<grid, block, 0, stream>>>(v, seq, seq_pad, vt);
   count_launch();

@@ -155,9 +155,12 @@ __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, 
           store32(dst + c * 32, t);
         }
       } else {
-        __nv_bfloat16* dst = ep.vt + bh * 128 * static_cast<size_t>(ep.seq_pad) + sj;
+        // V is a bf16 value of the attention (autocast precision); it is stored in fp16, which
+        // holds every such value exactly, because the PV product runs on fp16 operands
+        __half* dst = ep.vt + bh * 128 * static_cast<size_t>(ep.seq_pad) + sj;
 #pragma unroll
-        for (int j = 0; j < 128; ++j) dst[static_cast<size_t>(j) * ep.seq_pad] = __float2bfloat16_rn(v[j]);
+        for (int j = 0; j < 128; ++j)
+          dst[static_cast<size_t>(j) * ep.seq_pad] = __float2half_rn(__bfloat162float(__float2bfloat16_rn(v[j])));
       }
     }
   } else {

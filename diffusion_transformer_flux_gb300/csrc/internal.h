@@ -3,6 +3,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -36,7 +37,7 @@ struct EpiArgs {
   const float* rope_sin = nullptr;
   __nv_bfloat16* q = nullptr;  // [B, H, seq_joint, 128]
   __nv_bfloat16* k = nullptr;
-  __nv_bfloat16* vt = nullptr; // [B, H, 128, seq_pad]
+  __half* vt = nullptr;        // [B, H, 128, seq_pad] fp16 holding bf16-rounded values
   int seq_offset = 0;          // joint index of this stream's token 0
   int seq_joint = 0;
   int seq_pad = 0;
@@ -93,7 +94,7 @@ struct AttnProblem {
   int batch = 0, heads = 0, seq = 0, seq_pad = 0, split = 0;
   const __nv_bfloat16* q = nullptr;   // [B, H, S, 128]
   const __nv_bfloat16* k = nullptr;   // [B, H, S, 128]
-  const __nv_bfloat16* vt = nullptr;  // [B, H, 128, seq_pad]
+  const __half* vt = nullptr;         // [B, H, 128, seq_pad] fp16 (bf16-rounded values)
   void* out0 = nullptr;
   void* out1 = nullptr;
 };
@@ -134,9 +135,9 @@ cudaError_t launch_ln_modulate2(int act, int x_f32, const LnModJob* jobs, int nj
 // z [B, C, HW] fp32 -> tokens [B, HW, C] of the activation type.
 cudaError_t launch_patchify(int act, const float* z, int batch, int channels, int hw, void* out,
                             cudaStream_t stream);
-// v [B, H, S, 128] -> vt [B, H, 128, seq_pad]
-cudaError_t launch_transpose_v(const __nv_bfloat16* v, int bh, int seq, int seq_pad,
-                               __nv_bfloat16* vt, cudaStream_t stream);
+// v [B, H, S, 128] bf16 -> vt [B, H, 128, seq_pad] fp16 (exact: bf16 values fit fp16 here)
+cudaError_t launch_transpose_v(const __nv_bfloat16* v, int bh, int seq, int seq_pad, __half* vt,
+                               cudaStream_t stream);
 // Split-K finish: out[m, n] = sum_s partials[s][m][n] + bias[n] in the activation type, or, when
 // unpatchify_rows > 0, pred[b, n, r] (fp32) with m = b * unpatchify_rows + r.
 cudaError_t launch_splitk_reduce(int act, const float* partials, int splits, int M, int N,

@@ -252,7 +252,7 @@ mmdit_status mmdit_single_block_fwd(const mmdit_dims *dims, const mmdit_stream_w
 /* Byte offsets of named intermediates inside a block workspace, for inspection by tests:
  * out[0..9] = mod_img, mod_txt, Q, K, Vt, O_img, O_txt, x1_img, x1_txt, u_img (a single block
  * uses the *_img slots; unused slots are -1).  Q, K are [B, H, S, d] bf16, Vt is [B, H, d,
- * S_pad] bf16 with S_pad = S rounded up to 8.  Returns the count written or -1 on bad dims. */
+ * S_pad] fp16 (holding bf16-rounded values) with S_pad = S rounded up to 8.  Returns the count written or -1 on bad dims. */
 int32_t mmdit_block_workspace_offsets(const mmdit_dims *dims, int32_t single, int64_t *out,
                                       int32_t n);
 
