@@ -80,19 +80,26 @@ __device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t t
     tc_fence_after();
     const int kv0 = j * kKvTile;
     const bool tail = kv0 + kKvTile > seq;
-    // pass 1: the row maximum of the valid keys (two TMEM round trips of 64 columns)
-    float mx = -INFINITY;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t ra[32], rb[32];
-      tmem_ld64_wait(s_cols + h * 64, ra, rb);
+    // the 128 scores of this row: one TMEM round trip (four loads, one wait)
+    uint32_t r0[32], r1[32], r2[32], r3[32];
+    tmem_ld32(s_cols, r0);
+    tmem_ld32(s_cols + 32, r1);
+    tmem_ld64_wait(s_cols + 64, r2, r3);
+    tmem_ld_deps64(r0, r1);
+    if (tail) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float va = (tail && kv0 + h * 64 + i >= seq) ? -INFINITY : __uint_as_float(ra[i]);
-        const float vb = (tail && kv0 + h * 64 + 32 + i >= seq) ? -INFINITY : __uint_as_float(rb[i]);
-        mx = fmaxf(mx, fmaxf(va, vb));
+        if (kv0 + i >= seq) r0[i] = __float_as_uint(-INFINITY);
+        if (kv0 + 32 + i >= seq) r1[i] = __float_as_uint(-INFINITY);
+        if (kv0 + 64 + i >= seq) r2[i] = __float_as_uint(-INFINITY);
+        if (kv0 + 96 + i >= seq) r3[i] = __float_as_uint(-INFINITY);
       }
     }
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(r0[i]), __uint_as_float(r1[i])),
+                           fmaxf(__uint_as_float(r2[i]), __uint_as_float(r3[i]))));
     mx *= kScaleLog2;
     float alpha = 1.f;
     bool rescale = false;
@@ -103,7 +110,29 @@ __device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t t
       m_run = mx;
       rescale = true;
     }
-    // O holds sum_{t<j} P_t V_t: PV(j-1) was issued before S(j), whose completion we saw.
+    // P = exp2(s * scale - m) as fp16 pairs over the score columns (keys 2k, 2k+1 in column k),
+    // 16 columns per store so each chunk of scores dies as soon as it is used; masked keys
+    // hold -inf and give 0
+    float sum = 0.f;
+    auto emit = [&](const uint32_t (&sc)[32], uint32_t col) {
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float e0 = fast_exp2(fmaf(__uint_as_float(sc[2 * i]), kScaleLog2, -m_run));
+        const float e1 = fast_exp2(fmaf(__uint_as_float(sc[2 * i + 1]), kScaleLog2, -m_run));
+        pk[i] = pack_half2(e0, e1);
+        // normalise by the sum of the rounded weights the PV product actually uses
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
+        sum += f.x + f.y;
+      }
+      tmem_st16(s_cols + col, pk);
+    };
+    emit(r0, 0);   // keys [0, 32)   -> columns [0, 16)
+    emit(r1, 16);  // keys [32, 64)  -> columns [16, 32)
+    emit(r2, 32);  // keys [64, 96)  -> columns [32, 48)
+    emit(r3, 48);  // keys [96, 128) -> columns [48, 64)
+    // O holds sum_{t<j} P_t V_t (PV(j-1) was issued before S(j), whose completion we saw);
+    // rescaled after the scores are consumed, so the two never hold registers together
     if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -113,37 +142,6 @@ __device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t t
         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
         tmem_st32(o_cols + c * 32, r);
       }
-    }
-    // pass 2: P = exp2(s * scale - m) as bf16 pairs over the score columns (keys 2k, 2k+1 in
-    // column k); the packed columns of keys [64h, 64h+64) land in columns [32h, 32h+32), which
-    // hold scores already read.
-    float sum = 0.f;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      uint32_t r0[32], r1[32], pk[32];
-      tmem_ld64_wait(s_cols + h * 64, r0, r1);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        // keys kv0 + 64h + {2i, 2i+1} (from r0) and kv0 + 64h + 32 + {2i, 2i+1} (from r1)
-        float e0 = fast_exp2(fmaf(__uint_as_float(r0[2 * i]), kScaleLog2, -m_run));
-        float e1 = fast_exp2(fmaf(__uint_as_float(r0[2 * i + 1]), kScaleLog2, -m_run));
-        float e2 = fast_exp2(fmaf(__uint_as_float(r1[2 * i]), kScaleLog2, -m_run));
-        float e3 = fast_exp2(fmaf(__uint_as_float(r1[2 * i + 1]), kScaleLog2, -m_run));
-        if (tail) {
-          const int k = kv0 + h * 64 + 2 * i;
-          if (k >= seq) e0 = 0.f;
-          if (k + 1 >= seq) e1 = 0.f;
-          if (k + 32 >= seq) e2 = 0.f;
-          if (k + 33 >= seq) e3 = 0.f;
-        }
-        pk[i] = pack_half2(e0, e1);
-        pk[16 + i] = pack_half2(e2, e3);
-        // normalise by the sum of the rounded weights the PV product actually uses
-        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
-        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&pk[16 + i]));
-        sum += (f0.x + f0.y) + (f1.x + f1.y);
-      }
-      tmem_st32(s_cols + h * 32, pk);
     }
     tmem_st_wait();
     l_run = l_run * alpha + sum;
