@@ -95,12 +95,17 @@ __device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t t
         if (kv0 + 96 + i >= seq) r3[i] = __float_as_uint(-INFINITY);
       }
     }
-    float mx = -INFINITY;
+    // row maximum: two chains of three-input maxima
+    float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      mx = fmaxf(mx, fmaxf(fmaxf(__uint_as_float(r0[i]), __uint_as_float(r1[i])),
-                           fmaxf(__uint_as_float(r2[i]), __uint_as_float(r3[i]))));
-    mx *= kScaleLog2;
+    for (int i = 0; i < 32; i += 2) {
+      mx0 = fmax3(mx0, fmax3(__uint_as_float(r0[i]), __uint_as_float(r1[i]), __uint_as_float(r2[i])),
+                  __uint_as_float(r3[i]));
+      mx1 = fmax3(mx1, fmax3(__uint_as_float(r0[i + 1]), __uint_as_float(r1[i + 1]),
+                             __uint_as_float(r2[i + 1])),
+                  __uint_as_float(r3[i + 1]));
+    }
+    const float mx = fmaxf(mx0, mx1) * kScaleLog2;
     float alpha = 1.f;
     bool rescale = false;
     if (j == 0) {
@@ -112,18 +117,25 @@ __device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t t
     }
     // P = exp2(s * scale - m) as fp16 pairs over the score columns (keys 2k, 2k+1 in column k),
     // 16 columns per store so each chunk of scores dies as soon as it is used; masked keys
-    // hold -inf and give 0
-    float sum = 0.f;
+    // hold -inf and give 0.  The argument and the row sum run on packed fp32 pairs; the sum
+    // takes the fp32 weights (their fp16 rounding in P is 2^-12 relative).
+    const uint64_t scale2 = f32x2(kScaleLog2, kScaleLog2);
+    const uint64_t negm2 = f32x2(-m_run, -m_run);
+    uint64_t sum_a = f32x2(0.f, 0.f), sum_b = f32x2(0.f, 0.f);
     auto emit = [&](const uint32_t (&sc)[32], uint32_t col) {
       uint32_t pk[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float e0 = fast_exp2(fmaf(__uint_as_float(sc[2 * i]), kScaleLog2, -m_run));
-        const float e1 = fast_exp2(fmaf(__uint_as_float(sc[2 * i + 1]), kScaleLog2, -m_run));
+        float a, b;
+        f32x2_split(ffma2(f32x2(__uint_as_float(sc[2 * i]), __uint_as_float(sc[2 * i + 1])), scale2,
+                          negm2),
+                    a, b);
+        const float e0 = fast_exp2(a), e1 = fast_exp2(b);
         pk[i] = pack_half2(e0, e1);
-        // normalise by the sum of the rounded weights the PV product actually uses
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pk[i]));
-        sum += f.x + f.y;
+        if (i & 1)
+          sum_b = fadd2(sum_b, f32x2(e0, e1));
+        else
+          sum_a = fadd2(sum_a, f32x2(e0, e1));
       }
       tmem_st16(s_cols + col, pk);
     };
@@ -131,6 +143,13 @@ __device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t t
     emit(r1, 16);  // keys [32, 64)  -> columns [16, 32)
     emit(r2, 32);  // keys [64, 96)  -> columns [32, 48)
     emit(r3, 48);  // keys [96, 128) -> columns [48, 64)
+    float sum;
+    {
+      float a0, a1, b0, b1;
+      f32x2_split(sum_a, a0, a1);
+      f32x2_split(sum_b, b0, b1);
+      sum = (a0 + a1) + (b0 + b1);
+    }
     // O holds sum_{t<j} P_t V_t (PV(j-1) was issued before S(j), whose completion we saw);
     // rescaled after the scores are consumed, so the two never hold registers together
     if (__any_sync(0xffffffffu, rescale)) {
