@@ -7,17 +7,18 @@
 // One CTA owns two tiles of 128 query rows (A and B) of one head and streams the keys in tiles
 // of 128.  Twelve warps:
 //   warp 0       TMA producer: both Q tiles once, then K and V^T tiles into a two-stage ring
-//                (K and V of a stage have separate arrival barriers);
+//                (K and V of a stage have separate arrival barriers, so S can start before V
+//                lands);
 //   warp 1       MMA issuer, in the order S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ...
-//                so that the tensor core works on one query tile while the other's softmax runs;
+//                so that the tensor core works on one query tile while the other's softmax runs
+//                (a strict alternation: two independent issuers drift into lock-step);
 //   warps 4..7   softmax of tile A, warps 8..11 softmax of tile B: one query row per thread (its
-//                TMEM lane).  A first pass over the scores in TMEM takes the row maximum; a second
-//                pass writes P = exp2(S * log2(e)/sqrt(d) - m) as packed fp16 back over the score
-//                columns, where the PV product (fp16 P and V) reads it as its A operand straight
-//                from TMEM.  The
-//                running maximum is only moved (and O rescaled in TMEM) when a row's maximum grows
-//                by more than 2^8; the final division by the row sum of the rounded P makes the
-//                result exact either way.
+//                TMEM lane).  The row's 128 scores come out of TMEM in one round trip; a tree of
+//                three-input maxima gives the row maximum; P = exp2(S * log2(e)/sqrt(d) - m) is
+//                written back as packed fp16 over the score columns, where the PV product (fp16
+//                P and V) reads it as its A operand straight from TMEM.  The running maximum is
+//                only moved (and O rescaled in TMEM) when a row's maximum grows by more than
+//                2^8; the final division by the row sum makes the result exact either way.
 // TMEM columns: S/P of A [0,128), S/P of B [128,256), O of A [256,384), O of B [384,512).
 // V arrives transposed ([B, H, 128, S_pad], fp16 holding the bf16 values) so the PV product
 // reads a K-major operand.
@@ -30,10 +31,11 @@ namespace {
 constexpr int kAttnThreads = 384;
 constexpr int kQTile = 128;
 constexpr int kKvTile = 128;
-constexpr int kKvStages = 2;
+constexpr int kStages = 2;
 constexpr int kHalfTile = 128 * 128;  // 128 rows x 64 bf16 (one 128-byte swizzle column block)
 constexpr int kTileBytes = 2 * kHalfTile;  // 128 rows x 128 bf16 = 32 KB
-constexpr int kSmemData = 2 * kTileBytes + kKvStages * 2 * kTileBytes;  // Q_A Q_B | K,V x2 = 192 KB
+// Q_A Q_B | K x kStages | V x kStages: 192 KB
+constexpr int kSmemData = (2 + 2 * kStages) * kTileBytes;
 constexpr int kAttnSmem = kSmemData + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = make_idesc<kKindF16>(128, 128);      // S = Q K^T, bf16 operands
@@ -43,9 +45,9 @@ constexpr float kRescaleThreshold = 8.0f;           // in log2 units
 
 struct AttnBarriers {
   uint64_t q_full;
-  uint64_t k_full[kKvStages];
-  uint64_t v_full[kKvStages];
-  uint64_t kv_empty[kKvStages];
+  uint64_t k_full[kStages];
+  uint64_t v_full[kStages];
+  uint64_t kv_empty[kStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full;
@@ -56,9 +58,11 @@ struct AttnBarriers {
 
 __device__ __forceinline__ uint8_t* q_tile(uint8_t* smem, int x) { return smem + x * kTileBytes; }
 __device__ __forceinline__ uint8_t* k_tile(uint8_t* smem, int st) {
-  return smem + 2 * kTileBytes + st * 2 * kTileBytes;
+  return smem + (2 + st) * kTileBytes;
 }
-__device__ __forceinline__ uint8_t* v_tile(uint8_t* smem, int st) { return k_tile(smem, st) + kTileBytes; }
+__device__ __forceinline__ uint8_t* v_tile(uint8_t* smem, int st) {
+  return smem + (2 + kStages + st) * kTileBytes;
+}
 
 // Softmax, correction and output of query tile X (warps 4+4X .. 7+4X).
 template <typename OutT>
@@ -95,7 +99,6 @@ __device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t t
         if (kv0 + 96 + i >= seq) r3[i] = __float_as_uint(-INFINITY);
       }
     }
-    // row maximum: two chains of three-input maxima
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
@@ -153,13 +156,13 @@ __device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t t
     // O holds sum_{t<j} P_t V_t (PV(j-1) was issued before S(j), whose completion we saw);
     // rescaled after the scores are consumed, so the two never hold registers together
     if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t r[16];
+        tmem_ld16_wait(o_cols + c * 16, r);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32_wait(o_cols + c * 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-        tmem_st32(o_cols + c * 32, r);
+        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+        tmem_st16(o_cols + c * 16, r);
       }
     }
     tmem_st_wait();
@@ -210,7 +213,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&sb->q_full, 1);
-    for (int s = 0; s < kKvStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&sb->k_full[s], 1);
       mbar_init(&sb->v_full[s], 1);
       mbar_init(&sb->kv_empty[s], 1);
@@ -244,10 +247,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tma_load_3d(q_tile(smem, x), &tm_q, &sb->q_full, 0, q0 + x * kQTile, bh);
         tma_load_3d(q_tile(smem, x) + kHalfTile, &tm_q, &sb->q_full, 64, q0 + x * kQTile, bh);
       }
-      int last_parity[kKvStages] = {-1, -1};
+      int last_parity[kStages] = {-1, -1};
       for (int j = 0; j < n_kv; ++j) {
-        const int st = j % kKvStages;
-        const uint32_t ph = static_cast<uint32_t>(j / kKvStages) & 1u;
+        const int st = j % kStages;
+        const uint32_t ph = static_cast<uint32_t>(j / kStages) & 1u;
         if (!mbar_wait(&sb->kv_empty[st], ph ^ 1u, abort_flag, status, kErrAttnWait)) break;
         const int kv0 = j * kKvTile;
         mbar_arrive_expect_tx(&sb->k_full[st], kTileBytes);
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // give the copies already issued a bounded chance to land before the CTA exits
         int never = 0;
         mbar_wait(&sb->q_full, 0, &never, status, 0);
-        for (int s = 0; s < kKvStages; ++s)
+        for (int s = 0; s < kStages; ++s)
           if (last_parity[s] >= 0) {
             mbar_wait(&sb->k_full[s], static_cast<uint32_t>(last_parity[s]), &never, status, 0);
             mbar_wait(&sb->v_full[s], static_cast<uint32_t>(last_parity[s]), &never, status, 0);
@@ -271,54 +274,73 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---------------- MMA issuer
-      auto issue_s = [&](int x, int j) -> bool {
-        const int st = j % kKvStages;
-        if (!mbar_wait(&sb->k_full[st], static_cast<uint32_t>(j / kKvStages) & 1u, abort_flag,
-                       status, kErrAttnWait))
-          return false;
-        tc_fence_after();
-        const uint32_t qa = smem_addr(q_tile(smem, x));
-        const uint32_t kb = smem_addr(k_tile(smem, st));
+      // ---------------- MMA issuer.  Every wait or commit stalls this one thread for tens of
+      // cycles while the tensor core drains its short queue, so the loop keeps them few: one
+      // wait per K and per V tile (both query tiles read the same one), fences only after the
+      // softmax's P hand-off (the TMA barriers need none), one release commit per K/V stage,
+      // and shared-memory descriptors built once, each product then adding a constant.
+      const uint64_t dq[2] = {sdesc_kmajor_sw128(smem_addr(q_tile(smem, 0))),
+                              sdesc_kmajor_sw128(smem_addr(q_tile(smem, 1)))};
+      const uint64_t dk[2] = {sdesc_kmajor_sw128(smem_addr(k_tile(smem, 0))),
+                              sdesc_kmajor_sw128(smem_addr(k_tile(smem, 1)))};
+      const uint64_t dv[2] = {sdesc_kmajor_sw128(smem_addr(v_tile(smem, 0))),
+                              sdesc_kmajor_sw128(smem_addr(v_tile(smem, 1)))};
+      // K-step k of a 128 x 128 operand tile: 16 elements into its 128-byte swizzle atoms
+      auto koff = [](int k) -> uint64_t {
+        return static_cast<uint64_t>(((k >> 2) * kHalfTile + (k & 3) * 32) >> 4);
+      };
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return mbar_wait(bar, parity, abort_flag, status, kErrAttnWait);
+      };
+      auto mma_s = [&](int x, int j) {  // S_x(j) = Q_x K_j^T into columns [128x, 128x + 128)
+        const uint64_t k_desc = (j % kStages) ? dk[1] : dk[0];
         const uint32_t d_s = tmem + static_cast<uint32_t>(x * 128);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = static_cast<uint32_t>((k >> 2) * kHalfTile + (k & 3) * 32);
-          tc_mma<kKindF16>(d_s, sdesc_kmajor_sw128(qa + off), sdesc_kmajor_sw128(kb + off), kIdesc,
-                           k > 0 ? 1u : 0u);
-        }
+        for (int k = 0; k < 8; ++k)
+          tc_mma<kKindF16>(d_s, dq[x] + koff(k), k_desc + koff(k), kIdesc, k > 0 ? 1u : 0u);
         tc_commit(&sb->s_full[x]);
-        return true;
       };
-      auto issue_pv = [&](int x, int j) -> bool {
-        const int st = j % kKvStages;
-        if (!mbar_wait(&sb->p_full[x], static_cast<uint32_t>(j) & 1u, abort_flag, status,
-                       kErrAttnWait) ||
-            !mbar_wait(&sb->v_full[st], static_cast<uint32_t>(j / kKvStages) & 1u, abort_flag,
-                       status, kErrAttnWait))
-          return false;
-        tc_fence_after();
-        const uint32_t vb = smem_addr(v_tile(smem, st));
-        const uint32_t p_cols = tmem + static_cast<uint32_t>(x * 128);  // P: 16 keys per 8 columns
+      auto mma_pv = [&](int x, int j) {  // O_x += P_x(j) V_j, P read from TMEM over S_x
+        const uint64_t v_desc = (j % kStages) ? dv[1] : dv[0];
+        const uint32_t p_cols = tmem + static_cast<uint32_t>(x * 128);  // 16 keys per 8 columns
         const uint32_t d_o = tmem + 256u + static_cast<uint32_t>(x * 128);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = static_cast<uint32_t>((k >> 2) * kHalfTile + (k & 3) * 32);
-          tc_mma_ts_f16(d_o, p_cols + static_cast<uint32_t>(k * 8), sdesc_kmajor_sw128(vb + off),
-                        kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < 8; ++k)
+          tc_mma_ts_f16(d_o, p_cols + static_cast<uint32_t>(k * 8), v_desc + koff(k), kIdescPV,
+                        (j > 0 || k > 0) ? 1u : 0u);
+      };
+      auto k_ready = [&](int j) {
+        return wait(&sb->k_full[j % kStages], static_cast<uint32_t>(j / kStages) & 1u);
+      };
+      auto v_ready = [&](int j) {
+        return wait(&sb->v_full[j % kStages], static_cast<uint32_t>(j / kStages) & 1u);
+      };
+      auto p_ready = [&](int x, int j) {
+        if (!wait(&sb->p_full[x], static_cast<uint32_t>(j) & 1u)) return false;
+        tc_fence_after();
         return true;
       };
-      bool ok = mbar_wait(&sb->q_full, 0, abort_flag, status, kErrAttnWait) && issue_s(0, 0) &&
-                issue_s(1, 0);
+      bool ok = wait(&sb->q_full, 0) && k_ready(0);
+      if (ok) {
+        mma_s(0, 0);
+        mma_s(1, 0);
+      }
       for (int j = 0; ok && j < n_kv; ++j) {
         const bool more = j + 1 < n_kv;
-        ok = issue_pv(0, j) && (!more || issue_s(0, j + 1)) && issue_pv(1, j);
-        if (!ok) break;
-        tc_commit(&sb->kv_empty[j % kKvStages]);
-        if (more && !issue_s(1, j + 1)) ok = false;
+        // PV_A(j) S_A(j+1) PV_B(j) S_B(j+1): the tensor core works on one tile while the other
+        // tile's softmax runs
+        if (!(v_ready(j) && p_ready(0, j))) break;
+        mma_pv(0, j);
+        if (more) {
+          if (!k_ready(j + 1)) break;
+          mma_s(0, j + 1);
+        }
+        if (!p_ready(1, j)) break;
+        mma_pv(1, j);
+        tc_commit(&sb->kv_empty[j % kStages]);  // K_j and V_j fully consumed once this lands
+        if (more) mma_s(1, j + 1);
+        if (j + 1 == n_kv) tc_commit(&sb->o_full);
       }
-      if (ok) tc_commit(&sb->o_full);
       if (*abort_flag) {
         // wait (bounded) for every MMA issued so far before TMEM is released
         int never = 0;
