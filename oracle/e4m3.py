@@ -85,3 +85,42 @@ def fp8_linear(x, w, b, scale_x: float, scale_w: float):
     qw = e4m3_quantize(np.asarray(w, np.float64) * scale_w)
     y = qx @ qw.T / (scale_x * scale_w)
     return y if b is None else y + np.asarray(b, np.float64)
+
+
+class DelayedScaling:
+    """E4M3 casts of the block linears with per-tensor delayed scaling.
+
+    "FP8 training for Flux models", §Configuration › FP8 model configuration
+    (``fp8: "e4m3"``, ``amax_history_len: 1024``, ``amax_compute_algo:
+    most_recent``, ``margin: 0``): every linear's input and weight are cast
+    to E4M3 with the scale the tensor was given, the product is divided by
+    both scales, and the tensor's absolute maximum is recorded so that the
+    next call's scale is ``448 / amax`` (``delayed_scale``).
+
+    ``scales`` maps a tensor name (``"<linear>.x"`` for the input,
+    ``"<linear>.w"`` for the weight) to the scale it is cast with; names not
+    given use 1, the scale of an empty history.  ``amax`` collects, per name,
+    the largest |value| the tensor held in this evaluation.
+    """
+
+    def __init__(self, scales=None):
+        self.scales = dict(scales or {})
+        self.amax = {}
+
+    def _record(self, name, a):
+        m = float(np.max(np.abs(a))) if np.size(a) else 0.0
+        self.amax[name] = max(self.amax.get(name, 0.0), m)
+
+    def linear(self, name, x, w, b):
+        """y = x W^T + b on E4M3 operands: x and w are cast as given (no other rounding)."""
+        x = np.asarray(x, np.float64)
+        w = np.asarray(w, np.float64)
+        self._record(name + ".x", x)
+        self._record(name + ".w", w)
+        sx = float(self.scales.get(name + ".x", 1.0))
+        sw = float(self.scales.get(name + ".w", 1.0))
+        return fp8_linear(x, w, b, sx, sw)
+
+    def next_scales(self, margin: int = 0):
+        """The scales of the next call under ``most_recent``: 448 / amax / 2^margin."""
+        return {k: delayed_scale(a, margin) for k, a in self.amax.items()}

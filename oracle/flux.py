@@ -35,6 +35,11 @@ design notes of the repository as well):
     §Performance optimizations › 5. Mixed precision; API page, §Optimization tips): the
     operands of every linear layer and the attention's inputs q, k, v are rounded to bf16;
     everything else (including the softmax weights inside the fused attention) stays float64.
+  * FP8 (``fp8=oracle.e4m3.DelayedScaling(...)``, FP8 page §Configuration): the four linears
+    of each stream (QKV, attention output projection, fc1, fc2) cast input and weight to E4M3
+    with per-tensor scales; the modulation, embeddings, head and attention do not.  The
+    projection reads the attention output in the activation type (``mm_cast``); the LayerNorm
+    and GELU results are cast directly from the arithmetic that makes them (a fused cast).
 """
 from __future__ import annotations
 
@@ -158,6 +163,20 @@ def linear(x, w, b=None, mm_cast=None):
     return y if b is None else y + _f64(b)
 
 
+def block_linear(name, x, w, b, mm_cast=None, fp8=None):
+    """One of a block's four linears (QKV, attention output projection, fc1, fc2).
+
+    With ``fp8`` (an ``oracle.e4m3.DelayedScaling``) the input and weight are
+    cast to E4M3 with their per-tensor scales, as the FP8 page configures the
+    linears (§Configuration › FP8 model configuration); the modulation,
+    embedding and head linears and the attention are never FP8.  Otherwise
+    this is ``linear``.
+    """
+    if fp8 is None:
+        return linear(x, w, b, mm_cast)
+    return fp8.linear(name, x, w, b)
+
+
 # ----------------------------------------------------------------------------- AdaLN
 def modulation(vec, w_mod, b_mod, n_chunks=6, mm_cast=None):
     """AdaLN.forward: Linear(SiLU(vec)) split into chunks along the feature axis.
@@ -213,7 +232,8 @@ def _merge(x):
     return x.transpose(0, 2, 1, 3).reshape(B, S, H * d)
 
 
-def qkv_heads(x, shift, scale, w, heads, ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast=None):
+def qkv_heads(x, shift, scale, w, heads, ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast=None,
+              fp8=None, name=""):
     """Attention-branch pre-norm and projection of one stream, before RoPE.
 
     Architecture page, §3. MMDiT layer (double block), steps 1-2:
@@ -221,35 +241,46 @@ def qkv_heads(x, shift, scale, w, heads, ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast
     RMSNorm of q and k.  Returns q, k, v as [B, H, S, d].
     """
     h = modulate(x, shift, scale, ln_eps)
-    qkv = linear(h, w["w_qkv"], w["b_qkv"], mm_cast)
+    qkv = block_linear(name + ".qkv", h, w["w_qkv"], w["b_qkv"], mm_cast, fp8)
     q, k, v = np.split(qkv, 3, axis=-1)
     q = rmsnorm(_heads(q, heads), w["g_q"], rms_eps)
     k = rmsnorm(_heads(k, heads), w["g_k"], rms_eps)
     return q, k, _heads(v, heads)
 
 
-def mlp_branch(x, shift, scale, w, gelu_tanh=False, ln_eps=LN_EPS, mm_cast=None):
+def mlp_branch(x, shift, scale, w, gelu_tanh=False, ln_eps=LN_EPS, mm_cast=None, fp8=None,
+               name=""):
     """Architecture page, §3. MMDiT layer, step 4: AdaLN -> Linear -> GELU -> Linear."""
     h = modulate(x, shift, scale, ln_eps)
-    u = gelu(linear(h, w["w_1"], w["b_1"], mm_cast), gelu_tanh)
-    return linear(u, w["w_2"], w["b_2"], mm_cast)
+    u = gelu(block_linear(name + ".fc1", h, w["w_1"], w["b_1"], mm_cast, fp8), gelu_tanh)
+    return block_linear(name + ".fc2", u, w["w_2"], w["b_2"], mm_cast, fp8)
+
+
+def out_proj(o, w, name="", mm_cast=None, fp8=None):
+    """Attention output projection of one stream.  The attention returns its output in the
+    activation type (``mm_cast``), and that tensor is what the projection (or its E4M3 cast)
+    reads."""
+    return block_linear(name + ".o", _cast(o, mm_cast), w["w_o"], w["b_o"], mm_cast, fp8)
 
 
 def double_block(x_img, x_txt, vec, cos, sin, w_img, w_txt, heads,
-                 interleaved=True, gelu_tanh=False, ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast=None):
+                 interleaved=True, gelu_tanh=False, ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast=None,
+                 fp8=None):
     """Double-stream (joint) block forward.
 
     Architecture page, §Model components › 3. MMDiT layer (double block);
     API page, §Layer specifications › MMDiTLayer.  ``cos``/``sin`` are
-    ``[B, S_img + S_txt, d/2]`` in the joint order [image; text].
+    ``[B, S_img + S_txt, d/2]`` in the joint order [image; text].  ``fp8``
+    (``oracle.e4m3.DelayedScaling``) makes the four linears of each stream
+    E4M3, with tensors named ``img.*`` and ``txt.*``.
     Returns (y_img, y_txt).
     """
     c = mm_cast
     S_i = np.shape(x_img)[1]
     mi = modulation(vec, w_img["w_mod"], w_img["b_mod"], mm_cast=c)
     mt = modulation(vec, w_txt["w_mod"], w_txt["b_mod"], mm_cast=c)
-    qi, ki, vi = qkv_heads(x_img, mi[0], mi[1], w_img, heads, ln_eps, rms_eps, c)
-    qt, kt, vt = qkv_heads(x_txt, mt[0], mt[1], w_txt, heads, ln_eps, rms_eps, c)
+    qi, ki, vi = qkv_heads(x_img, mi[0], mi[1], w_img, heads, ln_eps, rms_eps, c, fp8, "img")
+    qt, kt, vt = qkv_heads(x_txt, mt[0], mt[1], w_txt, heads, ln_eps, rms_eps, c, fp8, "txt")
     q = np.concatenate([qi, qt], axis=2)
     k = np.concatenate([ki, kt], axis=2)
     v = np.concatenate([vi, vt], axis=2)
@@ -258,37 +289,39 @@ def double_block(x_img, x_txt, vec, cos, sin, w_img, w_txt, heads,
     k = apply_rope(k, cs, sn, interleaved)
     o = _merge(attention(q, k, v, c))
     o_img, o_txt = o[:, :S_i], o[:, S_i:]
-    x_img = gated_residual(x_img, mi[2], linear(o_img, w_img["w_o"], w_img["b_o"], c))
-    x_txt = gated_residual(x_txt, mt[2], linear(o_txt, w_txt["w_o"], w_txt["b_o"], c))
-    x_img = gated_residual(x_img, mi[5], mlp_branch(x_img, mi[3], mi[4], w_img, gelu_tanh, ln_eps, c))
-    x_txt = gated_residual(x_txt, mt[5], mlp_branch(x_txt, mt[3], mt[4], w_txt, gelu_tanh, ln_eps, c))
+    x_img = gated_residual(x_img, mi[2], out_proj(o_img, w_img, "img", c, fp8))
+    x_txt = gated_residual(x_txt, mt[2], out_proj(o_txt, w_txt, "txt", c, fp8))
+    x_img = gated_residual(x_img, mi[5],
+                           mlp_branch(x_img, mi[3], mi[4], w_img, gelu_tanh, ln_eps, c, fp8, "img"))
+    x_txt = gated_residual(x_txt, mt[5],
+                           mlp_branch(x_txt, mt[3], mt[4], w_txt, gelu_tanh, ln_eps, c, fp8, "txt"))
     return x_img, x_txt
 
 
 def single_block(x, vec, cos, sin, w, heads, interleaved=True, gelu_tanh=False,
-                 ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast=None):
+                 ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast=None, fp8=None):
     """Single-stream block forward over the concatenated sequence ``x = [img; txt]``.
 
     Architecture page, §Model components › 4. Flux single block: AdaLN,
     QKV, attention, gated residual, AdaLN, MLP, gated residual, all with one
     weight set.  Returns all rows (the caller keeps the image rows after the
-    last single block).
+    last single block).  ``fp8`` names its tensors ``single.*``.
     """
     c = mm_cast
     m = modulation(vec, w["w_mod"], w["b_mod"], mm_cast=c)
-    q, k, v = qkv_heads(x, m[0], m[1], w, heads, ln_eps, rms_eps, c)
+    q, k, v = qkv_heads(x, m[0], m[1], w, heads, ln_eps, rms_eps, c, fp8, "single")
     cs, sn = _f64(cos)[:, None], _f64(sin)[:, None]
     q = apply_rope(q, cs, sn, interleaved)
     k = apply_rope(k, cs, sn, interleaved)
     o = _merge(attention(q, k, v, c))
-    x = gated_residual(x, m[2], linear(o, w["w_o"], w["b_o"], c))
-    return gated_residual(x, m[5], mlp_branch(x, m[3], m[4], w, gelu_tanh, ln_eps, c))
+    x = gated_residual(x, m[2], out_proj(o, w, "single", c, fp8))
+    return gated_residual(x, m[5], mlp_branch(x, m[3], m[4], w, gelu_tanh, ln_eps, c, fp8, "single"))
 
 
 # ----------------------------------------------------------------------------- row-sampled blocks
-def _rows_after_attention(x_rows, o_rows, m, w, gelu_tanh, ln_eps, mm_cast):
-    x1 = gated_residual(x_rows, m[2], linear(o_rows, w["w_o"], w["b_o"], mm_cast))
-    return gated_residual(x1, m[5], mlp_branch(x1, m[3], m[4], w, gelu_tanh, ln_eps, mm_cast))
+def _rows_after_attention(x_rows, o_rows, m, w, gelu_tanh, ln_eps, mm_cast, fp8=None, name=""):
+    x1 = gated_residual(x_rows, m[2], out_proj(o_rows, w, name, mm_cast, fp8))
+    return gated_residual(x1, m[5], mlp_branch(x1, m[3], m[4], w, gelu_tanh, ln_eps, mm_cast, fp8, name))
 
 
 def _attend_rows(q_rows, k, v, c_rows, s_rows, c_all, s_all, interleaved, mm_cast):
@@ -299,46 +332,52 @@ def _attend_rows(q_rows, k, v, c_rows, s_rows, c_all, s_all, interleaved, mm_cas
 
 def double_block_rows(x_img, x_txt, vec, cos, sin, w_img, w_txt, heads, rows_img, rows_txt,
                       interleaved=True, gelu_tanh=False, ln_eps=LN_EPS, rms_eps=RMS_EPS,
-                      mm_cast=None):
+                      mm_cast=None, fp8=None):
     """The double block's output at selected rows only (same batch rows for every sample).
 
     Keys and values need every token; queries, attention, the output
     projection and the MLP are row-wise, so computing them for a subset of
-    rows gives those rows of ``double_block`` exactly.
+    rows gives those rows of ``double_block`` exactly.  With ``fp8`` the
+    scales must be given: the amax this records for the tensors after the
+    attention covers the selected rows only.
     """
     c = mm_cast
     S_i = np.shape(x_img)[1]
     mi = modulation(vec, w_img["w_mod"], w_img["b_mod"], mm_cast=c)
     mt = modulation(vec, w_txt["w_mod"], w_txt["b_mod"], mm_cast=c)
     # keys/values for every token (queries are recomputed only for the chosen rows)
-    _, ki, vi = qkv_heads(x_img, mi[0], mi[1], w_img, heads, ln_eps, rms_eps, c)
-    _, kt, vt = qkv_heads(x_txt, mt[0], mt[1], w_txt, heads, ln_eps, rms_eps, c)
+    _, ki, vi = qkv_heads(x_img, mi[0], mi[1], w_img, heads, ln_eps, rms_eps, c, fp8, "img")
+    _, kt, vt = qkv_heads(x_txt, mt[0], mt[1], w_txt, heads, ln_eps, rms_eps, c, fp8, "txt")
     k = np.concatenate([ki, kt], axis=2)
     v = np.concatenate([vi, vt], axis=2)
     cos, sin = _f64(cos), _f64(sin)
     rows_img = np.asarray(rows_img)
     rows_txt = np.asarray(rows_txt)
-    qi, _, _ = qkv_heads(_f64(x_img)[:, rows_img], mi[0], mi[1], w_img, heads, ln_eps, rms_eps, c)
-    qt, _, _ = qkv_heads(_f64(x_txt)[:, rows_txt], mt[0], mt[1], w_txt, heads, ln_eps, rms_eps, c)
+    qi, _, _ = qkv_heads(_f64(x_img)[:, rows_img], mi[0], mi[1], w_img, heads, ln_eps, rms_eps, c,
+                         fp8, "img")
+    qt, _, _ = qkv_heads(_f64(x_txt)[:, rows_txt], mt[0], mt[1], w_txt, heads, ln_eps, rms_eps, c,
+                         fp8, "txt")
     jr_i, jr_t = rows_img, S_i + rows_txt
     oi = _attend_rows(qi, k, v, cos[:, jr_i], sin[:, jr_i], cos, sin, interleaved, c)
     ot = _attend_rows(qt, k, v, cos[:, jr_t], sin[:, jr_t], cos, sin, interleaved, c)
-    yi = _rows_after_attention(_f64(x_img)[:, rows_img], oi, mi, w_img, gelu_tanh, ln_eps, c)
-    yt = _rows_after_attention(_f64(x_txt)[:, rows_txt], ot, mt, w_txt, gelu_tanh, ln_eps, c)
+    yi = _rows_after_attention(_f64(x_img)[:, rows_img], oi, mi, w_img, gelu_tanh, ln_eps, c, fp8,
+                               "img")
+    yt = _rows_after_attention(_f64(x_txt)[:, rows_txt], ot, mt, w_txt, gelu_tanh, ln_eps, c, fp8,
+                               "txt")
     return yi, yt
 
 
 def single_block_rows(x, vec, cos, sin, w, heads, rows, interleaved=True, gelu_tanh=False,
-                      ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast=None):
+                      ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast=None, fp8=None):
     """The single block's output at selected rows only (see ``double_block_rows``)."""
     c = mm_cast
     m = modulation(vec, w["w_mod"], w["b_mod"], mm_cast=c)
-    _, k, v = qkv_heads(x, m[0], m[1], w, heads, ln_eps, rms_eps, c)
+    _, k, v = qkv_heads(x, m[0], m[1], w, heads, ln_eps, rms_eps, c, fp8, "single")
     rows = np.asarray(rows)
-    q, _, _ = qkv_heads(_f64(x)[:, rows], m[0], m[1], w, heads, ln_eps, rms_eps, c)
+    q, _, _ = qkv_heads(_f64(x)[:, rows], m[0], m[1], w, heads, ln_eps, rms_eps, c, fp8, "single")
     cos, sin = _f64(cos), _f64(sin)
     o = _attend_rows(q, k, v, cos[:, rows], sin[:, rows], cos, sin, interleaved, c)
-    return _rows_after_attention(_f64(x)[:, rows], o, m, w, gelu_tanh, ln_eps, c)
+    return _rows_after_attention(_f64(x)[:, rows], o, m, w, gelu_tanh, ln_eps, c, fp8, "single")
 
 
 # ----------------------------------------------------------------------------- embeddings and head
