@@ -36,6 +36,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MMDiT block fwd TFLOP/s & % of GB300 bf16 tensor peak at 4096+512 tokens"
 WORKLOAD = "flux535m_bf16"
+FP8_WORKLOAD = "flux12b_2048px_fp8"
 AXES = (16, 56, 56)
 THETA = 10000.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -53,6 +54,9 @@ def parse_args():
                     help="time plain per-call launches instead of a CUDA-graph replay of the step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time of the oracle baseline sample")
+    ap.add_argument("--workload", choices=[WORKLOAD, FP8_WORKLOAD], default=WORKLOAD,
+                    help=f"{WORKLOAD}: the hot-path step above (the headline); {FP8_WORKLOAD}: the "
+                         "double + single block at 16384 + 512 tokens with E4M3 linears")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     return args
@@ -171,13 +175,88 @@ class DeviceStep:
         L.flow_match_noise_and_loss(self.z0, self.z1, self.t, pred=self.pred, loss=self.loss,
                                     ws=self.ws_flow)
 
-    def step_from_host(self, pinned: dict, loss_host):
-        """The same step with this step's inputs copied from pinned host memory and the loss
+    input_names = ("z0", "z1", "t", "txt", "vec", "ids")
+
+    def workspaces(self):
+        return (self.ws_block, self.ws_flow, self.ws_lin, self.ws_img, self.ws_final)
+
+    def result(self):
+        """The step's result read back by the end-to-end leg (the loss)."""
+        return self.loss
+
+    def step_from_host(self, pinned: dict, result_host):
+        """The same step with this step's inputs copied from pinned host memory and the result
         read back, all on the current stream."""
         for name, src in pinned.items():
             getattr(self, name).copy_(src, non_blocking=True)
         self.step()
-        loss_host.copy_(self.loss, non_blocking=True)
+        result_host.copy_(self.result(), non_blocking=True)
+
+
+class Fp8BlockStep(DeviceStep):
+    """The 12B block shapes at 2048 px with E4M3 linears: rope3d_freqs, then a double and a
+    single block whose four linears per stream run on E4M3 operands with delayed per-tensor
+    scaling (the blocks cast their weights at every call, as training does after each
+    optimizer step).  The workload names no text or image source, so the block inputs are
+    N(0, 1) at width D.  Each step records its amax into history column 0 (most_recent reads
+    only the latest), so that a captured graph replays the same step."""
+
+    def __init__(self, wl, device):
+        import torch
+        from diffusion_transformer_flux_gb300 import _lib as L
+        from diffusion_transformer_flux_gb300 import synth
+        self.L, self.torch, self.wl = L, torch, wl
+        B, D, H, F, S_i, S_t = wl.batch, wl.hidden, wl.heads, wl.mlp_hidden, wl.seq_img, wl.seq_txt
+        assert B == 1, "the concatenated-sequence views below assume batch 1"
+        S = S_i + S_t
+        bf = torch.bfloat16
+        inp = synth.block_inputs(B, S_i, S_t, D, "bf16", 1000 + wl.index, (wl.lat_h, wl.lat_w))
+        rng_w = np.random.Generator(np.random.PCG64(2000 + wl.index))
+        ws_ = [synth.stream_weights(rng_w, D, H, 128, F, "bf16") for _ in range(3)]
+
+        def dev(a, dt=bf):
+            return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device).to(dt)
+
+        self.w_dimg, self.w_dtxt, self.w_single = ({k: dev(v) for k, v in w.items()} for w in ws_)
+        self.X = dev(np.concatenate([inp.x_img, inp.x_txt], axis=1))
+        self.vec = dev(inp.vec)
+        self.ids = dev(inp.ids, torch.float32)
+        self.Y = torch.empty_like(self.X)
+        self.Z = torch.empty_like(self.X)
+        self.cos = torch.empty(B, S, 64, device=device)
+        self.sin = torch.empty_like(self.cos)
+        self.hist_d = torch.zeros(16, 1024, device=device)
+        self.scale_d = torch.ones(16, device=device)
+        self.hist_s = torch.zeros(8, 1024, device=device)
+        self.scale_s = torch.ones(8, device=device)
+        self.fp8_d = L.make_fp8_state(self.hist_d, self.scale_d, pos=0)
+        self.fp8_s = L.make_fp8_state(self.hist_s, self.scale_s, pos=0)
+        self.dims = L.make_dims(B, S_i, S_t, D, H, F, L.MMDIT_BF16, gemm=L.MMDIT_GEMM_FP8_E4M3)
+        ws_block = max(L.mmdit_double_block_workspace_size(self.dims),
+                       L.mmdit_single_block_workspace_size(self.dims))
+        self.ws_block = L.workspace(ws_block, device)
+        self.S, self.S_i = S, S_i
+        self.flops_blocks = 2 * block_flops(B, S, D, F, H)
+        self.flops_dense = self.flops_blocks
+        self.flops_linears = 2 * 2 * B * S * D * (3 * D + D + 2 * F)
+
+    input_names = ("X", "vec", "ids")
+
+    def workspaces(self):
+        return (self.ws_block,)
+
+    def result(self):
+        """The image rows of the single block's output (what a caller keeps)."""
+        return self.Z[:, :self.S_i]
+
+    def step(self):
+        L, S_i = self.L, self.S_i
+        L.rope3d_freqs(self.ids, AXES, THETA, self.cos, self.sin)
+        L.mmdit_double_block_fwd(self.dims, self.w_dimg, self.w_dtxt, self.vec, self.cos, self.sin,
+                                 self.X[:, :S_i], self.X[:, S_i:], self.Y[:, :S_i], self.Y[:, S_i:],
+                                 ws=self.ws_block, fp8=self.fp8_d)
+        L.mmdit_single_block_fwd(self.dims, self.w_single, self.vec, self.cos, self.sin, self.Y, self.Z,
+                                 ws=self.ws_block, fp8=self.fp8_s)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -263,10 +342,18 @@ def kernel_work(label: str, wl):
         if op == "modulation":
             sets = 2 if label == "double.modulation" else 1
             return "hbm", sets * (6.0 * D * D * 2 + B * 6 * D * 4) + B * D * 2, "B"
+        e_mm = 1 if wl.dtype == "fp8" else 2  # bytes per element of the linears' inputs
         if op == "ln1":
-            return "hbm", 2.0 * r * D * 2, "B"
+            return "hbm", r * D * 2 + r * D * e_mm, "B"
         if op == "ln2":
-            return "hbm", r * D * 4 + r * D * 2, "B"
+            return "hbm", r * D * 4 + r * D * e_mm, "B"
+        if op == "fp8_cast_w":  # every weight of the block's streams: bf16 in, E4M3 out
+            sets = 2 if parts[0] == "double" else 1
+            return "hbm", sets * 3.0 * (4 * D * D + 2 * F * D), "B"
+        if op == "fp8_cast_o":  # the attention output of every row: bf16 in, E4M3 out
+            return "hbm", 3.0 * B * S * D, "B"
+        if op == "fp8_scale":
+            return "latency", 0.0, ""
     n_lat = B * wl.channels * S_i
     if label == "rope3d_freqs":
         return "hbm", B * S * 3 * 4 + 2.0 * B * S * 64 * 4, "B"
@@ -402,9 +489,10 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     L.load()
-    wl = synth.WORKLOADS[WORKLOAD]
-    hw = HostWorkload(wl)
-    st = DeviceStep(hw, device)
+    wl = synth.WORKLOADS[args.workload]
+    fp8 = wl.dtype == "fp8"
+    hw = None if fp8 else HostWorkload(wl)
+    st = Fp8BlockStep(wl, device) if fp8 else DeviceStep(hw, device)
     peaks, peak_src = load_peaks()
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # > 129 MB of L2
@@ -439,7 +527,7 @@ def main():
     for _ in range(args.warmup):
         st.step()
     torch.cuda.synchronize()
-    for ws in (st.ws_block, st.ws_flow, st.ws_lin, st.ws_img, st.ws_final):
+    for ws in st.workspaces():
         if L.mmdit_workspace_status(ws) != 0:
             raise RuntimeError("a kernel gave up a bounded wait during warm-up")
 
@@ -472,19 +560,21 @@ def main():
         ms, _ = timed(step_fn, args.steps)
     launches = launches_per_step * args.steps
     clocks = clk.summary()
-    if not np.isfinite(st.loss.item()):
-        raise RuntimeError("non-finite loss")
+    if not bool(torch.isfinite(st.result()).all()):
+        raise RuntimeError("non-finite result")
     total_s = max_over_ranks(sum(ms) / 1e3)
     value = world * st.flops_blocks * args.steps / total_s / 1e12
 
     # end to end: this step's inputs from pinned host memory, the loss back to the host
-    pinned = {n: getattr(st, n).detach().cpu().pin_memory() for n in ("z0", "z1", "t", "txt", "vec", "ids")}
-    loss_host = torch.zeros(1, pin_memory=True)
+    pinned = {n: getattr(st, n).detach().cpu().pin_memory() for n in st.input_names}
+    res = st.result()
+    result_host = torch.empty(res.shape, dtype=res.dtype, pin_memory=True)
     for _ in range(2):
-        st.step_from_host(pinned, loss_host)
-    ms_e2e, _ = timed(lambda: st.step_from_host(pinned, loss_host), args.steps)
+        st.step_from_host(pinned, result_host)
+    ms_e2e, _ = timed(lambda: st.step_from_host(pinned, result_host), args.steps)
     e2e_s = max_over_ranks(sum(ms_e2e) / 1e3)
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = result_host.numel() * result_host.element_size()
 
     # per-kernel durations from CUDA events the library records around each of its steps
     L.mmdit_profile_enable(True)
@@ -501,6 +591,13 @@ def main():
     prof_total = sum(v[1] for v in agg.values()) or 1.0
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    # E4M3 contractions: the measured bf16 peak times the nominal dense fp8 : bf16 ratio (2)
+    fp8_peak = 2.0 * bf16_peak
+
+    def peak_of(name):
+        is_linear = name.split(".")[-1] in ("qkv", "out", "fc1", "fc2")
+        return fp8_peak if (fp8 and is_linear) else bf16_peak
+
     per_kernel = []
     for name, (n, t) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
         bound, amount, unit = kernel_work(name, wl)
@@ -509,7 +606,7 @@ def main():
                "bound": bound}
         if bound == "tensor":
             row["achieved_tflops"] = round(amount / avg_s / 1e12, 1)
-            row["frac"] = round(amount / avg_s / 1e12 / bf16_peak, 4)
+            row["frac"] = round(amount / avg_s / 1e12 / peak_of(name), 4)
         elif bound == "hbm":
             row["achieved_gbs"] = round(amount / avg_s / 1e9, 1)
             row["frac"] = round(amount / avg_s / 1e9 / hbm_peak, 4)
@@ -518,18 +615,20 @@ def main():
     bound, amount, unit = kernel_work(dom["kernel"], wl)
     dom_s = dom["avg_us"] / 1e6
     if bound == "tensor":
-        ach, peak, runit = amount / dom_s / 1e12, bf16_peak, "TFLOP/s"
+        ach, peak, runit = amount / dom_s / 1e12, peak_of(dom["kernel"]), "TFLOP/s"
     else:
         ach, peak, runit = amount / dom_s / 1e9, hbm_peak, "GB/s"
     roofline = {"kernel": dom["kernel"], "bound": bound, "achieved": round(ach, 2), "peak": peak,
                 "unit": runit, "frac": round(ach / peak, 4), "traffic": committed_traffic(dom["kernel"]),
                 "algorithmic_per_launch": amount, "algorithmic_unit": unit,
                 "peak_source": f"{peak_src}: {'bf16_tflops (burst)' if bound == 'tensor' else 'hbm_gbs'}"}
-    if bound == "tensor" and "bf16_tflops_sustained" in peaks:
+    if peak != bf16_peak and bound == "tensor":
+        roofline["peak_source"] += " x 2 (nominal dense fp8 : bf16 ratio)"
+    if bound == "tensor" and "bf16_tflops_sustained" in peaks and peak == bf16_peak:
         roofline["frac_of_sustained"] = round(ach / float(peaks["bf16_tflops_sustained"]), 4)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and hw is not None:
         cpu = run_cpu_baseline(hw, args.cpu_seconds)
 
     if rank == 0:
@@ -537,25 +636,34 @@ def main():
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 linears, bf16 attention and activations" if fp8 else "bf16",
             "data": "synthetic (seeded PCG64; N(0,0.02) weights, N(0,1) activations, text embeddings "
                     "and latents; no dataset or trained weights)",
-            "config": {"workload": WORKLOAD, "global_batch": world * wl.batch, "seq_len": S,
+            "config": {"workload": args.workload, "global_batch": world * wl.batch, "seq_len": S,
                        "tokens": f"{wl.seq_img} image + {wl.seq_txt} text", "hidden": wl.hidden,
                        "heads": wl.heads, "head_dim": 128, "mlp_hidden": wl.mlp_hidden,
                        "parallelism": f"{world} independent replica(s), no exchange",
                        "l2": "flushed before every timed step (256 MB write outside the events)",
                        "launch": "plain calls" if args.no_graph else
                                  "CUDA-graph replay of the step (e2e: plain calls)",
-                       "step": "rope3d_freqs, flow-matching noise, img_in, txt_in, double block, "
-                               "single block, output head, flow-matching loss",
+                       "step": ("rope3d_freqs, double block, single block (E4M3 linears with "
+                                "delayed per-tensor scaling; weights cast at every call)") if fp8 else
+                               ("rope3d_freqs, flow-matching noise, img_in, txt_in, double block, "
+                                "single block, output head, flow-matching loss"),
                        "flops_counted_per_step": st.flops_blocks,
                        "dense_flops_per_step_incl_embeds_and_head": st.flops_dense},
             "pct_of_bf16_peak": round(100 * value / world / bf16_peak, 2),
+            **({"fp8_peak_tflops": fp8_peak,
+                "linears_pct_of_fp8_peak": round(100 * sum(r["achieved_tflops"] * r["avg_us"] for r in per_kernel
+                                                           if r["bound"] == "tensor" and peak_of(r["kernel"]) == fp8_peak)
+                                                 / max(1e-9, sum(r["avg_us"] for r in per_kernel if r["bound"] == "tensor"
+                                                                 and peak_of(r["kernel"]) == fp8_peak)) / fp8_peak, 2)}
+               if fp8 else {}),
             "tokens_per_s": round(world * wl.batch * S * args.steps / total_s, 1),
             "clocks": clocks,
             "e2e": {"value": round(world * st.flops_blocks * args.steps / e2e_s / 1e12, 2), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_s / args.steps * 1e3, 4)},
             "gpu_launches": launches,
             "roofline": roofline,

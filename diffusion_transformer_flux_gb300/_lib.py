@@ -30,7 +30,8 @@ EXPORTED = [
     "mmdit_img_in_fwd", "mmdit_final_layer_workspace_size", "mmdit_final_layer_fwd",
     "mmdit_attention_workspace_size", "mmdit_attention_fwd", "mmdit_double_block_workspace_size",
     "mmdit_double_block_fwd", "mmdit_single_block_workspace_size", "mmdit_single_block_fwd",
-    "mmdit_block_workspace_offsets",
+    "mmdit_block_workspace_offsets", "mmdit_fp8_quantize_e4m3", "mmdit_fp8_linear_workspace_size",
+    "mmdit_fp8_linear_fwd",
 ]
 
 
@@ -56,8 +57,23 @@ class StreamW(C.Structure):
     _fields_ = [(n, C.c_void_p) for n in STREAM_W_FIELDS]
 
 
+class Fp8State(C.Structure):
+    _fields_ = [("amax_history", C.c_void_p), ("scale", C.c_void_p), ("hist_len", C.c_int32),
+                ("n_tensors", C.c_int32), ("pos", C.c_int32)]
+
+
+MMDIT_GEMM_NATIVE = 0
+MMDIT_GEMM_FP8_E4M3 = 1
+FP8_LINEARS = ("qkv", "o", "fc1", "fc2")
+
+
+def fp8_tensor(slot: int, linear: str, operand: str) -> int:
+    """Index of a tensor in the FP8 state: slot 0 image/single, 1 text; operand "x" or "w"."""
+    return 8 * slot + 2 * FP8_LINEARS.index(linear) + (1 if operand == "w" else 0)
+
+
 VP, SZ, I32, I64, F32 = C.c_void_p, C.c_size_t, C.c_int32, C.c_int64, C.c_float
-PDIMS, PW = C.POINTER(Dims), C.POINTER(StreamW)
+PDIMS, PW, PFP8 = C.POINTER(Dims), C.POINTER(StreamW), C.POINTER(Fp8State)
 
 _SIGS = {
     "mmdit_last_error": (C.c_char_p, []),
@@ -79,10 +95,13 @@ _SIGS = {
     "mmdit_attention_workspace_size": (SZ, [I32, I32, I32]),
     "mmdit_attention_fwd": (C.c_int, [I32, I32, I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_double_block_workspace_size": (SZ, [PDIMS]),
-    "mmdit_double_block_fwd": (C.c_int, [PDIMS, PW, PW, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_double_block_fwd": (C.c_int, [PDIMS, PW, PW, VP, VP, VP, VP, VP, VP, VP, PFP8, VP, SZ, VP]),
     "mmdit_single_block_workspace_size": (SZ, [PDIMS]),
-    "mmdit_single_block_fwd": (C.c_int, [PDIMS, PW, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_single_block_fwd": (C.c_int, [PDIMS, PW, VP, VP, VP, VP, VP, PFP8, VP, SZ, VP]),
     "mmdit_block_workspace_offsets": (I32, [PDIMS, I32, C.POINTER(I64), I32]),
+    "mmdit_fp8_quantize_e4m3": (C.c_int, [VP, I64, VP, VP, VP, VP]),
+    "mmdit_fp8_linear_workspace_size": (SZ, []),
+    "mmdit_fp8_linear_fwd": (C.c_int, [I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
 }
 
 _lib = None
@@ -282,30 +301,59 @@ def mmdit_single_block_workspace_size(dims: Dims) -> int:
 
 
 def mmdit_block_workspace_offsets(dims: Dims, single: bool) -> list:
-    out = (I64 * 10)()
-    n = load().mmdit_block_workspace_offsets(C.byref(dims), int(single), out, 10)
+    out = (I64 * 17)()
+    n = load().mmdit_block_workspace_offsets(C.byref(dims), int(single), out, 17)
     if n < 0:
         raise MMDitError(1, "bad dims")
     return list(out)[:n]
 
 
+def make_fp8_state(amax_history, scale, pos: int = 0) -> Fp8State:
+    """The C view of a delayed-scaling state: amax_history [n_tensors, hist_len] and scale
+    [n_tensors], fp32 device tensors the caller owns."""
+    n, h = amax_history.shape
+    return Fp8State(_ptr(amax_history), _ptr(scale), h, n, pos)
+
+
+def _fp8_arg(fp8):
+    return None if fp8 is None else C.byref(fp8)
+
+
 def mmdit_double_block_fwd(dims: Dims, w_img: dict, w_txt: dict, vec, rope_cos, rope_sin, x_img,
-                           x_txt, y_img, y_txt, ws=None, stream=None):
+                           x_txt, y_img, y_txt, ws=None, stream=None, fp8: Fp8State | None = None):
     if ws is None:
         ws = workspace(mmdit_double_block_workspace_size(dims), vec.device)
     wi, wt = make_stream_w(w_img), make_stream_w(w_txt)
     _check(load().mmdit_double_block_fwd(C.byref(dims), C.byref(wi), C.byref(wt), _ptr(vec),
                                          _ptr(rope_cos), _ptr(rope_sin), _ptr(x_img), _ptr(x_txt),
-                                         _ptr(y_img), _ptr(y_txt), None, _ptr(ws), ws.numel(),
-                                         _stream(stream)))
+                                         _ptr(y_img), _ptr(y_txt), _fp8_arg(fp8), _ptr(ws),
+                                         ws.numel(), _stream(stream)))
     return ws
 
 
-def mmdit_single_block_fwd(dims: Dims, w: dict, vec, rope_cos, rope_sin, x, y, ws=None, stream=None):
+def mmdit_single_block_fwd(dims: Dims, w: dict, vec, rope_cos, rope_sin, x, y, ws=None, stream=None,
+                           fp8: Fp8State | None = None):
     if ws is None:
         ws = workspace(mmdit_single_block_workspace_size(dims), vec.device)
     ww = make_stream_w(w)
     _check(load().mmdit_single_block_fwd(C.byref(dims), C.byref(ww), _ptr(vec), _ptr(rope_cos),
-                                         _ptr(rope_sin), _ptr(x), _ptr(y), None, _ptr(ws), ws.numel(),
-                                         _stream(stream)))
+                                         _ptr(rope_sin), _ptr(x), _ptr(y), _fp8_arg(fp8), _ptr(ws),
+                                         ws.numel(), _stream(stream)))
+    return ws
+
+
+def mmdit_fp8_quantize_e4m3(x, scale, amax, out, stream=None):
+    """out (uint8 E4M3 codes) = E4M3(x * scale); amax = max(amax, max|x|); x bf16."""
+    _check(load().mmdit_fp8_quantize_e4m3(_ptr(x), x.numel(), _ptr(scale), _ptr(amax), _ptr(out),
+                                          _stream(stream)))
+
+
+def mmdit_fp8_linear_fwd(x_q, w_q, scale_x, scale_w, b, y, ws=None, stream=None):
+    """y (bf16) = (x_q w_q^T) / (scale_x scale_w) + b on E4M3 codes x_q [M, K], w_q [N, K]."""
+    M, K = x_q.shape
+    N = w_q.shape[0]
+    if ws is None:
+        ws = workspace(load().mmdit_fp8_linear_workspace_size(), x_q.device)
+    _check(load().mmdit_fp8_linear_fwd(M, N, K, _ptr(x_q), _ptr(w_q), _ptr(scale_x), _ptr(scale_w),
+                                       _ptr(b), _ptr(y), _ptr(ws), ws.numel(), _stream(stream)))
     return ws

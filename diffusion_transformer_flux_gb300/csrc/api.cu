@@ -183,10 +183,19 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
 // ----------------------------------------------------------------------------- block planning
 struct BlockPlan {
   bool single;
+  bool fp8;  // E4M3 linears: h, u hold E4M3 codes; o8 and wq hold the cast attention output
+             // and weights
   int B, Si, St, S, S_pad, D, H, F;
   size_t elt;
   size_t mod[2], h[2], q, k, vt, o[2], x1[2], u[2];
+  size_t o8[2], wq[2];
   size_t total;
+  // byte offsets of the four weights inside a stream's wq slot
+  size_t wq_qkv() const { return 0; }
+  size_t wq_o() const { return static_cast<size_t>(3) * D * D; }
+  size_t wq_1() const { return static_cast<size_t>(4) * D * D; }
+  size_t wq_2() const { return static_cast<size_t>(4) * D * D + static_cast<size_t>(F) * D; }
+  size_t wq_bytes() const { return static_cast<size_t>(4) * D * D + static_cast<size_t>(2) * F * D; }
 };
 
 static bool plan_block(const mmdit_dims* d, bool single, BlockPlan* p) {
@@ -197,20 +206,24 @@ static bool plan_block(const mmdit_dims* d, bool single, BlockPlan* p) {
   p->S_pad = static_cast<int>(round_up(static_cast<size_t>(p->S), 8));
   p->D = d->hidden, p->H = d->heads, p->F = d->mlp_hidden;
   p->elt = elt_bytes(d->act);
+  p->fp8 = d->gemm == MMDIT_GEMM_FP8_E4M3;
+  const size_t mm_elt = p->fp8 ? 1 : p->elt;  // inputs of the QKV and fc1/fc2 linears
   Carver c;
   const size_t B = p->B, D = p->D, F = p->F, S = p->S;
   const size_t rows[2] = {B * (single ? S : static_cast<size_t>(p->Si)),
                           single ? 0 : B * static_cast<size_t>(p->St)};
   const int ns = single ? 1 : 2;
   for (int s = 0; s < 2; ++s) p->mod[s] = s < ns ? c.take(B * 6 * D * 4) : 0;
-  for (int s = 0; s < 2; ++s) p->h[s] = s < ns ? c.take(rows[s] * D * p->elt) : 0;
+  for (int s = 0; s < 2; ++s) p->h[s] = s < ns ? c.take(rows[s] * D * mm_elt) : 0;
   p->q = c.take(B * D * S * 2);
   p->k = c.take(B * D * S * 2);
   p->vt = c.take(B * D * static_cast<size_t>(p->S_pad) * 2);
   for (int s = 0; s < 2; ++s) p->o[s] = s < ns ? c.take(rows[s] * D * p->elt) : 0;
   // the in-block residual x1 stays fp32 so the output is rounded to the activation type once
   for (int s = 0; s < 2; ++s) p->x1[s] = s < ns ? c.take(rows[s] * D * 4) : 0;
-  for (int s = 0; s < 2; ++s) p->u[s] = s < ns ? c.take(rows[s] * F * p->elt) : 0;
+  for (int s = 0; s < 2; ++s) p->u[s] = s < ns ? c.take(rows[s] * F * mm_elt) : 0;
+  for (int s = 0; s < 2; ++s) p->o8[s] = p->fp8 && s < ns ? c.take(rows[s] * D) : 0;
+  for (int s = 0; s < 2; ++s) p->wq[s] = p->fp8 && s < ns ? c.take(p->wq_bytes()) : 0;
   p->total = c.off;
   return true;
 }
@@ -222,9 +235,13 @@ static mmdit_status check_dims(const mmdit_dims* d) {
                 d->seq_img, d->seq_txt);
   if (d->act != MMDIT_F32 && d->act != MMDIT_BF16)
     return fail(MMDIT_ERR_INVALID_ARG, "act must be MMDIT_F32 or MMDIT_BF16 (got %d)", d->act);
-  if (d->gemm == MMDIT_GEMM_FP8_E4M3)
-    return fail(MMDIT_ERR_UNSUPPORTED, "FP8 E4M3 linears are not implemented in this build");
-  if (d->gemm != MMDIT_GEMM_NATIVE) return fail(MMDIT_ERR_INVALID_ARG, "unknown gemm mode %d", d->gemm);
+  if (d->gemm != MMDIT_GEMM_NATIVE && d->gemm != MMDIT_GEMM_FP8_E4M3)
+    return fail(MMDIT_ERR_INVALID_ARG, "unknown gemm mode %d", d->gemm);
+  if (d->gemm == MMDIT_GEMM_FP8_E4M3 && d->act != MMDIT_BF16)
+    return fail(MMDIT_ERR_UNSUPPORTED, "FP8 E4M3 linears need bf16 activations (act = MMDIT_BF16)");
+  if (d->gemm == MMDIT_GEMM_FP8_E4M3 && d->mlp_hidden % 128 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "FP8 E4M3 linears need mlp_hidden %% 128 == 0 (got %d)",
+                d->mlp_hidden);
   if (d->head_dim != 128)
     return fail(MMDIT_ERR_UNSUPPORTED, "head_dim must be 128 (got %d)", d->head_dim);
   if (d->hidden > 6144)
@@ -263,6 +280,31 @@ static mmdit_status check_workspace(void* ws, size_t have, size_t need) {
     return fail(MMDIT_ERR_WORKSPACE, "workspace is not 256-byte aligned");
   if (have < need)
     return fail(MMDIT_ERR_WORKSPACE, "workspace too small: %zu bytes given, %zu needed", have, need);
+  return MMDIT_OK;
+}
+
+// Tensors of the FP8 state a block uses: per stream slot (0 image / single, 1 text), linear g
+// (0 QKV, 1 output projection, 2 fc1, 3 fc2) and operand (0 input, 1 weight), index
+// 8 * slot + 2 * g + operand.
+constexpr int kFp8TensorsPerStream = 8;
+inline int fp8_tensor(int slot, int g, int operand) { return kFp8TensorsPerStream * slot + 2 * g + operand; }
+
+static mmdit_status check_fp8(const mmdit_dims* d, const mmdit_fp8_state* f, int n_needed) {
+  if (d->gemm != MMDIT_GEMM_FP8_E4M3) {
+    if (f) return fail(MMDIT_ERR_INVALID_ARG, "fp8 state given but gemm mode is not MMDIT_GEMM_FP8_E4M3");
+    return MMDIT_OK;
+  }
+  if (!f) return fail(MMDIT_ERR_INVALID_ARG, "FP8 linears need an fp8 state (got NULL)");
+  if (!f->amax_history || !f->scale)
+    return fail(MMDIT_ERR_INVALID_ARG, "fp8 state: NULL amax_history or scale");
+  if ((reinterpret_cast<uintptr_t>(f->amax_history) & 3u) || (reinterpret_cast<uintptr_t>(f->scale) & 3u))
+    return fail(MMDIT_ERR_INVALID_ARG, "fp8 state: arrays must be 4-byte aligned");
+  if (f->hist_len < 1 || f->pos < 0 || f->pos >= f->hist_len)
+    return fail(MMDIT_ERR_INVALID_ARG, "fp8 state: need hist_len >= 1 and 0 <= pos < hist_len (got %d, %d)",
+                f->hist_len, f->pos);
+  if (f->n_tensors < n_needed)
+    return fail(MMDIT_ERR_INVALID_ARG, "fp8 state: %d tensors given, this block records %d",
+                f->n_tensors, n_needed);
   return MMDIT_OK;
 }
 
@@ -312,6 +354,14 @@ struct Streams {
   int rpb[2] = {0, 0};  // rows per batch element
 };
 
+// The FP8 state of one block call (f == nullptr when the linears are not FP8): where each
+// tensor's scale is read and where this call records its amax.
+struct Fp8 {
+  const mmdit_fp8_state* f = nullptr;
+  const float* scale(int t) const { return f->scale + t; }
+  float* amax(int t) const { return f->amax_history + static_cast<size_t>(t) * f->hist_len + f->pos; }
+};
+
 void add_problem(GemmProblem& g, int i, int M, const void* A, const void* W, const EpiArgs& ep) {
   if (i == 0)
     g.M = M, g.A = A, g.W = W, g.ep = ep;
@@ -320,22 +370,32 @@ void add_problem(GemmProblem& g, int i, int M, const void* A, const void* W, con
 }
 
 mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss, const float* cs,
-                     const float* sn, void* ws, cudaStream_t st) {
+                     const float* sn, const Fp8& f8, void* ws, cudaStream_t st) {
   {
     ProfScope ps_(p.single ? "single.ln1" : "double.ln1", st);
     LnModJob jobs[2];
     for (int i = 0; i < ss.n; ++i) {
       const float* mod = at<float>(ws, p.mod[ss.s[i]]);
       jobs[i] = {ss.x[i], mod, mod + p.D, 6 * p.D, at(ws, p.h[ss.s[i]]), p.B * ss.rpb[i], ss.rpb[i]};
+      if (f8.f) {
+        const int t = fp8_tensor(ss.s[i], 0, 0);
+        jobs[i].q_scale = f8.scale(t), jobs[i].q_amax = f8.amax(t);
+      }
     }
-    MMDIT_CUDA(launch_ln_modulate2(d->act, d->act == MMDIT_F32, jobs, ss.n, p.D, d->ln_eps, st),
+    MMDIT_CUDA(launch_ln_modulate2(d->act, d->act == MMDIT_F32, jobs, ss.n, p.D, d->ln_eps, st,
+                                   f8.f ? 1 : 0),
                "LayerNorm-modulate (attention branch)");
   }
   GemmProblem g;
-  g.act = d->act, g.epi = kEpiQkv, g.N = 3 * p.D, g.K = p.D;
+  g.act = f8.f ? 2 : d->act, g.epi = kEpiQkv, g.N = 3 * p.D, g.K = p.D;
   for (int i = 0; i < ss.n; ++i) {
     const mmdit_stream_w* w = ss.w[i];
     EpiArgs e;
+    const void* wmat = w->w_qkv;
+    if (f8.f) {
+      e.scale_a = f8.scale(fp8_tensor(ss.s[i], 0, 0)), e.scale_w = f8.scale(fp8_tensor(ss.s[i], 0, 1));
+      wmat = at(ws, p.wq[ss.s[i]] + p.wq_qkv());
+    }
     e.bias = w->b_qkv, e.g_q = w->g_q, e.g_k = w->g_k;
     e.rope_cos = cs, e.rope_sin = sn;
     e.q = at<__nv_bfloat16>(ws, p.q), e.k = at<__nv_bfloat16>(ws, p.k);
@@ -344,23 +404,47 @@ mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss,
     e.seq_offset = ss.s[i] == 0 ? 0 : p.Si;
     e.seq_joint = p.S, e.seq_pad = p.S_pad, e.heads = p.H, e.hidden = p.D;
     e.rms_eps = d->rms_eps, e.rope_interleaved = d->rope_interleaved ? 1 : 0;
-    add_problem(g, i, p.B * ss.rpb[i], at(ws, p.h[ss.s[i]]), w->w_qkv, e);
+    add_problem(g, i, p.B * ss.rpb[i], at(ws, p.h[ss.s[i]]), wmat, e);
   }
   ProfScope ps_(p.single ? "single.qkv" : "double.qkv", st);
   MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "QKV projection");
   return MMDIT_OK;
 }
 
-mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss, void* ws,
-                      cudaStream_t st) {
+mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss, const Fp8& f8,
+                      void* ws, cudaStream_t st) {
+  // the linears' operand type, and each stream's weight matrices as the GEMMs read them
+  const int mm = f8.f ? 2 : d->act;
+  auto weight = [&](int i, int g) -> const void* {
+    const mmdit_stream_w* w = ss.w[i];
+    if (!f8.f) return g == 1 ? w->w_o : (g == 2 ? w->w_1 : w->w_2);
+    const size_t off = g == 1 ? p.wq_o() : (g == 2 ? p.wq_1() : p.wq_2());
+    return at(ws, p.wq[ss.s[i]] + off);
+  };
+  auto dequant = [&](EpiArgs& e, int i, int g) {
+    if (!f8.f) return;
+    e.scale_a = f8.scale(fp8_tensor(ss.s[i], g, 0)), e.scale_w = f8.scale(fp8_tensor(ss.s[i], g, 1));
+  };
+  if (f8.f) {
+    // the attention output (bf16) cast to E4M3 for the output projection
+    ProfScope ps_(p.single ? "single.fp8_cast_o" : "double.fp8_cast_o", st);
+    QuantJob jobs[2];
+    for (int i = 0; i < ss.n; ++i) {
+      const int t = fp8_tensor(ss.s[i], 1, 0);
+      jobs[i] = {at<__nv_bfloat16>(ws, p.o[ss.s[i]]), at<uint8_t>(ws, p.o8[ss.s[i]]),
+                 static_cast<int64_t>(p.B) * ss.rpb[i] * p.D, f8.scale(t), f8.amax(t)};
+    }
+    MMDIT_CUDA(launch_quantize_e4m3(jobs, ss.n, st), "E4M3 cast of the attention output");
+  }
   GemmProblem g;
-  g.act = d->act, g.epi = kEpiGateResid, g.N = p.D, g.K = p.D;
+  g.act = mm, g.epi = kEpiGateResid, g.N = p.D, g.K = p.D;
   for (int i = 0; i < ss.n; ++i) {
     const float* mod = at<float>(ws, p.mod[ss.s[i]]);
     EpiArgs e;
     e.bias = ss.w[i]->b_o, e.resid = ss.x[i], e.gate = mod + 2 * p.D, e.gate_bstride = 6 * p.D;
     e.rows_per_batch = ss.rpb[i], e.out = at(ws, p.x1[ss.s[i]]), e.out_f32 = 1;
-    add_problem(g, i, p.B * ss.rpb[i], at(ws, p.o[ss.s[i]]), ss.w[i]->w_o, e);
+    dequant(e, i, 1);
+    add_problem(g, i, p.B * ss.rpb[i], at(ws, f8.f ? p.o8[ss.s[i]] : p.o[ss.s[i]]), weight(i, 1), e);
   }
   {
     ProfScope ps_(p.single ? "single.out" : "double.out", st);
@@ -373,32 +457,77 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
       const float* mod = at<float>(ws, p.mod[ss.s[i]]);
       jobs[i] = {at(ws, p.x1[ss.s[i]]), mod + 3 * p.D, mod + 4 * p.D, 6 * p.D, at(ws, p.h[ss.s[i]]),
                  p.B * ss.rpb[i], ss.rpb[i]};
+      if (f8.f) {
+        const int t = fp8_tensor(ss.s[i], 2, 0);
+        jobs[i].q_scale = f8.scale(t), jobs[i].q_amax = f8.amax(t);
+      }
     }
-    MMDIT_CUDA(launch_ln_modulate2(d->act, 1, jobs, ss.n, p.D, d->ln_eps, st),
+    MMDIT_CUDA(launch_ln_modulate2(d->act, 1, jobs, ss.n, p.D, d->ln_eps, st, f8.f ? 1 : 0),
                "LayerNorm-modulate (MLP branch)");
   }
   GemmProblem f1;
-  f1.act = d->act, f1.epi = kEpiGelu, f1.N = p.F, f1.K = p.D;
+  f1.act = mm, f1.epi = f8.f ? kEpiGeluF8 : kEpiGelu, f1.N = p.F, f1.K = p.D;
   for (int i = 0; i < ss.n; ++i) {
     EpiArgs e;
     e.bias = ss.w[i]->b_1, e.gelu_tanh = d->gelu_tanh, e.out = at(ws, p.u[ss.s[i]]);
-    add_problem(f1, i, p.B * ss.rpb[i], at(ws, p.h[ss.s[i]]), ss.w[i]->w_1, e);
+    dequant(e, i, 2);
+    if (f8.f) {
+      const int t = fp8_tensor(ss.s[i], 3, 0);  // GELU output = the input of fc2
+      e.out_scale = f8.scale(t), e.out_amax = f8.amax(t);
+    }
+    add_problem(f1, i, p.B * ss.rpb[i], at(ws, p.h[ss.s[i]]), weight(i, 2), e);
   }
   {
     ProfScope ps_(p.single ? "single.fc1" : "double.fc1", st);
     MMDIT_CUDA(launch_gemm(f1, status_word(ws), st), "MLP fc1 + GELU");
   }
   GemmProblem f2;
-  f2.act = d->act, f2.epi = kEpiGateResid, f2.N = p.D, f2.K = p.F;
+  f2.act = mm, f2.epi = kEpiGateResid, f2.N = p.D, f2.K = p.F;
   for (int i = 0; i < ss.n; ++i) {
     const float* mod = at<float>(ws, p.mod[ss.s[i]]);
     EpiArgs e;
     e.bias = ss.w[i]->b_2, e.resid = at(ws, p.x1[ss.s[i]]), e.resid_f32 = 1, e.gate = mod + 5 * p.D;
     e.gate_bstride = 6 * p.D, e.rows_per_batch = ss.rpb[i], e.out = ss.y[i];
-    add_problem(f2, i, p.B * ss.rpb[i], at(ws, p.u[ss.s[i]]), ss.w[i]->w_2, e);
+    dequant(e, i, 3);
+    add_problem(f2, i, p.B * ss.rpb[i], at(ws, p.u[ss.s[i]]), weight(i, 3), e);
   }
   ProfScope ps_(p.single ? "single.fc2" : "double.fc2", st);
   MMDIT_CUDA(launch_gemm(f2, status_word(ws), st), "MLP fc2 + gated residual");
+  return MMDIT_OK;
+}
+
+// FP8 calls: zero this call's amax slot of every tensor the block records, then cast all weights
+// of the block's streams to E4M3 in one launch.
+mmdit_status fp8_begin(const BlockPlan& p, const Streams& ss, const Fp8& f8, int n_tensors,
+                       void* ws, cudaStream_t st) {
+  ProfScope ps_(p.single ? "single.fp8_cast_w" : "double.fp8_cast_w", st);
+  MMDIT_CUDA(launch_amax_reset(f8.f->amax_history, f8.f->hist_len, n_tensors, f8.f->pos, st),
+             "FP8 amax slot reset");
+  QuantJob jobs[kQuantMaxJobs];
+  int n = 0;
+  for (int i = 0; i < ss.n; ++i) {
+    const mmdit_stream_w* w = ss.w[i];
+    const int slot = ss.s[i];
+    const void* src[4] = {w->w_qkv, w->w_o, w->w_1, w->w_2};
+    const size_t off[4] = {p.wq_qkv(), p.wq_o(), p.wq_1(), p.wq_2()};
+    const int64_t cnt[4] = {static_cast<int64_t>(3) * p.D * p.D, static_cast<int64_t>(p.D) * p.D,
+                            static_cast<int64_t>(p.F) * p.D, static_cast<int64_t>(p.D) * p.F};
+    for (int g = 0; g < 4; ++g) {
+      const int t = fp8_tensor(slot, g, 1);
+      jobs[n++] = {static_cast<const __nv_bfloat16*>(src[g]), at<uint8_t>(ws, p.wq[slot] + off[g]), cnt[g],
+                   f8.scale(t), f8.amax(t)};
+    }
+  }
+  MMDIT_CUDA(launch_quantize_e4m3(jobs, n, st), "E4M3 cast of the weights");
+  return MMDIT_OK;
+}
+
+// FP8 calls: the next call's scales from the amax this call recorded (most_recent, margin 0).
+mmdit_status fp8_end(const BlockPlan& p, const Fp8& f8, int n_tensors, cudaStream_t st) {
+  ProfScope ps_(p.single ? "single.fp8_scale" : "double.fp8_scale", st);
+  MMDIT_CUDA(launch_scale_update(f8.f->amax_history, f8.f->scale, f8.f->hist_len, n_tensors, f8.f->pos,
+                                 0, st),
+             "FP8 scale update");
   return MMDIT_OK;
 }
 
@@ -701,12 +830,14 @@ int32_t mmdit_block_workspace_offsets(const mmdit_dims* d, int32_t single, int64
   BlockPlan p;
   if (!out || check_dims(d) != MMDIT_OK || !plan_block(d, single != 0, &p)) return -1;
   const int64_t none = -1;
-  const int64_t v[10] = {static_cast<int64_t>(p.mod[0]), single ? none : static_cast<int64_t>(p.mod[1]),
-                         static_cast<int64_t>(p.q), static_cast<int64_t>(p.k), static_cast<int64_t>(p.vt),
-                         static_cast<int64_t>(p.o[0]), single ? none : static_cast<int64_t>(p.o[1]),
-                         static_cast<int64_t>(p.x1[0]), single ? none : static_cast<int64_t>(p.x1[1]),
-                         static_cast<int64_t>(p.u[0])};
-  const int m = n < 10 ? n : 10;
+  auto two = [&](size_t off, int s) { return (single && s == 1) ? none : static_cast<int64_t>(off); };
+  auto f8 = [&](size_t off, int s) { return p.fp8 ? two(off, s) : none; };
+  const int64_t v[17] = {two(p.mod[0], 0), two(p.mod[1], 1), static_cast<int64_t>(p.q),
+                         static_cast<int64_t>(p.k), static_cast<int64_t>(p.vt), two(p.o[0], 0),
+                         two(p.o[1], 1), two(p.x1[0], 0), two(p.x1[1], 1), two(p.u[0], 0),
+                         two(p.h[0], 0), two(p.h[1], 1), two(p.u[1], 1), f8(p.o8[0], 0),
+                         f8(p.o8[1], 1), f8(p.wq[0], 0), f8(p.wq[1], 1)};
+  const int m = n < 17 ? n : 17;
   for (int i = 0; i < m; ++i) out[i] = v[i];
   return m;
 }
@@ -718,7 +849,7 @@ mmdit_status mmdit_double_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
                                     void* workspace, size_t workspace_bytes, void* stream) {
   mmdit_status s = check_dims(d);
   if (s != MMDIT_OK) return s;
-  if (fp8) return fail(MMDIT_ERR_UNSUPPORTED, "fp8 state given but FP8 linears are not implemented");
+  if ((s = check_fp8(d, fp8, 2 * kFp8TensorsPerStream)) != MMDIT_OK) return s;
   if ((s = check_stream_w(w_img, "image weights")) != MMDIT_OK) return s;
   if ((s = check_stream_w(w_txt, "text weights")) != MMDIT_OK) return s;
   if ((s = check_ptrs({vec, rope_cos, rope_sin}, "double block conditioning")) != MMDIT_OK) return s;
@@ -749,9 +880,14 @@ mmdit_status mmdit_double_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
       ss.rpb[ss.n] = rpb[i];
       ++ss.n;
     }
-  if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, workspace, st)) != MMDIT_OK) return s;
+  Fp8 f8;
+  f8.f = fp8;
+  const int n_tensors = 2 * kFp8TensorsPerStream;
+  if (fp8 && (s = fp8_begin(p, ss, f8, n_tensors, workspace, st)) != MMDIT_OK) return s;
+  if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, f8, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
-  return run_post(d, p, ss, workspace, st);
+  if ((s = run_post(d, p, ss, f8, workspace, st)) != MMDIT_OK) return s;
+  return fp8 ? fp8_end(p, f8, n_tensors, st) : MMDIT_OK;
 }
 
 mmdit_status mmdit_single_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w, const void* vec,
@@ -760,7 +896,7 @@ mmdit_status mmdit_single_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
                                     size_t workspace_bytes, void* stream) {
   mmdit_status s = check_dims(d);
   if (s != MMDIT_OK) return s;
-  if (fp8) return fail(MMDIT_ERR_UNSUPPORTED, "fp8 state given but FP8 linears are not implemented");
+  if ((s = check_fp8(d, fp8, kFp8TensorsPerStream)) != MMDIT_OK) return s;
   if ((s = check_stream_w(w, "single-block weights")) != MMDIT_OK) return s;
   if ((s = check_ptrs({vec, rope_cos, rope_sin, x, y}, "single block")) != MMDIT_OK) return s;
   if (static_cast<int64_t>(d->batch) * d->heads > 65535)
@@ -778,9 +914,55 @@ mmdit_status mmdit_single_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
   }
   Streams ss;
   ss.n = 1, ss.s[0] = 0, ss.w[0] = w, ss.x[0] = x, ss.y[0] = y, ss.rpb[0] = p.S;
-  if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, workspace, st)) != MMDIT_OK) return s;
+  Fp8 f8;
+  f8.f = fp8;
+  if (fp8 && (s = fp8_begin(p, ss, f8, kFp8TensorsPerStream, workspace, st)) != MMDIT_OK) return s;
+  if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, f8, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
-  return run_post(d, p, ss, workspace, st);
+  if ((s = run_post(d, p, ss, f8, workspace, st)) != MMDIT_OK) return s;
+  return fp8 ? fp8_end(p, f8, kFp8TensorsPerStream, st) : MMDIT_OK;
+}
+
+mmdit_status mmdit_fp8_quantize_e4m3(const void* x, int64_t n, const float* scale, float* amax,
+                                     void* out, void* stream) {
+  if (n < 0) return fail(MMDIT_ERR_INVALID_ARG, "negative element count");
+  if (n % 16 != 0) return fail(MMDIT_ERR_UNSUPPORTED, "n must be a multiple of 16 (got %lld)",
+                               static_cast<long long>(n));
+  if (n == 0) return MMDIT_OK;
+  mmdit_status s = check_ptrs({x, out}, "E4M3 cast");
+  if (s != MMDIT_OK) return s;
+  if (!scale || !amax) return fail(MMDIT_ERR_INVALID_ARG, "E4M3 cast: NULL scale or amax");
+  if ((reinterpret_cast<uintptr_t>(scale) & 3u) || (reinterpret_cast<uintptr_t>(amax) & 3u))
+    return fail(MMDIT_ERR_INVALID_ARG, "E4M3 cast: scale and amax must be 4-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const QuantJob job{static_cast<const __nv_bfloat16*>(x), static_cast<uint8_t*>(out), n, scale, amax};
+  ProfScope ps_("fp8_quantize", st);
+  MMDIT_CUDA(launch_quantize_e4m3(&job, 1, st), "E4M3 cast");
+  return MMDIT_OK;
+}
+
+size_t mmdit_fp8_linear_workspace_size(void) { return kStatusBytes; }
+
+mmdit_status mmdit_fp8_linear_fwd(int32_t M, int32_t N, int32_t K, const void* x, const void* w,
+                                  const float* scale_x, const float* scale_w, const void* b, void* y,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 0 || N < 1 || K < 1) return fail(MMDIT_ERR_INVALID_ARG, "bad FP8 linear shape");
+  if (N % 128 != 0 || K % 16 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "FP8 linear needs N %% 128 == 0 and K %% 16 == 0 (got %d, %d)", N, K);
+  mmdit_status s = check_ptrs({x, w, y}, "FP8 linear");
+  if (s != MMDIT_OK) return s;
+  if (b && !aligned16(b)) return fail(MMDIT_ERR_INVALID_ARG, "FP8 linear: bias is not 16-byte aligned");
+  if (!scale_x || !scale_w) return fail(MMDIT_ERR_INVALID_ARG, "FP8 linear: NULL scale");
+  if ((s = check_workspace(workspace, workspace_bytes, kStatusBytes)) != MMDIT_OK) return s;
+  if (M == 0) return MMDIT_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  GemmProblem g;
+  g.act = 2, g.epi = kEpiBias, g.M = M, g.N = N, g.K = K, g.A = x, g.W = w;
+  g.ep.bias = b, g.ep.out = y, g.ep.scale_a = scale_x, g.ep.scale_w = scale_w;
+  ProfScope ps_("fp8_linear", st);
+  MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "FP8 linear");
+  return MMDIT_OK;
 }
 
 }  // extern "C"

@@ -374,6 +374,33 @@ __device__ __forceinline__ void store32(float* p, const float (&v)[32]) {
 }
 
 
+// ----------------------------------------------------------------------------- E4M3
+// Two floats -> two E4M3 codes (round to nearest even, saturating to +-448; NaN stays NaN),
+// `lo` in the low byte so that the pair is stored in element order.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Eight floats, each multiplied by `s`, as eight E4M3 codes in element order.
+__device__ __forceinline__ uint2 e4m3x8(const float* v, float s) {
+  uint2 u;
+  u.x = e4m3x2(v[0] * s, v[1] * s) | (e4m3x2(v[2] * s, v[3] * s) << 16);
+  u.y = e4m3x2(v[4] * s, v[5] * s) | (e4m3x2(v[6] * s, v[7] * s) << 16);
+  return u;
+}
+// Raises the non-negative float at `p` to at least `v` (non-negative floats order like their
+// bit patterns).  The plain read first skips the atomic when another thread already wrote more.
+__device__ __forceinline__ void atomic_max_nonneg(float* p, float v) {
+  if (!(v > *reinterpret_cast<volatile float*>(p))) return;
+  atomicMax(reinterpret_cast<int*>(p), __float_as_int(v));
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
 // Two 32-column tcgen05.ld's followed by one wait (both arrays threaded through the wait).
 __device__ __forceinline__ void tmem_ld64_wait(uint32_t taddr, uint32_t (&a)[32], uint32_t (&b)[32]) {
   tmem_ld32(taddr, a);

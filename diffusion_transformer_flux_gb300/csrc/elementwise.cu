@@ -170,6 +170,8 @@ struct LnJob {
   void* out;
   int rows;
   int rpb;
+  const float* q_scale;  // E4M3 output only
+  float* q_amax;
 };
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
@@ -224,6 +226,10 @@ __global__ void __launch_bounds__(kLnThreads) ln_modulate_kernel(LnJob j0, LnJob
   const float* sh = job.shift + b * job.mod_bstride;
   const float* sc = job.scale + b * job.mod_bstride;
   T* orow = static_cast<T*>(job.out) + static_cast<size_t>(r) * dim;
+  // E4M3 output (T = uint8_t): codes of the result times the tensor's scale, and its amax
+  constexpr bool kE4m3 = std::is_same<T, uint8_t>::value;
+  const float qs = kE4m3 ? __ldg(job.q_scale) : 1.f;
+  float amax = 0.f;
 #pragma unroll
   for (int c = 0; c < NCT; ++c) {
     const int k = (c * kLnThreads + threadIdx.x) * 8;
@@ -234,8 +240,18 @@ __global__ void __launch_bounds__(kLnThreads) ln_modulate_kernel(LnJob j0, LnJob
       load8(sc + k, m);
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = fmaf((v[e] - mean) * rstd, 1.f + m[e], a[e]);
-      store8(orow + k, v);
+      if constexpr (kE4m3) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
+        *reinterpret_cast<uint2*>(orow + k) = e4m3x8(v, qs);
+      } else {
+        store8(orow + k, v);
+      }
     }
+  }
+  if constexpr (kE4m3) {
+    amax = warp_max(amax);
+    if ((threadIdx.x & 31) == 0 && amax > 0.f) atomic_max_nonneg(job.q_amax, amax);
   }
 }
 
@@ -479,20 +495,26 @@ cudaError_t launch_modulation(int act, const void* vec, const void* w, const voi
 }
 
 cudaError_t launch_ln_modulate2(int act, int x_f32, const LnModJob* jobs, int njobs, int dim,
-                                float eps, cudaStream_t stream) {
-  LnJob j[2] = {{nullptr, nullptr, nullptr, 0, nullptr, 0, 1}, {nullptr, nullptr, nullptr, 0, nullptr, 0, 1}};
+                                float eps, cudaStream_t stream, int out_e4m3) {
+  LnJob j[2] = {{nullptr, nullptr, nullptr, 0, nullptr, 0, 1, nullptr, nullptr},
+                {nullptr, nullptr, nullptr, 0, nullptr, 0, 1, nullptr, nullptr}};
   int rows = 0;
   for (int i = 0; i < njobs && i < 2; ++i) {
     j[i] = {jobs[i].x, jobs[i].shift, jobs[i].scale, jobs[i].mod_bstride, jobs[i].out, jobs[i].rows,
-            jobs[i].rows_per_batch};
+            jobs[i].rows_per_batch, jobs[i].q_scale, jobs[i].q_amax};
     rows += jobs[i].rows;
   }
+  if (out_e4m3 && act != 1) return cudaErrorInvalidValue;
   if (rows == 0) return cudaSuccess;
   const int chunks = (dim + kLnThreads * 8 - 1) / (kLnThreads * 8);
   if (chunks > kLnMaxChunks) return cudaErrorInvalidValue;
   auto go = [&](auto nct_tag) {
     constexpr int NCT = decltype(nct_tag)::value;
-    if (act == 1 && x_f32)
+    if (out_e4m3 && x_f32)
+      ln_modulate_kernel<float, uint8_t, NCT><<<rows, kLnThreads, 0, stream>>>(j[0], j[1], dim, eps);
+    else if (out_e4m3)
+      ln_modulate_kernel<__nv_bfloat16, uint8_t, NCT><<<rows, kLnThreads, 0, stream>>>(j[0], j[1], dim, eps);
+    else if (act == 1 && x_f32)
       ln_modulate_kernel<float, __nv_bfloat16, NCT><<<rows, kLnThreads, 0, stream>>>(j[0], j[1], dim, eps);
     else if (act == 1)
       ln_modulate_kernel<__nv_bfloat16, __nv_bfloat16, NCT><<<rows, kLnThreads, 0, stream>>>(j[0], j[1], dim, eps);

@@ -1,0 +1,30 @@
+// gemm_fp8.cu -- E4M3 instantiations of the tcgen05 GEMM (kind::f8f6f4, fp32 accumulation).
+// Operands are E4M3 codes of x * scale_x and W * scale_w ("FP8 training for Flux models",
+// §Configuration, FP8 model configuration); the epilogue first divides the accumulator by
+// scale_x * scale_w, then applies the bf16 epilogue of the linear it replaces.
+#include "gemm_kernel.cuh"
+
+namespace mmdit {
+cudaError_t launch_gemm_fp8(const GemmProblem& p, uint32_t* status, cudaStream_t stream) {
+  if (p.N % 128 != 0 || p.K % 16 != 0) return cudaErrorInvalidValue;
+  if (!p.ep.scale_a || !p.ep.scale_w || (p.M1 > 0 && (!p.ep1.scale_a || !p.ep1.scale_w)))
+    return cudaErrorInvalidValue;
+  const bool wide = p.N % 256 == 0;
+  switch (p.epi) {
+    case kEpiQkv:
+      if (wide && p.ep.hidden % 256 == 0) return run_gemm<kKindF8, 256, kEpiQkv>(p, status, stream);
+      return run_gemm<kKindF8, 128, kEpiQkv>(p, status, stream);
+    case kEpiGateResid:
+      return wide ? run_gemm<kKindF8, 256, kEpiGateResid>(p, status, stream)
+                  : run_gemm<kKindF8, 128, kEpiGateResid>(p, status, stream);
+    case kEpiGeluF8:
+      return wide ? run_gemm<kKindF8, 256, kEpiGeluF8>(p, status, stream)
+                  : run_gemm<kKindF8, 128, kEpiGeluF8>(p, status, stream);
+    case kEpiBias:
+      return wide ? run_gemm<kKindF8, 256, kEpiBias>(p, status, stream)
+                  : run_gemm<kKindF8, 128, kEpiBias>(p, status, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+}  // namespace mmdit

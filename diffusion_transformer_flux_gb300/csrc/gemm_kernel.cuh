@@ -22,24 +22,33 @@ constexpr int kBM = 128;
 // one for the others (whose epilogues hide under the main loop already).
 template <int EPI>
 struct EpiGroups {
-  static constexpr int value = EPI == kEpiGelu ? 2 : 1;
+  static constexpr int value = (EPI == kEpiGelu || EPI == kEpiGeluF8) ? 2 : 1;
 };
 template <int EPI>
 constexpr int gemm_threads() {
   return 64 + 128 * EpiGroups<EPI>::value;
 }
 
+// Operand element size and the element type of the epilogue's bias, residual and output.
 template <int KIND>
 struct KindTraits;
 template <>
 struct KindTraits<kKindF16> {
-  using T = __nv_bfloat16;
+  using TE = __nv_bfloat16;
   static constexpr int kEltBytes = 2;
+  static constexpr CUtensorMapDataType kMapType = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
 };
 template <>
 struct KindTraits<kKindTF32> {
-  using T = float;
+  using TE = float;
   static constexpr int kEltBytes = 4;
+  static constexpr CUtensorMapDataType kMapType = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+};
+template <>
+struct KindTraits<kKindF8> {  // E4M3 operands, bf16 activations around them
+  using TE = __nv_bfloat16;
+  static constexpr int kEltBytes = 1;
+  static constexpr CUtensorMapDataType kMapType = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 };
 
 template <int BN>
@@ -73,10 +82,12 @@ __device__ __forceinline__ void tmem_load_f32(uint32_t taddr, float (&v)[32]) {
 // Row-wise epilogue of one 128 x BN accumulator tile.  `m` is this thread's output row, `n0`
 // the tile's first column.  All 32 lanes of the warp must call this (tcgen05.ld is collective).
 // `group` selects which part of the tile's columns (or heads) this warp handles.
-template <typename T, int BN, int EPI>
+// With DEQ (E4M3 operands) the accumulator is multiplied by 1 / (scale_a * scale_w) first.
+template <typename T, int BN, int EPI, bool DEQ>
 __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, int n0, int M, int N,
                                               const EpiArgs& ep) {
   const bool row_ok = m < M;
+  const float dq = DEQ ? 1.f / (__ldg(ep.scale_a) * __ldg(ep.scale_w)) : 1.f;
   if constexpr (EPI == kEpiQkv) {
     // BN covers whole heads (128 columns each); q|k|v blocks are `hidden` columns wide.
     const int b = row_ok ? m / ep.rows_per_batch : 0;
@@ -96,6 +107,10 @@ __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, 
         for (int i = 0; i < 32; ++i) v[c * 32 + i] = t[i];
       }
       if (!row_ok) continue;
+      if constexpr (DEQ) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) v[i] *= dq;
+      }
       if (ep.bias) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -164,15 +179,19 @@ __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, 
       }
     }
   } else {
-#pragma unroll 1
     constexpr int kChunks = BN / 32;
     constexpr int kPer = (kChunks + EpiGroups<EPI>::value - 1) / EpiGroups<EPI>::value;
+    float amax = 0.f;  // kEpiGeluF8: largest |GELU(.)| this thread wrote
     for (int c = group * kPer; c < (group + 1) * kPer && c < kChunks; ++c) {
       const int n = n0 + c * 32;
       if (n >= N) break;  // uniform across the warp
       float v[32];
       tmem_load_f32(taddr + c * 32, v);
       if (!row_ok) continue;
+      if constexpr (DEQ) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= dq;
+      }
       if constexpr (EPI == kEpiPartial) {
         store32(reinterpret_cast<float*>(ep.out) + static_cast<size_t>(m) * N + n, v);
         continue;
@@ -183,8 +202,7 @@ __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, 
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] += bb[i];
       }
-      if constexpr (EPI == kEpiGelu) {
-#pragma unroll
+      if constexpr (EPI == kEpiGelu || EPI == kEpiGeluF8) {
         // the variant is chosen once per chunk so the 32 evaluations interleave
         if (ep.gelu_tanh) {
 #pragma unroll
@@ -205,7 +223,17 @@ __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, 
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = fmaf(g[i], v[i], x[i]);
       }
-      if constexpr (EPI == kEpiUnpatchify) {
+      if constexpr (EPI == kEpiGeluF8) {
+        const float qs = __ldg(ep.out_scale);
+        uint2 u[4];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) u[i] = e4m3x8(v + 8 * i, qs);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(ep.out) + static_cast<size_t>(m) * N + n);
+        dst[0] = make_uint4(u[0].x, u[0].y, u[1].x, u[1].y);
+        dst[1] = make_uint4(u[2].x, u[2].y, u[3].x, u[3].y);
+      } else if constexpr (EPI == kEpiUnpatchify) {
         const int b = m / ep.rows_per_batch, s = m % ep.rows_per_batch;
         float* dst = reinterpret_cast<float*>(ep.out) +
                      (static_cast<size_t>(b) * N + n) * ep.rows_per_batch + s;
@@ -216,6 +244,10 @@ __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, 
       } else {
         store32(reinterpret_cast<T*>(ep.out) + static_cast<size_t>(m) * N + n, v);
       }
+    }
+    if constexpr (EPI == kEpiGeluF8) {
+      amax = warp_max(amax);
+      if ((threadIdx.x & 31) == 0 && amax > 0.f) atomic_max_nonneg(ep.out_amax, amax);
     }
   }
 }
@@ -229,7 +261,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
                    int M0, int M1, int N, int K, int splits, const __grid_constant__ EpiArgs ep0,
                    const __grid_constant__ EpiArgs ep1, uint32_t* status) {
   using Cfg = GemmCfg<BN>;
-  using T = typename KindTraits<KIND>::T;
+  using TE = typename KindTraits<KIND>::TE;
   constexpr int kBK = 128 / KindTraits<KIND>::kEltBytes;     // elements per 128-byte K slice
   constexpr int kUmmaK = 32 / KindTraits<KIND>::kEltBytes;   // K of one tcgen05.mma
   constexpr int kKSteps = kBK / kUmmaK;
@@ -385,7 +417,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       if constexpr (EPI == kEpiPartial)
         ep.out = reinterpret_cast<float*>(ep.out) +
                  static_cast<size_t>(tile / tiles) * static_cast<size_t>(prob ? M1 : M0) * N;
-      gemm_epilogue<T, BN, EPI>(group, taddr, mb * kBM + row, nb * BN, prob ? M1 : M0, N, ep);
+      gemm_epilogue<TE, BN, EPI, KIND == kKindF8>(group, taddr, mb * kBM + row, nb * BN,
+                                                  prob ? M1 : M0, N, ep);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       if (++acc == 2) acc = 0, acc_phase ^= 1;
@@ -405,8 +438,7 @@ cudaError_t run_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream
   using Cfg = GemmCfg<BN>;
   constexpr int kElt = KindTraits<KIND>::kEltBytes;
   constexpr int kBK = 128 / kElt;
-  const CUtensorMapDataType dt =
-      KIND == kKindF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUtensorMapDataType dt = KindTraits<KIND>::kMapType;
   const bool two = p.M1 > 0;
   CUtensorMap ta0, tb0, ta1, tb1;
   const uint64_t stride[1] = {static_cast<uint64_t>(p.K) * kElt};

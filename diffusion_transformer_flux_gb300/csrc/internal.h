@@ -17,7 +17,8 @@ enum EpiKind : int {
   kEpiGateResid = 2,  // out[m, n] = resid[m, n] + gate[b(m), n] * (acc + bias[n])
   kEpiQkv = 3,        // bias, per-head RMSNorm of q and k, RoPE, scatter to Q, K, Vt
   kEpiUnpatchify = 4, // pred[b, n, s] (fp32) = acc + bias[n], m = b * rows_per_batch + s
-  kEpiPartial = 5     // split-K: partial[split][m][n] (fp32) = acc over the split's K range
+  kEpiPartial = 5,    // split-K: partial[split][m][n] (fp32) = acc over the split's K range
+  kEpiGeluF8 = 6      // out[m, n] (E4M3) = GELU(acc + bias[n]) * out_scale, amax recorded
 };
 
 struct EpiArgs {
@@ -45,10 +46,18 @@ struct EpiArgs {
   int hidden = 0;
   float rms_eps = 1e-6f;
   int rope_interleaved = 1;
+  // E4M3 operands: the accumulator is first multiplied by 1 / (scale_a[0] * scale_w[0]), the
+  // scales the operands were cast with
+  const float* scale_a = nullptr;
+  const float* scale_w = nullptr;
+  // kEpiGeluF8: `out` receives E4M3 codes of GELU(.) * out_scale[0]; out_amax[0] is raised to
+  // the largest |GELU(.)| of the tile
+  const float* out_scale = nullptr;
+  float* out_amax = nullptr;
 };
 
 struct GemmProblem {
-  int act = 1;           // 0 = fp32 operands (tf32 MMA), 1 = bf16
+  int act = 1;           // 0 = fp32 operands (tf32 MMA), 1 = bf16, 2 = E4M3 (epilogue I/O bf16)
   int epi = kEpiBias;
   int M = 0, N = 0, K = 0;
   const void* A = nullptr;  // [M, K]
@@ -80,11 +89,15 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
                  const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                  CUtensorMapSwizzle swizzle);
 
-// gemm_bf16.cu / gemm_tf32.cu
+// gemm_bf16.cu / gemm_tf32.cu / gemm_fp8.cu
 cudaError_t launch_gemm_bf16(const GemmProblem& p, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_gemm_tf32(const GemmProblem& p, uint32_t* status, cudaStream_t stream);
+// E4M3 operands (K a multiple of 16, N a multiple of 128); epilogues kEpiBias, kEpiQkv,
+// kEpiGateResid and kEpiGeluF8, with scale_a / scale_w set in every EpiArgs.
+cudaError_t launch_gemm_fp8(const GemmProblem& p, uint32_t* status, cudaStream_t stream);
 inline cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream) {
-  return p.act == 1 ? launch_gemm_bf16(p, status, stream) : launch_gemm_tf32(p, status, stream);
+  return p.act == 2 ? launch_gemm_fp8(p, status, stream)
+                    : (p.act == 1 ? launch_gemm_bf16(p, status, stream) : launch_gemm_tf32(p, status, stream));
 }
 
 // attention.cu: O = softmax(Q K^T / sqrt(128)) V per (b, h); rows [0, split) of each batch go
@@ -129,9 +142,13 @@ struct LnModJob {
   void* out;
   int rows;
   int rows_per_batch;
+  // E4M3 output (out_e4m3 != 0 in the launch): out holds codes of the result * q_scale[0], and
+  // q_amax[0] is raised to the largest |result|
+  const float* q_scale = nullptr;
+  float* q_amax = nullptr;
 };
 cudaError_t launch_ln_modulate2(int act, int x_f32, const LnModJob* jobs, int njobs, int dim, float eps,
-                                cudaStream_t stream);
+                                cudaStream_t stream, int out_e4m3 = 0);
 // z [B, C, HW] fp32 -> tokens [B, HW, C] of the activation type.
 cudaError_t launch_patchify(int act, const float* z, int batch, int channels, int hw, void* out,
                             cudaStream_t stream);
@@ -143,6 +160,23 @@ cudaError_t launch_transpose_v(const __nv_bfloat16* v, int bh, int seq, int seq_
 cudaError_t launch_splitk_reduce(int act, const float* partials, int splits, int M, int N,
                                  const void* bias, void* out, int unpatchify_rows,
                                  cudaStream_t stream);
+// fp8.cu: E4M3 casts with delayed per-tensor scaling.
+// dst[i] = E4M3(src[i] * scale[0]) (round to nearest even, saturating), and amax[0] is raised to
+// max |src[i]|; n a multiple of 16, src and dst 16-byte aligned.
+struct QuantJob {
+  const __nv_bfloat16* src;
+  uint8_t* dst;
+  int64_t n;
+  const float* scale;
+  float* amax;
+};
+constexpr int kQuantMaxJobs = 8;
+cudaError_t launch_quantize_e4m3(const QuantJob* jobs, int njobs, cudaStream_t stream);
+// hist[i * hist_len + pos] = 0 for i < n.
+cudaError_t launch_amax_reset(float* hist, int hist_len, int n, int pos, cudaStream_t stream);
+// scale[i] = 448 / hist[i * hist_len + pos] / 2^margin where that amax is positive and finite.
+cudaError_t launch_scale_update(const float* hist, float* scale, int hist_len, int n, int pos,
+                                int margin, cudaStream_t stream);
 // Rectified-flow noise and loss.
 int flow_partial_blocks(int64_t n_total);
 cudaError_t launch_flow_match(int dtype, const void* z0, const void* z1, const float* t, int batch,

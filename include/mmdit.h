@@ -61,7 +61,10 @@ typedef enum mmdit_status {
 typedef enum mmdit_act_dtype { MMDIT_F32 = 0, MMDIT_BF16 = 1 } mmdit_act_dtype;
 
 /* Linear-layer arithmetic: NATIVE = tf32 for MMDIT_F32, bf16 for MMDIT_BF16.
- * FP8_E4M3 = E4M3 operands with delayed per-tensor scaling ([FP8] §Configuration). */
+ * FP8_E4M3 = the four block linears (QKV, output projection, fc1, fc2) on E4M3 operands with
+ * delayed per-tensor scaling ([FP8] §Configuration); needs act = MMDIT_BF16 and
+ * mlp_hidden % 128 == 0.  The modulation, the attention (bf16, [FP8] §Configuration:
+ * fp8_dot_product_attention false) and every other step keep the activation type. */
 typedef enum mmdit_gemm_mode { MMDIT_GEMM_NATIVE = 0, MMDIT_GEMM_FP8_E4M3 = 1 } mmdit_gemm_mode;
 
 /* Shapes and options of one block call ([API] §Configuration, FluxConfig). */
@@ -95,9 +98,22 @@ typedef struct mmdit_stream_w {
   const void *w_2, *b_2;
 } mmdit_stream_w;
 
-/* FP8 delayed-scaling state, caller-owned device memory ([FP8] §Configuration: history 1024,
- * most_recent, margin 0).  Reserved: MMDIT_GEMM_FP8_E4M3 returns MMDIT_ERR_UNSUPPORTED in this
- * build; pass NULL with MMDIT_GEMM_NATIVE. */
+/* FP8 delayed-scaling state of the block linears ([FP8] §Configuration, FP8 model
+ * configuration: E4M3, amax_history_len 1024, amax_compute_algo most_recent, margin 0).
+ * Caller-owned device memory; the struct itself is read on the host during the call.
+ *   amax_history [n_tensors, hist_len] fp32 (row t is tensor t's history)
+ *   scale        [n_tensors] fp32: the scale tensor t is cast with (E4M3(x * scale)); start
+ *                with 1 (an empty history) and let the library update it
+ *   pos          the history column this call records into, 0 <= pos < hist_len; the library
+ *                does not advance it (the caller moves it between calls, e.g. pos + 1 mod
+ *                hist_len; a replayed CUDA graph records into the column it was captured with)
+ * Tensor t = 8 * slot + 2 * linear + operand, with slot 0 = image stream (or the single
+ * block's one stream) and 1 = text stream; linear 0 = QKV, 1 = attention output projection,
+ * 2 = fc1, 3 = fc2; operand 0 = the linear's input, 1 = its weight.  A double block needs
+ * n_tensors >= 16, a single block >= 8.  A call zeroes column pos of those tensors, records
+ * max |x| of every tensor it casts there, and, after its last linear, sets
+ * scale[t] = 448 / amax_history[t, pos] for every such tensor with a positive, finite amax
+ * (the others keep their scale).  Calls sharing a state must be ordered on one stream. */
 typedef struct mmdit_fp8_state {
   float *amax_history; /* [n_tensors, hist_len] */
   float *scale;        /* [n_tensors] */
@@ -229,7 +245,12 @@ mmdit_status mmdit_attention_fwd(int32_t act, int32_t batch, int32_t heads, int3
  *   y_s = x1 + gate2 * (GELU((LN(x1) * (1 + scale2) + shift2) w_1^T + b_1) w_2^T + b_2).
  * vec [B, D]; rope_cos, rope_sin [B, S_i + S_t, d/2] fp32 (rope3d_freqs of the joint ids);
  * x_img, y_img [B, S_i, D]; x_txt, y_txt [B, S_t, D]; y may alias x.
- * fp8: NULL (reserved).  workspace >= mmdit_double_block_workspace_size(dims). */
+ * fp8: NULL with gemm = MMDIT_GEMM_NATIVE; the delayed-scaling state (n_tensors >= 16) with
+ * gemm = MMDIT_GEMM_FP8_E4M3, where every weight is cast to E4M3 at each call (as training
+ * does after each optimizer step) and the inputs of the four linears are cast where they are
+ * produced (LayerNorm-modulate, the attention output, the fc1 GELU).
+ * workspace >= mmdit_double_block_workspace_size(dims) (larger in FP8 mode: it holds the
+ * E4M3 weights). */
 size_t mmdit_double_block_workspace_size(const mmdit_dims *dims);
 mmdit_status mmdit_double_block_fwd(const mmdit_dims *dims, const mmdit_stream_w *w_img,
                                     const mmdit_stream_w *w_txt, const void *vec,
@@ -241,7 +262,8 @@ mmdit_status mmdit_double_block_fwd(const mmdit_dims *dims, const mmdit_stream_w
 /* Single-stream block forward ([ARCH] §Model components, 4. Flux single block; [API]
  * FluxSingleTransformerBlock): the same chain with one weight set over the whole concatenated
  * sequence x [B, S, D], S = S_i + S_t; returns all S rows in y (may alias x).
- * rope_cos, rope_sin [B, S, d/2].  workspace >= mmdit_single_block_workspace_size(dims). */
+ * rope_cos, rope_sin [B, S, d/2].  fp8 as for the double block (n_tensors >= 8).
+ * workspace >= mmdit_single_block_workspace_size(dims). */
 size_t mmdit_single_block_workspace_size(const mmdit_dims *dims);
 mmdit_status mmdit_single_block_fwd(const mmdit_dims *dims, const mmdit_stream_w *w,
                                     const void *vec, const float *rope_cos,
@@ -250,11 +272,35 @@ mmdit_status mmdit_single_block_fwd(const mmdit_dims *dims, const mmdit_stream_w
                                     size_t workspace_bytes, void *stream);
 
 /* Byte offsets of named intermediates inside a block workspace, for inspection by tests:
- * out[0..9] = mod_img, mod_txt, Q, K, Vt, O_img, O_txt, x1_img, x1_txt, u_img (a single block
- * uses the *_img slots; unused slots are -1).  Q, K are [B, H, S, d] bf16, Vt is [B, H, d,
- * S_pad] fp16 (holding bf16-rounded values) with S_pad = S rounded up to 8.  Returns the count written or -1 on bad dims. */
+ * out[0..16] = mod_img, mod_txt, Q, K, Vt, O_img, O_txt, x1_img, x1_txt, u_img, h_img, h_txt,
+ * u_txt, O8_img, O8_txt, Wq_img, Wq_txt (a single block uses the *_img slots; unused slots are
+ * -1).  Q, K are [B, H, S, d] bf16, Vt is [B, H, d, S_pad] fp16 (holding bf16-rounded values)
+ * with S_pad = S rounded up to 8; h (LayerNorm-modulate output) and u (GELU output) are of the
+ * activation type, or E4M3 codes in FP8 mode; O8 is the E4M3 attention output and Wq the E4M3
+ * weights (QKV, output projection, fc1, fc2, back to back), FP8 mode only.  Writes
+ * min(n, 17) entries and returns that count, or -1 on bad dims. */
 int32_t mmdit_block_workspace_offsets(const mmdit_dims *dims, int32_t single, int64_t *out,
                                       int32_t n);
+
+/* ---------------------------------------------------------------------------------------
+ * E4M3 cast with delayed scaling ([FP8] §Configuration; the E4M3 format of "FP8 Formats for
+ * Deep Learning", which the page selects): out[i] = E4M3(x[i] * scale[0]), rounded to nearest
+ * even and saturated to +-448 (NaN stays NaN); amax[0] = max(amax[0], max_i |x[i]|).
+ *   x [n] bf16, out [n] uint8 codes (device, 16-byte aligned); scale, amax: device fp32
+ *   scalars (e.g. entries of an mmdit_fp8_state).  n a multiple of 16; n == 0 is a no-op.
+ * No workspace. */
+mmdit_status mmdit_fp8_quantize_e4m3(const void *x, int64_t n, const float *scale, float *amax,
+                                     void *out, void *stream);
+
+/* Linear layer on E4M3 operands ([FP8] §Configuration: the FP8 GEMM of a linear under delayed
+ * scaling): y = (x_q w_q^T) / (scale_x[0] * scale_w[0]) + b, where x_q [M, K] and w_q [N, K]
+ * hold E4M3 codes (as written by mmdit_fp8_quantize_e4m3 with those scales), b [N] bf16 (may
+ * be NULL), y [M, N] bf16; fp32 accumulation on the tensor cores.  N % 128 == 0,
+ * K % 16 == 0.  workspace >= mmdit_fp8_linear_workspace_size() (the status word). */
+size_t mmdit_fp8_linear_workspace_size(void);
+mmdit_status mmdit_fp8_linear_fwd(int32_t M, int32_t N, int32_t K, const void *x, const void *w,
+                                  const float *scale_x, const float *scale_w, const void *b,
+                                  void *y, void *workspace, size_t workspace_bytes, void *stream);
 
 #ifdef __cplusplus
 }

@@ -57,11 +57,20 @@ def test_workspace_sizes(lib):
     assert single >= S * D * 2 * 5 + S * D * 4 + S * F * 2
     assert L.mmdit_double_block_workspace_size(_dims(head_dim=64)) == 0
     offs = L.mmdit_block_workspace_offsets(d, False)
-    assert len(offs) == 10 and offs[0] == 256
-    assert all(o % 256 == 0 for o in offs)
-    assert sorted(offs) == offs  # carved in order
+    assert len(offs) == 17 and offs[0] == 256
+    assert all(o % 256 == 0 for o in offs if o >= 0)
+    assert sorted(offs[:10]) == offs[:10]  # carved in order
+    assert offs[13:] == [-1, -1, -1, -1]  # E4M3 slots only in FP8 mode
     so = L.mmdit_block_workspace_offsets(d, True)
-    assert so[1] == -1 and so[6] == -1 and so[8] == -1
+    assert so[1] == -1 and so[6] == -1 and so[8] == -1 and so[11] == -1 and so[12] == -1
+    # FP8 mode: the LayerNorm and GELU outputs shrink to one byte per element, and the E4M3
+    # attention output and weights (12 D^2 bytes with F = 4D) are added
+    f8 = _dims(gemm=1)
+    ws8 = L.mmdit_double_block_workspace_size(f8)
+    assert ws8 >= ws - S * (D + F) + S * D + 2 * (4 * D * D + 2 * F * D)
+    o8 = L.mmdit_block_workspace_offsets(f8, False)
+    assert all(o >= 0 and o % 256 == 0 for o in o8)
+    assert o8[16] + 4 * D * D + 2 * F * D <= ws8
     assert L.flow_match_workspace_size(4, 64 * 32 * 32) >= 256 + 4
     assert lib.mmdit_linear_workspace_size(1, 4096, 3072, 3072) == 256  # wide: no split
     assert lib.mmdit_linear_workspace_size(1, 512, 3072, 4096) > 512 * 3072 * 4  # narrow: split K
@@ -76,10 +85,33 @@ def test_validation_errors_before_any_launch(lib):
     bad = _dims(head_dim=64)
     assert lib.mmdit_single_block_fwd(C.byref(bad), C.byref(w), None, None, None, None, None, None,
                                       None, 0, None) == 2
-    fp8 = _dims(gemm=1)
-    assert lib.mmdit_double_block_fwd(C.byref(fp8), C.byref(w), C.byref(w), None, None, None, None,
+    fp8_f32 = _dims(gemm=1, act=0)  # FP8 linears need bf16 activations
+    assert lib.mmdit_double_block_fwd(C.byref(fp8_f32), C.byref(w), C.byref(w), None, None, None, None,
                                       None, None, None, None, None, 0, None) == 2
     assert "FP8" in L.last_error()
+    fp8 = _dims(gemm=1, act=1)
+    assert lib.mmdit_double_block_fwd(C.byref(fp8), C.byref(w), C.byref(w), None, None, None, None,
+                                      None, None, None, None, None, 0, None) == 1
+    assert "fp8 state" in L.last_error()
+    # an FP8 state with too few tensors for a double block, or a position outside the history
+    st8 = L.Fp8State(0x1000, 0x2000, 1024, 8, 0)
+    assert lib.mmdit_double_block_fwd(C.byref(fp8), C.byref(w), C.byref(w), None, None, None, None,
+                                      None, None, None, C.byref(st8), None, 0, None) == 1
+    assert "tensors" in L.last_error()
+    st8 = L.Fp8State(0x1000, 0x2000, 1024, 16, 1024)
+    assert lib.mmdit_single_block_fwd(C.byref(fp8), C.byref(w), None, None, None, None, None,
+                                      C.byref(st8), None, 0, None) == 1
+    # a state given with the native linears
+    st8 = L.Fp8State(0x1000, 0x2000, 1024, 16, 0)
+    assert lib.mmdit_single_block_fwd(C.byref(d), C.byref(w), None, None, None, None, None,
+                                      C.byref(st8), None, 0, None) == 1
+    # E4M3 cast and FP8 linear shapes
+    assert lib.mmdit_fp8_quantize_e4m3(0x1000, 24, 0x2000, 0x3000, 0x4000, None) == 2
+    assert lib.mmdit_fp8_quantize_e4m3(0x1000, 0, None, None, None, None) == 0
+    assert lib.mmdit_fp8_linear_fwd(8, 96, 64, 0x1000, 0x2000, 0x3000, 0x3004, None, 0x4000, 0x5000,
+                                    256, None) == 2
+    assert lib.mmdit_fp8_linear_fwd(8, 128, 64, 0x1000, 0x2000, None, 0x3004, None, 0x4000, 0x5000,
+                                    256, None) == 1
     mism = _dims(heads=23)
     assert lib.mmdit_double_block_fwd(C.byref(mism), C.byref(w), C.byref(w), None, None, None, None,
                                       None, None, None, None, None, 0, None) == 1

@@ -157,17 +157,21 @@ def _sample(n, k, seed):
     return np.unique(np.concatenate([rows, [0, n - 1]]))
 
 
-@pytest.mark.parametrize("B,lat,S_t", [(1, 64, 512), (4, 32, 512)])
+@pytest.mark.parametrize("B,lat,S_t", [(1, 64, 512), (4, 32, 512), (2, 64, 512)])
 def test_double_block_flux_sized_sampled_rows(B, lat, S_t):
-    """12B/535M block shapes (D 3072, 24 heads, F 12288) at 4096+512 and 4x(1024+512) tokens."""
+    """12B/535M block shapes (D 3072, 24 heads, F 12288) at 4096+512, 4x(1024+512) and
+    2x(4096+512) tokens."""
     case = BlockCase(B, lat * lat, S_t, 3072, 24, 12288, "bf16", seed=1001 + B, std=0.02,
                      gain_jitter=0.0, lat_hw=(lat, lat))
     got, _, _ = case.run_gpu()
     _check_outputs(case, got, rows=(_sample(case.S_i, 96, 1), _sample(S_t, 32, 2)))
 
 
-def test_single_block_flux_sized_sampled_rows():
-    case = BlockCase(1, 4096, 512, 3072, 24, 12288, "bf16", seed=1011, std=0.02, gain_jitter=0.0,
+@pytest.mark.parametrize("B", [1, 2])
+def test_single_block_flux_sized_sampled_rows(B):
+    """The single block at 4096+512 tokens, batch 1 and 2 (the 535M-shaped and 1024 px
+    workloads)."""
+    case = BlockCase(B, 4096, 512, 3072, 24, 12288, "bf16", seed=1011 + B, std=0.02, gain_jitter=0.0,
                      lat_hw=(64, 64), single=True)
     got, _, _ = case.run_gpu()
     _check_outputs(case, got, rows=(_sample(case.S, 128, 3),))

@@ -1,0 +1,346 @@
+"""GPU parity of the FP8 E4M3 path: the cast, the FP8 linear, and the blocks with E4M3 linears.
+
+"FP8 training for Flux models", §Configuration › FP8 model configuration: the four linears
+of each stream run on E4M3 operands with per-tensor delayed scaling (most_recent, margin 0);
+attention stays bf16.
+
+What is compared, and why:
+* The cast is bit-exact: both sides round the float32 product x * scale to E4M3.
+* The FP8 linear, fed the same codes (power-of-two scales make the products exact on both
+  sides), agrees to fp32-accumulation level.
+* In a block, every E4M3 cast turns a difference smaller than one E4M3 step into a whole-step
+  difference in some codes, so two correct evaluations whose attention outputs differ at the
+  bf16 level already differ by ~0.3 x RMS element-wise at the output (measured on the oracle).
+  So the block is checked
+    - element-wise wherever both sides take the same decisions: the LayerNorm-modulate codes,
+      Q, K, V^T after the FP8 QKV linear, the attention output, and, with V = 0 (an attention
+      output of exact zeros), the whole chain after the attention;
+    - norm-wise at the output: ||y - y64|| / ||y64|| <= 6e-2 against the float64 block, and
+      no more than 1.5x the deviation of an exact FP8 evaluation (the oracle's) at the same
+      scales.
+* The delayed-scaling state: the recorded amax of every weight is its max |w| exactly, that of
+  the QKV input matches the oracle, and scale = 448 / amax afterwards.
+"""
+import numpy as np
+import pytest
+import torch
+
+from diffusion_transformer_flux_gb300 import _lib as L
+from diffusion_transformer_flux_gb300 import synth
+from oracle import e4m3 as E
+from oracle import flux as O
+
+from gpu_util import BlockCase, assert_parity, dev, host, upload_weights, workspace_view
+
+pytestmark = pytest.mark.gpu
+NAMES = ("qkv", "o", "fc1", "fc2")
+HIST = 1024
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib_loaded():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    L.load()
+
+
+def _codes_f32(x, s):
+    """E4M3 codes of x * s with the product rounded to float32 first (the kernels' order)."""
+    p = (np.asarray(x, np.float32) * np.float32(s)).astype(np.float64)
+    return E.e4m3_encode(p)
+
+
+_DEC = np.array([E.e4m3_decode(c) for c in range(256)])
+
+
+# ----------------------------------------------------------------------------- the cast
+@pytest.mark.parametrize("n", [16, 16 * 1001, 16384 * 3 + 48])
+@pytest.mark.parametrize("scale", [1.0, 448.0 / 3.7, 2.0 ** -5])
+def test_quantize_e4m3_bit_exact(n, scale):
+    rng = np.random.default_rng(n)
+    mag = rng.choice([1e-4, 1e-2, 1.0, 30.0, 3000.0], size=n)
+    x = synth.bf16_round(rng.standard_normal(n) * mag)
+    x[:8] = [0.0, -0.0, 448.0 / scale, -1e30, 2.0 ** -12, -2.0 ** -10, 1.0625, 1e-38]
+    x = synth.bf16_round(x)
+    xt = torch.from_numpy(x).cuda().to(torch.bfloat16)
+    s = torch.tensor([scale], dtype=torch.float32, device="cuda")
+    amax = torch.tensor([0.5], dtype=torch.float32, device="cuda")
+    out = torch.empty(n, dtype=torch.uint8, device="cuda")
+    L.mmdit_fp8_quantize_e4m3(xt, s, amax, out)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy(), _codes_f32(x, np.float32(scale)))
+    assert amax.item() == max(0.5, float(np.abs(x).max()))
+
+
+def test_quantize_keeps_a_larger_recorded_amax():
+    x = torch.ones(32, dtype=torch.bfloat16, device="cuda")
+    s = torch.ones(1, device="cuda")
+    amax = torch.tensor([7.0], device="cuda")
+    out = torch.empty(32, dtype=torch.uint8, device="cuda")
+    L.mmdit_fp8_quantize_e4m3(x, s, amax, out)
+    assert amax.item() == 7.0
+    assert (out == 0x38).all()  # 1.0
+
+
+# ----------------------------------------------------------------------------- the linear
+def _pow2_scale(a):
+    """The largest power of two s with amax * s <= 448."""
+    return 2.0 ** np.floor(np.log2(448.0 / a))
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 256, 3072), (130, 384, 112), (1, 128, 16), (257, 3072, 3072)])
+def test_fp8_linear_matches_oracle(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    x = synth.bf16_round(rng.standard_normal((M, K)))
+    w = synth.bf16_round(rng.standard_normal((N, K)) * 0.02)
+    b = synth.bf16_round(rng.standard_normal(N) * 0.02)
+    sx, sw = _pow2_scale(np.abs(x).max()), _pow2_scale(np.abs(w).max())
+    scales = torch.tensor([sx, sw], dtype=torch.float32, device="cuda")
+    amax = torch.zeros(2, device="cuda")
+    xq = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+    wq = torch.empty(N, K, dtype=torch.uint8, device="cuda")
+    L.mmdit_fp8_quantize_e4m3(dev(x), scales[0:1], amax[0:1], xq)
+    L.mmdit_fp8_quantize_e4m3(dev(w), scales[1:2], amax[1:2], wq)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    ws = L.mmdit_fp8_linear_fwd(xq, wq, scales[0:1], scales[1:2], dev(b), y)
+    torch.cuda.synchronize()
+    assert L.mmdit_workspace_status(ws) == 0
+    ref = E.fp8_linear(x, w, b, sx, sw)
+    # the same codes on both sides: only the fp32 accumulation order and the bf16 output differ
+    assert_parity(host(y), ref, 2e-3, "FP8 linear", out_bf16=True)
+
+
+# ----------------------------------------------------------------------------- blocks
+def _fp8_dims(case):
+    return L.make_dims(case.B, case.S_i, case.S_t, case.D, case.H, case.F, L.MMDIT_BF16,
+                       rope_interleaved=case.interleaved, gelu_tanh=case.gelu_tanh,
+                       gemm=L.MMDIT_GEMM_FP8_E4M3)
+
+
+class Fp8Run:
+    """A block case run through the C ABI with E4M3 linears, two calls in a row on the same
+    inputs: the first with the empty-history scales (1), the second with the scales the first
+    recorded (the delayed-scaling protocol)."""
+
+    def __init__(self, case: BlockCase, calls=2):
+        self.case = case
+        c = case
+        self.dims = _fp8_dims(c)
+        n_t = 8 if c.single else 16
+        self.hist = torch.zeros(n_t, HIST, device="cuda")
+        self.scale = torch.ones(n_t, device="cuda")
+        ids = torch.from_numpy(c.ids).cuda()
+        cos = torch.empty(c.B, c.S, 64, device="cuda")
+        sin = torch.empty_like(cos)
+        L.rope3d_freqs(ids, (16, 56, 56), 10000.0, cos, sin)
+        vec = dev(c.vec)
+        wi = upload_weights(c.w_img, "bf16")
+        self.scales_used = []
+        for call in range(calls):
+            self.scales_used.append(self.scale.cpu().numpy().copy())
+            st = L.make_fp8_state(self.hist, self.scale, pos=call)
+            if c.single:
+                x = dev(c.x_joint())
+                y = torch.empty_like(x)
+                ws = L.mmdit_single_block_fwd(self.dims, wi, vec, cos, sin, x, y, fp8=st)
+                outs = (y,)
+            else:
+                wt = upload_weights(c.w_txt, "bf16")
+                xi, xt = dev(c.x_img), dev(c.x_txt)
+                yi, yt = torch.empty_like(xi), torch.empty_like(xt)
+                ws = L.mmdit_double_block_fwd(self.dims, wi, wt, vec, cos, sin, xi, xt, yi, yt, fp8=st)
+                outs = (yi, yt)
+            torch.cuda.synchronize()
+            assert L.mmdit_workspace_status(ws) == 0
+        self.ws = ws
+        self.y = tuple(host(o) for o in outs)
+        self.amax = self.hist.cpu().numpy()  # [n_t, HIST]
+        self.scale_after = self.scale.cpu().numpy()
+
+    def slots(self):
+        return [("single", 0)] if self.case.single else [("img", 0), ("txt", 1)]
+
+    def name_of(self, t):
+        slot, rem = divmod(t, 8)
+        s = self.slots()[slot][0] if slot < len(self.slots()) else None
+        return f"{s}.{NAMES[rem // 2]}.{'xw'[rem % 2]}"
+
+
+def _oracle_fp8(case, scales=None, rows=None):
+    """The oracle with E4M3 linears (bf16 elsewhere) at the given scales; returns (outputs, ds)."""
+    ds = E.DelayedScaling(scales or {})
+    args = dict(mm_cast=O.round_bf16, fp8=ds, interleaved=case.interleaved, gelu_tanh=case.gelu_tanh)
+    if case.single:
+        x = case.x_joint()
+        if rows is None:
+            y = (O.single_block(x, case.vec, case.cos, case.sin, case.w_img, case.H, **args),)
+        else:
+            y = (O.single_block_rows(x, case.vec, case.cos, case.sin, case.w_img, case.H, rows[0], **args),)
+    elif rows is None:
+        y = O.double_block(case.x_img, case.x_txt, case.vec, case.cos, case.sin, case.w_img, case.w_txt,
+                           case.H, **args)
+    else:
+        y = O.double_block_rows(case.x_img, case.x_txt, case.vec, case.cos, case.sin, case.w_img,
+                                case.w_txt, case.H, rows[0], rows[1], **args)
+    return y, ds
+
+
+def _oracle_two_calls(case, rows=None):
+    _, ds1 = _oracle_fp8(case, rows=rows)
+    sc = ds1.next_scales()
+    y, ds2 = _oracle_fp8(case, sc, rows=rows)
+    return y, sc, ds1
+
+
+def _check_state(run: Fp8Run, ds1, tol=None, sampled=False):
+    """The amax the first call recorded (column 0) and the scales the last call left.
+
+    Weights: max |w| exactly.  Inputs: within tol[linear] (relative) of the oracle's amax; with
+    `sampled` rows the oracle saw only some rows after the attention, so there the recorded
+    amax must only be at least the oracle's (less a bf16-level margin)."""
+    tol = dict({"qkv": 1e-5, "o": 0.1, "fc1": 0.1, "fc2": 0.1}, **(tol or {}))
+    a0 = run.amax[:, 0]
+    for t in range(len(a0)):
+        name = run.name_of(t)
+        ref = ds1.amax[name]
+        lin = name.split(".")[1]
+        if name.endswith(".w"):
+            assert a0[t] == np.float32(ref), (name, a0[t], ref)  # max |w| of bf16 values, exact
+        elif sampled and lin != "qkv":
+            assert a0[t] >= ref * (1 - 1e-2), (name, a0[t], ref)
+        else:
+            assert abs(a0[t] - ref) <= tol[lin] * ref, (name, a0[t], ref)
+    # scale after the last call = 448 / its recorded amax (float32 division)
+    last = run.amax[:, len(run.scales_used) - 1]
+    for t in range(len(last)):
+        if last[t] > 0:
+            assert run.scale_after[t] == np.float32(448.0) / np.float32(last[t]), run.name_of(t)
+        else:
+            assert run.scale_after[t] == run.scales_used[-1][t]
+
+
+def _check_codes(got, h, s_gpu, s_oracle, what):
+    """E4M3 codes `got` of the values h: each is a valid rounding of h * s_gpu (half an E4M3
+    step, or half a subnormal step, plus float32 rounding of h), and the oracle's decisions at
+    its own scale agree almost everywhere."""
+    hs = h * s_gpu
+    err = np.abs(_DEC[got] - hs)
+    assert np.all(err <= 2.0 ** -4 * np.abs(hs) * (1 + 1e-5) + 2.0 ** -10 + 1e-6 * np.abs(hs)), what
+    same = np.mean(got == E.e4m3_encode(h * s_oracle))
+    assert same >= 0.999, (what, same)
+
+
+def _check_pre_attention(run: Fp8Run, sc):
+    """Q, K, V^T after the FP8 QKV linear, and the attention output, of the last call."""
+    case = run.case
+    offs = L.mmdit_block_workspace_offsets(run.dims, case.single)
+    B, H, S, D = case.B, case.H, case.S, case.D
+    S_pad = (S + 7) // 8 * 8
+    streams = [("single" if case.single else "img", case.x_joint() if case.single else case.x_img,
+                case.w_img)]
+    if not case.single:
+        streams.append(("txt", case.x_txt, case.w_txt))
+    qs, ks, vs = [], [], []
+    for name, x, w in streams:
+        m = O.modulation(case.vec, w["w_mod"], w["b_mod"], mm_cast=O.round_bf16)
+        q, kk, v = O.qkv_heads(x, m[0], m[1], w, H, mm_cast=O.round_bf16, fp8=E.DelayedScaling(sc),
+                               name=name)
+        qs.append(q), ks.append(kk), vs.append(v)
+    q, k, v = (np.concatenate(a, axis=2) for a in (qs, ks, vs))
+    cs, sn = case.cos[:, None], case.sin[:, None]
+    q = O.apply_rope(q, cs, sn, case.interleaved)
+    k = O.apply_rope(k, cs, sn, case.interleaved)
+    gq = host(workspace_view(run.ws, offs[2], (B, H, S, 128), torch.bfloat16))
+    gk = host(workspace_view(run.ws, offs[3], (B, H, S, 128), torch.bfloat16))
+    gvt = host(workspace_view(run.ws, offs[4], (B, H, 128, S_pad), torch.float16))[..., :S]
+    assert_parity(gq, q, 2e-2, "Q after FP8 QKV + RMSNorm + RoPE", out_bf16=True)
+    assert_parity(gk, k, 2e-2, "K after FP8 QKV + RMSNorm + RoPE", out_bf16=True)
+    assert_parity(gvt, np.swapaxes(v, -1, -2), 2e-2, "V^T after FP8 QKV", out_bf16=True)
+    o = O.attention(q, k, v, O.round_bf16).transpose(0, 2, 1, 3).reshape(B, S, D)
+    rows_i = B * (S if case.single else case.S_i)
+    go = host(workspace_view(run.ws, offs[5], (rows_i, D), torch.bfloat16)).reshape(B, -1, D)
+    assert_parity(go, o if case.single else o[:, :case.S_i], 2e-2, "attention output", out_bf16=True)
+
+
+def _check_norm_wise(got, y8, y64, what, factor=1.5):
+    for g, a, r, n in zip(got, y8, y64, ("first", "second")):
+        if r.size == 0:
+            continue
+        e_gpu = np.linalg.norm(g - r) / np.linalg.norm(r)
+        e_fp8 = np.linalg.norm(a - r) / np.linalg.norm(r)
+        print(f"[fp8] {what} ({n} output): GPU {e_gpu:.4e}, exact FP8 {e_fp8:.4e} (norm-wise vs float64)")
+        assert e_gpu <= 6e-2, f"{what} ({n} output): ||y - y64|| / ||y64|| = {e_gpu:.3e} > 6e-2"
+        assert e_gpu <= factor * e_fp8, (f"{what} ({n} output): {e_gpu:.3e} vs exact-FP8 "
+                                         f"{e_fp8:.3e}")
+
+
+SMALL = [
+    # B, S_i, S_t, D, H, F, single
+    (2, 300, 45, 256, 2, 1024, False),
+    (1, 200, 77, 512, 4, 1536, False),
+    (2, 300, 45, 256, 2, 1024, True),
+]
+
+
+@pytest.mark.parametrize("B,S_i,S_t,D,H,F,single", SMALL)
+def test_fp8_block_small(B, S_i, S_t, D, H, F, single):
+    case = BlockCase(B, S_i, S_t, D, H, F, "bf16", seed=31 + S_i + D, std=0.05, single=single)
+    run = Fp8Run(case)
+    y8, sc, ds1 = _oracle_two_calls(case)
+    _check_state(run, ds1)
+    _check_pre_attention(run, sc)
+    _check_norm_wise(run.y, y8, case.oracle(None), "FP8 block")
+
+
+@pytest.mark.parametrize("single", [False, True])
+def test_fp8_block_after_attention_elementwise(single):
+    """V = 0 makes the attention output exactly zero on both sides, so the output projection,
+    LayerNorm-modulate -> E4M3, fc1 + GELU -> E4M3 and fc2 take the same decisions as the oracle
+    and can be held to the element-wise bar."""
+    case = BlockCase(2, 300, 45, 256, 2, 1024, "bf16", seed=77, std=0.05, single=single)
+    for w in [case.w_img] + ([] if single else [case.w_txt]):
+        D = case.D
+        w["w_qkv"][2 * D:] = 0.0
+        w["b_qkv"][2 * D:] = 0.0
+    run = Fp8Run(case)
+    y8, sc, ds1 = _oracle_two_calls(case)
+    # every amax, o's (exactly 0) included, is now decided like the oracle's
+    _check_state(run, ds1, tol={"o": 0.0, "fc1": 1e-5, "fc2": 1e-3})
+    xs = [case.x_joint()] if single else [case.x_img, case.x_txt]
+    ws_names = ["single"] if single else ["img", "txt"]
+    wsets = [case.w_img] if single else [case.w_img, case.w_txt]
+    offs = L.mmdit_block_workspace_offsets(run.dims, single)
+    for k, (x, w, name) in enumerate(zip(xs, wsets, ws_names)):
+        # the MLP branch's LayerNorm-modulate codes (the h slot holds them after the call): the
+        # attention output is zero, so the output projection is its bias
+        m = O.modulation(case.vec, w["w_mod"], w["b_mod"], mm_cast=O.round_bf16)
+        x1 = O.gated_residual(x, m[2], np.broadcast_to(np.asarray(w["b_o"], np.float64), x.shape))
+        h2 = O.modulate(x1, m[3], m[4])
+        got = workspace_view(run.ws, offs[10 + k], (x.shape[0] * x.shape[1], case.D), torch.uint8)
+        _check_codes(got.cpu().numpy().reshape(h2.shape), h2, run.scales_used[-1][8 * k + 4],
+                     sc[f"{name}.fc1.x"], f"{name} MLP-branch LayerNorm codes")
+    for g, r, x in zip(run.y, y8, xs):
+        e = assert_parity(g, r, 2e-2, "FP8 block output (V = 0)", out_bf16=True)
+        print(f"[fp8] V = 0 block output: max|err| / RMS beyond bf16 rounding = {e:.3e}")
+        assert_parity(g - x, r - x, 0.1, "FP8 block branch (V = 0)", out_bf16=True)
+
+
+def _sample(n, k, seed):
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(n, size=min(k, n), replace=False))
+    return np.unique(np.concatenate([rows, [0, n - 1]]))
+
+
+@pytest.mark.parametrize("single", [False, True])
+def test_fp8_blocks_at_2048px_sampled_rows(single):
+    """The 12B block shapes at 2048 px (16384 image + 512 text tokens, batch 1) with E4M3
+    linears, in the launch configuration the benchmark times, on seeded rows."""
+    case = BlockCase(1, 128 * 128, 512, 3072, 24, 12288, "bf16", seed=1004 + single, std=0.02,
+                     gain_jitter=0.0, lat_hw=(128, 128), single=single)
+    run = Fp8Run(case)
+    rows = (_sample(case.S, 96, 5),) if single else (_sample(case.S_i, 64, 5), _sample(case.S_t, 32, 6))
+    y8, sc, ds1 = _oracle_two_calls(case, rows=rows)
+    _check_state(run, ds1, sampled=True)
+    y64 = case.oracle_rows(*rows, mm_cast=None)
+    got = [g[:, r] for g, r in zip(run.y, rows)]
+    _check_norm_wise(got, y8, y64, "FP8 block at 2048 px")
