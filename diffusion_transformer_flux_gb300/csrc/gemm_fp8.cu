@@ -3,6 +3,7 @@
 // §Configuration, FP8 model configuration); the epilogue first divides the accumulator by
 // scale_x * scale_w, then applies the bf16 epilogue of the linear it replaces.
 #include "gemm_kernel.cuh"
+#include "gemm_pair.cuh"
 
 namespace mmdit {
 cudaError_t launch_gemm_fp8(const GemmProblem& p, uint32_t* status, cudaStream_t stream) {
@@ -10,6 +11,14 @@ cudaError_t launch_gemm_fp8(const GemmProblem& p, uint32_t* status, cudaStream_t
   if (!p.ep.scale_a || !p.ep.scale_w || (p.M1 > 0 && (!p.ep1.scale_a || !p.ep1.scale_w)))
     return cudaErrorInvalidValue;
   const bool wide = p.N % 256 == 0;
+  if (use_pair(p)) {
+    switch (p.epi) {
+      case kEpiQkv: return run_gemm_pair<kKindF8, 256, kEpiQkv>(p, status, stream);
+      case kEpiGateResid: return run_gemm_pair<kKindF8, 256, kEpiGateResid>(p, status, stream);
+      case kEpiGeluF8: return run_gemm_pair<kKindF8, 256, kEpiGeluF8>(p, status, stream);
+      default: break;
+    }
+  }
   switch (p.epi) {
     case kEpiQkv:
       if (wide && p.ep.hidden % 256 == 0) return run_gemm<kKindF8, 256, kEpiQkv>(p, status, stream);

@@ -496,9 +496,30 @@ cudaError_t run_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream
   return cudaGetLastError();
 }
 
+template <int KIND, int BN, int EPI>
+cudaError_t run_gemm_pair(const GemmProblem& p, uint32_t* status, cudaStream_t stream);
+
+// GEMMs that take the CTA-pair kernel (gemm_pair.cuh): the block linears' epilogues, N a
+// multiple of 256, and enough rows for the 256-row tiles to pay.
+inline bool use_pair(const GemmProblem& p) {
+  const bool epi_ok = p.epi == kEpiQkv || p.epi == kEpiGateResid || p.epi == kEpiGelu || p.epi == kEpiGeluF8;
+  const bool qkv_ok = p.epi != kEpiQkv || p.ep.hidden % 256 == 0;
+  return epi_ok && qkv_ok && p.N % 256 == 0 && p.M + p.M1 >= 512;
+}
+
 // Picks the tile width for N and the epilogue, then launches.
 template <int KIND>
 cudaError_t dispatch_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream) {
+  if constexpr (KIND == kKindF16) {
+    if (use_pair(p)) {
+      switch (p.epi) {
+        case kEpiQkv: return run_gemm_pair<KIND, 256, kEpiQkv>(p, status, stream);
+        case kEpiGateResid: return run_gemm_pair<KIND, 256, kEpiGateResid>(p, status, stream);
+        case kEpiGelu: return run_gemm_pair<KIND, 256, kEpiGelu>(p, status, stream);
+        default: break;
+      }
+    }
+  }
 #define MMDIT_GEMM_EPI(BN)                                                          \
   switch (p.epi) {                                                                  \
     case kEpiBias: return run_gemm<KIND, BN, kEpiBias>(p, status, stream);          \
