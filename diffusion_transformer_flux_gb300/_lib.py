@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "MMDIT_OK", 1: "MMDIT_ERR_INVALID_ARG", 2: "MMDIT_ERR_UNSUPPO
 EXPORTED = [
     "mmdit_last_error", "mmdit_workspace_status", "mmdit_launch_count", "mmdit_launch_count_reset",
     "mmdit_profile_enable", "mmdit_profile_collect",
-    "rope3d_freqs", "flow_match_workspace_size", "flow_match_noise_and_loss",
+    "rope3d_freqs", "mmdit_modulation_fwd", "flow_match_workspace_size", "flow_match_noise_and_loss",
     "flow_match_noise_and_loss_noalloc",
     "mmdit_linear_workspace_size", "mmdit_linear_fwd", "mmdit_img_in_workspace_size",
     "mmdit_img_in_fwd", "mmdit_final_layer_workspace_size", "mmdit_final_layer_fwd",
@@ -54,7 +54,7 @@ STREAM_W_FIELDS = ["w_mod", "b_mod", "w_qkv", "b_qkv", "g_q", "g_k", "w_o", "b_o
 
 
 class StreamW(C.Structure):
-    _fields_ = [(n, C.c_void_p) for n in STREAM_W_FIELDS]
+    _fields_ = [(n, C.c_void_p) for n in STREAM_W_FIELDS] + [("mod", C.c_void_p)]
 
 
 class Fp8State(C.Structure):
@@ -83,6 +83,7 @@ _SIGS = {
     "mmdit_profile_enable": (None, [I32]),
     "mmdit_profile_collect": (I32, [VP, C.c_char_p, SZ, C.POINTER(F32), I32]),
     "rope3d_freqs": (C.c_int, [VP, I32, I32, C.POINTER(I32), F32, VP, VP, VP]),
+    "mmdit_modulation_fwd": (C.c_int, [I32, I32, I32, I32, VP, VP, VP, VP, VP]),
     "flow_match_workspace_size": (SZ, [I32, I64]),
     "flow_match_noise_and_loss": (C.c_int, [I32, VP, VP, VP, I32, I64, VP, VP, VP, VP, SZ, VP]),
     "flow_match_noise_and_loss_noalloc": (C.c_int, [I32, VP, VP, VP, I32, I64, VP, VP, VP, VP]),
@@ -165,7 +166,9 @@ def make_dims(batch, seq_img, seq_txt, hidden, heads, mlp_hidden, act, head_dim=
 
 
 def make_stream_w(w: dict) -> StreamW:
-    return StreamW(*[_ptr(w[n]) for n in STREAM_W_FIELDS])
+    """The C view of one stream's weights; an optional "mod" entry is a precomputed
+    modulation [B, 6D] fp32 (see mmdit_modulation_fwd)."""
+    return StreamW(*[_ptr(w[n]) for n in STREAM_W_FIELDS], _ptr(w.get("mod")))
 
 
 def workspace(nbytes: int, device="cuda") -> torch.Tensor:
@@ -210,6 +213,14 @@ def rope3d_freqs(ids, axes_dim, theta, cos_out, sin_out, stream=None):
     axes = (I32 * 3)(*axes_dim)
     _check(load().rope3d_freqs(_ptr(ids), B, S, axes, float(theta), _ptr(cos_out), _ptr(sin_out),
                                _stream(stream)))
+
+
+def mmdit_modulation_fwd(vec, w, b, out, stream=None):
+    """out [B, rows] fp32 = SiLU(vec) w^T + b (the AdaLN modulation linear)."""
+    B, dim = vec.shape
+    rows = w.shape[0]
+    _check(load().mmdit_modulation_fwd(act_of(vec), B, rows, dim, _ptr(vec), _ptr(w), _ptr(b), _ptr(out),
+                                       _stream(stream)))
 
 
 def flow_match_workspace_size(batch, n_per_sample) -> int:

@@ -269,6 +269,8 @@ static mmdit_status check_ptrs(std::initializer_list<const void*> ptrs, const ch
 
 static mmdit_status check_stream_w(const mmdit_stream_w* w, const char* what) {
   if (!w) return fail(MMDIT_ERR_INVALID_ARG, "%s: weight set is NULL", what);
+  if (w->mod && !aligned16(w->mod))
+    return fail(MMDIT_ERR_INVALID_ARG, "%s: precomputed modulation is not 16-byte aligned", what);
   return check_ptrs({w->w_mod, w->b_mod, w->w_qkv, w->b_qkv, w->g_q, w->g_k, w->w_o, w->b_o, w->w_1,
                      w->b_1, w->w_2, w->b_2},
                     what);
@@ -352,6 +354,7 @@ struct Streams {
   const void* x[2] = {nullptr, nullptr};
   void* y[2] = {nullptr, nullptr};
   int rpb[2] = {0, 0};  // rows per batch element
+  const float* mod[2] = {nullptr, nullptr};  // [B, 6D] modulation (precomputed or in the workspace)
 };
 
 // The FP8 state of one block call (f == nullptr when the linears are not FP8): where each
@@ -375,7 +378,7 @@ mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss,
     ProfScope ps_(p.single ? "single.ln1" : "double.ln1", st);
     LnModJob jobs[2];
     for (int i = 0; i < ss.n; ++i) {
-      const float* mod = at<float>(ws, p.mod[ss.s[i]]);
+      const float* mod = ss.mod[i];
       jobs[i] = {ss.x[i], mod, mod + p.D, 6 * p.D, at(ws, p.h[ss.s[i]]), p.B * ss.rpb[i], ss.rpb[i]};
       if (f8.f) {
         const int t = fp8_tensor(ss.s[i], 0, 0);
@@ -439,7 +442,7 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
   GemmProblem g;
   g.act = mm, g.epi = kEpiGateResid, g.N = p.D, g.K = p.D;
   for (int i = 0; i < ss.n; ++i) {
-    const float* mod = at<float>(ws, p.mod[ss.s[i]]);
+    const float* mod = ss.mod[i];
     EpiArgs e;
     e.bias = ss.w[i]->b_o, e.resid = ss.x[i], e.gate = mod + 2 * p.D, e.gate_bstride = 6 * p.D;
     e.rows_per_batch = ss.rpb[i], e.out = at(ws, p.x1[ss.s[i]]), e.out_f32 = 1;
@@ -454,7 +457,7 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
     ProfScope ps_(p.single ? "single.ln2" : "double.ln2", st);
     LnModJob jobs[2];
     for (int i = 0; i < ss.n; ++i) {
-      const float* mod = at<float>(ws, p.mod[ss.s[i]]);
+      const float* mod = ss.mod[i];
       jobs[i] = {at(ws, p.x1[ss.s[i]]), mod + 3 * p.D, mod + 4 * p.D, 6 * p.D, at(ws, p.h[ss.s[i]]),
                  p.B * ss.rpb[i], ss.rpb[i]};
       if (f8.f) {
@@ -484,7 +487,7 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
   GemmProblem f2;
   f2.act = mm, f2.epi = kEpiGateResid, f2.N = p.D, f2.K = p.F;
   for (int i = 0; i < ss.n; ++i) {
-    const float* mod = at<float>(ws, p.mod[ss.s[i]]);
+    const float* mod = ss.mod[i];
     EpiArgs e;
     e.bias = ss.w[i]->b_2, e.resid = at(ws, p.x1[ss.s[i]]), e.resid_f32 = 1, e.gate = mod + 5 * p.D;
     e.gate_bstride = 6 * p.D, e.rows_per_batch = ss.rpb[i], e.out = ss.y[i];
@@ -608,6 +611,21 @@ mmdit_status rope3d_freqs(const float* ids, int32_t batch, int32_t seq, const in
   MMDIT_CUDA(launch_rope3d(ids, batch, seq, axes, theta, cos_out, sin_out,
                            static_cast<cudaStream_t>(stream)),
              "rope3d_freqs");
+  return MMDIT_OK;
+}
+
+mmdit_status mmdit_modulation_fwd(int32_t act, int32_t batch, int32_t rows, int32_t dim, const void* vec,
+                                  const void* w, const void* bias, float* out, void* stream) {
+  if (act != MMDIT_F32 && act != MMDIT_BF16) return fail(MMDIT_ERR_INVALID_ARG, "bad act %d", act);
+  if (batch < 0 || rows < 0 || dim < 1) return fail(MMDIT_ERR_INVALID_ARG, "bad modulation shape");
+  if (dim % 8 != 0 || dim > 6144)
+    return fail(MMDIT_ERR_UNSUPPORTED, "modulation: dim must be a multiple of 8, at most 6144 (got %d)", dim);
+  if (static_cast<int64_t>(batch) * rows == 0) return MMDIT_OK;
+  mmdit_status s = check_ptrs({vec, w, out}, "modulation");
+  if (s != MMDIT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ProfScope ps_("modulation", st);
+  MMDIT_CUDA(launch_modulation(act, vec, w, bias, batch, rows, dim, out, st), "modulation");
   return MMDIT_OK;
 }
 
@@ -863,11 +881,15 @@ mmdit_status mmdit_double_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
   {
-    // both streams' AdaLN modulation in one launch (they share vec)
-    ProfScope ps_("double.modulation", st);
-    const ModulationJob jobs[2] = {{w_img->w_mod, w_img->b_mod, at<float>(workspace, p.mod[0]), 6 * p.D},
-                                   {w_txt->w_mod, w_txt->b_mod, at<float>(workspace, p.mod[1]), 6 * p.D}};
-    MMDIT_CUDA(launch_modulation2(d->act, vec, jobs, 2, p.B, p.D, st), "modulation");
+    // both streams' AdaLN modulation in one launch (they share vec), unless precomputed
+    ModulationJob jobs[2];
+    int nj = 0;
+    if (!w_img->mod) jobs[nj++] = {w_img->w_mod, w_img->b_mod, at<float>(workspace, p.mod[0]), 6 * p.D};
+    if (!w_txt->mod) jobs[nj++] = {w_txt->w_mod, w_txt->b_mod, at<float>(workspace, p.mod[1]), 6 * p.D};
+    if (nj) {
+      ProfScope ps_("double.modulation", st);
+      MMDIT_CUDA(launch_modulation2(d->act, vec, jobs, nj, p.B, p.D, st), "modulation");
+    }
   }
   Streams ss;
   const mmdit_stream_w* wsets[2] = {w_img, w_txt};
@@ -878,6 +900,7 @@ mmdit_status mmdit_double_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
     if (rpb[i] > 0) {
       ss.s[ss.n] = i, ss.w[ss.n] = wsets[i], ss.x[ss.n] = xs[i], ss.y[ss.n] = ys[i];
       ss.rpb[ss.n] = rpb[i];
+      ss.mod[ss.n] = wsets[i]->mod ? wsets[i]->mod : at<float>(workspace, p.mod[i]);
       ++ss.n;
     }
   Fp8 f8;
@@ -906,7 +929,7 @@ mmdit_status mmdit_single_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
   if ((s = check_workspace(workspace, workspace_bytes, p.total)) != MMDIT_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
-  {
+  if (!w->mod) {
     ProfScope ps_("single.modulation", st);
     MMDIT_CUDA(launch_modulation(d->act, vec, w->w_mod, w->b_mod, p.B, 6 * p.D, p.D,
                                  at<float>(workspace, p.mod[0]), st),
@@ -914,6 +937,7 @@ mmdit_status mmdit_single_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
   }
   Streams ss;
   ss.n = 1, ss.s[0] = 0, ss.w[0] = w, ss.x[0] = x, ss.y[0] = y, ss.rpb[0] = p.S;
+  ss.mod[0] = w->mod ? w->mod : at<float>(workspace, p.mod[0]);
   Fp8 f8;
   f8.f = fp8;
   if (fp8 && (s = fp8_begin(p, ss, f8, kFp8TensorsPerStream, workspace, st)) != MMDIT_OK) return s;

@@ -115,18 +115,23 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __rest
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   const int total = j0.rows + j1.rows;
-  for (int g = blockIdx.x * warps + warp; g < total; g += gridDim.x * warps) {
+  const int stride = gridDim.x * warps;
+  // Rows are software-pipelined: the loads of a warp's next row are issued before its current
+  // row is reduced, so every warp keeps one row (NC 16-byte loads per lane) in flight.
+  auto load_row = [&](int g, Raw8<T> (&raw)[NC]) {
     const bool second = g >= j0.rows;
     const ModJob& job = second ? j1 : j0;
-    const int r = second ? g - j0.rows : g;
-    const T* wr = reinterpret_cast<const T*>(job.w) + static_cast<size_t>(r) * dim;
-    // the whole row in one round of 16-byte loads (NC per lane)
-    Raw8<T> raw[NC];
+    const T* wr = reinterpret_cast<const T*>(job.w) + static_cast<size_t>(second ? g - j0.rows : g) * dim;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       const int k = c * 256 + lane * 8;
       if (k < dim) raw[c].load(wr + k);
     }
+  };
+  auto reduce_row = [&](int g, const Raw8<T> (&raw)[NC]) {
+    const bool second = g >= j0.rows;
+    const ModJob& job = second ? j1 : j0;
+    const int r = second ? g - j0.rows : g;
     float acc[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[b] = 0.f;
@@ -151,6 +156,18 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __rest
       const float sum = warp_sum(acc[b]);
       if (lane == 0) job.m[static_cast<size_t>(b) * job.rows + r] = sum + bb;
     }
+  };
+  Raw8<T> ra[NC], rb[NC];
+  int g = blockIdx.x * warps + warp;
+  if (g < total) load_row(g, ra);
+  while (g < total) {
+    const int g1 = g + stride;
+    if (g1 < total) load_row(g1, rb);
+    reduce_row(g, ra);
+    const int g2 = g1 + stride;
+    if (g2 < total) load_row(g2, ra);
+    if (g1 < total) reduce_row(g1, rb);
+    g = g2;
   }
 }
 

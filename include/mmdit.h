@@ -88,7 +88,11 @@ typedef struct mmdit_dims {
  * element type `act`.  Shapes: w_mod [6D, D], b_mod [6D] (AdaLN chunks in the order shift,
  * scale, gate, shift_mlp, scale_mlp, gate_mlp -- [API] §Normalization, AdaLN); w_qkv [3D, D],
  * b_qkv [3D]; g_q, g_k [d] (per-head QK-RMSNorm gains); w_o [D, D], b_o [D] (attention output
- * projection); w_1 [F, D], b_1 [F]; w_2 [D, F], b_2 [D] (GELU MLP). */
+ * projection); w_1 [F, D], b_1 [F]; w_2 [D, F], b_2 [D] (GELU MLP).
+ * mod: NULL, or this stream's modulation [B, 6D] fp32 (16-byte aligned) as mmdit_modulation_fwd
+ * computes it from w_mod, b_mod and the call's vec -- for example on another stream, overlapped
+ * with earlier work.  The block then reads it instead of recomputing it; the caller orders that
+ * computation before the block call and keeps the buffer until the call has completed. */
 typedef struct mmdit_stream_w {
   const void *w_mod, *b_mod;
   const void *w_qkv, *b_qkv;
@@ -96,6 +100,7 @@ typedef struct mmdit_stream_w {
   const void *w_o, *b_o;
   const void *w_1, *b_1;
   const void *w_2, *b_2;
+  const float *mod;
 } mmdit_stream_w;
 
 /* FP8 delayed-scaling state of the block linears ([FP8] §Configuration, FP8 model
@@ -157,6 +162,18 @@ int32_t mmdit_profile_collect(void *stream, char *names_out, size_t names_len, f
  * No workspace.  batch*seq == 0 is a no-op. */
 mmdit_status rope3d_freqs(const float *ids, int32_t batch, int32_t seq, const int32_t *axes_dim,
                           float theta, float *cos_out, float *sin_out, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * AdaLN modulation ([API] §Normalization, AdaLN; [ARCH] §Implementation details, Adaptive
+ * layer normalization): out[b, r] = sum_k SiLU(vec[b, k]) w[r, k] + bias[r], the linear of the
+ * SiLU of the conditioning vector whose 6D rows a block splits into (shift, scale, gate) for the
+ * attention and MLP branches (2D rows for the output head).
+ *   vec [batch, dim], w [rows, dim], bias [rows] (may be NULL): element type `act`
+ *   out [batch, rows] fp32.  dim a multiple of 8, at most 6144.  No workspace.
+ * The result can be handed to a block through mmdit_stream_w.mod. */
+mmdit_status mmdit_modulation_fwd(int32_t act, int32_t batch, int32_t rows, int32_t dim,
+                                  const void *vec, const void *w, const void *bias, float *out,
+                                  void *stream);
 
 /* ---------------------------------------------------------------------------------------
  * Rectified flow ([ARCH] §Mathematical formulation, Flow matching objective; [API] §Training

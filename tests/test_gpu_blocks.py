@@ -150,6 +150,41 @@ def test_block_output_may_alias_input():
     assert_parity(host(xt), ref[1], 2e-2, "aliased y_txt", out_bf16=True)
 
 
+@pytest.mark.parametrize("single", [False, True])
+def test_precomputed_modulation_gives_identical_blocks(single):
+    """A modulation computed ahead by mmdit_modulation_fwd and handed over through the weight
+    set's `mod` gives the same bits as the block computing it itself."""
+    case = BlockCase(2, 300, 45, 256, 2, 1024, "bf16", seed=19, std=0.05, single=single)
+    from gpu_util import dev, upload_weights
+    t = torch.bfloat16
+    ids = torch.from_numpy(case.ids).cuda()
+    cos = torch.empty(case.B, case.S, 64, device="cuda")
+    sin = torch.empty_like(cos)
+    L.rope3d_freqs(ids, (16, 56, 56), 10000.0, cos, sin)
+    vec = dev(case.vec, t)
+    sets = [upload_weights(case.w_img, "bf16")] + ([] if single else [upload_weights(case.w_txt, "bf16")])
+    outs = []
+    for pre in (False, True):
+        ws_ = [dict(w) for w in sets]
+        if pre:
+            for w in ws_:
+                w["mod"] = torch.empty(case.B, 6 * case.D, device="cuda")
+                L.mmdit_modulation_fwd(vec, w["w_mod"], w["b_mod"], w["mod"])
+        if single:
+            x = dev(case.x_joint(), t)
+            y = torch.empty_like(x)
+            L.mmdit_single_block_fwd(case.dims, ws_[0], vec, cos, sin, x, y)
+            outs.append((y,))
+        else:
+            xi, xt = dev(case.x_img, t), dev(case.x_txt, t)
+            yi, yt = torch.empty_like(xi), torch.empty_like(xt)
+            L.mmdit_double_block_fwd(case.dims, ws_[0], ws_[1], vec, cos, sin, xi, xt, yi, yt)
+            outs.append((yi, yt))
+    torch.cuda.synchronize()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
 # ----------------------------------------------------------------------------- Flux-sized workloads
 def _sample(n, k, seed):
     rng = np.random.default_rng(seed)

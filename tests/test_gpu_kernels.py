@@ -82,6 +82,28 @@ def test_flow_match_endpoints_on_gpu():
     assert loss.item() == 0.0
 
 
+# ----------------------------------------------------------------------------- modulation GEMV
+@pytest.mark.parametrize("act,B,rows,dim", [("bf16", 1, 6 * 3072, 3072), ("bf16", 3, 6 * 256, 256),
+                                            ("bf16", 9, 2 * 512, 512), ("f32", 2, 6 * 256, 256)])
+def test_modulation_matches_oracle(act, B, rows, dim):
+    """SiLU(vec) w^T + b in fp32 accumulation; in bf16 mode SiLU(vec) is a bf16 operand of the
+    linear (autocast), so the oracle at that precision is the reference.  Batch 9 runs two
+    passes of the kernel (at most 8 batch rows each)."""
+    rng = np.random.default_rng(rows + B)
+    cast = synth.bf16_round if act == "bf16" else (lambda a: a.astype(np.float32))
+    vec = cast(rng.standard_normal((B, dim)).astype(np.float32))
+    w = cast((rng.standard_normal((rows, dim)) * 0.02).astype(np.float32))
+    b = cast((rng.standard_normal(rows) * 0.02).astype(np.float32))
+    t = torch.bfloat16 if act == "bf16" else torch.float32
+    out = torch.empty(B, rows, device="cuda")
+    L.mmdit_modulation_fwd(dev(vec, t), dev(w, t), dev(b, t), out)
+    torch.cuda.synchronize()
+    ref = np.concatenate(O.modulation(vec, w, b, n_chunks=1, mm_cast=O.round_bf16 if act == "bf16" else None),
+                         axis=-1)
+    # only the order of the fp32 accumulation differs from the oracle at the same precision
+    assert_parity(host(out), ref, 1e-4, f"modulation {act} B={B} rows={rows}")
+
+
 # ----------------------------------------------------------------------------- linear (GEMM core)
 @pytest.mark.parametrize("act,M,N,K", [
     ("bf16", 300, 96, 200),      # ragged M, 32-wide tiles, K tail
