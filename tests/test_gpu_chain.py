@@ -1,0 +1,93 @@
+"""The 12B block shapes at 512 px as one chain, against the oracle chain on the same inputs.
+
+rope3d_freqs -> rectified-flow noise z_t -> img_in -> double block -> output head ->
+flow-matching loss, batch 4, 32 x 32 x 64 latents (1024 image tokens) and 512 text tokens drawn
+N(0, 1) at width D (the workload names no text source), t ~ U(0, 1), D 3072, 24 heads, F 12288.
+
+The oracle runs the chain at the bf16-autocast precision, holding every tensor the chain stores
+in bf16 (the embedded tokens, the block output) as bf16 values.  The bars: z_t to float32
+rounding; the prediction within 2e-2 x RMS (the block bar); the loss within 1e-4 relative (the
+loss bar for fp32 latents).  (On these inputs the bf16-autocast and the pure float64 chains'
+losses differ by 6e-5 relative, so the float64 chain, twice the CPU time, is not rerun here.)
+"""
+import numpy as np
+import pytest
+import torch
+
+from diffusion_transformer_flux_gb300 import _lib as L
+from diffusion_transformer_flux_gb300 import synth
+from oracle import flux as O
+
+from gpu_util import assert_parity, dev, host, upload_weights
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib_loaded():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    L.load()
+
+
+def _oracle_chain(z0, z1, t, txt, vec, ids, wi, wt, emb, head, H, lat, mm_cast):
+    rb = mm_cast if mm_cast is not None else (lambda a: np.asarray(a, np.float64))
+    zt = O.flow_match_noise(z0, z1, t)
+    x_img = rb(O.img_in(rb(zt), emb["w"], emb["b"], mm_cast))
+    cos, sin = O.rope_cos_sin(ids)
+    y_img, _ = O.double_block(x_img, txt, vec, cos, sin, wi, wt, H, mm_cast=mm_cast)
+    pred = O.final_layer(rb(y_img), vec, head["w_ada"], head["b_ada"], head["w_out"], head["b_out"],
+                         lat, lat, mm_cast=mm_cast)
+    return zt, pred, O.flow_match_loss(pred, z0, z1)
+
+
+def test_chain_12b_blocks_at_512px():
+    B, lat, S_t, D, H, F, C = 4, 32, 512, 3072, 24, 12288, 64
+    S_i = lat * lat
+    rng_in = np.random.Generator(np.random.PCG64(1002))
+    rng_w = np.random.Generator(np.random.PCG64(2002))
+    z0, z1 = synth.latent_pair(rng_in, B, C, lat, lat)
+    t = synth.timesteps(rng_in, B, "uniform")
+    txt = synth.bf16_round(rng_in.standard_normal((B, S_t, D), dtype=np.float32))
+    vec = synth.bf16_round(rng_in.standard_normal((B, D), dtype=np.float32))
+    ids = synth.position_ids(B, lat, lat, S_t)
+    emb = synth.embed_weights(rng_w, C, D, "bf16")
+    wi = synth.stream_weights(rng_w, D, H, 128, F, "bf16")
+    wt = synth.stream_weights(rng_w, D, H, 128, F, "bf16")
+    head = synth.final_layer_weights(rng_w, D, C, "bf16")
+
+    # ---- GPU chain through the C ABI
+    bf = torch.bfloat16
+    g_z0, g_z1 = dev(z0, torch.float32), dev(z1, torch.float32)
+    g_t = dev(t, torch.float32)
+    g_ids = torch.from_numpy(ids).cuda()
+    cos = torch.empty(B, S_i + S_t, 64, device="cuda")
+    sin = torch.empty_like(cos)
+    L.rope3d_freqs(g_ids, (16, 56, 56), 10000.0, cos, sin)
+    zt = torch.empty_like(g_z0)
+    ws_flow = L.flow_match_noise_and_loss(g_z0, g_z1, g_t, z_t=zt)
+    x_img = torch.empty(B, S_i, D, device="cuda", dtype=bf)
+    L.mmdit_img_in_fwd(zt, dev(emb["w"]), dev(emb["b"]), x_img)
+    x_txt = dev(txt)
+    y_img, y_txt = torch.empty_like(x_img), torch.empty_like(x_txt)
+    dims = L.make_dims(B, S_i, S_t, D, H, F, L.MMDIT_BF16)
+    ws = L.mmdit_double_block_fwd(dims, upload_weights(wi, "bf16"), upload_weights(wt, "bf16"), dev(vec),
+                                  cos, sin, x_img, x_txt, y_img, y_txt)
+    pred = torch.empty_like(g_z0)
+    dims_head = L.make_dims(B, S_i, 0, D, H, F, L.MMDIT_BF16)
+    L.mmdit_final_layer_fwd(dims_head, lat, lat, y_img, dev(vec), dev(head["w_ada"]), dev(head["b_ada"]),
+                            dev(head["w_out"]), dev(head["b_out"]), pred)
+    loss = torch.zeros(1, device="cuda")
+    L.flow_match_noise_and_loss(g_z0, g_z1, g_t, pred=pred, loss=loss, ws=ws_flow)
+    torch.cuda.synchronize()
+    assert L.mmdit_workspace_status(ws) == 0
+
+    # ---- oracle chains
+    args = (z0, z1, t, txt, vec, ids, wi, wt, emb, head, H, lat)
+    zt_ref, pred_ref, loss_ref = _oracle_chain(*args, mm_cast=O.round_bf16)
+
+    assert_parity(host(zt), zt_ref, 1e-6, "z_t")
+    assert_parity(host(pred), pred_ref, 2e-2, "predicted velocity")
+    got = float(loss.item())
+    print(f"[chain 512px] loss GPU {got:.6f}, bf16-autocast oracle {loss_ref:.6f}")
+    assert abs(got - loss_ref) <= 1e-4 * loss_ref, (got, loss_ref)
