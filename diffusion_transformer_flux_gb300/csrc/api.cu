@@ -65,6 +65,16 @@ struct Carver {
 
 void count_launch(int n) { g_launches += static_cast<uint64_t>(n); }
 
+namespace {
+thread_local bool g_pdl_armed = false;
+}
+void pdl_begin_call() { g_pdl_armed = false; }
+bool pdl_next_launch() {
+  const bool armed = g_pdl_armed;
+  g_pdl_armed = true;
+  return armed;
+}
+
 int set_last_error(int status, const char* msg) {
   return static_cast<int>(fail(static_cast<mmdit_status>(status), "%s", msg));
 }
@@ -607,6 +617,7 @@ mmdit_status rope3d_freqs(const float* ids, int32_t batch, int32_t seq, const in
   if (static_cast<int64_t>(batch) * seq == 0) return MMDIT_OK;
   if (!ids || !cos_out || !sin_out) return fail(MMDIT_ERR_INVALID_ARG, "NULL ids or output");
   const int axes[3] = {axes_dim[0], axes_dim[1], axes_dim[2]};
+  pdl_begin_call();
   ProfScope ps_("rope3d_freqs", static_cast<cudaStream_t>(stream));
   MMDIT_CUDA(launch_rope3d(ids, batch, seq, axes, theta, cos_out, sin_out,
                            static_cast<cudaStream_t>(stream)),
@@ -624,6 +635,7 @@ mmdit_status mmdit_modulation_fwd(int32_t act, int32_t batch, int32_t rows, int3
   mmdit_status s = check_ptrs({vec, w, out}, "modulation");
   if (s != MMDIT_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  pdl_begin_call();
   ProfScope ps_("modulation", st);
   MMDIT_CUDA(launch_modulation(act, vec, w, bias, batch, rows, dim, out, st), "modulation");
   return MMDIT_OK;
@@ -658,6 +670,7 @@ mmdit_status flow_match_noise_and_loss(int32_t dtype, const void* z0, const void
   const int64_t n = static_cast<int64_t>(batch) * n_per_sample;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
   ProfScope ps_(pred ? (z_t ? "flow_match.noise_loss" : "flow_match.loss") : "flow_match.noise", st);
   MMDIT_CUDA(launch_flow_match(dtype, z0, z1, t, batch, n_per_sample, z_t, pred, loss,
                                at<float>(workspace, kStatusBytes), flow_partial_blocks(n), st),
@@ -689,6 +702,7 @@ mmdit_status mmdit_linear_fwd(int32_t act, int32_t M, int32_t N, int32_t K, cons
     return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
   if (M == 0) return MMDIT_OK;
   const int splits = choose_splits(M, N, K, static_cast<int>(elt_bytes(act)));
   GemmProblem g;
@@ -731,6 +745,7 @@ mmdit_status mmdit_img_in_fwd(int32_t act, int32_t batch, int32_t channels, int3
     return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
   void* tokens = at(workspace, kStatusBytes);
   const int hw = lat_h * lat_w;
   ProfScope ps_("img_in", st);
@@ -771,6 +786,7 @@ mmdit_status mmdit_final_layer_fwd(const mmdit_dims* d, int32_t channels, int32_
     return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
   Carver c;
   float* mod = at<float>(workspace, c.take(static_cast<size_t>(d->batch) * 2 * d->hidden * 4));
   void* h = at(workspace, c.take(static_cast<size_t>(d->batch) * d->seq_img * d->hidden * elt_bytes(d->act)));
@@ -819,6 +835,7 @@ mmdit_status mmdit_attention_fwd(int32_t act, int32_t batch, int32_t heads, int3
     return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
   const int seq_pad = static_cast<int>(round_up(static_cast<size_t>(seq), 8));
   __half* vt = at<__half>(workspace, kStatusBytes);
   ProfScope ps_("attention", st);
@@ -880,6 +897,7 @@ mmdit_status mmdit_double_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
   if ((s = check_workspace(workspace, workspace_bytes, p.total)) != MMDIT_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
   {
     // both streams' AdaLN modulation in one launch (they share vec), unless precomputed
     ModulationJob jobs[2];
@@ -929,6 +947,7 @@ mmdit_status mmdit_single_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
   if ((s = check_workspace(workspace, workspace_bytes, p.total)) != MMDIT_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
   if (!w->mod) {
     ProfScope ps_("single.modulation", st);
     MMDIT_CUDA(launch_modulation(d->act, vec, w->w_mod, w->b_mod, p.B, 6 * p.D, p.D,
@@ -960,6 +979,7 @@ mmdit_status mmdit_fp8_quantize_e4m3(const void* x, int64_t n, const float* scal
     return fail(MMDIT_ERR_INVALID_ARG, "E4M3 cast: scale and amax must be 4-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const QuantJob job{static_cast<const __nv_bfloat16*>(x), static_cast<uint8_t*>(out), n, scale, amax};
+  pdl_begin_call();
   ProfScope ps_("fp8_quantize", st);
   MMDIT_CUDA(launch_quantize_e4m3(&job, 1, st), "E4M3 cast");
   return MMDIT_OK;
@@ -981,6 +1001,7 @@ mmdit_status mmdit_fp8_linear_fwd(int32_t M, int32_t N, int32_t K, const void* x
   if (M == 0) return MMDIT_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
   GemmProblem g;
   g.act = 2, g.epi = kEpiBias, g.M = M, g.N = N, g.K = K, g.A = x, g.W = w;
   g.ep.bias = b, g.ep.out = y, g.ep.scale_a = scale_x, g.ep.scale_w = scale_w;

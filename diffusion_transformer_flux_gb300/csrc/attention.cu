@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sb->tmem_slot;
+  pdl_wait();  // the set-up above overlapped the previous kernel; its results are visible now
 
   if (warp == 0) {
     if (lane == 0) {
@@ -390,14 +391,17 @@ cudaError_t launch_attention(const AttnProblem& p, uint32_t* status, cudaStream_
     if (e != cudaSuccess) return e;
     configured = dev;
   }
-  if (p.act == 1)
-    attention_kernel<__nv_bfloat16><<<grid, kAttnThreads, kAttnSmem, stream>>>(
+  if (p.act == 1) {
+    const cudaError_t e_ = launch_pdl(attention_kernel<__nv_bfloat16>, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream,
         tq, tk, tv, p.heads, p.seq, p.split, static_cast<__nv_bfloat16*>(p.out0),
         static_cast<__nv_bfloat16*>(p.out1), status);
-  else
-    attention_kernel<float><<<grid, kAttnThreads, kAttnSmem, stream>>>(
+    if (e_ != cudaSuccess) return e_;
+  } else {
+    const cudaError_t e_ = launch_pdl(attention_kernel<float>, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream,
         tq, tk, tv, p.heads, p.seq, p.split, static_cast<float*>(p.out0), static_cast<float*>(p.out1),
         status);
+    if (e_ != cudaSuccess) return e_;
+  }
   count_launch();
   return cudaGetLastError();
 }

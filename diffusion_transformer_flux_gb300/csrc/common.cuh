@@ -380,6 +380,17 @@ __device__ __forceinline__ void store32(float* p, const float (&v)[32]) {
 }
 
 
+// ----------------------------------------------------------------------------- dependent launch
+// Kernels are launched with programmatic stream serialization (launch_pdl in internal.h), so a
+// kernel's CTAs may be scheduled, and run their set-up, while the previous kernel in the stream
+// finishes.  pdl_wait() blocks until that kernel has completed and its memory is visible (a
+// no-op when there is none); every kernel calls it before it touches global memory.
+// pdl_trigger() lets the next kernel in the stream begin launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------- CTA pairs
 // Two CTAs of a cluster working as one tcgen05 pair (cta_group::2): rank 0 is the leader that
 // issues the MMAs; the pair's operands and accumulators live in both CTAs' shared and tensor

@@ -48,6 +48,7 @@ struct RopeTable {
 
 __global__ void rope3d_kernel(const float* __restrict__ ids, int64_t n_tok, RopeTable tab,
                               float* __restrict__ cos_out, float* __restrict__ sin_out) {
+  pdl_wait();  // the previous kernel's results are visible from here on
   const int64_t total = n_tok * tab.pairs;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -101,6 +102,7 @@ struct Raw8<float> {
 template <typename T, int NC, int NB>
 __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __restrict__ vec, ModJob j0,
                                                                  ModJob j1, int dim) {
+  pdl_wait();  // the previous kernel's results are visible from here on
   constexpr int batch = NB;  // batch rows handled by this launch (compile time: no idle lanes)
   extern __shared__ float svec[];  // [batch, dim] SiLU(vec), a bf16 operand in bf16 mode
   for (int i = threadIdx.x; i < batch * dim; i += blockDim.x) {
@@ -205,6 +207,7 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 
 template <typename TI, typename T, int NCT>
 __global__ void __launch_bounds__(kLnThreads) ln_modulate_kernel(LnJob j0, LnJob j1, int dim, float eps) {
+  pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ float red[kLnThreads / 32];
   const int g = blockIdx.x;
   const bool second = g >= j0.rows;
@@ -276,6 +279,7 @@ __global__ void __launch_bounds__(kLnThreads) ln_modulate_kernel(LnJob j0, LnJob
 // z [B, C, HW] fp32 -> out [B, HW, C]
 template <typename T>
 __global__ void patchify_kernel(const float* __restrict__ z, int channels, int hw, T* __restrict__ out) {
+  pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ float tile[32][33];
   const int b = blockIdx.z;
   const int s0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
@@ -300,6 +304,7 @@ __global__ void patchify_kernel(const float* __restrict__ z, int channels, int h
 // v [BH, S, 128] bf16 -> vt [BH, 128, S_pad] fp16
 __global__ void transpose_v_kernel(const __nv_bfloat16* __restrict__ v, int seq, int seq_pad,
                                    __half* __restrict__ vt) {
+  pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ __nv_bfloat16 tile[32][34];
   const size_t bh = blockIdx.z;
   const int s0 = blockIdx.x * 32, j0 = blockIdx.y * 32;
@@ -321,6 +326,7 @@ template <typename T>
 __global__ void splitk_reduce_kernel(const float* __restrict__ partials, int splits, int M, int N,
                                      const T* __restrict__ bias, void* __restrict__ out,
                                      int unpatchify_rows) {
+  pdl_wait();  // the previous kernel's results are visible from here on
   const int64_t total = static_cast<int64_t>(M) * N / 8;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -361,6 +367,7 @@ __global__ void __launch_bounds__(kFlowThreads) flow_kernel(const T* __restrict_
                                                             int64_t n_total, T* __restrict__ z_t,
                                                             const T* __restrict__ pred,
                                                             float* __restrict__ partials) {
+  pdl_wait();  // the previous kernel's results are visible from here on
   float acc = 0.f;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
   for (int64_t i = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) * 8; i < n_total;
@@ -401,6 +408,7 @@ __global__ void __launch_bounds__(kFlowThreads) flow_kernel(const T* __restrict_
 __global__ void __launch_bounds__(kFlowThreads) flow_finish_kernel(const float* __restrict__ partials,
                                                                    int n, double inv_total,
                                                                    float* __restrict__ loss) {
+  pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ float red[kFlowThreads / 32];
   float v = 0.f;
   for (int i = threadIdx.x; i < n; i += blockDim.x) v += partials[i];
@@ -436,7 +444,10 @@ cudaError_t launch_rope3d(const float* ids, int batch, int seq, const int axes[3
   const int64_t n_tok = static_cast<int64_t>(batch) * seq;
   if (n_tok == 0 || j == 0) return cudaSuccess;
   const int grid = blocks_for(n_tok * j, 256, num_sms() * 8);
-  rope3d_kernel<<<grid, 256, 0, stream>>>(ids, n_tok, tab, cos_out, sin_out);
+  {
+    const cudaError_t e_ = launch_pdl(rope3d_kernel, dim3(grid), dim3(256), 0, stream, ids, n_tok, tab, cos_out, sin_out);
+    if (e_ != cudaSuccess) return e_;
+  }
   count_launch();
   return cudaGetLastError();
 }
@@ -458,7 +469,10 @@ cudaError_t launch_mod(const void* vec, const ModJob& j0, const ModJob& j1, int 
   if (per_sm < 1) per_sm = 1;
   const int rows = j0.rows + j1.rows;
   const int grid = blocks_for(rows, kModThreads / 32, num_sms() * per_sm);
-  kern<<<grid, kModThreads, smem, stream>>>(static_cast<const T*>(vec), j0, j1, dim);
+  {
+    const cudaError_t e_ = launch_pdl(kern, dim3(grid), dim3(kModThreads), smem, stream, static_cast<const T*>(vec), j0, j1, dim);
+    if (e_ != cudaSuccess) return e_;
+  }
   count_launch();
   return cudaGetLastError();
 }
@@ -525,18 +539,19 @@ cudaError_t launch_ln_modulate2(int act, int x_f32, const LnModJob* jobs, int nj
   if (rows == 0) return cudaSuccess;
   const int chunks = (dim + kLnThreads * 8 - 1) / (kLnThreads * 8);
   if (chunks > kLnMaxChunks) return cudaErrorInvalidValue;
+  cudaError_t launch_err = cudaSuccess;
   auto go = [&](auto nct_tag) {
     constexpr int NCT = decltype(nct_tag)::value;
     if (out_e4m3 && x_f32)
-      ln_modulate_kernel<float, uint8_t, NCT><<<rows, kLnThreads, 0, stream>>>(j[0], j[1], dim, eps);
+      launch_err = launch_pdl(ln_modulate_kernel<float, uint8_t, NCT>, dim3(rows), dim3(kLnThreads), 0, stream, j[0], j[1], dim, eps);
     else if (out_e4m3)
-      ln_modulate_kernel<__nv_bfloat16, uint8_t, NCT><<<rows, kLnThreads, 0, stream>>>(j[0], j[1], dim, eps);
+      launch_err = launch_pdl(ln_modulate_kernel<__nv_bfloat16, uint8_t, NCT>, dim3(rows), dim3(kLnThreads), 0, stream, j[0], j[1], dim, eps);
     else if (act == 1 && x_f32)
-      ln_modulate_kernel<float, __nv_bfloat16, NCT><<<rows, kLnThreads, 0, stream>>>(j[0], j[1], dim, eps);
+      launch_err = launch_pdl(ln_modulate_kernel<float, __nv_bfloat16, NCT>, dim3(rows), dim3(kLnThreads), 0, stream, j[0], j[1], dim, eps);
     else if (act == 1)
-      ln_modulate_kernel<__nv_bfloat16, __nv_bfloat16, NCT><<<rows, kLnThreads, 0, stream>>>(j[0], j[1], dim, eps);
+      launch_err = launch_pdl(ln_modulate_kernel<__nv_bfloat16, __nv_bfloat16, NCT>, dim3(rows), dim3(kLnThreads), 0, stream, j[0], j[1], dim, eps);
     else
-      ln_modulate_kernel<float, float, NCT><<<rows, kLnThreads, 0, stream>>>(j[0], j[1], dim, eps);
+      launch_err = launch_pdl(ln_modulate_kernel<float, float, NCT>, dim3(rows), dim3(kLnThreads), 0, stream, j[0], j[1], dim, eps);
   };
   if (chunks <= 1)
     go(std::integral_constant<int, 1>());
@@ -548,8 +563,9 @@ cudaError_t launch_ln_modulate2(int act, int x_f32, const LnModJob* jobs, int nj
     go(std::integral_constant<int, 4>());
   else
     go(std::integral_constant<int, kLnMaxChunks>());
+  if (launch_err != cudaSuccess) return launch_err;
   count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_ln_modulate(int act, int x_f32, const void* x, const float* shift, const float* scale,
@@ -562,11 +578,14 @@ cudaError_t launch_ln_modulate(int act, int x_f32, const void* x, const float* s
 cudaError_t launch_patchify(int act, const float* z, int batch, int channels, int hw, void* out,
                             cudaStream_t stream) {
   const dim3 grid((hw + 31) / 32, (channels + 31) / 32, batch), block(32, 8);
-  if (act == 1)
-    patchify_kernel<__nv_bfloat16><<<grid, block, 0, stream>>>(z, channels, hw,
+  if (act == 1) {
+    const cudaError_t e_ = launch_pdl(patchify_kernel<__nv_bfloat16>, dim3(grid), dim3(block), 0, stream, z, channels, hw,
                                                                static_cast<__nv_bfloat16*>(out));
-  else
-    patchify_kernel<float><<<grid, block, 0, stream>>>(z, channels, hw, static_cast<float*>(out));
+    if (e_ != cudaSuccess) return e_;
+  } else {
+    const cudaError_t e_ = launch_pdl(patchify_kernel<float>, dim3(grid), dim3(block), 0, stream, z, channels, hw, static_cast<float*>(out));
+    if (e_ != cudaSuccess) return e_;
+  }
   count_launch();
   return cudaGetLastError();
 }
@@ -574,7 +593,10 @@ cudaError_t launch_patchify(int act, const float* z, int batch, int channels, in
 cudaError_t launch_transpose_v(const __nv_bfloat16* v, int bh, int seq, int seq_pad, __half* vt,
                                cudaStream_t stream) {
   const dim3 grid((seq + 31) / 32, 4, bh), block(32, 8);
-  transpose_v_kernel<<<grid, block, 0, stream>>>(v, seq, seq_pad, vt);
+  {
+    const cudaError_t e_ = launch_pdl(transpose_v_kernel, dim3(grid), dim3(block), 0, stream, v, seq, seq_pad, vt);
+    if (e_ != cudaSuccess) return e_;
+  }
   count_launch();
   return cudaGetLastError();
 }
@@ -585,13 +607,16 @@ cudaError_t launch_splitk_reduce(int act, const float* partials, int splits, int
   const int64_t total = static_cast<int64_t>(M) * N / 8;
   if (total == 0) return cudaSuccess;
   const int grid = blocks_for(total, 256, num_sms() * 8);
-  if (act == 1)
-    splitk_reduce_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+  if (act == 1) {
+    const cudaError_t e_ = launch_pdl(splitk_reduce_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, stream,
         partials, splits, M, N, static_cast<const __nv_bfloat16*>(bias), out, unpatchify_rows);
-  else
-    splitk_reduce_kernel<float><<<grid, 256, 0, stream>>>(partials, splits, M, N,
+    if (e_ != cudaSuccess) return e_;
+  } else {
+    const cudaError_t e_ = launch_pdl(splitk_reduce_kernel<float>, dim3(grid), dim3(256), 0, stream, partials, splits, M, N,
                                                           static_cast<const float*>(bias), out,
                                                           unpatchify_rows);
+    if (e_ != cudaSuccess) return e_;
+  }
   count_launch();
   return cudaGetLastError();
 }
@@ -607,21 +632,27 @@ cudaError_t launch_flow_match(int dtype, const void* z0, const void* z1, const f
   if (n_total == 0) return cudaSuccess;
   const bool want_loss = pred != nullptr && loss != nullptr;
   const int grid = n_partials;
-  if (dtype == 1)
-    flow_kernel<__nv_bfloat16><<<grid, kFlowThreads, 0, stream>>>(
+  if (dtype == 1) {
+    const cudaError_t e_ = launch_pdl(flow_kernel<__nv_bfloat16>, dim3(grid), dim3(kFlowThreads), 0, stream,
         static_cast<const __nv_bfloat16*>(z0), static_cast<const __nv_bfloat16*>(z1), t,
         n_per_sample, n_total, static_cast<__nv_bfloat16*>(z_t),
         want_loss ? static_cast<const __nv_bfloat16*>(pred) : nullptr, want_loss ? partials : nullptr);
-  else
-    flow_kernel<float><<<grid, kFlowThreads, 0, stream>>>(
+    if (e_ != cudaSuccess) return e_;
+  } else {
+    const cudaError_t e_ = launch_pdl(flow_kernel<float>, dim3(grid), dim3(kFlowThreads), 0, stream,
         static_cast<const float*>(z0), static_cast<const float*>(z1), t, n_per_sample, n_total,
         static_cast<float*>(z_t), want_loss ? static_cast<const float*>(pred) : nullptr,
         want_loss ? partials : nullptr);
+    if (e_ != cudaSuccess) return e_;
+  }
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !want_loss) return e;
-  flow_finish_kernel<<<1, kFlowThreads, 0, stream>>>(partials, grid, 1.0 / static_cast<double>(n_total),
+  {
+    const cudaError_t e_ = launch_pdl(flow_finish_kernel, dim3(1), dim3(kFlowThreads), 0, stream, partials, grid, 1.0 / static_cast<double>(n_total),
                                                      loss);
+    if (e_ != cudaSuccess) return e_;
+  }
   count_launch();
   return cudaGetLastError();
 }

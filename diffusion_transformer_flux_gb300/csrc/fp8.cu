@@ -27,6 +27,7 @@ struct QuantJobs {
 // Every tile lies inside one job; a thread converts kQRounds groups of 16 elements.
 __global__ void __launch_bounds__(kQThreads) quantize_e4m3_kernel(const __grid_constant__ QuantJobs jobs,
                                                                   int64_t tiles) {
+  pdl_wait();  // the previous kernel's results are visible from here on
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
     int j = 0;
     while (j + 1 < jobs.njobs && t >= jobs.tile_start[j + 1]) ++j;
@@ -69,12 +70,14 @@ __global__ void __launch_bounds__(kQThreads) quantize_e4m3_kernel(const __grid_c
 }
 
 __global__ void amax_reset_kernel(float* hist, int hist_len, int n, int pos) {
+  pdl_wait();  // the previous kernel's results are visible from here on
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) hist[static_cast<size_t>(i) * hist_len + pos] = 0.f;
 }
 
 __global__ void scale_update_kernel(const float* hist, float* scale, int hist_len, int n, int pos,
                                     int margin) {
+  pdl_wait();  // the previous kernel's results are visible from here on
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   const float a = hist[static_cast<size_t>(i) * hist_len + pos];
@@ -101,14 +104,20 @@ cudaError_t launch_quantize_e4m3(const QuantJob* jobs, int njobs, cudaStream_t s
   if (tiles == 0) return cudaSuccess;
   const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
-  quantize_e4m3_kernel<<<grid, kQThreads, 0, stream>>>(q, tiles);
+  {
+    const cudaError_t e_ = launch_pdl(quantize_e4m3_kernel, dim3(grid), dim3(kQThreads), 0, stream, q, tiles);
+    if (e_ != cudaSuccess) return e_;
+  }
   count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_amax_reset(float* hist, int hist_len, int n, int pos, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
-  amax_reset_kernel<<<(n + 127) / 128, 128, 0, stream>>>(hist, hist_len, n, pos);
+  {
+    const cudaError_t e_ = launch_pdl(amax_reset_kernel, dim3((n + 127) / 128), dim3(128), 0, stream, hist, hist_len, n, pos);
+    if (e_ != cudaSuccess) return e_;
+  }
   count_launch();
   return cudaGetLastError();
 }
@@ -116,7 +125,10 @@ cudaError_t launch_amax_reset(float* hist, int hist_len, int n, int pos, cudaStr
 cudaError_t launch_scale_update(const float* hist, float* scale, int hist_len, int n, int pos,
                                 int margin, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
-  scale_update_kernel<<<(n + 127) / 128, 128, 0, stream>>>(hist, scale, hist_len, n, pos, margin);
+  {
+    const cudaError_t e_ = launch_pdl(scale_update_kernel, dim3((n + 127) / 128), dim3(128), 0, stream, hist, scale, hist_len, n, pos, margin);
+    if (e_ != cudaSuccess) return e_;
+  }
   count_launch();
   return cudaGetLastError();
 }

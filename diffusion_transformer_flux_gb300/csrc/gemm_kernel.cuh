@@ -340,6 +340,8 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the set-up above overlapped the previous kernel; its results are visible now
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -490,8 +492,12 @@ cudaError_t run_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream
   const int tiles = ((p.M + kBM - 1) / kBM + (two ? (p.M1 + kBM - 1) / kBM : 0)) * num_n * splits;
   if (tiles == 0) return cudaSuccess;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  kern<<<grid, gemm_threads<EPI>(), Cfg::kSmemBytes, stream>>>(ta0, tb0, ta1, tb1, p.M, two ? p.M1 : 0, p.N,
-                                                        p.K, splits, p.ep, two ? p.ep1 : p.ep, status);
+  {
+    const cudaError_t e_ = launch_pdl(kern, dim3(grid), dim3(gemm_threads<EPI>()), Cfg::kSmemBytes, stream, ta0,
+                                        tb0, ta1, tb1, p.M, two ? p.M1 : 0, p.N, p.K, splits, p.ep,
+                                        two ? p.ep1 : p.ep, status);
+    if (e_ != cudaSuccess) return e_;
+  }
   count_launch();
   return cudaGetLastError();
 }

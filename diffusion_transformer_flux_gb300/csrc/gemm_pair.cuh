@@ -91,6 +91,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<EPI>(),
   cluster_sync();  // both CTAs' barriers initialised and tensor memory allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the set-up above overlapped the previous kernel; its results are visible now
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -252,8 +254,12 @@ cudaError_t run_gemm_pair(const GemmProblem& p, uint32_t* status, cudaStream_t s
   const int tiles = ((p.M + 2 * kBM - 1) / (2 * kBM) + (two ? (p.M1 + 2 * kBM - 1) / (2 * kBM) : 0)) * num_n;
   if (tiles == 0) return cudaSuccess;
   const int pairs = tiles < max_pairs ? tiles : max_pairs;
-  kern<<<2 * pairs, gemm_threads<EPI>(), Cfg::kSmemBytes, stream>>>(
-      ta0, tb0, ta1, tb1, p.M, two ? p.M1 : 0, p.N, p.K, p.ep, two ? p.ep1 : p.ep, status);
+  {
+    const cudaError_t e_ = launch_pdl(kern, dim3(2 * pairs), dim3(gemm_threads<EPI>()), Cfg::kSmemBytes, stream,
+                                        ta0, tb0, ta1, tb1, p.M, two ? p.M1 : 0, p.N, p.K, p.ep,
+                                        two ? p.ep1 : p.ep, status);
+    if (e_ != cudaSuccess) return e_;
+  }
   count_launch();
   return cudaGetLastError();
 }

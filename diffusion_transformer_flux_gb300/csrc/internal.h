@@ -71,6 +71,31 @@ struct GemmProblem {
   EpiArgs ep1;
 };
 
+// Programmatic dependent launch within one library call.  pdl_begin_call() marks the start of
+// a call on the calling thread; its first kernel then launches as an ordinary launch (it must
+// wait for whatever the caller enqueued before it: copies, memsets, other libraries' kernels),
+// and each later kernel of the call launches with programmatic stream serialization, so it may
+// be scheduled while the call's previous kernel finishes.  Every kernel calls pdl_wait()
+// (common.cuh) before it touches global memory, so results are those of ordinary launches.
+void pdl_begin_call();
+bool pdl_next_launch();  // false for the call's first launch, true afterwards
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_next_launch() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Device status word layout: the first 4 bytes of every workspace.
 constexpr size_t kStatusBytes = 256;
 

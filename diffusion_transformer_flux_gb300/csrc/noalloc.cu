@@ -94,6 +94,7 @@ extern "C" mmdit_status flow_match_noise_and_loss_noalloc(int32_t dtype, const v
   cudaError_t e = noalloc_partials(&partials);
   if (e != cudaSuccess) return err(MMDIT_ERR_CUDA, cudaGetErrorString(e));
   const int n_partials = static_cast<int>((n_total + kElemsPerPartial - 1) / kElemsPerPartial);
+  pdl_begin_call();  // the first kernel waits for everything enqueued before the call
   e = launch_flow_match(dtype, z0, z1, t, batch, n_per_sample, z_t, pred, loss, partials,
                         n_partials, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return err(MMDIT_ERR_CUDA, cudaGetErrorString(e));
