@@ -104,12 +104,15 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __rest
                                                                  ModJob j1, int dim) {
   pdl_wait();  // the previous kernel's results are visible from here on
   constexpr int batch = NB;  // batch rows handled by this launch (compile time: no idle lanes)
-  extern __shared__ float svec[];  // [batch, dim] SiLU(vec), a bf16 operand in bf16 mode
+  // [batch, dim] SiLU(vec): fp32, or in bf16 mode the bf16 operand it is there (stored as bf16,
+  // so each 16-byte weight load pairs with one 16-byte shared-memory load)
+  extern __shared__ float svec[];
+  __nv_bfloat16* svec_bf = reinterpret_cast<__nv_bfloat16*>(svec);
   for (int i = threadIdx.x; i < batch * dim; i += blockDim.x) {
     const float v = to_f32(vec[i]);
     const float sv = v / (1.f + expf(-v));
     if constexpr (sizeof(T) == 2)
-      svec[i] = __bfloat162float(__float2bfloat16_rn(sv));
+      svec_bf[i] = __float2bfloat16_rn(sv);
     else
       svec[i] = sv;
   }
@@ -145,10 +148,19 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __rest
         raw[c].to_f32(wv);
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-          const float4 s0 = *reinterpret_cast<const float4*>(svec + b * dim + k);
-          const float4 s1 = *reinterpret_cast<const float4*>(svec + b * dim + k + 4);
-          acc[b] += wv[0] * s0.x + wv[1] * s0.y + wv[2] * s0.z + wv[3] * s0.w + wv[4] * s1.x +
-                    wv[5] * s1.y + wv[6] * s1.z + wv[7] * s1.w;
+          float sv[8];
+          if constexpr (sizeof(T) == 2) {
+            const uint4 u = *reinterpret_cast<const uint4*>(svec_bf + b * dim + k);
+            sv[0] = bf16_lo(u.x), sv[1] = bf16_hi(u.x), sv[2] = bf16_lo(u.y), sv[3] = bf16_hi(u.y);
+            sv[4] = bf16_lo(u.z), sv[5] = bf16_hi(u.z), sv[6] = bf16_lo(u.w), sv[7] = bf16_hi(u.w);
+          } else {
+            const float4 s0 = *reinterpret_cast<const float4*>(svec + b * dim + k);
+            const float4 s1 = *reinterpret_cast<const float4*>(svec + b * dim + k + 4);
+            sv[0] = s0.x, sv[1] = s0.y, sv[2] = s0.z, sv[3] = s0.w;
+            sv[4] = s1.x, sv[5] = s1.y, sv[6] = s1.z, sv[7] = s1.w;
+          }
+          acc[b] += wv[0] * sv[0] + wv[1] * sv[1] + wv[2] * sv[2] + wv[3] * sv[3] + wv[4] * sv[4] +
+                    wv[5] * sv[5] + wv[6] * sv[6] + wv[7] * sv[7];
         }
       }
     }
