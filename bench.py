@@ -69,6 +69,21 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(dist, x: float, device="cpu") -> float:
+    """The largest of every rank's x (the slowest rank's time); x itself on one process."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step: float, steps: int, world: int, seconds: float) -> float:
+    """Work of all ranks (each runs the same step on its own replica) over the slowest time."""
+    return world * flops_per_rank_step * steps / seconds / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -549,12 +564,6 @@ def main():
         if dist is not None:
             dist.barrier()
 
-    def max_over_ranks(x: float) -> float:
-        if dist is None:
-            return x
-        t = torch.tensor([x], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
     def timed(fn, k):
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -610,8 +619,8 @@ def main():
     clocks = clk.summary()
     if not bool(torch.isfinite(st.result()).all()):
         raise RuntimeError("non-finite result")
-    total_s = max_over_ranks(sum(ms) / 1e3)
-    value = world * st.flops_blocks * args.steps / total_s / 1e12
+    total_s = max_over_ranks(dist, sum(ms) / 1e3, device)
+    value = whole_job_tflops(st.flops_blocks, args.steps, world, total_s)
 
     # end to end: this step's inputs from pinned host memory, the loss back to the host
     pinned = {n: getattr(st, n).detach().cpu().pin_memory() for n in st.input_names}
@@ -620,7 +629,7 @@ def main():
     for _ in range(2):
         st.step_from_host(pinned, result_host)
     ms_e2e, _ = timed(lambda: st.step_from_host(pinned, result_host), args.steps)
-    e2e_s = max_over_ranks(sum(ms_e2e) / 1e3)
+    e2e_s = max_over_ranks(dist, sum(ms_e2e) / 1e3, device)
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = result_host.numel() * result_host.element_size()
 
@@ -712,7 +721,7 @@ def main():
                if fp8 else {}),
             "tokens_per_s": round(world * wl.batch * S * args.steps / total_s, 1),
             "clocks": clocks,
-            "e2e": {"value": round(world * st.flops_blocks * args.steps / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+            "e2e": {"value": round(whole_job_tflops(st.flops_blocks, args.steps, world, e2e_s), 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_s / args.steps * 1e3, 4)},
             "gpu_launches": launches,
