@@ -486,6 +486,27 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def measure_euler_step(L, torch, device, hbm_peak, n=1 << 26, reps=10):
+    """The sampling step (flow_match_euler_step: guidance combine + Euler update) on n fp32
+    elements, 4 * n * 4 bytes per call (z, v_cond, v_uncond read; z_out written), inputs far
+    larger than L2; CUDA events around `reps` calls after one warm-up."""
+    z, vc, vu = (torch.randn(n, device=device) for _ in range(3))
+    out = torch.empty_like(z)
+    L.flow_match_euler_step(z, vc, vu, 3.5, 0.05, out)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        L.flow_match_euler_step(z, vc, vu, 3.5, 0.05, out)
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / reps
+    gbs = 16.0 * n / us / 1e3
+    del z, vc, vu, out
+    return {"kernel": "flow_match.euler_step", "n": n, "dtype": "f32", "bytes_per_call": 16 * n,
+            "avg_us": round(us, 2), "achieved_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4)}
+
+
 def run_cpu_baseline(hw: HostWorkload, min_seconds: float, rows=(32, 8)):
     flops, n, t0 = 0.0, 0, time.perf_counter()
     while True:
@@ -684,6 +705,8 @@ def main():
     if bound == "tensor" and "bf16_tflops_sustained" in peaks and peak == bf16_peak:
         roofline["frac_of_sustained"] = round(ach / float(peaks["bf16_tflops_sustained"]), 4)
 
+    extras = {} if fp8 else {"sampling_step": measure_euler_step(L, torch, device, hbm_peak)}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and hw is not None:
         cpu = run_cpu_baseline(hw, args.cpu_seconds)
@@ -728,6 +751,7 @@ def main():
             "roofline": roofline,
             "per_kernel": per_kernel,
             "cpu_baseline": cpu,
+            "extras": extras,
             "peaks": {"bf16_tflops": bf16_peak, "hbm_gbs": hbm_peak, "source": peak_src},
         }
         print(json.dumps(line), flush=True)

@@ -25,7 +25,7 @@ EXPORTED = [
     "mmdit_last_error", "mmdit_workspace_status", "mmdit_launch_count", "mmdit_launch_count_reset",
     "mmdit_profile_enable", "mmdit_profile_collect",
     "rope3d_freqs", "mmdit_modulation_fwd", "flow_match_workspace_size", "flow_match_noise_and_loss",
-    "flow_match_noise_and_loss_noalloc",
+    "flow_match_noise_and_loss_noalloc", "flow_match_euler_step",
     "mmdit_linear_workspace_size", "mmdit_linear_fwd", "mmdit_img_in_workspace_size",
     "mmdit_img_in_fwd", "mmdit_final_layer_workspace_size", "mmdit_final_layer_fwd",
     "mmdit_attention_workspace_size", "mmdit_attention_fwd", "mmdit_double_block_workspace_size",
@@ -59,7 +59,12 @@ class StreamW(C.Structure):
 
 class Fp8State(C.Structure):
     _fields_ = [("amax_history", C.c_void_p), ("scale", C.c_void_p), ("hist_len", C.c_int32),
-                ("n_tensors", C.c_int32), ("pos", C.c_int32)]
+                ("n_tensors", C.c_int32), ("pos", C.c_int32), ("amax_compute_algo", C.c_int32),
+                ("margin", C.c_int32)]
+
+
+AMAX_MOST_RECENT = 0
+AMAX_MAX = 1
 
 
 MMDIT_GEMM_NATIVE = 0
@@ -87,6 +92,7 @@ _SIGS = {
     "flow_match_workspace_size": (SZ, [I32, I64]),
     "flow_match_noise_and_loss": (C.c_int, [I32, VP, VP, VP, I32, I64, VP, VP, VP, VP, SZ, VP]),
     "flow_match_noise_and_loss_noalloc": (C.c_int, [I32, VP, VP, VP, I32, I64, VP, VP, VP, VP]),
+    "flow_match_euler_step": (C.c_int, [I32, I64, VP, VP, VP, F32, F32, VP, VP]),
     "mmdit_linear_workspace_size": (SZ, [I32, I32, I32, I32]),
     "mmdit_linear_fwd": (C.c_int, [I32, I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_img_in_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
@@ -247,6 +253,12 @@ def flow_match_noise_and_loss_noalloc(z0, z1, t, z_t=None, pred=None, loss=None,
                                                     _stream(stream)))
 
 
+def flow_match_euler_step(z, v_cond, v_uncond, guidance, dt, z_out, stream=None):
+    """z_out = z - dt (v_uncond + guidance (v_cond - v_uncond)); v_uncond may be None."""
+    _check(load().flow_match_euler_step(act_of(z), z.numel(), _ptr(z), _ptr(v_cond), _ptr(v_uncond),
+                                        float(guidance), float(dt), _ptr(z_out), _stream(stream)))
+
+
 def mmdit_linear_workspace_size(act, M, N, K) -> int:
     return load().mmdit_linear_workspace_size(act, M, N, K)
 
@@ -319,11 +331,12 @@ def mmdit_block_workspace_offsets(dims: Dims, single: bool) -> list:
     return list(out)[:n]
 
 
-def make_fp8_state(amax_history, scale, pos: int = 0) -> Fp8State:
+def make_fp8_state(amax_history, scale, pos: int = 0, algo: int = AMAX_MOST_RECENT,
+                   margin: int = 0) -> Fp8State:
     """The C view of a delayed-scaling state: amax_history [n_tensors, hist_len] and scale
     [n_tensors], fp32 device tensors the caller owns."""
     n, h = amax_history.shape
-    return Fp8State(_ptr(amax_history), _ptr(scale), h, n, pos)
+    return Fp8State(_ptr(amax_history), _ptr(scale), h, n, pos, algo, margin)
 
 
 def _fp8_arg(fp8):

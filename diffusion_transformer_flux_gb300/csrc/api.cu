@@ -317,6 +317,11 @@ static mmdit_status check_fp8(const mmdit_dims* d, const mmdit_fp8_state* f, int
   if (f->n_tensors < n_needed)
     return fail(MMDIT_ERR_INVALID_ARG, "fp8 state: %d tensors given, this block records %d",
                 f->n_tensors, n_needed);
+  if (f->amax_compute_algo != 0 && f->amax_compute_algo != 1)
+    return fail(MMDIT_ERR_INVALID_ARG, "fp8 state: amax_compute_algo must be 0 (most_recent) or 1 (max), got %d",
+                f->amax_compute_algo);
+  if (f->margin < 0 || f->margin > 16)
+    return fail(MMDIT_ERR_INVALID_ARG, "fp8 state: margin must be in [0, 16] (got %d)", f->margin);
   return MMDIT_OK;
 }
 
@@ -535,11 +540,11 @@ mmdit_status fp8_begin(const BlockPlan& p, const Streams& ss, const Fp8& f8, int
   return MMDIT_OK;
 }
 
-// FP8 calls: the next call's scales from the amax this call recorded (most_recent, margin 0).
+// FP8 calls: the next call's scales from the recorded amax (most_recent or the history's max).
 mmdit_status fp8_end(const BlockPlan& p, const Fp8& f8, int n_tensors, cudaStream_t st) {
   ProfScope ps_(p.single ? "single.fp8_scale" : "double.fp8_scale", st);
   MMDIT_CUDA(launch_scale_update(f8.f->amax_history, f8.f->scale, f8.f->hist_len, n_tensors, f8.f->pos,
-                                 0, st),
+                                 f8.f->margin, f8.f->amax_compute_algo, st),
              "FP8 scale update");
   return MMDIT_OK;
 }
@@ -675,6 +680,26 @@ mmdit_status flow_match_noise_and_loss(int32_t dtype, const void* z0, const void
   MMDIT_CUDA(launch_flow_match(dtype, z0, z1, t, batch, n_per_sample, z_t, pred, loss,
                                at<float>(workspace, kStatusBytes), flow_partial_blocks(n), st),
              "flow_match_noise_and_loss");
+  return MMDIT_OK;
+}
+
+mmdit_status flow_match_euler_step(int32_t dtype, int64_t n, const void* z, const void* v_cond,
+                                   const void* v_uncond, float guidance, float dt, void* z_out,
+                                   void* stream) {
+  if (dtype != MMDIT_F32 && dtype != MMDIT_BF16)
+    return fail(MMDIT_ERR_INVALID_ARG, "dtype must be MMDIT_F32 or MMDIT_BF16");
+  if (n < 0) return fail(MMDIT_ERR_INVALID_ARG, "negative element count");
+  if (n % 8 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "n must be a multiple of 8 (got %lld)", static_cast<long long>(n));
+  if (n == 0) return MMDIT_OK;
+  mmdit_status s = check_ptrs({z, v_cond, z_out}, "Euler step");
+  if (s != MMDIT_OK) return s;
+  if (v_uncond && !aligned16(v_uncond))
+    return fail(MMDIT_ERR_INVALID_ARG, "Euler step: v_uncond is not 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  pdl_begin_call();
+  ProfScope ps_("flow_match.euler_step", st);
+  MMDIT_CUDA(launch_euler_cfg(dtype, n, z, v_cond, v_uncond, guidance, dt, z_out, st), "Euler step");
   return MMDIT_OK;
 }
 

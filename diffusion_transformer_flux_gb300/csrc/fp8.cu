@@ -4,7 +4,8 @@
 //   quantize_e4m3_kernel   bf16 -> E4M3 codes of x * scale, recording max |x| (one launch casts
 //                          up to eight tensors, e.g. every weight of a block)
 //   amax_reset_kernel      zeroes the history slot a call is about to record into
-//   scale_update_kernel    scale = 448 / amax of that slot (most_recent), where amax > 0
+//   scale_update_kernel    scale = 448 / amax / 2^margin, amax of that slot (most_recent) or the
+//                          largest in the history (max), where amax > 0
 #include <math.h>
 
 #include "common.cuh"
@@ -75,13 +76,23 @@ __global__ void amax_reset_kernel(float* hist, int hist_len, int n, int pos) {
   if (i < n) hist[static_cast<size_t>(i) * hist_len + pos] = 0.f;
 }
 
+// One warp per tensor: lane 0 reads the most recent entry (algo 0), or the warp takes the
+// largest entry of the tensor's history row (algo 1).
 __global__ void scale_update_kernel(const float* hist, float* scale, int hist_len, int n, int pos,
-                                    int margin) {
+                                    int margin, int algo) {
   pdl_wait();  // the previous kernel's results are visible from here on
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int i = blockIdx.x;
   if (i >= n) return;
-  const float a = hist[static_cast<size_t>(i) * hist_len + pos];
-  if (a > 0.f && isfinite(a)) scale[i] = ldexpf(448.f / a, -margin);
+  const float* row = hist + static_cast<size_t>(i) * hist_len;
+  float a;
+  if (algo == 1) {
+    a = 0.f;
+    for (int j = threadIdx.x; j < hist_len; j += 32) a = fmaxf(a, row[j]);
+    a = warp_max(a);
+  } else {
+    a = row[pos];
+  }
+  if (threadIdx.x == 0 && a > 0.f && isfinite(a)) scale[i] = ldexpf(448.f / a, -margin);
 }
 
 }  // namespace
@@ -123,10 +134,11 @@ cudaError_t launch_amax_reset(float* hist, int hist_len, int n, int pos, cudaStr
 }
 
 cudaError_t launch_scale_update(const float* hist, float* scale, int hist_len, int n, int pos,
-                                int margin, cudaStream_t stream) {
+                                int margin, int algo, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
   {
-    const cudaError_t e_ = launch_pdl(scale_update_kernel, dim3((n + 127) / 128), dim3(128), 0, stream, hist, scale, hist_len, n, pos, margin);
+    const cudaError_t e_ = launch_pdl(scale_update_kernel, dim3(n), dim3(32), 0, stream, hist, scale,
+                                      hist_len, n, pos, margin, algo);
     if (e_ != cudaSuccess) return e_;
   }
   count_launch();

@@ -199,9 +199,15 @@ constexpr int kQuantMaxJobs = 8;
 cudaError_t launch_quantize_e4m3(const QuantJob* jobs, int njobs, cudaStream_t stream);
 // hist[i * hist_len + pos] = 0 for i < n.
 cudaError_t launch_amax_reset(float* hist, int hist_len, int n, int pos, cudaStream_t stream);
-// scale[i] = 448 / hist[i * hist_len + pos] / 2^margin where that amax is positive and finite.
+// scale[i] = 448 / amax / 2^margin where amax, positive and finite, is hist[i * hist_len + pos]
+// (algo 0, most_recent) or the largest of hist[i * hist_len + 0 .. hist_len) (algo 1, max).
 cudaError_t launch_scale_update(const float* hist, float* scale, int hist_len, int n, int pos,
-                                int margin, cudaStream_t stream);
+                                int margin, int algo, cudaStream_t stream);
+// One Euler step with classifier-free guidance: z_out = z - dt (v_uncond + w (v_cond - v_uncond)),
+// or z - dt v_cond when v_uncond is null; n a multiple of 8.
+cudaError_t launch_euler_cfg(int dtype, int64_t n, const void* z, const void* v_cond,
+                             const void* v_uncond, float guidance, float dt, void* z_out,
+                             cudaStream_t stream);
 // Rectified-flow noise and loss.
 int flow_partial_blocks(int64_t n_total);
 cudaError_t launch_flow_match(int dtype, const void* z0, const void* z1, const float* t, int batch,

@@ -117,14 +117,20 @@ typedef struct mmdit_stream_w {
  * 2 = fc1, 3 = fc2; operand 0 = the linear's input, 1 = its weight.  A double block needs
  * n_tensors >= 16, a single block >= 8.  A call zeroes column pos of those tensors, records
  * max |x| of every tensor it casts there, and, after its last linear, sets
- * scale[t] = 448 / amax_history[t, pos] for every such tensor with a positive, finite amax
- * (the others keep their scale).  Calls sharing a state must be ordered on one stream. */
+ * scale[t] = 448 / amax / 2^margin for every such tensor whose amax is positive and finite (the
+ * others keep their scale), where amax is amax_history[t, pos] with amax_compute_algo 0
+ * (most_recent) or the largest entry of row t with amax_compute_algo 1 (max; [FP8]
+ * §Troubleshooting and §Training configuration give it as the conservative choice).
+ * margin: 0 to 16 ([FP8] §Configuration fp8_margin).  Calls sharing a state must be ordered on
+ * one stream. */
 typedef struct mmdit_fp8_state {
   float *amax_history; /* [n_tensors, hist_len] */
   float *scale;        /* [n_tensors] */
   int32_t hist_len;
   int32_t n_tensors;
   int32_t pos;
+  int32_t amax_compute_algo; /* 0: most_recent, 1: max over the history */
+  int32_t margin;            /* scale = 448 / amax / 2^margin */
 } mmdit_fp8_state;
 
 /* Message for the calling thread's most recent non-OK status (never NULL). */
@@ -205,6 +211,16 @@ mmdit_status flow_match_noise_and_loss_noalloc(int32_t dtype, const void *z0, co
                                                const float *t, int32_t batch,
                                                int64_t n_per_sample, void *z_t,
                                                const void *pred, float *loss, void *stream);
+
+/* One sampling step ([ARCH] §Mathematical formulation, Sampling (inference): Euler integration
+ * from t = 1 towards t = 0, and Classifier-free guidance):
+ *   v     = v_uncond + guidance * (v_cond - v_uncond)   (v = v_cond when v_uncond is NULL)
+ *   z_out = z - dt * v                                    (z_{t - dt} = z_t - dt v_t)
+ * z, v_cond, v_uncond, z_out: [n] of type `dtype` (MMDIT_F32 or MMDIT_BF16), 16-byte aligned;
+ * z_out may alias z.  n a multiple of 8; n == 0 is a no-op.  fp32 arithmetic.  No workspace. */
+mmdit_status flow_match_euler_step(int32_t dtype, int64_t n, const void *z, const void *v_cond,
+                                   const void *v_uncond, float guidance, float dt, void *z_out,
+                                   void *stream);
 
 /* ---------------------------------------------------------------------------------------
  * Plain linear layer y = x W^T + b on the tensor cores (the text embedding txt_in of [ARCH]

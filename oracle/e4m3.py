@@ -124,3 +124,23 @@ class DelayedScaling:
     def next_scales(self, margin: int = 0):
         """The scales of the next call under ``most_recent``: 448 / amax / 2^margin."""
         return {k: delayed_scale(a, margin) for k, a in self.amax.items()}
+
+
+def history_scale(amaxes, algo: str = "most_recent", margin: int = 0) -> float:
+    """The delayed scale from a tensor's recorded amax values, oldest first.
+
+    "FP8 training for Flux models", §Configuration (``fp8_amax_compute_algo: most_recent`` or
+    ``max``, ``fp8_margin``) and §Troubleshooting (``max`` as the conservative choice): the amax
+    the scale is taken from is the most recent recorded value, or the largest in the history
+    window; the scale is then ``448 / amax / 2^margin`` (1 while no positive amax is recorded).
+    """
+    vals = [float(a) for a in amaxes]
+    if not vals:
+        return 1.0
+    if algo == "most_recent":
+        a = vals[-1]
+    elif algo == "max":
+        a = max(vals)
+    else:
+        raise ValueError(algo)
+    return delayed_scale(a, margin)

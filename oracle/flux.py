@@ -435,3 +435,17 @@ def flow_match_loss(pred, z0, z1):
     compute_flow_matching_loss)."""
     diff = _f64(pred) - flow_match_target(z0, z1)
     return float(np.mean(diff * diff))
+
+
+# ----------------------------------------------------------------------------- sampling
+def cfg_combine(v_cond, v_uncond, w):
+    """Classifier-free guidance: v_uncond + w (v_cond - v_uncond) (architecture page,
+    §Mathematical formulation › Classifier-free guidance)."""
+    v_cond, v_uncond = _f64(v_cond), _f64(v_uncond)
+    return v_uncond + float(w) * (v_cond - v_uncond)
+
+
+def euler_step(z, v, dt):
+    """One Euler step of the flow ODE towards t = 0: z_{t - dt} = z_t - dt v_t (architecture
+    page, §Sampling (inference) › Euler integration)."""
+    return _f64(z) - float(dt) * _f64(v)

@@ -94,17 +94,22 @@ def test_validation_errors_before_any_launch(lib):
                                       None, None, None, None, None, 0, None) == 1
     assert "fp8 state" in L.last_error()
     # an FP8 state with too few tensors for a double block, or a position outside the history
-    st8 = L.Fp8State(0x1000, 0x2000, 1024, 8, 0)
+    st8 = L.Fp8State(0x1000, 0x2000, 1024, 8, 0, 0, 0)
     assert lib.mmdit_double_block_fwd(C.byref(fp8), C.byref(w), C.byref(w), None, None, None, None,
                                       None, None, None, C.byref(st8), None, 0, None) == 1
     assert "tensors" in L.last_error()
-    st8 = L.Fp8State(0x1000, 0x2000, 1024, 16, 1024)
+    st8 = L.Fp8State(0x1000, 0x2000, 1024, 16, 1024, 0, 0)
     assert lib.mmdit_single_block_fwd(C.byref(fp8), C.byref(w), None, None, None, None, None,
                                       C.byref(st8), None, 0, None) == 1
     # a state given with the native linears
-    st8 = L.Fp8State(0x1000, 0x2000, 1024, 16, 0)
+    st8 = L.Fp8State(0x1000, 0x2000, 1024, 16, 0, 0, 0)
     assert lib.mmdit_single_block_fwd(C.byref(d), C.byref(w), None, None, None, None, None,
                                       C.byref(st8), None, 0, None) == 1
+    # an unknown amax algorithm, a margin out of range
+    for algo, margin in ((2, 0), (0, -1), (1, 17)):
+        st8 = L.Fp8State(0x1000, 0x2000, 1024, 16, 0, algo, margin)
+        assert lib.mmdit_double_block_fwd(C.byref(fp8), C.byref(w), C.byref(w), None, None, None, None,
+                                          None, None, None, C.byref(st8), None, 0, None) == 1
     # E4M3 cast and FP8 linear shapes
     assert lib.mmdit_fp8_quantize_e4m3(0x1000, 24, 0x2000, 0x3000, 0x4000, None) == 2
     assert lib.mmdit_fp8_quantize_e4m3(0x1000, 0, None, None, None, None) == 0
@@ -137,6 +142,10 @@ def test_validation_errors_before_any_launch(lib):
                                          0x4000, 4096, None) == 1
     assert lib.mmdit_attention_fwd(1, 1, 1, 16, 64, 0x1000, 0x1000, 0x1000, 0x1000, 0x4000, 1 << 20,
                                    None) == 2
+    # sampling step: n a multiple of 8, aligned pointers, v_uncond optional
+    assert lib.flow_match_euler_step(1, 12, 0x1000, 0x2000, None, 3.5, 0.1, 0x3000, None) == 2
+    assert lib.flow_match_euler_step(1, 16, 0x1000, 0x2000, 0x2008, 3.5, 0.1, 0x3000, None) == 1
+    assert lib.flow_match_euler_step(0, 0, None, None, None, 1.0, 0.1, None, None) == 0
 
 
 def test_library_does_not_fall_back(tmp_path, monkeypatch):

@@ -344,3 +344,39 @@ def test_fp8_blocks_at_2048px_sampled_rows(single):
     y64 = case.oracle_rows(*rows, mm_cast=None)
     got = [g[:, r] for g, r in zip(run.y, rows)]
     _check_norm_wise(got, y8, y64, "FP8 block at 2048 px")
+
+
+@pytest.mark.parametrize("algo,margin", [(L.AMAX_MAX, 0), (L.AMAX_MOST_RECENT, 1), (L.AMAX_MAX, 2)])
+def test_scale_update_over_three_calls(algo, margin):
+    """Three calls recording into history columns 0, 1, 2 with a conditioning vector scaled by
+    1, 3 and 0.5 (so the casts' amax differ from call to call); after each call every recorded
+    tensor's scale is 448 / amax / 2^margin, with amax the latest column (most_recent) or the
+    row's largest entry (max), in float32 as the pages' formula gives it (oracle.e4m3)."""
+    case = BlockCase(1, 200, 40, 256, 2, 512, "bf16", seed=5, std=0.05)
+    dims = _fp8_dims(case)
+    hist = torch.zeros(16, HIST, device="cuda")
+    scale = torch.ones(16, device="cuda")
+    ids = torch.from_numpy(case.ids).cuda()
+    cos = torch.empty(case.B, case.S, 64, device="cuda")
+    sin = torch.empty_like(cos)
+    L.rope3d_freqs(ids, (16, 56, 56), 10000.0, cos, sin)
+    wi, wt = upload_weights(case.w_img, "bf16"), upload_weights(case.w_txt, "bf16")
+    xi, xt = dev(case.x_img), dev(case.x_txt)
+    yi, yt = torch.empty_like(xi), torch.empty_like(xt)
+    name = "max" if algo == L.AMAX_MAX else "most_recent"
+    for call, f in enumerate((1.0, 3.0, 0.5)):
+        vec = dev(synth.bf16_round(case.vec * np.float32(f)))
+        st = L.make_fp8_state(hist, scale, pos=call, algo=algo, margin=margin)
+        ws = L.mmdit_double_block_fwd(dims, wi, wt, vec, cos, sin, xi, xt, yi, yt, fp8=st)
+        torch.cuda.synchronize()
+        assert L.mmdit_workspace_status(ws) == 0
+        h = hist.cpu().numpy()[:, :call + 1]
+        sc = scale.cpu().numpy()
+        assert np.all(h > 0), "every tensor records an amax in every call"
+        for t in range(16):
+            a = np.float32(h[t, -1] if name == "most_recent" else h[t].max())
+            expect = np.float32(np.ldexp(np.float32(448.0) / a, -margin))
+            assert sc[t] == expect, (call, t, sc[t], expect)
+            # the same rule as the oracle's, to float32 rounding
+            assert abs(sc[t] - E.history_scale(h[t], name, margin)) <= 1e-6 * sc[t]
+    assert not np.all(hist.cpu().numpy()[:, 0] == hist.cpu().numpy()[:, 1]), "the calls differ"

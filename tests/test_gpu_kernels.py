@@ -190,3 +190,34 @@ def test_final_layer_matches_oracle(act, B, Hh, Ww, D):
     cast = O.round_bf16 if act == "bf16" else None
     ref = O.final_layer(x, vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], Hh, Ww, mm_cast=cast)
     assert_parity(host(pred), ref, 2e-2, "final layer")
+
+
+# ----------------------------------------------------------------------------- sampling step
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("n,guided,inplace", [(8, True, False), (8 * 1001, False, False),
+                                              (262144, True, True)])
+def test_euler_cfg_step_matches_oracle(dtype, n, guided, inplace):
+    rng = np.random.default_rng(n + guided)
+    cast = synth.bf16_round if dtype == torch.bfloat16 else (lambda a: a.astype(np.float32))
+    z, vc, vu = (cast(rng.standard_normal(n).astype(np.float32)) for _ in range(3))
+    w, dt = 3.5, 0.05
+    gz, gvc = dev(z, dtype), dev(vc, dtype)
+    gvu = dev(vu, dtype) if guided else None
+    out = gz if inplace else torch.empty_like(gz)
+    L.flow_match_euler_step(gz, gvc, gvu, w, dt, out)
+    torch.cuda.synchronize()
+    ref = O.euler_step(z, O.cfg_combine(vc, vu, w) if guided else vc, dt)
+    # fp32 arithmetic, then the output's own rounding
+    assert_parity(host(out), ref, 1e-6, f"Euler step n={n}", out_bf16=dtype == torch.bfloat16)
+
+
+def test_euler_steps_follow_the_straight_line_flow_on_gpu():
+    """Ten Euler steps of 0.1 from z1 along v = z1 - z0 land on z0 (Euler is exact there)."""
+    rng = np.random.default_rng(17)
+    z0, z1 = synth.latent_pair(rng, 2, 64, 16, 16)
+    v = dev((z1 - z0).astype(np.float32), torch.float32)
+    z = dev(z1, torch.float32)
+    for _ in range(10):
+        L.flow_match_euler_step(z, v, None, 1.0, 0.1, z)
+    torch.cuda.synchronize()
+    assert_parity(host(z), z0, 1e-5, "z after ten Euler steps")

@@ -146,3 +146,29 @@ def test_fp8_linear_is_exact_on_representable_operands():
     x = np.vectorize(E.e4m3_decode)(codes)
     w = np.vectorize(E.e4m3_decode)(RNG.integers(0x30, 0x48, size=(3, 6)))
     np.testing.assert_array_equal(E.fp8_linear(x, w, None, 1.0, 1.0), x @ w.T)
+
+
+# ----------------------------------------------------------------------------- sampling
+def test_cfg_combine_special_cases():
+    vc, vu = RNG.standard_normal(50), RNG.standard_normal(50)
+    # w = 1 gives the conditional velocity, w = 0 the unconditional one (to rounding)
+    np.testing.assert_allclose(O.cfg_combine(vc, vu, 1.0), vc, rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(O.cfg_combine(vc, vu, 0.0), vu)
+    # affine in w: the midpoint of w = 1 and w = 3 is w = 2
+    np.testing.assert_allclose(O.cfg_combine(vc, vu, 2.0),
+                               0.5 * (O.cfg_combine(vc, vu, 1.0) + O.cfg_combine(vc, vu, 3.0)), atol=1e-14)
+
+
+def test_euler_is_exact_on_the_straight_line_flow():
+    # z_t = (1 - t) z0 + t z1 has the constant velocity z1 - z0: stepping from z1 (t = 1) to
+    # t = 0 in any number of Euler steps lands on z0, and every intermediate is z_t
+    z0, z1 = RNG.standard_normal(40), RNG.standard_normal(40)
+    v = O.flow_match_target(z0, z1)
+    for n in (1, 4, 10):
+        z, t = z1.copy(), 1.0
+        for _ in range(n):
+            z = O.euler_step(z, v, 1.0 / n)
+            t -= 1.0 / n
+            np.testing.assert_allclose(z, O.flow_match_noise(z0[None], z1[None], np.array([t]))[0],
+                                       atol=1e-12)
+        np.testing.assert_allclose(z, z0, atol=1e-12)

@@ -126,3 +126,23 @@ def test_fp8_block_stays_near_the_exact_block():
     for a, r in zip(y, ref):
         rel = np.linalg.norm(a - r) / np.linalg.norm(r)
         assert 1e-4 < rel < 0.15, rel
+
+
+def test_history_scale_algorithms_and_margin():
+    hist = [3.0, 10.0, 0.5, 2.0]
+    assert E.history_scale(hist, "most_recent") == 448.0 / 2.0
+    assert E.history_scale(hist, "max") == 448.0 / 10.0
+    # the margin halves the scale per unit, exactly
+    assert E.history_scale(hist, "max", margin=2) == 448.0 / 10.0 / 4.0
+    assert E.history_scale([], "max") == 1.0 and E.history_scale([0.0, 0.0], "max") == 1.0
+    # most_recent over a run of evaluations is what DelayedScaling.next_scales gives
+    rng = np.random.default_rng(4)
+    seen = []
+    for f in (1.0, 5.0, 0.25):
+        ds = E.DelayedScaling()
+        ds.linear("t", rng.standard_normal((4, 16)) * f, rng.standard_normal((3, 16)), None)
+        seen.append(ds.amax["t.x"])
+        assert E.history_scale(seen, "most_recent") == ds.next_scales()["t.x"]
+    # max never lets a value that was seen saturate: 448 / max keeps every recorded amax <= 448
+    s = E.history_scale(seen, "max")
+    assert all(a * s <= 448.0 * (1 + 1e-15) for a in seen)
