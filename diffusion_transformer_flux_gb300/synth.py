@@ -160,6 +160,30 @@ def final_layer_weights(rng, hidden, channels, dtype="bf16", std=0.02):
             "b_out": _cast(_normal(rng, (channels,), std), dtype)}
 
 
+def mlp_embedder_weights(rng, in_dim, hidden, dtype="bf16", std=0.02):
+    """Two-layer embedder (timestep or pooled-vector MLP): w1 [D, in], b1 [D], w2 [D, D], b2 [D]."""
+    return (_cast(_normal(rng, (hidden, in_dim), std), dtype), _cast(_normal(rng, (hidden,), std), dtype),
+            _cast(_normal(rng, (hidden, hidden), std), dtype), _cast(_normal(rng, (hidden,), std), dtype))
+
+
+def flux_weights(rng, hidden, heads, mlp_hidden, n_double, n_single, txt_dim=4096, vec_dim=768,
+                 time_dim=256, channels=64, guidance=False, dtype="bf16", std=0.02):
+    """Random weights of the whole model: embedders, ``n_double`` double blocks (an image and a
+    text stream each), ``n_single`` single blocks and the output head."""
+    d = hidden // heads
+    w = {"img_in": tuple(embed_weights(rng, channels, hidden, dtype, std).values()),
+         "txt_in": tuple(embed_weights(rng, txt_dim, hidden, dtype, std).values()),
+         "time_in": mlp_embedder_weights(rng, time_dim, hidden, dtype, std),
+         "vector_in": mlp_embedder_weights(rng, vec_dim, hidden, dtype, std)}
+    if guidance:
+        w["guidance_in"] = (_cast(_normal(rng, (hidden,), std), dtype), _cast(_normal(rng, (hidden,), std), dtype))
+    w["double"] = [(stream_weights(rng, hidden, heads, d, mlp_hidden, dtype, std),
+                    stream_weights(rng, hidden, heads, d, mlp_hidden, dtype, std)) for _ in range(n_double)]
+    w["single"] = [stream_weights(rng, hidden, heads, d, mlp_hidden, dtype, std) for _ in range(n_single)]
+    w["final"] = final_layer_weights(rng, hidden, channels, dtype, std)
+    return w
+
+
 # --------------------------------------------------------------------------- structure
 def position_ids(batch, lat_h, lat_w, seq_txt, img_first=True) -> np.ndarray:
     """Token ids ``[B, S, 3]`` (float32) in the joint order [image; text].

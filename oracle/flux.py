@@ -30,6 +30,9 @@ design notes of the repository as well):
     chunks, over the whole concatenated sequence, and returns every row.
   * The output head takes (shift, scale) from a SiLU + linear of ``vec``.
   * Loss is the mean over all elements.
+  * Conditioning: the timestep enters as tau = 1000 t (the TimeStepEmbedder's input range),
+    encoded as [cos(tau f_i), sin(tau f_i)] with f_i = 10000^(-i/128), i < 128; both
+    embedders are Linear, SiLU, Linear; the optional guidance term is a Linear of the scalar.
   * Precision: by default every step runs in float64.  ``mm_cast=round_bf16`` evaluates the
     method at the precision the pages fix for training, bf16 autocast (architecture page,
     §Performance optimizations › 5. Mixed precision; API page, §Optimization tips): the
@@ -414,6 +417,80 @@ def final_layer(x_img, vec, w_ada, b_ada, w_out, b_out, H, W, ln_eps=LN_EPS, mm_
     shift, scale = modulation(vec, w_ada, b_ada, 2, mm_cast)
     y = linear(modulate(x_img, shift, scale, ln_eps), w_out, b_out, mm_cast)
     return unpatchify(y, H, W)
+
+
+# ----------------------------------------------------------------------------- conditioning
+TIME_DIM = 256
+TIME_FACTOR = 1000.0
+TIME_MAX_PERIOD = 10000.0
+
+
+def timestep_features(t, dim=TIME_DIM, time_factor=TIME_FACTOR, max_period=TIME_MAX_PERIOD):
+    """Sinusoidal encoding of the timestep: t in [0, 1] -> [B, 256] (architecture page,
+    §Model components › 1. Input embeddings › Conditioning; API page, §Components API ›
+    Embeddings › TimeStepEmbedder, whose inputs lie in [0, 1000]).
+
+    Reading (the pages print no formula): tau = 1000 t; frequencies f_i = max_period^(-i/half)
+    for i < half = dim/2; features [cos(tau f_0 .. f_half-1), sin(tau f_0 .. f_half-1)].
+    """
+    tau = time_factor * _f64(t).reshape(-1, 1)
+    half = dim // 2
+    freqs = max_period ** (-np.arange(half, dtype=F64) / half)
+    ang = tau * freqs[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1)
+
+
+def mlp_embedder(x, w1, b1, w2, b2, mm_cast=None):
+    """Two-layer MLP: Linear(in -> D), SiLU, Linear(D -> D) (API page, §Components API ›
+    Embeddings › MLPEmbedder; the TimeStepEmbedder's MLP after the sinusoidal encoding).
+    Reading: SiLU between the two layers (the activation of the conditioning path)."""
+    return linear(silu(linear(x, w1, b1, mm_cast)), w2, b2, mm_cast)
+
+
+def guidance_embed(g, w, b):
+    """Guidance scale g -> Linear -> [B, D] (architecture page, §Conditioning, the optional
+    guidance term).  Reading: a Linear of the scalar, g w + b with w, b of length D."""
+    return _f64(g).reshape(-1, 1) * _f64(w)[None, :] + _f64(b)[None, :]
+
+
+def conditioning_vec(t, y, w, g=None, mm_cast=None):
+    """vec = timestep_emb + clip_pooled_emb [+ guidance_emb] (architecture page,
+    §Conditioning, Combined Conditioning Vector).  ``w["time_in"]`` and ``w["vector_in"]``
+    hold (w1, b1, w2, b2); ``w["guidance_in"]`` holds (w, b)."""
+    vec = mlp_embedder(timestep_features(t), *w["time_in"], mm_cast=mm_cast)
+    vec = vec + mlp_embedder(y, *w["vector_in"], mm_cast=mm_cast)
+    if g is not None:
+        vec = vec + guidance_embed(g, *w["guidance_in"])
+    return vec
+
+
+def flux_forward(z_t, txt, t, y, ids, w, heads, g=None, interleaved=True, gelu_tanh=False,
+                 mm_cast=None, store=None, axes_dim=AXES_DIM):
+    """The whole model (architecture page, §Data flow › Complete forward pass; §Model variants:
+    19 double and 38 single blocks for Flux 12B, 1 and 1 for Flux 535M).
+
+    conditioning vector; img_in(z_t), txt_in(txt); the double blocks in order; the single
+    blocks over the concatenation [img; txt]; the output head on the image rows of the last
+    block.  ``store`` (e.g. ``round_bf16``) is applied to every tensor the model hands from one
+    step to the next (vec, the embedded tokens, each block's outputs), the values an
+    implementation that stores them in the activation type holds.
+    """
+    keep = store if store is not None else _f64
+    B, C, H, W = np.shape(z_t)
+    vec = keep(conditioning_vec(t, y, w, g, mm_cast))
+    x_img = keep(img_in(z_t, w["img_in"][0], w["img_in"][1], mm_cast))
+    x_txt = keep(txt_in(txt, w["txt_in"][0], w["txt_in"][1], mm_cast))
+    cos, sin = rope_cos_sin(ids, axes_dim)
+    for wi, wt in w["double"]:
+        x_img, x_txt = double_block(x_img, x_txt, vec, cos, sin, wi, wt, heads, interleaved,
+                                    gelu_tanh, mm_cast=mm_cast)
+        x_img, x_txt = keep(x_img), keep(x_txt)
+    c = np.concatenate([x_img, x_txt], axis=1)
+    for ws in w["single"]:
+        c = keep(single_block(c, vec, cos, sin, ws, heads, interleaved, gelu_tanh, mm_cast=mm_cast))
+    f = w["final"]
+    return final_layer(c[:, : H * W], vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], H, W,
+                       mm_cast=mm_cast)
 
 
 # ----------------------------------------------------------------------------- rectified flow
