@@ -31,7 +31,8 @@ EXPORTED = [
     "mmdit_attention_workspace_size", "mmdit_attention_fwd", "mmdit_double_block_workspace_size",
     "mmdit_double_block_fwd", "mmdit_single_block_workspace_size", "mmdit_single_block_fwd",
     "mmdit_block_workspace_offsets", "mmdit_fp8_quantize_e4m3", "mmdit_fp8_linear_workspace_size",
-    "mmdit_fp8_linear_fwd",
+    "mmdit_fp8_linear_fwd", "mmdit_modulation_batched_fwd", "mmdit_conditioning_workspace_size",
+    "mmdit_conditioning_fwd", "mmdit_flux_workspace_size", "mmdit_flux_forward",
 ]
 
 
@@ -80,6 +81,33 @@ def fp8_tensor(slot: int, linear: str, operand: str) -> int:
 VP, SZ, I32, I64, F32 = C.c_void_p, C.c_size_t, C.c_int32, C.c_int64, C.c_float
 PDIMS, PW, PFP8 = C.POINTER(Dims), C.POINTER(StreamW), C.POINTER(Fp8State)
 
+
+class GemvJob(C.Structure):
+    _fields_ = [("w", VP), ("b", VP), ("out", VP), ("rows", I32)]
+
+
+class MlpEmbedderW(C.Structure):
+    _fields_ = [("w1", VP), ("b1", VP), ("w2", VP), ("b2", VP)]
+
+
+class CondW(C.Structure):
+    _fields_ = [("time_in", MlpEmbedderW), ("vector_in", MlpEmbedderW), ("w_guidance", VP),
+                ("b_guidance", VP)]
+
+
+class FluxConfig(C.Structure):
+    _fields_ = [("block", Dims), ("n_double", I32), ("n_single", I32), ("lat_h", I32), ("lat_w", I32),
+                ("channels", I32), ("txt_dim", I32), ("time_dim", I32), ("vec_in_dim", I32)]
+
+
+class FluxW(C.Structure):
+    _fields_ = [("w_img_in", VP), ("b_img_in", VP), ("w_txt_in", VP), ("b_txt_in", VP), ("cond", CondW),
+                ("double_img", PW), ("double_txt", PW), ("single", PW), ("w_ada", VP), ("b_ada", VP),
+                ("w_out", VP), ("b_out", VP)]
+
+
+PCOND, PFLUXC, PFLUXW = C.POINTER(CondW), C.POINTER(FluxConfig), C.POINTER(FluxW)
+
 _SIGS = {
     "mmdit_last_error": (C.c_char_p, []),
     "mmdit_workspace_status": (C.c_int, [VP, C.POINTER(C.c_uint32), VP]),
@@ -109,6 +137,11 @@ _SIGS = {
     "mmdit_fp8_quantize_e4m3": (C.c_int, [VP, I64, VP, VP, VP, VP]),
     "mmdit_fp8_linear_workspace_size": (SZ, []),
     "mmdit_fp8_linear_fwd": (C.c_int, [I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_modulation_batched_fwd": (C.c_int, [I32, I32, I32, VP, I32, C.POINTER(GemvJob), VP]),
+    "mmdit_conditioning_workspace_size": (SZ, [I32, I32, I32, I32]),
+    "mmdit_conditioning_fwd": (C.c_int, [I32, I32, I32, I32, I32, PCOND, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_flux_workspace_size": (SZ, [PFLUXC]),
+    "mmdit_flux_forward": (C.c_int, [PFLUXC, PFLUXW, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
 }
 
 _lib = None
@@ -380,4 +413,71 @@ def mmdit_fp8_linear_fwd(x_q, w_q, scale_x, scale_w, b, y, ws=None, stream=None)
         ws = workspace(load().mmdit_fp8_linear_workspace_size(), x_q.device)
     _check(load().mmdit_fp8_linear_fwd(M, N, K, _ptr(x_q), _ptr(w_q), _ptr(scale_x), _ptr(scale_w),
                                        _ptr(b), _ptr(y), _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+# ----------------------------------------------------------------------------- whole model
+def mmdit_modulation_batched_fwd(vec, jobs, stream=None):
+    """jobs: [(w, b, out), ...]; out_j [B, rows_j] fp32 = SiLU(vec) w_j^T + b_j, one launch."""
+    B, dim = vec.shape
+    arr = (GemvJob * max(len(jobs), 1))(*[GemvJob(_ptr(w), _ptr(b), _ptr(o), w.shape[0]) for w, b, o in jobs])
+    _check(load().mmdit_modulation_batched_fwd(act_of(vec), B, dim, _ptr(vec), len(jobs), arr,
+                                               _stream(stream)))
+
+
+def make_cond_w(w: dict) -> CondW:
+    """w["time_in"], w["vector_in"]: (w1, b1, w2, b2) device tensors; w["guidance_in"]: (w, b) or absent."""
+    g = w.get("guidance_in") or (None, None)
+    return CondW(MlpEmbedderW(*[_ptr(x) for x in w["time_in"]]),
+                 MlpEmbedderW(*[_ptr(x) for x in w["vector_in"]]), _ptr(g[0]), _ptr(g[1]))
+
+
+def mmdit_conditioning_workspace_size(act, batch, hidden, time_dim=256) -> int:
+    return load().mmdit_conditioning_workspace_size(act, batch, hidden, time_dim)
+
+
+def mmdit_conditioning_fwd(t, y, w: dict, vec, guidance=None, time_dim=256, ws=None, stream=None):
+    """vec [B, D] = time MLP(sinusoid(1000 t)) + vector MLP(y) (+ guidance term)."""
+    B, vec_in_dim = y.shape
+    D = vec.shape[1]
+    act = act_of(vec)
+    if ws is None:
+        ws = workspace(mmdit_conditioning_workspace_size(act, B, D, time_dim), vec.device)
+    cw = make_cond_w(w)
+    _check(load().mmdit_conditioning_fwd(act, B, D, time_dim, vec_in_dim, C.byref(cw), _ptr(t), _ptr(y),
+                                         _ptr(guidance), _ptr(vec), _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+def make_flux_config(dims: Dims, n_double, n_single, lat_h, lat_w, channels=64, txt_dim=4096,
+                     time_dim=256, vec_in_dim=768) -> FluxConfig:
+    return FluxConfig(dims, n_double, n_single, lat_h, lat_w, channels, txt_dim, time_dim, vec_in_dim)
+
+
+def make_flux_w(w: dict) -> FluxW:
+    """The C view of the model's device weights (the layout of ``synth.flux_weights``)."""
+    di = (StreamW * max(len(w["double"]), 1))(*[make_stream_w(a) for a, _ in w["double"]])
+    dt = (StreamW * max(len(w["double"]), 1))(*[make_stream_w(b) for _, b in w["double"]])
+    sg = (StreamW * max(len(w["single"]), 1))(*[make_stream_w(x) for x in w["single"]])
+    f = w["final"]
+    fw = FluxW(_ptr(w["img_in"][0]), _ptr(w["img_in"][1]), _ptr(w["txt_in"][0]), _ptr(w["txt_in"][1]),
+               make_cond_w(w), C.cast(di, PW), C.cast(dt, PW), C.cast(sg, PW), _ptr(f["w_ada"]),
+               _ptr(f["b_ada"]), _ptr(f["w_out"]), _ptr(f["b_out"]))
+    fw._keep = (di, dt, sg)  # the arrays the struct points to live as long as it does
+    return fw
+
+
+def mmdit_flux_workspace_size(cfg: FluxConfig) -> int:
+    return load().mmdit_flux_workspace_size(C.byref(cfg))
+
+
+def mmdit_flux_forward(cfg: FluxConfig, w, z_t, txt, t, y, rope_cos, rope_sin, pred, guidance=None,
+                       ws=None, stream=None):
+    """pred = the whole model at (z_t, txt, t, y); ``w`` is a dict of device weights or a FluxW."""
+    fw = w if isinstance(w, FluxW) else make_flux_w(w)
+    if ws is None:
+        ws = workspace(mmdit_flux_workspace_size(cfg), z_t.device)
+    _check(load().mmdit_flux_forward(C.byref(cfg), C.byref(fw), _ptr(z_t), _ptr(txt), _ptr(t), _ptr(y),
+                                     _ptr(guidance), _ptr(rope_cos), _ptr(rope_sin), _ptr(pred), _ptr(ws),
+                                     ws.numel(), _stream(stream)))
     return ws

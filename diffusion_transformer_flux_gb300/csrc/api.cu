@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <initializer_list>
+#include <vector>
 
 #include "../../include/mmdit.h"
 #include "internal.h"
@@ -562,6 +563,245 @@ mmdit_status run_attention(const BlockPlan& p, int act, void* ws, cudaStream_t s
   return MMDIT_OK;
 }
 
+// ----------------------------------------------------------------------------- step bodies
+// The work of an entry point after its checks, on a workspace whose first word is the status
+// word the caller cleared: the whole-model forward runs them back to back on one workspace, so
+// a timeout in any step stays visible.
+
+mmdit_status double_block_body(const mmdit_dims* d, const BlockPlan& p, const mmdit_stream_w* w_img,
+                               const mmdit_stream_w* w_txt, const void* vec, const float* rope_cos,
+                               const float* rope_sin, const void* x_img, const void* x_txt,
+                               void* y_img, void* y_txt, mmdit_fp8_state* fp8, void* workspace,
+                               cudaStream_t st) {
+  mmdit_status s = MMDIT_OK;
+  {
+    // both streams' AdaLN modulation in one launch (they share vec), unless precomputed
+    ModulationJob jobs[2];
+    int nj = 0;
+    if (!w_img->mod) jobs[nj++] = {w_img->w_mod, w_img->b_mod, at<float>(workspace, p.mod[0]), 6 * p.D};
+    if (!w_txt->mod) jobs[nj++] = {w_txt->w_mod, w_txt->b_mod, at<float>(workspace, p.mod[1]), 6 * p.D};
+    if (nj) {
+      ProfScope ps_("double.modulation", st);
+      MMDIT_CUDA(launch_modulation2(d->act, vec, jobs, nj, p.B, p.D, st), "modulation");
+    }
+  }
+  Streams ss;
+  const mmdit_stream_w* wsets[2] = {w_img, w_txt};
+  const void* xs[2] = {x_img, x_txt};
+  void* ys[2] = {y_img, y_txt};
+  const int rpb[2] = {p.Si, p.St};
+  for (int i = 0; i < 2; ++i)
+    if (rpb[i] > 0) {
+      ss.s[ss.n] = i, ss.w[ss.n] = wsets[i], ss.x[ss.n] = xs[i], ss.y[ss.n] = ys[i];
+      ss.rpb[ss.n] = rpb[i];
+      ss.mod[ss.n] = wsets[i]->mod ? wsets[i]->mod : at<float>(workspace, p.mod[i]);
+      ++ss.n;
+    }
+  Fp8 f8;
+  f8.f = fp8;
+  const int n_tensors = 2 * kFp8TensorsPerStream;
+  if (fp8 && (s = fp8_begin(p, ss, f8, n_tensors, workspace, st)) != MMDIT_OK) return s;
+  if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, f8, workspace, st)) != MMDIT_OK) return s;
+  if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
+  if ((s = run_post(d, p, ss, f8, workspace, st)) != MMDIT_OK) return s;
+  return fp8 ? fp8_end(p, f8, n_tensors, st) : MMDIT_OK;
+}
+
+mmdit_status single_block_body(const mmdit_dims* d, const BlockPlan& p, const mmdit_stream_w* w,
+                               const void* vec, const float* rope_cos, const float* rope_sin,
+                               const void* x, void* y, mmdit_fp8_state* fp8, void* workspace,
+                               cudaStream_t st) {
+  mmdit_status s = MMDIT_OK;
+  if (!w->mod) {
+    ProfScope ps_("single.modulation", st);
+    MMDIT_CUDA(launch_modulation(d->act, vec, w->w_mod, w->b_mod, p.B, 6 * p.D, p.D,
+                                 at<float>(workspace, p.mod[0]), st),
+               "modulation");
+  }
+  Streams ss;
+  ss.n = 1, ss.s[0] = 0, ss.w[0] = w, ss.x[0] = x, ss.y[0] = y, ss.rpb[0] = p.S;
+  ss.mod[0] = w->mod ? w->mod : at<float>(workspace, p.mod[0]);
+  Fp8 f8;
+  f8.f = fp8;
+  if (fp8 && (s = fp8_begin(p, ss, f8, kFp8TensorsPerStream, workspace, st)) != MMDIT_OK) return s;
+  if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, f8, workspace, st)) != MMDIT_OK) return s;
+  if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
+  if ((s = run_post(d, p, ss, f8, workspace, st)) != MMDIT_OK) return s;
+  return fp8 ? fp8_end(p, f8, kFp8TensorsPerStream, st) : MMDIT_OK;
+}
+
+mmdit_status final_layer_body(const mmdit_dims* d, int channels, const void* x_img, const void* vec,
+                              const void* w_ada, const void* b_ada, const void* w_out,
+                              const void* b_out, float* pred, void* workspace, cudaStream_t st) {
+  Carver c;
+  float* mod = at<float>(workspace, c.take(static_cast<size_t>(d->batch) * 2 * d->hidden * 4));
+  void* h = at(workspace, c.take(static_cast<size_t>(d->batch) * d->seq_img * d->hidden * elt_bytes(d->act)));
+  const int D = d->hidden, rows = d->batch * d->seq_img;
+  ProfScope ps_("final_layer", st);
+  MMDIT_CUDA(launch_modulation(d->act, vec, w_ada, b_ada, d->batch, 2 * D, D, mod, st), "final modulation");
+  MMDIT_CUDA(launch_ln_modulate(d->act, d->act == MMDIT_F32, x_img, mod, mod + D, 2 * D, rows, d->seq_img, D, d->ln_eps, h, st),
+             "final LayerNorm-modulate");
+  GemmProblem g;
+  g.act = d->act, g.M = rows, g.N = channels, g.K = D, g.A = h, g.W = w_out;
+  const int splits = choose_splits(rows, channels, D, static_cast<int>(elt_bytes(d->act)));
+  if (splits > 1) {
+    float* partials = at<float>(workspace, c.take(static_cast<size_t>(splits) * rows * channels * 4));
+    g.epi = kEpiPartial, g.splits = splits, g.ep.out = partials;
+    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "final projection (split K)");
+    MMDIT_CUDA(launch_splitk_reduce(d->act, partials, splits, rows, channels, b_out, pred,
+                                    d->seq_img, st),
+               "final projection (split-K sum)");
+  } else {
+    g.epi = kEpiUnpatchify, g.ep.bias = b_out, g.ep.out = pred, g.ep.rows_per_batch = d->seq_img;
+    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "final projection");
+  }
+  return MMDIT_OK;
+}
+
+mmdit_status img_in_body(int act, int batch, int channels, int lat_h, int lat_w, int hidden,
+                         const float* z, const void* w, const void* b, void* out, void* workspace,
+                         cudaStream_t st) {
+  void* tokens = at(workspace, kStatusBytes);
+  const int hw = lat_h * lat_w;
+  ProfScope ps_("img_in", st);
+  MMDIT_CUDA(launch_patchify(act, z, batch, channels, hw, tokens, st), "patchify");
+  GemmProblem g;
+  g.act = act, g.epi = kEpiBias, g.M = batch * hw, g.N = hidden, g.K = channels;
+  g.A = tokens, g.W = w, g.ep.bias = b, g.ep.out = out;
+  MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "img_in linear");
+  return MMDIT_OK;
+}
+
+mmdit_status linear_body(int act, int M, int N, int K, const void* x, const void* w, const void* b,
+                         void* y, void* workspace, cudaStream_t st) {
+  if (M == 0) return MMDIT_OK;
+  const int splits = choose_splits(M, N, K, static_cast<int>(elt_bytes(act)));
+  GemmProblem g;
+  g.act = act, g.M = M, g.N = N, g.K = K, g.A = x, g.W = w;
+  ProfScope ps_("linear", st);
+  if (splits > 1) {
+    // narrow GEMM: K split across work items, fp32 partials, then a fixed-order finish
+    float* partials = at<float>(workspace, kStatusBytes);
+    g.epi = kEpiPartial, g.splits = splits, g.ep.out = partials;
+    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "linear (split K)");
+    MMDIT_CUDA(launch_splitk_reduce(act, partials, splits, M, N, b, y, 0, st), "linear (split-K sum)");
+  } else {
+    g.epi = kEpiBias, g.ep.bias = b, g.ep.out = y;
+    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "linear");
+  }
+  return MMDIT_OK;
+}
+
+size_t conditioning_workspace(int act, int batch, int hidden, int time_dim) {
+  Carver c;
+  const size_t e = elt_bytes(act);
+  c.take(static_cast<size_t>(batch) * time_dim * e);  // sinusoidal features
+  c.take(static_cast<size_t>(batch) * hidden * e);    // timestep MLP hidden layer
+  c.take(static_cast<size_t>(batch) * hidden * e);    // vector MLP hidden layer
+  c.take(static_cast<size_t>(batch) * hidden * 4);    // fp32 sum of the embeddings
+  return c.off;
+}
+
+mmdit_status conditioning_body(int act, int B, int D, int time_dim, int vec_in_dim, const mmdit_cond_w* w,
+                               const float* t, const void* y, const float* g, void* vec, void* workspace,
+                               cudaStream_t st) {
+  Carver c;
+  const size_t e = elt_bytes(act);
+  void* feat = at(workspace, c.take(static_cast<size_t>(B) * time_dim * e));
+  void* ht = at(workspace, c.take(static_cast<size_t>(B) * D * e));
+  void* hy = at(workspace, c.take(static_cast<size_t>(B) * D * e));
+  float* v32 = at<float>(workspace, c.take(static_cast<size_t>(B) * D * 4));
+  ProfScope ps_("conditioning", st);
+  MMDIT_CUDA(launch_timestep_features(act, t, B, time_dim, 1000.0, 10000.0, feat, st), "timestep features");
+  // first layers (no activation on their inputs), kept in the activation type
+  const ModulationJob l1t{w->time_in.w1, w->time_in.b1, ht, D};
+  MMDIT_CUDA(launch_gemv(act, feat, &l1t, 1, B, time_dim, 0, kGemvOutAct, st), "timestep MLP layer 1");
+  const ModulationJob l1y{w->vector_in.w1, w->vector_in.b1, hy, D};
+  MMDIT_CUDA(launch_gemv(act, y, &l1y, 1, B, vec_in_dim, 0, kGemvOutAct, st), "vector MLP layer 1");
+  // second layers read SiLU of the hidden layers; the vector MLP adds onto the timestep's
+  const ModulationJob l2t{w->time_in.w2, w->time_in.b2, v32, D};
+  MMDIT_CUDA(launch_gemv(act, ht, &l2t, 1, B, D, 1, kGemvOutF32, st), "timestep MLP layer 2");
+  const ModulationJob l2y{w->vector_in.w2, w->vector_in.b2, v32, D};
+  MMDIT_CUDA(launch_gemv(act, hy, &l2y, 1, B, D, 1, kGemvOutF32Add, st), "vector MLP layer 2");
+  MMDIT_CUDA(launch_vec_finish(act, v32, g, w->w_guidance, w->b_guidance, B, D, vec, st), "conditioning vector");
+  return MMDIT_OK;
+}
+
+// Workspace of the whole-model forward: one region that every step in turn uses from its start
+// (status word first), then the model's own tensors.
+struct FluxPlan {
+  BlockPlan dbl, sgl;
+  size_t vec, mods, x_img, x_txt, c, total;
+  int n_mod;
+};
+
+bool plan_flux(const mmdit_flux_config* cfg, FluxPlan* f) {
+  const mmdit_dims* d = &cfg->block;
+  const int B = d->batch, D = d->hidden, Si = d->seq_img, St = d->seq_txt, S = Si + St;
+  const size_t e = elt_bytes(d->act);
+  size_t region = conditioning_workspace(d->act, B, D, cfg->time_dim);
+  auto grow = [&](size_t x) { region = x > region ? x : region; };
+  if (!plan_block(d, false, &f->dbl) || !plan_block(d, true, &f->sgl)) return false;
+  if (cfg->n_double > 0) grow(f->dbl.total);
+  if (cfg->n_single > 0) grow(f->sgl.total);
+  grow(mmdit_final_layer_workspace_size(d, cfg->channels));
+  grow(mmdit_img_in_workspace_size(d->act, B, cfg->channels, cfg->lat_h, cfg->lat_w));
+  grow(mmdit_linear_workspace_size(d->act, B * St, D, cfg->txt_dim));
+  Carver c;
+  c.off = round_up(region, 256);
+  f->n_mod = 2 * cfg->n_double + cfg->n_single;
+  f->vec = c.take(static_cast<size_t>(B) * D * e);
+  f->mods = c.take(static_cast<size_t>(f->n_mod) * B * 6 * D * 4);
+  f->c = c.take(static_cast<size_t>(B) * S * D * e);
+  if (B == 1) {
+    // one sample: the streams sit back to back inside [img; txt], so joining them is free
+    f->x_img = f->c;
+    f->x_txt = f->c + static_cast<size_t>(Si) * D * e;
+  } else {
+    f->x_img = c.take(static_cast<size_t>(B) * Si * D * e);
+    f->x_txt = c.take(static_cast<size_t>(B) * St * D * e);
+  }
+  f->total = c.off;
+  return true;
+}
+
+mmdit_status check_flux(const mmdit_flux_config* cfg) {
+  if (!cfg) return fail(MMDIT_ERR_INVALID_ARG, "flux config is NULL");
+  const mmdit_dims* d = &cfg->block;
+  mmdit_status s = check_dims(d);
+  if (s != MMDIT_OK) return s;
+  if (d->gemm != MMDIT_GEMM_NATIVE)
+    return fail(MMDIT_ERR_UNSUPPORTED, "whole-model forward: native GEMMs only (FP8 runs per block)");
+  if (d->batch < 1 || d->seq_img < 1) return fail(MMDIT_ERR_INVALID_ARG, "whole-model forward: empty batch or image");
+  if (cfg->n_double < 0 || cfg->n_single < 0) return fail(MMDIT_ERR_INVALID_ARG, "negative block count");
+  if (cfg->lat_h < 1 || cfg->lat_w < 1 || d->seq_img != cfg->lat_h * cfg->lat_w)
+    return fail(MMDIT_ERR_INVALID_ARG, "seq_img must equal lat_h * lat_w");
+  if (cfg->channels < 32 || cfg->channels % 32 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "channels must be a multiple of 32");
+  if (d->hidden % 256 != 0) return fail(MMDIT_ERR_UNSUPPORTED, "whole-model forward: hidden must be a multiple of 256");
+  if (d->seq_txt > 0 && (cfg->txt_dim < 8 || cfg->txt_dim % 8 != 0))
+    return fail(MMDIT_ERR_UNSUPPORTED, "txt_dim must be a positive multiple of 8");
+  if (cfg->time_dim < 8 || cfg->time_dim % 8 != 0 || cfg->time_dim > 512)
+    return fail(MMDIT_ERR_UNSUPPORTED, "time_dim must be a multiple of 8 in [8, 512]");
+  if (cfg->vec_in_dim < 8 || cfg->vec_in_dim % 8 != 0 || cfg->vec_in_dim > 6144)
+    return fail(MMDIT_ERR_UNSUPPORTED, "vec_in_dim must be a multiple of 8 in [8, 6144]");
+  if (static_cast<int64_t>(d->batch) * d->heads > 65535)
+    return fail(MMDIT_ERR_UNSUPPORTED, "batch * heads must be <= 65535");
+  return MMDIT_OK;
+}
+
+mmdit_status check_cond_w(const mmdit_cond_w* w, bool guided) {
+  if (!w) return fail(MMDIT_ERR_INVALID_ARG, "conditioning weights are NULL");
+  mmdit_status s = check_ptrs({w->time_in.w1, w->time_in.b1, w->time_in.w2, w->time_in.b2},
+                              "timestep embedder weights");
+  if (s != MMDIT_OK) return s;
+  if ((s = check_ptrs({w->vector_in.w1, w->vector_in.b1, w->vector_in.w2, w->vector_in.b2},
+                      "vector embedder weights")) != MMDIT_OK)
+    return s;
+  if (guided && (s = check_ptrs({w->w_guidance, w->b_guidance}, "guidance weights")) != MMDIT_OK) return s;
+  return MMDIT_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -728,22 +968,7 @@ mmdit_status mmdit_linear_fwd(int32_t act, int32_t M, int32_t N, int32_t K, cons
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
   pdl_begin_call();
-  if (M == 0) return MMDIT_OK;
-  const int splits = choose_splits(M, N, K, static_cast<int>(elt_bytes(act)));
-  GemmProblem g;
-  g.act = act, g.M = M, g.N = N, g.K = K, g.A = x, g.W = w;
-  ProfScope ps_("linear", st);
-  if (splits > 1) {
-    // narrow GEMM: K split across work items, fp32 partials, then a fixed-order finish
-    float* partials = at<float>(workspace, kStatusBytes);
-    g.epi = kEpiPartial, g.splits = splits, g.ep.out = partials;
-    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "linear (split K)");
-    MMDIT_CUDA(launch_splitk_reduce(act, partials, splits, M, N, b, y, 0, st), "linear (split-K sum)");
-  } else {
-    g.epi = kEpiBias, g.ep.bias = b, g.ep.out = y;
-    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "linear");
-  }
-  return MMDIT_OK;
+  return linear_body(act, M, N, K, x, w, b, y, workspace, st);
 }
 
 size_t mmdit_img_in_workspace_size(int32_t act, int32_t batch, int32_t channels, int32_t lat_h,
@@ -771,15 +996,7 @@ mmdit_status mmdit_img_in_fwd(int32_t act, int32_t batch, int32_t channels, int3
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
   pdl_begin_call();
-  void* tokens = at(workspace, kStatusBytes);
-  const int hw = lat_h * lat_w;
-  ProfScope ps_("img_in", st);
-  MMDIT_CUDA(launch_patchify(act, z, batch, channels, hw, tokens, st), "patchify");
-  GemmProblem g;
-  g.act = act, g.epi = kEpiBias, g.M = batch * hw, g.N = hidden, g.K = channels;
-  g.A = tokens, g.W = w, g.ep.bias = b, g.ep.out = out;
-  MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "img_in linear");
-  return MMDIT_OK;
+  return img_in_body(act, batch, channels, lat_h, lat_w, hidden, z, w, b, out, workspace, st);
 }
 
 size_t mmdit_final_layer_workspace_size(const mmdit_dims* d, int32_t channels) {
@@ -812,29 +1029,7 @@ mmdit_status mmdit_final_layer_fwd(const mmdit_dims* d, int32_t channels, int32_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
   pdl_begin_call();
-  Carver c;
-  float* mod = at<float>(workspace, c.take(static_cast<size_t>(d->batch) * 2 * d->hidden * 4));
-  void* h = at(workspace, c.take(static_cast<size_t>(d->batch) * d->seq_img * d->hidden * elt_bytes(d->act)));
-  const int D = d->hidden, rows = d->batch * d->seq_img;
-  ProfScope ps_("final_layer", st);
-  MMDIT_CUDA(launch_modulation(d->act, vec, w_ada, b_ada, d->batch, 2 * D, D, mod, st), "final modulation");
-  MMDIT_CUDA(launch_ln_modulate(d->act, d->act == MMDIT_F32, x_img, mod, mod + D, 2 * D, rows, d->seq_img, D, d->ln_eps, h, st),
-             "final LayerNorm-modulate");
-  GemmProblem g;
-  g.act = d->act, g.M = rows, g.N = channels, g.K = D, g.A = h, g.W = w_out;
-  const int splits = choose_splits(rows, channels, D, static_cast<int>(elt_bytes(d->act)));
-  if (splits > 1) {
-    float* partials = at<float>(workspace, c.take(static_cast<size_t>(splits) * rows * channels * 4));
-    g.epi = kEpiPartial, g.splits = splits, g.ep.out = partials;
-    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "final projection (split K)");
-    MMDIT_CUDA(launch_splitk_reduce(d->act, partials, splits, rows, channels, b_out, pred,
-                                    d->seq_img, st),
-               "final projection (split-K sum)");
-  } else {
-    g.epi = kEpiUnpatchify, g.ep.bias = b_out, g.ep.out = pred, g.ep.rows_per_batch = d->seq_img;
-    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "final projection");
-  }
-  return MMDIT_OK;
+  return final_layer_body(d, channels, x_img, vec, w_ada, b_ada, w_out, b_out, pred, workspace, st);
 }
 
 
@@ -923,37 +1118,8 @@ mmdit_status mmdit_double_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
   pdl_begin_call();
-  {
-    // both streams' AdaLN modulation in one launch (they share vec), unless precomputed
-    ModulationJob jobs[2];
-    int nj = 0;
-    if (!w_img->mod) jobs[nj++] = {w_img->w_mod, w_img->b_mod, at<float>(workspace, p.mod[0]), 6 * p.D};
-    if (!w_txt->mod) jobs[nj++] = {w_txt->w_mod, w_txt->b_mod, at<float>(workspace, p.mod[1]), 6 * p.D};
-    if (nj) {
-      ProfScope ps_("double.modulation", st);
-      MMDIT_CUDA(launch_modulation2(d->act, vec, jobs, nj, p.B, p.D, st), "modulation");
-    }
-  }
-  Streams ss;
-  const mmdit_stream_w* wsets[2] = {w_img, w_txt};
-  const void* xs[2] = {x_img, x_txt};
-  void* ys[2] = {y_img, y_txt};
-  const int rpb[2] = {p.Si, p.St};
-  for (int i = 0; i < 2; ++i)
-    if (rpb[i] > 0) {
-      ss.s[ss.n] = i, ss.w[ss.n] = wsets[i], ss.x[ss.n] = xs[i], ss.y[ss.n] = ys[i];
-      ss.rpb[ss.n] = rpb[i];
-      ss.mod[ss.n] = wsets[i]->mod ? wsets[i]->mod : at<float>(workspace, p.mod[i]);
-      ++ss.n;
-    }
-  Fp8 f8;
-  f8.f = fp8;
-  const int n_tensors = 2 * kFp8TensorsPerStream;
-  if (fp8 && (s = fp8_begin(p, ss, f8, n_tensors, workspace, st)) != MMDIT_OK) return s;
-  if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, f8, workspace, st)) != MMDIT_OK) return s;
-  if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
-  if ((s = run_post(d, p, ss, f8, workspace, st)) != MMDIT_OK) return s;
-  return fp8 ? fp8_end(p, f8, n_tensors, st) : MMDIT_OK;
+  return double_block_body(d, p, w_img, w_txt, vec, rope_cos, rope_sin, x_img, x_txt, y_img, y_txt, fp8,
+                           workspace, st);
 }
 
 mmdit_status mmdit_single_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w, const void* vec,
@@ -973,22 +1139,7 @@ mmdit_status mmdit_single_block_fwd(const mmdit_dims* d, const mmdit_stream_w* w
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
   pdl_begin_call();
-  if (!w->mod) {
-    ProfScope ps_("single.modulation", st);
-    MMDIT_CUDA(launch_modulation(d->act, vec, w->w_mod, w->b_mod, p.B, 6 * p.D, p.D,
-                                 at<float>(workspace, p.mod[0]), st),
-               "modulation");
-  }
-  Streams ss;
-  ss.n = 1, ss.s[0] = 0, ss.w[0] = w, ss.x[0] = x, ss.y[0] = y, ss.rpb[0] = p.S;
-  ss.mod[0] = w->mod ? w->mod : at<float>(workspace, p.mod[0]);
-  Fp8 f8;
-  f8.f = fp8;
-  if (fp8 && (s = fp8_begin(p, ss, f8, kFp8TensorsPerStream, workspace, st)) != MMDIT_OK) return s;
-  if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, f8, workspace, st)) != MMDIT_OK) return s;
-  if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
-  if ((s = run_post(d, p, ss, f8, workspace, st)) != MMDIT_OK) return s;
-  return fp8 ? fp8_end(p, f8, kFp8TensorsPerStream, st) : MMDIT_OK;
+  return single_block_body(d, p, w, vec, rope_cos, rope_sin, x, y, fp8, workspace, st);
 }
 
 mmdit_status mmdit_fp8_quantize_e4m3(const void* x, int64_t n, const float* scale, float* amax,
@@ -1033,6 +1184,167 @@ mmdit_status mmdit_fp8_linear_fwd(int32_t M, int32_t N, int32_t K, const void* x
   ProfScope ps_("fp8_linear", st);
   MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "FP8 linear");
   return MMDIT_OK;
+}
+
+size_t mmdit_conditioning_workspace_size(int32_t act, int32_t batch, int32_t hidden, int32_t time_dim) {
+  if (batch < 1 || hidden < 1 || time_dim < 1) return kStatusBytes;
+  return conditioning_workspace(act, batch, hidden, time_dim);
+}
+
+mmdit_status mmdit_conditioning_fwd(int32_t act, int32_t batch, int32_t hidden, int32_t time_dim,
+                                    int32_t vec_in_dim, const mmdit_cond_w* w, const float* t,
+                                    const void* y, const float* guidance, void* vec, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  if (act != MMDIT_F32 && act != MMDIT_BF16) return fail(MMDIT_ERR_INVALID_ARG, "bad act %d", act);
+  if (batch < 0) return fail(MMDIT_ERR_INVALID_ARG, "negative batch");
+  if (hidden < 8 || hidden % 8 != 0 || hidden > 6144)
+    return fail(MMDIT_ERR_UNSUPPORTED, "hidden must be a multiple of 8 in [8, 6144] (got %d)", hidden);
+  if (time_dim < 8 || time_dim % 8 != 0 || time_dim > 512)
+    return fail(MMDIT_ERR_UNSUPPORTED, "time_dim must be a multiple of 8 in [8, 512] (got %d)", time_dim);
+  if (vec_in_dim < 8 || vec_in_dim % 8 != 0 || vec_in_dim > 6144)
+    return fail(MMDIT_ERR_UNSUPPORTED, "vec_in_dim must be a multiple of 8 in [8, 6144] (got %d)", vec_in_dim);
+  mmdit_status s = check_cond_w(w, guidance != nullptr);
+  if (s != MMDIT_OK) return s;
+  if (batch == 0) return MMDIT_OK;
+  if ((s = check_ptrs({t, y, vec}, "conditioning")) != MMDIT_OK) return s;
+  if ((s = check_workspace(workspace, workspace_bytes,
+                           mmdit_conditioning_workspace_size(act, batch, hidden, time_dim))) != MMDIT_OK)
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
+  return conditioning_body(act, batch, hidden, time_dim, vec_in_dim, w, t, y, guidance, vec, workspace, st);
+}
+
+mmdit_status mmdit_modulation_batched_fwd(int32_t act, int32_t batch, int32_t dim, const void* vec,
+                                          int32_t n_jobs, const mmdit_gemv_job* jobs, void* stream) {
+  if (act != MMDIT_F32 && act != MMDIT_BF16) return fail(MMDIT_ERR_INVALID_ARG, "bad act %d", act);
+  if (batch < 0 || dim < 1 || n_jobs < 0) return fail(MMDIT_ERR_INVALID_ARG, "bad batched modulation shape");
+  if (dim % 8 != 0 || dim > 6144)
+    return fail(MMDIT_ERR_UNSUPPORTED, "modulation: dim must be a multiple of 8, at most 6144 (got %d)", dim);
+  if (n_jobs > 0 && !jobs) return fail(MMDIT_ERR_INVALID_ARG, "jobs is NULL");
+  if (batch == 0 || n_jobs == 0) return MMDIT_OK;
+  mmdit_status s = check_ptrs({vec}, "batched modulation input");
+  if (s != MMDIT_OK) return s;
+  std::vector<ModulationJob> mj(static_cast<size_t>(n_jobs));
+  for (int i = 0; i < n_jobs; ++i) {
+    if (jobs[i].rows < 0) return fail(MMDIT_ERR_INVALID_ARG, "job %d: negative rows", i);
+    if (jobs[i].rows > 0 && (s = check_ptrs({jobs[i].w, jobs[i].out}, "batched modulation job")) != MMDIT_OK)
+      return s;
+    mj[i] = {jobs[i].w, jobs[i].b, jobs[i].out, jobs[i].rows};
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  pdl_begin_call();
+  ProfScope ps_("modulation.batched", st);
+  MMDIT_CUDA(launch_gemv(act, vec, mj.data(), n_jobs, batch, dim, 1, kGemvOutF32, st), "batched modulation");
+  return MMDIT_OK;
+}
+
+size_t mmdit_flux_workspace_size(const mmdit_flux_config* cfg) {
+  FluxPlan f;
+  if (check_flux(cfg) != MMDIT_OK || !plan_flux(cfg, &f)) return 0;
+  return f.total;
+}
+
+mmdit_status mmdit_flux_forward(const mmdit_flux_config* cfg, const mmdit_flux_w* w, const float* z_t,
+                                const void* txt, const float* t, const void* y, const float* guidance,
+                                const float* rope_cos, const float* rope_sin, float* pred, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  mmdit_status s = check_flux(cfg);
+  if (s != MMDIT_OK) return s;
+  if (!w) return fail(MMDIT_ERR_INVALID_ARG, "model weights are NULL");
+  const mmdit_dims* d = &cfg->block;
+  const int B = d->batch, D = d->hidden, Si = d->seq_img, St = d->seq_txt, S = Si + St;
+  if ((s = check_cond_w(&w->cond, guidance != nullptr)) != MMDIT_OK) return s;
+  if ((s = check_ptrs({z_t, t, y, rope_cos, rope_sin, pred}, "whole-model inputs")) != MMDIT_OK) return s;
+  if ((s = check_ptrs({w->w_img_in, w->b_img_in, w->w_ada, w->b_ada, w->w_out, w->b_out},
+                      "embedding and head weights")) != MMDIT_OK)
+    return s;
+  if (St > 0 && (s = check_ptrs({txt, w->w_txt_in, w->b_txt_in}, "text input")) != MMDIT_OK) return s;
+  if (cfg->n_double > 0 && (!w->double_img || !w->double_txt))
+    return fail(MMDIT_ERR_INVALID_ARG, "double-block weight arrays are NULL");
+  if (cfg->n_single > 0 && !w->single) return fail(MMDIT_ERR_INVALID_ARG, "single-block weight array is NULL");
+  for (int i = 0; i < cfg->n_double; ++i) {
+    if ((s = check_stream_w(&w->double_img[i], "double block image weights")) != MMDIT_OK) return s;
+    if ((s = check_stream_w(&w->double_txt[i], "double block text weights")) != MMDIT_OK) return s;
+  }
+  for (int i = 0; i < cfg->n_single; ++i)
+    if ((s = check_stream_w(&w->single[i], "single block weights")) != MMDIT_OK) return s;
+  FluxPlan f;
+  if (!plan_flux(cfg, &f)) return fail(MMDIT_ERR_INVALID_ARG, "bad whole-model dims");
+  if ((s = check_workspace(workspace, workspace_bytes, f.total)) != MMDIT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t e = elt_bytes(d->act);
+  void* vec = at(workspace, f.vec);
+  float* mods = at<float>(workspace, f.mods);
+  void* x_img = at(workspace, f.x_img);
+  void* x_txt = at(workspace, f.x_txt);
+  void* c = at(workspace, f.c);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
+  if ((s = conditioning_body(d->act, B, D, cfg->time_dim, cfg->vec_in_dim, &w->cond, t, y, guidance, vec,
+                             workspace, st)) != MMDIT_OK)
+    return s;
+  // every block's modulation in one launch: they all read vec
+  std::vector<mmdit_stream_w> wd(2 * static_cast<size_t>(cfg->n_double)), ws1(static_cast<size_t>(cfg->n_single));
+  std::vector<ModulationJob> jobs;
+  jobs.reserve(static_cast<size_t>(f.n_mod));
+  const size_t mod_stride = static_cast<size_t>(B) * 6 * D;
+  for (int i = 0; i < cfg->n_double; ++i)
+    for (int k = 0; k < 2; ++k) {
+      mmdit_stream_w& sw = wd[2 * i + k];
+      sw = k ? w->double_txt[i] : w->double_img[i];
+      float* m = mods + (2 * static_cast<size_t>(i) + k) * mod_stride;
+      sw.mod = m;
+      jobs.push_back({sw.w_mod, sw.b_mod, m, 6 * D});
+    }
+  for (int i = 0; i < cfg->n_single; ++i) {
+    ws1[i] = w->single[i];
+    float* m = mods + (2 * static_cast<size_t>(cfg->n_double) + i) * mod_stride;
+    ws1[i].mod = m;
+    jobs.push_back({ws1[i].w_mod, ws1[i].b_mod, m, 6 * D});
+  }
+  if (!jobs.empty()) {
+    ProfScope ps_("modulation.batched", st);
+    MMDIT_CUDA(launch_gemv(d->act, vec, jobs.data(), static_cast<int>(jobs.size()), B, D, 1, kGemvOutF32, st),
+               "every block's modulation");
+  }
+  if ((s = img_in_body(d->act, B, cfg->channels, cfg->lat_h, cfg->lat_w, D, z_t, w->w_img_in, w->b_img_in,
+                       x_img, workspace, st)) != MMDIT_OK)
+    return s;
+  if (St > 0 && (s = linear_body(d->act, B * St, D, cfg->txt_dim, txt, w->w_txt_in, w->b_txt_in, x_txt,
+                                 workspace, st)) != MMDIT_OK)
+    return s;
+  for (int i = 0; i < cfg->n_double; ++i)
+    if ((s = double_block_body(d, f.dbl, &wd[2 * i], &wd[2 * i + 1], vec, rope_cos, rope_sin, x_img, x_txt,
+                               x_img, x_txt, nullptr, workspace, st)) != MMDIT_OK)
+      return s;
+  const void* img_rows = x_img;
+  if (cfg->n_single > 0) {
+    if (B > 1) {
+      // [img; txt] per sample (strided copies), then the next kernel launches normally
+      MMDIT_CUDA(cudaMemcpy2DAsync(c, S * D * e, x_img, Si * D * e, Si * D * e, B, cudaMemcpyDeviceToDevice, st),
+                 "join image rows");
+      if (St > 0)
+        MMDIT_CUDA(cudaMemcpy2DAsync(static_cast<uint8_t*>(c) + Si * D * e, S * D * e, x_txt, St * D * e,
+                                     St * D * e, B, cudaMemcpyDeviceToDevice, st),
+                   "join text rows");
+      pdl_begin_call();
+    }
+    for (int i = 0; i < cfg->n_single; ++i)
+      if ((s = single_block_body(d, f.sgl, &ws1[i], vec, rope_cos, rope_sin, c, c, nullptr, workspace, st)) !=
+          MMDIT_OK)
+        return s;
+    if (B > 1) {
+      MMDIT_CUDA(cudaMemcpy2DAsync(x_img, Si * D * e, c, S * D * e, Si * D * e, B, cudaMemcpyDeviceToDevice, st),
+                 "image rows of the last block");
+      pdl_begin_call();
+    } else {
+      img_rows = c;
+    }
+  }
+  return final_layer_body(d, cfg->channels, img_rows, vec, w->w_ada, w->b_ada, w->w_out, w->b_out, pred,
+                          workspace, st);
 }
 
 }  // extern "C"

@@ -5,6 +5,8 @@
 
 #include <type_traits>
 
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -72,8 +74,17 @@ constexpr int kModThreads = 128;
 struct ModJob {
   const void* w;
   const void* bias;
-  float* m;  // [batch, rows]
+  void* out;  // [batch, rows]: fp32, or the activation type under kGemvOutAct
   int rows;
+};
+
+// Up to kModMaxJobs weight matrices that read the same input share a launch; their rows form
+// one index space, job i owning rows [start[i], start[i + 1]).
+constexpr int kModMaxJobs = 80;
+struct ModJobs {
+  ModJob j[kModMaxJobs];
+  int start[kModMaxJobs + 1];
+  int n;
 };
 
 template <typename T>
@@ -100,17 +111,19 @@ struct Raw8<float> {
 };
 
 template <typename T, int NC, int NB>
-__global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __restrict__ vec, ModJob j0,
-                                                                 ModJob j1, int dim) {
+__global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __restrict__ vec,
+                                                                 const __grid_constant__ ModJobs jobs,
+                                                                 int dim, int silu, int mode) {
   pdl_wait();  // the previous kernel's results are visible from here on
   constexpr int batch = NB;  // batch rows handled by this launch (compile time: no idle lanes)
-  // [batch, dim] SiLU(vec): fp32, or in bf16 mode the bf16 operand it is there (stored as bf16,
-  // so each 16-byte weight load pairs with one 16-byte shared-memory load)
+  // [batch, dim] SiLU(vec) (or vec itself when silu == 0): fp32, or in bf16 mode the bf16
+  // operand it is there (stored as bf16, so each 16-byte weight load pairs with one 16-byte
+  // shared-memory load)
   extern __shared__ float svec[];
   __nv_bfloat16* svec_bf = reinterpret_cast<__nv_bfloat16*>(svec);
   for (int i = threadIdx.x; i < batch * dim; i += blockDim.x) {
     const float v = to_f32(vec[i]);
-    const float sv = v / (1.f + expf(-v));
+    const float sv = silu ? v / (1.f + expf(-v)) : v;
     if constexpr (sizeof(T) == 2)
       svec_bf[i] = __float2bfloat16_rn(sv);
     else
@@ -119,24 +132,33 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __rest
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
-  const int total = j0.rows + j1.rows;
+  const int total = jobs.start[jobs.n];
   const int stride = gridDim.x * warps;
+  auto job_of = [&](int g) {  // the job owning row g (binary search over the row starts)
+    int lo = 0, hi = jobs.n - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (g >= jobs.start[mid])
+        lo = mid;
+      else
+        hi = mid - 1;
+    }
+    return lo;
+  };
   // Rows are software-pipelined: the loads of a warp's next row are issued before its current
   // row is reduced, so every warp keeps one row (NC 16-byte loads per lane) in flight.
-  auto load_row = [&](int g, Raw8<T> (&raw)[NC]) {
-    const bool second = g >= j0.rows;
-    const ModJob& job = second ? j1 : j0;
-    const T* wr = reinterpret_cast<const T*>(job.w) + static_cast<size_t>(second ? g - j0.rows : g) * dim;
+  auto load_row = [&](int g, int ji, Raw8<T> (&raw)[NC]) {
+    const ModJob& job = jobs.j[ji];
+    const T* wr = reinterpret_cast<const T*>(job.w) + static_cast<size_t>(g - jobs.start[ji]) * dim;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       const int k = c * 256 + lane * 8;
       if (k < dim) raw[c].load(wr + k);
     }
   };
-  auto reduce_row = [&](int g, const Raw8<T> (&raw)[NC]) {
-    const bool second = g >= j0.rows;
-    const ModJob& job = second ? j1 : j0;
-    const int r = second ? g - j0.rows : g;
+  auto reduce_row = [&](int g, int ji, const Raw8<T> (&raw)[NC]) {
+    const ModJob& job = jobs.j[ji];
+    const int r = g - jobs.start[ji];
     float acc[NB];
 #pragma unroll
     for (int b = 0; b < NB; ++b) acc[b] = 0.f;
@@ -167,20 +189,42 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __rest
     const float bb = job.bias ? to_f32(reinterpret_cast<const T*>(job.bias)[r]) : 0.f;
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
-      const float sum = warp_sum(acc[b]);
-      if (lane == 0) job.m[static_cast<size_t>(b) * job.rows + r] = sum + bb;
+      const float sum = warp_sum(acc[b]) + bb;
+      if (lane == 0) {
+        const size_t o = static_cast<size_t>(b) * job.rows + r;
+        if (mode == kGemvOutAct) {
+          if constexpr (sizeof(T) == 2)
+            reinterpret_cast<__nv_bfloat16*>(job.out)[o] = __float2bfloat16_rn(sum);
+          else
+            reinterpret_cast<float*>(job.out)[o] = sum;
+        } else if (mode == kGemvOutF32Add) {
+          reinterpret_cast<float*>(job.out)[o] += sum;
+        } else {
+          reinterpret_cast<float*>(job.out)[o] = sum;
+        }
+      }
     }
   };
   Raw8<T> ra[NC], rb[NC];
   int g = blockIdx.x * warps + warp;
-  if (g < total) load_row(g, ra);
+  int ja = 0, jb = 0;
+  if (g < total) {
+    ja = job_of(g);
+    load_row(g, ja, ra);
+  }
   while (g < total) {
     const int g1 = g + stride;
-    if (g1 < total) load_row(g1, rb);
-    reduce_row(g, ra);
+    if (g1 < total) {
+      jb = job_of(g1);
+      load_row(g1, jb, rb);
+    }
+    reduce_row(g, ja, ra);
     const int g2 = g1 + stride;
-    if (g2 < total) load_row(g2, ra);
-    if (g1 < total) reduce_row(g1, rb);
+    if (g2 < total) {
+      ja = job_of(g2);
+      load_row(g2, ja, ra);
+    }
+    if (g1 < total) reduce_row(g1, jb, rb);
     g = g2;
   }
 }
@@ -468,6 +512,49 @@ int blocks_for(int64_t n, int per_block, int cap) {
 
 }  // namespace
 
+// ----------------------------------------------------------------------------- conditioning
+// Sinusoidal timestep features [B, 2 half] ("Flux architecture deep dive", §Model components ›
+// 1. Input embeddings › Conditioning): cos(tau f_k) in column k, sin(tau f_k) in column
+// half + k, tau = time_factor * t[b].  The frequencies come from the host in double; the angle
+// and its sine and cosine are taken in double (the angle reaches 1000 rad), then rounded once.
+constexpr int kTimeMaxHalf = 256;
+struct TimeFreqs {
+  double f[kTimeMaxHalf];
+};
+
+template <typename T>
+__global__ void timestep_features_kernel(const float* __restrict__ t, int batch, int half,
+                                         double time_factor, const __grid_constant__ TimeFreqs fr,
+                                         T* __restrict__ out) {
+  pdl_wait();  // the previous kernel's results are visible from here on
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= batch * half) return;
+  const int b = i / half, k = i - b * half;
+  const double ang = time_factor * static_cast<double>(__ldg(t + b)) * fr.f[k];
+  double sn, cs;
+  sincos(ang, &sn, &cs);
+  T* row = out + static_cast<size_t>(b) * 2 * half;
+  row[k] = static_cast<T>(static_cast<float>(cs));
+  row[half + k] = static_cast<T>(static_cast<float>(sn));
+}
+
+// vec[b, k] = v32[b, k] + g[b] w_g[k] + b_g[k] (the guidance term only when g is given), in
+// the activation type.
+template <typename T>
+__global__ void vec_finish_kernel(const float* __restrict__ v32, const float* __restrict__ g,
+                                  const T* __restrict__ wg, const T* __restrict__ bg, int batch,
+                                  int dim, T* __restrict__ vec) {
+  pdl_wait();  // the previous kernel's results are visible from here on
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= batch * dim) return;
+  float v = v32[i];
+  if (g) {
+    const int b = i / dim, k = i - b * dim;
+    v += __ldg(g + b) * to_f32(wg[k]) + to_f32(bg[k]);
+  }
+  vec[i] = static_cast<T>(v);
+}
+
 // ----------------------------------------------------------------------------- launchers
 cudaError_t launch_rope3d(const float* ids, int batch, int seq, const int axes[3], float theta,
                           float* cos_out, float* sin_out, cudaStream_t stream) {
@@ -491,7 +578,7 @@ cudaError_t launch_rope3d(const float* ids, int batch, int seq, const int axes[3
 }
 
 template <typename T, int NC, int NB>
-cudaError_t launch_mod(const void* vec, const ModJob& j0, const ModJob& j1, int dim, size_t smem,
+cudaError_t launch_mod(const void* vec, const ModJobs& jobs, int dim, int silu, int mode, size_t smem,
                        cudaStream_t stream) {
   auto kern = modulation_kernel<T, NC, NB>;
   static int configured = -1;
@@ -505,10 +592,11 @@ cudaError_t launch_mod(const void* vec, const ModJob& j0, const ModJob& j1, int 
   int per_sm = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kModThreads, smem);
   if (per_sm < 1) per_sm = 1;
-  const int rows = j0.rows + j1.rows;
+  const int rows = jobs.start[jobs.n];
   const int grid = blocks_for(rows, kModThreads / 32, num_sms() * per_sm);
   {
-    const cudaError_t e_ = launch_pdl(kern, dim3(grid), dim3(kModThreads), smem, stream, static_cast<const T*>(vec), j0, j1, dim);
+    const cudaError_t e_ = launch_pdl(kern, dim3(grid), dim3(kModThreads), smem, stream,
+                                      static_cast<const T*>(vec), jobs, dim, silu, mode);
     if (e_ != cudaSuccess) return e_;
   }
   count_launch();
@@ -516,45 +604,65 @@ cudaError_t launch_mod(const void* vec, const ModJob& j0, const ModJob& j1, int 
 }
 
 template <typename T, int NC>
-cudaError_t launch_mod_nb(const void* vec, const ModJob& j0, const ModJob& j1, int nb, int dim,
+cudaError_t launch_mod_nb(const void* vec, const ModJobs& jobs, int nb, int dim, int silu, int mode,
                           size_t smem, cudaStream_t stream) {
   switch (nb) {
-    case 1: return launch_mod<T, NC, 1>(vec, j0, j1, dim, smem, stream);
-    case 2: return launch_mod<T, NC, 2>(vec, j0, j1, dim, smem, stream);
-    case 3: return launch_mod<T, NC, 3>(vec, j0, j1, dim, smem, stream);
-    case 4: return launch_mod<T, NC, 4>(vec, j0, j1, dim, smem, stream);
-    case 5: return launch_mod<T, NC, 5>(vec, j0, j1, dim, smem, stream);
-    case 6: return launch_mod<T, NC, 6>(vec, j0, j1, dim, smem, stream);
-    case 7: return launch_mod<T, NC, 7>(vec, j0, j1, dim, smem, stream);
-    default: return launch_mod<T, NC, 8>(vec, j0, j1, dim, smem, stream);
+    case 1: return launch_mod<T, NC, 1>(vec, jobs, dim, silu, mode, smem, stream);
+    case 2: return launch_mod<T, NC, 2>(vec, jobs, dim, silu, mode, smem, stream);
+    case 3: return launch_mod<T, NC, 3>(vec, jobs, dim, silu, mode, smem, stream);
+    case 4: return launch_mod<T, NC, 4>(vec, jobs, dim, silu, mode, smem, stream);
+    case 5: return launch_mod<T, NC, 5>(vec, jobs, dim, silu, mode, smem, stream);
+    case 6: return launch_mod<T, NC, 6>(vec, jobs, dim, silu, mode, smem, stream);
+    case 7: return launch_mod<T, NC, 7>(vec, jobs, dim, silu, mode, smem, stream);
+    default: return launch_mod<T, NC, 8>(vec, jobs, dim, silu, mode, smem, stream);
   }
+}
+
+cudaError_t launch_gemv(int act, const void* vec, const ModulationJob* jobs, int njobs, int batch,
+                        int dim, int silu, int mode, cudaStream_t stream) {
+  const size_t elt = act == 1 ? 2 : 4;
+  const size_t out_elt = mode == kGemvOutAct ? elt : 4;
+  const int chunks = (dim + 255) / 256;
+  for (int j0 = 0; j0 < njobs; j0 += kModMaxJobs) {
+    const int nj = njobs - j0 < kModMaxJobs ? njobs - j0 : kModMaxJobs;
+    for (int b0 = 0; b0 < batch; b0 += kModMaxBatch) {
+      const int nb = batch - b0 < kModMaxBatch ? batch - b0 : kModMaxBatch;
+      const size_t smem = static_cast<size_t>(nb) * dim * sizeof(float);
+      ModJobs mj{};
+      int rows = 0;
+      mj.n = 0;
+      for (int i = 0; i < nj; ++i) {
+        const ModulationJob& jb = jobs[j0 + i];
+        if (jb.rows <= 0) continue;
+        mj.j[mj.n] = {jb.w, jb.bias, static_cast<uint8_t*>(jb.out) + static_cast<size_t>(b0) * jb.rows * out_elt,
+                      jb.rows};
+        mj.start[mj.n] = rows;
+        rows += jb.rows;
+        ++mj.n;
+      }
+      mj.start[mj.n] = rows;
+      if (rows == 0) continue;
+      const void* vb = static_cast<const uint8_t*>(vec) + static_cast<size_t>(b0) * dim * elt;
+      cudaError_t e;
+      if (act == 1) {
+        if (chunks <= 4) e = launch_mod_nb<__nv_bfloat16, 4>(vb, mj, nb, dim, silu, mode, smem, stream);
+        else if (chunks <= 8) e = launch_mod_nb<__nv_bfloat16, 8>(vb, mj, nb, dim, silu, mode, smem, stream);
+        else if (chunks <= 12) e = launch_mod_nb<__nv_bfloat16, 12>(vb, mj, nb, dim, silu, mode, smem, stream);
+        else e = launch_mod_nb<__nv_bfloat16, 24>(vb, mj, nb, dim, silu, mode, smem, stream);
+      } else {
+        if (chunks <= 4) e = launch_mod_nb<float, 4>(vb, mj, nb, dim, silu, mode, smem, stream);
+        else if (chunks <= 8) e = launch_mod_nb<float, 8>(vb, mj, nb, dim, silu, mode, smem, stream);
+        else e = launch_mod_nb<float, 16>(vb, mj, nb, dim, silu, mode, smem, stream);
+      }
+      if (e != cudaSuccess) return e;
+    }
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_modulation2(int act, const void* vec, const ModulationJob* jobs, int njobs,
                                int batch, int dim, cudaStream_t stream) {
-  const size_t elt = act == 1 ? 2 : 4;
-  const int chunks = (dim + 255) / 256;
-  for (int b0 = 0; b0 < batch; b0 += kModMaxBatch) {
-    const int nb = batch - b0 < kModMaxBatch ? batch - b0 : kModMaxBatch;
-    const size_t smem = static_cast<size_t>(nb) * dim * sizeof(float);
-    ModJob j[2] = {{nullptr, nullptr, nullptr, 0}, {nullptr, nullptr, nullptr, 0}};
-    for (int i = 0; i < njobs && i < 2; ++i)
-      j[i] = {jobs[i].w, jobs[i].bias, jobs[i].m + static_cast<size_t>(b0) * jobs[i].rows, jobs[i].rows};
-    const void* vb = static_cast<const uint8_t*>(vec) + static_cast<size_t>(b0) * dim * elt;
-    cudaError_t e;
-    if (act == 1) {
-      if (chunks <= 4) e = launch_mod_nb<__nv_bfloat16, 4>(vb, j[0], j[1], nb, dim, smem, stream);
-      else if (chunks <= 8) e = launch_mod_nb<__nv_bfloat16, 8>(vb, j[0], j[1], nb, dim, smem, stream);
-      else if (chunks <= 12) e = launch_mod_nb<__nv_bfloat16, 12>(vb, j[0], j[1], nb, dim, smem, stream);
-      else e = launch_mod_nb<__nv_bfloat16, 24>(vb, j[0], j[1], nb, dim, smem, stream);
-    } else {
-      if (chunks <= 4) e = launch_mod_nb<float, 4>(vb, j[0], j[1], nb, dim, smem, stream);
-      else if (chunks <= 8) e = launch_mod_nb<float, 8>(vb, j[0], j[1], nb, dim, smem, stream);
-      else e = launch_mod_nb<float, 16>(vb, j[0], j[1], nb, dim, smem, stream);
-    }
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
+  return launch_gemv(act, vec, jobs, njobs, batch, dim, 1, kGemvOutF32, stream);
 }
 
 cudaError_t launch_modulation(int act, const void* vec, const void* w, const void* bias, int batch,
@@ -711,6 +819,49 @@ cudaError_t launch_euler_cfg(int dtype, int64_t n, const void* z, const void* v_
                                       static_cast<const float*>(z), static_cast<const float*>(v_cond),
                                       static_cast<const float*>(v_uncond), guidance, dt, n,
                                       static_cast<float*>(z_out));
+    if (e_ != cudaSuccess) return e_;
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_timestep_features(int act, const float* t, int batch, int dim,
+                                     double time_factor, double max_period, void* out,
+                                     cudaStream_t stream) {
+  const int half = dim / 2;
+  if (dim % 2 != 0 || half < 1 || half > kTimeMaxHalf) return cudaErrorInvalidValue;
+  if (batch <= 0) return cudaSuccess;
+  TimeFreqs fr{};
+  for (int k = 0; k < half; ++k) fr.f[k] = std::pow(max_period, -static_cast<double>(k) / half);
+  const int grid = (batch * half + 255) / 256;
+  if (act == 1) {
+    const cudaError_t e_ = launch_pdl(timestep_features_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0,
+                                      stream, t, batch, half, time_factor, fr,
+                                      static_cast<__nv_bfloat16*>(out));
+    if (e_ != cudaSuccess) return e_;
+  } else {
+    const cudaError_t e_ = launch_pdl(timestep_features_kernel<float>, dim3(grid), dim3(256), 0, stream,
+                                      t, batch, half, time_factor, fr, static_cast<float*>(out));
+    if (e_ != cudaSuccess) return e_;
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_vec_finish(int act, const float* v32, const float* g, const void* wg,
+                              const void* bg, int batch, int dim, void* vec, cudaStream_t stream) {
+  if (batch <= 0 || dim <= 0) return cudaSuccess;
+  const int grid = (batch * dim + 255) / 256;
+  if (act == 1) {
+    const cudaError_t e_ = launch_pdl(vec_finish_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, stream, v32,
+                                      g, static_cast<const __nv_bfloat16*>(wg),
+                                      static_cast<const __nv_bfloat16*>(bg), batch, dim,
+                                      static_cast<__nv_bfloat16*>(vec));
+    if (e_ != cudaSuccess) return e_;
+  } else {
+    const cudaError_t e_ = launch_pdl(vec_finish_kernel<float>, dim3(grid), dim3(256), 0, stream, v32, g,
+                                      static_cast<const float*>(wg), static_cast<const float*>(bg), batch,
+                                      dim, static_cast<float*>(vec));
     if (e_ != cudaSuccess) return e_;
   }
   count_launch();

@@ -148,11 +148,25 @@ cudaError_t launch_modulation(int act, const void* vec, const void* w, const voi
 struct ModulationJob {
   const void* w;
   const void* bias;
-  float* m;
+  void* out;  // [batch, rows]: fp32, or the activation type under kGemvOutAct
   int rows;
 };
 cudaError_t launch_modulation2(int act, const void* vec, const ModulationJob* jobs, int njobs,
                                int batch, int dim, cudaStream_t stream);
+// The GEMV behind the modulation, for any number of weight matrices that read one input:
+// out_j[b, :] (=, or +=) f(vec[b, :]) W_j^T + b_j, f = SiLU when silu != 0, else the identity.
+// Jobs are grouped into launches of up to 80, batch rows into groups of up to 8.
+enum { kGemvOutF32 = 0, kGemvOutF32Add = 1, kGemvOutAct = 2 };
+cudaError_t launch_gemv(int act, const void* vec, const ModulationJob* jobs, int njobs, int batch,
+                        int dim, int silu, int mode, cudaStream_t stream);
+// Sinusoidal timestep features out[b, :] = [cos(tau f_k), sin(tau f_k)], tau = time_factor t[b],
+// f_k = max_period^(-k / half), k < half = dim / 2 (dim even, half <= 256).
+cudaError_t launch_timestep_features(int act, const float* t, int batch, int dim,
+                                     double time_factor, double max_period, void* out,
+                                     cudaStream_t stream);
+// vec = v32 (+ g[b] w_g + b_g when g != NULL), written in the activation type.
+cudaError_t launch_vec_finish(int act, const float* v32, const float* g, const void* wg,
+                              const void* bg, int batch, int dim, void* vec, cudaStream_t stream);
 // out[r, :] = LN(x[r, :]) * (1 + scale[b]) + shift[b], b = r / rows_per_batch; x, out [R, D].
 // x is fp32 when x_f32 != 0, else of the activation type; out is of the activation type.
 cudaError_t launch_ln_modulate(int act, int x_f32, const void* x, const float* shift, const float* scale,

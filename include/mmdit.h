@@ -335,6 +335,86 @@ mmdit_status mmdit_fp8_linear_fwd(int32_t M, int32_t N, int32_t K, const void *x
                                   const float *scale_x, const float *scale_w, const void *b,
                                   void *y, void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Many modulations in one launch: the AdaLN modulation of mmdit_modulation_fwd for every job
+ * in `jobs` (every block of a model, which all read the same vec), out_j[b, r] =
+ * sum_k SiLU(vec[b, k]) w_j[r, k] + b_j[r].  The weight traffic is the whole cost, so one
+ * launch streams all of it at the HBM rate instead of one short launch per block.
+ *   vec [batch, dim] of type `act`; each job: w [rows, dim], b [rows] (may be NULL) of type
+ *   `act`, out [batch, rows] fp32 (16-byte aligned); jobs is a host array of n_jobs entries.
+ * dim a multiple of 8, at most 6144.  No workspace. */
+typedef struct mmdit_gemv_job {
+  const void *w, *b;
+  float *out;
+  int32_t rows;
+} mmdit_gemv_job;
+mmdit_status mmdit_modulation_batched_fwd(int32_t act, int32_t batch, int32_t dim, const void *vec,
+                                          int32_t n_jobs, const mmdit_gemv_job *jobs, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Conditioning vector ([ARCH] §Model components, 1. Input embeddings, Conditioning; [API]
+ * §Components API, Embeddings, TimeStepEmbedder and MLPEmbedder):
+ *   vec = MLP_t(sinusoid(1000 t)) + MLP_y(y) [+ g w_g + b_g]
+ * sinusoid(tau)[b] = [cos(tau f_0 .. f_{h-1}), sin(tau f_0 .. f_{h-1})], f_k = 10000^(-k/h),
+ * h = time_dim / 2 (the pages print no formula: a reading); MLP(x) = Linear2(SiLU(Linear1(x)));
+ * the optional guidance term is a Linear of the scalar guidance scale.
+ *   t [batch] fp32 in [0, 1]; y [batch, vec_in_dim] (pooled text vector) of type `act`;
+ *   guidance [batch] fp32 or NULL (then w_guidance, b_guidance are not read);
+ *   weights of type `act`: time_in.w1 [D, time_dim], vector_in.w1 [D, vec_in_dim],
+ *   *.w2 [D, D], biases [D], w_guidance and b_guidance [D]; vec [batch, D] of type `act`.
+ * time_dim even, at most 512; time_dim, vec_in_dim and D multiples of 8, at most 6144.
+ * workspace >= mmdit_conditioning_workspace_size(). */
+typedef struct mmdit_mlp_embedder_w {
+  const void *w1, *b1; /* [D, in_dim], [D] */
+  const void *w2, *b2; /* [D, D], [D] */
+} mmdit_mlp_embedder_w;
+typedef struct mmdit_cond_w {
+  mmdit_mlp_embedder_w time_in;   /* in_dim = time_dim (256) */
+  mmdit_mlp_embedder_w vector_in; /* in_dim = vec_in_dim (768) */
+  const void *w_guidance, *b_guidance;
+} mmdit_cond_w;
+size_t mmdit_conditioning_workspace_size(int32_t act, int32_t batch, int32_t hidden, int32_t time_dim);
+mmdit_status mmdit_conditioning_fwd(int32_t act, int32_t batch, int32_t hidden, int32_t time_dim,
+                                    int32_t vec_in_dim, const mmdit_cond_w *w, const float *t,
+                                    const void *y, const float *guidance, void *vec,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * The whole model forward ([ARCH] §Data flow, Complete forward pass; §Overview, Model
+ * variants: Flux 12B has 19 double and 38 single blocks):
+ *   vec = conditioning(t, y, guidance); x_img = img_in(z_t); x_txt = txt_in(txt);
+ *   n_double double blocks on (x_img, x_txt); c = [x_img; x_txt];
+ *   n_single single blocks on c; pred = output head on the image rows of c.
+ * Every block's modulation is computed up front in one launch (they all read vec).
+ *   cfg->block: the block dims (seq_img = lat_h * lat_w, gemm = MMDIT_GEMM_NATIVE);
+ *   z_t [batch, channels, lat_h, lat_w] fp32; txt [batch, seq_txt, txt_dim] of type `act`;
+ *   t, guidance, y as for mmdit_conditioning_fwd; rope_cos, rope_sin [batch, seq, 64] fp32 as
+ *   rope3d_freqs writes them for the joint [image; text] ids; pred like z_t.
+ *   w->double_img, double_txt: host arrays of n_double stream weights; w->single: host array
+ *   of n_single (their `mod` fields are ignored: the call computes every modulation).
+ * workspace >= mmdit_flux_workspace_size(cfg); a bounded-wait timeout in any step is reported
+ * by mmdit_workspace_status on that workspace. */
+typedef struct mmdit_flux_config {
+  mmdit_dims block;
+  int32_t n_double, n_single;
+  int32_t lat_h, lat_w, channels; /* latent grid and channels (64) */
+  int32_t txt_dim;                /* text embedding width (4096) */
+  int32_t time_dim, vec_in_dim;   /* 256, 768 */
+} mmdit_flux_config;
+typedef struct mmdit_flux_w {
+  const void *w_img_in, *b_img_in; /* [D, channels], [D] */
+  const void *w_txt_in, *b_txt_in; /* [D, txt_dim], [D] */
+  mmdit_cond_w cond;
+  const mmdit_stream_w *double_img, *double_txt, *single;
+  const void *w_ada, *b_ada;       /* output head: [2D, D], [2D] */
+  const void *w_out, *b_out;       /* [channels, D], [channels] */
+} mmdit_flux_w;
+size_t mmdit_flux_workspace_size(const mmdit_flux_config *cfg);
+mmdit_status mmdit_flux_forward(const mmdit_flux_config *cfg, const mmdit_flux_w *w, const float *z_t,
+                                const void *txt, const float *t, const void *y,
+                                const float *guidance, const float *rope_cos, const float *rope_sin,
+                                float *pred, void *workspace, size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -153,3 +153,53 @@ def test_library_does_not_fall_back(tmp_path, monkeypatch):
     monkeypatch.setattr(L, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         L.load()
+
+
+def _flux_cfg(**kw):
+    d = _dims(batch=kw.pop("batch", 1), seq_img=1024, seq_txt=512, gemm=kw.pop("gemm", 0))
+    base = dict(n_double=19, n_single=38, lat_h=32, lat_w=32)
+    base.update(kw)
+    return L.make_flux_config(d, **base)
+
+
+def test_whole_model_workspace_and_validation(lib):
+    D, Si, St = 3072, 1024, 512
+    cfg = _flux_cfg()
+    ws = L.mmdit_flux_workspace_size(cfg)
+    # one block region plus vec, 76 modulations and the joint sequence (batch 1: the streams
+    # live inside it)
+    block = max(L.mmdit_double_block_workspace_size(cfg.block), L.mmdit_single_block_workspace_size(cfg.block))
+    floor = block + D * 2 + 76 * 6 * D * 4 + (Si + St) * D * 2
+    assert floor <= ws < floor + 64 * 1024
+    # batch 2 adds separate image and text streams
+    ws2 = L.mmdit_flux_workspace_size(_flux_cfg(batch=2))
+    assert ws2 > 2 * ws - block
+    # unsupported or inconsistent configurations size to 0 and are rejected before any launch
+    assert L.mmdit_flux_workspace_size(_flux_cfg(gemm=1)) == 0
+    assert L.mmdit_flux_workspace_size(_flux_cfg(lat_h=16)) == 0
+    assert L.mmdit_flux_workspace_size(_flux_cfg(time_dim=1024)) == 0
+    assert L.mmdit_flux_workspace_size(_flux_cfg(n_double=-1)) == 0
+    fw = L.FluxW()
+    for bad, status in ((_flux_cfg(gemm=1), 2), (_flux_cfg(lat_w=31), 1), (_flux_cfg(channels=48), 2)):
+        assert lib.mmdit_flux_forward(C.byref(bad), C.byref(fw), 16, 16, 16, 16, None, 16, 16, 16, 16,
+                                      1 << 30, None) == status
+    # NULL weights are reported, not dereferenced
+    assert lib.mmdit_flux_forward(C.byref(cfg), C.byref(fw), 16, 16, 16, 16, None, 16, 16, 16, 16,
+                                  1 << 30, None) == 1
+    assert "NULL" in L.last_error()
+
+
+def test_conditioning_and_batched_modulation_validation(lib):
+    assert lib.mmdit_conditioning_workspace_size(1, 2, 3072, 256) >= 256 + 2 * 256 * 2 + 2 * 3072 * (2 + 2 + 4)
+    cw = L.CondW()
+    # odd or oversized time_dim, misaligned widths: unsupported before the weights are looked at
+    assert lib.mmdit_conditioning_fwd(1, 2, 3072, 1024, 768, C.byref(cw), 16, 16, None, 16, 16, 1 << 20, None) == 2
+    assert lib.mmdit_conditioning_fwd(1, 2, 3072, 256, 770, C.byref(cw), 16, 16, None, 16, 16, 1 << 20, None) == 2
+    assert lib.mmdit_conditioning_fwd(1, 2, 3072, 256, 768, C.byref(cw), 16, 16, None, 16, 16, 1 << 20, None) == 1
+    job = L.GemvJob(16, None, 16, -1)
+    assert lib.mmdit_modulation_batched_fwd(1, 1, 3072, 16, 1, C.byref(job), None) == 1
+    assert lib.mmdit_modulation_batched_fwd(1, 1, 3070, 16, 1, C.byref(job), None) == 2
+    assert lib.mmdit_modulation_batched_fwd(1, 1, 3072, 16, 1, None, None) == 1
+    # nothing to do: no jobs, or an empty batch
+    assert lib.mmdit_modulation_batched_fwd(1, 1, 3072, 16, 0, None, None) == 0
+    assert lib.mmdit_modulation_batched_fwd(1, 0, 3072, 16, 1, C.byref(job), None) == 0
