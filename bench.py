@@ -39,6 +39,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MMDiT block fwd TFLOP/s & % of GB300 bf16 tensor peak at 4096+512 tokens"
 WORKLOAD = "flux535m_bf16"
 FP8_WORKLOAD = "flux12b_2048px_fp8"
+MODEL_WORKLOAD = "flux12b_512px_model"
 AXES = (16, 56, 56)
 THETA = 10000.0
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -56,9 +57,11 @@ def parse_args():
                     help="time plain per-call launches instead of a CUDA-graph replay of the step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time of the oracle baseline sample")
-    ap.add_argument("--workload", choices=[WORKLOAD, FP8_WORKLOAD], default=WORKLOAD,
+    ap.add_argument("--workload", choices=[WORKLOAD, FP8_WORKLOAD, MODEL_WORKLOAD], default=WORKLOAD,
                     help=f"{WORKLOAD}: the hot-path step above (the headline); {FP8_WORKLOAD}: the "
-                         "double + single block at 16384 + 512 tokens with E4M3 linears")
+                         "double + single block at 16384 + 512 tokens with E4M3 linears; "
+                         f"{MODEL_WORKLOAD}: the whole Flux 12B forward (19 double + 38 single "
+                         "blocks) at 1024 + 512 tokens through mmdit_flux_forward")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     return args
@@ -320,6 +323,86 @@ class Fp8BlockStep(DeviceStep):
                                  self.sin, self.Y, self.Z, ws=self.ws_block, fp8=self.fp8_s)
 
 
+class ModelStep(DeviceStep):
+    """The whole Flux 12B forward at 512 px through mmdit_flux_forward: rope3d_freqs, the
+    flow-matching noise, the model (conditioning vector from t and a pooled text vector, every
+    block's modulation in one launch, img_in, txt_in, 19 double and 38 single blocks, the output
+    head), the flow-matching loss.  Batch 1, 32 x 32 x 64 latents, a [1, 512, 4096] text
+    embedding and a [1, 768] pooled vector, N(0, 1).  The block weights (26 GB of bf16) are
+    drawn on the device from a seeded torch generator, N(0, 0.02), gains 1; the embedders and
+    the head from the seeded numpy generator."""
+
+    def __init__(self, wl, device):
+        import torch
+        from diffusion_transformer_flux_gb300 import _lib as L
+        from diffusion_transformer_flux_gb300 import synth
+        self.L, self.torch, self.wl = L, torch, wl
+        B, D, H, F, S_i, S_t = wl.batch, wl.hidden, wl.heads, wl.mlp_hidden, wl.seq_img, wl.seq_txt
+        S = S_i + S_t
+        bf = torch.bfloat16
+        rng_in = np.random.Generator(np.random.PCG64(1000 + wl.index))
+        rng_w = np.random.Generator(np.random.PCG64(2000 + wl.index))
+
+        def dev(a, dt=bf):
+            return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device).to(dt)
+
+        z0, z1 = synth.latent_pair(rng_in, B, wl.channels, wl.lat_h, wl.lat_w)
+        self.z0, self.z1 = dev(z0, torch.float32), dev(z1, torch.float32)
+        self.t = dev(synth.timesteps(rng_in, B, wl.t_dist), torch.float32)
+        self.txt = dev(synth.bf16_round(rng_in.standard_normal((B, S_t, wl.ctx_dim), dtype=np.float32)))
+        self.y = dev(synth.bf16_round(rng_in.standard_normal((B, wl.vec_dim), dtype=np.float32)))
+        self.ids = dev(synth.position_ids(B, wl.lat_h, wl.lat_w, S_t), torch.float32)
+        w = {"img_in": tuple(dev(a) for a in synth.embed_weights(rng_w, wl.channels, D).values()),
+             "txt_in": tuple(dev(a) for a in synth.embed_weights(rng_w, wl.ctx_dim, D).values()),
+             "time_in": tuple(dev(a) for a in synth.mlp_embedder_weights(rng_w, 256, D)),
+             "vector_in": tuple(dev(a) for a in synth.mlp_embedder_weights(rng_w, wl.vec_dim, D)),
+             "final": {k: dev(v) for k, v in synth.final_layer_weights(rng_w, D, wl.channels).items()}}
+        gen = torch.Generator(device=device).manual_seed(2000 + wl.index)
+
+        def n(*shape):
+            return (torch.randn(*shape, device=device, generator=gen) * 0.02).to(bf)
+
+        def stream():
+            one = torch.ones(128, device=device, dtype=bf)
+            return {"w_mod": n(6 * D, D), "b_mod": n(6 * D), "w_qkv": n(3 * D, D), "b_qkv": n(3 * D),
+                    "g_q": one, "g_k": one.clone(), "w_o": n(D, D), "b_o": n(D), "w_1": n(F, D), "b_1": n(F),
+                    "w_2": n(D, F), "b_2": n(D)}
+
+        w["double"] = [(stream(), stream()) for _ in range(wl.n_double)]
+        w["single"] = [stream() for _ in range(wl.n_single)]
+        self.weights = w
+        self.fw = L.make_flux_w(w)
+        dims = L.make_dims(B, S_i, S_t, D, H, F, L.MMDIT_BF16)
+        self.cfg = L.make_flux_config(dims, wl.n_double, wl.n_single, wl.lat_h, wl.lat_w, wl.channels,
+                                      wl.ctx_dim, 256, wl.vec_dim)
+        self.ws_model = L.workspace(L.mmdit_flux_workspace_size(self.cfg), device)
+        self.ws_flow = L.workspace(L.flow_match_workspace_size(B, self.z0[0].numel()), device)
+        self.cos = torch.empty(B, S, 64, device=device)
+        self.sin = torch.empty_like(self.cos)
+        self.zt = torch.empty_like(self.z0)
+        self.pred = torch.empty_like(self.z0)
+        self.loss = torch.zeros(1, device=device)
+        self.S, self.S_i = S, S_i
+        n_blocks = wl.n_double + wl.n_single
+        self.flops_blocks = n_blocks * block_flops(B, S, D, F, H)
+        self.flops_dense = (self.flops_blocks + 2 * B * S_i * wl.channels * D + 2 * B * S_t * wl.ctx_dim * D
+                            + 2 * B * S_i * D * wl.channels)
+
+    input_names = ("z0", "z1", "t", "txt", "y", "ids")
+
+    def workspaces(self):
+        return (self.ws_model, self.ws_flow)
+
+    def step(self):
+        L = self.L
+        L.rope3d_freqs(self.ids, AXES, THETA, self.cos, self.sin)
+        L.flow_match_noise_and_loss(self.z0, self.z1, self.t, z_t=self.zt, ws=self.ws_flow)
+        L.mmdit_flux_forward(self.cfg, self.fw, self.zt, self.txt, self.t, self.y, self.cos, self.sin,
+                             self.pred, ws=self.ws_model)
+        L.flow_match_noise_and_loss(self.z0, self.z1, self.t, pred=self.pred, loss=self.loss,
+                                    ws=self.ws_flow)
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     """Samples SM clock, power and throttle reasons with nvidia-smi while running."""
@@ -416,6 +499,11 @@ def kernel_work(label: str, wl):
         if op == "fp8_scale":
             return "latency", 0.0, ""
     n_lat = B * wl.channels * S_i
+    if label == "conditioning":  # the two embedders' weights
+        return "hbm", 2.0 * (256 * D + wl.vec_dim * D + 2 * D * D), "B"
+    if label == "modulation.batched":  # every block stream's 6D x D modulation weights
+        n_mod = 2 * wl.n_double + wl.n_single
+        return "hbm", n_mod * (6.0 * D * D * 2 + B * 6 * D * 4) + B * D * 2, "B"
     if label == "modulation":  # one block stream's 6D x D weights (mmdit_modulation_fwd)
         return "hbm", 6.0 * D * D * 2 + B * 6 * D * 4 + B * D * 2, "B"
     if label == "rope3d_freqs":
@@ -575,8 +663,9 @@ def main():
     L.load()
     wl = synth.WORKLOADS[args.workload]
     fp8 = wl.dtype == "fp8"
-    hw = None if fp8 else HostWorkload(wl)
-    st = Fp8BlockStep(wl, device) if fp8 else DeviceStep(hw, device)
+    model = args.workload == MODEL_WORKLOAD
+    hw = None if (fp8 or model) else HostWorkload(wl)
+    st = Fp8BlockStep(wl, device) if fp8 else ModelStep(wl, device) if model else DeviceStep(hw, device)
     peaks, peak_src = load_peaks()
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # > 129 MB of L2
@@ -729,10 +818,15 @@ def main():
                                  "CUDA-graph replay of the step (e2e: plain calls)",
                        "step": ("rope3d_freqs, double block, single block (E4M3 linears with "
                                 "delayed per-tensor scaling; weights cast at every call)") if fp8 else
+                               ("rope3d_freqs, flow-matching noise, mmdit_flux_forward (conditioning, "
+                                "every block's modulation in one launch, img_in, txt_in, "
+                                f"{wl.n_double} double + {wl.n_single} single blocks, output head), "
+                                "flow-matching loss") if model else
                                ("rope3d_freqs, flow-matching noise, img_in, txt_in, double block, "
                                 "single block, output head, flow-matching loss"),
-                       "streams": "the three block modulations (mmdit_modulation_fwd) on a second "
-                                  "stream, joined before each block",
+                       "streams": "one stream (the model's modulations run up front in one launch)"
+                                  if model else "the three block modulations (mmdit_modulation_fwd) on "
+                                  "a second stream, joined before each block",
                        "flops_counted_per_step": st.flops_blocks,
                        "dense_flops_per_step_incl_embeds_and_head": st.flops_dense},
             "pct_of_bf16_peak": round(100 * value / world / bf16_peak, 2),

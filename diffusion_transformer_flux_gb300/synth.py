@@ -51,6 +51,9 @@ class Workload:
     loss: bool = False     # output head + flow-matching loss on the image stream
     t_dist: str = "uniform"  # "uniform" | "logit_normal"
     index: int = 0
+    n_double: int = 0     # whole-model workloads ("model" blocks): double and single block counts
+    n_single: int = 0
+    vec_dim: int = 768    # pooled text vector feeding the conditioning embedder
 
     @property
     def seq_img(self) -> int:
@@ -76,6 +79,10 @@ WORKLOADS = {
     "flux12b_2048px_fp8": Workload(
         "flux12b_2048px_fp8", "fp8", 1, 128, 128, 512, 3072, 24, 128, 12288, ("double", "single"),
         index=4),
+    "flux12b_512px_model": Workload(
+        "flux12b_512px_model", "bf16", 1, 32, 32, 512, 3072, 24, 128, 12288, ("model",),
+        txt_from_ctx=True, img_from_latents=True, loss=True, t_dist="uniform", index=5,
+        n_double=19, n_single=38),
 }
 
 
