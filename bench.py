@@ -528,9 +528,9 @@ def source_digest():
     return h.hexdigest()[:16]
 
 
-def committed_traffic(label: str):
-    """DRAM bytes per launch of `label` from the committed ncu summary, if it was taken on the
-    current kernel sources (else None)."""
+def committed_traffic(label: str, workload: str):
+    """DRAM bytes per launch of `label` in `workload` from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -539,7 +539,7 @@ def committed_traffic(label: str):
         return None
     if t.get("source_digest") != source_digest():
         return None
-    v = t.get("bytes_per_launch", {}).get(label)
+    v = t.get("workloads", {}).get(workload, {}).get(label)
     return float(v) if v is not None else None
 
 
@@ -786,7 +786,7 @@ def main():
     else:
         ach, peak, runit = amount / dom_s / 1e9, hbm_peak, "GB/s"
     roofline = {"kernel": dom["kernel"], "bound": bound, "achieved": round(ach, 2), "peak": peak,
-                "unit": runit, "frac": round(ach / peak, 4), "traffic": committed_traffic(dom["kernel"]),
+                "unit": runit, "frac": round(ach / peak, 4), "traffic": committed_traffic(dom["kernel"], args.workload),
                 "algorithmic_per_launch": amount, "algorithmic_unit": unit,
                 "peak_source": f"{peak_src}: {'bf16_tflops (burst)' if bound == 'tensor' else 'hbm_gbs'}"}
     if peak != bf16_peak and bound == "tensor":
