@@ -383,6 +383,41 @@ def single_block_rows(x, vec, cos, sin, w, heads, rows, interleaved=True, gelu_t
     return _rows_after_attention(_f64(x)[:, rows], o, m, w, gelu_tanh, ln_eps, c, fp8, "single")
 
 
+# ----------------------------------------------------------------------------- parallel single block
+def _parallel_branches(x_rows, o_rows, shift, scale, gate, w, gelu_tanh, ln_eps, mm_cast):
+    """x + gate ([o | m] [W_o | W_2]^T + b_o + b_2), m = GELU(h W_1^T + b_1), h the one
+    LayerNorm-modulate both branches share: the fused output linear on the concatenation."""
+    h = modulate(x_rows, shift, scale, ln_eps)
+    m = gelu(linear(h, w["w_1"], w["b_1"], mm_cast), gelu_tanh)
+    om = np.concatenate([_cast(o_rows, mm_cast), m], axis=-1)
+    w_cat = np.concatenate([_f64(w["w_o"]), _f64(w["w_2"])], axis=1)
+    return gated_residual(x_rows, gate, linear(om, w_cat, _f64(w["b_o"]) + _f64(w["b_2"]), mm_cast))
+
+
+def single_block_parallel(x, vec, cos, sin, w, heads, interleaved=True, gelu_tanh=False,
+                          ln_eps=LN_EPS, rms_eps=RMS_EPS, mm_cast=None, rows=None):
+    """Single-stream block with parallel branches (the whole-model row's shape option: the
+    attention and the MLP fed from one LayerNorm, the QKV and fc1 linears reading the same
+    modulated input, and one gated residual through the output linear of the concatenation).
+
+    Modulation: three chunks (shift, scale, gate) of SiLU(vec) W_mod^T + b_mod, W_mod [3D, D].
+    The output linear is [W_o | W_2] [D, D + F] with bias b_o + b_2 (the stream's output
+    projection and fc2 weights side by side).  ``rows``: compute only those rows of the output
+    (keys and values still come from every token; everything after the attention is row-wise).
+    """
+    c = mm_cast
+    shift, scale, gate = modulation(vec, w["w_mod"], w["b_mod"], 3, mm_cast=c)
+    q, k, v = qkv_heads(x, shift, scale, w, heads, ln_eps, rms_eps, c)
+    cos, sin = _f64(cos), _f64(sin)
+    if rows is None:
+        rows = np.arange(np.shape(x)[1])
+    else:
+        rows = np.asarray(rows)
+        q, _, _ = qkv_heads(_f64(x)[:, rows], shift, scale, w, heads, ln_eps, rms_eps, c)
+    o = _attend_rows(q, k, v, cos[:, rows], sin[:, rows], cos, sin, interleaved, c)
+    return _parallel_branches(_f64(x)[:, rows], o, shift, scale, gate, w, gelu_tanh, ln_eps, c)
+
+
 # ----------------------------------------------------------------------------- embeddings and head
 def patchify(z):
     """[B, C, H, W] -> [B, H*W, C] with patch size 1 (architecture page, §Memory layout)."""
