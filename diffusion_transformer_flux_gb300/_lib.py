@@ -31,7 +31,7 @@ EXPORTED = [
     "mmdit_attention_workspace_size", "mmdit_attention_fwd", "mmdit_double_block_workspace_size",
     "mmdit_double_block_fwd", "mmdit_single_block_workspace_size", "mmdit_single_block_fwd",
     "mmdit_block_workspace_offsets", "mmdit_fp8_quantize_e4m3", "mmdit_fp8_linear_workspace_size",
-    "mmdit_fp8_linear_fwd", "mmdit_modulation_batched_fwd", "mmdit_conditioning_workspace_size",
+    "mmdit_fp8_linear_fwd", "mmdit_single_block_parallel_fwd", "mmdit_modulation_batched_fwd", "mmdit_conditioning_workspace_size",
     "mmdit_conditioning_fwd", "mmdit_flux_workspace_size", "mmdit_flux_forward",
 ]
 
@@ -137,6 +137,7 @@ _SIGS = {
     "mmdit_fp8_quantize_e4m3": (C.c_int, [VP, I64, VP, VP, VP, VP]),
     "mmdit_fp8_linear_workspace_size": (SZ, []),
     "mmdit_fp8_linear_fwd": (C.c_int, [I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_single_block_parallel_fwd": (C.c_int, [PDIMS, PW, VP, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_modulation_batched_fwd": (C.c_int, [I32, I32, I32, VP, I32, C.POINTER(GemvJob), VP]),
     "mmdit_conditioning_workspace_size": (SZ, [I32, I32, I32, I32]),
     "mmdit_conditioning_fwd": (C.c_int, [I32, I32, I32, I32, I32, PCOND, VP, VP, VP, VP, VP, SZ, VP]),
@@ -480,4 +481,15 @@ def mmdit_flux_forward(cfg: FluxConfig, w, z_t, txt, t, y, rope_cos, rope_sin, p
     _check(load().mmdit_flux_forward(C.byref(cfg), C.byref(fw), _ptr(z_t), _ptr(txt), _ptr(t), _ptr(y),
                                      _ptr(guidance), _ptr(rope_cos), _ptr(rope_sin), _ptr(pred), _ptr(ws),
                                      ws.numel(), _stream(stream)))
+    return ws
+
+
+def mmdit_single_block_parallel_fwd(dims: Dims, w: dict, vec, rope_cos, rope_sin, x, y, ws=None, stream=None):
+    """The parallel-branch single block: w["w_mod"] is [3D, D] (shift, scale, gate)."""
+    if ws is None:
+        ws = workspace(mmdit_single_block_workspace_size(dims), x.device)
+    sw = make_stream_w(w)
+    _check(load().mmdit_single_block_parallel_fwd(C.byref(dims), C.byref(sw), _ptr(vec), _ptr(rope_cos),
+                                                  _ptr(rope_sin), _ptr(x), _ptr(y), _ptr(ws), ws.numel(),
+                                                  _stream(stream)))
     return ws

@@ -194,6 +194,8 @@ bool encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const vo
 // ----------------------------------------------------------------------------- block planning
 struct BlockPlan {
   bool single;
+  bool parallel = false;  // single block with parallel branches: one LayerNorm feeds QKV and fc1
+  int mod_chunks = 6;     // modulation chunks per stream: 6, or 3 (shift, scale, gate) when parallel
   bool fp8;  // E4M3 linears: h, u hold E4M3 codes; o8 and wq hold the cast attention output
              // and weights
   int B, Si, St, S, S_pad, D, H, F;
@@ -395,7 +397,8 @@ mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss,
     LnModJob jobs[2];
     for (int i = 0; i < ss.n; ++i) {
       const float* mod = ss.mod[i];
-      jobs[i] = {ss.x[i], mod, mod + p.D, 6 * p.D, at(ws, p.h[ss.s[i]]), p.B * ss.rpb[i], ss.rpb[i]};
+      jobs[i] = {ss.x[i], mod, mod + p.D, static_cast<int64_t>(p.mod_chunks) * p.D, at(ws, p.h[ss.s[i]]),
+                 p.B * ss.rpb[i], ss.rpb[i]};
       if (f8.f) {
         const int t = fp8_tensor(ss.s[i], 0, 0);
         jobs[i].q_scale = f8.scale(t), jobs[i].q_amax = f8.amax(t);
@@ -460,7 +463,8 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
   for (int i = 0; i < ss.n; ++i) {
     const float* mod = ss.mod[i];
     EpiArgs e;
-    e.bias = ss.w[i]->b_o, e.resid = ss.x[i], e.gate = mod + 2 * p.D, e.gate_bstride = 6 * p.D;
+    e.bias = ss.w[i]->b_o, e.resid = ss.x[i], e.gate = mod + 2 * p.D,
+    e.gate_bstride = static_cast<int64_t>(p.mod_chunks) * p.D;
     e.rows_per_batch = ss.rpb[i], e.out = at(ws, p.x1[ss.s[i]]), e.out_f32 = 1;
     dequant(e, i, 1);
     add_problem(g, i, p.B * ss.rpb[i], at(ws, f8.f ? p.o8[ss.s[i]] : p.o[ss.s[i]]), weight(i, 1), e);
@@ -469,7 +473,8 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
     ProfScope ps_(p.single ? "single.out" : "double.out", st);
     MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "attention output projection");
   }
-  {
+  if (!p.parallel) {
+    // (the parallel block's fc1 reads the attention branch's LayerNorm output, still in h)
     ProfScope ps_(p.single ? "single.ln2" : "double.ln2", st);
     LnModJob jobs[2];
     for (int i = 0; i < ss.n; ++i) {
@@ -505,8 +510,11 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
   for (int i = 0; i < ss.n; ++i) {
     const float* mod = ss.mod[i];
     EpiArgs e;
-    e.bias = ss.w[i]->b_2, e.resid = at(ws, p.x1[ss.s[i]]), e.resid_f32 = 1, e.gate = mod + 5 * p.D;
-    e.gate_bstride = 6 * p.D, e.rows_per_batch = ss.rpb[i], e.out = ss.y[i];
+    // the parallel block adds both branches under its one gate: x1 + gate (u W_2^T + b_2) after
+    // x1 = x + gate (o W_o^T + b_o) is x + gate ([o | u] [W_o | W_2]^T + b_o + b_2)
+    e.bias = ss.w[i]->b_2, e.resid = at(ws, p.x1[ss.s[i]]), e.resid_f32 = 1;
+    e.gate = mod + (p.parallel ? 2 : 5) * p.D;
+    e.gate_bstride = static_cast<int64_t>(p.mod_chunks) * p.D, e.rows_per_batch = ss.rpb[i], e.out = ss.y[i];
     dequant(e, i, 3);
     add_problem(f2, i, p.B * ss.rpb[i], at(ws, p.u[ss.s[i]]), weight(i, 3), e);
   }
@@ -614,7 +622,7 @@ mmdit_status single_block_body(const mmdit_dims* d, const BlockPlan& p, const mm
   mmdit_status s = MMDIT_OK;
   if (!w->mod) {
     ProfScope ps_("single.modulation", st);
-    MMDIT_CUDA(launch_modulation(d->act, vec, w->w_mod, w->b_mod, p.B, 6 * p.D, p.D,
+    MMDIT_CUDA(launch_modulation(d->act, vec, w->w_mod, w->b_mod, p.B, p.mod_chunks * p.D, p.D,
                                  at<float>(workspace, p.mod[0]), st),
                "modulation");
   }
@@ -1184,6 +1192,27 @@ mmdit_status mmdit_fp8_linear_fwd(int32_t M, int32_t N, int32_t K, const void* x
   ProfScope ps_("fp8_linear", st);
   MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "FP8 linear");
   return MMDIT_OK;
+}
+
+mmdit_status mmdit_single_block_parallel_fwd(const mmdit_dims* d, const mmdit_stream_w* w, const void* vec,
+                                             const float* rope_cos, const float* rope_sin, const void* x,
+                                             void* y, void* workspace, size_t workspace_bytes, void* stream) {
+  mmdit_status s = check_dims(d);
+  if (s != MMDIT_OK) return s;
+  if (d->gemm != MMDIT_GEMM_NATIVE)
+    return fail(MMDIT_ERR_UNSUPPORTED, "parallel single block: native GEMMs only");
+  if ((s = check_stream_w(w, "parallel single-block weights")) != MMDIT_OK) return s;
+  if ((s = check_ptrs({vec, rope_cos, rope_sin, x, y}, "parallel single block")) != MMDIT_OK) return s;
+  if (static_cast<int64_t>(d->batch) * d->heads > 65535)
+    return fail(MMDIT_ERR_UNSUPPORTED, "batch * heads must be <= 65535");
+  BlockPlan p;
+  plan_block(d, true, &p);
+  p.parallel = true, p.mod_chunks = 3;
+  if ((s = check_workspace(workspace, workspace_bytes, p.total)) != MMDIT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
+  return single_block_body(d, p, w, vec, rope_cos, rope_sin, x, y, nullptr, workspace, st);
 }
 
 size_t mmdit_conditioning_workspace_size(int32_t act, int32_t batch, int32_t hidden, int32_t time_dim) {

@@ -336,6 +336,22 @@ mmdit_status mmdit_fp8_linear_fwd(int32_t M, int32_t N, int32_t K, const void *x
                                   void *y, void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Single-stream block with parallel branches (the whole-model row's shape option; [ARCH]
+ * §Model components, 4. Flux single block draws the sequential form above).  One
+ * LayerNorm-modulate h = LN(x)(1 + scale) + shift feeds both the attention (QKV, QK-RMSNorm,
+ * RoPE, joint attention -> o) and the MLP (u = GELU(h W_1^T + b_1)); one gated residual adds both
+ * through the output linear of the concatenation:
+ *   y = x + gate ([o | u] [W_o | W_2]^T + b_o + b_2)
+ * Modulation: three chunks (shift, scale, gate) = SiLU(vec) w_mod^T + b_mod with w_mod [3D, D],
+ * b_mod [3D] (mod, if given, is [B, 3D] fp32); the other weights as mmdit_stream_w states.
+ * Arguments, layouts and aliasing as mmdit_single_block_fwd; gemm must be MMDIT_GEMM_NATIVE.
+ * workspace >= mmdit_single_block_workspace_size(dims). */
+mmdit_status mmdit_single_block_parallel_fwd(const mmdit_dims *dims, const mmdit_stream_w *w,
+                                             const void *vec, const float *rope_cos,
+                                             const float *rope_sin, const void *x, void *y,
+                                             void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
  * Many modulations in one launch: the AdaLN modulation of mmdit_modulation_fwd for every job
  * in `jobs` (every block of a model, which all read the same vec), out_j[b, r] =
  * sum_k SiLU(vec[b, k]) w_j[r, k] + b_j[r].  The weight traffic is the whole cost, so one

@@ -203,3 +203,12 @@ def test_conditioning_and_batched_modulation_validation(lib):
     # nothing to do: no jobs, or an empty batch
     assert lib.mmdit_modulation_batched_fwd(1, 1, 3072, 16, 0, None, None) == 0
     assert lib.mmdit_modulation_batched_fwd(1, 0, 3072, 16, 1, C.byref(job), None) == 0
+
+
+def test_parallel_single_block_validation(lib):
+    sw = L.StreamW()
+    # FP8 is not offered for the parallel block; NULL weights are reported
+    assert lib.mmdit_single_block_parallel_fwd(C.byref(_dims(gemm=1)), C.byref(sw), 16, 16, 16, 16, 16, 16,
+                                               1 << 30, None) == 2
+    assert lib.mmdit_single_block_parallel_fwd(C.byref(_dims()), C.byref(sw), 16, 16, 16, 16, 16, 16,
+                                               1 << 30, None) == 1
