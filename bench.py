@@ -595,6 +595,29 @@ def measure_euler_step(L, torch, device, hbm_peak, n=1 << 26, reps=10):
             "avg_us": round(us, 2), "achieved_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4)}
 
 
+def measure_parallel_block(st, L, torch, peak, reps=10):
+    """The parallel-branch single block (mmdit_single_block_parallel_fwd) at the step's shapes:
+    the single block's weights with their first three modulation chunks, CUDA events around
+    `reps` calls after one warm-up (283 MB of weights per call, more than L2 holds)."""
+    wl = st.wl
+    D = wl.hidden
+    w = dict(st.w_single, w_mod=st.w_single["w_mod"][:3 * D], b_mod=st.w_single["b_mod"][:3 * D])
+    L.mmdit_single_block_parallel_fwd(st.dims, w, st.vec, st.cos, st.sin, st.Y, st.Z, ws=st.ws_block)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        L.mmdit_single_block_parallel_fwd(st.dims, w, st.vec, st.cos, st.sin, st.Y, st.Z, ws=st.ws_block)
+    b.record()
+    torch.cuda.synchronize()
+    if L.mmdit_workspace_status(st.ws_block) != 0:
+        raise RuntimeError("a kernel gave up a bounded wait in the parallel block")
+    us = a.elapsed_time(b) * 1e3 / reps
+    flops = block_flops(wl.batch, wl.seq, D, wl.mlp_hidden, wl.heads)
+    return {"block": "single block with parallel branches", "tokens": wl.seq, "avg_us": round(us, 2),
+            "achieved_tflops": round(flops / us / 1e6, 1), "frac": round(flops / us / 1e6 / peak, 4)}
+
+
 def run_cpu_baseline(hw: HostWorkload, min_seconds: float, rows=(32, 8)):
     flops, n, t0 = 0.0, 0, time.perf_counter()
     while True:
@@ -794,7 +817,10 @@ def main():
     if bound == "tensor" and "bf16_tflops_sustained" in peaks and peak == bf16_peak:
         roofline["frac_of_sustained"] = round(ach / float(peaks["bf16_tflops_sustained"]), 4)
 
-    extras = {} if fp8 else {"sampling_step": measure_euler_step(L, torch, device, hbm_peak)}
+    extras = {}
+    if not fp8 and not model:
+        extras["sampling_step"] = measure_euler_step(L, torch, device, hbm_peak)
+        extras["single_block_parallel"] = measure_parallel_block(st, L, torch, bf16_peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and hw is not None:
