@@ -1,0 +1,287 @@
+"""fp64 CPU oracle of the Flux block backward: gradients of the double- and single-block
+forward of ``oracle.flux`` with respect to its inputs, its conditioning vector and every weight.
+
+TEST INFRASTRUCTURE ONLY, like ``oracle.flux``: nothing in the library imports it and it shares
+no code with the CUDA path.  The pages train these blocks ("Flux architecture deep dive",
+§Training data flow; "Flux model API reference", §Training workflow example) but print no
+backward.  Each function here is the chain rule applied to the forward step it names, written
+out op by op in reverse order, in float64.  The forward intermediates the backward needs are
+recomputed here from their definitions, not taken from ``oracle.flux``.  The gradients are
+pinned in the tests by finite differences of the (separately pinned) forward.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+LN_EPS = 1e-6
+RMS_EPS = 1e-6
+
+
+def _f(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+# ----------------------------------------------------------------------------- per-op backward
+def linear_fwd(x, w, b):
+    """y = x W^T + b, W [out, in]."""
+    return _f(x) @ _f(w).T + _f(b)
+
+
+def linear_bwd(dy, x, w):
+    """(dx, dW, db) of y = x W^T + b: dx = dy W, dW = sum over rows of dy^T x, db = sum dy."""
+    dy, x, w = _f(dy), _f(x), _f(w)
+    dx = dy @ w
+    dw = dy.reshape(-1, dy.shape[-1]).T @ x.reshape(-1, x.shape[-1])
+    db = dy.reshape(-1, dy.shape[-1]).sum(axis=0)
+    return dx, dw, db
+
+
+def layernorm_fwd(x, eps=LN_EPS):
+    """xhat = (x - mean) r with r = 1/sqrt(biased var + eps); returns (xhat, r)."""
+    x = _f(x)
+    mu = x.mean(axis=-1, keepdims=True)
+    r = 1.0 / np.sqrt(((x - mu) ** 2).mean(axis=-1, keepdims=True) + eps)
+    return (x - mu) * r, r
+
+
+def layernorm_bwd(dxhat, xhat, r):
+    """dx of xhat = (x - mean(x)) r(x): r (dxhat - mean(dxhat) - xhat mean(dxhat xhat))."""
+    dxhat = _f(dxhat)
+    return r * (dxhat - dxhat.mean(axis=-1, keepdims=True)
+                - xhat * (dxhat * xhat).mean(axis=-1, keepdims=True))
+
+
+def modulate_bwd(dh, xhat, r, scale):
+    """Gradients of h = xhat (1 + scale[b]) + shift[b] (xhat the LayerNorm of x):
+    (dx, dshift [B, D], dscale [B, D])."""
+    dh = _f(dh)
+    dshift = dh.sum(axis=1)
+    dscale = (dh * xhat).sum(axis=1)
+    dx = layernorm_bwd(dh * (1.0 + _f(scale)[:, None, :]), xhat, r)
+    return dx, dshift, dscale
+
+
+def gated_residual_bwd(dy, gate, z):
+    """Gradients of y = x + gate[b] z: (dx, dz, dgate [B, D])."""
+    dy = _f(dy)
+    return dy, dy * _f(gate)[:, None, :], (dy * _f(z)).sum(axis=1)
+
+
+def rmsnorm_fwd(x, g, eps=RMS_EPS):
+    """y = x r g with r = 1/sqrt(mean(x^2) + eps) over the last axis; returns (y, xn, r), xn = x r."""
+    x = _f(x)
+    r = 1.0 / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps)
+    xn = x * r
+    return xn * _f(g), xn, r
+
+
+def rmsnorm_bwd(dy, xn, r, g):
+    """(dx, dg) of y = x r(x) g: dg = sum dy xn; dx = r (dy g - xn mean(dy g xn))."""
+    dy = _f(dy)
+    dyg = dy * _f(g)
+    dx = r * (dyg - xn * (dyg * xn).mean(axis=-1, keepdims=True))
+    dg = (dy * xn).reshape(-1, xn.shape[-1]).sum(axis=0)
+    return dx, dg
+
+
+def rope_rotate(x, cos, sin, interleaved=True):
+    """Each pair (a, b) of x's last axis -> (a cos - b sin, a sin + b cos)."""
+    x = _f(x)
+    d = x.shape[-1]
+    a, b = (x[..., 0::2], x[..., 1::2]) if interleaved else (x[..., : d // 2], x[..., d // 2:])
+    out = np.empty_like(x)
+    ra, rb = a * cos - b * sin, a * sin + b * cos
+    if interleaved:
+        out[..., 0::2], out[..., 1::2] = ra, rb
+    else:
+        out[..., : d // 2], out[..., d // 2:] = ra, rb
+    return out
+
+
+def rope_bwd(dy, cos, sin, interleaved=True):
+    """The rotation is orthogonal: its gradient is the rotation by the opposite angle."""
+    return rope_rotate(dy, cos, -_f(sin), interleaved)
+
+
+def attention_fwd(q, k, v):
+    """O = P V with P = softmax(q k^T / sqrt(d)); returns (O, P)."""
+    q, k, v = _f(q), _f(k), _f(v)
+    s = q @ np.swapaxes(k, -1, -2) / math.sqrt(q.shape[-1])
+    p = np.exp(s - s.max(axis=-1, keepdims=True))
+    p = p / p.sum(axis=-1, keepdims=True)
+    return p @ v, p
+
+
+def attention_bwd(do, q, k, v, p):
+    """(dq, dk, dv): dV = P^T dO; dP = dO V^T; dS = P (dP - rowsum(P dP)); dQ = dS K / sqrt(d);
+    dK = dS^T Q / sqrt(d)."""
+    do, q, k, v = _f(do), _f(q), _f(k), _f(v)
+    dv = np.swapaxes(p, -1, -2) @ do
+    dp = do @ np.swapaxes(v, -1, -2)
+    ds = p * (dp - (p * dp).sum(axis=-1, keepdims=True))
+    sc = 1.0 / math.sqrt(q.shape[-1])
+    return ds @ k * sc, np.swapaxes(ds, -1, -2) @ q * sc, dv
+
+
+def gelu_fwd(u, tanh=False):
+    u = _f(u)
+    if tanh:
+        c = math.sqrt(2.0 / math.pi)
+        return 0.5 * u * (1.0 + np.tanh(c * (u + 0.044715 * u ** 3)))
+    return 0.5 * u * (1.0 + np.vectorize(math.erf, otypes=[np.float64])(u / math.sqrt(2.0)))
+
+
+def gelu_grad(u, tanh=False):
+    """d/du of GELU: Phi(u) + u phi(u) (erf form), or the derivative of the tanh form."""
+    u = _f(u)
+    if tanh:
+        c = math.sqrt(2.0 / math.pi)
+        t = np.tanh(c * (u + 0.044715 * u ** 3))
+        return 0.5 * (1.0 + t) + 0.5 * u * (1.0 - t * t) * c * (1.0 + 3 * 0.044715 * u * u)
+    cdf = 0.5 * (1.0 + np.vectorize(math.erf, otypes=[np.float64])(u / math.sqrt(2.0)))
+    return cdf + u * np.exp(-0.5 * u * u) / math.sqrt(2.0 * math.pi)
+
+
+def silu_fwd(v):
+    v = _f(v)
+    return v / (1.0 + np.exp(-v))
+
+
+def silu_grad(v):
+    """d/dv of v sigma(v): sigma(v) (1 + v (1 - sigma(v)))."""
+    sg = 1.0 / (1.0 + np.exp(-_f(v)))
+    return sg * (1.0 + _f(v) * (1.0 - sg))
+
+
+def _heads(x, h):
+    B, S, HD = x.shape
+    return x.reshape(B, S, h, HD // h).transpose(0, 2, 1, 3)
+
+
+def _merge(x):
+    B, H, S, d = x.shape
+    return x.transpose(0, 2, 1, 3).reshape(B, S, H * d)
+
+
+# ----------------------------------------------------------------------------- one stream
+def _stream_pre(x, m, w, heads, ln_eps, rms_eps):
+    """Attention-branch prologue of one stream: LN1-modulate, QKV linear, per-head RMSNorm."""
+    D = np.shape(x)[-1]
+    xhat1, r1 = layernorm_fwd(x, ln_eps)
+    h1 = xhat1 * (1.0 + m[1][:, None, :]) + m[0][:, None, :]
+    qkv = linear_fwd(h1, w["w_qkv"], w["b_qkv"])
+    q, k, v = (_heads(qkv[..., i * D:(i + 1) * D], heads) for i in range(3))
+    qn, qxn, qr = rmsnorm_fwd(q, w["g_q"], rms_eps)
+    kn, kxn, kr = rmsnorm_fwd(k, w["g_k"], rms_eps)
+    return dict(xhat1=xhat1, r1=r1, h1=h1, qn=qn, qxn=qxn, qr=qr, kn=kn, kxn=kxn, kr=kr, v=v)
+
+
+def _stream_post(x, o, m, w, gelu_tanh, ln_eps):
+    """Everything after the attention for one stream, with its intermediates."""
+    a = linear_fwd(o, w["w_o"], w["b_o"])
+    x1 = _f(x) + m[2][:, None, :] * a
+    xhat2, r2 = layernorm_fwd(x1, ln_eps)
+    h2 = xhat2 * (1.0 + m[4][:, None, :]) + m[3][:, None, :]
+    u_pre = linear_fwd(h2, w["w_1"], w["b_1"])
+    u = gelu_fwd(u_pre, gelu_tanh)
+    z = linear_fwd(u, w["w_2"], w["b_2"])
+    y = x1 + m[5][:, None, :] * z
+    return y, dict(o=o, a=a, x1=x1, xhat2=xhat2, r2=r2, h2=h2, u_pre=u_pre, u=u, z=z)
+
+
+def _stream_post_bwd(dy, m, w, c, gelu_tanh):
+    """Backward of _stream_post: (dx, do, dm [6 chunks], weight grads)."""
+    g = {}
+    dx1, dz, dg2 = gated_residual_bwd(dy, m[5], c["z"])
+    du, g["w_2"], g["b_2"] = linear_bwd(dz, c["u"], w["w_2"])
+    du_pre = du * gelu_grad(c["u_pre"], gelu_tanh)
+    dh2, g["w_1"], g["b_1"] = linear_bwd(du_pre, c["h2"], w["w_1"])
+    dx1_ln, dsh2, dsc2 = modulate_bwd(dh2, c["xhat2"], c["r2"], m[4])
+    dx1 = dx1 + dx1_ln
+    dx, da, dg1 = gated_residual_bwd(dx1, m[2], c["a"])
+    do, g["w_o"], g["b_o"] = linear_bwd(da, c["o"], w["w_o"])
+    return dx, do, [None, None, dg1, dsh2, dsc2, dg2], g
+
+
+def _stream_pre_bwd(dq, dk, dv, m, w, c, heads):
+    """Backward of _stream_pre given the gradients of the normalized q, k and of v ([B,H,S,d]):
+    (dx, dshift1, dscale1, weight grads)."""
+    g = {}
+    dq_raw, g["g_q"] = rmsnorm_bwd(dq, c["qxn"], c["qr"], w["g_q"])
+    dk_raw, g["g_k"] = rmsnorm_bwd(dk, c["kxn"], c["kr"], w["g_k"])
+    dqkv = np.concatenate([_merge(dq_raw), _merge(dk_raw), _merge(_f(dv))], axis=-1)
+    dh1, g["w_qkv"], g["b_qkv"] = linear_bwd(dqkv, c["h1"], w["w_qkv"])
+    dx, dsh1, dsc1 = modulate_bwd(dh1, c["xhat1"], c["r1"], m[1])
+    return dx, dsh1, dsc1, g
+
+
+def _modulation(vec, w, n_chunks=6):
+    sv = silu_fwd(vec)
+    return np.split(linear_fwd(sv, w["w_mod"], w["b_mod"]), n_chunks, axis=-1)
+
+
+def _modulation_bwd(dm_chunks, vec, w):
+    """(dvec, dW_mod, db_mod) of m = SiLU(vec) W_mod^T + b_mod."""
+    dm = np.concatenate(dm_chunks, axis=-1)
+    sv = silu_fwd(vec)
+    dsv, dw, db = linear_bwd(dm, sv, w["w_mod"])
+    return dsv * silu_grad(vec), dw, db
+
+
+# ----------------------------------------------------------------------------- blocks
+def double_block_backward(x_img, x_txt, vec, cos, sin, w_img, w_txt, heads, dy_img, dy_txt,
+                          interleaved=True, gelu_tanh=False, ln_eps=LN_EPS, rms_eps=RMS_EPS):
+    """Gradients of the double block (architecture page, §Model components › 3. MMDiT layer).
+
+    Returns (dx_img, dx_txt, dvec, grads_img, grads_txt); each grads dict has the stream weight
+    names (w_mod, b_mod, w_qkv, b_qkv, g_q, g_k, w_o, b_o, w_1, b_1, w_2, b_2).
+    """
+    S_i = np.shape(x_img)[1]
+    mi, mt = _modulation(vec, w_img), _modulation(vec, w_txt)
+    ci = _stream_pre(x_img, mi, w_img, heads, ln_eps, rms_eps)
+    ct = _stream_pre(x_txt, mt, w_txt, heads, ln_eps, rms_eps)
+    cs, sn = _f(cos)[:, None], _f(sin)[:, None]
+    q = rope_rotate(np.concatenate([ci["qn"], ct["qn"]], axis=2), cs, sn, interleaved)
+    k = rope_rotate(np.concatenate([ci["kn"], ct["kn"]], axis=2), cs, sn, interleaved)
+    v = np.concatenate([ci["v"], ct["v"]], axis=2)
+    o, p = attention_fwd(q, k, v)
+    o = _merge(o)
+    _, pi = _stream_post(x_img, o[:, :S_i], mi, w_img, gelu_tanh, ln_eps)
+    _, pt = _stream_post(x_txt, o[:, S_i:], mt, w_txt, gelu_tanh, ln_eps)
+    # reverse
+    dxi, doi, dmi, gi = _stream_post_bwd(dy_img, mi, w_img, pi, gelu_tanh)
+    dxt, dot, dmt, gt = _stream_post_bwd(dy_txt, mt, w_txt, pt, gelu_tanh)
+    do = _heads(np.concatenate([doi, dot], axis=1), heads)
+    dq, dk, dv = attention_bwd(do, q, k, v, p)
+    dq, dk = rope_bwd(dq, cs, sn, interleaved), rope_bwd(dk, cs, sn, interleaved)
+    dxi2, dmi[0], dmi[1], gi2 = _stream_pre_bwd(dq[:, :, :S_i], dk[:, :, :S_i], dv[:, :, :S_i], mi,
+                                                w_img, ci, heads)
+    dxt2, dmt[0], dmt[1], gt2 = _stream_pre_bwd(dq[:, :, S_i:], dk[:, :, S_i:], dv[:, :, S_i:], mt,
+                                                w_txt, ct, heads)
+    gi.update(gi2)
+    gt.update(gt2)
+    dvi, gi["w_mod"], gi["b_mod"] = _modulation_bwd(dmi, vec, w_img)
+    dvt, gt["w_mod"], gt["b_mod"] = _modulation_bwd(dmt, vec, w_txt)
+    return dxi + dxi2, dxt + dxt2, dvi + dvt, gi, gt
+
+
+def single_block_backward(x, vec, cos, sin, w, heads, dy, interleaved=True, gelu_tanh=False,
+                          ln_eps=LN_EPS, rms_eps=RMS_EPS):
+    """Gradients of the single block over [img; txt] (architecture page, §Model components ›
+    4. Flux single block): (dx, dvec, grads)."""
+    m = _modulation(vec, w)
+    c = _stream_pre(x, m, w, heads, ln_eps, rms_eps)
+    cs, sn = _f(cos)[:, None], _f(sin)[:, None]
+    q = rope_rotate(c["qn"], cs, sn, interleaved)
+    k = rope_rotate(c["kn"], cs, sn, interleaved)
+    o, p = attention_fwd(q, k, c["v"])
+    _, pc = _stream_post(x, _merge(o), m, w, gelu_tanh, ln_eps)
+    dx, do, dm, g = _stream_post_bwd(dy, m, w, pc, gelu_tanh)
+    dq, dk, dv = attention_bwd(_heads(do, heads), q, k, c["v"], p)
+    dq, dk = rope_bwd(dq, cs, sn, interleaved), rope_bwd(dk, cs, sn, interleaved)
+    dx2, dm[0], dm[1], g2 = _stream_pre_bwd(dq, dk, dv, m, w, c, heads)
+    g.update(g2)
+    dvec, g["w_mod"], g["b_mod"] = _modulation_bwd(dm, vec, w)
+    return dx + dx2, dvec, g

@@ -1,0 +1,102 @@
+"""Pins of the block-backward oracle by finite differences of the forward (CPU only).
+
+For L = <dy, block(inputs, weights)> with a random dy, the gradient of L with respect to any
+tensor T is what the backward returns for T.  Each check compares <grad_T, V> for a random
+direction V with the central difference (L(T + eps V) - L(T - eps V)) / (2 eps) of the forward
+oracle in float64: an error in any step of the backward (a dropped term, a transposed operand,
+a wrong sign) shows as a mismatch far above the O(eps^2) difference error.  Covered: the double
+block (both streams, the joint attention, both RoPE pairings, the tanh GELU) and the single
+block, for the block inputs, the conditioning vector and every weight.
+"""
+import numpy as np
+import pytest
+
+from diffusion_transformer_flux_gb300 import synth
+from oracle import backward as BW
+from oracle import flux as O
+
+AX = (2, 2, 4)  # RoPE axes of the 8-wide heads below
+EPS = 1e-6
+
+
+def _case(seed, single, B=2, S_i=5, S_t=3, D=16, H=2, F=32):
+    rng = np.random.default_rng(seed)
+    # float64 copies: a perturbation of EPS must not be rounded away by a float32 tensor
+    w_img = {k: v.astype(np.float64) for k, v in synth.stream_weights(rng, D, H, D // H, F, "f32", 0.3,
+                                                                      gain_jitter=0.2).items()}
+    w_txt = {k: v.astype(np.float64) for k, v in synth.stream_weights(rng, D, H, D // H, F, "f32", 0.3,
+                                                                      gain_jitter=0.2).items()}
+    x_img = rng.standard_normal((B, S_i, D))
+    x_txt = rng.standard_normal((B, S_t, D))
+    vec = rng.standard_normal((B, D))
+    ids = synth.position_ids(B, 1, S_i, S_t)
+    ids[..., 0] = rng.integers(0, 3, size=ids.shape[:-1])  # non-zero ids on every axis
+    cos, sin = O.rope_cos_sin(ids, AX)
+    if single:
+        x = np.concatenate([x_img, x_txt], axis=1)
+        return dict(x=x), dict(w=w_img), vec, cos, sin, H, rng
+    return dict(x_img=x_img, x_txt=x_txt), dict(w_img=w_img, w_txt=w_txt), vec, cos, sin, H, rng
+
+
+def _directional(loss, grad, T, rng, n=3):
+    """Compare <grad, V> with the central difference of loss along V for n random V."""
+    for _ in range(n):
+        V = rng.standard_normal(np.shape(T))
+        base = np.array(T, dtype=np.float64, copy=True)
+
+        def at(s):
+            T[...] = base + s * EPS * V
+            return loss()
+        fd = (at(1.0) - at(-1.0)) / (2 * EPS)
+        T[...] = base
+        an = float(np.sum(grad * V))
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(fd)), (fd, an)
+
+
+@pytest.mark.parametrize("interleaved,tanh", [(True, False), (False, True)])
+def test_double_block_gradients_match_finite_differences(interleaved, tanh):
+    xs, ws, vec, cos, sin, H, rng = _case(11, False)
+    dy_i = rng.standard_normal(xs["x_img"].shape)
+    dy_t = rng.standard_normal(xs["x_txt"].shape)
+
+    def loss():
+        yi, yt = O.double_block(xs["x_img"], xs["x_txt"], vec, cos, sin, ws["w_img"], ws["w_txt"], H,
+                                interleaved, tanh)
+        return float(np.sum(yi * dy_i) + np.sum(yt * dy_t))
+
+    dxi, dxt, dvec, gi, gt = BW.double_block_backward(xs["x_img"], xs["x_txt"], vec, cos, sin, ws["w_img"],
+                                                      ws["w_txt"], H, dy_i, dy_t, interleaved, tanh)
+    _directional(loss, dxi, xs["x_img"], rng)
+    _directional(loss, dxt, xs["x_txt"], rng)
+    _directional(loss, dvec, vec, rng)
+    for w, g in ((ws["w_img"], gi), (ws["w_txt"], gt)):
+        assert set(g) == set(w)
+        for name in w:
+            _directional(loss, g[name], w[name], rng, n=2)
+
+
+def test_single_block_gradients_match_finite_differences():
+    xs, ws, vec, cos, sin, H, rng = _case(12, True)
+    dy = rng.standard_normal(xs["x"].shape)
+
+    def loss():
+        return float(np.sum(O.single_block(xs["x"], vec, cos, sin, ws["w"], H) * dy))
+
+    dx, dvec, g = BW.single_block_backward(xs["x"], vec, cos, sin, ws["w"], H, dy)
+    _directional(loss, dx, xs["x"], rng)
+    _directional(loss, dvec, vec, rng)
+    for name in ws["w"]:
+        _directional(loss, g[name], ws["w"][name], rng, n=2)
+
+
+def test_backward_forward_intermediates_match_the_forward_oracle():
+    # the backward's own recomputation of the forward agrees with oracle.flux (so the pins above
+    # test the gradient of the block the forward oracle defines)
+    xs, ws, vec, cos, sin, H, rng = _case(13, True)
+    m = BW._modulation(vec, ws["w"])
+    c = BW._stream_pre(xs["x"], m, ws["w"], H, BW.LN_EPS, BW.RMS_EPS)
+    q = BW.rope_rotate(c["qn"], cos[:, None], sin[:, None])
+    k = BW.rope_rotate(c["kn"], cos[:, None], sin[:, None])
+    o, _ = BW.attention_fwd(q, k, c["v"])
+    y, _ = BW._stream_post(xs["x"], BW._merge(o), m, ws["w"], False, BW.LN_EPS)
+    np.testing.assert_allclose(y, O.single_block(xs["x"], vec, cos, sin, ws["w"], H), atol=1e-12)
