@@ -618,6 +618,30 @@ def measure_parallel_block(st, L, torch, peak, reps=10):
             "achieved_tflops": round(flops / us / 1e6, 1), "frac": round(flops / us / 1e6 / peak, 4)}
 
 
+def measure_linear_bwd(L, torch, device, peak, M=4608, N=12288, K=3072, reps=5):
+    """The backward of the block's fc1-shaped linear (mmdit_linear_bwd: dx and dW through the
+    tensor-core GEMM on transposed operands, db): 4 M N K FLOPs per call, CUDA events around
+    `reps` calls after one warm-up."""
+    dy = torch.randn(M, N, device=device).to(torch.bfloat16)
+    x = torch.randn(M, K, device=device).to(torch.bfloat16)
+    w = (torch.randn(N, K, device=device) * 0.02).to(torch.bfloat16)
+    dx = torch.empty(M, K, device=device, dtype=torch.bfloat16)
+    dw = torch.empty(N, K, device=device)
+    db = torch.empty(N, device=device)
+    ws = L.mmdit_linear_bwd(dy, x, w, dx, dw, db)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        L.mmdit_linear_bwd(dy, x, w, dx, dw, db, ws=ws)
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / reps
+    flops = 4.0 * M * N * K
+    return {"op": "linear backward (dx, dW, db)", "M": M, "N": N, "K": K, "avg_us": round(us, 2),
+            "achieved_tflops": round(flops / us / 1e6, 1), "frac": round(flops / us / 1e6 / peak, 4)}
+
+
 def run_cpu_baseline(hw: HostWorkload, min_seconds: float, rows=(32, 8)):
     flops, n, t0 = 0.0, 0, time.perf_counter()
     while True:
@@ -821,6 +845,7 @@ def main():
     if not fp8 and not model:
         extras["sampling_step"] = measure_euler_step(L, torch, device, hbm_peak)
         extras["single_block_parallel"] = measure_parallel_block(st, L, torch, bf16_peak)
+        extras["linear_backward"] = measure_linear_bwd(L, torch, device, bf16_peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and hw is not None:

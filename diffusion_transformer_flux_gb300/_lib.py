@@ -31,7 +31,8 @@ EXPORTED = [
     "mmdit_attention_workspace_size", "mmdit_attention_fwd", "mmdit_double_block_workspace_size",
     "mmdit_double_block_fwd", "mmdit_single_block_workspace_size", "mmdit_single_block_fwd",
     "mmdit_block_workspace_offsets", "mmdit_fp8_quantize_e4m3", "mmdit_fp8_linear_workspace_size",
-    "mmdit_fp8_linear_fwd", "mmdit_single_block_parallel_fwd", "mmdit_modulation_batched_fwd", "mmdit_conditioning_workspace_size",
+    "mmdit_fp8_linear_fwd", "mmdit_single_block_parallel_fwd", "mmdit_linear_bwd_workspace_size",
+    "mmdit_linear_bwd", "mmdit_modulation_batched_fwd", "mmdit_conditioning_workspace_size",
     "mmdit_conditioning_fwd", "mmdit_flux_workspace_size", "mmdit_flux_forward",
 ]
 
@@ -138,6 +139,8 @@ _SIGS = {
     "mmdit_fp8_linear_workspace_size": (SZ, []),
     "mmdit_fp8_linear_fwd": (C.c_int, [I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_single_block_parallel_fwd": (C.c_int, [PDIMS, PW, VP, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_linear_bwd_workspace_size": (SZ, [I32, I32, I32, I32]),
+    "mmdit_linear_bwd": (C.c_int, [I32, I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_modulation_batched_fwd": (C.c_int, [I32, I32, I32, VP, I32, C.POINTER(GemvJob), VP]),
     "mmdit_conditioning_workspace_size": (SZ, [I32, I32, I32, I32]),
     "mmdit_conditioning_fwd": (C.c_int, [I32, I32, I32, I32, I32, PCOND, VP, VP, VP, VP, VP, SZ, VP]),
@@ -492,4 +495,20 @@ def mmdit_single_block_parallel_fwd(dims: Dims, w: dict, vec, rope_cos, rope_sin
     _check(load().mmdit_single_block_parallel_fwd(C.byref(dims), C.byref(sw), _ptr(vec), _ptr(rope_cos),
                                                   _ptr(rope_sin), _ptr(x), _ptr(y), _ptr(ws), ws.numel(),
                                                   _stream(stream)))
+    return ws
+
+
+def mmdit_linear_bwd_workspace_size(act, M, N, K) -> int:
+    return load().mmdit_linear_bwd_workspace_size(act, M, N, K)
+
+
+def mmdit_linear_bwd(dy, x, w, dx=None, dw=None, db=None, ws=None, stream=None):
+    """Backward of y = x W^T + b: dx = dy W, dW = dy^T x (fp32), db = sum of dy (fp32)."""
+    M, N = dy.reshape(-1, dy.shape[-1]).shape
+    K = w.shape[1]
+    act = act_of(dy)
+    if ws is None:
+        ws = workspace(mmdit_linear_bwd_workspace_size(act, M, N, K), dy.device)
+    _check(load().mmdit_linear_bwd(act, M, N, K, _ptr(dy), _ptr(x), _ptr(w), _ptr(dx), _ptr(dw), _ptr(db),
+                                   _ptr(ws), ws.numel(), _stream(stream)))
     return ws

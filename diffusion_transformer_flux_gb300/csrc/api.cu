@@ -50,6 +50,7 @@ EncodeTiledFn encode_fn() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+constexpr int kColsumChunks = 32;  // row chunks of the bias-gradient column sums
 size_t elt_bytes(int act) { return act == MMDIT_BF16 ? 2 : 4; }
 
 // Sequential 256-byte-aligned carving of a workspace.
@@ -1213,6 +1214,68 @@ mmdit_status mmdit_single_block_parallel_fwd(const mmdit_dims* d, const mmdit_st
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
   pdl_begin_call();
   return single_block_body(d, p, w, vec, rope_cos, rope_sin, x, y, nullptr, workspace, st);
+}
+
+size_t mmdit_linear_bwd_workspace_size(int32_t act, int32_t M, int32_t N, int32_t K) {
+  if (M < 0 || N <= 0 || K <= 0) return kStatusBytes;
+  const size_t e = elt_bytes(act), Mp = round_up(static_cast<size_t>(M), 8);
+  Carver c;
+  c.take(static_cast<size_t>(K) * N * e);   // W^T
+  c.take(static_cast<size_t>(N) * Mp * e);  // dy^T (rows padded with zeros to a multiple of 8)
+  c.take(static_cast<size_t>(K) * Mp * e);  // x^T
+  c.take(static_cast<size_t>(kColsumChunks) * N * 4);  // partial column sums of dy
+  return c.off;
+}
+
+mmdit_status mmdit_linear_bwd(int32_t act, int32_t M, int32_t N, int32_t K, const void* dy, const void* x,
+                              const void* w, void* dx, float* dw, float* db, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  if (act != MMDIT_F32 && act != MMDIT_BF16) return fail(MMDIT_ERR_INVALID_ARG, "bad act %d", act);
+  if (M < 0 || N <= 0 || K <= 0) return fail(MMDIT_ERR_INVALID_ARG, "bad shape M=%d N=%d K=%d", M, N, K);
+  if (K % 32 != 0 || N % 8 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "linear backward: K must be a multiple of 32 and N of 8 (K=%d, N=%d)", K, N);
+  mmdit_status s = MMDIT_OK;
+  if (M > 0 && (dx || dw || db) && (s = check_ptrs({dy}, "linear backward dy")) != MMDIT_OK) return s;
+  if (dx && ((s = check_ptrs({w, dx}, "linear backward dx")) != MMDIT_OK)) return s;
+  if (dw && ((s = check_ptrs({dw}, "linear backward dW")) != MMDIT_OK)) return s;
+  if (dw && M > 0 && ((s = check_ptrs({x}, "linear backward x")) != MMDIT_OK)) return s;
+  if (db && !aligned16(db)) return fail(MMDIT_ERR_INVALID_ARG, "linear backward: db not 16-byte aligned");
+  if ((s = check_workspace(workspace, workspace_bytes, mmdit_linear_bwd_workspace_size(act, M, N, K))) != MMDIT_OK)
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  if (M == 0) {  // an empty batch: zero weight and bias gradients, nothing else
+    if (dw) MMDIT_CUDA(cudaMemsetAsync(dw, 0, static_cast<size_t>(N) * K * 4, st), "dW clear");
+    if (db) MMDIT_CUDA(cudaMemsetAsync(db, 0, static_cast<size_t>(N) * 4, st), "db clear");
+    return MMDIT_OK;
+  }
+  pdl_begin_call();
+  const size_t e = elt_bytes(act);
+  const int Mp = static_cast<int>(round_up(static_cast<size_t>(M), 8));
+  Carver c;
+  void* wt = at(workspace, c.take(static_cast<size_t>(K) * N * e));
+  void* dyt = at(workspace, c.take(static_cast<size_t>(N) * Mp * e));
+  void* xt = at(workspace, c.take(static_cast<size_t>(K) * Mp * e));
+  float* part = at<float>(workspace, c.take(static_cast<size_t>(kColsumChunks) * N * 4));
+  ProfScope ps_("linear_bwd", st);
+  if (dx) {
+    // dx [M, K] = dy [M, N] W [N, K]: the GEMM's K-major operands are dy and W^T [K, N]
+    MMDIT_CUDA(launch_transpose_pad(act, w, N, K, N, wt, st), "W transpose");
+    GemmProblem g;
+    g.act = act, g.epi = kEpiBias, g.M = M, g.N = K, g.K = N, g.A = dy, g.W = wt, g.ep.out = dx;
+    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "dx GEMM");
+  }
+  if (dw) {
+    // dW [N, K] = dy^T x, contracted over the M rows: operands dy^T [N, Mp] and x^T [K, Mp]
+    MMDIT_CUDA(launch_transpose_pad(act, dy, M, N, Mp, dyt, st), "dy transpose");
+    MMDIT_CUDA(launch_transpose_pad(act, x, M, K, Mp, xt, st), "x transpose");
+    GemmProblem g;
+    g.act = act, g.epi = kEpiBias, g.M = N, g.N = K, g.K = Mp, g.A = dyt, g.W = xt, g.ep.out = dw;
+    g.ep.out_f32 = 1;
+    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "dW GEMM");
+  }
+  if (db) MMDIT_CUDA(launch_colsum(act, dy, M, N, part, kColsumChunks, db, st), "db column sums");
+  return MMDIT_OK;
 }
 
 size_t mmdit_conditioning_workspace_size(int32_t act, int32_t batch, int32_t hidden, int32_t time_dim) {

@@ -555,6 +555,50 @@ __global__ void vec_finish_kernel(const float* __restrict__ v32, const float* __
   vec[i] = static_cast<T>(v);
 }
 
+// ----------------------------------------------------------------------------- linear backward
+// out [C, ld_out] = in [R, C] transposed, with columns R .. ld_out - 1 of out set to zero (32 x 32
+// tiles through shared memory; 32 x 8 threads).  The backward GEMMs read the transposes as
+// K-major operands.
+template <typename T>
+__global__ void transpose_pad_kernel(const T* __restrict__ in, int R, int C, int ld_out, T* __restrict__ out) {
+  pdl_wait();  // the previous kernel's results are visible from here on
+  __shared__ float tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    tile[i][threadIdx.x] = (r < R && c < C) ? to_f32(in[static_cast<size_t>(r) * C + c]) : 0.f;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (c < C && r < ld_out) out[static_cast<size_t>(c) * ld_out + r] = static_cast<T>(tile[threadIdx.x][i]);
+  }
+}
+
+// Column sums of in [R, C] in a fixed order: chunk y of the rows into part[y, c], then the
+// chunks added in order.
+template <typename T>
+__global__ void colsum_partial_kernel(const T* __restrict__ in, int R, int C, float* __restrict__ part) {
+  pdl_wait();  // the previous kernel's results are visible from here on
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= C) return;
+  const int per = (R + gridDim.y - 1) / gridDim.y;
+  const int r0 = blockIdx.y * per;
+  const int r1 = r0 + per < R ? r0 + per : R;
+  float acc = 0.f;
+  for (int r = r0; r < r1; ++r) acc += to_f32(in[static_cast<size_t>(r) * C + c]);
+  part[static_cast<size_t>(blockIdx.y) * C + c] = acc;
+}
+
+__global__ void colsum_finish_kernel(const float* __restrict__ part, int chunks, int C, float* __restrict__ out) {
+  pdl_wait();  // the previous kernel's results are visible from here on
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= C) return;
+  float acc = 0.f;
+  for (int i = 0; i < chunks; ++i) acc += part[static_cast<size_t>(i) * C + c];
+  out[c] = acc;
+}
+
 // ----------------------------------------------------------------------------- launchers
 cudaError_t launch_rope3d(const float* ids, int batch, int seq, const int axes[3], float theta,
                           float* cos_out, float* sin_out, cudaStream_t stream) {
@@ -862,6 +906,49 @@ cudaError_t launch_vec_finish(int act, const float* v32, const float* g, const v
     const cudaError_t e_ = launch_pdl(vec_finish_kernel<float>, dim3(grid), dim3(256), 0, stream, v32, g,
                                       static_cast<const float*>(wg), static_cast<const float*>(bg), batch,
                                       dim, static_cast<float*>(vec));
+    if (e_ != cudaSuccess) return e_;
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_pad(int act, const void* in, int R, int C, int ld_out, void* out,
+                                 cudaStream_t stream) {
+  if (R <= 0 && ld_out <= 0) return cudaSuccess;
+  if (C <= 0 || ld_out < R) return cudaErrorInvalidValue;
+  const dim3 grid((C + 31) / 32, (ld_out + 31) / 32), block(32, 8);
+  if (act == 1) {
+    const cudaError_t e_ = launch_pdl(transpose_pad_kernel<__nv_bfloat16>, grid, block, 0, stream,
+                                      static_cast<const __nv_bfloat16*>(in), R, C, ld_out,
+                                      static_cast<__nv_bfloat16*>(out));
+    if (e_ != cudaSuccess) return e_;
+  } else {
+    const cudaError_t e_ = launch_pdl(transpose_pad_kernel<float>, grid, block, 0, stream,
+                                      static_cast<const float*>(in), R, C, ld_out, static_cast<float*>(out));
+    if (e_ != cudaSuccess) return e_;
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_colsum(int act, const void* in, int R, int C, float* part, int chunks, float* out,
+                          cudaStream_t stream) {
+  if (C <= 0) return cudaSuccess;
+  if (chunks < 1) return cudaErrorInvalidValue;
+  const dim3 grid((C + 255) / 256, chunks);
+  if (act == 1) {
+    const cudaError_t e_ = launch_pdl(colsum_partial_kernel<__nv_bfloat16>, grid, dim3(256), 0, stream,
+                                      static_cast<const __nv_bfloat16*>(in), R, C, part);
+    if (e_ != cudaSuccess) return e_;
+  } else {
+    const cudaError_t e_ = launch_pdl(colsum_partial_kernel<float>, grid, dim3(256), 0, stream,
+                                      static_cast<const float*>(in), R, C, part);
+    if (e_ != cudaSuccess) return e_;
+  }
+  count_launch();
+  {
+    const cudaError_t e_ = launch_pdl(colsum_finish_kernel, dim3((C + 255) / 256), dim3(256), 0, stream, part,
+                                      chunks, C, out);
     if (e_ != cudaSuccess) return e_;
   }
   count_launch();

@@ -164,6 +164,13 @@ cudaError_t launch_gemv(int act, const void* vec, const ModulationJob* jobs, int
 cudaError_t launch_timestep_features(int act, const float* t, int batch, int dim,
                                      double time_factor, double max_period, void* out,
                                      cudaStream_t stream);
+// out [C, ld_out] = in [R, C] transposed (activation type), columns R .. ld_out - 1 zero.
+cudaError_t launch_transpose_pad(int act, const void* in, int R, int C, int ld_out, void* out,
+                                 cudaStream_t stream);
+// out[c] = sum over rows of in [R, C] (fp32), fixed order: `chunks` row chunks into part
+// [chunks, C], then summed in chunk order.
+cudaError_t launch_colsum(int act, const void* in, int R, int C, float* part, int chunks, float* out,
+                          cudaStream_t stream);
 // vec = v32 (+ g[b] w_g + b_g when g != NULL), written in the activation type.
 cudaError_t launch_vec_finish(int act, const float* v32, const float* g, const void* wg,
                               const void* bg, int batch, int dim, void* vec, cudaStream_t stream);

@@ -352,6 +352,19 @@ mmdit_status mmdit_single_block_parallel_fwd(const mmdit_dims *dims, const mmdit
                                              void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Backward of a linear layer y = x W^T + b (the block backward's building block; the pages
+ * train these blocks, [ARCH] §Training data flow, and print no backward: the chain rule):
+ *   dx = dy W [M, K] (activation type), dW = dy^T x [N, K] fp32, db = column sums of dy [N] fp32.
+ * dy [M, N], x [M, K], W [N, K] of type `act`.  Any of dx, dw, db may be NULL (not computed);
+ * x is read only for dw and W only for dx.  bf16 operands with fp32 accumulation on the tensor
+ * cores (tf32 for MMDIT_F32); db in a fixed order (deterministic).  K % 32 == 0, N % 8 == 0;
+ * M == 0 zeroes dw and db.  workspace >= mmdit_linear_bwd_workspace_size(act, M, N, K). */
+size_t mmdit_linear_bwd_workspace_size(int32_t act, int32_t M, int32_t N, int32_t K);
+mmdit_status mmdit_linear_bwd(int32_t act, int32_t M, int32_t N, int32_t K, const void *dy, const void *x,
+                              const void *w, void *dx, float *dw, float *db, void *workspace,
+                              size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
  * Many modulations in one launch: the AdaLN modulation of mmdit_modulation_fwd for every job
  * in `jobs` (every block of a model, which all read the same vec), out_j[b, r] =
  * sum_k SiLU(vec[b, k]) w_j[r, k] + b_j[r].  The weight traffic is the whole cost, so one
