@@ -505,10 +505,14 @@ cudaError_t run_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream
 template <int KIND, int BN, int EPI>
 cudaError_t run_gemm_pair(const GemmProblem& p, uint32_t* status, cudaStream_t stream);
 
-// GEMMs that take the CTA-pair kernel (gemm_pair.cuh): the block linears' epilogues, N a
-// multiple of 256, and enough rows for the 256-row tiles to pay.
+// GEMMs that take the CTA-pair kernel (gemm_pair.cuh): the block linears' epilogues and plain
+// bias outputs (embeddings, the backward's GEMMs), N a multiple of 256, and enough rows for the
+// 256-row tiles to pay.
 inline bool use_pair(const GemmProblem& p) {
-  const bool epi_ok = p.epi == kEpiQkv || p.epi == kEpiGateResid || p.epi == kEpiGelu || p.epi == kEpiGeluF8;
+  // (a plain-bias GEMM with a short K, such as img_in's 64, is one k-step: the pair's set-up
+  // does not pay there)
+  const bool epi_ok = p.epi == kEpiQkv || p.epi == kEpiGateResid || p.epi == kEpiGelu || p.epi == kEpiGeluF8 ||
+                      (p.epi == kEpiBias && p.K >= 512);
   const bool qkv_ok = p.epi != kEpiQkv || p.ep.hidden % 256 == 0;
   return epi_ok && qkv_ok && p.N % 256 == 0 && p.M + p.M1 >= 512;
 }
@@ -522,6 +526,7 @@ cudaError_t dispatch_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t s
         case kEpiQkv: return run_gemm_pair<KIND, 256, kEpiQkv>(p, status, stream);
         case kEpiGateResid: return run_gemm_pair<KIND, 256, kEpiGateResid>(p, status, stream);
         case kEpiGelu: return run_gemm_pair<KIND, 256, kEpiGelu>(p, status, stream);
+        case kEpiBias: return run_gemm_pair<KIND, 256, kEpiBias>(p, status, stream);
         default: break;
       }
     }
