@@ -285,3 +285,143 @@ def single_block_backward(x, vec, cos, sin, w, heads, dy, interleaved=True, gelu
     g.update(g2)
     dvec, g["w_mod"], g["b_mod"] = _modulation_bwd(dm, vec, w)
     return dx + dx2, dvec, g
+
+
+# ----------------------------------------------------------------------------- whole model
+def flow_match_loss_grad(pred, z0, z1):
+    """d/dpred of mean((pred - (z1 - z0))^2) over all elements: 2 (pred - target) / N."""
+    pred = _f(pred)
+    return 2.0 * (pred - (_f(z1) - _f(z0))) / pred.size
+
+
+def _patchify(z):
+    B, C, H, W = np.shape(z)
+    return _f(z).reshape(B, C, H * W).transpose(0, 2, 1)
+
+
+def _unpatchify(tok, H, W):
+    B, S, C = np.shape(tok)
+    return _f(tok).transpose(0, 2, 1).reshape(B, C, H, W)
+
+
+def _sinusoid(t, dim, time_factor, max_period):
+    """[cos(tau f), sin(tau f)], tau = time_factor t, f_i = max_period^(-i/half); also tau f."""
+    half = dim // 2
+    f = max_period ** (-np.arange(half, dtype=np.float64) / half)
+    ang = time_factor * _f(t).reshape(-1, 1) * f[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1), ang, f
+
+
+def _embedder_fwd(x, w1, b1, w2, b2):
+    h = linear_fwd(x, w1, b1)
+    a = silu_fwd(h)
+    return linear_fwd(a, w2, b2), (x, h, a)
+
+
+def _embedder_bwd(dout, cache, w1, w2):
+    """Backward of Linear2(SiLU(Linear1(x))): (dx, (dw1, db1, dw2, db2))."""
+    x, h, a = cache
+    da, dw2, db2 = linear_bwd(dout, a, w2)
+    dx, dw1, db1 = linear_bwd(da * silu_grad(h), x, w1)
+    return dx, (dw1, db1, dw2, db2)
+
+
+def _double_fwd(x_img, x_txt, vec, cos, sin, wi, wt, heads, interleaved, gelu_tanh):
+    """The double block's outputs, recomputed from the pieces above."""
+    S_i = np.shape(x_img)[1]
+    mi, mt = _modulation(vec, wi), _modulation(vec, wt)
+    ci = _stream_pre(x_img, mi, wi, heads, LN_EPS, RMS_EPS)
+    ct = _stream_pre(x_txt, mt, wt, heads, LN_EPS, RMS_EPS)
+    cs, sn = _f(cos)[:, None], _f(sin)[:, None]
+    q = rope_rotate(np.concatenate([ci["qn"], ct["qn"]], axis=2), cs, sn, interleaved)
+    k = rope_rotate(np.concatenate([ci["kn"], ct["kn"]], axis=2), cs, sn, interleaved)
+    o, _ = attention_fwd(q, k, np.concatenate([ci["v"], ct["v"]], axis=2))
+    o = _merge(o)
+    yi, _ = _stream_post(x_img, o[:, :S_i], mi, wi, gelu_tanh, LN_EPS)
+    yt, _ = _stream_post(x_txt, o[:, S_i:], mt, wt, gelu_tanh, LN_EPS)
+    return yi, yt
+
+
+def _single_fwd(x, vec, cos, sin, w, heads, interleaved, gelu_tanh):
+    m = _modulation(vec, w)
+    c = _stream_pre(x, m, w, heads, LN_EPS, RMS_EPS)
+    cs, sn = _f(cos)[:, None], _f(sin)[:, None]
+    o, _ = attention_fwd(rope_rotate(c["qn"], cs, sn, interleaved), rope_rotate(c["kn"], cs, sn, interleaved),
+                         c["v"])
+    y, _ = _stream_post(x, _merge(o), m, w, gelu_tanh, LN_EPS)
+    return y
+
+
+def model_backward(z_t, txt, t, y, cos, sin, w, heads, dpred, g=None, interleaved=True, gelu_tanh=False,
+                   time_dim=256, time_factor=1000.0, max_period=10000.0):
+    """Gradients of the whole forward of ``oracle.flux.flux_forward`` (conditioning, img_in,
+    txt_in, the double blocks, the single blocks over [img; txt], the output head) for the
+    cotangent ``dpred`` of the prediction.  ``cos``/``sin`` are the RoPE tables of the joint
+    ids.  Returns (inputs, weights): inputs holds dz_t, dtxt, dt, dy (and dg with guidance);
+    weights mirrors ``w`` (tuples and stream dicts of the same names)."""
+    B, C, H, W = np.shape(z_t)
+    S_i = H * W
+    # forward, keeping what the backward reads
+    feat, ang, freqs = _sinusoid(t, time_dim, time_factor, max_period)
+    vt, c_t = _embedder_fwd(feat, *w["time_in"])
+    vy, c_y = _embedder_fwd(y, *w["vector_in"])
+    vec = vt + vy
+    if g is not None:
+        wg, bg = (_f(a) for a in w["guidance_in"])
+        vec = vec + _f(g).reshape(-1, 1) * wg[None, :] + bg[None, :]
+    patches = _patchify(z_t)
+    x_img = linear_fwd(patches, *w["img_in"])
+    x_txt = linear_fwd(txt, *w["txt_in"])
+    ins_d = []
+    for wi, wt in w["double"]:
+        ins_d.append((x_img, x_txt))
+        x_img, x_txt = _double_fwd(x_img, x_txt, vec, cos, sin, wi, wt, heads, interleaved, gelu_tanh)
+    c = np.concatenate([x_img, x_txt], axis=1)
+    ins_s = []
+    for ws in w["single"]:
+        ins_s.append(c)
+        c = _single_fwd(c, vec, cos, sin, ws, heads, interleaved, gelu_tanh)
+    f = w["final"]
+    sv = silu_fwd(vec)
+    shift, scale = np.split(linear_fwd(sv, f["w_ada"], f["b_ada"]), 2, axis=-1)
+    xhat, r = layernorm_fwd(c[:, :S_i], LN_EPS)
+    h = xhat * (1.0 + scale[:, None, :]) + shift[:, None, :]
+    # backward: head
+    gw = {"final": {}}
+    dh, gw["final"]["w_out"], gw["final"]["b_out"] = linear_bwd(_patchify(dpred), h, f["w_out"])
+    dx_img, dshift, dscale = modulate_bwd(dh, xhat, r, scale)
+    dsv, gw["final"]["w_ada"], gw["final"]["b_ada"] = linear_bwd(np.concatenate([dshift, dscale], axis=-1), sv,
+                                                                 f["w_ada"])
+    dvec = dsv * silu_grad(vec)
+    # the single blocks, last first, then the split of [img; txt]
+    dc = np.zeros_like(c)
+    dc[:, :S_i] = dx_img
+    gw["single"] = [None] * len(w["single"])
+    for i in reversed(range(len(w["single"]))):
+        dc, dv, gw["single"][i] = single_block_backward(ins_s[i], vec, cos, sin, w["single"][i], heads, dc,
+                                                        interleaved, gelu_tanh)
+        dvec = dvec + dv
+    d_img, d_txt = dc[:, :S_i], dc[:, S_i:]
+    gw["double"] = [None] * len(w["double"])
+    for i in reversed(range(len(w["double"]))):
+        wi, wt = w["double"][i]
+        d_img, d_txt, dv, gi, gt = double_block_backward(ins_d[i][0], ins_d[i][1], vec, cos, sin, wi, wt, heads,
+                                                         d_img, d_txt, interleaved, gelu_tanh)
+        gw["double"][i] = (gi, gt)
+        dvec = dvec + dv
+    # embeddings
+    dpatch, dw_in, db_in = linear_bwd(d_img, patches, w["img_in"][0])
+    gw["img_in"] = (dw_in, db_in)
+    dtxt, dw_t, db_t = linear_bwd(d_txt, txt, w["txt_in"][0])
+    gw["txt_in"] = (dw_t, db_t)
+    # conditioning: both embedders, the guidance term, and t through the sinusoid
+    dfeat, gw["time_in"] = _embedder_bwd(dvec, c_t, w["time_in"][0], w["time_in"][2])
+    dy_in, gw["vector_in"] = _embedder_bwd(dvec, c_y, w["vector_in"][0], w["vector_in"][2])
+    half = time_dim // 2
+    dang = -dfeat[:, :half] * np.sin(ang) + dfeat[:, half:] * np.cos(ang)
+    dt = (dang * freqs[None, :]).sum(axis=1) * time_factor
+    ins = {"z_t": _unpatchify(dpatch, H, W), "txt": dtxt, "t": dt, "y": dy_in}
+    if g is not None:
+        gw["guidance_in"] = ((dvec * _f(g).reshape(-1, 1)).sum(axis=0), dvec.sum(axis=0))
+        ins["g"] = (dvec * wg[None, :]).sum(axis=1)
+    return ins, gw

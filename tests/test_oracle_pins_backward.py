@@ -100,3 +100,62 @@ def test_backward_forward_intermediates_match_the_forward_oracle():
     o, _ = BW.attention_fwd(q, k, c["v"])
     y, _ = BW._stream_post(xs["x"], BW._merge(o), m, ws["w"], False, BW.LN_EPS)
     np.testing.assert_allclose(y, O.single_block(xs["x"], vec, cos, sin, ws["w"], H), atol=1e-12)
+
+
+def _f64_tree(w):
+    if isinstance(w, dict):
+        return {k: _f64_tree(v) for k, v in w.items()}
+    if isinstance(w, (list, tuple)):
+        return type(w)(_f64_tree(v) for v in w)
+    return np.array(w, dtype=np.float64)
+
+
+def test_loss_gradient_matches_finite_differences():
+    rng = np.random.default_rng(20)
+    z0, z1, pred = (rng.standard_normal((2, 3, 4, 5)) for _ in range(3))
+    grad = BW.flow_match_loss_grad(pred, z0, z1)
+    _directional(lambda: O.flow_match_loss(pred, z0, z1), grad, pred, rng)
+
+
+def test_whole_model_gradients_match_finite_differences():
+    # 1 double + 1 single block, 8-wide heads, guidance on: every input and every weight group
+    rng = np.random.default_rng(21)
+    D, H, F, lat_h, lat_w, S_t, txt_dim, vec_dim, B = 16, 2, 32, 2, 3, 3, 8, 8, 2
+    w = _f64_tree(synth.flux_weights(rng, D, H, F, 1, 1, txt_dim=txt_dim, vec_dim=vec_dim, guidance=True,
+                                     dtype="f32", std=0.3))
+    z = rng.standard_normal((B, 64, lat_h, lat_w))
+    txt = rng.standard_normal((B, S_t, txt_dim))
+    t = rng.uniform(0.1, 0.9, B)
+    y = rng.standard_normal((B, vec_dim))
+    g = np.array([1.5, 3.0])
+    ids = synth.position_ids(B, lat_h, lat_w, S_t)
+    cos, sin = O.rope_cos_sin(ids, AX)
+    dpred = rng.standard_normal(z.shape)
+
+    def loss():
+        return float(np.sum(O.flux_forward(z, txt, t, y, ids, w, H, g=g, axes_dim=AX) * dpred))
+
+    ins, gw = BW.model_backward(z, txt, t, y, cos, sin, w, H, dpred, g=g)
+    for name, T in (("z_t", z), ("txt", txt), ("y", y), ("g", g)):
+        _directional(loss, ins[name], T, rng, n=2)
+    # t: through the sinusoid (angles up to 1000 rad: a smaller step keeps the difference exact)
+    base = t.copy()
+    for _ in range(2):
+        V = rng.standard_normal(t.shape)
+        e = 1e-8
+        t[...] = base + e * V
+        a = loss()
+        t[...] = base - e * V
+        b = loss()
+        t[...] = base
+        fd, an = (a - b) / (2 * e), float(np.sum(ins["t"] * V))
+        assert abs(fd - an) <= 1e-4 * max(1.0, abs(fd)), (fd, an)
+    for key in ("img_in", "txt_in", "time_in", "vector_in", "guidance_in"):
+        for T, G in zip(w[key], gw[key]):
+            _directional(loss, G, T, rng, n=1)
+    for name in w["final"]:
+        _directional(loss, gw["final"][name], w["final"][name], rng, n=1)
+    for name in ("w_mod", "w_qkv", "g_k", "w_1", "b_2"):
+        _directional(loss, gw["double"][0][0][name], w["double"][0][0][name], rng, n=1)
+        _directional(loss, gw["double"][0][1][name], w["double"][0][1][name], rng, n=1)
+        _directional(loss, gw["single"][0][name], w["single"][0][name], rng, n=1)
