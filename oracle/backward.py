@@ -425,3 +425,34 @@ def model_backward(z_t, txt, t, y, cos, sin, w, heads, dpred, g=None, interleave
         gw["guidance_in"] = ((dvec * _f(g).reshape(-1, 1)).sum(axis=0), dvec.sum(axis=0))
         ins["g"] = (dvec * wg[None, :]).sum(axis=1)
     return ins, gw
+
+
+def single_block_parallel_backward(x, vec, cos, sin, w, heads, dy, interleaved=True, gelu_tanh=False,
+                                   ln_eps=LN_EPS, rms_eps=RMS_EPS):
+    """Gradients of the parallel-branch single block of ``oracle.flux.single_block_parallel``
+    (one LayerNorm-modulate h feeding QKV and fc1; y = x + gate ([o | u] [W_o | W_2]^T + b_o + b_2);
+    three modulation chunks): (dx, dvec, grads).  The two branches' gradients meet at h."""
+    m = _modulation(vec, w, 3)
+    c = _stream_pre(x, m, w, heads, ln_eps, rms_eps)
+    cs, sn = _f(cos)[:, None], _f(sin)[:, None]
+    q = rope_rotate(c["qn"], cs, sn, interleaved)
+    k = rope_rotate(c["kn"], cs, sn, interleaved)
+    o, p = attention_fwd(q, k, c["v"])
+    o = _merge(o)
+    u_pre = linear_fwd(c["h1"], w["w_1"], w["b_1"])
+    u = gelu_fwd(u_pre, gelu_tanh)
+    branch = linear_fwd(o, w["w_o"], w["b_o"]) + linear_fwd(u, w["w_2"], w["b_2"])
+    g = {}
+    dx, dbranch, dgate = gated_residual_bwd(dy, m[2], branch)
+    do, g["w_o"], g["b_o"] = linear_bwd(dbranch, o, w["w_o"])
+    du, g["w_2"], g["b_2"] = linear_bwd(dbranch, u, w["w_2"])
+    dh_mlp, g["w_1"], g["b_1"] = linear_bwd(du * gelu_grad(u_pre, gelu_tanh), c["h1"], w["w_1"])
+    dq, dk, dv = attention_bwd(_heads(do, heads), q, k, c["v"], p)
+    dq, dk = rope_bwd(dq, cs, sn, interleaved), rope_bwd(dk, cs, sn, interleaved)
+    dq_raw, g["g_q"] = rmsnorm_bwd(dq, c["qxn"], c["qr"], w["g_q"])
+    dk_raw, g["g_k"] = rmsnorm_bwd(dk, c["kxn"], c["kr"], w["g_k"])
+    dqkv = np.concatenate([_merge(dq_raw), _merge(dk_raw), _merge(dv)], axis=-1)
+    dh_att, g["w_qkv"], g["b_qkv"] = linear_bwd(dqkv, c["h1"], w["w_qkv"])
+    dx_ln, dshift, dscale = modulate_bwd(dh_att + dh_mlp, c["xhat1"], c["r1"], m[1])
+    dvec, g["w_mod"], g["b_mod"] = _modulation_bwd([dshift, dscale, dgate], vec, w)
+    return dx + dx_ln, dvec, g

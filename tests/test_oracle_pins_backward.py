@@ -159,3 +159,21 @@ def test_whole_model_gradients_match_finite_differences():
         _directional(loss, gw["double"][0][0][name], w["double"][0][0][name], rng, n=1)
         _directional(loss, gw["double"][0][1][name], w["double"][0][1][name], rng, n=1)
         _directional(loss, gw["single"][0][name], w["single"][0][name], rng, n=1)
+
+
+def test_parallel_single_block_gradients_match_finite_differences():
+    xs, ws, vec, cos, sin, H, rng = _case(14, True)
+    w = ws["w"]
+    D = w["w_o"].shape[0]
+    w["w_mod"], w["b_mod"] = w["w_mod"][:3 * D].copy(), w["b_mod"][:3 * D].copy()
+    dy = rng.standard_normal(xs["x"].shape)
+
+    def loss():
+        return float(np.sum(O.single_block_parallel(xs["x"], vec, cos, sin, w, H) * dy))
+
+    dx, dvec, g = BW.single_block_parallel_backward(xs["x"], vec, cos, sin, w, H, dy)
+    _directional(loss, dx, xs["x"], rng)
+    _directional(loss, dvec, vec, rng)
+    assert set(g) == set(w)
+    for name in w:
+        _directional(loss, g[name], w[name], rng, n=2)
