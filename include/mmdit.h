@@ -31,7 +31,7 @@
  *    status word that the call clears on entry; kernels with bounded waits set bits there if a
  *    wait gives up (they then return early and the outputs are undefined).  Read it with
  *    mmdit_workspace_status after the stream has run.
- *  - Errors: argument problems return MMDIT_ERR_INVALID_ARG, shapes or modes this build does
+ *  - Errors: argument problems return MMDIT_ERR_INVALID_ARG, shapes or modes the library does
  *    not implement return MMDIT_ERR_UNSUPPORTED, a short workspace returns
  *    MMDIT_ERR_WORKSPACE -- all before anything is enqueued.  A failed CUDA call or launch
  *    returns MMDIT_ERR_CUDA.  mmdit_last_error() gives a message for the calling thread's last
