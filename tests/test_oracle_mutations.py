@@ -59,6 +59,19 @@ MUTATIONS = [
     ("e4m3.py", "E4M3 ties rounded up instead of to even",
      "take_hi = (hi < len(_VALS)) & ((dhi < dlo) | ((dhi == dlo) & lo_odd))",
      "take_hi = (hi < len(_VALS)) & (dhi <= dlo)"),
+    ("e5m2.py", "E5M2 exponent bias 16",
+     "return sign * (1.0 + man / 4.0) * 2.0 ** (exp - 15)", "return sign * (1.0 + man / 4.0) * 2.0 ** (exp - 16)"),
+    ("e5m2.py", "E5M2 ties rounded away from zero",
+     "take_hi = (hi < len(_VALS)) & ((dhi < dlo) | ((dhi == dlo) & lo_odd))",
+     "take_hi = (hi < len(_VALS)) & (dhi <= dlo)"),
+    ("fp8_backward.py", "hybrid gradients cast to E4M3",
+     "return e5m2_quantize, E5M2_MAX", "return e4m3_quantize, E5M2_MAX"),
+    ("fp8_backward.py", "dgrad not divided by the weight scale",
+     "dx = g @ e4m3_quantize(w * s_w) / (s_dy * s_w)", "dx = g @ e4m3_quantize(w * s_w) / s_dy"),
+    ("fp8_backward.py", "FP8 wgrad on the unquantised input",
+     "dw = g2.T @ e4m3_quantize(x2 * s_x) / (s_dy * s_x)", "dw = g2.T @ x2 / s_dy"),
+    ("fp8_backward.py", "gradient scales against the E4M3 maximum under every recipe",
+     "out[k] = gradient_scale(a, self.recipe, margin)", 'out[k] = gradient_scale(a, "e4m3", margin)'),
     ("backward.py", "RoPE backward rotates the same way",
      "return rope_rotate(dy, cos, -_f(sin), interleaved)", "return rope_rotate(dy, cos, _f(sin), interleaved)"),
     ("backward.py", "softmax backward without the row-sum term",
