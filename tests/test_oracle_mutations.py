@@ -72,6 +72,21 @@ MUTATIONS = [
      "dw = g2.T @ e4m3_quantize(x2 * s_x) / (s_dy * s_x)", "dw = g2.T @ x2 / s_dy"),
     ("fp8_backward.py", "gradient scales against the E4M3 maximum under every recipe",
      "out[k] = gradient_scale(a, self.recipe, margin)", 'out[k] = gradient_scale(a, "e4m3", margin)'),
+    ("fp8_recipes.py", "MX shared exponent one too high",
+     "e = np.where(pos, k.astype(np.int64) - 1 - E4M3_EMAX, E8M0_MIN_EXP)",
+     "e = np.where(pos, k.astype(np.int64) - E4M3_EMAX, E8M0_MIN_EXP)"),
+    ("fp8_recipes.py", "MX elements multiplied by the block scale instead of divided",
+     "p[..., sl] = e4m3_quantize(np.ldexp(part, -ej[..., None]))",
+     "p[..., sl] = e4m3_quantize(np.ldexp(part, ej[..., None]))"),
+    ("fp8_recipes.py", "MX linear takes the input's block exponent twice",
+     "scale = np.ldexp(1.0, ex[..., j][..., None] + ew[:, j])",
+     "scale = np.ldexp(1.0, 2 * ex[..., j][..., None] + 0 * ew[:, j])"),
+    ("fp8_recipes.py", "blockwise weight tiles one row high",
+     "ns, ks = _slices(w.shape[0], tile), _slices(w.shape[1], tile)",
+     "ns, ks = _slices(w.shape[0], 1), _slices(w.shape[1], tile)"),
+    ("fp8_recipes.py", "tensorwise input cast with the weight's scale",
+     "sx, sw = tensorwise_scale(x, margin), tensorwise_scale(w, margin)",
+     "sx, sw = tensorwise_scale(w, margin), tensorwise_scale(w, margin)"),
     ("backward.py", "RoPE backward rotates the same way",
      "return rope_rotate(dy, cos, -_f(sin), interleaved)", "return rope_rotate(dy, cos, _f(sin), interleaved)"),
     ("backward.py", "softmax backward without the row-sum term",
