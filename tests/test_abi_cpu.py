@@ -212,3 +212,38 @@ def test_parallel_single_block_validation(lib):
                                                1 << 30, None) == 2
     assert lib.mmdit_single_block_parallel_fwd(C.byref(_dims()), C.byref(sw), 16, 16, 16, 16, 16, 16,
                                                1 << 30, None) == 1
+
+
+def test_linear_bwd_embedding_head_and_modulation_validation(lib):
+    # every case below is rejected before any CUDA call (no launch, no memset)
+    ws = L.mmdit_linear_bwd_workspace_size(1, 64, 128, 256)
+    assert ws >= 256 + 256 * 128 * 2 + 128 * 64 * 2 + 256 * 64 * 2
+    assert lib.mmdit_linear_bwd(7, 64, 128, 256, 16, 16, 16, 16, 16, 16, 16, 1 << 30, None) == 1
+    assert lib.mmdit_linear_bwd(1, -1, 128, 256, 16, 16, 16, 16, 16, 16, 16, 1 << 30, None) == 1
+    assert lib.mmdit_linear_bwd(1, 64, 128, 48, 16, 16, 16, 16, 16, 16, 16, 1 << 30, None) == 2
+    assert lib.mmdit_linear_bwd(1, 64, 100, 256, 16, 16, 16, 16, 16, 16, 16, 1 << 30, None) == 2
+    assert lib.mmdit_linear_bwd(1, 64, 128, 256, 0x1008, 16, 16, 16, None, None, 16, 1 << 30, None) == 1
+    assert lib.mmdit_linear_bwd(1, 64, 128, 256, 16, None, 16, None, 16, None, 16, 1 << 30, None) == 1
+    assert "linear backward x" in L.last_error()
+    assert lib.mmdit_linear_bwd(1, 64, 128, 256, 16, 16, 16, None, None, 0x1004, 16, 1 << 30, None) == 1
+    assert lib.mmdit_linear_bwd(1, 64, 128, 256, 16, 16, 16, 16, 16, 16, 16, ws - 1, None) == 3
+    # img_in: channels a multiple of 8, hidden of 32, every pointer given, workspace big enough
+    assert lib.mmdit_img_in_fwd(1, 1, 12, 8, 8, 256, 16, 16, 16, 16, 16, 1 << 30, None) == 2
+    assert lib.mmdit_img_in_fwd(1, 1, 64, 8, 8, 48, 16, 16, 16, 16, 16, 1 << 30, None) == 2
+    assert lib.mmdit_img_in_fwd(1, 0, 64, 8, 8, 256, 16, 16, 16, 16, 16, 1 << 30, None) == 1
+    assert lib.mmdit_img_in_fwd(1, 1, 64, 8, 8, 256, None, 16, 16, 16, 16, 1 << 30, None) == 1
+    assert lib.mmdit_img_in_fwd(1, 1, 64, 8, 8, 256, 16, 16, 16, 16, 16, 16, None) == 3
+    # output head: seq_img must be lat_h * lat_w; channels a multiple of 32, hidden of 256
+    d = _dims(seq_img=64, hidden=256, heads=2, mlp_hidden=1024)
+    assert lib.mmdit_final_layer_fwd(C.byref(d), 64, 8, 7, 16, 16, 16, 16, 16, 16, 16, 16, 1 << 30, None) == 1
+    assert lib.mmdit_final_layer_fwd(C.byref(d), 48, 8, 8, 16, 16, 16, 16, 16, 16, 16, 16, 1 << 30, None) == 2
+    d2 = _dims(seq_img=64, hidden=384, heads=3, mlp_hidden=1536)
+    assert lib.mmdit_final_layer_fwd(C.byref(d2), 64, 8, 8, 16, 16, 16, 16, 16, 16, 16, 16, 1 << 30, None) == 2
+    assert lib.mmdit_final_layer_fwd(C.byref(d), 64, 8, 8, 16, None, 16, 16, 16, 16, 16, 16, 1 << 30, None) == 1
+    assert lib.mmdit_final_layer_fwd(None, 64, 8, 8, 16, 16, 16, 16, 16, 16, 16, 16, 1 << 30, None) == 1
+    # modulation GEMV: dim a multiple of 8 and at most 6144; an empty batch does nothing
+    assert lib.mmdit_modulation_fwd(1, 1, 6 * 3072, 3070, 16, 16, 16, 16, None) == 2
+    assert lib.mmdit_modulation_fwd(1, 1, 6 * 3072, 6152, 16, 16, 16, 16, None) == 2
+    assert lib.mmdit_modulation_fwd(1, -1, 6 * 3072, 3072, 16, 16, 16, 16, None) == 1
+    assert lib.mmdit_modulation_fwd(1, 1, 6 * 3072, 3072, None, 16, 16, 16, None) == 1
+    assert lib.mmdit_modulation_fwd(1, 0, 6 * 3072, 3072, None, None, None, None, None) == 0
