@@ -14,7 +14,9 @@
  * ---------------------------------------
  *  - Every pointer argument is DEVICE memory owned by the caller, except `dims`, the weight-set
  *    structs and `axes_dim`, which are host memory read during the call.  The library
- *    allocates no device memory and keeps no device state between calls.
+ *    allocates no device memory and keeps no device state between calls, with one exception:
+ *    flow_match_noise_and_loss_noalloc keeps its partial sums in a static device array of
+ *    its own (described at its declaration).
  *  - Calls are asynchronous: kernels are enqueued on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream) and the call returns without synchronising.
  *  - Layouts are row-major.  Activations are token-major [B, S, features].  Linear weights are
