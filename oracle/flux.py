@@ -24,7 +24,9 @@ design notes of the repository as well):
   * LayerNorm has no affine parameters (the modulation supplies scale/shift),
     biased variance, eps 1e-6 (API page, §Configuration, layernorm_epsilon).
   * Every linear has a bias.  The attention output projection is included.
-  * GELU is the exact erf form; the tanh form is behind ``gelu_tanh=True``.
+  * GELU is the exact erf form; the tanh form is behind ``gelu_tanh=True``.  Both forms are
+    pinned to textbook values; which of them the pages mean is a reading that no outside
+    value settles (parity unpinned for that choice only).
   * Attention scale is 1/sqrt(head_dim), no mask.
   * The single block runs attention then MLP in sequence with six modulation
     chunks, over the whole concatenated sequence, and returns every row.
