@@ -8,6 +8,8 @@ a wrong sign) shows as a mismatch far above the O(eps^2) difference error.  Cove
 block (both streams, the joint attention, both RoPE pairings, the tanh GELU) and the single
 block, for the block inputs, the conditioning vector and every weight.
 """
+import math
+
 import numpy as np
 import pytest
 
@@ -177,3 +179,33 @@ def test_parallel_single_block_gradients_match_finite_differences():
     assert set(g) == set(w)
     for name in w:
         _directional(loss, g[name], w[name], rng, n=2)
+
+
+def test_attention_backward_in_the_saved_log_sum_exp_form():
+    # The form a flash-style backward computes in: P recomputed from the scores and the row
+    # log-sum-exp L saved by the forward, P = exp(S / sqrt(d) - L); and the row term of the
+    # softmax gradient taken as D = rowsum(dO * O) instead of rowsum(P * dP).  Both are
+    # identities (O = P V, so rowsum(P * (dO V^T)) = rowsum(dO * (P V))); they are checked here
+    # against brute force over the keys, and the oracle's gradients against the form they give.
+    rng = np.random.default_rng(7)
+    B, H, S, d = 1, 2, 37, 16
+    q, k, v = (rng.standard_normal((B, H, S, d)) * 2.0 for _ in range(3))
+    do = rng.standard_normal((B, H, S, d))
+    s = q @ np.swapaxes(k, -1, -2) / math.sqrt(d)
+    lse = np.empty((B, H, S))
+    for h in range(H):
+        for i in range(S):
+            m = max(s[0, h, i])
+            lse[0, h, i] = m + math.log(sum(math.exp(x - m) for x in s[0, h, i]))
+    p = np.exp(s - lse[..., None])
+    o, p_oracle = BW.attention_fwd(q, k, v)
+    np.testing.assert_allclose(p, p_oracle, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(p.sum(axis=-1), 1.0, rtol=1e-13)
+    dp = do @ np.swapaxes(v, -1, -2)
+    D = (do * o).sum(axis=-1)
+    np.testing.assert_allclose(D, (p * dp).sum(axis=-1), rtol=1e-10, atol=1e-12)
+    ds = p * (dp - D[..., None])
+    dq, dk, dv = BW.attention_bwd(do, q, k, v, p_oracle)
+    np.testing.assert_allclose(dq, ds @ k / math.sqrt(d), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, np.swapaxes(ds, -1, -2) @ q / math.sqrt(d), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, np.swapaxes(p, -1, -2) @ do, rtol=1e-10, atol=1e-12)
