@@ -138,3 +138,42 @@ def test_stack_with_no_blocks_and_identity_blocks_agree():
     w2["double"] = w["double"] + [tuple(_zero_gates(s) for s in w["double"][0])]
     w2["single"] = w["single"] + [_zero_gates(w["single"][0])]
     np.testing.assert_allclose(O.flux_forward(z, txt, t, y, ids, w2, H, axes_dim=AX), base, atol=1e-13)
+
+
+def _tree_params(w):
+    """Number of parameters in a weight tree (dicts, lists and tuples of arrays)."""
+    if isinstance(w, dict):
+        return sum(_tree_params(v) for v in w.values())
+    if isinstance(w, (list, tuple)):
+        return sum(_tree_params(v) for v in w)
+    return int(np.size(w))
+
+
+def _count(D, F, d, n_double, n_single, parallel, txt_dim=4096, vec_dim=768, time_dim=256, channels=64):
+    """Parameters of the whole model from its weight shapes (the trees flux_weights draws)."""
+    stream = 6 * D * D + 6 * D + 3 * D * D + 3 * D + 2 * d + D * D + D + F * D + F + D * F + D
+    single = stream - 3 * D * D - 3 * D if parallel else stream   # three modulation chunks, not six
+    emb = (channels * D + D) + (txt_dim * D + D) + (time_dim * D + D + D * D + D) \
+        + (vec_dim * D + D + D * D + D) + (2 * D * D + 2 * D + channels * D + channels)
+    return n_double * 2 * stream + n_single * single + emb
+
+
+def test_parameter_counts_against_the_model_variants_table():
+    # The architecture page's parameter table prints ~535 million for 1 double + 1 single block
+    # and ~12 billion for 19 + 38 (hidden 3072, MLP 12288).  The shape formula is first checked
+    # against real weight trees at a small size, then evaluated at those sizes: the blocks as
+    # built land within 0.5% and 1% of the printed counts with the parallel-branch single block, while
+    # the sequential single block drawn in the single-block section gives 563.6 million and 12.97
+    # billion (5% and 8% high).  The printed counts thus favour the parallel form.
+    rng = np.random.default_rng(3)
+    D, H, F = 64, 2, 256
+    w = synth.flux_weights(rng, D, H, F, 2, 3, txt_dim=48, vec_dim=24, time_dim=16, channels=8, dtype="f32")
+    assert _tree_params(w) == _count(D, F, D // H, 2, 3, False, 48, 24, 16, 8)
+    for s in w["single"]:
+        s["w_mod"], s["b_mod"] = s["w_mod"][:3 * D], s["b_mod"][:3 * D]
+    assert _tree_params(w) == _count(D, F, D // H, 2, 3, True, 48, 24, 16, 8)
+    D, F, d = 3072, 12288, 128
+    par535, par12 = _count(D, F, d, 1, 1, True), _count(D, F, d, 19, 38, True)
+    seq535, seq12 = _count(D, F, d, 1, 1, False), _count(D, F, d, 19, 38, False)
+    assert abs(par535 / 535e6 - 1) < 0.005 and abs(par12 / 12e9 - 1) < 0.015   # 535.3 M, 11.89 B
+    assert seq535 / 535e6 > 1.04 and seq12 / 12e9 > 1.07                      # 563.6 M, 12.97 B
