@@ -174,9 +174,11 @@ def mlp_embedder_weights(rng, in_dim, hidden, dtype="bf16", std=0.02):
 
 
 def flux_weights(rng, hidden, heads, mlp_hidden, n_double, n_single, txt_dim=4096, vec_dim=768,
-                 time_dim=256, channels=64, guidance=False, dtype="bf16", std=0.02):
+                 time_dim=256, channels=64, guidance=False, dtype="bf16", std=0.02, single_parallel=False):
     """Random weights of the whole model: embedders, ``n_double`` double blocks (an image and a
-    text stream each), ``n_single`` single blocks and the output head."""
+    text stream each), ``n_single`` single blocks and the output head.  ``single_parallel``: the
+    single blocks take the parallel-branch form's three modulation chunks (the first 3D rows of
+    the same draw)."""
     d = hidden // heads
     w = {"img_in": tuple(embed_weights(rng, channels, hidden, dtype, std).values()),
          "txt_in": tuple(embed_weights(rng, txt_dim, hidden, dtype, std).values()),
@@ -187,6 +189,9 @@ def flux_weights(rng, hidden, heads, mlp_hidden, n_double, n_single, txt_dim=409
     w["double"] = [(stream_weights(rng, hidden, heads, d, mlp_hidden, dtype, std),
                     stream_weights(rng, hidden, heads, d, mlp_hidden, dtype, std)) for _ in range(n_double)]
     w["single"] = [stream_weights(rng, hidden, heads, d, mlp_hidden, dtype, std) for _ in range(n_single)]
+    if single_parallel:
+        for ws in w["single"]:
+            ws["w_mod"], ws["b_mod"] = ws["w_mod"][:3 * hidden].copy(), ws["b_mod"][:3 * hidden].copy()
     w["final"] = final_layer_weights(rng, hidden, channels, dtype, std)
     return w
 

@@ -352,13 +352,27 @@ def _single_fwd(x, vec, cos, sin, w, heads, interleaved, gelu_tanh):
     return y
 
 
+def _single_parallel_fwd(x, vec, cos, sin, w, heads, interleaved, gelu_tanh):
+    m = _modulation(vec, w, 3)
+    c = _stream_pre(x, m, w, heads, LN_EPS, RMS_EPS)
+    cs, sn = _f(cos)[:, None], _f(sin)[:, None]
+    o, _ = attention_fwd(rope_rotate(c["qn"], cs, sn, interleaved), rope_rotate(c["kn"], cs, sn, interleaved),
+                         c["v"])
+    u = gelu_fwd(linear_fwd(c["h1"], w["w_1"], w["b_1"]), gelu_tanh)
+    branch = linear_fwd(_merge(o), w["w_o"], w["b_o"]) + linear_fwd(u, w["w_2"], w["b_2"])
+    return _f(x) + m[2][:, None, :] * branch
+
+
 def model_backward(z_t, txt, t, y, cos, sin, w, heads, dpred, g=None, interleaved=True, gelu_tanh=False,
-                   time_dim=256, time_factor=1000.0, max_period=10000.0):
+                   time_dim=256, time_factor=1000.0, max_period=10000.0, single_parallel=False):
     """Gradients of the whole forward of ``oracle.flux.flux_forward`` (conditioning, img_in,
     txt_in, the double blocks, the single blocks over [img; txt], the output head) for the
     cotangent ``dpred`` of the prediction.  ``cos``/``sin`` are the RoPE tables of the joint
     ids.  Returns (inputs, weights): inputs holds dz_t, dtxt, dt, dy (and dg with guidance);
-    weights mirrors ``w`` (tuples and stream dicts of the same names)."""
+    weights mirrors ``w`` (tuples and stream dicts of the same names).  ``single_parallel``: the
+    single blocks are the parallel-branch form, as in ``flux_forward``."""
+    single_fwd = _single_parallel_fwd if single_parallel else _single_fwd
+    single_bwd = single_block_parallel_backward if single_parallel else single_block_backward
     B, C, H, W = np.shape(z_t)
     S_i = H * W
     # forward, keeping what the backward reads
@@ -380,7 +394,7 @@ def model_backward(z_t, txt, t, y, cos, sin, w, heads, dpred, g=None, interleave
     ins_s = []
     for ws in w["single"]:
         ins_s.append(c)
-        c = _single_fwd(c, vec, cos, sin, ws, heads, interleaved, gelu_tanh)
+        c = single_fwd(c, vec, cos, sin, ws, heads, interleaved, gelu_tanh)
     f = w["final"]
     sv = silu_fwd(vec)
     shift, scale = np.split(linear_fwd(sv, f["w_ada"], f["b_ada"]), 2, axis=-1)
@@ -398,8 +412,8 @@ def model_backward(z_t, txt, t, y, cos, sin, w, heads, dpred, g=None, interleave
     dc[:, :S_i] = dx_img
     gw["single"] = [None] * len(w["single"])
     for i in reversed(range(len(w["single"]))):
-        dc, dv, gw["single"][i] = single_block_backward(ins_s[i], vec, cos, sin, w["single"][i], heads, dc,
-                                                        interleaved, gelu_tanh)
+        dc, dv, gw["single"][i] = single_bwd(ins_s[i], vec, cos, sin, w["single"][i], heads, dc,
+                                             interleaved, gelu_tanh)
         dvec = dvec + dv
     d_img, d_txt = dc[:, :S_i], dc[:, S_i:]
     gw["double"] = [None] * len(w["double"])

@@ -502,7 +502,7 @@ def conditioning_vec(t, y, w, g=None, mm_cast=None):
 
 
 def flux_forward(z_t, txt, t, y, ids, w, heads, g=None, interleaved=True, gelu_tanh=False,
-                 mm_cast=None, store=None, axes_dim=AXES_DIM):
+                 mm_cast=None, store=None, axes_dim=AXES_DIM, single_parallel=False):
     """The whole model (architecture page, §Data flow › Complete forward pass; §Model variants:
     19 double and 38 single blocks for Flux 12B, 1 and 1 for Flux 535M).
 
@@ -510,9 +510,12 @@ def flux_forward(z_t, txt, t, y, ids, w, heads, g=None, interleaved=True, gelu_t
     blocks over the concatenation [img; txt]; the output head on the image rows of the last
     block.  ``store`` (e.g. ``round_bf16``) is applied to every tensor the model hands from one
     step to the next (vec, the embedded tokens, each block's outputs), the values an
-    implementation that stores them in the activation type holds.
+    implementation that stores them in the activation type holds.  ``single_parallel``: the single
+    blocks are the parallel-branch form (``single_block_parallel``), the form whose parameter
+    count matches the architecture page's variant table.
     """
     keep = store if store is not None else _f64
+    single = single_block_parallel if single_parallel else single_block
     B, C, H, W = np.shape(z_t)
     vec = keep(conditioning_vec(t, y, w, g, mm_cast))
     x_img = keep(img_in(z_t, w["img_in"][0], w["img_in"][1], mm_cast))
@@ -524,7 +527,7 @@ def flux_forward(z_t, txt, t, y, ids, w, heads, g=None, interleaved=True, gelu_t
         x_img, x_txt = keep(x_img), keep(x_txt)
     c = np.concatenate([x_img, x_txt], axis=1)
     for ws in w["single"]:
-        c = keep(single_block(c, vec, cos, sin, ws, heads, interleaved, gelu_tanh, mm_cast=mm_cast))
+        c = keep(single(c, vec, cos, sin, ws, heads, interleaved, gelu_tanh, mm_cast=mm_cast))
     f = w["final"]
     return final_layer(c[:, : H * W], vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], H, W,
                        mm_cast=mm_cast)

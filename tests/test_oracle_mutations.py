@@ -87,6 +87,11 @@ MUTATIONS = [
     ("fp8_recipes.py", "tensorwise input cast with the weight's scale",
      "sx, sw = tensorwise_scale(x, margin), tensorwise_scale(w, margin)",
      "sx, sw = tensorwise_scale(w, margin), tensorwise_scale(w, margin)"),
+    ("flux.py", "whole model with the parallel switch still runs the sequential single block",
+     "single = single_block_parallel if single_parallel else single_block", "single = single_block"),
+    ("backward.py", "the whole-model backward's parallel single forward drops its MLP branch",
+     'branch = linear_fwd(_merge(o), w["w_o"], w["b_o"]) + linear_fwd(u, w["w_2"], w["b_2"])\n    return',
+     'branch = linear_fwd(_merge(o), w["w_o"], w["b_o"])\n    return'),
     ("backward.py", "RoPE backward rotates the same way",
      "return rope_rotate(dy, cos, -_f(sin), interleaved)", "return rope_rotate(dy, cos, _f(sin), interleaved)"),
     ("backward.py", "softmax backward without the row-sum term",

@@ -209,3 +209,32 @@ def test_attention_backward_in_the_saved_log_sum_exp_form():
     np.testing.assert_allclose(dq, ds @ k / math.sqrt(d), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(dk, np.swapaxes(ds, -1, -2) @ q / math.sqrt(d), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(dv, np.swapaxes(p, -1, -2) @ do, rtol=1e-10, atol=1e-12)
+
+
+def test_whole_model_with_parallel_single_blocks_matches_finite_differences():
+    # the parallel-branch single blocks in the whole model: inputs, the conditioning path and the
+    # single block's weights (three modulation chunks)
+    rng = np.random.default_rng(22)
+    D, H, F, lat_h, lat_w, S_t, txt_dim, vec_dim, B = 16, 2, 32, 2, 3, 3, 8, 8, 2
+    w = _f64_tree(synth.flux_weights(rng, D, H, F, 1, 2, txt_dim=txt_dim, vec_dim=vec_dim, dtype="f32",
+                                     std=0.3, single_parallel=True))
+    z = rng.standard_normal((B, 64, lat_h, lat_w))
+    txt = rng.standard_normal((B, S_t, txt_dim))
+    t = rng.uniform(0.1, 0.9, B)
+    y = rng.standard_normal((B, vec_dim))
+    ids = synth.position_ids(B, lat_h, lat_w, S_t)
+    cos, sin = O.rope_cos_sin(ids, AX)
+    dpred = rng.standard_normal(z.shape)
+
+    def loss():
+        return float(np.sum(O.flux_forward(z, txt, t, y, ids, w, H, axes_dim=AX, single_parallel=True) * dpred))
+
+    ins, gw = BW.model_backward(z, txt, t, y, cos, sin, w, H, dpred, single_parallel=True)
+    for name, T in (("z_t", z), ("txt", txt), ("y", y)):
+        _directional(loss, ins[name], T, rng, n=2)
+    for key in ("time_in", "vector_in"):
+        for T, G in zip(w[key], gw[key]):
+            _directional(loss, G, T, rng, n=1)
+    for i in range(2):
+        for name in ("w_mod", "b_mod", "w_qkv", "g_q", "w_o", "w_1", "b_1", "w_2", "b_o"):
+            _directional(loss, gw["single"][i][name], w["single"][i][name], rng, n=1)

@@ -82,9 +82,11 @@ def test_conditioning_vec_is_the_sum_of_its_terms():
                                atol=1e-14)
 
 
-def _stack(n_double=2, n_single=2, D=32, H=2, F=64, lat=4, S_t=5, B=2, txt_dim=16, vec_dim=12, seed=0):
+def _stack(n_double=2, n_single=2, D=32, H=2, F=64, lat=4, S_t=5, B=2, txt_dim=16, vec_dim=12, seed=0,
+           single_parallel=False):
     rng = np.random.default_rng(seed)
-    w = synth.flux_weights(rng, D, H, F, n_double, n_single, txt_dim, vec_dim, dtype="f32", std=0.2)
+    w = synth.flux_weights(rng, D, H, F, n_double, n_single, txt_dim, vec_dim, dtype="f32", std=0.2,
+                           single_parallel=single_parallel)
     z = rng.standard_normal((B, 64, lat, lat))
     txt = rng.standard_normal((B, S_t, txt_dim))
     t = rng.uniform(size=B)
@@ -169,11 +171,35 @@ def test_parameter_counts_against_the_model_variants_table():
     D, H, F = 64, 2, 256
     w = synth.flux_weights(rng, D, H, F, 2, 3, txt_dim=48, vec_dim=24, time_dim=16, channels=8, dtype="f32")
     assert _tree_params(w) == _count(D, F, D // H, 2, 3, False, 48, 24, 16, 8)
-    for s in w["single"]:
-        s["w_mod"], s["b_mod"] = s["w_mod"][:3 * D], s["b_mod"][:3 * D]
+    w = synth.flux_weights(rng, D, H, F, 2, 3, txt_dim=48, vec_dim=24, time_dim=16, channels=8, dtype="f32",
+                           single_parallel=True)
     assert _tree_params(w) == _count(D, F, D // H, 2, 3, True, 48, 24, 16, 8)
     D, F, d = 3072, 12288, 128
     par535, par12 = _count(D, F, d, 1, 1, True), _count(D, F, d, 19, 38, True)
     seq535, seq12 = _count(D, F, d, 1, 1, False), _count(D, F, d, 19, 38, False)
     assert abs(par535 / 535e6 - 1) < 0.005 and abs(par12 / 12e9 - 1) < 0.015   # 535.3 M, 11.89 B
     assert seq535 / 535e6 > 1.04 and seq12 / 12e9 > 1.07                      # 563.6 M, 12.97 B
+
+
+def test_parallel_stack_with_zero_gates_and_its_wiring():
+    # single blocks of the parallel form: zero gates everywhere give the head of the embedded
+    # latents; with the gates on, one double and one parallel single block equal that chain
+    # written out (the single block over [img; txt], the head on the image rows)
+    w, z, txt, t, y, ids, H = _stack(seed=11, single_parallel=True)
+    w0 = dict(w)
+    w0["double"] = [(_zero_gates(a), _zero_gates(b)) for a, b in w["double"]]
+    w0["single"] = [_zero_gates(s, (2,)) for s in w["single"]]
+    vec = O.conditioning_vec(t, y, w)
+    f = w["final"]
+    exp = O.final_layer(O.img_in(z, *w["img_in"]), vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], 4, 4)
+    np.testing.assert_allclose(O.flux_forward(z, txt, t, y, ids, w0, H, axes_dim=AX, single_parallel=True), exp,
+                               atol=1e-13)
+    w1 = dict(w, double=w["double"][:1], single=w["single"][:1])
+    cos, sin = O.rope_cos_sin(ids, AX)
+    xi, xt = O.double_block(O.img_in(z, *w["img_in"]), O.txt_in(txt, *w["txt_in"]), vec, cos, sin,
+                            *w["double"][0], H)
+    c = O.single_block_parallel(np.concatenate([xi, xt], axis=1), vec, cos, sin, w["single"][0], H)
+    chain = O.final_layer(c[:, :16], vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], 4, 4)
+    got = O.flux_forward(z, txt, t, y, ids, w1, H, axes_dim=AX, single_parallel=True)
+    np.testing.assert_allclose(got, chain, atol=1e-12)
+    assert np.abs(got - exp).max() > 1e-3
