@@ -92,6 +92,11 @@ MUTATIONS = [
     ("backward.py", "the whole-model backward's parallel single forward drops its MLP branch",
      'branch = linear_fwd(_merge(o), w["w_o"], w["b_o"]) + linear_fwd(u, w["w_2"], w["b_2"])\n    return',
      'branch = linear_fwd(_merge(o), w["w_o"], w["b_o"])\n    return'),
+    ("fp8_attention.py", "FP8 attention without the division by the row sum",
+     "return o / pt.sum(axis=-1, keepdims=True)", "return o"),
+    ("fp8_attention.py", "FP8 attention casts the probabilities at scale 1",
+     "def fp8_attention(q, k, v, s_q: float, s_k: float, s_v: float, s_p: float = E4M3_MAX):",
+     "def fp8_attention(q, k, v, s_q: float, s_k: float, s_v: float, s_p: float = 1.0):"),
     ("backward.py", "RoPE backward rotates the same way",
      "return rope_rotate(dy, cos, -_f(sin), interleaved)", "return rope_rotate(dy, cos, _f(sin), interleaved)"),
     ("backward.py", "softmax backward without the row-sum term",
