@@ -56,7 +56,7 @@ typedef enum mmdit_status {
   MMDIT_ERR_UNSUPPORTED = 2,
   MMDIT_ERR_WORKSPACE = 3,
   MMDIT_ERR_CUDA = 4,
-  MMDIT_ERR_NONFINITE = 5,
+  MMDIT_ERR_NONFINITE = 5, /* reserved for a non-finite check of the outputs; no entry point returns it */
   MMDIT_ERR_DEVICE = 6 /* a kernel's bounded wait gave up; see mmdit_workspace_status */
 } mmdit_status;
 
