@@ -181,10 +181,16 @@ def _check(status: int):
 
 
 def _ptr(t) -> int | None:
+    """Device address of a CUDA tensor (ints pass through).  Every tensor argument of the library is
+    device memory (host-side arguments are ctypes structs and arrays), so a tensor on another device
+    is refused here rather than handed to a kernel."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if t.device.type != "cuda":
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}: the library reads and writes "
+                         "device memory")
     return t.data_ptr()
 
 

@@ -247,3 +247,11 @@ def test_linear_bwd_embedding_head_and_modulation_validation(lib):
     assert lib.mmdit_modulation_fwd(1, -1, 6 * 3072, 3072, 16, 16, 16, 16, None) == 1
     assert lib.mmdit_modulation_fwd(1, 1, 6 * 3072, 3072, None, 16, 16, 16, None) == 1
     assert lib.mmdit_modulation_fwd(1, 0, 6 * 3072, 3072, None, None, None, None, None) == 0
+
+
+def test_binding_refuses_host_tensors():
+    # a host tensor's address would reach a kernel as if it were device memory
+    import torch
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        L._ptr(torch.zeros(8))
+    assert L._ptr(None) is None and L._ptr(0x1000) == 0x1000
