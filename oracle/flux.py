@@ -512,7 +512,7 @@ def flux_forward(z_t, txt, t, y, ids, w, heads, g=None, interleaved=True, gelu_t
     step to the next (vec, the embedded tokens, each block's outputs), the values an
     implementation that stores them in the activation type holds.  ``single_parallel``: the single
     blocks are the parallel-branch form (``single_block_parallel``), the form whose parameter
-    count matches the architecture page's variant table.
+    count matches the API reference's parameter-count table.
     """
     keep = store if store is not None else _f64
     single = single_block_parallel if single_parallel else single_block

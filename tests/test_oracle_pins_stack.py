@@ -12,7 +12,9 @@ Each pin fixes a fact independently of the oracle's code:
   zero no image row can see the text, so the prediction ignores the text (this fails if the
   head reads the wrong rows or the concatenation order is wrong).
 """
+import json
 import math
+import os
 
 import numpy as np
 
@@ -161,7 +163,7 @@ def _count(D, F, d, n_double, n_single, parallel, txt_dim=4096, vec_dim=768, tim
 
 
 def test_parameter_counts_against_the_model_variants_table():
-    # The architecture page's parameter table prints ~535 million for 1 double + 1 single block
+    # The API reference's parameter-count table prints ~535 million for 1 double + 1 single block
     # and ~12 billion for 19 + 38 (hidden 3072, MLP 12288).  The shape formula is first checked
     # against real weight trees at a small size, then evaluated at those sizes: the blocks as
     # built land within 0.5% and 1% of the printed counts with the parallel-branch single block, while
@@ -174,11 +176,17 @@ def test_parameter_counts_against_the_model_variants_table():
     w = synth.flux_weights(rng, D, H, F, 2, 3, txt_dim=48, vec_dim=24, time_dim=16, channels=8, dtype="f32",
                            single_parallel=True)
     assert _tree_params(w) == _count(D, F, D // H, 2, 3, True, 48, 24, 16, 8)
-    D, F, d = 3072, 12288, 128
-    par535, par12 = _count(D, F, d, 1, 1, True), _count(D, F, d, 19, 38, True)
-    seq535, seq12 = _count(D, F, d, 1, 1, False), _count(D, F, d, 19, 38, False)
-    assert abs(par535 / 535e6 - 1) < 0.005 and abs(par12 / 12e9 - 1) < 0.015   # 535.3 M, 11.89 B
-    assert seq535 / 535e6 > 1.04 and seq12 / 12e9 > 1.07                      # 563.6 M, 12.97 B
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "parameter_counts.json")))
+    D, F = gold["hidden"], gold["mlp_hidden"]
+    d = D // gold["heads"]
+    (small, large) = gold["variants"]
+    par535 = _count(D, F, d, small["joint_layers"], small["single_layers"], True)
+    par12 = _count(D, F, d, large["joint_layers"], large["single_layers"], True)
+    seq535 = _count(D, F, d, small["joint_layers"], small["single_layers"], False)
+    seq12 = _count(D, F, d, large["joint_layers"], large["single_layers"], False)
+    # parallel: 535.3 M and 11.89 B; sequential: 563.6 M and 12.97 B
+    assert abs(par535 / small["total_params"] - 1) < 0.005 and abs(par12 / large["total_params"] - 1) < 0.015
+    assert seq535 / small["total_params"] > 1.04 and seq12 / large["total_params"] > 1.07
 
 
 def test_parallel_stack_with_zero_gates_and_its_wiring():
