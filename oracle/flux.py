@@ -29,7 +29,9 @@ design notes of the repository as well):
     value settles (parity unpinned for that choice only).
   * Attention scale is 1/sqrt(head_dim), no mask.
   * The single block runs attention then MLP in sequence with six modulation
-    chunks, over the whole concatenated sequence, and returns every row.
+    chunks, over the whole concatenated sequence, and returns every row.  The
+    parallel-branch form (``single_block_parallel``) is the one the API page's
+    parameter-count table fits; ``flux_forward(..., single_parallel=True)`` uses it.
   * The output head takes (shift, scale) from a SiLU + linear of ``vec``.
   * Loss is the mean over all elements.
   * Conditioning: the timestep enters as tau = 1000 t (the TimeStepEmbedder's input range),
