@@ -5,11 +5,14 @@ One step is one pass of the whole hot path on the 535M-shaped Flux workload (hid
 24 heads x 128, MLP 12288, 4096 image tokens from 64x64x64 latents + 512 text tokens from a
 [1, 512, 4096] text embedding, batch 1):
 
-    rope3d_freqs -> flow-matching noise z_t -> img_in -> txt_in -> double block
-    -> single block -> output head -> flow-matching loss
+    rope3d_freqs -> img_in of z_t (the flow-matching noise formed while patchifying) -> txt_in
+    -> double block -> single block -> output head with the flow-matching loss fused on
 
 all through the C ABI of libmmdit.so, with inputs resident in HBM when the timed region
-starts (``value``) or copied from pinned host memory inside it (``e2e``).  The blocks' AdaLN
+starts (``value``) or copied from pinned host memory inside it (``e2e``).  Other workloads:
+the same step at batch 2 with 4096 + 512 tokens (the metric's second point), the double block
+at batch 4 with 1024 + 512 tokens, the blocks at 16384 + 512 tokens with E4M3 linears, and the
+whole Flux 12B forward.  The blocks' AdaLN
 modulations (mmdit_modulation_fwd) run on a second stream, overlapped with the embeddings and
 the double block, and are joined before each block needs them.  The metric is the
 dense-contraction throughput of the two blocks (2 * B * S * D * (3D + D + 2F) + 4 * B * S^2 *
@@ -38,6 +41,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MMDiT block fwd TFLOP/s & % of GB300 bf16 tensor peak at 4096+512 tokens"
 WORKLOAD = "flux535m_bf16"
+C3_WORKLOAD = "flux12b_512px_bf16"
+C4_WORKLOAD = "flux12b_1024px_bf16"
 FP8_WORKLOAD = "flux12b_2048px_fp8"
 MODEL_WORKLOAD = "flux12b_512px_model"
 AXES = (16, 56, 56)
@@ -57,8 +62,12 @@ def parse_args():
                     help="time plain per-call launches instead of a CUDA-graph replay of the step")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="minimum CPU time of the oracle baseline sample")
-    ap.add_argument("--workload", choices=[WORKLOAD, FP8_WORKLOAD, MODEL_WORKLOAD], default=WORKLOAD,
-                    help=f"{WORKLOAD}: the hot-path step above (the headline); {FP8_WORKLOAD}: the "
+    ap.add_argument("--workload", choices=[WORKLOAD, C3_WORKLOAD, C4_WORKLOAD, FP8_WORKLOAD, MODEL_WORKLOAD],
+                    default=WORKLOAD,
+                    help=f"{WORKLOAD}: the hot-path step above (the headline); {C4_WORKLOAD}: the same "
+                         "step at batch 2 with N(0, 1) text tokens of width D and logit-normal t (the "
+                         f"metric's second point); {C3_WORKLOAD}: the double block alone at batch 4, "
+                         f"1024 + 512 tokens, with the noise, output head and loss; {FP8_WORKLOAD}: the "
                          "double + single block at 16384 + 512 tokens with E4M3 linears; "
                          f"{MODEL_WORKLOAD}: the whole Flux 12B forward (19 double + 38 single "
                          "blocks) at 1024 + 512 tokens through mmdit_flux_forward")
@@ -103,7 +112,9 @@ def block_flops(B, S, D, F, H, d=128):
 
 
 class HostWorkload:
-    """Seeded host-side inputs and weights (float32 arrays holding bf16-rounded values)."""
+    """Seeded host-side inputs and weights (float32 arrays holding bf16-rounded values).  The text
+    tokens are a [B, S_t, 4096] embedding fed through txt_in where the workload names that source,
+    else N(0, 1) at width D (the block input itself)."""
 
     def __init__(self, wl):
         from diffusion_transformer_flux_gb300 import synth
@@ -113,14 +124,16 @@ class HostWorkload:
         rng_w = np.random.Generator(np.random.PCG64(2000 + wl.index))
         self.z0, self.z1 = synth.latent_pair(rng_in, B, wl.channels, wl.lat_h, wl.lat_w)
         self.t = synth.timesteps(rng_in, B, wl.t_dist)
-        self.txt = synth.bf16_round(rng_in.standard_normal((B, wl.seq_txt, wl.ctx_dim), dtype=np.float32))
+        txt_w = wl.ctx_dim if wl.txt_from_ctx else D
+        self.txt = synth.bf16_round(rng_in.standard_normal((B, wl.seq_txt, txt_w), dtype=np.float32))
         self.vec = synth.bf16_round(rng_in.standard_normal((B, D), dtype=np.float32))
         self.ids = synth.position_ids(B, wl.lat_h, wl.lat_w, wl.seq_txt)
         self.img_in = synth.embed_weights(rng_w, wl.channels, D, "bf16")
-        self.txt_in = synth.embed_weights(rng_w, wl.ctx_dim, D, "bf16")
+        self.txt_in = synth.embed_weights(rng_w, wl.ctx_dim, D, "bf16") if wl.txt_from_ctx else None
         self.w_dimg = synth.stream_weights(rng_w, D, H, 128, F, "bf16")
         self.w_dtxt = synth.stream_weights(rng_w, D, H, 128, F, "bf16")
-        self.w_single = synth.stream_weights(rng_w, D, H, 128, F, "bf16")
+        self.has_single = "single" in wl.blocks
+        self.w_single = synth.stream_weights(rng_w, D, H, 128, F, "bf16") if self.has_single else None
         self.final = synth.final_layer_weights(rng_w, D, wl.channels, "bf16")
 
 
@@ -161,14 +174,13 @@ class SideModulation:
 class DeviceStep:
     """Device buffers, weights and workspaces of one replica, and the step itself."""
 
-    def __init__(self, hw: HostWorkload, device):
+    def __init__(self, hw: HostWorkload, device, keep_pred=False):
         import torch
         from diffusion_transformer_flux_gb300 import _lib as L
         self.L, self.torch = L, torch
         wl = hw.wl
         self.wl = wl
         B, D, H, F, S_i, S_t = wl.batch, wl.hidden, wl.heads, wl.mlp_hidden, wl.seq_img, wl.seq_txt
-        assert B == 1, "the concatenated-sequence views below assume batch 1"
         S = S_i + S_t
         bf = torch.bfloat16
 
@@ -182,62 +194,101 @@ class DeviceStep:
         self.t = dev(hw.t, torch.float32)
         self.txt, self.vec = dev(hw.txt), dev(hw.vec)
         self.ids = dev(hw.ids, torch.float32)
-        self.img_in, self.txt_in = devw(hw.img_in), devw(hw.txt_in)
-        self.w_dimg, self.w_dtxt, self.w_single = devw(hw.w_dimg), devw(hw.w_dtxt), devw(hw.w_single)
+        self.img_in = devw(hw.img_in)
+        self.txt_in = devw(hw.txt_in) if hw.txt_in is not None else None
+        self.w_dimg, self.w_dtxt = devw(hw.w_dimg), devw(hw.w_dtxt)
+        self.w_single = devw(hw.w_single) if hw.has_single else None
         self.final = devw(hw.final)
-        self.sw_dimg, self.sw_dtxt = L.make_stream_w(self.w_dimg), L.make_stream_w(self.w_dtxt)
-        self.sw_single = L.make_stream_w(self.w_single)
         self.cos = torch.empty(B, S, 64, device=device)
         self.sin = torch.empty_like(self.cos)
-        self.zt = torch.empty_like(self.z0)
-        self.X = torch.empty(B, S, D, device=device, dtype=bf)   # embeddings [img; txt]
-        self.Y = torch.empty_like(self.X)                        # double-block output
-        self.Z = torch.empty_like(self.X)                        # single-block output
-        self.pred = torch.empty_like(self.z0)
+        # Activations.  Batch 1: [img; txt] is one contiguous buffer per stage, so the double block's
+        # streams are views of it and the single block reads it directly.  Batch > 1: the streams are
+        # separate [B, S_s, D] buffers, joined into [B, S, D] (and the image rows taken back out) by
+        # strided copies on the copy engine (mmdit_copy_rows).
+        self.joint = B == 1
+        if self.joint:
+            self.X = torch.empty(B, S, D, device=device, dtype=bf)   # embeddings [img; txt]
+            self.Y = torch.empty_like(self.X)                        # double-block output
+            self.Z = torch.empty_like(self.X)                        # single-block output
+            self.x_img, self.x_txt = self.X[:, :S_i], self.X[:, S_i:]
+            self.y_img, self.y_txt = self.Y[:, :S_i], self.Y[:, S_i:]
+        else:
+            self.x_img = torch.empty(B, S_i, D, device=device, dtype=bf)
+            self.x_txt = torch.empty(B, S_t, D, device=device, dtype=bf)
+            self.y_img, self.y_txt = torch.empty_like(self.x_img), torch.empty_like(self.x_txt)
+            self.C = torch.empty(B, S, D, device=device, dtype=bf) if hw.has_single else None
+        if not wl.txt_from_ctx:
+            self.x_txt = self.txt  # the text tokens are the block input itself
+            if self.joint:
+                raise ValueError("batch-1 workloads take their text through txt_in")
         self.loss = torch.zeros(1, device=device)
+        # the prediction is written only when asked for (the step's result is the loss)
+        self.pred = torch.empty_like(self.z0) if keep_pred else None
         self.dims = L.make_dims(B, S_i, S_t, D, H, F, L.MMDIT_BF16)
         self.dims_final = L.make_dims(B, S_i, 0, D, H, F, L.MMDIT_BF16)
         ws_block = max(L.mmdit_double_block_workspace_size(self.dims),
                        L.mmdit_single_block_workspace_size(self.dims))
         self.ws_block = L.workspace(ws_block, device)
-        self.ws_flow = L.workspace(L.flow_match_workspace_size(B, self.z0[0].numel()), device)
-        self.ws_lin = L.workspace(L.mmdit_linear_workspace_size(L.MMDIT_BF16, B * S_t, D, wl.ctx_dim), device)
+        self.ws_lin = (L.workspace(L.mmdit_linear_workspace_size(L.MMDIT_BF16, B * S_t, D, wl.ctx_dim), device)
+                       if self.txt_in is not None else None)
         self.ws_img = L.workspace(L.mmdit_img_in_workspace_size(L.MMDIT_BF16, B, wl.channels, wl.lat_h,
                                                                 wl.lat_w), device)
-        self.ws_final = L.workspace(L.mmdit_final_layer_workspace_size(self.dims_final, wl.channels), device)
-        self.S, self.S_i = S, S_i
-        self.side = SideModulation(torch, L, self.vec, [("dimg", self.w_dimg), ("dtxt", self.w_dtxt),
-                                                        ("single", self.w_single)], device)
-        self.flops_blocks = 2 * block_flops(B, S, D, F, H)
+        self.ws_final = L.workspace(L.mmdit_final_layer_loss_workspace_size(self.dims_final, wl.channels), device)
+        self.S, self.S_i, self.B, self.D = S, S_i, B, D
+        sets = [("dimg", self.w_dimg), ("dtxt", self.w_dtxt)]
+        if hw.has_single:
+            sets.append(("single", self.w_single))
+        self.side = SideModulation(torch, L, self.vec, sets, device)
+        n_blocks = 2 if hw.has_single else 1
+        self.flops_blocks = n_blocks * block_flops(B, S, D, F, H)
         self.flops_dense = (self.flops_blocks + 2 * B * S_i * wl.channels * D
-                            + 2 * B * S_t * wl.ctx_dim * D + 2 * B * S_i * D * wl.channels)
+                            + (2 * B * S_t * wl.ctx_dim * D if wl.txt_from_ctx else 0)
+                            + 2 * B * S_i * D * wl.channels)
+
+    def _rows(self, dst, src, rows_per_sample, dst_off=0, src_off=0):
+        """Copy rows_per_sample token rows of each sample between [B, ., D] bf16 buffers."""
+        e = 2 * self.D
+        self.L.mmdit_copy_rows(dst.data_ptr() + dst_off * e, dst.shape[1] * e, src.data_ptr() + src_off * e,
+                               src.shape[1] * e, rows_per_sample * e, self.B)
 
     def step(self):
         """One pass of the hot path; every computation runs in libmmdit.so kernels."""
         L, wl, side = self.L, self.wl, self.side
         S_i = self.S_i
-        side.fork()  # the three block modulations, on the side stream
+        side.fork()  # the block modulations, on the side stream
         L.rope3d_freqs(self.ids, AXES, THETA, self.cos, self.sin)
-        L.flow_match_noise_and_loss(self.z0, self.z1, self.t, z_t=self.zt, ws=self.ws_flow)
-        L.mmdit_img_in_fwd(self.zt, self.img_in["w"], self.img_in["b"], self.X[:, :S_i], ws=self.ws_img)
-        L.mmdit_linear_fwd(self.txt, self.txt_in["w"], self.txt_in["b"], self.X[:, S_i:], ws=self.ws_lin)
+        # z_t = (1 - t) z0 + t z1 formed while patchifying, then projected
+        L.mmdit_img_in_noise_fwd(self.z0, self.z1, self.t, self.img_in["w"], self.img_in["b"], self.x_img,
+                                 ws=self.ws_img)
+        if self.txt_in is not None:
+            L.mmdit_linear_fwd(self.txt, self.txt_in["w"], self.txt_in["b"], self.x_txt, ws=self.ws_lin)
         side.join("dimg", "dtxt")
         L.mmdit_double_block_fwd(self.dims, side.weights("dimg", self.w_dimg), side.weights("dtxt", self.w_dtxt),
-                                 self.vec, self.cos, self.sin, self.X[:, :S_i], self.X[:, S_i:],
-                                 self.Y[:, :S_i], self.Y[:, S_i:], ws=self.ws_block)
-        side.join("single")
-        L.mmdit_single_block_fwd(self.dims, side.weights("single", self.w_single), self.vec, self.cos,
-                                 self.sin, self.Y, self.Z, ws=self.ws_block)
-        L.mmdit_final_layer_fwd(self.dims_final, wl.lat_h, wl.lat_w, self.Z[:, :S_i], self.vec,
-                                self.final["w_ada"], self.final["b_ada"], self.final["w_out"],
-                                self.final["b_out"], self.pred, ws=self.ws_final)
-        L.flow_match_noise_and_loss(self.z0, self.z1, self.t, pred=self.pred, loss=self.loss,
-                                    ws=self.ws_flow)
+                                 self.vec, self.cos, self.sin, self.x_img, self.x_txt,
+                                 self.y_img, self.y_txt, ws=self.ws_block)
+        head_in = self.y_img
+        if self.w_single is not None:
+            side.join("single")
+            if self.joint:
+                L.mmdit_single_block_fwd(self.dims, side.weights("single", self.w_single), self.vec, self.cos,
+                                         self.sin, self.Y, self.Z, ws=self.ws_block)
+                head_in = self.Z[:, :S_i]
+            else:
+                self._rows(self.C, self.y_img, S_i)
+                self._rows(self.C, self.y_txt, self.S - S_i, dst_off=S_i)
+                L.mmdit_single_block_fwd(self.dims, side.weights("single", self.w_single), self.vec, self.cos,
+                                         self.sin, self.C, self.C, ws=self.ws_block)
+                self._rows(self.y_img, self.C, S_i)
+        # output head with the flow-matching loss fused onto its last kernel
+        L.mmdit_final_layer_loss_fwd(self.dims_final, wl.lat_h, wl.lat_w, head_in, self.vec,
+                                     self.final["w_ada"], self.final["b_ada"], self.final["w_out"],
+                                     self.final["b_out"], self.z0, self.z1, self.loss, pred=self.pred,
+                                     ws=self.ws_final)
 
     input_names = ("z0", "z1", "t", "txt", "vec", "ids")
 
     def workspaces(self):
-        return (self.ws_block, self.ws_flow, self.ws_lin, self.ws_img, self.ws_final)
+        return tuple(w for w in (self.ws_block, self.ws_lin, self.ws_img, self.ws_final) if w is not None)
 
     def result(self):
         """The step's result read back by the end-to-end leg (the loss)."""
@@ -510,11 +561,11 @@ def kernel_work(label: str, wl):
         return "hbm", B * S * 3 * 4 + 2.0 * B * S * 64 * 4, "B"
     if label in ("flow_match.noise", "flow_match.loss"):
         return "hbm", 3.0 * n_lat * 4, "B"
-    if label == "img_in":
+    if label in ("img_in", "img_in_noise"):  # (the noised variant forms z_t while patchifying)
         return "tensor", 2.0 * B * S_i * wl.channels * D, "FLOP"
     if label == "linear":
         return "tensor", 2.0 * B * S_t * wl.ctx_dim * D, "FLOP"
-    if label == "final_layer":
+    if label in ("final_layer", "final_layer_loss"):  # (the loss variant adds the fused MSE)
         return "tensor", 2.0 * B * S_i * D * wl.channels, "FLOP"
     return "unknown", 0.0, ""
 
@@ -557,14 +608,37 @@ def oracle_sample(hw: HostWorkload, n_img_rows: int, n_txt_rows: int, seed: int)
     rt = rng.choice(S_t, n_txt_rows, replace=False)
     zt = O.flow_match_noise(hw.z0, hw.z1, hw.t)
     x_img = O.img_in(zt, hw.img_in["w"], hw.img_in["b"])
-    x_txt = O.txt_in(hw.txt, hw.txt_in["w"], hw.txt_in["b"])
+    x_txt = O.txt_in(hw.txt, hw.txt_in["w"], hw.txt_in["b"]) if hw.txt_in is not None else hw.txt
     cos, sin = O.rope_cos_sin(hw.ids)
     O.double_block_rows(x_img, x_txt, hw.vec, cos, sin, hw.w_dimg, hw.w_dtxt, H, ri, rt)
     nr = B * (n_img_rows + n_txt_rows)
-    return (2.0 * B * S_i * wl.channels * D + 2.0 * B * S_t * wl.ctx_dim * D
+    return (2.0 * B * S_i * wl.channels * D + (2.0 * B * S_t * wl.ctx_dim * D if hw.txt_in is not None else 0.0)
             + 2 * 2.0 * B * D * 6 * D                       # two modulation linears
             + 2.0 * B * S * D * 3 * D + 2.0 * nr * D * 3 * D  # K/V for all tokens, Q for the rows
             + 4.0 * nr * S * 128 * H + 2.0 * nr * D * D + 4.0 * nr * D * F)
+
+
+def oracle_full_step(hw: HostWorkload):
+    """The whole step computed by the fp64 oracle (no rounding anywhere): noise, img_in, the text
+    tokens (txt_in where the workload has it), the double block, the single block where the
+    workload has one, the output head and the flow-matching loss.  Returns (the blocks' dense
+    floating-point operations, the loss)."""
+    from oracle import flux as O
+    wl = hw.wl
+    B, D, H, F, S_i, S_t = wl.batch, wl.hidden, wl.heads, wl.mlp_hidden, wl.seq_img, wl.seq_txt
+    zt = O.flow_match_noise(hw.z0, hw.z1, hw.t)
+    x_img = O.img_in(zt, hw.img_in["w"], hw.img_in["b"])
+    x_txt = O.txt_in(hw.txt, hw.txt_in["w"], hw.txt_in["b"]) if hw.txt_in is not None else hw.txt
+    cos, sin = O.rope_cos_sin(hw.ids)
+    y_img, y_txt = O.double_block(x_img, x_txt, hw.vec, cos, sin, hw.w_dimg, hw.w_dtxt, H)
+    n_blocks = 1
+    if hw.has_single:
+        c = O.single_block(np.concatenate([y_img, y_txt], axis=1), hw.vec, cos, sin, hw.w_single, H)
+        y_img = c[:, :S_i]
+        n_blocks = 2
+    f = hw.final
+    pred = O.final_layer(y_img, hw.vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], wl.lat_h, wl.lat_w)
+    return n_blocks * block_flops(B, S_i + S_t, D, F, H), O.flow_match_loss(pred, hw.z0, hw.z1)
 
 
 def cpu_cores():
@@ -593,6 +667,82 @@ def measure_euler_step(L, torch, device, hbm_peak, n=1 << 26, reps=10):
     del z, vc, vu, out
     return {"kernel": "flow_match.euler_step", "n": n, "dtype": "f32", "bytes_per_call": 16 * n,
             "avg_us": round(us, 2), "achieved_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4)}
+
+
+def _time_calls(torch, fn, reps):
+    """Average microseconds of fn over `reps` calls after one warm-up (CUDA events)."""
+    fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps
+
+
+def measure_fp8_peak(torch, device, n=8192, reps=10):
+    """Dense E4M3 tensor throughput of this GPU: torch._scaled_mm (cuBLASLt) on n^3 E4M3 operands
+    with bf16 output, best of `reps` single calls timed with CUDA events (the bf16 peak's
+    protocol).  None if the call is not available."""
+    try:
+        a = torch.randn(n, n, device=device).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=device).to(torch.float8_e4m3fn)
+        one = torch.ones((), device=device)
+        bt = b.t()  # column-major second operand, as the call wants
+
+        def mm():
+            return torch._scaled_mm(a, bt, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        mm()
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            mm()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        del a, b
+        return {"tflops": round(2.0 * n ** 3 / (best * 1e-3) / 1e12, 1), "n": n,
+                "how": f"torch._scaled_mm E4M3 {n}^3, bf16 out, best of {reps} (CUDA events)"}
+    except Exception as exc:  # noqa: BLE001 - any failure leaves the nominal ratio in place
+        return {"tflops": None, "error": f"{type(exc).__name__}: {exc}"[:200]}
+
+
+def measure_hbm_sweeps(L, torch, device, hbm_peak, reps=10):
+    """The element-wise passes at inputs far larger than L2 (>= 256 MB per operand), against the HBM
+    peak: the flow-matching noise (z0, z1 read; z_t written) and loss (z0, z1, pred read) over
+    2^26 fp32 elements, and LayerNorm-modulate over 65536 x 4096 bf16 rows (x read, out written)
+    and over 32768 x 4096 fp32 rows (the blocks' fp32 residual) to bf16."""
+    out = []
+    n = 1 << 26
+    z0, z1 = torch.randn(n, device=device), torch.randn(n, device=device)
+    t = torch.rand(1, device=device)
+    zt, pred, loss = torch.empty_like(z0), torch.randn(n, device=device), torch.zeros(1, device=device)
+    ws = L.workspace(L.flow_match_workspace_size(1, n), device)
+    for label, kw, nbytes in (("flow_match.noise", dict(z_t=zt), 12 * n),
+                              ("flow_match.loss", dict(pred=pred, loss=loss), 12 * n)):
+        us = _time_calls(torch, lambda: L.flow_match_noise_and_loss(z0.view(1, n), z1.view(1, n), t, ws=ws, **kw),
+                         reps)
+        gbs = nbytes / us / 1e3
+        out.append({"kernel": label, "bytes_per_call": nbytes, "avg_us": round(us, 2),
+                    "achieved_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4)})
+    del z0, z1, zt, pred
+    D = 4096
+    mod = torch.randn(1, 6 * D, device=device) * 0.1
+    for rows, xdt, label in ((65536, torch.bfloat16, "ln_modulate bf16 -> bf16"),
+                             (32768, torch.float32, "ln_modulate fp32 -> bf16")):
+        x = torch.randn(1, rows, D, device=device).to(xdt)
+        y = torch.empty(1, rows, D, device=device, dtype=torch.bfloat16)
+        nbytes = rows * D * (x.element_size() + 2)
+        us = _time_calls(torch, lambda: L.mmdit_ln_modulate_fwd(x, mod[:, :D], mod[:, D:2 * D], y, 6 * D), reps)
+        gbs = nbytes / us / 1e3
+        out.append({"kernel": label, "rows": rows, "dim": D, "bytes_per_call": nbytes, "avg_us": round(us, 2),
+                    "achieved_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / hbm_peak, 4)})
+        del x, y
+    return out
 
 
 def measure_parallel_block(st, L, torch, peak, reps=10):
@@ -640,6 +790,19 @@ def measure_linear_bwd(L, torch, device, peak, M=4608, N=12288, K=3072, reps=5):
     flops = 4.0 * M * N * K
     return {"op": "linear backward (dx, dW, db)", "M": M, "N": N, "K": K, "avg_us": round(us, 2),
             "achieved_tflops": round(flops / us / 1e6, 1), "frac": round(flops / us / 1e6 / peak, 4)}
+
+
+def run_cpu_baseline_full(hw: HostWorkload):
+    """One full step of the fp64 oracle, timed; its loss checks the GPU's."""
+    t0 = time.perf_counter()
+    flops, loss = oracle_full_step(hw)
+    dt = time.perf_counter() - t0
+    blocks = "double and single blocks" if hw.has_single else "double block"
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": (f"1 x the whole step in the fp64 oracle at full size ({wl_desc(hw.wl)}, batch "
+                       f"{hw.wl.batch}): noise, img_in, text tokens, the full {blocks}, output head, "
+                       "loss; the value counts the blocks' dense FLOPs over the step's time"),
+            "seconds": round(dt, 2)}, loss
 
 
 def run_cpu_baseline(hw: HostWorkload, min_seconds: float, rows=(32, 8)):
@@ -776,6 +939,9 @@ def main():
     clocks = clk.summary()
     if not bool(torch.isfinite(st.result()).all()):
         raise RuntimeError("non-finite result")
+    for ws in st.workspaces():
+        if L.mmdit_workspace_status(ws) != 0:
+            raise RuntimeError("a kernel gave up a bounded wait in the timed steps")
     total_s = max_over_ranks(dist, sum(ms) / 1e3, device)
     value = whole_job_tflops(st.flops_blocks, args.steps, world, total_s)
 
@@ -805,8 +971,11 @@ def main():
     prof_total = sum(v[1] for v in agg.values()) or 1.0
     bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    # E4M3 contractions: the measured bf16 peak times the nominal dense fp8 : bf16 ratio (2)
-    fp8_peak = 2.0 * bf16_peak
+    # E4M3 contractions: this GPU's measured E4M3 GEMM throughput where it could be taken, else
+    # the measured bf16 peak times the nominal dense fp8 : bf16 ratio (2)
+    fp8_meas = measure_fp8_peak(torch, device) if fp8 else None
+    fp8_measured = bool(fp8_meas and fp8_meas.get("tflops"))
+    fp8_peak = float(fp8_meas["tflops"]) if fp8_measured else 2.0 * bf16_peak
 
     def peak_of(name):
         is_linear = name.split(".")[-1] in ("qkv", "out", "fc1", "fc2")
@@ -837,19 +1006,30 @@ def main():
                 "algorithmic_per_launch": amount, "algorithmic_unit": unit,
                 "peak_source": f"{peak_src}: {'bf16_tflops (burst)' if bound == 'tensor' else 'hbm_gbs'}"}
     if peak != bf16_peak and bound == "tensor":
-        roofline["peak_source"] += " x 2 (nominal dense fp8 : bf16 ratio)"
+        roofline["peak_source"] = ("measured in this run: torch._scaled_mm E4M3 8192^3 (burst)" if fp8_measured
+                                   else roofline["peak_source"] + " x 2 (nominal dense fp8 : bf16 ratio)")
     if bound == "tensor" and "bf16_tflops_sustained" in peaks and peak == bf16_peak:
         roofline["frac_of_sustained"] = round(ach / float(peaks["bf16_tflops_sustained"]), 4)
 
     extras = {}
-    if not fp8 and not model:
+    if args.workload == WORKLOAD:
         extras["sampling_step"] = measure_euler_step(L, torch, device, hbm_peak)
+        extras["hbm_sweeps"] = measure_hbm_sweeps(L, torch, device, hbm_peak)
         extras["single_block_parallel"] = measure_parallel_block(st, L, torch, bf16_peak)
         extras["linear_backward"] = measure_linear_bwd(L, torch, device, bf16_peak)
+    if fp8:
+        extras["fp8_peak"] = fp8_meas
 
-    cpu = None
+    cpu, loss_check = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and hw is not None:
-        cpu = run_cpu_baseline(hw, args.cpu_seconds)
+        if args.workload in (WORKLOAD, C3_WORKLOAD):
+            # the whole step in the fp64 oracle, once: the CPU baseline, and the reference loss
+            cpu, ref_loss = run_cpu_baseline_full(hw)
+            gpu_loss = float(st.loss.item())
+            loss_check = {"gpu": gpu_loss, "oracle_fp64": ref_loss,
+                          "rel_err": abs(gpu_loss - ref_loss) / abs(ref_loss)}
+        else:
+            cpu = run_cpu_baseline(hw, args.cpu_seconds)
 
     if rank == 0:
         S = wl.seq
@@ -873,15 +1053,19 @@ def main():
                                 "every block's modulation in one launch, img_in, txt_in, "
                                 f"{wl.n_double} double + {wl.n_single} single blocks, output head), "
                                 "flow-matching loss") if model else
-                               ("rope3d_freqs, flow-matching noise, img_in, txt_in, double block, "
-                                "single block, output head, flow-matching loss"),
+                               ("rope3d_freqs, img_in of z_t (noise fused into the patchify), "
+                                + ("txt_in, " if wl.txt_from_ctx else "")
+                                + ("double block, single block, " if "single" in wl.blocks else "double block, ")
+                                + "output head with the flow-matching loss fused on"
+                                + ("" if wl.batch == 1 else "; streams joined and split by strided "
+                                   "copy-engine copies (mmdit_copy_rows)")),
                        "streams": "one stream (the model's modulations run up front in one launch)"
                                   if model else "the three block modulations (mmdit_modulation_fwd) on "
                                   "a second stream, joined before each block",
                        "flops_counted_per_step": st.flops_blocks,
                        "dense_flops_per_step_incl_embeds_and_head": st.flops_dense},
             "pct_of_bf16_peak": round(100 * value / world / bf16_peak, 2),
-            **({"fp8_peak_tflops": fp8_peak,
+            **({"fp8_peak_tflops": fp8_peak, "fp8_peak_measured": fp8_measured,
                 "linears_pct_of_fp8_peak": round(100 * sum(r["achieved_tflops"] * r["avg_us"] for r in per_kernel
                                                            if r["bound"] == "tensor" and peak_of(r["kernel"]) == fp8_peak)
                                                  / max(1e-9, sum(r["avg_us"] for r in per_kernel if r["bound"] == "tensor"
@@ -896,6 +1080,7 @@ def main():
             "roofline": roofline,
             "per_kernel": per_kernel,
             "cpu_baseline": cpu,
+            "loss_check": loss_check,
             "extras": extras,
             "peaks": {"bf16_tflops": bf16_peak, "hbm_gbs": hbm_peak, "source": peak_src},
         }

@@ -27,7 +27,9 @@ EXPORTED = [
     "rope3d_freqs", "mmdit_modulation_fwd", "flow_match_workspace_size", "flow_match_noise_and_loss",
     "flow_match_noise_and_loss_noalloc", "flow_match_euler_step",
     "mmdit_linear_workspace_size", "mmdit_linear_fwd", "mmdit_img_in_workspace_size",
-    "mmdit_img_in_fwd", "mmdit_final_layer_workspace_size", "mmdit_final_layer_fwd",
+    "mmdit_img_in_fwd", "mmdit_img_in_noise_fwd", "mmdit_final_layer_workspace_size",
+    "mmdit_final_layer_fwd", "mmdit_final_layer_loss_workspace_size", "mmdit_final_layer_loss_fwd",
+    "mmdit_ln_modulate_fwd", "mmdit_copy_rows",
     "mmdit_attention_workspace_size", "mmdit_attention_fwd", "mmdit_double_block_workspace_size",
     "mmdit_double_block_fwd", "mmdit_single_block_workspace_size", "mmdit_single_block_fwd",
     "mmdit_block_workspace_offsets", "mmdit_fp8_quantize_e4m3", "mmdit_fp8_linear_workspace_size",
@@ -126,8 +128,15 @@ _SIGS = {
     "mmdit_linear_fwd": (C.c_int, [I32, I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_img_in_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
     "mmdit_img_in_fwd": (C.c_int, [I32, I32, I32, I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_img_in_noise_fwd": (C.c_int, [I32, I32, I32, I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, VP, SZ,
+                                         VP]),
     "mmdit_final_layer_workspace_size": (SZ, [PDIMS, I32]),
+    "mmdit_final_layer_loss_workspace_size": (SZ, [PDIMS, I32]),
+    "mmdit_final_layer_loss_fwd": (C.c_int, [PDIMS, I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP,
+                                             VP, SZ, VP]),
     "mmdit_final_layer_fwd": (C.c_int, [PDIMS, I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_ln_modulate_fwd": (C.c_int, [I32, I32, I32, I32, I32, F32, VP, VP, VP, I64, VP, VP]),
+    "mmdit_copy_rows": (C.c_int, [VP, I64, VP, I64, I64, I32, VP]),
     "mmdit_attention_workspace_size": (SZ, [I32, I32, I32]),
     "mmdit_attention_fwd": (C.c_int, [I32, I32, I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_double_block_workspace_size": (SZ, [PDIMS]),
@@ -330,6 +339,18 @@ def mmdit_img_in_fwd(z, w, b, out, ws=None, stream=None):
     return ws
 
 
+def mmdit_img_in_noise_fwd(z0, z1, t, w, b, out, z_t=None, ws=None, stream=None):
+    """img_in of the noised latents z_t = (1 - t) z0 + t z1, formed while patchifying."""
+    B, Cc, H, W = z0.shape
+    act = act_of(w)
+    if ws is None:
+        ws = workspace(mmdit_img_in_workspace_size(act, B, Cc, H, W), z0.device)
+    _check(load().mmdit_img_in_noise_fwd(act, B, Cc, H, W, w.shape[0], _ptr(z0), _ptr(z1), _ptr(t), _ptr(w),
+                                         _ptr(b), _ptr(out), _ptr(z_t), _ptr(ws), ws.numel(),
+                                         _stream(stream)))
+    return ws
+
+
 def mmdit_final_layer_workspace_size(dims: Dims, channels: int) -> int:
     return load().mmdit_final_layer_workspace_size(C.byref(dims), channels)
 
@@ -343,6 +364,38 @@ def mmdit_final_layer_fwd(dims: Dims, lat_h, lat_w, x_img, vec, w_ada, b_ada, w_
                                         _ptr(w_ada), _ptr(b_ada), _ptr(w_out), _ptr(b_out), _ptr(pred),
                                         _ptr(ws), ws.numel(), _stream(stream)))
     return ws
+
+
+def mmdit_final_layer_loss_workspace_size(dims: Dims, channels: int) -> int:
+    return load().mmdit_final_layer_loss_workspace_size(C.byref(dims), channels)
+
+
+def mmdit_final_layer_loss_fwd(dims: Dims, lat_h, lat_w, x_img, vec, w_ada, b_ada, w_out, b_out, z0, z1,
+                               loss, pred=None, ws=None, stream=None):
+    """The output head with the flow-matching loss fused onto its last kernel."""
+    channels = w_out.shape[0]
+    if ws is None:
+        ws = workspace(mmdit_final_layer_loss_workspace_size(dims, channels), x_img.device)
+    _check(load().mmdit_final_layer_loss_fwd(C.byref(dims), channels, lat_h, lat_w, _ptr(x_img), _ptr(vec),
+                                             _ptr(w_ada), _ptr(b_ada), _ptr(w_out), _ptr(b_out), _ptr(z0),
+                                             _ptr(z1), _ptr(pred), _ptr(loss), _ptr(ws), ws.numel(),
+                                             _stream(stream)))
+    return ws
+
+
+def mmdit_ln_modulate_fwd(x, shift, scale, out, mod_bstride, eps=1e-6, stream=None):
+    """out = LN(x) (1 + scale[b]) + shift[b]; x [B, R, D] (bf16/fp32, or fp32 with a bf16 out)."""
+    B, R, D = x.shape
+    act = act_of(out)
+    x_f32 = int(x.dtype == torch.float32 and act == MMDIT_BF16)
+    _check(load().mmdit_ln_modulate_fwd(act, x_f32, B, R, D, float(eps), _ptr(x), _ptr(shift), _ptr(scale),
+                                        int(mod_bstride), _ptr(out), _stream(stream)))
+
+
+def mmdit_copy_rows(dst, dst_stride, src, src_stride, row_bytes, n_rows, stream=None):
+    """Copy n_rows rows of row_bytes bytes between strided device buffers (strides in bytes)."""
+    _check(load().mmdit_copy_rows(_ptr(dst), int(dst_stride), _ptr(src), int(src_stride), int(row_bytes),
+                                  int(n_rows), _stream(stream)))
 
 
 def mmdit_attention_workspace_size(batch, heads, seq) -> int:

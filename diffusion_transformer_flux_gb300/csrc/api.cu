@@ -639,22 +639,56 @@ mmdit_status single_block_body(const mmdit_dims* d, const BlockPlan& p, const mm
   return fp8 ? fp8_end(p, f8, kFp8TensorsPerStream, st) : MMDIT_OK;
 }
 
+// Output-head workspace: the head's modulation, its LayerNorm-modulate output, the split-K
+// partials, and (loss variant) one partial sum per finishing block.  The loss variant's ticket
+// counter sits inside the status region (kHeadTicketOffset), cleared with the status word.
+constexpr size_t kHeadTicketOffset = 128;
+struct HeadPlan {
+  size_t mod, h, partials, loss_partials, total;
+  int splits;
+};
+HeadPlan plan_head(const mmdit_dims* d, int channels, bool with_loss) {
+  HeadPlan p;
+  Carver c;
+  const int M = d->batch * d->seq_img;
+  p.mod = c.take(static_cast<size_t>(d->batch) * 2 * d->hidden * 4);
+  p.h = c.take(static_cast<size_t>(M) * d->hidden * elt_bytes(d->act));
+  p.splits = choose_splits(M, channels, d->hidden, static_cast<int>(elt_bytes(d->act)));
+  // the loss variant always takes the partials path: its finishing kernel forms pred and the loss
+  p.partials = p.splits > 1 || with_loss ? c.take(static_cast<size_t>(p.splits) * M * channels * sizeof(float)) : 0;
+  p.loss_partials = with_loss ? c.take(static_cast<size_t>(head_finish_blocks(M, channels)) * sizeof(float)) : 0;
+  p.total = c.off;
+  return p;
+}
+
 mmdit_status final_layer_body(const mmdit_dims* d, int channels, const void* x_img, const void* vec,
                               const void* w_ada, const void* b_ada, const void* w_out,
-                              const void* b_out, float* pred, void* workspace, cudaStream_t st) {
-  Carver c;
-  float* mod = at<float>(workspace, c.take(static_cast<size_t>(d->batch) * 2 * d->hidden * 4));
-  void* h = at(workspace, c.take(static_cast<size_t>(d->batch) * d->seq_img * d->hidden * elt_bytes(d->act)));
+                              const void* b_out, float* pred, void* workspace, cudaStream_t st,
+                              const float* z0 = nullptr, const float* z1 = nullptr,
+                              float* loss = nullptr) {
+  const bool with_loss = loss != nullptr;
+  const HeadPlan hp = plan_head(d, channels, with_loss);
+  float* mod = at<float>(workspace, hp.mod);
+  void* h = at(workspace, hp.h);
   const int D = d->hidden, rows = d->batch * d->seq_img;
-  ProfScope ps_("final_layer", st);
+  ProfScope ps_(with_loss ? "final_layer_loss" : "final_layer", st);
   MMDIT_CUDA(launch_modulation(d->act, vec, w_ada, b_ada, d->batch, 2 * D, D, mod, st), "final modulation");
   MMDIT_CUDA(launch_ln_modulate(d->act, d->act == MMDIT_F32, x_img, mod, mod + D, 2 * D, rows, d->seq_img, D, d->ln_eps, h, st),
              "final LayerNorm-modulate");
   GemmProblem g;
   g.act = d->act, g.M = rows, g.N = channels, g.K = D, g.A = h, g.W = w_out;
-  const int splits = choose_splits(rows, channels, D, static_cast<int>(elt_bytes(d->act)));
-  if (splits > 1) {
-    float* partials = at<float>(workspace, c.take(static_cast<size_t>(splits) * rows * channels * 4));
+  const int splits = hp.splits;
+  if (with_loss) {
+    // the projection's fp32 partials, then one kernel forming pred and the fused loss
+    float* partials = at<float>(workspace, hp.partials);
+    g.epi = kEpiPartial, g.splits = splits, g.ep.out = partials;
+    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "final projection (partials)");
+    MMDIT_CUDA(launch_head_finish(d->act, partials, splits, rows, channels, b_out, d->seq_img, pred, z0, z1,
+                                  at<float>(workspace, hp.loss_partials),
+                                  at<unsigned int>(workspace, kHeadTicketOffset), loss, st),
+               "final projection sum + flow-matching loss");
+  } else if (splits > 1) {
+    float* partials = at<float>(workspace, hp.partials);
     g.epi = kEpiPartial, g.splits = splits, g.ep.out = partials;
     MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "final projection (split K)");
     MMDIT_CUDA(launch_splitk_reduce(d->act, partials, splits, rows, channels, b_out, pred,
@@ -669,11 +703,13 @@ mmdit_status final_layer_body(const mmdit_dims* d, int channels, const void* x_i
 
 mmdit_status img_in_body(int act, int batch, int channels, int lat_h, int lat_w, int hidden,
                          const float* z, const void* w, const void* b, void* out, void* workspace,
-                         cudaStream_t st) {
+                         cudaStream_t st, const float* z1 = nullptr, const float* t = nullptr,
+                         float* z_t = nullptr) {
   void* tokens = at(workspace, kStatusBytes);
   const int hw = lat_h * lat_w;
-  ProfScope ps_("img_in", st);
-  MMDIT_CUDA(launch_patchify(act, z, batch, channels, hw, tokens, st), "patchify");
+  ProfScope ps_(z1 ? "img_in_noise" : "img_in", st);
+  MMDIT_CUDA(launch_patchify(act, z, batch, channels, hw, tokens, st, z1, t, z_t),
+             z1 ? "patchify of z_t" : "patchify");
   GemmProblem g;
   g.act = act, g.epi = kEpiBias, g.M = batch * hw, g.N = hidden, g.K = channels;
   g.A = tokens, g.W = w, g.ep.bias = b, g.ep.out = out;
@@ -705,8 +741,8 @@ size_t conditioning_workspace(int act, int batch, int hidden, int time_dim) {
   Carver c;
   const size_t e = elt_bytes(act);
   c.take(static_cast<size_t>(batch) * time_dim * e);  // sinusoidal features
-  c.take(static_cast<size_t>(batch) * hidden * e);    // timestep MLP hidden layer
-  c.take(static_cast<size_t>(batch) * hidden * e);    // vector MLP hidden layer
+  c.take(static_cast<size_t>(batch) * hidden * 4);    // timestep MLP hidden layer (fp32)
+  c.take(static_cast<size_t>(batch) * hidden * 4);    // vector MLP hidden layer (fp32)
   c.take(static_cast<size_t>(batch) * hidden * 4);    // fp32 sum of the embeddings
   return c.off;
 }
@@ -717,21 +753,22 @@ mmdit_status conditioning_body(int act, int B, int D, int time_dim, int vec_in_d
   Carver c;
   const size_t e = elt_bytes(act);
   void* feat = at(workspace, c.take(static_cast<size_t>(B) * time_dim * e));
-  void* ht = at(workspace, c.take(static_cast<size_t>(B) * D * e));
-  void* hy = at(workspace, c.take(static_cast<size_t>(B) * D * e));
+  float* ht = at<float>(workspace, c.take(static_cast<size_t>(B) * D * 4));
+  float* hy = at<float>(workspace, c.take(static_cast<size_t>(B) * D * 4));
   float* v32 = at<float>(workspace, c.take(static_cast<size_t>(B) * D * 4));
   ProfScope ps_("conditioning", st);
   MMDIT_CUDA(launch_timestep_features(act, t, B, time_dim, 1000.0, 10000.0, feat, st), "timestep features");
-  // first layers (no activation on their inputs), kept in the activation type
+  // first layers (no activation on their inputs); the hidden layers stay fp32, so the second
+  // layers' operand SiLU(h) is rounded once, where it enters the linear
   const ModulationJob l1t{w->time_in.w1, w->time_in.b1, ht, D};
-  MMDIT_CUDA(launch_gemv(act, feat, &l1t, 1, B, time_dim, 0, kGemvOutAct, st), "timestep MLP layer 1");
+  MMDIT_CUDA(launch_gemv(act, feat, &l1t, 1, B, time_dim, 0, kGemvOutF32, st), "timestep MLP layer 1");
   const ModulationJob l1y{w->vector_in.w1, w->vector_in.b1, hy, D};
-  MMDIT_CUDA(launch_gemv(act, y, &l1y, 1, B, vec_in_dim, 0, kGemvOutAct, st), "vector MLP layer 1");
+  MMDIT_CUDA(launch_gemv(act, y, &l1y, 1, B, vec_in_dim, 0, kGemvOutF32, st), "vector MLP layer 1");
   // second layers read SiLU of the hidden layers; the vector MLP adds onto the timestep's
   const ModulationJob l2t{w->time_in.w2, w->time_in.b2, v32, D};
-  MMDIT_CUDA(launch_gemv(act, ht, &l2t, 1, B, D, 1, kGemvOutF32, st), "timestep MLP layer 2");
+  MMDIT_CUDA(launch_gemv(act, ht, &l2t, 1, B, D, 1, kGemvOutF32, st, 1), "timestep MLP layer 2");
   const ModulationJob l2y{w->vector_in.w2, w->vector_in.b2, v32, D};
-  MMDIT_CUDA(launch_gemv(act, hy, &l2y, 1, B, D, 1, kGemvOutF32Add, st), "vector MLP layer 2");
+  MMDIT_CUDA(launch_gemv(act, hy, &l2y, 1, B, D, 1, kGemvOutF32Add, st, 1), "vector MLP layer 2");
   MMDIT_CUDA(launch_vec_finish(act, v32, g, w->w_guidance, w->b_guidance, B, D, vec, st), "conditioning vector");
   return MMDIT_OK;
 }
@@ -896,7 +933,10 @@ mmdit_status mmdit_modulation_fwd(int32_t act, int32_t batch, int32_t rows, int3
 }
 
 size_t flow_match_workspace_size(int32_t batch, int64_t n_per_sample) {
-  const int64_t n = static_cast<int64_t>(batch > 0 ? batch : 0) * (n_per_sample > 0 ? n_per_sample : 0);
+  // the partial-sum count saturates at kFlowMaxPartials, so a product that would overflow
+  // needs the same workspace as any other large call
+  const int64_t b = batch > 0 ? batch : 0, n1 = n_per_sample > 0 ? n_per_sample : 0;
+  const int64_t n = b > 0 && n1 > INT64_MAX / b ? INT64_MAX : b * n1;
   return kStatusBytes + round_up(static_cast<size_t>(flow_partial_blocks(n)) * sizeof(float), 256);
 }
 
@@ -910,6 +950,8 @@ mmdit_status flow_match_noise_and_loss(int32_t dtype, const void* z0, const void
   if (n_per_sample % 8 != 0)
     return fail(MMDIT_ERR_UNSUPPORTED, "n_per_sample must be a multiple of 8 (got %lld)",
                 static_cast<long long>(n_per_sample));
+  if (batch > 0 && n_per_sample > INT64_MAX / batch)
+    return fail(MMDIT_ERR_INVALID_ARG, "batch * n_per_sample overflows a 64-bit count");
   if ((pred == nullptr) != (loss == nullptr))
     return fail(MMDIT_ERR_INVALID_ARG, "pred and loss must both be given or both be NULL");
   mmdit_status s = check_ptrs({z0, z1}, "flow_match latents");
@@ -1008,15 +1050,37 @@ mmdit_status mmdit_img_in_fwd(int32_t act, int32_t batch, int32_t channels, int3
   return img_in_body(act, batch, channels, lat_h, lat_w, hidden, z, w, b, out, workspace, st);
 }
 
+mmdit_status mmdit_img_in_noise_fwd(int32_t act, int32_t batch, int32_t channels, int32_t lat_h,
+                                    int32_t lat_w, int32_t hidden, const float* z0, const float* z1,
+                                    const float* t, const void* w, const void* b, void* out,
+                                    float* z_t, void* workspace, size_t workspace_bytes, void* stream) {
+  if (act != MMDIT_F32 && act != MMDIT_BF16) return fail(MMDIT_ERR_INVALID_ARG, "bad act %d", act);
+  if (batch < 1 || channels < 1 || lat_h < 1 || lat_w < 1 || hidden < 1)
+    return fail(MMDIT_ERR_INVALID_ARG, "bad img_in shape");
+  if (channels % 8 != 0 || hidden % 32 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "channels must be a multiple of 8 and hidden of 32");
+  mmdit_status s = check_ptrs({z0, z1, t, w, b, out}, "img_in + noise");
+  if (s != MMDIT_OK) return s;
+  if (z_t && (s = check_ptrs({z_t}, "img_in + noise: z_t")) != MMDIT_OK) return s;
+  if (z_t && (z_t == z0 || z_t == z1))
+    return fail(MMDIT_ERR_INVALID_ARG, "img_in + noise: z_t may not alias z0 or z1");
+  if ((s = check_workspace(workspace, workspace_bytes,
+                           mmdit_img_in_workspace_size(act, batch, channels, lat_h, lat_w))) != MMDIT_OK)
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
+  return img_in_body(act, batch, channels, lat_h, lat_w, hidden, z0, w, b, out, workspace, st, z1, t, z_t);
+}
+
 size_t mmdit_final_layer_workspace_size(const mmdit_dims* d, int32_t channels) {
   if (!d || d->batch < 1 || d->hidden < 1 || d->seq_img < 0 || channels < 1) return 0;
-  Carver c;
-  c.take(static_cast<size_t>(d->batch) * 2 * d->hidden * 4);
-  c.take(static_cast<size_t>(d->batch) * d->seq_img * d->hidden * elt_bytes(d->act));
-  const int M = d->batch * d->seq_img;
-  const int splits = choose_splits(M, channels, d->hidden, static_cast<int>(elt_bytes(d->act)));
-  if (splits > 1) c.take(static_cast<size_t>(splits) * M * channels * sizeof(float));
-  return c.off;
+  return plan_head(d, channels, false).total;
+}
+
+size_t mmdit_final_layer_loss_workspace_size(const mmdit_dims* d, int32_t channels) {
+  if (!d || d->batch < 1 || d->hidden < 1 || d->seq_img < 0 || channels < 1) return 0;
+  return plan_head(d, channels, true).total;
 }
 
 mmdit_status mmdit_final_layer_fwd(const mmdit_dims* d, int32_t channels, int32_t lat_h,
@@ -1041,6 +1105,74 @@ mmdit_status mmdit_final_layer_fwd(const mmdit_dims* d, int32_t channels, int32_
   return final_layer_body(d, channels, x_img, vec, w_ada, b_ada, w_out, b_out, pred, workspace, st);
 }
 
+mmdit_status mmdit_final_layer_loss_fwd(const mmdit_dims* d, int32_t channels, int32_t lat_h,
+                                        int32_t lat_w, const void* x_img, const void* vec,
+                                        const void* w_ada, const void* b_ada, const void* w_out,
+                                        const void* b_out, const float* z0, const float* z1,
+                                        float* pred, float* loss, void* workspace,
+                                        size_t workspace_bytes, void* stream) {
+  if (!d) return fail(MMDIT_ERR_INVALID_ARG, "dims is NULL");
+  if (d->act != MMDIT_F32 && d->act != MMDIT_BF16) return fail(MMDIT_ERR_INVALID_ARG, "bad act");
+  if (d->batch < 1 || lat_h < 1 || lat_w < 1 || d->seq_img != lat_h * lat_w)
+    return fail(MMDIT_ERR_INVALID_ARG, "final layer + loss: seq_img must equal lat_h * lat_w");
+  if (channels < 32 || channels % 32 != 0 || d->hidden % 256 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "final layer + loss: channels multiple of 32, hidden of 256");
+  mmdit_status s = check_ptrs({x_img, vec, w_ada, b_ada, w_out, b_out, z0, z1, loss}, "final layer + loss");
+  if (s != MMDIT_OK) return s;
+  if (pred && (s = check_ptrs({pred}, "final layer + loss: pred")) != MMDIT_OK) return s;
+  if (pred && (pred == z0 || pred == z1))
+    return fail(MMDIT_ERR_INVALID_ARG, "final layer + loss: pred may not alias z0 or z1");
+  if ((s = check_workspace(workspace, workspace_bytes, mmdit_final_layer_loss_workspace_size(d, channels))) !=
+      MMDIT_OK)
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the status word and the loss ticket counter (both inside the status region)
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, kStatusBytes, st), "status clear");
+  pdl_begin_call();
+  return final_layer_body(d, channels, x_img, vec, w_ada, b_ada, w_out, b_out, pred, workspace, st, z0,
+                          z1, loss);
+}
+
+
+mmdit_status mmdit_ln_modulate_fwd(int32_t act, int32_t x_f32, int32_t batch, int32_t rows_per_batch,
+                                   int32_t dim, float eps, const void* x, const float* shift,
+                                   const float* scale, int64_t mod_bstride, void* out, void* stream) {
+  if (act != MMDIT_F32 && act != MMDIT_BF16) return fail(MMDIT_ERR_INVALID_ARG, "bad act %d", act);
+  if (batch < 0 || rows_per_batch < 0 || dim < 1 || mod_bstride < 0 || !(eps >= 0.f))
+    return fail(MMDIT_ERR_INVALID_ARG, "LayerNorm-modulate: bad shape or eps");
+  if (dim % 8 != 0 || dim > 8192)
+    return fail(MMDIT_ERR_UNSUPPORTED, "LayerNorm-modulate: dim must be a multiple of 8, at most 8192 (got %d)", dim);
+  const int64_t rows = static_cast<int64_t>(batch) * rows_per_batch;
+  if (rows > INT32_MAX) return fail(MMDIT_ERR_UNSUPPORTED, "LayerNorm-modulate: more than 2^31 - 1 rows");
+  if (rows == 0) return MMDIT_OK;
+  if (mod_bstride % 4 != 0)
+    return fail(MMDIT_ERR_INVALID_ARG, "LayerNorm-modulate: mod_bstride must be a multiple of 4 (16-byte rows)");
+  mmdit_status s = check_ptrs({x, shift, scale, out}, "LayerNorm-modulate");
+  if (s != MMDIT_OK) return s;
+  if (out == x) return fail(MMDIT_ERR_INVALID_ARG, "LayerNorm-modulate: out may not alias x");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  pdl_begin_call();
+  ProfScope ps_("ln_modulate", st);
+  MMDIT_CUDA(launch_ln_modulate(act, x_f32 ? 1 : 0, x, shift, scale, mod_bstride, static_cast<int>(rows),
+                                rows_per_batch, dim, eps, out, st),
+             "LayerNorm-modulate");
+  return MMDIT_OK;
+}
+
+mmdit_status mmdit_copy_rows(void* dst, int64_t dst_stride, const void* src, int64_t src_stride,
+                             int64_t row_bytes, int32_t n_rows, void* stream) {
+  if (n_rows < 0 || row_bytes < 0 || dst_stride < row_bytes || src_stride < row_bytes)
+    return fail(MMDIT_ERR_INVALID_ARG, "copy_rows: bad sizes or strides");
+  if (n_rows == 0 || row_bytes == 0) return MMDIT_OK;
+  if (!dst || !src) return fail(MMDIT_ERR_INVALID_ARG, "copy_rows: NULL pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemcpy2DAsync(dst, static_cast<size_t>(dst_stride), src, static_cast<size_t>(src_stride),
+                               static_cast<size_t>(row_bytes), static_cast<size_t>(n_rows),
+                               cudaMemcpyDeviceToDevice, st),
+             "copy_rows");
+  pdl_begin_call();  // a later kernel of this thread follows a copy, not a kernel
+  return MMDIT_OK;
+}
 
 size_t mmdit_attention_workspace_size(int32_t batch, int32_t heads, int32_t seq) {
   if (batch < 1 || heads < 1 || seq < 1) return kStatusBytes;

@@ -111,9 +111,10 @@ struct Raw8<float> {
 };
 
 template <typename T, int NC, int NB>
-__global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __restrict__ vec,
+__global__ void __launch_bounds__(kModThreads) modulation_kernel(const void* __restrict__ vec,
                                                                  const __grid_constant__ ModJobs jobs,
-                                                                 int dim, int silu, int mode) {
+                                                                 int dim, int silu, int mode,
+                                                                 int vec_f32) {
   pdl_wait();  // the previous kernel's results are visible from here on
   constexpr int batch = NB;  // batch rows handled by this launch (compile time: no idle lanes)
   // [batch, dim] SiLU(vec) (or vec itself when silu == 0): fp32, or in bf16 mode the bf16
@@ -122,7 +123,8 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const T* __rest
   extern __shared__ float svec[];
   __nv_bfloat16* svec_bf = reinterpret_cast<__nv_bfloat16*>(svec);
   for (int i = threadIdx.x; i < batch * dim; i += blockDim.x) {
-    const float v = to_f32(vec[i]);
+    // vec is of the weights' type, or fp32 (an fp32 hidden layer feeding a bf16 linear)
+    const float v = vec_f32 ? static_cast<const float*>(vec)[i] : to_f32(static_cast<const T*>(vec)[i]);
     const float sv = silu ? v / (1.f + expf(-v)) : v;
     if constexpr (sizeof(T) == 2)
       svec_bf[i] = __float2bfloat16_rn(sv);
@@ -332,17 +334,33 @@ __global__ void __launch_bounds__(kLnThreads) ln_modulate_kernel(LnJob j0, LnJob
 }
 
 // ----------------------------------------------------------------------------- transposes
-// z [B, C, HW] fp32 -> out [B, HW, C]
+// z [B, C, HW] fp32 -> out [B, HW, C].  With z1 non-null the latents are the rectified-flow
+// interpolation z = (1 - t[b]) z0 + t[b] z1 of z0 = `z` and z1, formed as they are read (the same
+// arithmetic as flow_kernel, so the values are bit-equal) and, with z_t non-null, also written to
+// z_t [B, C, HW] fp32.
 template <typename T>
-__global__ void patchify_kernel(const float* __restrict__ z, int channels, int hw, T* __restrict__ out) {
+__global__ void patchify_kernel(const float* __restrict__ z, int channels, int hw, T* __restrict__ out,
+                                const float* __restrict__ z1, const float* __restrict__ t,
+                                float* __restrict__ z_t) {
   pdl_wait();  // the previous kernel's results are visible from here on
   __shared__ float tile[32][33];
   const int b = blockIdx.z;
   const int s0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
-  const float* zb = z + static_cast<size_t>(b) * channels * hw;
+  const size_t boff = static_cast<size_t>(b) * channels * hw;
+  const float* zb = z + boff;
+  const float tt = z1 ? t[b] : 0.f;
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int c = c0 + i, s = s0 + threadIdx.x;
-    tile[i][threadIdx.x] = (c < channels && s < hw) ? zb[static_cast<size_t>(c) * hw + s] : 0.f;
+    float v = 0.f;
+    if (c < channels && s < hw) {
+      const size_t o = static_cast<size_t>(c) * hw + s;
+      v = zb[o];
+      if (z1) {
+        v = fmaf(tt, z1[boff + o], (1.f - tt) * v);
+        if (z_t) z_t[boff + o] = v;
+      }
+    }
+    tile[i][threadIdx.x] = v;
   }
   __syncthreads();
   T* ob = out + static_cast<size_t>(b) * hw * channels;
@@ -413,9 +431,116 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partials, int spl
   }
 }
 
+// ----------------------------------------------------------------------------- output head + loss
+// The output stage of the output head with the rectified-flow loss fused on: per tile of
+// kHeadRows tokens x kHeadCols channels,
+//   v[m, n] = sum_s partial[s][m][n] + bias[n]       (split order: deterministic)
+//   pred[b, n, r] = v (unpatchified, m = b * hw + r)   (if pred is non-null)
+//   acc += (v - (z1[b, n, r] - z0[b, n, r]))^2         (if z0 is non-null)
+// The partials are read along n and pred, z0, z1 along r, both coalesced, through a shared-memory
+// transpose.  Each block writes one partial sum of squares; the last block to finish (a ticket
+// counter that it resets to 0) adds them in block order and writes loss = sum / (M * N).
+constexpr int kHeadRows = 32, kHeadCols = 64, kHeadThreads = 256;
+
+__device__ __forceinline__ float block_sum_fixed(float v, float* red) {
+  // a fixed-shape tree: lane shuffles, then warp 0 over the warps' sums (same order every call)
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float w = 0.f;
+  if (threadIdx.x < 32) {
+    w = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0.f;
+    w = warp_sum(w);
+  }
+  __syncthreads();
+  return w;  // valid in thread 0
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kHeadThreads) head_finish_kernel(
+    const float* __restrict__ partials, int splits, int M, int N, const T* __restrict__ bias, int hw,
+    float* __restrict__ pred, const float* __restrict__ z0, const float* __restrict__ z1,
+    float* __restrict__ loss_partials, unsigned int* __restrict__ ticket, float* __restrict__ loss,
+    double inv_total) {
+  pdl_wait();  // the previous kernel's results are visible from here on
+  __shared__ float tile[kHeadCols][kHeadRows + 1];
+  __shared__ float red[kHeadThreads / 32];
+  __shared__ bool last;
+  const int col_tiles = (N + kHeadCols - 1) / kHeadCols;
+  const int n_tiles = ((M + kHeadRows - 1) / kHeadRows) * col_tiles;
+  float acc = 0.f;
+  for (int tile_i = blockIdx.x; tile_i < n_tiles; tile_i += gridDim.x) {
+    const int m0 = (tile_i / col_tiles) * kHeadRows, n0 = (tile_i % col_tiles) * kHeadCols;
+    {
+      // 8 consecutive columns of one row per thread
+      const int rl = threadIdx.x / (kHeadCols / 8), cl = (threadIdx.x % (kHeadCols / 8)) * 8;
+      const int m = m0 + rl, n = n0 + cl;
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = 0.f;
+      if (m < M && n < N) {  // N is a multiple of 32 and n of 8: the 8 columns are all in range
+        const size_t e = static_cast<size_t>(m) * N + n;
+        load8(partials + e, v);
+        for (int sp = 1; sp < splits; ++sp) {
+          float w[8];
+          load8(partials + static_cast<size_t>(sp) * M * N + e, w);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] += w[q];
+        }
+        if (bias) {
+          float bb[8];
+          load8(bias + n, bb);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[q] += bb[q];
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) tile[cl + q][rl] = v[q];
+    }
+    __syncthreads();
+    {
+      // one token per lane, kHeadThreads / kHeadRows channels per pass
+      const int rl = threadIdx.x % kHeadRows;
+      const int m = m0 + rl;
+      if (m < M) {
+        const int b = m / hw, r = m % hw;
+        for (int cl = threadIdx.x / kHeadRows; cl < kHeadCols; cl += kHeadThreads / kHeadRows) {
+          const int n = n0 + cl;
+          if (n >= N) break;
+          const float v = tile[cl][rl];
+          const size_t o = (static_cast<size_t>(b) * N + n) * hw + r;
+          if (pred) pred[o] = v;
+          if (z0) {
+            const float d = v - (z1[o] - z0[o]);
+            acc = fmaf(d, d, acc);
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+  if (!z0) return;
+  const float part = block_sum_fixed(acc, red);
+  if (threadIdx.x == 0) {
+    loss_partials[blockIdx.x] = part;
+    __threadfence();  // the partial is visible device-wide before the ticket is taken
+    last = atomicAdd(ticket, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  float v = 0.f;
+  for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += blockDim.x) v += __ldcg(loss_partials + i);
+  const float total = block_sum_fixed(v, red);
+  if (threadIdx.x == 0) {
+    *loss = static_cast<float>(static_cast<double>(total) * inv_total);
+    *ticket = 0u;  // ready for the next call on this workspace
+  }
+}
+
 // ----------------------------------------------------------------------------- rectified flow
 constexpr int kFlowThreads = 256;
-constexpr int kFlowMaxPartials = 1024;
+static_assert(kFlowElemsPerPartial == kFlowThreads * 8 * 4, "four rounds of 8 elements per thread");
 
 template <typename T>
 __global__ void __launch_bounds__(kFlowThreads) flow_kernel(const T* __restrict__ z0, const T* __restrict__ z1,
@@ -622,8 +747,8 @@ cudaError_t launch_rope3d(const float* ids, int batch, int seq, const int axes[3
 }
 
 template <typename T, int NC, int NB>
-cudaError_t launch_mod(const void* vec, const ModJobs& jobs, int dim, int silu, int mode, size_t smem,
-                       cudaStream_t stream) {
+cudaError_t launch_mod(const void* vec, const ModJobs& jobs, int dim, int silu, int mode, int vec_f32,
+                       size_t smem, cudaStream_t stream) {
   auto kern = modulation_kernel<T, NC, NB>;
   static int configured = -1;
   int dev = 0;
@@ -640,7 +765,7 @@ cudaError_t launch_mod(const void* vec, const ModJobs& jobs, int dim, int silu, 
   const int grid = blocks_for(rows, kModThreads / 32, num_sms() * per_sm);
   {
     const cudaError_t e_ = launch_pdl(kern, dim3(grid), dim3(kModThreads), smem, stream,
-                                      static_cast<const T*>(vec), jobs, dim, silu, mode);
+                                      vec, jobs, dim, silu, mode, vec_f32);
     if (e_ != cudaSuccess) return e_;
   }
   count_launch();
@@ -649,22 +774,23 @@ cudaError_t launch_mod(const void* vec, const ModJobs& jobs, int dim, int silu, 
 
 template <typename T, int NC>
 cudaError_t launch_mod_nb(const void* vec, const ModJobs& jobs, int nb, int dim, int silu, int mode,
-                          size_t smem, cudaStream_t stream) {
+                          int vec_f32, size_t smem, cudaStream_t stream) {
   switch (nb) {
-    case 1: return launch_mod<T, NC, 1>(vec, jobs, dim, silu, mode, smem, stream);
-    case 2: return launch_mod<T, NC, 2>(vec, jobs, dim, silu, mode, smem, stream);
-    case 3: return launch_mod<T, NC, 3>(vec, jobs, dim, silu, mode, smem, stream);
-    case 4: return launch_mod<T, NC, 4>(vec, jobs, dim, silu, mode, smem, stream);
-    case 5: return launch_mod<T, NC, 5>(vec, jobs, dim, silu, mode, smem, stream);
-    case 6: return launch_mod<T, NC, 6>(vec, jobs, dim, silu, mode, smem, stream);
-    case 7: return launch_mod<T, NC, 7>(vec, jobs, dim, silu, mode, smem, stream);
-    default: return launch_mod<T, NC, 8>(vec, jobs, dim, silu, mode, smem, stream);
+    case 1: return launch_mod<T, NC, 1>(vec, jobs, dim, silu, mode, vec_f32, smem, stream);
+    case 2: return launch_mod<T, NC, 2>(vec, jobs, dim, silu, mode, vec_f32, smem, stream);
+    case 3: return launch_mod<T, NC, 3>(vec, jobs, dim, silu, mode, vec_f32, smem, stream);
+    case 4: return launch_mod<T, NC, 4>(vec, jobs, dim, silu, mode, vec_f32, smem, stream);
+    case 5: return launch_mod<T, NC, 5>(vec, jobs, dim, silu, mode, vec_f32, smem, stream);
+    case 6: return launch_mod<T, NC, 6>(vec, jobs, dim, silu, mode, vec_f32, smem, stream);
+    case 7: return launch_mod<T, NC, 7>(vec, jobs, dim, silu, mode, vec_f32, smem, stream);
+    default: return launch_mod<T, NC, 8>(vec, jobs, dim, silu, mode, vec_f32, smem, stream);
   }
 }
 
 cudaError_t launch_gemv(int act, const void* vec, const ModulationJob* jobs, int njobs, int batch,
-                        int dim, int silu, int mode, cudaStream_t stream) {
+                        int dim, int silu, int mode, cudaStream_t stream, int vec_f32) {
   const size_t elt = act == 1 ? 2 : 4;
+  const size_t vec_elt = vec_f32 ? 4 : elt;
   const size_t out_elt = mode == kGemvOutAct ? elt : 4;
   const int chunks = (dim + 255) / 256;
   for (int j0 = 0; j0 < njobs; j0 += kModMaxJobs) {
@@ -686,17 +812,17 @@ cudaError_t launch_gemv(int act, const void* vec, const ModulationJob* jobs, int
       }
       mj.start[mj.n] = rows;
       if (rows == 0) continue;
-      const void* vb = static_cast<const uint8_t*>(vec) + static_cast<size_t>(b0) * dim * elt;
+      const void* vb = static_cast<const uint8_t*>(vec) + static_cast<size_t>(b0) * dim * vec_elt;
       cudaError_t e;
       if (act == 1) {
-        if (chunks <= 4) e = launch_mod_nb<__nv_bfloat16, 4>(vb, mj, nb, dim, silu, mode, smem, stream);
-        else if (chunks <= 8) e = launch_mod_nb<__nv_bfloat16, 8>(vb, mj, nb, dim, silu, mode, smem, stream);
-        else if (chunks <= 12) e = launch_mod_nb<__nv_bfloat16, 12>(vb, mj, nb, dim, silu, mode, smem, stream);
-        else e = launch_mod_nb<__nv_bfloat16, 24>(vb, mj, nb, dim, silu, mode, smem, stream);
+        if (chunks <= 4) e = launch_mod_nb<__nv_bfloat16, 4>(vb, mj, nb, dim, silu, mode, vec_f32, smem, stream);
+        else if (chunks <= 8) e = launch_mod_nb<__nv_bfloat16, 8>(vb, mj, nb, dim, silu, mode, vec_f32, smem, stream);
+        else if (chunks <= 12) e = launch_mod_nb<__nv_bfloat16, 12>(vb, mj, nb, dim, silu, mode, vec_f32, smem, stream);
+        else e = launch_mod_nb<__nv_bfloat16, 24>(vb, mj, nb, dim, silu, mode, vec_f32, smem, stream);
       } else {
-        if (chunks <= 4) e = launch_mod_nb<float, 4>(vb, mj, nb, dim, silu, mode, smem, stream);
-        else if (chunks <= 8) e = launch_mod_nb<float, 8>(vb, mj, nb, dim, silu, mode, smem, stream);
-        else e = launch_mod_nb<float, 16>(vb, mj, nb, dim, silu, mode, smem, stream);
+        if (chunks <= 4) e = launch_mod_nb<float, 4>(vb, mj, nb, dim, silu, mode, vec_f32, smem, stream);
+        else if (chunks <= 8) e = launch_mod_nb<float, 8>(vb, mj, nb, dim, silu, mode, vec_f32, smem, stream);
+        else e = launch_mod_nb<float, 16>(vb, mj, nb, dim, silu, mode, vec_f32, smem, stream);
       }
       if (e != cudaSuccess) return e;
     }
@@ -766,14 +892,15 @@ cudaError_t launch_ln_modulate(int act, int x_f32, const void* x, const float* s
 }
 
 cudaError_t launch_patchify(int act, const float* z, int batch, int channels, int hw, void* out,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, const float* z1, const float* t, float* z_t) {
   const dim3 grid((hw + 31) / 32, (channels + 31) / 32, batch), block(32, 8);
   if (act == 1) {
     const cudaError_t e_ = launch_pdl(patchify_kernel<__nv_bfloat16>, dim3(grid), dim3(block), 0, stream, z, channels, hw,
-                                                               static_cast<__nv_bfloat16*>(out));
+                                      static_cast<__nv_bfloat16*>(out), z1, t, z_t);
     if (e_ != cudaSuccess) return e_;
   } else {
-    const cudaError_t e_ = launch_pdl(patchify_kernel<float>, dim3(grid), dim3(block), 0, stream, z, channels, hw, static_cast<float*>(out));
+    const cudaError_t e_ = launch_pdl(patchify_kernel<float>, dim3(grid), dim3(block), 0, stream, z, channels, hw,
+                                      static_cast<float*>(out), z1, t, z_t);
     if (e_ != cudaSuccess) return e_;
   }
   count_launch();
@@ -811,8 +938,34 @@ cudaError_t launch_splitk_reduce(int act, const float* partials, int splits, int
   return cudaGetLastError();
 }
 
+int head_finish_blocks(int M, int N) {
+  const int64_t tiles = static_cast<int64_t>((M + kHeadRows - 1) / kHeadRows) * ((N + kHeadCols - 1) / kHeadCols);
+  return blocks_for(tiles, 1, num_sms() * 4);
+}
+
+cudaError_t launch_head_finish(int act, const float* partials, int splits, int M, int N, const void* bias,
+                               int hw, float* pred, const float* z0, const float* z1,
+                               float* loss_partials, unsigned int* ticket, float* loss,
+                               cudaStream_t stream) {
+  if (M == 0) return cudaSuccess;
+  const int grid = head_finish_blocks(M, N);
+  const double inv_total = 1.0 / (static_cast<double>(M) * N);
+  cudaError_t e;
+  if (act == 1)
+    e = launch_pdl(head_finish_kernel<__nv_bfloat16>, dim3(grid), dim3(kHeadThreads), 0, stream, partials,
+                   splits, M, N, static_cast<const __nv_bfloat16*>(bias), hw, pred, z0, z1, loss_partials,
+                   ticket, loss, inv_total);
+  else
+    e = launch_pdl(head_finish_kernel<float>, dim3(grid), dim3(kHeadThreads), 0, stream, partials, splits, M,
+                   N, static_cast<const float*>(bias), hw, pred, z0, z1, loss_partials, ticket, loss,
+                   inv_total);
+  if (e != cudaSuccess) return e;
+  count_launch();
+  return cudaGetLastError();
+}
+
 int flow_partial_blocks(int64_t n_total) {
-  return blocks_for(n_total, kFlowThreads * 8 * 4, kFlowMaxPartials);
+  return blocks_for(n_total, static_cast<int>(kFlowElemsPerPartial), kFlowMaxPartials);
 }
 
 cudaError_t launch_flow_match(int dtype, const void* z0, const void* z1, const float* t, int batch,

@@ -155,10 +155,11 @@ cudaError_t launch_modulation2(int act, const void* vec, const ModulationJob* jo
                                int batch, int dim, cudaStream_t stream);
 // The GEMV behind the modulation, for any number of weight matrices that read one input:
 // out_j[b, :] (=, or +=) f(vec[b, :]) W_j^T + b_j, f = SiLU when silu != 0, else the identity.
-// Jobs are grouped into launches of up to 80, batch rows into groups of up to 8.
+// Jobs are grouped into launches of up to 80, batch rows into groups of up to 8.  vec is of the
+// activation type, or fp32 when vec_f32 != 0 (the weights keep the activation type).
 enum { kGemvOutF32 = 0, kGemvOutF32Add = 1, kGemvOutAct = 2 };
 cudaError_t launch_gemv(int act, const void* vec, const ModulationJob* jobs, int njobs, int batch,
-                        int dim, int silu, int mode, cudaStream_t stream);
+                        int dim, int silu, int mode, cudaStream_t stream, int vec_f32 = 0);
 // Sinusoidal timestep features out[b, :] = [cos(tau f_k), sin(tau f_k)], tau = time_factor t[b],
 // f_k = max_period^(-k / half), k < half = dim / 2 (dim even, half <= 256).
 cudaError_t launch_timestep_features(int act, const float* t, int batch, int dim,
@@ -195,9 +196,22 @@ struct LnModJob {
 };
 cudaError_t launch_ln_modulate2(int act, int x_f32, const LnModJob* jobs, int njobs, int dim, float eps,
                                 cudaStream_t stream, int out_e4m3 = 0);
-// z [B, C, HW] fp32 -> tokens [B, HW, C] of the activation type.
+// z [B, C, HW] fp32 -> tokens [B, HW, C] of the activation type.  With z1 and t non-null the
+// tokens are those of (1 - t[b]) z + t[b] z1 (the rectified-flow z_t, formed while reading), also
+// written to z_t [B, C, HW] fp32 when z_t is non-null.
 cudaError_t launch_patchify(int act, const float* z, int batch, int channels, int hw, void* out,
-                            cudaStream_t stream);
+                            cudaStream_t stream, const float* z1 = nullptr, const float* t = nullptr,
+                            float* z_t = nullptr);
+// The output head's last stage with the flow-matching loss fused on: v = sum of the split-K
+// partials [splits, M, N] + bias; pred[b, n, r] = v (m = b * hw + r; skipped if pred is null);
+// with z0 non-null, loss = mean over M * N of (v - (z1 - z0))^2 (z0, z1 [B, N, hw] fp32), reduced
+// in a fixed order through loss_partials [head_finish_blocks(M, N)] and a ticket counter that must
+// be 0 on entry (the kernel leaves it 0).  N a multiple of 32.
+int head_finish_blocks(int M, int N);
+cudaError_t launch_head_finish(int act, const float* partials, int splits, int M, int N, const void* bias,
+                               int hw, float* pred, const float* z0, const float* z1,
+                               float* loss_partials, unsigned int* ticket, float* loss,
+                               cudaStream_t stream);
 // v [B, H, S, 128] bf16 -> vt [B, H, 128, seq_pad] fp16 (exact: bf16 values fit fp16 here)
 cudaError_t launch_transpose_v(const __nv_bfloat16* v, int bh, int seq, int seq_pad, __half* vt,
                                cudaStream_t stream);
@@ -229,7 +243,11 @@ cudaError_t launch_scale_update(const float* hist, float* scale, int hist_len, i
 cudaError_t launch_euler_cfg(int dtype, int64_t n, const void* z, const void* v_cond,
                              const void* v_uncond, float guidance, float dt, void* z_out,
                              cudaStream_t stream);
-// Rectified-flow noise and loss.
+// Rectified-flow noise and loss.  The loss kernel writes one partial sum per block, each block
+// covering kFlowElemsPerPartial elements (fewer blocks, with a grid-stride loop, past
+// kFlowMaxPartials); flow_partial_blocks gives that count, and launch_flow_match must be given it.
+constexpr int64_t kFlowElemsPerPartial = 256 * 8 * 4;
+constexpr int kFlowMaxPartials = 1024;
 int flow_partial_blocks(int64_t n_total);
 cudaError_t launch_flow_match(int dtype, const void* z0, const void* z1, const float* t, int batch,
                               int64_t n_per_sample, void* z_t, const void* pred, float* loss,

@@ -1,17 +1,18 @@
 // noalloc.cu -- flow_match_noise_and_loss_noalloc: the rectified-flow noise and loss for
 // callers that cannot allocate device memory.
 //
-// Some callers cannot call cudaMalloc or any allocating routine: code running while a CUDA graph
-// is being captured on a stream whose memory pool they do not own, real-time or embedded hosts
+// Some callers cannot call cudaMalloc or any allocating routine: real-time or embedded hosts
 // whose memory budget is fixed at start-up, and plug-ins living inside another framework's
 // process that must not touch its allocator.  flow_match_noise_and_loss needs a caller-provided
 // workspace for the per-block partial sums of the loss; this variant keeps them instead in the
 // file-scope device array below, so the caller passes only inputs and outputs.
 //
 // The array holds kNoAllocPartials floats (1 KiB) on every GPU that loads the library, until the
-// process exits.  One partial sum covers 8192 elements, so a call handles at most
-// kNoAllocPartials * 8192 = 2,097,152 elements (batch * n_per_sample); larger calls are rejected
-// with MMDIT_ERR_UNSUPPORTED before anything is launched.
+// process exits.  One partial sum covers kFlowElemsPerPartial = 8192 elements (the loss kernel's
+// per-block share, which the workspace entry point uses too, so both reduce in the same order),
+// and a call handles at most kNoAllocPartials * 8192 = 2,097,152 elements (batch *
+// n_per_sample); larger calls are rejected with MMDIT_ERR_UNSUPPORTED before anything is
+// launched.
 //
 // Every call on a device shares the array and leaves its last contents there.  Each call
 // rewrites all the partial sums it reads before reading them, so nothing has to start at zero,
@@ -21,7 +22,9 @@
 // The array's name is a host-side stand-in in host code, not a device address.  The first
 // call on each device, with that device current, looks the address up with
 // cudaGetSymbolAddress; that lookup is a CUDA API call, so the first call on a device should
-// come before any stream capture.
+// come before any stream capture.  The address is kept for the life of the process: a
+// cudaDeviceReset of a device invalidates it, and this entry point must not be called on that
+// device after such a reset.
 #include <mutex>
 
 #include "../../include/mmdit.h"
@@ -31,7 +34,8 @@ namespace mmdit {
 namespace {
 
 constexpr int kNoAllocPartials = 256;
-constexpr int64_t kElemsPerPartial = 8192;  // the per-block share used by the loss reduction
+constexpr int64_t kNoAllocMaxElems = kNoAllocPartials * kFlowElemsPerPartial;  // 2,097,152
+static_assert(kNoAllocPartials <= kFlowMaxPartials, "one partial per block, with no grid-stride wrap");
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_noalloc_partials[kNoAllocPartials];
@@ -76,8 +80,8 @@ extern "C" mmdit_status flow_match_noise_and_loss_noalloc(int32_t dtype, const v
     return err(MMDIT_ERR_INVALID_ARG, "flow_match_noise_and_loss_noalloc: negative size");
   if (n_per_sample % 8 != 0)
     return err(MMDIT_ERR_UNSUPPORTED, "flow_match_noise_and_loss_noalloc: n_per_sample must be a multiple of 8");
-  const int64_t n_total = static_cast<int64_t>(batch) * n_per_sample;
-  if (n_total > kNoAllocPartials * kElemsPerPartial)
+  // compared before multiplying, so that no product can overflow
+  if (batch > 0 && n_per_sample > kNoAllocMaxElems / batch)
     return err(MMDIT_ERR_UNSUPPORTED,
                "flow_match_noise_and_loss_noalloc: batch * n_per_sample exceeds the 2,097,152 "
                "elements its fixed 256-entry device scratch covers; use flow_match_noise_and_loss "
@@ -89,11 +93,15 @@ extern "C" mmdit_status flow_match_noise_and_loss_noalloc(int32_t dtype, const v
     return err(MMDIT_ERR_INVALID_ARG, "flow_match_noise_and_loss_noalloc: NULL or misaligned pointer");
   if (pred && z_t && (z_t == z0 || z_t == z1))
     return err(MMDIT_ERR_INVALID_ARG, "flow_match_noise_and_loss_noalloc: z_t may not alias z0/z1 with the loss");
+  const int64_t n_total = static_cast<int64_t>(batch) * n_per_sample;
   if (n_total == 0) return MMDIT_OK;
+  // the same count (and so the same grid and reduction order) as the workspace entry point
+  const int n_partials = flow_partial_blocks(n_total);
+  if (n_partials > kNoAllocPartials)
+    return err(MMDIT_ERR_UNSUPPORTED, "flow_match_noise_and_loss_noalloc: partial-sum count exceeds the scratch");
   float* partials = nullptr;
   cudaError_t e = noalloc_partials(&partials);
   if (e != cudaSuccess) return err(MMDIT_ERR_CUDA, cudaGetErrorString(e));
-  const int n_partials = static_cast<int>((n_total + kElemsPerPartial - 1) / kElemsPerPartial);
   pdl_begin_call();  // the first kernel waits for everything enqueued before the call
   e = launch_flow_match(dtype, z0, z1, t, batch, n_per_sample, z_t, pred, loss, partials,
                         n_partials, static_cast<cudaStream_t>(stream));

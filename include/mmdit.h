@@ -200,15 +200,16 @@ mmdit_status flow_match_noise_and_loss(int32_t dtype, const void *z0, const void
                                        void *workspace, size_t workspace_bytes, void *stream);
 
 /* flow_match_noise_and_loss without a workspace, for callers that cannot allocate device
- * memory (code running under another framework's allocator or inside a stream capture whose
- * pool it does not own, or a host whose memory is fixed at start-up).  The pages have no
- * counterpart; this is a packaging variant of the entry point above with the same results.
- * The partial sums of the loss live in a static device array of 256 floats (1 KiB) that every
- * GPU loading the library keeps until the process exits, so batch * n_per_sample may be at
- * most 2,097,152; larger calls return MMDIT_ERR_UNSUPPORTED.  Nothing is allocated.  The
- * first call on each device looks up the array's address (cudaGetSymbolAddress) and should
- * precede any stream capture.  All calls share the array: calls whose kernels overlap on the
- * GPU race, so order them on one stream. */
+ * memory (a plug-in running under another framework's allocator, or a host whose memory is
+ * fixed at start-up).  The pages have no counterpart; this is a packaging variant of the entry
+ * point above with the same results.  The partial sums of the loss live in a static device
+ * array of 256 floats (1 KiB) that every GPU loading the library keeps until the process exits,
+ * so batch * n_per_sample may be at most 2,097,152; larger calls return MMDIT_ERR_UNSUPPORTED
+ * (checked without forming the product).  Nothing is allocated.  The first call on each device
+ * looks up the array's address (cudaGetSymbolAddress) and should precede any stream capture;
+ * the address is kept for the life of the process, so after a cudaDeviceReset of a device this
+ * entry point must not be called on it again.  All calls share the array: calls whose kernels
+ * overlap on the GPU race, so order them on one stream. */
 mmdit_status flow_match_noise_and_loss_noalloc(int32_t dtype, const void *z0, const void *z1,
                                                const float *t, int32_t batch,
                                                int64_t n_per_sample, void *z_t,
@@ -246,6 +247,19 @@ mmdit_status mmdit_img_in_fwd(int32_t act, int32_t batch, int32_t channels, int3
                               const void *b, void *out, void *workspace, size_t workspace_bytes,
                               void *stream);
 
+/* img_in with the rectified-flow noise fused into its load ([ARCH] §Mathematical formulation,
+ * Flow matching objective, and §Training data flow: the noised latents enter the image
+ * embedding): the latents are z_t = (1 - t[b]) z0 + t[b] z1, formed while patchifying (the same
+ * fp32 arithmetic as flow_match_noise_and_loss, so z_t is bit-equal), then projected as
+ * mmdit_img_in_fwd projects z.
+ *   z0, z1 [B, C, H, W] fp32; t [B] fp32; w, b, out as for mmdit_img_in_fwd;
+ *   z_t: NULL, or [B, C, H, W] fp32 receiving the noised latents (may not alias z0 or z1).
+ * workspace >= mmdit_img_in_workspace_size(act, batch, channels, lat_h, lat_w). */
+mmdit_status mmdit_img_in_noise_fwd(int32_t act, int32_t batch, int32_t channels, int32_t lat_h,
+                                    int32_t lat_w, int32_t hidden, const float *z0, const float *z1,
+                                    const float *t, const void *w, const void *b, void *out,
+                                    float *z_t, void *workspace, size_t workspace_bytes, void *stream);
+
 /* Output head ([ARCH] §Model components, 5. Output processing; [API] AdaLNContinuous):
  * (shift, scale) = SiLU(vec) w_ada^T + b_ada (w_ada [2D, D]); y = (LN(x_img) * (1 + scale) +
  * shift) w_out^T + b_out (w_out [C, D]); pred [B, C, H, W] fp32 with token r*W + c at [.., r, c].
@@ -256,6 +270,45 @@ mmdit_status mmdit_final_layer_fwd(const mmdit_dims *dims, int32_t channels, int
                                    const void *w_ada, const void *b_ada, const void *w_out,
                                    const void *b_out, float *pred, void *workspace,
                                    size_t workspace_bytes, void *stream);
+
+/* Output head with the flow-matching loss fused onto its output stage ([ARCH] §Training data
+ * flow: the prediction feeds the loss; §Mathematical formulation, Flow matching objective; [API]
+ * §Training utilities, compute_flow_matching_loss): the head of mmdit_final_layer_fwd, whose last
+ * kernel also forms
+ *   loss = mean over all B * C * H * W elements of (pred - (z1 - z0))^2
+ * from the prediction while it is in registers (one fp32 scalar; partial sums per block added
+ * in a fixed order by the last block: deterministic).
+ *   z0, z1 [B, C, H, W] fp32 (the latent pair of this step); loss: device fp32 scalar;
+ *   pred: NULL, or [B, C, H, W] fp32 receiving the prediction (may not alias z0 or z1).
+ * Other arguments as mmdit_final_layer_fwd.
+ * workspace >= mmdit_final_layer_loss_workspace_size(dims, channels). */
+size_t mmdit_final_layer_loss_workspace_size(const mmdit_dims *dims, int32_t channels);
+mmdit_status mmdit_final_layer_loss_fwd(const mmdit_dims *dims, int32_t channels, int32_t lat_h,
+                                        int32_t lat_w, const void *x_img, const void *vec,
+                                        const void *w_ada, const void *b_ada, const void *w_out,
+                                        const void *b_out, const float *z0, const float *z1,
+                                        float *pred, float *loss, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * LayerNorm + modulate on its own ([ARCH] §Implementation details, Adaptive layer normalization;
+ * [API] §Normalization, AdaLN): the HBM pass the blocks run before their QKV and fc1 linears,
+ *   out[b, r, :] = LN(x[b, r, :]) * (1 + scale[b * mod_bstride + :]) + shift[b * mod_bstride + :]
+ * LN without affine, biased variance, fp32 statistics.  x [batch, rows_per_batch, dim] of type
+ * `act` (fp32 when x_f32 != 0, as the blocks' fp32 residual), out of type `act` (may not alias x);
+ * shift, scale fp32 (16-byte aligned; mod_bstride a multiple of 4 floats).  dim a multiple of 8, at
+ * most 8192.  No workspace. */
+mmdit_status mmdit_ln_modulate_fwd(int32_t act, int32_t x_f32, int32_t batch, int32_t rows_per_batch,
+                                   int32_t dim, float eps, const void *x, const float *shift,
+                                   const float *scale, int64_t mod_bstride, void *out, void *stream);
+
+/* Strided row copy for callers that join or split the image and text streams themselves (the
+ * single block reads [img; txt] per sample, the output head the image rows): for i < n_rows, copies
+ * row_bytes bytes from src + i * src_stride to dst + i * dst_stride (device memory, through the copy
+ * engine: cudaMemcpy2DAsync; no kernel).  Strides >= row_bytes; the ranges may not overlap.  Not a
+ * step of the method: layout plumbing. */
+mmdit_status mmdit_copy_rows(void *dst, int64_t dst_stride, const void *src, int64_t src_stride,
+                             int64_t row_bytes, int32_t n_rows, void *stream);
 
 /* ---------------------------------------------------------------------------------------
  * Joint softmax attention ([ARCH] §Implementation details, Attention implementation (no mask)

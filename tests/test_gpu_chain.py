@@ -1,4 +1,6 @@
-"""The 12B block shapes at 512 px as one chain, against the oracle chain on the same inputs.
+"""The benchmarked chains against the oracle on the same inputs.
+
+The 12B block shapes at 512 px as one chain (the first test below):
 
 rope3d_freqs -> rectified-flow noise z_t -> img_in -> double block -> output head ->
 flow-matching loss, batch 4, 32 x 32 x 64 latents (1024 image tokens) and 512 text tokens drawn
@@ -91,3 +93,74 @@ def test_chain_12b_blocks_at_512px():
     got = float(loss.item())
     print(f"[chain 512px] loss GPU {got:.6f}, bf16-autocast oracle {loss_ref:.6f}")
     assert abs(got - loss_ref) <= 1e-4 * loss_ref, (got, loss_ref)
+
+
+# ----------------------------------------------------------------------------- benchmarked steps
+def _bench_step(name):
+    """The benchmark's own step object (its inputs, weights and launch sequence) for a workload."""
+    import os
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    import bench
+    hw = bench.HostWorkload(synth.WORKLOADS[name])
+    return hw, bench.DeviceStep(hw, "cuda", keep_pred=True)
+
+
+def _sample_rows(n, k, seed):
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(n, size=min(k, n), replace=False))
+    return np.unique(np.concatenate([rows, [0, n - 1]]))
+
+
+@pytest.mark.parametrize("name", ["flux535m_bf16", "flux12b_1024px_bf16"])
+def test_benchmarked_step_against_the_oracle(name):
+    """The step bench.py times, run once through the C ABI, against the oracle chain on seeded
+    rows: latents -> img_in of z_t (noise fused) -> txt_in (535M-shaped) -> double block -> single
+    block -> output head with the fused loss.  The oracle runs at the bf16-autocast precision with
+    every stored tensor rounded as the GPU stores it: the embeddings and the double block in full
+    (the single block needs keys and values of every row), the single block and the head at the
+    sampled image rows (row-wise after the attention).  Bars: the block outputs and the sampled
+    predictions within 2e-2 x RMS; the loss within 1e-5 of the oracle's MSE of the GPU's own
+    prediction (the fused reduction; the loss over every element needs every prediction, which
+    the bench's own full-step oracle run compares)."""
+    hw, st = _bench_step(name)
+    wl = hw.wl
+    st.step()
+    torch.cuda.synchronize()
+    for w in st.workspaces():
+        assert L.mmdit_workspace_status(w) == 0
+    B, S_i, S_t, H, lat = wl.batch, wl.seq_img, wl.seq_txt, wl.heads, wl.lat_h
+    rb = O.round_bf16
+    mm = O.round_bf16
+    zt = O.flow_match_noise(hw.z0, hw.z1, hw.t)
+    x_img = rb(O.img_in(rb(zt), hw.img_in["w"], hw.img_in["b"], mm))
+    x_txt = rb(O.txt_in(hw.txt, hw.txt_in["w"], hw.txt_in["b"], mm)) if hw.txt_in is not None else hw.txt
+    assert_parity(host(st.x_img), x_img, 2e-2, f"{name}: img_in of z_t", out_bf16=True)
+    assert_parity(host(st.x_txt), x_txt, 2e-2, f"{name}: text tokens", out_bf16=True)
+    cos, sin = O.rope_cos_sin(hw.ids)
+    y_img, y_txt = O.double_block(x_img, x_txt, hw.vec, cos, sin, hw.w_dimg, hw.w_dtxt, H, mm_cast=mm)
+    y_img, y_txt = rb(y_img), rb(y_txt)
+    c = np.concatenate([y_img, y_txt], axis=1)
+    # the double block's output: the joint buffer at batch 1; at batch > 1 the text stream (the
+    # image stream's buffer is reused for the single block's image rows)
+    got_dbl, ref_dbl = (host(st.Y), c) if st.joint else (host(st.y_txt), y_txt)
+    e = assert_parity(got_dbl, ref_dbl, 2e-2, f"{name}: double block output", out_bf16=True)
+    print(f"[step {name}] double block max|err|/RMS = {e:.3e}")
+    rows = _sample_rows(S_i, 48, 11)
+    z_rows = rb(O.single_block_rows(c, hw.vec, cos, sin, hw.w_single, H, rows, mm_cast=mm))
+    got_single = host(st.Z if st.joint else st.C)[:, rows]
+    e = assert_parity(got_single, z_rows, 2e-2, f"{name}: single block rows", out_bf16=True)
+    print(f"[step {name}] single block (sampled rows) max|err|/RMS = {e:.3e}")
+    f = hw.final
+    # the head is row-wise: its prediction at the sampled tokens from those rows
+    pred_rows = O.final_layer(z_rows, hw.vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], len(rows), 1,
+                              mm_cast=mm)[..., 0]  # [B, C, rows]
+    got_pred = host(st.pred).reshape(B, wl.channels, S_i)[:, :, rows]
+    e = assert_parity(got_pred, pred_rows, 2e-2, f"{name}: prediction at sampled tokens")
+    print(f"[step {name}] prediction (sampled tokens) max|err|/RMS = {e:.3e}")
+    loss = float(st.loss.item())
+    own = O.flow_match_loss(host(st.pred), hw.z0, hw.z1)
+    assert abs(loss - own) <= 1e-5 * own, (loss, own)
+    print(f"[step {name}] loss {loss:.6f}; oracle MSE of the GPU prediction {own:.6f}")

@@ -144,7 +144,7 @@ def test_attention_matches_oracle(B, H, S, qscale, act):
     ws = L.mmdit_attention_fwd(dev(q), dev(k), dev(v), out)
     torch.cuda.synchronize()
     assert L.mmdit_workspace_status(ws) == 0
-    # q, k, v are bf16 already; at the bf16-autocast precision the probabilities are bf16 too
+    # q, k, v are bf16 already; the bf16-autocast oracle keeps the softmax weights exact
     rows = np.random.default_rng(0).choice(S, 200, replace=False) if S > 1000 else np.arange(S)
     ref = O.attention(q[:, :, rows], k, v, O.round_bf16).transpose(0, 2, 1, 3).reshape(B, len(rows), H * 128)
     ref64 = O.attention(q[:, :, rows], k, v).transpose(0, 2, 1, 3).reshape(B, len(rows), H * 128)
@@ -190,6 +190,94 @@ def test_final_layer_matches_oracle(act, B, Hh, Ww, D):
     cast = O.round_bf16 if act == "bf16" else None
     ref = O.final_layer(x, vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], Hh, Ww, mm_cast=cast)
     assert_parity(host(pred), ref, 2e-2, "final layer")
+
+
+@pytest.mark.parametrize("act", ["bf16", "f32"])
+@pytest.mark.parametrize("B,Hh,Ww", [(2, 10, 12), (4, 32, 32)])
+def test_img_in_noise_matches_oracle(act, B, Hh, Ww):
+    """img_in of z_t formed while patchifying: z_t bit-equal to the standalone noise pass, the
+    embedding against the oracle's img_in of the oracle's z_t."""
+    rng = np.random.default_rng(18 + B)
+    Cc, D = 64, 256
+    z0, z1 = synth.latent_pair(rng, B, Cc, Hh, Ww)
+    tt = synth.timesteps(rng, B, "logit_normal")
+    cast = "bf16" if act == "bf16" else "f32"
+    e = synth.embed_weights(rng, Cc, D, cast, std=0.1)
+    t = torch.bfloat16 if act == "bf16" else torch.float32
+    d0, d1, dt = dev(z0, torch.float32), dev(z1, torch.float32), dev(tt, torch.float32)
+    out = torch.empty(B, Hh * Ww, D, device="cuda", dtype=t)
+    zt = torch.full_like(d0, float("nan"))
+    ws = L.mmdit_img_in_noise_fwd(d0, d1, dt, dev(e["w"], t), dev(e["b"], t), out, z_t=zt)
+    zt_ref = torch.empty_like(d0)
+    L.flow_match_noise_and_loss(d0, d1, dt, z_t=zt_ref)
+    out_ref = torch.empty_like(out)
+    L.mmdit_img_in_fwd(zt_ref, dev(e["w"], t), dev(e["b"], t), out_ref)
+    torch.cuda.synchronize()
+    assert L.mmdit_workspace_status(ws) == 0
+    assert torch.equal(zt, zt_ref), "z_t differs from the standalone noise pass"
+    assert torch.equal(out, out_ref), "embedding differs from img_in of the same z_t"
+    ztr = O.flow_match_noise(z0, z1, tt)
+    assert_parity(host(zt), ztr, 1e-6, "z_t")
+    zr = synth.bf16_round(ztr.astype(np.float32)) if act == "bf16" else ztr
+    assert_parity(host(out), O.img_in(zr, e["w"], e["b"]), 2e-2, "img_in of z_t", out_bf16=act == "bf16")
+
+
+@pytest.mark.parametrize("act", ["bf16", "f32"])
+@pytest.mark.parametrize("B,Hh,Ww,D", [(2, 10, 12, 256), (1, 32, 32, 1024), (4, 32, 32, 256),
+                                       (1, 128, 128, 256)])  # split K, and the last one does not
+def test_final_layer_loss_matches_oracle(act, B, Hh, Ww, D):
+    """The output head with the loss fused on: pred equal to the plain head's, the loss within
+    1e-5 of the oracle's MSE of that pred, and pred against the oracle's head; two calls in a row
+    (the finishing kernel's ticket counter resets itself) give bit-equal losses."""
+    rng = np.random.default_rng(19 + Hh)
+    Cc = 64
+    cast = "bf16" if act == "bf16" else "f32"
+    rnd = synth.bf16_round if act == "bf16" else (lambda a: a)
+    x = rnd(rng.standard_normal((B, Hh * Ww, D)).astype(np.float32))
+    vec = rnd(rng.standard_normal((B, D)).astype(np.float32))
+    f = synth.final_layer_weights(rng, D, Cc, cast, std=0.1)
+    z0, z1 = synth.latent_pair(rng, B, Cc, Hh, Ww)
+    t = torch.bfloat16 if act == "bf16" else torch.float32
+    dims = L.make_dims(B, Hh * Ww, 0, D, D // 128, 4 * D, L.MMDIT_BF16 if act == "bf16" else L.MMDIT_F32)
+    args = (dev(x, t), dev(vec, t), dev(f["w_ada"], t), dev(f["b_ada"], t), dev(f["w_out"], t),
+            dev(f["b_out"], t))
+    d0, d1 = dev(z0, torch.float32), dev(z1, torch.float32)
+    pred = torch.full((B, Cc, Hh, Ww), float("nan"), device="cuda")
+    loss = torch.full((2,), float("nan"), device="cuda")
+    ws = L.mmdit_final_layer_loss_fwd(dims, Hh, Ww, *args, d0, d1, loss[0:1], pred=pred)
+    L.mmdit_final_layer_loss_fwd(dims, Hh, Ww, *args, d0, d1, loss[1:2], ws=ws)  # no pred written
+    pred_ref = torch.empty_like(pred)
+    L.mmdit_final_layer_fwd(dims, Hh, Ww, *args, pred_ref)
+    torch.cuda.synchronize()
+    assert L.mmdit_workspace_status(ws) == 0
+    assert torch.equal(pred, pred_ref), "pred differs from the plain output head's"
+    lv = loss.cpu().numpy()
+    assert lv[0] == lv[1], f"two calls gave {lv[0]} and {lv[1]}"
+    ref_loss = O.flow_match_loss(host(pred), z0, z1)
+    assert abs(lv[0] - ref_loss) <= 1e-5 * ref_loss, (lv[0], ref_loss)
+    mm = O.round_bf16 if act == "bf16" else None
+    ref = O.final_layer(x, vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], Hh, Ww, mm_cast=mm)
+    assert_parity(host(pred), ref, 2e-2, "final layer (loss variant)")
+    ref_loss64 = O.flow_match_loss(ref, z0, z1)
+    assert abs(lv[0] - ref_loss64) <= 1e-3 * ref_loss64, (lv[0], ref_loss64)
+
+
+@pytest.mark.parametrize("xdt,odt", [("bf16", "bf16"), ("f32", "bf16"), ("f32", "f32")])
+@pytest.mark.parametrize("B,R,D", [(2, 300, 3072), (1, 7, 8192), (3, 65, 256)])
+def test_ln_modulate_matches_oracle(xdt, odt, B, R, D):
+    rng = np.random.default_rng(B * R + D)
+    x = rng.standard_normal((B, R, D)).astype(np.float32) * 3.0 + 0.5
+    if xdt == "bf16":
+        x = synth.bf16_round(x)
+    mod = (rng.standard_normal((B, 6 * D)) * 0.3).astype(np.float32)  # [shift | scale | ...] per sample
+    gx = dev(x, torch.bfloat16 if xdt == "bf16" else torch.float32)
+    out = torch.empty(B, R, D, device="cuda", dtype=torch.bfloat16 if odt == "bf16" else torch.float32)
+    gm = dev(mod, torch.float32)
+    L.mmdit_ln_modulate_fwd(gx, gm[:, :D], gm[:, D:2 * D], out, 6 * D)
+    torch.cuda.synchronize()
+    ref = O.modulate(x, mod[:, :D], mod[:, D:2 * D])
+    tol = 2e-2 if odt == "bf16" else 1e-5
+    assert_parity(host(out), ref, tol, f"LayerNorm-modulate {xdt}->{odt}", out_bf16=odt == "bf16")
 
 
 # ----------------------------------------------------------------------------- sampling step

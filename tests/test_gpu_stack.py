@@ -7,7 +7,8 @@ through the C ABI, against the oracle on the same seeded inputs.
   equals the per-job modulation bit for bit;
 * the whole model at a small width (D 256, 2 heads, 2 double + 2 single blocks, 8 x 8 latents,
   16 text tokens), batch 1 (the streams inside the joint buffer) and batch 2 (joined by copies),
-  bf16 against the bf16-autocast oracle and fp32 against the float64 oracle, within 2e-2 x RMS;
+  bf16 against the bf16-autocast oracle over nine seeds and fp32 against the float64 oracle,
+  within 2e-2 x RMS;
 * the 12B stack at 512 px (19 double + 38 single blocks, 1024 + 512 tokens) with every gate at
   zero: the blocks pass the residual stream through, so the prediction is the output head of the
   embedded latents, which the oracle computes at full size.
@@ -118,17 +119,26 @@ def _run_model(w, z, txt, t, y, ids, shape, B, act, n_double, n_single, guidance
     return host(pred)
 
 
+# Seeds of the whole-model case: every one drawn is kept (5678 is the one that came out at
+# 2.057e-2 x RMS while the embedders' hidden layer was stored in bf16).
+MODEL_SEEDS = [(1, 61), (1, 5678), (1, 1), (1, 2), (1, 3), (1, 4), (2, 62), (2, 5), (2, 6)]
+
+
+@pytest.mark.parametrize("B,seed", MODEL_SEEDS)
+def test_small_model_matches_oracle_bf16(B, seed):
+    w, z, txt, t, y, ids, shape = _small_model(B, "bf16", seed)
+    got = _run_model(_up(w, "bf16"), z, txt, t, y, ids, shape, B, "bf16", 2, 2)
+    ref = O.flux_forward(z, txt, t, y, ids, w, shape[1], mm_cast=O.round_bf16, store=O.round_bf16)
+    e = assert_parity(got, ref, 2e-2, f"whole model bf16 B={B} seed {seed}")
+    print(f"[model] bf16 B={B} seed {seed}: max|err|/RMS vs bf16-autocast oracle = {e:.3e}")
+
+
 @pytest.mark.parametrize("B", [1, 2])
-@pytest.mark.parametrize("act", ["bf16", "f32"])
-def test_small_model_matches_oracle(B, act):
-    w, z, txt, t, y, ids, shape = _small_model(B, act, 60 + B)
-    got = _run_model(_up(w, act), z, txt, t, y, ids, shape, B, act, 2, 2)
-    H = shape[1]
-    if act == "bf16":
-        ref = O.flux_forward(z, txt, t, y, ids, w, H, mm_cast=O.round_bf16, store=O.round_bf16)
-    else:
-        ref = O.flux_forward(z, txt, t, y, ids, w, H)
-    assert_parity(got, ref, 2e-2, f"whole model {act} B={B}")
+def test_small_model_matches_oracle_f32(B):
+    w, z, txt, t, y, ids, shape = _small_model(B, "f32", 60 + B)
+    got = _run_model(_up(w, "f32"), z, txt, t, y, ids, shape, B, "f32", 2, 2)
+    ref = O.flux_forward(z, txt, t, y, ids, w, shape[1])
+    assert_parity(got, ref, 2e-2, f"whole model f32 B={B}")
 
 
 def test_small_model_without_single_blocks_and_text():

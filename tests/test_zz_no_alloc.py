@@ -1,7 +1,8 @@
 """flow_match_noise_and_loss_noalloc: the flow-matching noise and loss for callers that cannot
-allocate device memory (they run inside another framework's allocator or a stream capture they
-do not own, or on a host whose memory is fixed at start-up).  Its partial sums live in a static
-device array instead of a caller workspace; its results must equal the workspace entry point's.
+allocate device memory (a plug-in under another framework's allocator, or a host whose memory is
+fixed at start-up).  Its partial sums live in a static device array instead of a caller
+workspace; its results must equal the workspace entry point's bit for bit, and a call must not
+change the memory torch has allocated.
 
 This file is collected last so that a run stopping at the first failure has run every other
 test first.
@@ -24,6 +25,12 @@ def test_no_alloc_rejects_sizes_beyond_its_scratch():
                                                0x4000, 0x5000, None)
     assert st == 2
     assert "2,097,152" in L.last_error()
+    # a per-sample count whose product with the batch overflows int64 is rejected the same way
+    # (the limit is checked before the product is formed)
+    st = lib.flow_match_noise_and_loss_noalloc(0, 0x1000, 0x2000, 0x3000, 4, (1 << 62) + 8, None,
+                                               0x4000, 0x5000, None)
+    assert st == 2
+    assert "2,097,152" in L.last_error()
 
 
 @pytest.mark.gpu
@@ -42,9 +49,12 @@ def test_no_alloc_matches_workspace_entry_point_twice(dtype):
         zt_ref, loss_ref = torch.empty_like(d0), torch.zeros(1, device="cuda")
         L.flow_match_noise_and_loss(d0, d1, t, z_t=zt_ref, pred=pred, loss=loss_ref)
         zt, loss = torch.full_like(d0, float("nan")), torch.full((1,), float("nan"), device="cuda")
+        torch.cuda.synchronize()
+        allocated = torch.cuda.memory_allocated()
         L.flow_match_noise_and_loss_noalloc(d0, d1, t, z_t=zt, pred=pred, loss=loss)
         torch.cuda.synchronize()
-        # same kernels, same reduction order: equal results (the tests' loss bound is 1e-4 relative)
+        assert torch.cuda.memory_allocated() == allocated, "the call allocated device memory"
+        # same kernels, same grid, same reduction order: bit-equal results
         assert torch.equal(zt, zt_ref), f"call {call}: z_t differs"
-        assert abs(loss.item() - loss_ref.item()) <= 1e-4 * abs(loss_ref.item()), f"call {call}: loss"
+        assert loss.item() == loss_ref.item(), f"call {call}: loss {loss.item()} vs {loss_ref.item()}"
         assert np.isfinite(loss.item())
