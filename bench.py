@@ -138,9 +138,9 @@ class HostWorkload:
 
 
 class SideModulation:
-    """The blocks' AdaLN modulations computed on a second stream, overlapped with the work the
-    main stream does first (the embeddings, then the double block's tensor-core kernels): they
-    depend only on vec and the weights and are HBM-bound.  The blocks then read them through
+    """The blocks' AdaLN modulations computed on a second stream in one launch, overlapped with the
+    work the main stream does first (the RoPE tables and the embeddings): they depend only on vec
+    and the weights and are HBM-bound.  The blocks then read them through
     the weight sets' `mod` entries.  Fork and join are CUDA events, so the step still captures
     as one graph."""
 
@@ -158,8 +158,11 @@ class SideModulation:
         self.ev_start.record(main)
         self.side.wait_event(self.ev_start)
         with self.torch.cuda.stream(self.side):
-            for n, w in self.sets:
-                self.L.mmdit_modulation_fwd(self.vec, w["w_mod"], w["b_mod"], self.mods[n])
+            # every block's modulation in one launch (mmdit_modulation_batched_fwd): the weights
+            # stream at the HBM rate instead of one short launch per block
+            self.L.mmdit_modulation_batched_fwd(self.vec, [(w["w_mod"], w["b_mod"], self.mods[n])
+                                                           for n, w in self.sets])
+            for n, _ in self.sets:
                 self.ready[n].record(self.side)
 
     def join(self, *names):
@@ -216,7 +219,10 @@ class DeviceStep:
             self.x_img = torch.empty(B, S_i, D, device=device, dtype=bf)
             self.x_txt = torch.empty(B, S_t, D, device=device, dtype=bf)
             self.y_img, self.y_txt = torch.empty_like(self.x_img), torch.empty_like(self.x_txt)
+            # the single block's input and output, and the image rows the head reads
             self.C = torch.empty(B, S, D, device=device, dtype=bf) if hw.has_single else None
+            self.Zc = torch.empty_like(self.C) if hw.has_single else None
+            self.z_img = torch.empty_like(self.x_img) if hw.has_single else None
         if not wl.txt_from_ctx:
             self.x_txt = self.txt  # the text tokens are the block input itself
             if self.joint:
@@ -277,8 +283,9 @@ class DeviceStep:
                 self._rows(self.C, self.y_img, S_i)
                 self._rows(self.C, self.y_txt, self.S - S_i, dst_off=S_i)
                 L.mmdit_single_block_fwd(self.dims, side.weights("single", self.w_single), self.vec, self.cos,
-                                         self.sin, self.C, self.C, ws=self.ws_block)
-                self._rows(self.y_img, self.C, S_i)
+                                         self.sin, self.C, self.Zc, ws=self.ws_block)
+                self._rows(self.z_img, self.Zc, S_i)
+                head_in = self.z_img
         # output head with the flow-matching loss fused onto its last kernel
         L.mmdit_final_layer_loss_fwd(self.dims_final, wl.lat_h, wl.lat_w, head_in, self.vec,
                                      self.final["w_ada"], self.final["b_ada"], self.final["w_out"],
@@ -553,7 +560,8 @@ def kernel_work(label: str, wl):
     if label == "conditioning":  # the two embedders' weights
         return "hbm", 2.0 * (256 * D + wl.vec_dim * D + 2 * D * D), "B"
     if label == "modulation.batched":  # every block stream's 6D x D modulation weights
-        n_mod = 2 * wl.n_double + wl.n_single
+        n_mod = (2 * wl.n_double + wl.n_single if "model" in wl.blocks
+                 else 2 + (1 if "single" in wl.blocks else 0))
         return "hbm", n_mod * (6.0 * D * D * 2 + B * 6 * D * 4) + B * D * 2, "B"
     if label == "modulation":  # one block stream's 6D x D weights (mmdit_modulation_fwd)
         return "hbm", 6.0 * D * D * 2 + B * 6 * D * 4 + B * D * 2, "B"
@@ -1060,8 +1068,8 @@ def main():
                                 + ("" if wl.batch == 1 else "; streams joined and split by strided "
                                    "copy-engine copies (mmdit_copy_rows)")),
                        "streams": "one stream (the model's modulations run up front in one launch)"
-                                  if model else "the three block modulations (mmdit_modulation_fwd) on "
-                                  "a second stream, joined before each block",
+                                  if model else "the block modulations (mmdit_modulation_batched_fwd, one "
+                                  "launch) on a second stream, joined before each block",
                        "flops_counted_per_step": st.flops_blocks,
                        "dense_flops_per_step_incl_embeds_and_head": st.flops_dense},
             "pct_of_bf16_peak": round(100 * value / world / bf16_peak, 2),

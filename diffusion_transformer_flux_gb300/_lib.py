@@ -34,7 +34,8 @@ EXPORTED = [
     "mmdit_double_block_fwd", "mmdit_single_block_workspace_size", "mmdit_single_block_fwd",
     "mmdit_block_workspace_offsets", "mmdit_fp8_quantize_e4m3", "mmdit_fp8_linear_workspace_size",
     "mmdit_fp8_linear_fwd", "mmdit_single_block_parallel_fwd", "mmdit_linear_bwd_workspace_size",
-    "mmdit_linear_bwd", "mmdit_modulation_batched_fwd", "mmdit_conditioning_workspace_size",
+    "mmdit_linear_bwd", "mmdit_double_block_bwd_workspace_size", "mmdit_double_block_bwd",
+    "mmdit_single_block_bwd_workspace_size", "mmdit_single_block_bwd", "mmdit_modulation_batched_fwd", "mmdit_conditioning_workspace_size",
     "mmdit_conditioning_fwd", "mmdit_flux_workspace_size", "mmdit_flux_forward",
 ]
 
@@ -83,6 +84,13 @@ def fp8_tensor(slot: int, linear: str, operand: str) -> int:
 
 VP, SZ, I32, I64, F32 = C.c_void_p, C.c_size_t, C.c_int32, C.c_int64, C.c_float
 PDIMS, PW, PFP8 = C.POINTER(Dims), C.POINTER(StreamW), C.POINTER(Fp8State)
+
+
+class StreamGrads(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in STREAM_W_FIELDS]
+
+
+PGRADS = C.POINTER(StreamGrads)
 
 
 class GemvJob(C.Structure):
@@ -150,6 +158,11 @@ _SIGS = {
     "mmdit_single_block_parallel_fwd": (C.c_int, [PDIMS, PW, VP, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_linear_bwd_workspace_size": (SZ, [I32, I32, I32, I32]),
     "mmdit_linear_bwd": (C.c_int, [I32, I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_double_block_bwd_workspace_size": (SZ, [PDIMS]),
+    "mmdit_double_block_bwd": (C.c_int, [PDIMS, PW, PW, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, PGRADS, PGRADS,
+                                         VP, SZ, VP]),
+    "mmdit_single_block_bwd_workspace_size": (SZ, [PDIMS]),
+    "mmdit_single_block_bwd": (C.c_int, [PDIMS, PW, VP, VP, VP, VP, VP, VP, VP, PGRADS, VP, SZ, VP]),
     "mmdit_modulation_batched_fwd": (C.c_int, [I32, I32, I32, VP, I32, C.POINTER(GemvJob), VP]),
     "mmdit_conditioning_workspace_size": (SZ, [I32, I32, I32, I32]),
     "mmdit_conditioning_fwd": (C.c_int, [I32, I32, I32, I32, I32, PCOND, VP, VP, VP, VP, VP, SZ, VP]),
@@ -570,4 +583,48 @@ def mmdit_linear_bwd(dy, x, w, dx=None, dw=None, db=None, ws=None, stream=None):
         ws = workspace(mmdit_linear_bwd_workspace_size(act, M, N, K), dy.device)
     _check(load().mmdit_linear_bwd(act, M, N, K, _ptr(dy), _ptr(x), _ptr(w), _ptr(dx), _ptr(dw), _ptr(db),
                                    _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+# ----------------------------------------------------------------------------- block backward
+def make_stream_grads(g: dict | None):
+    """The C view of one stream's fp32 weight gradients (missing names: not computed)."""
+    if g is None:
+        return None
+    return StreamGrads(*[_ptr(g.get(n)) for n in STREAM_W_FIELDS])
+
+
+def mmdit_double_block_bwd_workspace_size(dims: Dims) -> int:
+    return load().mmdit_double_block_bwd_workspace_size(C.byref(dims))
+
+
+def mmdit_single_block_bwd_workspace_size(dims: Dims) -> int:
+    return load().mmdit_single_block_bwd_workspace_size(C.byref(dims))
+
+
+def mmdit_double_block_bwd(dims: Dims, w_img: dict, w_txt: dict, vec, cos, sin, x_img, x_txt, dy_img, dy_txt,
+                           dx_img, dx_txt, dvec=None, g_img=None, g_txt=None, ws=None, stream=None):
+    """Gradients of the double block (see include/mmdit.h); g_img / g_txt are dicts of fp32 tensors
+    named like the weights."""
+    if ws is None:
+        ws = workspace(mmdit_double_block_bwd_workspace_size(dims), x_img.device)
+    wi, wt = make_stream_w(w_img), make_stream_w(w_txt)
+    gi, gt = make_stream_grads(g_img), make_stream_grads(g_txt)
+    _check(load().mmdit_double_block_bwd(C.byref(dims), C.byref(wi), C.byref(wt), _ptr(vec), _ptr(cos), _ptr(sin),
+                                         _ptr(x_img), _ptr(x_txt), _ptr(dy_img), _ptr(dy_txt), _ptr(dx_img),
+                                         _ptr(dx_txt), _ptr(dvec), C.byref(gi) if gi else None,
+                                         C.byref(gt) if gt else None, _ptr(ws), ws.numel(), _stream(stream)))
+    return ws
+
+
+def mmdit_single_block_bwd(dims: Dims, w: dict, vec, cos, sin, x, dy, dx, dvec=None, g=None, ws=None,
+                           stream=None):
+    """Gradients of the single block (see include/mmdit.h)."""
+    if ws is None:
+        ws = workspace(mmdit_single_block_bwd_workspace_size(dims), x.device)
+    sw = make_stream_w(w)
+    gg = make_stream_grads(g)
+    _check(load().mmdit_single_block_bwd(C.byref(dims), C.byref(sw), _ptr(vec), _ptr(cos), _ptr(sin), _ptr(x),
+                                         _ptr(dy), _ptr(dx), _ptr(dvec), C.byref(gg) if gg else None, _ptr(ws),
+                                         ws.numel(), _stream(stream)))
     return ws

@@ -6,6 +6,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <initializer_list>
 #include <vector>
 
@@ -773,6 +774,278 @@ mmdit_status conditioning_body(int act, int B, int D, int time_dim, int vec_in_d
   return MMDIT_OK;
 }
 
+// ----------------------------------------------------------------------------- block backward
+// Scratch of one linear backward (the weight transpose, the transposed operands of dW, the bias
+// gradient's partial column sums).
+size_t linear_bwd_scratch(size_t e, size_t M, size_t N, size_t K) {
+  const size_t Mp = round_up(M, 8);
+  Carver c;
+  c.off = 0;
+  c.take(K * N * e);
+  c.take(N * Mp * e);
+  c.take(K * Mp * e);
+  c.take(static_cast<size_t>(kColsumChunks) * N * 4);
+  return c.off;
+}
+
+// dx = dy W [M, K] (activation type), dW = dy^T x [N, K] fp32, db = column sums of dy [N] fp32, each
+// skipped when its pointer is null; `scratch` holds linear_bwd_scratch bytes, `ws` the status word.
+mmdit_status linear_bwd_body(int act, int M, int N, int K, const void* dy, const void* x, const void* w, void* dx,
+                             float* dw, float* db, void* scratch, void* ws, cudaStream_t st) {
+  const size_t e = elt_bytes(act);
+  const int Mp = static_cast<int>(round_up(static_cast<size_t>(M), 8));
+  Carver c;
+  c.off = 0;
+  void* wt = at(scratch, c.take(static_cast<size_t>(K) * N * e));
+  void* dyt = at(scratch, c.take(static_cast<size_t>(N) * Mp * e));
+  void* xt = at(scratch, c.take(static_cast<size_t>(K) * Mp * e));
+  float* part = at<float>(scratch, c.take(static_cast<size_t>(kColsumChunks) * N * 4));
+  if (dx) {
+    // dx [M, K] = dy [M, N] W [N, K]: the GEMM's K-major operands are dy and W^T [K, N]
+    MMDIT_CUDA(launch_transpose_pad(act, w, N, K, N, wt, st), "W transpose");
+    GemmProblem g;
+    g.act = act, g.epi = kEpiBias, g.M = M, g.N = K, g.K = N, g.A = dy, g.W = wt, g.ep.out = dx;
+    MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "dx GEMM");
+  }
+  if (dw) {
+    // dW [N, K] = dy^T x, contracted over the M rows: operands dy^T [N, Mp] and x^T [K, Mp]
+    MMDIT_CUDA(launch_transpose_pad(act, dy, M, N, Mp, dyt, st), "dy transpose");
+    MMDIT_CUDA(launch_transpose_pad(act, x, M, K, Mp, xt, st), "x transpose");
+    GemmProblem g;
+    g.act = act, g.epi = kEpiBias, g.M = N, g.N = K, g.K = Mp, g.A = dyt, g.W = xt, g.ep.out = dw;
+    g.ep.out_f32 = 1;
+    MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "dW GEMM");
+  }
+  if (db) MMDIT_CUDA(launch_colsum(act, dy, M, N, part, kColsumChunks, db, st), "db column sums");
+  return MMDIT_OK;
+}
+
+// Workspace of a block backward: the forward's own slots first (the backward recomputes the
+// forward into them), then what the backward reads of the forward and its own gradients.
+struct BwdPlan {
+  BlockPlan f;
+  size_t h1[2], qkv_pre[2], a[2], u_pre[2], fo[2], ytmp[2];
+  size_t dx1[2], df[2], du[2], dh[2], dO[2], dqkv[2], dm[2];
+  size_t lse, dsum, doh, dot, qt, kt, v, dq, dk, dv, amax;
+  size_t part, lin;
+  size_t total;
+};
+
+bool plan_block_bwd(const mmdit_dims* d, bool single, BwdPlan* p) {
+  if (!plan_block(d, single, &p->f)) return false;
+  const BlockPlan& f = p->f;
+  const size_t B = f.B, D = f.D, F = f.F, e = f.elt, H = f.H, S = f.S, Sp = f.S_pad;
+  const int ns = single ? 1 : 2;
+  const size_t rows[2] = {B * (single ? S : static_cast<size_t>(f.Si)), single ? 0 : B * static_cast<size_t>(f.St)};
+  Carver c;
+  c.off = round_up(f.total, 256);
+  for (int s = 0; s < 2; ++s) {
+    const size_t R = s < ns ? rows[s] : 0;
+    p->h1[s] = c.take(R * D * e), p->qkv_pre[s] = c.take(R * 3 * D * e), p->a[s] = c.take(R * D * e);
+    p->u_pre[s] = c.take(R * F * e), p->fo[s] = c.take(R * D * e), p->ytmp[s] = c.take(R * D * e);
+    p->dx1[s] = c.take(R * D * 4), p->df[s] = c.take(R * D * e), p->du[s] = c.take(R * F * e);
+    p->dh[s] = c.take(R * D * e), p->dO[s] = c.take(R * D * e), p->dqkv[s] = c.take(R * 3 * D * e);
+    p->dm[s] = c.take(s < ns ? B * 6 * D * 4 : 0);
+  }
+  // L and D are read in 64-row tiles by bulk copies: 64 floats of slack past the end
+  p->lse = c.take((B * H * Sp + 64) * 4), p->dsum = c.take((B * H * Sp + 64) * 4);
+  p->doh = c.take(B * H * S * 128 * 2), p->dot = c.take(B * H * 128 * Sp * 2);
+  p->qt = c.take(B * H * 128 * Sp * 2), p->kt = c.take(B * H * 128 * Sp * 2);
+  p->v = c.take(B * H * S * 128 * 2);
+  p->dq = c.take(B * H * S * 128 * 4), p->dk = c.take(B * H * S * 128 * 4), p->dv = c.take(B * H * S * 128 * 4);
+  p->amax = c.take(256);
+  size_t part = static_cast<size_t>(qk_norm_rope_bwd_blocks()) * 2 * 128 * 4;
+  part = std::max(part, static_cast<size_t>(modulation_dvec_chunks(6 * f.D)) * B * D * 4);
+  size_t lin = 0;
+  for (int s = 0; s < ns; ++s) {
+    const int rpb = single ? f.S : (s ? f.St : f.Si);
+    part = std::max(part, ln_modulate_bwd_part_bytes(f.B, rpb, f.D));
+    part = std::max(part, gated_residual_bwd_part_bytes(f.B, rpb, f.D));
+    lin = std::max(lin, linear_bwd_scratch(e, rows[s], D, F));      // fc2
+    lin = std::max(lin, linear_bwd_scratch(e, rows[s], F, D));      // fc1
+    lin = std::max(lin, linear_bwd_scratch(e, rows[s], 3 * D, D));  // QKV
+    lin = std::max(lin, linear_bwd_scratch(e, rows[s], D, D));      // attention output projection
+  }
+  p->part = c.take(part);
+  p->lin = c.take(lin);
+  p->total = c.off;
+  return true;
+}
+
+mmdit_status plain_linear(int act, int M, int N, int K, const void* x, const void* w, const void* b, void* y,
+                          void* ws, cudaStream_t st) {
+  GemmProblem g;
+  g.act = act, g.epi = kEpiBias, g.M = M, g.N = N, g.K = K, g.A = x, g.W = w, g.ep.bias = b, g.ep.out = y;
+  MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "recomputed linear");
+  return MMDIT_OK;
+}
+
+// The backward of a double block (ns = 2: image and text streams) or a single block (ns = 1, one
+// stream over the joint rows).  The forward is recomputed into the workspace first (activation
+// recomputation: the call needs only the block's inputs), keeping what the backward reads: the
+// attention branch's LayerNorm output h1, the QKV linear before its norm, the attention output
+// and its log-sum-exp, the output projection a, the fp32 residual x1, the MLP's LayerNorm output,
+// its pre-GELU u_pre, GELU output and fc2 output.  Then, per stream, the MLP branch and the
+// attention projection backward; the joint attention backward; per stream the QK-RMSNorm + RoPE,
+// QKV and LayerNorm backward and the modulation backward.
+mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, const mmdit_stream_w* const* W,
+                            const void* vec, const float* rope_cos, const float* rope_sin, const void* const* X,
+                            const void* const* DY, void* const* DX, float* dvec,
+                            const mmdit_stream_grads* const* G, void* ws, cudaStream_t st) {
+  const BlockPlan& p = bp.f;
+  const int act = d->act, B = p.B, D = p.D, F = p.F, H = p.H, S = p.S;
+  const size_t e = p.elt;
+  const int rpb[2] = {ns == 1 ? p.S : p.Si, p.St};
+  const int off[2] = {0, p.Si};
+  const mmdit_stream_grads none = {};
+  mmdit_status s = MMDIT_OK;
+  // ---------------- forward, keeping what the backward reads
+  {
+    ModulationJob jobs[2];
+    for (int i = 0; i < ns; ++i) jobs[i] = {W[i]->w_mod, W[i]->b_mod, at<float>(ws, p.mod[i]), 6 * D};
+    ProfScope ps_("bwd.recompute.modulation", st);
+    MMDIT_CUDA(launch_modulation2(act, vec, jobs, ns, B, D, st), "modulation");
+  }
+  Streams ss;
+  ss.n = 0;
+  for (int i = 0; i < ns; ++i) {
+    if (rpb[i] == 0) continue;
+    ss.s[ss.n] = i, ss.w[ss.n] = W[i], ss.x[ss.n] = X[i], ss.y[ss.n] = at(ws, bp.ytmp[i]), ss.rpb[ss.n] = rpb[i];
+    ss.mod[ss.n] = at<float>(ws, p.mod[i]);
+    ++ss.n;
+  }
+  Fp8 no_fp8;
+  if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, no_fp8, ws, st)) != MMDIT_OK) return s;
+  for (int i = 0; i < ns; ++i) {
+    const size_t R = static_cast<size_t>(B) * rpb[i];
+    if (R == 0) continue;
+    ProfScope ps_("bwd.recompute.qkv_pre", st);
+    MMDIT_CUDA(cudaMemcpyAsync(at(ws, bp.h1[i]), at(ws, p.h[i]), R * D * e, cudaMemcpyDeviceToDevice, st), "keep h1");
+    pdl_begin_call();  // the next kernel follows a copy
+    if ((s = plain_linear(act, static_cast<int>(R), 3 * D, D, at(ws, p.h[i]), W[i]->w_qkv, W[i]->b_qkv,
+                          at(ws, bp.qkv_pre[i]), ws, st)) != MMDIT_OK)
+      return s;
+  }
+  {
+    AttnProblem a;
+    a.act = act, a.batch = B, a.heads = H, a.seq = S, a.seq_pad = p.S_pad, a.split = ns == 1 ? S : p.Si;
+    a.q = at<__nv_bfloat16>(ws, p.q), a.k = at<__nv_bfloat16>(ws, p.k), a.vt = at<__half>(ws, p.vt);
+    a.out0 = at(ws, p.o[0]), a.out1 = ns == 1 ? nullptr : at(ws, p.o[1]);
+    a.lse = at<float>(ws, bp.lse);
+    ProfScope ps_("bwd.recompute.attention", st);
+    MMDIT_CUDA(launch_attention(a, status_word(ws), st), "joint attention (with log-sum-exp)");
+  }
+  if ((s = run_post(d, p, ss, no_fp8, ws, st)) != MMDIT_OK) return s;  // x1, the MLP's h (in h), u
+  for (int i = 0; i < ns; ++i) {
+    const int R = B * rpb[i];
+    if (R == 0) continue;
+    ProfScope ps_("bwd.recompute.linears", st);
+    if ((s = plain_linear(act, R, D, D, at(ws, p.o[i]), W[i]->w_o, W[i]->b_o, at(ws, bp.a[i]), ws, st)) != MMDIT_OK)
+      return s;
+    if ((s = plain_linear(act, R, F, D, at(ws, p.h[i]), W[i]->w_1, W[i]->b_1, at(ws, bp.u_pre[i]), ws, st)) !=
+        MMDIT_OK)
+      return s;
+    if ((s = plain_linear(act, R, D, F, at(ws, p.u[i]), W[i]->w_2, W[i]->b_2, at(ws, bp.fo[i]), ws, st)) != MMDIT_OK)
+      return s;
+  }
+  // ---------------- backward: MLP branch and the attention projection, per stream
+  float* part = at<float>(ws, bp.part);
+  void* lin = at(ws, bp.lin);
+  const int64_t bstr = 6 * static_cast<int64_t>(D);
+  for (int i = 0; i < ns; ++i) {
+    const int R = B * rpb[i];
+    const mmdit_stream_grads* g = G[i] ? G[i] : &none;
+    float* dm = at<float>(ws, bp.dm[i]);
+    if (R == 0) continue;  // (the entry points reject streams without rows)
+    const float* mod = at<float>(ws, p.mod[i]);
+    float* dx1 = at<float>(ws, bp.dx1[i]);
+    ProfScope ps_("bwd.mlp_and_out_proj", st);
+    MMDIT_CUDA(launch_convert(act, 1, DY[i], static_cast<int64_t>(R) * D, dx1, st), "dy to fp32");
+    MMDIT_CUDA(launch_gated_residual_bwd(act, dx1, at(ws, bp.fo[i]), mod + 5 * D, bstr, B, rpb[i], D,
+                                         at(ws, bp.df[i]), dm + 5 * D, part, st), "gate2 backward");
+    if ((s = linear_bwd_body(act, R, D, F, at(ws, bp.df[i]), at(ws, p.u[i]), W[i]->w_2, at(ws, bp.du[i]), g->w_2,
+                             g->b_2, lin, ws, st)) != MMDIT_OK)
+      return s;
+    MMDIT_CUDA(launch_gelu_bwd(act, at(ws, bp.du[i]), at(ws, bp.u_pre[i]), static_cast<int64_t>(R) * F,
+                               d->gelu_tanh, at(ws, bp.du[i]), st), "GELU backward");
+    if ((s = linear_bwd_body(act, R, F, D, at(ws, bp.du[i]), at(ws, p.h[i]), W[i]->w_1, at(ws, bp.dh[i]), g->w_1,
+                             g->b_1, lin, ws, st)) != MMDIT_OK)
+      return s;
+    MMDIT_CUDA(launch_ln_modulate_bwd(act, 1, at(ws, p.x1[i]), at(ws, bp.dh[i]), mod + 4 * D, bstr, B, rpb[i], D,
+                                      d->ln_eps, dx1, dm + 4 * D, dm + 3 * D, 0, part, st), "LN2 backward");
+    MMDIT_CUDA(launch_gated_residual_bwd(act, dx1, at(ws, bp.a[i]), mod + 2 * D, bstr, B, rpb[i], D,
+                                         at(ws, bp.df[i]), dm + 2 * D, part, st), "gate1 backward");
+    if ((s = linear_bwd_body(act, R, D, D, at(ws, bp.df[i]), at(ws, p.o[i]), W[i]->w_o, at(ws, bp.dO[i]), g->w_o,
+                             g->b_o, lin, ws, st)) != MMDIT_OK)
+      return s;
+  }
+  // ---------------- the joint attention backward
+  const int bh = B * H;
+  float* amax = at<float>(ws, bp.amax);
+  {
+    ProfScope ps_("bwd.attention_prepass", st);
+    bool first = true;
+    for (int i = 0; i < ns; ++i) {
+      if (rpb[i] == 0) continue;
+      MMDIT_CUDA(launch_grad_amax(at<__nv_bfloat16>(ws, bp.dO[i]), static_cast<int64_t>(B) * rpb[i] * D, amax,
+                                  first, st), "dO amax");
+      first = false;
+    }
+    for (int i = 0; i < ns; ++i)
+      MMDIT_CUDA(launch_attn_bwd_pre(at<__nv_bfloat16>(ws, p.o[i]), at<__nv_bfloat16>(ws, bp.dO[i]), B, rpb[i], S,
+                                     p.S_pad, off[i], H, amax, at<float>(ws, bp.dsum),
+                                     at<__nv_bfloat16>(ws, bp.doh), st), "attention pre-pass");
+    MMDIT_CUDA(launch_transpose_v(at<__nv_bfloat16>(ws, p.k), bh, S, p.S_pad, at<__half>(ws, bp.kt), st), "K^T");
+    MMDIT_CUDA(launch_transpose_v(at<__nv_bfloat16>(ws, p.q), bh, S, p.S_pad, at<__half>(ws, bp.qt), st), "Q^T");
+    MMDIT_CUDA(launch_transpose_v(at<__nv_bfloat16>(ws, bp.doh), bh, S, p.S_pad, at<__half>(ws, bp.dot), st),
+               "dO^T");
+    MMDIT_CUDA(launch_untranspose_vt(at<__half>(ws, p.vt), bh, S, p.S_pad, at<__nv_bfloat16>(ws, bp.v), st), "V");
+  }
+  {
+    AttnBwdProblem a;
+    a.batch = B, a.heads = H, a.seq = S, a.seq_pad = p.S_pad;
+    a.q = at<__nv_bfloat16>(ws, p.q), a.k = at<__nv_bfloat16>(ws, p.k), a.v = at<__nv_bfloat16>(ws, bp.v);
+    a.dout = at<__nv_bfloat16>(ws, bp.doh);
+    a.kt = at<__half>(ws, bp.kt), a.qt = at<__half>(ws, bp.qt), a.dout_t = at<__half>(ws, bp.dot);
+    a.lse = at<float>(ws, bp.lse), a.dsum = at<float>(ws, bp.dsum);
+    a.dq = at<float>(ws, bp.dq), a.dk = at<float>(ws, bp.dk), a.dv = at<float>(ws, bp.dv);
+    ProfScope ps_("bwd.attention", st);
+    MMDIT_CUDA(launch_attention_bwd(a, status_word(ws), st), "attention backward");
+  }
+  // ---------------- QK-RMSNorm + RoPE, QKV and LayerNorm backward, the modulation, per stream
+  bool dvec_written = false;
+  for (int i = 0; i < ns; ++i) {
+    const int R = B * rpb[i];
+    const mmdit_stream_grads* g = G[i] ? G[i] : &none;
+    float* dm = at<float>(ws, bp.dm[i]);
+    const float* mod = at<float>(ws, p.mod[i]);
+    float* dx1 = at<float>(ws, bp.dx1[i]);
+    ProfScope ps_("bwd.qkv_and_ln1", st);
+    if (R > 0) {
+      QkBwdArgs q;
+      q.qkv_pre = at(ws, bp.qkv_pre[i]), q.g_q = W[i]->g_q, q.g_k = W[i]->g_k;
+      q.cos = rope_cos, q.sin = rope_sin;
+      q.dq = at(ws, bp.dq), q.dk = at(ws, bp.dk), q.dv = at(ws, bp.dv), q.dqkv = at(ws, bp.dqkv[i]);
+      q.part = part, q.amax = amax;
+      q.batch = B, q.seq_s = rpb[i], q.seq_joint = S, q.seq_offset = off[i], q.heads = H, q.hidden = D;
+      q.interleaved = d->rope_interleaved ? 1 : 0, q.eps = d->rms_eps;
+      MMDIT_CUDA(launch_qk_norm_rope_bwd(act, q, g->g_q, g->g_k, st), "QK-RMSNorm + RoPE backward");
+      if ((s = linear_bwd_body(act, R, 3 * D, D, at(ws, bp.dqkv[i]), at(ws, bp.h1[i]), W[i]->w_qkv,
+                               at(ws, bp.dh[i]), g->w_qkv, g->b_qkv, lin, ws, st)) != MMDIT_OK)
+        return s;
+      MMDIT_CUDA(launch_ln_modulate_bwd(act, 0, X[i], at(ws, bp.dh[i]), mod + D, bstr, B, rpb[i], D, d->ln_eps,
+                                        dx1, dm + D, dm, 0, part, st),
+                 "LN1 backward");
+    }
+    MMDIT_CUDA(launch_modulation_bwd(act, vec, W[i]->w_mod, dm, B, 6 * D, D, g->w_mod, g->b_mod, dvec,
+                                     dvec_written ? 1 : 0, part, st),
+               "modulation backward");
+    dvec_written = dvec_written || dvec != nullptr;
+    if (R > 0) MMDIT_CUDA(launch_convert(act, 0, dx1, static_cast<int64_t>(R) * D, DX[i], st), "dx to the activation type");
+  }
+  return MMDIT_OK;
+}
+
 // Workspace of the whole-model forward: one region that every step in turn uses from its start
 // (status word first), then the model's own tensors.
 struct FluxPlan {
@@ -1117,8 +1390,11 @@ mmdit_status mmdit_final_layer_loss_fwd(const mmdit_dims* d, int32_t channels, i
     return fail(MMDIT_ERR_INVALID_ARG, "final layer + loss: seq_img must equal lat_h * lat_w");
   if (channels < 32 || channels % 32 != 0 || d->hidden % 256 != 0)
     return fail(MMDIT_ERR_UNSUPPORTED, "final layer + loss: channels multiple of 32, hidden of 256");
-  mmdit_status s = check_ptrs({x_img, vec, w_ada, b_ada, w_out, b_out, z0, z1, loss}, "final layer + loss");
+  mmdit_status s = check_ptrs({x_img, vec, w_ada, b_ada, w_out, b_out, z0, z1}, "final layer + loss");
   if (s != MMDIT_OK) return s;
+  // the loss is one fp32 scalar: its own alignment is enough
+  if (!loss || (reinterpret_cast<uintptr_t>(loss) & 3u))
+    return fail(MMDIT_ERR_INVALID_ARG, "final layer + loss: loss is NULL or not 4-byte aligned");
   if (pred && (s = check_ptrs({pred}, "final layer + loss: pred")) != MMDIT_OK) return s;
   if (pred && (pred == z0 || pred == z1))
     return fail(MMDIT_ERR_INVALID_ARG, "final layer + loss: pred may not alias z0 or z1");
@@ -1382,32 +1658,8 @@ mmdit_status mmdit_linear_bwd(int32_t act, int32_t M, int32_t N, int32_t K, cons
     return MMDIT_OK;
   }
   pdl_begin_call();
-  const size_t e = elt_bytes(act);
-  const int Mp = static_cast<int>(round_up(static_cast<size_t>(M), 8));
-  Carver c;
-  void* wt = at(workspace, c.take(static_cast<size_t>(K) * N * e));
-  void* dyt = at(workspace, c.take(static_cast<size_t>(N) * Mp * e));
-  void* xt = at(workspace, c.take(static_cast<size_t>(K) * Mp * e));
-  float* part = at<float>(workspace, c.take(static_cast<size_t>(kColsumChunks) * N * 4));
   ProfScope ps_("linear_bwd", st);
-  if (dx) {
-    // dx [M, K] = dy [M, N] W [N, K]: the GEMM's K-major operands are dy and W^T [K, N]
-    MMDIT_CUDA(launch_transpose_pad(act, w, N, K, N, wt, st), "W transpose");
-    GemmProblem g;
-    g.act = act, g.epi = kEpiBias, g.M = M, g.N = K, g.K = N, g.A = dy, g.W = wt, g.ep.out = dx;
-    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "dx GEMM");
-  }
-  if (dw) {
-    // dW [N, K] = dy^T x, contracted over the M rows: operands dy^T [N, Mp] and x^T [K, Mp]
-    MMDIT_CUDA(launch_transpose_pad(act, dy, M, N, Mp, dyt, st), "dy transpose");
-    MMDIT_CUDA(launch_transpose_pad(act, x, M, K, Mp, xt, st), "x transpose");
-    GemmProblem g;
-    g.act = act, g.epi = kEpiBias, g.M = N, g.N = K, g.K = Mp, g.A = dyt, g.W = xt, g.ep.out = dw;
-    g.ep.out_f32 = 1;
-    MMDIT_CUDA(launch_gemm(g, status_word(workspace), st), "dW GEMM");
-  }
-  if (db) MMDIT_CUDA(launch_colsum(act, dy, M, N, part, kColsumChunks, db, st), "db column sums");
-  return MMDIT_OK;
+  return linear_bwd_body(act, M, N, K, dy, x, w, dx, dw, db, at(workspace, kStatusBytes), workspace, st);
 }
 
 size_t mmdit_conditioning_workspace_size(int32_t act, int32_t batch, int32_t hidden, int32_t time_dim) {
@@ -1438,6 +1690,99 @@ mmdit_status mmdit_conditioning_fwd(int32_t act, int32_t batch, int32_t hidden, 
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
   pdl_begin_call();
   return conditioning_body(act, batch, hidden, time_dim, vec_in_dim, w, t, y, guidance, vec, workspace, st);
+}
+
+static mmdit_status check_block_bwd(const mmdit_dims* d, bool single) {
+  mmdit_status s = check_dims(d);
+  if (s != MMDIT_OK) return s;
+  if (d->act != MMDIT_BF16) return fail(MMDIT_ERR_UNSUPPORTED, "block backward: bf16 activations only");
+  if (d->gemm != MMDIT_GEMM_NATIVE) return fail(MMDIT_ERR_UNSUPPORTED, "block backward: native (bf16) linears only");
+  if (d->batch > 8) return fail(MMDIT_ERR_UNSUPPORTED, "block backward: batch must be at most 8 (got %d)", d->batch);
+  if (!single && (d->seq_img < 1 || d->seq_txt < 1))
+    return fail(MMDIT_ERR_UNSUPPORTED, "double block backward: both streams need rows (S_i=%d, S_t=%d)", d->seq_img,
+                d->seq_txt);
+  if (d->mlp_hidden % 32 != 0) return fail(MMDIT_ERR_UNSUPPORTED, "block backward: mlp_hidden must be a multiple of 32");
+  return MMDIT_OK;
+}
+
+static mmdit_status check_grads(const mmdit_stream_grads* g, const char* what) {
+  if (!g) return MMDIT_OK;
+  const float* p[12] = {g->w_mod, g->b_mod, g->w_qkv, g->b_qkv, g->g_q, g->g_k, g->w_o, g->b_o, g->w_1, g->b_1,
+                        g->w_2, g->b_2};
+  for (int i = 0; i < 12; ++i)
+    if (p[i] && !aligned16(p[i])) return fail(MMDIT_ERR_INVALID_ARG, "%s: gradient %d is not 16-byte aligned", what, i);
+  return MMDIT_OK;
+}
+
+size_t mmdit_double_block_bwd_workspace_size(const mmdit_dims* d) {
+  BwdPlan p;
+  if (check_dims(d) != MMDIT_OK || !plan_block_bwd(d, false, &p)) return 0;
+  return p.total;
+}
+
+size_t mmdit_single_block_bwd_workspace_size(const mmdit_dims* d) {
+  BwdPlan p;
+  if (check_dims(d) != MMDIT_OK || !plan_block_bwd(d, true, &p)) return 0;
+  return p.total;
+}
+
+mmdit_status mmdit_double_block_bwd(const mmdit_dims* d, const mmdit_stream_w* w_img, const mmdit_stream_w* w_txt,
+                                    const void* vec, const float* rope_cos, const float* rope_sin, const void* x_img,
+                                    const void* x_txt, const void* dy_img, const void* dy_txt, void* dx_img,
+                                    void* dx_txt, float* dvec, const mmdit_stream_grads* g_img,
+                                    const mmdit_stream_grads* g_txt, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  mmdit_status s = check_block_bwd(d, false);
+  if (s != MMDIT_OK) return s;
+  if ((s = check_stream_w(w_img, "image weights")) != MMDIT_OK || (s = check_stream_w(w_txt, "text weights")) != MMDIT_OK)
+    return s;
+  if ((s = check_ptrs({vec, rope_cos, rope_sin, x_img, x_txt, dy_img, dy_txt, dx_img, dx_txt},
+                      "double block backward")) != MMDIT_OK)
+    return s;
+  if (dvec && !aligned16(dvec)) return fail(MMDIT_ERR_INVALID_ARG, "dvec is not 16-byte aligned");
+  if ((s = check_grads(g_img, "image gradients")) != MMDIT_OK || (s = check_grads(g_txt, "text gradients")) != MMDIT_OK)
+    return s;
+  BwdPlan p;
+  plan_block_bwd(d, false, &p);
+  if ((s = check_workspace(workspace, workspace_bytes, p.total)) != MMDIT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
+  // the forward's modulation is recomputed from the weights (a precomputed `mod` is not used)
+  mmdit_stream_w wi = *w_img, wt = *w_txt;
+  wi.mod = nullptr, wt.mod = nullptr;
+  const mmdit_stream_w* W[2] = {&wi, &wt};
+  const void* X[2] = {x_img, x_txt};
+  const void* DY[2] = {dy_img, dy_txt};
+  void* DX[2] = {dx_img, dx_txt};
+  const mmdit_stream_grads* G[2] = {g_img, g_txt};
+  return block_bwd_body(d, p, 2, W, vec, rope_cos, rope_sin, X, DY, DX, dvec, G, workspace, st);
+}
+
+mmdit_status mmdit_single_block_bwd(const mmdit_dims* d, const mmdit_stream_w* w, const void* vec,
+                                    const float* rope_cos, const float* rope_sin, const void* x, const void* dy,
+                                    void* dx, float* dvec, const mmdit_stream_grads* g, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  mmdit_status s = check_block_bwd(d, true);
+  if (s != MMDIT_OK) return s;
+  if ((s = check_stream_w(w, "single block weights")) != MMDIT_OK) return s;
+  if ((s = check_ptrs({vec, rope_cos, rope_sin, x, dy, dx}, "single block backward")) != MMDIT_OK) return s;
+  if (dvec && !aligned16(dvec)) return fail(MMDIT_ERR_INVALID_ARG, "dvec is not 16-byte aligned");
+  if ((s = check_grads(g, "single block gradients")) != MMDIT_OK) return s;
+  BwdPlan p;
+  plan_block_bwd(d, true, &p);
+  if ((s = check_workspace(workspace, workspace_bytes, p.total)) != MMDIT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
+  mmdit_stream_w w1 = *w;
+  w1.mod = nullptr;
+  const mmdit_stream_w* W[1] = {&w1};
+  const void* X[1] = {x};
+  const void* DY[1] = {dy};
+  void* DX[1] = {dx};
+  const mmdit_stream_grads* G[1] = {g};
+  return block_bwd_body(d, p, 1, W, vec, rope_cos, rope_sin, X, DY, DX, dvec, G, workspace, st);
 }
 
 mmdit_status mmdit_modulation_batched_fwd(int32_t act, int32_t batch, int32_t dim, const void* vec,

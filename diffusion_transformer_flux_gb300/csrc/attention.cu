@@ -68,7 +68,7 @@ __device__ __forceinline__ uint8_t* v_tile(uint8_t* smem, int st) {
 template <typename OutT>
 __device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t tmem, int q0, int bh,
                                              int heads, int seq, int split, int n_kv, OutT* out0,
-                                             OutT* out1, uint32_t* status) {
+                                             OutT* out1, float* lse, int lse_stride, uint32_t* status) {
   volatile int* abort_flag = &sb->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
@@ -175,6 +175,10 @@ __device__ __forceinline__ void softmax_role(AttnBarriers* sb, int X, uint32_t t
   tc_fence_after();
   const int s_row = q0 + X * kQTile + row;
   const float inv_l = 1.f / l_run;
+  // training forward: the row's log-sum-exp in log2 units of the scaled scores, so that the
+  // backward recomputes P = exp2(s log2(e) / sqrt(d) - L) (m_run and l_run agree however lazily
+  // the maximum moved)
+  if (lse && s_row < seq) lse[static_cast<size_t>(bh) * lse_stride + s_row] = m_run + log2f(l_run);
   OutT* dst = nullptr;
   if (s_row < seq) {
     const int b = bh / heads, hh = bh % heads;
@@ -199,7 +203,7 @@ template <typename OutT>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_vt, int heads, int seq, int split,
-                     OutT* out0, OutT* out1, uint32_t* status) {
+                     OutT* out0, OutT* out1, float* lse, int lse_stride, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -350,7 +354,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
     }
   } else if (warp >= 4) {
-    softmax_role<OutT>(sb, (warp - 4) >> 2, tmem, q0, bh, heads, seq, split, n_kv, out0, out1, status);
+    softmax_role<OutT>(sb, (warp - 4) >> 2, tmem, q0, bh, heads, seq, split, n_kv, out0, out1, lse,
+                       lse_stride, status);
   }
 
   __syncthreads();
@@ -394,12 +399,12 @@ cudaError_t launch_attention(const AttnProblem& p, uint32_t* status, cudaStream_
   if (p.act == 1) {
     const cudaError_t e_ = launch_pdl(attention_kernel<__nv_bfloat16>, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream,
         tq, tk, tv, p.heads, p.seq, p.split, static_cast<__nv_bfloat16*>(p.out0),
-        static_cast<__nv_bfloat16*>(p.out1), status);
+        static_cast<__nv_bfloat16*>(p.out1), p.lse, p.seq_pad, status);
     if (e_ != cudaSuccess) return e_;
   } else {
     const cudaError_t e_ = launch_pdl(attention_kernel<float>, dim3(grid), dim3(kAttnThreads), kAttnSmem, stream,
         tq, tk, tv, p.heads, p.seq, p.split, static_cast<float*>(p.out0), static_cast<float*>(p.out1),
-        status);
+        p.lse, p.seq_pad, status);
     if (e_ != cudaSuccess) return e_;
   }
   count_launch();

@@ -135,8 +135,81 @@ struct AttnProblem {
   const __half* vt = nullptr;         // [B, H, 128, seq_pad] fp16 (bf16-rounded values)
   void* out0 = nullptr;
   void* out1 = nullptr;
+  // training forward: each row's log-sum-exp of the scaled scores in log2 units,
+  // L = log2 sum_t exp2(q . k_t log2(e) / sqrt(d)), at lse[(b * H + h) * seq_pad + s]; or null
+  float* lse = nullptr;
 };
 cudaError_t launch_attention(const AttnProblem& p, uint32_t* status, cudaStream_t stream);
+
+// attention_bwd.cu: the joint attention's backward from the forward's log-sum-exp L and the
+// pre-pass's D = rowsum(dO * O): dV = P^T dO, dS = P (dO V^T - D) / sqrt(d), dK = dS^T Q, dQ = dS K,
+// P = exp2(q . k log2(e) / sqrt(d) - L).  dO (and so D and every output) carries the pre-pass's
+// power-of-two gradient scale.
+struct AttnBwdProblem {
+  int batch = 0, heads = 0, seq = 0, seq_pad = 0;
+  const __nv_bfloat16 *q = nullptr, *k = nullptr, *v = nullptr, *dout = nullptr;  // [B, H, S, 128]
+  const __half *kt = nullptr, *qt = nullptr, *dout_t = nullptr;  // [B, H, 128, S_pad] fp16
+  const float *lse = nullptr, *dsum = nullptr;  // [B, H, S_pad] (+ 64 floats of slack)
+  float *dq = nullptr, *dk = nullptr, *dv = nullptr;  // [B, H, S, 128] fp32; dq zeroed by the launcher
+};
+cudaError_t launch_attention_bwd(const AttnBwdProblem& p, uint32_t* status, cudaStream_t stream);
+
+// backward.cu: the row-wise steps of the block backward.
+// QK-RMSNorm + RoPE backward of one stream.  q_pre, k_pre are columns [0, D) and [D, 2D) of
+// qkv_pre [B, S_s, 3D] (the QKV linear's output with bias, before the norm); dq, dk, dv are the
+// attention backward's fp32 [B, H, S_joint, 128] at joint rows seq_offset + s, scaled by the
+// gradient scale of `amax` (null: 1); dqkv [B, S_s, 3D] receives dq_pre | dk_pre | dv unscaled.
+struct QkBwdArgs {
+  const void* qkv_pre = nullptr;
+  const void* g_q = nullptr;  // [128] activation type
+  const void* g_k = nullptr;
+  const float* cos = nullptr;  // [B, S_joint, 64]
+  const float* sin = nullptr;
+  const void* dq = nullptr;
+  const void* dk = nullptr;
+  const void* dv = nullptr;
+  void* dqkv = nullptr;
+  float* part = nullptr;  // [qk_norm_rope_bwd_blocks(), 2, 128]
+  const float* amax = nullptr;
+  int batch = 0, seq_s = 0, seq_joint = 0, seq_offset = 0, heads = 0, hidden = 0, interleaved = 1;
+  float eps = 1e-6f;
+};
+// h = LN(x)(1 + scale) + shift: dx (fp32) += the input gradient; dscale, dshift (per batch at
+// b * mod_bstride; = or += with accumulate) through part (ln_modulate_bwd_part_bytes).
+size_t ln_modulate_bwd_part_bytes(int batch, int rows_per_batch, int dim);
+cudaError_t launch_ln_modulate_bwd(int act, int x_f32, const void* x, const void* dh, const float* scale,
+                                   int64_t mod_bstride, int batch, int rows_per_batch, int dim, float eps,
+                                   float* dx, float* dscale, float* dshift, int accumulate, float* part,
+                                   cudaStream_t stream);
+// y = x + gate f: df = dy gate (activation type), dgate (per batch, written) through part.
+size_t gated_residual_bwd_part_bytes(int batch, int rows_per_batch, int dim);
+cudaError_t launch_gated_residual_bwd(int act, const float* dy, const void* f, const float* gate,
+                                      int64_t gate_bstride, int batch, int rows_per_batch, int dim,
+                                      void* df, float* dgate, float* part, cudaStream_t stream);
+// out = du GELU'(u_pre) (out may alias du).
+cudaError_t launch_gelu_bwd(int act, const void* du, const void* u_pre, int64_t n, int tanh_form, void* out,
+                            cudaStream_t stream);
+int qk_norm_rope_bwd_blocks();
+cudaError_t launch_qk_norm_rope_bwd(int act, const QkBwdArgs& a, float* dg_q, float* dg_k, cudaStream_t stream);
+// amax[0] = max(amax[0], max |x|) (amax zeroed first when zero_first).
+cudaError_t launch_grad_amax(const __nv_bfloat16* x, int64_t n, float* amax, bool zero_first, cudaStream_t stream);
+// D[b, h, seq_offset + s] = g rowsum(dO O) and dOh = g dO head-major [B, H, S_joint, 128], with g
+// the gradient scale of amax(dO).
+cudaError_t launch_attn_bwd_pre(const __nv_bfloat16* o, const __nv_bfloat16* dout, int batch, int seq_s,
+                                int seq_joint, int seq_pad, int seq_offset, int heads, const float* amax,
+                                float* Dsum, __nv_bfloat16* doh, cudaStream_t stream);
+// V [BH, S, 128] bf16 from V^T [BH, 128, S_pad] fp16 (holding bf16 values: exact).
+cudaError_t launch_untranspose_vt(const __half* vt, int bh, int seq, int seq_pad, __nv_bfloat16* v,
+                                  cudaStream_t stream);
+// m = SiLU(vec) W^T + b: dW [rows, dim] and db [rows] fp32 (written; either may be null) and dvec
+// [batch, dim] fp32 (= or += with accumulate) through part (modulation_dvec_chunks(rows) * batch *
+// dim floats).  batch <= 8.
+int modulation_dvec_chunks(int rows);
+cudaError_t launch_modulation_bwd(int act, const void* vec, const void* w, const float* dm, int batch, int rows,
+                                  int dim, float* dw, float* db, float* dvec, int accumulate, float* part,
+                                  cudaStream_t stream);
+// dst = src between the activation type and fp32 (to_f32 = 1: activation type -> fp32).
+cudaError_t launch_convert(int act, int to_f32, const void* src, int64_t n, void* dst, cudaStream_t stream);
 
 // elementwise.cu
 cudaError_t launch_rope3d(const float* ids, int batch, int seq, const int axes[3], float theta,

@@ -278,7 +278,8 @@ mmdit_status mmdit_final_layer_fwd(const mmdit_dims *dims, int32_t channels, int
  *   loss = mean over all B * C * H * W elements of (pred - (z1 - z0))^2
  * from the prediction while it is in registers (one fp32 scalar; partial sums per block added
  * in a fixed order by the last block: deterministic).
- *   z0, z1 [B, C, H, W] fp32 (the latent pair of this step); loss: device fp32 scalar;
+ *   z0, z1 [B, C, H, W] fp32 (the latent pair of this step); loss: device fp32 scalar (4-byte
+ *   aligned);
  *   pred: NULL, or [B, C, H, W] fp32 receiving the prediction (may not alias z0 or z1).
  * Other arguments as mmdit_final_layer_fwd.
  * workspace >= mmdit_final_layer_loss_workspace_size(dims, channels). */
@@ -418,6 +419,49 @@ size_t mmdit_linear_bwd_workspace_size(int32_t act, int32_t M, int32_t N, int32_
 mmdit_status mmdit_linear_bwd(int32_t act, int32_t M, int32_t N, int32_t K, const void *dy, const void *x,
                               const void *w, void *dx, float *dw, float *db, void *workspace,
                               size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Block backward (the pages train these blocks: [ARCH] §Training data flow, and §Performance
+ * optimizations, 5. Mixed precision, which calls loss.backward(); they print no backward, so
+ * each gradient is the chain rule of the forward step it belongs to).
+ * Given the block's inputs and dy (the gradient of the loss with respect to its outputs), a call
+ * recomputes the forward (activation recomputation: nothing has to be kept from a forward call)
+ * and writes
+ *   dx   the gradient with respect to each input stream (type `act`; may not alias x or dy),
+ *   dvec [B, D] fp32 (NULL: not computed) with respect to the conditioning vector,
+ *   and, for each non-NULL member of a stream's mmdit_stream_grads, the fp32 gradient of that
+ *   weight (same shape as the weight; written, not accumulated; NULL struct: none).
+ * The attention backward recomputes its probabilities from the forward's row log-sum-exp
+ * (flash style) and runs on the tensor cores with fp16 operands under a power-of-two gradient
+ * scale; every reduction over rows (weight, bias, gain and modulation gradients) is a fixed-order
+ * sum, so results are deterministic except dQ's atomic accumulation order in the attention
+ * backward (fp32 additions).
+ * Supported: act = MMDIT_BF16, gemm = MMDIT_GEMM_NATIVE, batch <= 8, mlp_hidden % 32 == 0; the
+ * double block needs both streams non-empty.  A precomputed `mod` in the weights is ignored.
+ * Arguments otherwise as for the forward entry points. */
+typedef struct mmdit_stream_grads {
+  float *w_mod, *b_mod;
+  float *w_qkv, *b_qkv;
+  float *g_q, *g_k;
+  float *w_o, *b_o;
+  float *w_1, *b_1;
+  float *w_2, *b_2;
+} mmdit_stream_grads;
+size_t mmdit_double_block_bwd_workspace_size(const mmdit_dims *dims);
+mmdit_status mmdit_double_block_bwd(const mmdit_dims *dims, const mmdit_stream_w *w_img,
+                                    const mmdit_stream_w *w_txt, const void *vec,
+                                    const float *rope_cos, const float *rope_sin,
+                                    const void *x_img, const void *x_txt, const void *dy_img,
+                                    const void *dy_txt, void *dx_img, void *dx_txt, float *dvec,
+                                    const mmdit_stream_grads *g_img,
+                                    const mmdit_stream_grads *g_txt, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+size_t mmdit_single_block_bwd_workspace_size(const mmdit_dims *dims);
+mmdit_status mmdit_single_block_bwd(const mmdit_dims *dims, const mmdit_stream_w *w,
+                                    const void *vec, const float *rope_cos,
+                                    const float *rope_sin, const void *x, const void *dy,
+                                    void *dx, float *dvec, const mmdit_stream_grads *g,
+                                    void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------------------
  * Many modulations in one launch: the AdaLN modulation of mmdit_modulation_fwd for every job

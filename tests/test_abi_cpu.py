@@ -248,6 +248,7 @@ def test_linear_bwd_embedding_head_and_modulation_validation(lib):
     assert fl(C.byref(d), 48, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 64, 80, 256, 1 << 30, None) == 2
     assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, None, 48, 64, 80, 256, 1 << 30, None) == 1
     assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 64, None, 256, 1 << 30, None) == 1
+    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 64, 82, 256, 1 << 30, None) == 1
     assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 32, 80, 256, 1 << 30, None) == 1
     assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 0x1004, 80, 256, 1 << 30, None) == 1
     need = L.mmdit_final_layer_loss_workspace_size(d, 64)
@@ -266,6 +267,35 @@ def test_linear_bwd_embedding_head_and_modulation_validation(lib):
     assert lib.mmdit_modulation_fwd(1, -1, 6 * 3072, 3072, 16, 16, 16, 16, None) == 1
     assert lib.mmdit_modulation_fwd(1, 1, 6 * 3072, 3072, None, 16, 16, 16, None) == 1
     assert lib.mmdit_modulation_fwd(1, 0, 6 * 3072, 3072, None, None, None, None, None) == 0
+
+
+def test_block_backward_rejects_bad_arguments_before_any_cuda_call(lib):
+    d = _dims(seq_img=256, seq_txt=45, hidden=256, heads=2, mlp_hidden=1024)
+    need = L.mmdit_double_block_bwd_workspace_size(d)
+    assert need > L.mmdit_double_block_workspace_size(d)
+    assert L.mmdit_single_block_bwd_workspace_size(d) > 0
+    w = L.StreamW(*([16] * 12), None)
+    bad_w = L.StreamW(*([16] * 11 + [0x1004]), None)
+    g_bad = L.StreamGrads(*([None] * 6 + [0x1004] + [None] * 5))
+    ptrs = [16] * 9  # vec, cos, sin, x_img, x_txt, dy_img, dy_txt, dx_img, dx_txt
+    db = lib.mmdit_double_block_bwd
+
+    def call(dims=d, wi=w, wt=w, p=ptrs, dvec=None, gi=None, gt=None, ws=256, nbytes=1 << 40):
+        return db(C.byref(dims), C.byref(wi), C.byref(wt), *p, dvec, gi, gt, ws, nbytes, None)
+
+    assert call(dims=_dims(seq_img=256, seq_txt=45, hidden=256, heads=2, mlp_hidden=1024, act=L.MMDIT_F32)) == 2
+    assert call(dims=_dims(seq_img=256, seq_txt=0, hidden=256, heads=2, mlp_hidden=1024)) == 2
+    assert call(dims=_dims(batch=9, seq_img=256, seq_txt=45, hidden=256, heads=2, mlp_hidden=1024)) == 2
+    assert call(dims=_dims(seq_img=256, seq_txt=45, hidden=256, heads=2, mlp_hidden=1024, gemm=1)) == 2
+    assert call(wi=bad_w) == 1
+    assert call(p=[16] * 8 + [None]) == 1
+    assert call(dvec=0x1004) == 1
+    assert call(gi=C.byref(g_bad)) == 1
+    assert "gradient 6" in L.last_error()
+    assert call(nbytes=need - 1) == 3
+    sb = lib.mmdit_single_block_bwd
+    assert sb(C.byref(d), C.byref(w), 16, 16, 16, 16, 16, None, None, None, 256, 1 << 40, None) == 1
+    assert sb(C.byref(d), C.byref(w), 16, 16, 16, 16, 16, 16, None, None, 256, 16, None) == 3
 
 
 def test_binding_refuses_host_tensors():

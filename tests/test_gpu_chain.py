@@ -116,51 +116,61 @@ def _sample_rows(n, k, seed):
 
 @pytest.mark.parametrize("name", ["flux535m_bf16", "flux12b_1024px_bf16"])
 def test_benchmarked_step_against_the_oracle(name):
-    """The step bench.py times, run once through the C ABI, against the oracle chain on seeded
-    rows: latents -> img_in of z_t (noise fused) -> txt_in (535M-shaped) -> double block -> single
-    block -> output head with the fused loss.  The oracle runs at the bf16-autocast precision with
-    every stored tensor rounded as the GPU stores it: the embeddings and the double block in full
-    (the single block needs keys and values of every row), the single block and the head at the
-    sampled image rows (row-wise after the attention).  Bars: the block outputs and the sampled
-    predictions within 2e-2 x RMS; the loss within 1e-5 of the oracle's MSE of the GPU's own
-    prediction (the fused reduction; the loss over every element needs every prediction, which
-    the bench's own full-step oracle run compares)."""
+    """The step bench.py times, run once through the C ABI: latents -> img_in of z_t (noise fused)
+    -> text tokens (txt_in for the 535M-shaped workload) -> double block -> single block -> output
+    head with the fused loss.
+
+    Stage by stage, each stage's oracle is fed the GPU's own output of the stage before (so every
+    stage is held to the bar of its own row, 2e-2 x RMS at the bf16-autocast precision): the
+    embeddings; the double block in full; the single block at seeded image rows (its keys and
+    values need every row of its input); the output head's prediction at those tokens (row-wise).
+    The loss is held to 1e-5 of the oracle's MSE of the GPU's prediction (the fused reduction).
+    End to end, the prediction at the sampled tokens is held to 2e-2 x RMS against the oracle
+    chain that starts from the latents and the text alone.  (The block outputs themselves are not
+    compared end to end: a one-ulp bf16 difference in a block's input passes straight through its
+    residual, so chained block outputs differ by more than one block's bar.)"""
     hw, st = _bench_step(name)
     wl = hw.wl
     st.step()
     torch.cuda.synchronize()
     for w in st.workspaces():
         assert L.mmdit_workspace_status(w) == 0
-    B, S_i, S_t, H, lat = wl.batch, wl.seq_img, wl.seq_txt, wl.heads, wl.lat_h
-    rb = O.round_bf16
-    mm = O.round_bf16
+    B, S_i, H = wl.batch, wl.seq_img, wl.heads
+    rb = mm = O.round_bf16
+    f = hw.final
     zt = O.flow_match_noise(hw.z0, hw.z1, hw.t)
     x_img = rb(O.img_in(rb(zt), hw.img_in["w"], hw.img_in["b"], mm))
     x_txt = rb(O.txt_in(hw.txt, hw.txt_in["w"], hw.txt_in["b"], mm)) if hw.txt_in is not None else hw.txt
-    assert_parity(host(st.x_img), x_img, 2e-2, f"{name}: img_in of z_t", out_bf16=True)
-    assert_parity(host(st.x_txt), x_txt, 2e-2, f"{name}: text tokens", out_bf16=True)
+    g_xi, g_xt = host(st.x_img), host(st.x_txt)
+    assert_parity(g_xi, x_img, 2e-2, f"{name}: img_in of z_t", out_bf16=True)
+    assert_parity(g_xt, x_txt, 2e-2, f"{name}: text tokens", out_bf16=True)
     cos, sin = O.rope_cos_sin(hw.ids)
-    y_img, y_txt = O.double_block(x_img, x_txt, hw.vec, cos, sin, hw.w_dimg, hw.w_dtxt, H, mm_cast=mm)
-    y_img, y_txt = rb(y_img), rb(y_txt)
-    c = np.concatenate([y_img, y_txt], axis=1)
-    # the double block's output: the joint buffer at batch 1; at batch > 1 the text stream (the
-    # image stream's buffer is reused for the single block's image rows)
-    got_dbl, ref_dbl = (host(st.Y), c) if st.joint else (host(st.y_txt), y_txt)
-    e = assert_parity(got_dbl, ref_dbl, 2e-2, f"{name}: double block output", out_bf16=True)
-    print(f"[step {name}] double block max|err|/RMS = {e:.3e}")
+    # the double block on the GPU's embeddings
+    y_img, y_txt = O.double_block(g_xi, g_xt, hw.vec, cos, sin, hw.w_dimg, hw.w_dtxt, H, mm_cast=mm)
+    g_c = host(st.Y) if st.joint else host(st.C)   # [y_img; y_txt] as the GPU holds it
+    e = assert_parity(g_c, np.concatenate([y_img, y_txt], axis=1), 2e-2, f"{name}: double block output",
+                      out_bf16=True)
+    print(f"[step {name}] double block (GPU inputs) max|err|/RMS = {e:.3e}")
+    # the single block at sampled image rows, on the GPU's double-block output
     rows = _sample_rows(S_i, 48, 11)
-    z_rows = rb(O.single_block_rows(c, hw.vec, cos, sin, hw.w_single, H, rows, mm_cast=mm))
-    got_single = host(st.Z if st.joint else st.C)[:, rows]
-    e = assert_parity(got_single, z_rows, 2e-2, f"{name}: single block rows", out_bf16=True)
-    print(f"[step {name}] single block (sampled rows) max|err|/RMS = {e:.3e}")
-    f = hw.final
-    # the head is row-wise: its prediction at the sampled tokens from those rows
-    pred_rows = O.final_layer(z_rows, hw.vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], len(rows), 1,
-                              mm_cast=mm)[..., 0]  # [B, C, rows]
+    z_rows = O.single_block_rows(g_c, hw.vec, cos, sin, hw.w_single, H, rows, mm_cast=mm)
+    g_z = host(st.Z if st.joint else st.Zc)[:, rows]
+    e = assert_parity(g_z, z_rows, 2e-2, f"{name}: single block rows", out_bf16=True)
+    print(f"[step {name}] single block (GPU inputs, sampled rows) max|err|/RMS = {e:.3e}")
+    # the head at the sampled tokens, on the GPU's single-block rows
     got_pred = host(st.pred).reshape(B, wl.channels, S_i)[:, :, rows]
-    e = assert_parity(got_pred, pred_rows, 2e-2, f"{name}: prediction at sampled tokens")
-    print(f"[step {name}] prediction (sampled tokens) max|err|/RMS = {e:.3e}")
+    pred_rows = O.final_layer(g_z, hw.vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], len(rows), 1,
+                              mm_cast=mm)[..., 0]
+    e = assert_parity(got_pred, pred_rows, 2e-2, f"{name}: prediction (GPU inputs)")
+    print(f"[step {name}] prediction (GPU inputs, sampled tokens) max|err|/RMS = {e:.3e}")
     loss = float(st.loss.item())
     own = O.flow_match_loss(host(st.pred), hw.z0, hw.z1)
     assert abs(loss - own) <= 1e-5 * own, (loss, own)
-    print(f"[step {name}] loss {loss:.6f}; oracle MSE of the GPU prediction {own:.6f}")
+    # end to end: the oracle's own chain from the latents and text to the sampled predictions
+    c64 = np.concatenate([rb(O.double_block(x_img, x_txt, hw.vec, cos, sin, hw.w_dimg, hw.w_dtxt, H,
+                                            mm_cast=mm)[k]) for k in (0, 1)], axis=1)
+    z64 = rb(O.single_block_rows(c64, hw.vec, cos, sin, hw.w_single, H, rows, mm_cast=mm))
+    pred64 = O.final_layer(z64, hw.vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], len(rows), 1,
+                           mm_cast=mm)[..., 0]
+    e = assert_parity(got_pred, pred64, 2e-2, f"{name}: prediction end to end")
+    print(f"[step {name}] prediction end to end max|err|/RMS = {e:.3e}; loss {loss:.6f}")
