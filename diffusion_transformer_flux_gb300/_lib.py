@@ -74,6 +74,7 @@ AMAX_MAX = 1
 
 MMDIT_GEMM_NATIVE = 0
 MMDIT_GEMM_FP8_E4M3 = 1
+MMDIT_GEMM_FP8_TENSORWISE = 2
 FP8_LINEARS = ("qkv", "o", "fc1", "fc2")
 
 
@@ -108,7 +109,8 @@ class CondW(C.Structure):
 
 class FluxConfig(C.Structure):
     _fields_ = [("block", Dims), ("n_double", I32), ("n_single", I32), ("lat_h", I32), ("lat_w", I32),
-                ("channels", I32), ("txt_dim", I32), ("time_dim", I32), ("vec_in_dim", I32)]
+                ("channels", I32), ("txt_dim", I32), ("time_dim", I32), ("vec_in_dim", I32),
+                ("single_parallel", I32)]
 
 
 class FluxW(C.Structure):
@@ -526,8 +528,9 @@ def mmdit_conditioning_fwd(t, y, w: dict, vec, guidance=None, time_dim=256, ws=N
 
 
 def make_flux_config(dims: Dims, n_double, n_single, lat_h, lat_w, channels=64, txt_dim=4096,
-                     time_dim=256, vec_in_dim=768) -> FluxConfig:
-    return FluxConfig(dims, n_double, n_single, lat_h, lat_w, channels, txt_dim, time_dim, vec_in_dim)
+                     time_dim=256, vec_in_dim=768, single_parallel=False) -> FluxConfig:
+    return FluxConfig(dims, n_double, n_single, lat_h, lat_w, channels, txt_dim, time_dim, vec_in_dim,
+                      int(bool(single_parallel)))
 
 
 def make_flux_w(w: dict) -> FluxW:

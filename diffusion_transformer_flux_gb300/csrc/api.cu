@@ -200,10 +200,11 @@ struct BlockPlan {
   int mod_chunks = 6;     // modulation chunks per stream: 6, or 3 (shift, scale, gate) when parallel
   bool fp8;  // E4M3 linears: h, u hold E4M3 codes; o8 and wq hold the cast attention output
              // and weights
+  bool fp8_current = false;  // tensorwise (current) scaling: inputs staged in bf16 before their cast
   int B, Si, St, S, S_pad, D, H, F;
   size_t elt;
   size_t mod[2], h[2], q, k, vt, o[2], x1[2], u[2];
-  size_t o8[2], wq[2];
+  size_t o8[2], wq[2], stage[2];
   size_t total;
   // byte offsets of the four weights inside a stream's wq slot
   size_t wq_qkv() const { return 0; }
@@ -221,7 +222,8 @@ static bool plan_block(const mmdit_dims* d, bool single, BlockPlan* p) {
   p->S_pad = static_cast<int>(round_up(static_cast<size_t>(p->S), 8));
   p->D = d->hidden, p->H = d->heads, p->F = d->mlp_hidden;
   p->elt = elt_bytes(d->act);
-  p->fp8 = d->gemm == MMDIT_GEMM_FP8_E4M3;
+  p->fp8 = d->gemm == MMDIT_GEMM_FP8_E4M3 || d->gemm == MMDIT_GEMM_FP8_TENSORWISE;
+  p->fp8_current = d->gemm == MMDIT_GEMM_FP8_TENSORWISE;
   const size_t mm_elt = p->fp8 ? 1 : p->elt;  // inputs of the QKV and fc1/fc2 linears
   Carver c;
   const size_t B = p->B, D = p->D, F = p->F, S = p->S;
@@ -239,6 +241,9 @@ static bool plan_block(const mmdit_dims* d, bool single, BlockPlan* p) {
   for (int s = 0; s < 2; ++s) p->u[s] = s < ns ? c.take(rows[s] * F * mm_elt) : 0;
   for (int s = 0; s < 2; ++s) p->o8[s] = p->fp8 && s < ns ? c.take(rows[s] * D) : 0;
   for (int s = 0; s < 2; ++s) p->wq[s] = p->fp8 && s < ns ? c.take(p->wq_bytes()) : 0;
+  // tensorwise: a linear's bf16 input (LayerNorm-modulate output or GELU output) before its cast
+  for (int s = 0; s < 2; ++s)
+    p->stage[s] = p->fp8_current && s < ns ? c.take(rows[s] * (F > D ? F : D) * 2) : 0;
   p->total = c.off;
   return true;
 }
@@ -250,11 +255,11 @@ static mmdit_status check_dims(const mmdit_dims* d) {
                 d->seq_img, d->seq_txt);
   if (d->act != MMDIT_F32 && d->act != MMDIT_BF16)
     return fail(MMDIT_ERR_INVALID_ARG, "act must be MMDIT_F32 or MMDIT_BF16 (got %d)", d->act);
-  if (d->gemm != MMDIT_GEMM_NATIVE && d->gemm != MMDIT_GEMM_FP8_E4M3)
+  if (d->gemm != MMDIT_GEMM_NATIVE && d->gemm != MMDIT_GEMM_FP8_E4M3 && d->gemm != MMDIT_GEMM_FP8_TENSORWISE)
     return fail(MMDIT_ERR_INVALID_ARG, "unknown gemm mode %d", d->gemm);
-  if (d->gemm == MMDIT_GEMM_FP8_E4M3 && d->act != MMDIT_BF16)
+  if (d->gemm != MMDIT_GEMM_NATIVE && d->act != MMDIT_BF16)
     return fail(MMDIT_ERR_UNSUPPORTED, "FP8 E4M3 linears need bf16 activations (act = MMDIT_BF16)");
-  if (d->gemm == MMDIT_GEMM_FP8_E4M3 && d->mlp_hidden % 128 != 0)
+  if (d->gemm != MMDIT_GEMM_NATIVE && d->mlp_hidden % 128 != 0)
     return fail(MMDIT_ERR_UNSUPPORTED, "FP8 E4M3 linears need mlp_hidden %% 128 == 0 (got %d)",
                 d->mlp_hidden);
   if (d->head_dim != 128)
@@ -307,8 +312,8 @@ constexpr int kFp8TensorsPerStream = 8;
 inline int fp8_tensor(int slot, int g, int operand) { return kFp8TensorsPerStream * slot + 2 * g + operand; }
 
 static mmdit_status check_fp8(const mmdit_dims* d, const mmdit_fp8_state* f, int n_needed) {
-  if (d->gemm != MMDIT_GEMM_FP8_E4M3) {
-    if (f) return fail(MMDIT_ERR_INVALID_ARG, "fp8 state given but gemm mode is not MMDIT_GEMM_FP8_E4M3");
+  if (d->gemm == MMDIT_GEMM_NATIVE) {
+    if (f) return fail(MMDIT_ERR_INVALID_ARG, "fp8 state given but the gemm mode is native");
     return MMDIT_OK;
   }
   if (!f) return fail(MMDIT_ERR_INVALID_ARG, "FP8 linears need an fp8 state (got NULL)");
@@ -381,9 +386,25 @@ struct Streams {
 // tensor's scale is read and where this call records its amax.
 struct Fp8 {
   const mmdit_fp8_state* f = nullptr;
+  bool current = false;  // tensorwise: every scale from the tensor's own amax in this call
+  int n_tensors = 0;     // tensors this block records (16 double, 8 single)
   const float* scale(int t) const { return f->scale + t; }
   float* amax(int t) const { return f->amax_history + static_cast<size_t>(t) * f->hist_len + f->pos; }
 };
+
+// Current (tensorwise) scaling of bf16 tensors about to be cast: record each one's amax (a first
+// pass that casts nothing), turn the recorded amax into scales (448 / amax / 2^margin), then cast
+// with them.  The cast records the same amax again.
+mmdit_status fp8_cast_current(const Fp8& f8, const QuantJob* jobs, int n, cudaStream_t st, const char* what) {
+  QuantJob amax_only[kQuantMaxJobs];
+  for (int i = 0; i < n; ++i) amax_only[i] = jobs[i], amax_only[i].dst = nullptr;
+  MMDIT_CUDA(launch_quantize_e4m3(amax_only, n, st), what);
+  MMDIT_CUDA(launch_scale_update(f8.f->amax_history, f8.f->scale, f8.f->hist_len, f8.n_tensors, f8.f->pos,
+                                 f8.f->margin, 0, st),
+             what);
+  MMDIT_CUDA(launch_quantize_e4m3(jobs, n, st), what);
+  return MMDIT_OK;
+}
 
 void add_problem(GemmProblem& g, int i, int M, const void* A, const void* W, const EpiArgs& ep) {
   if (i == 0)
@@ -399,16 +420,29 @@ mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss,
     LnModJob jobs[2];
     for (int i = 0; i < ss.n; ++i) {
       const float* mod = ss.mod[i];
-      jobs[i] = {ss.x[i], mod, mod + p.D, static_cast<int64_t>(p.mod_chunks) * p.D, at(ws, p.h[ss.s[i]]),
+      // tensorwise: the bf16 output is staged, then cast once its amax is known
+      void* out = f8.current ? at(ws, p.stage[ss.s[i]]) : at(ws, p.h[ss.s[i]]);
+      jobs[i] = {ss.x[i], mod, mod + p.D, static_cast<int64_t>(p.mod_chunks) * p.D, out,
                  p.B * ss.rpb[i], ss.rpb[i]};
-      if (f8.f) {
+      if (f8.f && !f8.current) {
         const int t = fp8_tensor(ss.s[i], 0, 0);
         jobs[i].q_scale = f8.scale(t), jobs[i].q_amax = f8.amax(t);
       }
     }
     MMDIT_CUDA(launch_ln_modulate2(d->act, d->act == MMDIT_F32, jobs, ss.n, p.D, d->ln_eps, st,
-                                   f8.f ? 1 : 0),
+                                   f8.f && !f8.current ? 1 : 0),
                "LayerNorm-modulate (attention branch)");
+  }
+  if (f8.current) {
+    ProfScope ps_(p.single ? "single.fp8_cast_h1" : "double.fp8_cast_h1", st);
+    QuantJob q[2];
+    for (int i = 0; i < ss.n; ++i) {
+      const int t = fp8_tensor(ss.s[i], 0, 0);
+      q[i] = {at<__nv_bfloat16>(ws, p.stage[ss.s[i]]), at<uint8_t>(ws, p.h[ss.s[i]]),
+              static_cast<int64_t>(p.B) * ss.rpb[i] * p.D, f8.scale(t), f8.amax(t)};
+    }
+    mmdit_status s = fp8_cast_current(f8, q, ss.n, st, "E4M3 cast of the QKV input (current scaling)");
+    if (s != MMDIT_OK) return s;
   }
   GemmProblem g;
   g.act = f8.f ? 2 : d->act, g.epi = kEpiQkv, g.N = 3 * p.D, g.K = p.D;
@@ -458,7 +492,12 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
       jobs[i] = {at<__nv_bfloat16>(ws, p.o[ss.s[i]]), at<uint8_t>(ws, p.o8[ss.s[i]]),
                  static_cast<int64_t>(p.B) * ss.rpb[i] * p.D, f8.scale(t), f8.amax(t)};
     }
-    MMDIT_CUDA(launch_quantize_e4m3(jobs, ss.n, st), "E4M3 cast of the attention output");
+    if (f8.current) {
+      mmdit_status s = fp8_cast_current(f8, jobs, ss.n, st, "E4M3 cast of the attention output (current scaling)");
+      if (s != MMDIT_OK) return s;
+    } else {
+      MMDIT_CUDA(launch_quantize_e4m3(jobs, ss.n, st), "E4M3 cast of the attention output");
+    }
   }
   GemmProblem g;
   g.act = mm, g.epi = kEpiGateResid, g.N = p.D, g.K = p.D;
@@ -481,23 +520,36 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
     LnModJob jobs[2];
     for (int i = 0; i < ss.n; ++i) {
       const float* mod = ss.mod[i];
-      jobs[i] = {at(ws, p.x1[ss.s[i]]), mod + 3 * p.D, mod + 4 * p.D, 6 * p.D, at(ws, p.h[ss.s[i]]),
+      void* out = f8.current ? at(ws, p.stage[ss.s[i]]) : at(ws, p.h[ss.s[i]]);
+      jobs[i] = {at(ws, p.x1[ss.s[i]]), mod + 3 * p.D, mod + 4 * p.D, 6 * p.D, out,
                  p.B * ss.rpb[i], ss.rpb[i]};
-      if (f8.f) {
+      if (f8.f && !f8.current) {
         const int t = fp8_tensor(ss.s[i], 2, 0);
         jobs[i].q_scale = f8.scale(t), jobs[i].q_amax = f8.amax(t);
       }
     }
-    MMDIT_CUDA(launch_ln_modulate2(d->act, 1, jobs, ss.n, p.D, d->ln_eps, st, f8.f ? 1 : 0),
+    MMDIT_CUDA(launch_ln_modulate2(d->act, 1, jobs, ss.n, p.D, d->ln_eps, st, f8.f && !f8.current ? 1 : 0),
                "LayerNorm-modulate (MLP branch)");
   }
+  if (f8.current && !p.parallel) {
+    ProfScope ps_(p.single ? "single.fp8_cast_h2" : "double.fp8_cast_h2", st);
+    QuantJob q[2];
+    for (int i = 0; i < ss.n; ++i) {
+      const int t = fp8_tensor(ss.s[i], 2, 0);
+      q[i] = {at<__nv_bfloat16>(ws, p.stage[ss.s[i]]), at<uint8_t>(ws, p.h[ss.s[i]]),
+              static_cast<int64_t>(p.B) * ss.rpb[i] * p.D, f8.scale(t), f8.amax(t)};
+    }
+    mmdit_status s = fp8_cast_current(f8, q, ss.n, st, "E4M3 cast of the fc1 input (current scaling)");
+    if (s != MMDIT_OK) return s;
+  }
   GemmProblem f1;
-  f1.act = mm, f1.epi = f8.f ? kEpiGeluF8 : kEpiGelu, f1.N = p.F, f1.K = p.D;
+  f1.act = mm, f1.epi = f8.f && !f8.current ? kEpiGeluF8 : kEpiGelu, f1.N = p.F, f1.K = p.D;
   for (int i = 0; i < ss.n; ++i) {
     EpiArgs e;
-    e.bias = ss.w[i]->b_1, e.gelu_tanh = d->gelu_tanh, e.out = at(ws, p.u[ss.s[i]]);
+    e.bias = ss.w[i]->b_1, e.gelu_tanh = d->gelu_tanh;
+    e.out = f8.current ? at(ws, p.stage[ss.s[i]]) : at(ws, p.u[ss.s[i]]);
     dequant(e, i, 2);
-    if (f8.f) {
+    if (f8.f && !f8.current) {
       const int t = fp8_tensor(ss.s[i], 3, 0);  // GELU output = the input of fc2
       e.out_scale = f8.scale(t), e.out_amax = f8.amax(t);
     }
@@ -506,6 +558,17 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
   {
     ProfScope ps_(p.single ? "single.fc1" : "double.fc1", st);
     MMDIT_CUDA(launch_gemm(f1, status_word(ws), st), "MLP fc1 + GELU");
+  }
+  if (f8.current) {
+    ProfScope ps_(p.single ? "single.fp8_cast_u" : "double.fp8_cast_u", st);
+    QuantJob q[2];
+    for (int i = 0; i < ss.n; ++i) {
+      const int t = fp8_tensor(ss.s[i], 3, 0);
+      q[i] = {at<__nv_bfloat16>(ws, p.stage[ss.s[i]]), at<uint8_t>(ws, p.u[ss.s[i]]),
+              static_cast<int64_t>(p.B) * ss.rpb[i] * p.F, f8.scale(t), f8.amax(t)};
+    }
+    mmdit_status s = fp8_cast_current(f8, q, ss.n, st, "E4M3 cast of the fc2 input (current scaling)");
+    if (s != MMDIT_OK) return s;
   }
   GemmProblem f2;
   f2.act = mm, f2.epi = kEpiGateResid, f2.N = p.D, f2.K = p.F;
@@ -547,6 +610,7 @@ mmdit_status fp8_begin(const BlockPlan& p, const Streams& ss, const Fp8& f8, int
                    f8.scale(t), f8.amax(t)};
     }
   }
+  if (f8.current) return fp8_cast_current(f8, jobs, n, st, "E4M3 cast of the weights (current scaling)");
   MMDIT_CUDA(launch_quantize_e4m3(jobs, n, st), "E4M3 cast of the weights");
   return MMDIT_OK;
 }
@@ -555,7 +619,7 @@ mmdit_status fp8_begin(const BlockPlan& p, const Streams& ss, const Fp8& f8, int
 mmdit_status fp8_end(const BlockPlan& p, const Fp8& f8, int n_tensors, cudaStream_t st) {
   ProfScope ps_(p.single ? "single.fp8_scale" : "double.fp8_scale", st);
   MMDIT_CUDA(launch_scale_update(f8.f->amax_history, f8.f->scale, f8.f->hist_len, n_tensors, f8.f->pos,
-                                 f8.f->margin, f8.f->amax_compute_algo, st),
+                                 f8.f->margin, f8.current ? 0 : f8.f->amax_compute_algo, st),
              "FP8 scale update");
   return MMDIT_OK;
 }
@@ -610,6 +674,7 @@ mmdit_status double_block_body(const mmdit_dims* d, const BlockPlan& p, const mm
   Fp8 f8;
   f8.f = fp8;
   const int n_tensors = 2 * kFp8TensorsPerStream;
+  f8.current = p.fp8_current, f8.n_tensors = n_tensors;
   if (fp8 && (s = fp8_begin(p, ss, f8, n_tensors, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, f8, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
@@ -633,6 +698,7 @@ mmdit_status single_block_body(const mmdit_dims* d, const BlockPlan& p, const mm
   ss.mod[0] = w->mod ? w->mod : at<float>(workspace, p.mod[0]);
   Fp8 f8;
   f8.f = fp8;
+  f8.current = p.fp8_current, f8.n_tensors = kFp8TensorsPerStream;
   if (fp8 && (s = fp8_begin(p, ss, f8, kFp8TensorsPerStream, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, f8, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
@@ -1061,6 +1127,7 @@ bool plan_flux(const mmdit_flux_config* cfg, FluxPlan* f) {
   size_t region = conditioning_workspace(d->act, B, D, cfg->time_dim);
   auto grow = [&](size_t x) { region = x > region ? x : region; };
   if (!plan_block(d, false, &f->dbl) || !plan_block(d, true, &f->sgl)) return false;
+  if (cfg->single_parallel) f->sgl.parallel = true, f->sgl.mod_chunks = 3;
   if (cfg->n_double > 0) grow(f->dbl.total);
   if (cfg->n_single > 0) grow(f->sgl.total);
   grow(mmdit_final_layer_workspace_size(d, cfg->channels));
@@ -1093,6 +1160,8 @@ mmdit_status check_flux(const mmdit_flux_config* cfg) {
     return fail(MMDIT_ERR_UNSUPPORTED, "whole-model forward: native GEMMs only (FP8 runs per block)");
   if (d->batch < 1 || d->seq_img < 1) return fail(MMDIT_ERR_INVALID_ARG, "whole-model forward: empty batch or image");
   if (cfg->n_double < 0 || cfg->n_single < 0) return fail(MMDIT_ERR_INVALID_ARG, "negative block count");
+  if (cfg->single_parallel != 0 && cfg->single_parallel != 1)
+    return fail(MMDIT_ERR_INVALID_ARG, "single_parallel must be 0 or 1");
   if (cfg->lat_h < 1 || cfg->lat_w < 1 || d->seq_img != cfg->lat_h * cfg->lat_w)
     return fail(MMDIT_ERR_INVALID_ARG, "seq_img must equal lat_h * lat_w");
   if (cfg->channels < 32 || cfg->channels % 32 != 0)
@@ -1871,7 +1940,7 @@ mmdit_status mmdit_flux_forward(const mmdit_flux_config* cfg, const mmdit_flux_w
     ws1[i] = w->single[i];
     float* m = mods + (2 * static_cast<size_t>(cfg->n_double) + i) * mod_stride;
     ws1[i].mod = m;
-    jobs.push_back({ws1[i].w_mod, ws1[i].b_mod, m, 6 * D});
+    jobs.push_back({ws1[i].w_mod, ws1[i].b_mod, m, (cfg->single_parallel ? 3 : 6) * D});
   }
   if (!jobs.empty()) {
     ProfScope ps_("modulation.batched", st);

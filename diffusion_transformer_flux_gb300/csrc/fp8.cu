@@ -2,7 +2,8 @@
 // §Configuration, FP8 model configuration: E4M3, amax history 1024, most_recent, margin 0).
 //
 //   quantize_e4m3_kernel   bf16 -> E4M3 codes of x * scale, recording max |x| (one launch casts
-//                          up to eight tensors, e.g. every weight of a block)
+//                          up to eight tensors, e.g. every weight of a block); a job without a
+//                          destination records max |x| only (the first pass of current scaling)
 //   amax_reset_kernel      zeroes the history slot a call is about to record into
 //   scale_update_kernel    scale = 448 / amax / 2^margin, amax of that slot (most_recent) or the
 //                          largest in the history (max), where amax > 0
@@ -34,7 +35,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_e4m3_kernel(const __grid_c
     while (j + 1 < jobs.njobs && t >= jobs.tile_start[j + 1]) ++j;
     const QuantJob& q = jobs.j[j];
     const int64_t base = (t - jobs.tile_start[j]) * kQTile;
-    const float s = __ldg(q.scale);
+    const float s = q.dst ? __ldg(q.scale) : 1.f;
     uint4 raw[kQRounds][2];
 #pragma unroll
     for (int r = 0; r < kQRounds; ++r) {
@@ -61,8 +62,10 @@ __global__ void __launch_bounds__(kQThreads) quantize_e4m3_kernel(const __grid_c
         }
 #pragma unroll
         for (int e = 0; e < 16; ++e) mx = fmaxf(mx, fabsf(v[e]));
-        const uint2 a = e4m3x8(v, s), b = e4m3x8(v + 8, s);
-        *reinterpret_cast<uint4*>(q.dst + i) = make_uint4(a.x, a.y, b.x, b.y);
+        if (q.dst) {  // (a job without a destination records its amax only)
+          const uint2 a = e4m3x8(v, s), b = e4m3x8(v + 8, s);
+          *reinterpret_cast<uint4*>(q.dst + i) = make_uint4(a.x, a.y, b.x, b.y);
+        }
       }
     }
     mx = warp_max(mx);

@@ -16,6 +16,7 @@ cudaError_t launch_gemm_fp8(const GemmProblem& p, uint32_t* status, cudaStream_t
       case kEpiQkv: return run_gemm_pair<kKindF8, 256, kEpiQkv>(p, status, stream);
       case kEpiGateResid: return run_gemm_pair<kKindF8, 256, kEpiGateResid>(p, status, stream);
       case kEpiGeluF8: return run_gemm_pair<kKindF8, 256, kEpiGeluF8>(p, status, stream);
+      case kEpiGelu: return run_gemm_pair<kKindF8, 256, kEpiGelu>(p, status, stream);  // tensorwise
       default: break;
     }
   }
@@ -29,6 +30,9 @@ cudaError_t launch_gemm_fp8(const GemmProblem& p, uint32_t* status, cudaStream_t
     case kEpiGeluF8:
       return wide ? run_gemm<kKindF8, 256, kEpiGeluF8>(p, status, stream)
                   : run_gemm<kKindF8, 128, kEpiGeluF8>(p, status, stream);
+    case kEpiGelu:  // tensorwise scaling: the bf16 GELU output is cast after its amax is taken
+      return wide ? run_gemm<kKindF8, 256, kEpiGelu>(p, status, stream)
+                  : run_gemm<kKindF8, 128, kEpiGelu>(p, status, stream);
     case kEpiBias:
       return wide ? run_gemm<kKindF8, 256, kEpiBias>(p, status, stream)
                   : run_gemm<kKindF8, 128, kEpiBias>(p, status, stream);

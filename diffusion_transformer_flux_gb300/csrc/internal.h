@@ -298,7 +298,7 @@ cudaError_t launch_splitk_reduce(int act, const float* partials, int splits, int
 // max |src[i]|; n a multiple of 16, src and dst 16-byte aligned.
 struct QuantJob {
   const __nv_bfloat16* src;
-  uint8_t* dst;
+  uint8_t* dst;  // null: record max |src| into amax only
   int64_t n;
   const float* scale;
   float* amax;

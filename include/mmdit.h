@@ -67,7 +67,17 @@ typedef enum mmdit_act_dtype { MMDIT_F32 = 0, MMDIT_BF16 = 1 } mmdit_act_dtype;
  * delayed per-tensor scaling ([FP8] §Configuration); needs act = MMDIT_BF16 and
  * mlp_hidden % 128 == 0.  The modulation, the attention (bf16, [FP8] §Configuration:
  * fp8_dot_product_attention false) and every other step keep the activation type. */
-typedef enum mmdit_gemm_mode { MMDIT_GEMM_NATIVE = 0, MMDIT_GEMM_FP8_E4M3 = 1 } mmdit_gemm_mode;
+/* FP8_TENSORWISE = the same four linears on E4M3 operands with per-tensor CURRENT scaling ([FP8]
+ * §Configuration, fp8_recipe "tensorwise"; §Training configuration, Aggressive): each operand's
+ * scale comes from its own absolute maximum in the same call, scale = 448 / amax / 2^margin, so
+ * every input is first written in bf16, its amax taken, then cast (weights likewise at every
+ * call).  The state's history column `pos` records those amax and `scale` ends holding the scales
+ * used; amax_compute_algo is not read. */
+typedef enum mmdit_gemm_mode {
+  MMDIT_GEMM_NATIVE = 0,
+  MMDIT_GEMM_FP8_E4M3 = 1,
+  MMDIT_GEMM_FP8_TENSORWISE = 2
+} mmdit_gemm_mode;
 
 /* Shapes and options of one block call ([API] §Configuration, FluxConfig). */
 typedef struct mmdit_dims {
@@ -528,6 +538,9 @@ typedef struct mmdit_flux_config {
   int32_t lat_h, lat_w, channels; /* latent grid and channels (64) */
   int32_t txt_dim;                /* text embedding width (4096) */
   int32_t time_dim, vec_in_dim;   /* 256, 768 */
+  int32_t single_parallel;        /* 0: sequential single blocks (six modulation chunks);
+                                     1: parallel-branch single blocks as in
+                                     mmdit_single_block_parallel_fwd (w_mod [3D, D]) */
 } mmdit_flux_config;
 typedef struct mmdit_flux_w {
   const void *w_img_in, *b_img_in; /* [D, channels], [D] */

@@ -66,6 +66,32 @@ def tensorwise_linear(x, w, b, margin: int = 0):
     return y if b is None else y + np.asarray(b, np.float64)
 
 
+class TensorwiseScaling:
+    """The tensorwise recipe as the block oracle's ``fp8`` object (``oracle.flux.block_linear``
+    calls ``linear``): every linear's input and weight are cast with scales from their own
+    absolute maxima in the same call (``tensorwise_linear``).  ``act_cast``, if given, is applied
+    to a linear's input first -- the value it holds as a stored activation tensor (e.g.
+    ``oracle.flux.round_bf16``: the LayerNorm and GELU outputs are bf16 tensors that the recipe
+    then scales and casts).  ``scales`` and ``amax`` record, per tensor name (``"<linear>.x"``,
+    ``"<linear>.w"``), the scale used and the absolute maximum it came from."""
+
+    def __init__(self, margin: int = 0, act_cast=None):
+        self.margin = margin
+        self.act_cast = act_cast
+        self.scales = {}
+        self.amax = {}
+
+    def linear(self, name, x, w, b):
+        x = np.asarray(x, np.float64)
+        if self.act_cast is not None:
+            x = np.asarray(self.act_cast(x), np.float64)
+        w = np.asarray(w, np.float64)
+        for key, t in ((name + ".x", x), (name + ".w", w)):
+            self.amax[key] = _amax(t)
+            self.scales[key] = _scale_of(self.amax[key], self.margin)
+        return tensorwise_linear(x, w, b, self.margin)
+
+
 # --------------------------------------------------------------------------------- blockwise
 def _slices(n: int, tile: int):
     return [slice(j, min(j + tile, n)) for j in range(0, n, tile)]

@@ -398,3 +398,70 @@ def test_scale_update_over_three_calls(algo, margin):
             # the same rule as the oracle's, to float32 rounding
             assert abs(sc[t] - E.history_scale(h[t], name, margin)) <= 1e-6 * sc[t]
     assert not np.all(hist.cpu().numpy()[:, 0] == hist.cpu().numpy()[:, 1]), "the calls differ"
+
+
+# ----------------------------------------------------------------------------- tensorwise recipe
+def _tensorwise_run(case, margin=0):
+    """One call of the block with gemm = MMDIT_GEMM_FP8_TENSORWISE (current per-tensor scaling);
+    returns (outputs, recorded amax [n_t], scales after the call [n_t])."""
+    dims = L.make_dims(case.B, case.S_i, case.S_t, case.D, case.H, case.F, L.MMDIT_BF16,
+                       rope_interleaved=case.interleaved, gelu_tanh=case.gelu_tanh,
+                       gemm=L.MMDIT_GEMM_FP8_TENSORWISE)
+    n_t = 8 if case.single else 16
+    hist = torch.zeros(n_t, 4, device="cuda")
+    scale = torch.full((n_t,), 123.0, device="cuda")  # overwritten: the recipe keeps no history
+    st = L.make_fp8_state(hist, scale, pos=2, margin=margin)
+    ids = torch.from_numpy(case.ids).cuda()
+    cos = torch.empty(case.B, case.S, 64, device="cuda")
+    sin = torch.empty_like(cos)
+    L.rope3d_freqs(ids, (16, 56, 56), 10000.0, cos, sin)
+    wi = upload_weights(case.w_img, "bf16")
+    if case.single:
+        x = dev(case.x_joint())
+        y = torch.empty_like(x)
+        ws = L.mmdit_single_block_fwd(dims, wi, dev(case.vec), cos, sin, x, y, fp8=st)
+        outs = (y,)
+    else:
+        wt = upload_weights(case.w_txt, "bf16")
+        xi, xt = dev(case.x_img), dev(case.x_txt)
+        yi, yt = torch.empty_like(xi), torch.empty_like(xt)
+        ws = L.mmdit_double_block_fwd(dims, wi, wt, dev(case.vec), cos, sin, xi, xt, yi, yt, fp8=st)
+        outs = (yi, yt)
+    torch.cuda.synchronize()
+    assert L.mmdit_workspace_status(ws) == 0
+    h = hist.cpu().numpy()
+    assert np.all(h[:, [0, 1, 3]] == 0), "only history column pos is written"
+    return tuple(host(o) for o in outs), h[:, 2], scale.cpu().numpy()
+
+
+@pytest.mark.parametrize("B,S_i,S_t,D,H,F,single", SMALL)
+def test_fp8_tensorwise_block_small(B, S_i, S_t, D, H, F, single):
+    """The tensorwise recipe ("FP8 training for Flux models", §Configuration, fp8_recipe
+    "tensorwise"): one call, no history.  Recorded amax: every weight's max |w| exactly, every input
+    within a bf16 step of the oracle's (the GPU takes the amax of its own bf16 LayerNorm, attention
+    and GELU outputs); each scale 448 / that amax in float32; the block output under the FP8 bars
+    against the exact tensorwise evaluation (oracle.fp8_recipes.TensorwiseScaling on bf16-stored
+    inputs) and the float64 block."""
+    from oracle import fp8_recipes as R
+    case = BlockCase(B, S_i, S_t, D, H, F, "bf16", seed=41 + S_i + D, std=0.05, single=single)
+    y, amax, scale = _tensorwise_run(case)
+    tw = R.TensorwiseScaling(act_cast=O.round_bf16)
+    args = dict(mm_cast=O.round_bf16, fp8=tw, interleaved=case.interleaved, gelu_tanh=case.gelu_tanh)
+    if single:
+        y8 = (O.single_block(case.x_joint(), case.vec, case.cos, case.sin, case.w_img, case.H, **args),)
+        slots = [("single", 0)]
+    else:
+        y8 = O.double_block(case.x_img, case.x_txt, case.vec, case.cos, case.sin, case.w_img, case.w_txt,
+                            case.H, **args)
+        slots = [("img", 0), ("txt", 1)]
+    for name, slot in slots:
+        for g, lin in enumerate(NAMES):
+            for op, tag in ((1, "w"), (0, "x")):
+                t = 8 * slot + 2 * g + op
+                ref = tw.amax[f"{name}.{lin}.{tag}"]
+                if tag == "w":
+                    assert amax[t] == np.float32(ref), (name, lin, amax[t], ref)
+                else:
+                    assert abs(amax[t] - ref) <= 2.0 ** -7 * ref, (name, lin, amax[t], ref)
+                assert scale[t] == np.float32(448.0) / np.float32(amax[t]), (name, lin)
+    _check_norm_wise(y, y8, case.oracle(None), "FP8 tensorwise block")

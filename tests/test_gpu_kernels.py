@@ -258,8 +258,12 @@ def test_final_layer_loss_matches_oracle(act, B, Hh, Ww, D):
     mm = O.round_bf16 if act == "bf16" else None
     ref = O.final_layer(x, vec, f["w_ada"], f["b_ada"], f["w_out"], f["b_out"], Hh, Ww, mm_cast=mm)
     assert_parity(host(pred), ref, 2e-2, "final layer (loss variant)")
+    # against the oracle head's own loss: the prediction's rounding moves the MSE by about twice
+    # the relative error of the prediction (bf16 operands at the autocast precision; tf32 operands,
+    # 2^-11 relative, against the pure float64 head for f32)
     ref_loss64 = O.flow_match_loss(ref, z0, z1)
-    assert abs(lv[0] - ref_loss64) <= 1e-3 * ref_loss64, (lv[0], ref_loss64)
+    tol = 1e-3 if act == "bf16" else 5e-3
+    assert abs(lv[0] - ref_loss64) <= tol * ref_loss64, (lv[0], ref_loss64)
 
 
 @pytest.mark.parametrize("xdt,odt", [("bf16", "bf16"), ("f32", "bf16"), ("f32", "f32")])

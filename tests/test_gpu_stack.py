@@ -9,6 +9,9 @@ through the C ABI, against the oracle on the same seeded inputs.
   16 text tokens), batch 1 (the streams inside the joint buffer) and batch 2 (joined by copies),
   bf16 against the bf16-autocast oracle over nine seeds and fp32 against the float64 oracle,
   within 2e-2 x RMS;
+* the model with parallel-branch single blocks at the small width;
+* a full-width stack (D 3072, 2 double + 2 single blocks, both single-block forms, 1024 + 512
+  tokens) with every gate active, against the oracle's whole forward;
 * the 12B stack at 512 px (19 double + 38 single blocks, 1024 + 512 tokens) with every gate at
   zero: the blocks pass the residual stream through, so the prediction is the output head of the
   embedded latents, which the oracle computes at full size.
@@ -103,14 +106,15 @@ def _small_model(B, act, seed):
     return w, z, txt, t, y, ids, (D, H, F, lat, S_t, txt_dim)
 
 
-def _run_model(w, z, txt, t, y, ids, shape, B, act, n_double, n_single, guidance=None):
+def _run_model(w, z, txt, t, y, ids, shape, B, act, n_double, n_single, guidance=None, single_parallel=False):
     D, H, F, lat, S_t, txt_dim = shape
     S = lat * lat + S_t
     cos = torch.empty(B, S, 64, device="cuda")
     sin = torch.empty_like(cos)
     L.rope3d_freqs(torch.from_numpy(ids).cuda(), (16, 56, 56), 10000.0, cos, sin)
     dims = L.make_dims(B, lat * lat, S_t, D, H, F, L.MMDIT_BF16 if act == "bf16" else L.MMDIT_F32)
-    cfg = L.make_flux_config(dims, n_double, n_single, lat, lat, 64, txt_dim, 256, y.shape[1])
+    cfg = L.make_flux_config(dims, n_double, n_single, lat, lat, 64, txt_dim, 256, y.shape[1],
+                             single_parallel=single_parallel)
     pred = torch.empty(B, 64, lat, lat, device="cuda")
     ws = L.mmdit_flux_forward(cfg, w, dev(z, torch.float32), dev(txt, torch_dtype(act)), dev(t, torch.float32),
                               dev(y, torch_dtype(act)), cos, sin, pred, guidance=guidance)
@@ -141,6 +145,30 @@ def test_small_model_matches_oracle_f32(B):
     assert_parity(got, ref, 2e-2, f"whole model f32 B={B}")
 
 
+@pytest.mark.parametrize("B", [1, 2])
+def test_small_model_with_parallel_single_blocks_matches_oracle(B):
+    """The whole model with parallel-branch single blocks (the form whose parameter count matches
+    the API reference's ~535 M / ~12 B), against the oracle's flux_forward(single_parallel=True)."""
+    rng = np.random.default_rng(80 + B)
+    D, H, F, lat, S_t, txt_dim = 256, 2, 1024, 8, 16, 64
+    w = synth.flux_weights(rng, D, H, F, 2, 2, txt_dim=txt_dim, vec_dim=64, dtype="bf16", std=0.05,
+                           single_parallel=True)
+    z = rng.standard_normal((B, 64, lat, lat)).astype(np.float32)
+    txt = synth.bf16_round(rng.standard_normal((B, S_t, txt_dim)).astype(np.float32))
+    t = synth.timesteps(rng, B, "uniform")
+    y = synth.bf16_round(rng.standard_normal((B, 64)).astype(np.float32))
+    ids = synth.position_ids(B, lat, lat, S_t)
+    got = _run_model(_up(w, "bf16"), z, txt, t, y, ids, (D, H, F, lat, S_t, txt_dim), B, "bf16", 2, 2,
+                     single_parallel=True)
+    ref = O.flux_forward(z, txt, t, y, ids, w, H, mm_cast=O.round_bf16, store=O.round_bf16,
+                         single_parallel=True)
+    e = assert_parity(got, ref, 2e-2, f"whole model, parallel single blocks, B={B}")
+    print(f"[model] parallel single blocks B={B}: max|err|/RMS = {e:.3e}")
+    # the switch reaches the single blocks: without them the prediction differs
+    seq = O.flux_forward(z, txt, t, y, ids, dict(w, single=[]), H, mm_cast=O.round_bf16, store=O.round_bf16)
+    assert np.abs(got - seq).max() > 1e-3
+
+
 def test_small_model_without_single_blocks_and_text():
     # no single blocks: the head reads the double blocks' image stream directly
     w, z, txt, t, y, ids, shape = _small_model(2, "bf16", 71)
@@ -148,6 +176,28 @@ def test_small_model_without_single_blocks_and_text():
     got = _run_model(_up(w, "bf16"), z, txt, t, y, ids, shape, 2, "bf16", 2, 0)
     ref = O.flux_forward(z, txt, t, y, ids, w, shape[1], mm_cast=O.round_bf16, store=O.round_bf16)
     assert_parity(got, ref, 2e-2, "whole model, double blocks only")
+
+
+@pytest.mark.parametrize("single_parallel", [False, True])
+def test_full_width_stack_matches_oracle(single_parallel):
+    """A non-trivial stack at the 12B block width: D 3072, 24 heads, F 12288, 2 double + 2 single
+    blocks (sequential or parallel-branch) at 32 x 32 latents and 512 text tokens, batch 1,
+    against the oracle's whole forward at the bf16-autocast precision (every gate active)."""
+    B, lat, S_t, D, H, F, txt_dim = 1, 32, 512, 3072, 24, 12288, 4096
+    rng = np.random.default_rng(3000 + single_parallel)
+    w = synth.flux_weights(rng, D, H, F, 2, 2, txt_dim=txt_dim, vec_dim=768, dtype="bf16", std=0.02,
+                           single_parallel=single_parallel)
+    z = rng.standard_normal((B, 64, lat, lat)).astype(np.float32)
+    txt = synth.bf16_round(rng.standard_normal((B, S_t, txt_dim)).astype(np.float32))
+    t = synth.timesteps(rng, B, "uniform")
+    y = synth.bf16_round(rng.standard_normal((B, 768)).astype(np.float32))
+    ids = synth.position_ids(B, lat, lat, S_t)
+    got = _run_model(_up(w, "bf16"), z, txt, t, y, ids, (D, H, F, lat, S_t, txt_dim), B, "bf16", 2, 2,
+                     single_parallel=single_parallel)
+    ref = O.flux_forward(z, txt, t, y, ids, w, H, mm_cast=O.round_bf16, store=O.round_bf16,
+                         single_parallel=single_parallel)
+    e = assert_parity(got, ref, 2e-2, f"full-width stack (parallel={single_parallel})")
+    print(f"[model] full-width 2 + 2 stack, parallel={single_parallel}: max|err|/RMS = {e:.3e}")
 
 
 def _zero_gate_rows(w_mod, b_mod, D):

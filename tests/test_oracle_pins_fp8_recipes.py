@@ -273,3 +273,32 @@ def test_recipes_zero_operand(f):
     w = RNG.standard_normal((3, 64))
     b = RNG.standard_normal(3)
     np.testing.assert_array_equal(f(x, w, b), np.broadcast_to(b, (2, 3)))
+
+
+def test_tensorwise_recipe_object_in_a_block_is_the_tensorwise_linear():
+    """The block oracle's tensorwise object: each linear equals tensorwise_linear of its
+    (optionally bf16-stored) input, records 448 / amax per tensor, and a whole double block run
+    with it differs from the delayed recipe at the scales those amax give only through the
+    delayed recipe's use of the previous call's scales (equal here: same inputs twice)."""
+    from oracle import flux as O
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((2, 7, 64)) * 3.0
+    w = rng.standard_normal((96, 64)) * 0.05
+    b = rng.standard_normal(96) * 0.01
+    tw = R.TensorwiseScaling()
+    assert np.array_equal(tw.linear("fc1", x, w, b), R.tensorwise_linear(x, w, b))
+    assert tw.scales["fc1.x"] == 448.0 / np.abs(x).max() and tw.scales["fc1.w"] == 448.0 / np.abs(w).max()
+    tb = R.TensorwiseScaling(act_cast=O.round_bf16)
+    assert np.array_equal(tb.linear("fc1", x, w, b), R.tensorwise_linear(O.round_bf16(x), w, b))
+    # a whole block: tensorwise == delayed scaling handed the tensorwise scales of the same inputs
+    from diffusion_transformer_flux_gb300 import synth
+    inp = synth.block_inputs(1, 16, 5, 256, "f32", 3, (4, 4))
+    wi = synth.stream_weights(rng, 256, 2, 128, 512, "f32", 0.05)
+    wt = synth.stream_weights(rng, 256, 2, 128, 512, "f32", 0.05)
+    c, s = O.rope_cos_sin(inp.ids)
+    t1 = R.TensorwiseScaling()
+    y_tw = O.double_block(inp.x_img, inp.x_txt, inp.vec, c, s, wi, wt, 2, fp8=t1)
+    y_dl = O.double_block(inp.x_img, inp.x_txt, inp.vec, c, s, wi, wt, 2,
+                          fp8=E4.DelayedScaling(dict(t1.scales)))
+    for a, bb in zip(y_tw, y_dl):
+        assert np.array_equal(a, bb)
