@@ -148,10 +148,12 @@ class SideModulation:
         self.torch, self.L, self.vec = torch, L, vec
         self.side = torch.cuda.Stream(device=device)
         self.ev_start = torch.cuda.Event()
-        self.sets = weight_sets  # [(name, weights), ...] in the order the blocks need them
-        B, D = vec.shape
-        self.mods = {n: torch.empty(B, 6 * D, device=device) for n, _ in weight_sets}
-        self.ready = {n: torch.cuda.Event() for n, _ in weight_sets}
+        # [(name, w_mod, b_mod), ...] in the order the steps need them (the blocks' six-chunk
+        # modulations, the output head's shift and scale)
+        self.sets = weight_sets
+        B = vec.shape[0]
+        self.mods = {n: torch.empty(B, w.shape[0], device=device) for n, w, _ in weight_sets}
+        self.ready = {n: torch.cuda.Event() for n, _, _ in weight_sets}
 
     def fork(self):
         main = self.torch.cuda.current_stream()
@@ -160,9 +162,8 @@ class SideModulation:
         with self.torch.cuda.stream(self.side):
             # every block's modulation in one launch (mmdit_modulation_batched_fwd): the weights
             # stream at the HBM rate instead of one short launch per block
-            self.L.mmdit_modulation_batched_fwd(self.vec, [(w["w_mod"], w["b_mod"], self.mods[n])
-                                                           for n, w in self.sets])
-            for n, _ in self.sets:
+            self.L.mmdit_modulation_batched_fwd(self.vec, [(w, b, self.mods[n]) for n, w, b in self.sets])
+            for n, _, _ in self.sets:
                 self.ready[n].record(self.side)
 
     def join(self, *names):
@@ -241,9 +242,11 @@ class DeviceStep:
                                                                 wl.lat_w), device)
         self.ws_final = L.workspace(L.mmdit_final_layer_loss_workspace_size(self.dims_final, wl.channels), device)
         self.S, self.S_i, self.B, self.D = S, S_i, B, D
-        sets = [("dimg", self.w_dimg), ("dtxt", self.w_dtxt)]
+        sets = [("dimg", self.w_dimg["w_mod"], self.w_dimg["b_mod"]),
+                ("dtxt", self.w_dtxt["w_mod"], self.w_dtxt["b_mod"])]
         if hw.has_single:
-            sets.append(("single", self.w_single))
+            sets.append(("single", self.w_single["w_mod"], self.w_single["b_mod"]))
+        sets.append(("head", self.final["w_ada"], self.final["b_ada"]))
         self.side = SideModulation(torch, L, self.vec, sets, device)
         n_blocks = 2 if hw.has_single else 1
         self.flops_blocks = n_blocks * block_flops(B, S, D, F, H)
@@ -286,11 +289,13 @@ class DeviceStep:
                                          self.sin, self.C, self.Zc, ws=self.ws_block)
                 self._rows(self.z_img, self.Zc, S_i)
                 head_in = self.z_img
-        # output head with the flow-matching loss fused onto its last kernel
+        # output head (its shift and scale from the batched modulation launch) with the
+        # flow-matching loss fused onto its last kernel
+        side.join("head")
         L.mmdit_final_layer_loss_fwd(self.dims_final, wl.lat_h, wl.lat_w, head_in, self.vec,
                                      self.final["w_ada"], self.final["b_ada"], self.final["w_out"],
                                      self.final["b_out"], self.z0, self.z1, self.loss, pred=self.pred,
-                                     ws=self.ws_final)
+                                     mod=side.mods["head"], ws=self.ws_final)
 
     input_names = ("z0", "z1", "t", "txt", "vec", "ids")
 
@@ -353,8 +358,10 @@ class Fp8BlockStep(DeviceStep):
                        L.mmdit_single_block_workspace_size(self.dims))
         self.ws_block = L.workspace(ws_block, device)
         self.S, self.S_i = S, S_i
-        self.side = SideModulation(torch, L, self.vec, [("dimg", self.w_dimg), ("dtxt", self.w_dtxt),
-                                                        ("single", self.w_single)], device)
+        self.side = SideModulation(torch, L, self.vec,
+                                   [(n, w["w_mod"], w["b_mod"]) for n, w in (("dimg", self.w_dimg),
+                                                                            ("dtxt", self.w_dtxt),
+                                                                            ("single", self.w_single))], device)
         self.flops_blocks = 2 * block_flops(B, S, D, F, H)
         self.flops_dense = self.flops_blocks
         self.flops_linears = 2 * 2 * B * S * D * (3 * D + D + 2 * F)

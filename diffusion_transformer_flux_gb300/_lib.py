@@ -33,7 +33,8 @@ EXPORTED = [
     "mmdit_attention_workspace_size", "mmdit_attention_fwd", "mmdit_double_block_workspace_size",
     "mmdit_double_block_fwd", "mmdit_single_block_workspace_size", "mmdit_single_block_fwd",
     "mmdit_block_workspace_offsets", "mmdit_fp8_quantize_e4m3", "mmdit_fp8_linear_workspace_size",
-    "mmdit_fp8_linear_fwd", "mmdit_single_block_parallel_fwd", "mmdit_linear_bwd_workspace_size",
+    "mmdit_fp8_linear_fwd", "mmdit_fp8_linear_bwd_workspace_size", "mmdit_fp8_linear_bwd",
+    "mmdit_single_block_parallel_fwd", "mmdit_linear_bwd_workspace_size",
     "mmdit_linear_bwd", "mmdit_double_block_bwd_workspace_size", "mmdit_double_block_bwd",
     "mmdit_single_block_bwd_workspace_size", "mmdit_single_block_bwd", "mmdit_modulation_batched_fwd", "mmdit_conditioning_workspace_size",
     "mmdit_conditioning_fwd", "mmdit_flux_workspace_size", "mmdit_flux_forward",
@@ -143,7 +144,7 @@ _SIGS = {
     "mmdit_final_layer_workspace_size": (SZ, [PDIMS, I32]),
     "mmdit_final_layer_loss_workspace_size": (SZ, [PDIMS, I32]),
     "mmdit_final_layer_loss_fwd": (C.c_int, [PDIMS, I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP,
-                                             VP, SZ, VP]),
+                                             VP, VP, SZ, VP]),
     "mmdit_final_layer_fwd": (C.c_int, [PDIMS, I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_ln_modulate_fwd": (C.c_int, [I32, I32, I32, I32, I32, F32, VP, VP, VP, I64, VP, VP]),
     "mmdit_copy_rows": (C.c_int, [VP, I64, VP, I64, I64, I32, VP]),
@@ -157,6 +158,9 @@ _SIGS = {
     "mmdit_fp8_quantize_e4m3": (C.c_int, [VP, I64, VP, VP, VP, VP]),
     "mmdit_fp8_linear_workspace_size": (SZ, []),
     "mmdit_fp8_linear_fwd": (C.c_int, [I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_fp8_linear_bwd_workspace_size": (SZ, [I32, I32, I32, I32]),
+    "mmdit_fp8_linear_bwd": (C.c_int, [I32, I32, I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ,
+                                       VP]),
     "mmdit_single_block_parallel_fwd": (C.c_int, [PDIMS, PW, VP, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_linear_bwd_workspace_size": (SZ, [I32, I32, I32, I32]),
     "mmdit_linear_bwd": (C.c_int, [I32, I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
@@ -386,14 +390,14 @@ def mmdit_final_layer_loss_workspace_size(dims: Dims, channels: int) -> int:
 
 
 def mmdit_final_layer_loss_fwd(dims: Dims, lat_h, lat_w, x_img, vec, w_ada, b_ada, w_out, b_out, z0, z1,
-                               loss, pred=None, ws=None, stream=None):
+                               loss, pred=None, mod=None, ws=None, stream=None):
     """The output head with the flow-matching loss fused onto its last kernel."""
     channels = w_out.shape[0]
     if ws is None:
         ws = workspace(mmdit_final_layer_loss_workspace_size(dims, channels), x_img.device)
     _check(load().mmdit_final_layer_loss_fwd(C.byref(dims), channels, lat_h, lat_w, _ptr(x_img), _ptr(vec),
                                              _ptr(w_ada), _ptr(b_ada), _ptr(w_out), _ptr(b_out), _ptr(z0),
-                                             _ptr(z1), _ptr(pred), _ptr(loss), _ptr(ws), ws.numel(),
+                                             _ptr(z1), _ptr(pred), _ptr(loss), _ptr(mod), _ptr(ws), ws.numel(),
                                              _stream(stream)))
     return ws
 
@@ -630,4 +634,18 @@ def mmdit_single_block_bwd(dims: Dims, w: dict, vec, cos, sin, x, dy, dx, dvec=N
     _check(load().mmdit_single_block_bwd(C.byref(dims), C.byref(sw), _ptr(vec), _ptr(cos), _ptr(sin), _ptr(x),
                                          _ptr(dy), _ptr(dx), _ptr(dvec), C.byref(gg) if gg else None, _ptr(ws),
                                          ws.numel(), _stream(stream)))
+    return ws
+
+
+def mmdit_fp8_linear_bwd(dy, x_q, w_q, scale_x, scale_w, scale_dy, amax_dy, dx, dw=None, db=None, x=None,
+                         recipe="e4m3", fp8_wgrad=True, ws=None, stream=None):
+    """Backward of the FP8 linear (see include/mmdit.h); recipe "e4m3" or "hybrid"."""
+    M, N = dy.shape
+    K = w_q.shape[1]
+    if ws is None:
+        ws = workspace(load().mmdit_fp8_linear_bwd_workspace_size(M, N, K, int(fp8_wgrad)), dy.device)
+    _check(load().mmdit_fp8_linear_bwd(M, N, K, {"e4m3": 0, "hybrid": 1}[recipe], int(fp8_wgrad), _ptr(dy),
+                                       _ptr(x_q), _ptr(w_q), _ptr(x), _ptr(scale_x), _ptr(scale_w),
+                                       _ptr(scale_dy), _ptr(amax_dy), _ptr(dx), _ptr(dw), _ptr(db), _ptr(ws),
+                                       ws.numel(), _stream(stream)))
     return ws

@@ -732,14 +732,17 @@ mmdit_status final_layer_body(const mmdit_dims* d, int channels, const void* x_i
                               const void* w_ada, const void* b_ada, const void* w_out,
                               const void* b_out, float* pred, void* workspace, cudaStream_t st,
                               const float* z0 = nullptr, const float* z1 = nullptr,
-                              float* loss = nullptr) {
+                              float* loss = nullptr, const float* mod_in = nullptr) {
   const bool with_loss = loss != nullptr;
   const HeadPlan hp = plan_head(d, channels, with_loss);
-  float* mod = at<float>(workspace, hp.mod);
+  // the head's (shift, scale): precomputed by the caller, or computed here
+  const float* mod = mod_in ? mod_in : at<float>(workspace, hp.mod);
   void* h = at(workspace, hp.h);
   const int D = d->hidden, rows = d->batch * d->seq_img;
   ProfScope ps_(with_loss ? "final_layer_loss" : "final_layer", st);
-  MMDIT_CUDA(launch_modulation(d->act, vec, w_ada, b_ada, d->batch, 2 * D, D, mod, st), "final modulation");
+  if (!mod_in)
+    MMDIT_CUDA(launch_modulation(d->act, vec, w_ada, b_ada, d->batch, 2 * D, D, at<float>(workspace, hp.mod), st),
+               "final modulation");
   MMDIT_CUDA(launch_ln_modulate(d->act, d->act == MMDIT_F32, x_img, mod, mod + D, 2 * D, rows, d->seq_img, D, d->ln_eps, h, st),
              "final LayerNorm-modulate");
   GemmProblem g;
@@ -1451,7 +1454,7 @@ mmdit_status mmdit_final_layer_loss_fwd(const mmdit_dims* d, int32_t channels, i
                                         int32_t lat_w, const void* x_img, const void* vec,
                                         const void* w_ada, const void* b_ada, const void* w_out,
                                         const void* b_out, const float* z0, const float* z1,
-                                        float* pred, float* loss, void* workspace,
+                                        float* pred, float* loss, const float* mod, void* workspace,
                                         size_t workspace_bytes, void* stream) {
   if (!d) return fail(MMDIT_ERR_INVALID_ARG, "dims is NULL");
   if (d->act != MMDIT_F32 && d->act != MMDIT_BF16) return fail(MMDIT_ERR_INVALID_ARG, "bad act");
@@ -1467,6 +1470,7 @@ mmdit_status mmdit_final_layer_loss_fwd(const mmdit_dims* d, int32_t channels, i
   if (pred && (s = check_ptrs({pred}, "final layer + loss: pred")) != MMDIT_OK) return s;
   if (pred && (pred == z0 || pred == z1))
     return fail(MMDIT_ERR_INVALID_ARG, "final layer + loss: pred may not alias z0 or z1");
+  if (mod && !aligned16(mod)) return fail(MMDIT_ERR_INVALID_ARG, "final layer + loss: mod is not 16-byte aligned");
   if ((s = check_workspace(workspace, workspace_bytes, mmdit_final_layer_loss_workspace_size(d, channels))) !=
       MMDIT_OK)
     return s;
@@ -1475,7 +1479,7 @@ mmdit_status mmdit_final_layer_loss_fwd(const mmdit_dims* d, int32_t channels, i
   MMDIT_CUDA(cudaMemsetAsync(workspace, 0, kStatusBytes, st), "status clear");
   pdl_begin_call();
   return final_layer_body(d, channels, x_img, vec, w_ada, b_ada, w_out, b_out, pred, workspace, st, z0,
-                          z1, loss);
+                          z1, loss, mod);
 }
 
 
@@ -1780,6 +1784,97 @@ static mmdit_status check_grads(const mmdit_stream_grads* g, const char* what) {
                         g->w_2, g->b_2};
   for (int i = 0; i < 12; ++i)
     if (p[i] && !aligned16(p[i])) return fail(MMDIT_ERR_INVALID_ARG, "%s: gradient %d is not 16-byte aligned", what, i);
+  return MMDIT_OK;
+}
+
+// FP8 linear backward workspace: the gradient's codes G [M, N], W^T codes [K, N], and for the FP8
+// weight gradient G^T [N, Mp] and x^T codes [K, Mp] (Mp = M rounded up to 16, zero columns), or
+// the bf16 linear-backward scratch for the unquantised weight gradient; the bias gradient's
+// partial column sums.
+struct Fp8BwdPlan {
+  size_t g, wt, gt, xt, lin, part, total;
+  int Mp;
+};
+Fp8BwdPlan plan_fp8_bwd(int M, int N, int K, int fp8_wgrad) {
+  Fp8BwdPlan p;
+  Carver c;
+  p.Mp = static_cast<int>(round_up(static_cast<size_t>(M > 0 ? M : 0), 16));
+  p.g = c.take(static_cast<size_t>(M) * N);
+  p.wt = c.take(static_cast<size_t>(K) * N);
+  p.gt = fp8_wgrad ? c.take(static_cast<size_t>(N) * p.Mp) : 0;
+  p.xt = fp8_wgrad ? c.take(static_cast<size_t>(K) * p.Mp) : 0;
+  p.lin = fp8_wgrad ? 0 : c.take(linear_bwd_scratch(2, static_cast<size_t>(M), N, K));
+  p.part = c.take(static_cast<size_t>(kColsumChunks) * N * 4);
+  p.total = c.off;
+  return p;
+}
+
+size_t mmdit_fp8_linear_bwd_workspace_size(int32_t M, int32_t N, int32_t K, int32_t fp8_wgrad) {
+  if (M < 0 || N <= 0 || K <= 0) return kStatusBytes;
+  return plan_fp8_bwd(M, N, K, fp8_wgrad).total;
+}
+
+mmdit_status mmdit_fp8_linear_bwd(int32_t M, int32_t N, int32_t K, int32_t recipe, int32_t fp8_wgrad,
+                                  const void* dy, const void* x_q, const void* w_q, const void* x,
+                                  const float* scale_x, const float* scale_w, const float* scale_dy,
+                                  float* amax_dy, void* dx, float* dw, float* db, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (M < 0 || N <= 0 || K <= 0) return fail(MMDIT_ERR_INVALID_ARG, "FP8 linear backward: bad shape M=%d N=%d K=%d", M, N, K);
+  if (recipe != 0 && recipe != 1)
+    return fail(MMDIT_ERR_INVALID_ARG, "FP8 linear backward: recipe must be 0 (e4m3) or 1 (hybrid), got %d", recipe);
+  if (fp8_wgrad != 0 && fp8_wgrad != 1) return fail(MMDIT_ERR_INVALID_ARG, "fp8_wgrad must be 0 or 1");
+  if (K % 128 != 0 || N % 16 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "FP8 linear backward: K must be a multiple of 128 and N of 16 (K=%d, N=%d)", K, N);
+  mmdit_status s = check_ptrs({dy, w_q, dx}, "FP8 linear backward");
+  if (s != MMDIT_OK) return s;
+  if (!scale_x || !scale_w || !scale_dy || !amax_dy)
+    return fail(MMDIT_ERR_INVALID_ARG, "FP8 linear backward: NULL scale or amax");
+  if (dw && !aligned16(dw)) return fail(MMDIT_ERR_INVALID_ARG, "FP8 linear backward: dW not 16-byte aligned");
+  if (db && !aligned16(db)) return fail(MMDIT_ERR_INVALID_ARG, "FP8 linear backward: db not 16-byte aligned");
+  if (dw && fp8_wgrad && (s = check_ptrs({x_q}, "FP8 linear backward x_q")) != MMDIT_OK) return s;
+  if (dw && !fp8_wgrad && (s = check_ptrs({x}, "FP8 linear backward x")) != MMDIT_OK) return s;
+  const Fp8BwdPlan fp = plan_fp8_bwd(M, N, K, fp8_wgrad);
+  if ((s = check_workspace(workspace, workspace_bytes, fp.total)) != MMDIT_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  if (M == 0) {
+    if (dw) MMDIT_CUDA(cudaMemsetAsync(dw, 0, static_cast<size_t>(N) * K * 4, st), "dW clear");
+    if (db) MMDIT_CUDA(cudaMemsetAsync(db, 0, static_cast<size_t>(N) * 4, st), "db clear");
+    return MMDIT_OK;
+  }
+  pdl_begin_call();
+  ProfScope ps_("fp8_linear_bwd", st);
+  uint8_t* g = at<uint8_t>(workspace, fp.g);
+  // G = Qg(dy scale_dy): E4M3 or, under the hybrid recipe, E5M2; amax_dy records max |dy|
+  QuantJob q{static_cast<const __nv_bfloat16*>(dy), g, static_cast<int64_t>(M) * N, scale_dy, amax_dy, recipe};
+  MMDIT_CUDA(launch_quantize_e4m3(&q, 1, st), "gradient cast");
+  const int kind = recipe ? 3 : 2;
+  {
+    // dx [M, K] = G W_q / (s_dy s_w): K-major operands G [M, N] and W_q^T [K, N]
+    MMDIT_CUDA(launch_transpose_u8(static_cast<const uint8_t*>(w_q), N, K, N, at<uint8_t>(workspace, fp.wt), st),
+               "W codes transpose");
+    GemmProblem gp;
+    gp.act = kind, gp.epi = kEpiBias, gp.M = M, gp.N = K, gp.K = N, gp.A = g, gp.W = at(workspace, fp.wt);
+    gp.ep.out = dx, gp.ep.scale_a = scale_dy, gp.ep.scale_w = scale_w;
+    MMDIT_CUDA(launch_gemm(gp, status_word(workspace), st), "FP8 dgrad GEMM");
+  }
+  if (dw && fp8_wgrad) {
+    // dW [N, K] = G^T X_q / (s_dy s_x), contracted over the M rows (zero-padded to Mp)
+    MMDIT_CUDA(launch_transpose_u8(g, M, N, fp.Mp, at<uint8_t>(workspace, fp.gt), st), "G transpose");
+    MMDIT_CUDA(launch_transpose_u8(static_cast<const uint8_t*>(x_q), M, K, fp.Mp, at<uint8_t>(workspace, fp.xt), st),
+               "x codes transpose");
+    GemmProblem gp;
+    gp.act = kind, gp.epi = kEpiBias, gp.M = N, gp.N = K, gp.K = fp.Mp, gp.A = at(workspace, fp.gt);
+    gp.W = at(workspace, fp.xt), gp.ep.out = dw, gp.ep.out_f32 = 1, gp.ep.scale_a = scale_dy, gp.ep.scale_w = scale_x;
+    MMDIT_CUDA(launch_gemm(gp, status_word(workspace), st), "FP8 wgrad GEMM");
+  } else if (dw) {
+    // without fp8_wgrad the weight gradient is dy^T x on the unquantised bf16 tensors
+    mmdit_status r = linear_bwd_body(MMDIT_BF16, M, N, K, dy, x, nullptr, nullptr, dw, nullptr,
+                                     at(workspace, fp.lin), workspace, st);
+    if (r != MMDIT_OK) return r;
+  }
+  if (db) MMDIT_CUDA(launch_colsum(MMDIT_BF16, dy, M, N, at<float>(workspace, fp.part), kColsumChunks, db, st),
+                     "db column sums");
   return MMDIT_OK;
 }
 

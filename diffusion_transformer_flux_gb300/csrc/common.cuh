@@ -140,7 +140,9 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 }
 
 // D(tmem) (+)= A(smem) * B(smem)^T.  KIND selects the operand family.
-enum MmaKind { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2 };
+// kKindF8: E4M3 A and B; kKindF8E5M2: E5M2 A with E4M3 B (kind::f8f6f4 takes each operand's
+// format separately: the hybrid FP8 recipe's gradient times an E4M3 weight or activation).
+enum MmaKind { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2, kKindF8E5M2 = 3 };
 
 template <int KIND>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -193,11 +195,12 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
 
 // Instruction descriptor: fp32 accumulator (bits 4-5 = 1), A/B formats (bits 7-9, 10-12),
 // both operands K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-// Formats: kind::f16 -> 1 = bf16; kind::tf32 -> 2 = tf32; kind::f8f6f4 -> 0 = E4M3.
+// Formats: kind::f16 -> 1 = bf16; kind::tf32 -> 2 = tf32; kind::f8f6f4 -> 0 = E4M3, 1 = E5M2.
 template <int KIND>
 __host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
-  uint32_t fmt = KIND == kKindF16 ? 1u : (KIND == kKindTF32 ? 2u : 0u);
-  return (1u << 4) | (fmt << 7) | (fmt << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+  const uint32_t fmt = KIND == kKindF16 ? 1u : (KIND == kKindTF32 ? 2u : 0u);
+  const uint32_t fmt_a = KIND == kKindF8E5M2 ? 1u : fmt;
+  return (1u << 4) | (fmt_a << 7) | (fmt << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 // kind::f16 with fp16 (format 0) A and B operands.
@@ -483,7 +486,7 @@ __device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t a_desc, ui
         "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
-  } else if constexpr (KIND == kKindF8) {
+  } else if constexpr (KIND == kKindF8 || KIND == kKindF8E5M2) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
@@ -525,6 +528,20 @@ __device__ __forceinline__ uint2 e4m3x8(const float* v, float s) {
   uint2 u;
   u.x = e4m3x2(v[0] * s, v[1] * s) | (e4m3x2(v[2] * s, v[3] * s) << 16);
   u.y = e4m3x2(v[4] * s, v[5] * s) | (e4m3x2(v[6] * s, v[7] * s) << 16);
+  return u;
+}
+
+// E5M2 (5 exponent bits, 2 mantissa bits, largest finite 57344): round to nearest even and
+// saturate, as the E4M3 pair conversion above.
+__device__ __forceinline__ uint32_t e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint2 e5m2x8(const float* v, float s) {
+  uint2 u;
+  u.x = e5m2x2(v[0] * s, v[1] * s) | (e5m2x2(v[2] * s, v[3] * s) << 16);
+  u.y = e5m2x2(v[4] * s, v[5] * s) | (e5m2x2(v[6] * s, v[7] * s) << 16);
   return u;
 }
 // Raises the non-negative float at `p` to at least `v` (non-negative floats order like their

@@ -63,13 +63,31 @@ __global__ void __launch_bounds__(kQThreads) quantize_e4m3_kernel(const __grid_c
 #pragma unroll
         for (int e = 0; e < 16; ++e) mx = fmaxf(mx, fabsf(v[e]));
         if (q.dst) {  // (a job without a destination records its amax only)
-          const uint2 a = e4m3x8(v, s), b = e4m3x8(v + 8, s);
+          const uint2 a = q.e5m2 ? e5m2x8(v, s) : e4m3x8(v, s), b = q.e5m2 ? e5m2x8(v + 8, s) : e4m3x8(v + 8, s);
           *reinterpret_cast<uint4*>(q.dst + i) = make_uint4(a.x, a.y, b.x, b.y);
         }
       }
     }
     mx = warp_max(mx);
     if ((threadIdx.x & 31) == 0 && mx > 0.f) atomic_max_nonneg(q.amax, mx);
+  }
+}
+
+// out [C, ld_out] = in [R, C]^T for bytes through a 64 x 64 shared tile (one byte per thread
+// and element); the padding columns R .. ld_out - 1 are written as zero codes.
+__global__ void transpose_u8_kernel(const uint8_t* __restrict__ in, int R, int C, int ld_out,
+                                    uint8_t* __restrict__ out) {
+  pdl_wait();  // the previous kernel's results are visible from here on
+  __shared__ uint8_t tile[64][65];
+  const int r0 = blockIdx.x * 64, c0 = blockIdx.y * 64;
+  for (int i = threadIdx.y; i < 64; i += blockDim.y) {
+    const int r = r0 + i, c = c0 + threadIdx.x;
+    tile[i][threadIdx.x] = (r < R && c < C) ? in[static_cast<size_t>(r) * C + c] : 0;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 64; i += blockDim.y) {
+    const int c = c0 + i, r = r0 + threadIdx.x;
+    if (c < C && r < ld_out) out[static_cast<size_t>(c) * ld_out + r] = tile[threadIdx.x][i];
   }
 }
 
@@ -120,6 +138,18 @@ cudaError_t launch_quantize_e4m3(const QuantJob* jobs, int njobs, cudaStream_t s
   const int grid = static_cast<int>(tiles < cap ? tiles : cap);
   {
     const cudaError_t e_ = launch_pdl(quantize_e4m3_kernel, dim3(grid), dim3(kQThreads), 0, stream, q, tiles);
+    if (e_ != cudaSuccess) return e_;
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_u8(const uint8_t* in, int R, int C, int ld_out, uint8_t* out, cudaStream_t stream) {
+  if (C == 0 || ld_out == 0) return cudaSuccess;
+  if (ld_out < R) return cudaErrorInvalidValue;
+  const dim3 grid((ld_out + 63) / 64, (C + 63) / 64), block(64, 4);
+  {
+    const cudaError_t e_ = launch_pdl(transpose_u8_kernel, grid, block, 0, stream, in, R, C, ld_out, out);
     if (e_ != cudaSuccess) return e_;
   }
   count_launch();

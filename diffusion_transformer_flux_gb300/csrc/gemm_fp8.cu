@@ -11,6 +11,12 @@ cudaError_t launch_gemm_fp8(const GemmProblem& p, uint32_t* status, cudaStream_t
   if (!p.ep.scale_a || !p.ep.scale_w || (p.M1 > 0 && (!p.ep1.scale_a || !p.ep1.scale_w)))
     return cudaErrorInvalidValue;
   const bool wide = p.N % 256 == 0;
+  if (p.act == 3) {
+    // E5M2 A (the hybrid recipe's gradient) with E4M3 B: the backward's plain products only
+    if (p.epi != kEpiBias) return cudaErrorInvalidValue;
+    return wide ? run_gemm<kKindF8E5M2, 256, kEpiBias>(p, status, stream)
+                : run_gemm<kKindF8E5M2, 128, kEpiBias>(p, status, stream);
+  }
   if (use_pair(p)) {
     switch (p.epi) {
       case kEpiQkv: return run_gemm_pair<kKindF8, 256, kEpiQkv>(p, status, stream);

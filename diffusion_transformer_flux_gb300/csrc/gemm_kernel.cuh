@@ -52,6 +52,13 @@ struct KindTraits<kKindF8> {  // E4M3 operands, bf16 activations around them
   static constexpr CUtensorMapDataType kMapType = CU_TENSOR_MAP_DATA_TYPE_UINT8;
 };
 
+template <>
+struct KindTraits<kKindF8E5M2> {  // E5M2 A (a gradient), E4M3 B, bf16 or fp32 output
+  using TE = __nv_bfloat16;
+  static constexpr int kEltBytes = 1;
+  static constexpr CUtensorMapDataType kMapType = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+};
+
 template <int BN>
 struct GemmCfg {
   static constexpr int kStages = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
@@ -442,7 +449,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       if constexpr (EPI == kEpiPartial)
         ep.out = reinterpret_cast<float*>(ep.out) +
                  static_cast<size_t>(tile / tiles) * static_cast<size_t>(prob ? M1 : M0) * N;
-      gemm_epilogue<TE, BN, EPI, KIND == kKindF8>(group, taddr, mb * kBM + row, nb * BN,
+      gemm_epilogue<TE, BN, EPI, (KIND == kKindF8 || KIND == kKindF8E5M2)>(group, taddr, mb * kBM + row, nb * BN,
                                                   prob ? M1 : M0, N, ep);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);

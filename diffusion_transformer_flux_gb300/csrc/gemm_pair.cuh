@@ -187,7 +187,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<EPI>(),
       const uint32_t taddr =
           tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
       EpiArgs ep = prob ? ep1 : ep0;
-      gemm_epilogue<TE, BN, EPI, KIND == kKindF8>(group, taddr, m0 + row, nb * BN, prob ? M1 : M0, N, ep);
+      gemm_epilogue<TE, BN, EPI, (KIND == kKindF8 || KIND == kKindF8E5M2)>(group, taddr, m0 + row, nb * BN, prob ? M1 : M0, N, ep);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(tempty_leader + static_cast<uint32_t>(acc * sizeof(uint64_t)));

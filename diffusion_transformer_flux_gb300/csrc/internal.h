@@ -57,7 +57,8 @@ struct EpiArgs {
 };
 
 struct GemmProblem {
-  int act = 1;           // 0 = fp32 operands (tf32 MMA), 1 = bf16, 2 = E4M3 (epilogue I/O bf16)
+  int act = 1;           // 0 = fp32 operands (tf32 MMA), 1 = bf16, 2 = E4M3 (epilogue I/O bf16),
+                         // 3 = E5M2 A with E4M3 B (kEpiBias only)
   int epi = kEpiBias;
   int M = 0, N = 0, K = 0;
   const void* A = nullptr;  // [M, K]
@@ -121,7 +122,7 @@ cudaError_t launch_gemm_tf32(const GemmProblem& p, uint32_t* status, cudaStream_
 // kEpiGateResid and kEpiGeluF8, with scale_a / scale_w set in every EpiArgs.
 cudaError_t launch_gemm_fp8(const GemmProblem& p, uint32_t* status, cudaStream_t stream);
 inline cudaError_t launch_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream) {
-  return p.act == 2 ? launch_gemm_fp8(p, status, stream)
+  return p.act >= 2 ? launch_gemm_fp8(p, status, stream)
                     : (p.act == 1 ? launch_gemm_bf16(p, status, stream) : launch_gemm_tf32(p, status, stream));
 }
 
@@ -302,9 +303,13 @@ struct QuantJob {
   int64_t n;
   const float* scale;
   float* amax;
+  int e5m2 = 0;  // 1: E5M2 codes (the hybrid recipe's gradient format) instead of E4M3
 };
 constexpr int kQuantMaxJobs = 8;
 cudaError_t launch_quantize_e4m3(const QuantJob* jobs, int njobs, cudaStream_t stream);
+// out [C, ld_out] = in [R, C] transposed, for bytes (E4M3 / E5M2 codes); columns R .. ld_out - 1
+// are zero.
+cudaError_t launch_transpose_u8(const uint8_t* in, int R, int C, int ld_out, uint8_t* out, cudaStream_t stream);
 // hist[i * hist_len + pos] = 0 for i < n.
 cudaError_t launch_amax_reset(float* hist, int hist_len, int n, int pos, cudaStream_t stream);
 // scale[i] = 448 / amax / 2^margin where amax, positive and finite, is hist[i * hist_len + pos]

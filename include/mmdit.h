@@ -290,7 +290,10 @@ mmdit_status mmdit_final_layer_fwd(const mmdit_dims *dims, int32_t channels, int
  * in a fixed order by the last block: deterministic).
  *   z0, z1 [B, C, H, W] fp32 (the latent pair of this step); loss: device fp32 scalar (4-byte
  *   aligned);
- *   pred: NULL, or [B, C, H, W] fp32 receiving the prediction (may not alias z0 or z1).
+ *   pred: NULL, or [B, C, H, W] fp32 receiving the prediction (may not alias z0 or z1);
+ *   mod: NULL, or the head's (shift, scale) [B, 2D] fp32 = SiLU(vec) w_ada^T + b_ada computed ahead
+ *   (mmdit_modulation_fwd or the batched launch, which also takes the blocks' modulations);
+ *   w_ada and b_ada are then not read.
  * Other arguments as mmdit_final_layer_fwd.
  * workspace >= mmdit_final_layer_loss_workspace_size(dims, channels). */
 size_t mmdit_final_layer_loss_workspace_size(const mmdit_dims *dims, int32_t channels);
@@ -298,7 +301,7 @@ mmdit_status mmdit_final_layer_loss_fwd(const mmdit_dims *dims, int32_t channels
                                         int32_t lat_w, const void *x_img, const void *vec,
                                         const void *w_ada, const void *b_ada, const void *w_out,
                                         const void *b_out, const float *z0, const float *z1,
-                                        float *pred, float *loss, void *workspace,
+                                        float *pred, float *loss, const float *mod, void *workspace,
                                         size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------------------
@@ -400,6 +403,28 @@ size_t mmdit_fp8_linear_workspace_size(void);
 mmdit_status mmdit_fp8_linear_fwd(int32_t M, int32_t N, int32_t K, const void *x, const void *w,
                                   const float *scale_x, const float *scale_w, const void *b,
                                   void *y, void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Backward of the FP8 linear ([FP8] §Configuration, FP8 model configuration: fp8 "e4m3" or
+ * "hybrid", fp8_wgrad; the chain rule of mmdit_fp8_linear_fwd), for a forward that ran on
+ * x_q = E4M3(x scale_x) and w_q = E4M3(W scale_w):
+ *   G  = Qg(dy * scale_dy[0])          Qg = E4M3 (recipe 0, "e4m3") or E5M2 (recipe 1, "hybrid";
+ *                                      round to nearest even, saturating at 57344);
+ *                                      amax_dy[0] = max(amax_dy[0], max |dy|)
+ *   dx = G w_q / (scale_dy scale_w)    [M, K] bf16
+ *   dW = G^T x_q / (scale_dy scale_x)  [N, K] fp32 with fp8_wgrad = 1; dy^T x on the bf16 tensors
+ *                                      with fp8_wgrad = 0 (x read only then)
+ *   db = column sums of dy             [N] fp32 (fixed order)
+ * dy [M, N] bf16; x_q [M, K], w_q [N, K] uint8 codes; x [M, K] bf16; scales and amax_dy device
+ * fp32 scalars; dw and db may be NULL.  K % 128 == 0, N % 16 == 0; both products run on the
+ * tensor cores (kind::f8f6f4, E5M2 x E4M3 under "hybrid"), fp32 accumulation.
+ * workspace >= mmdit_fp8_linear_bwd_workspace_size(M, N, K, fp8_wgrad). */
+size_t mmdit_fp8_linear_bwd_workspace_size(int32_t M, int32_t N, int32_t K, int32_t fp8_wgrad);
+mmdit_status mmdit_fp8_linear_bwd(int32_t M, int32_t N, int32_t K, int32_t recipe, int32_t fp8_wgrad,
+                                  const void *dy, const void *x_q, const void *w_q, const void *x,
+                                  const float *scale_x, const float *scale_w, const float *scale_dy,
+                                  float *amax_dy, void *dx, float *dw, float *db, void *workspace,
+                                  size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------------------
  * Single-stream block with parallel branches (the whole-model row's shape option; [ARCH]

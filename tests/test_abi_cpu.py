@@ -244,16 +244,17 @@ def test_linear_bwd_embedding_head_and_modulation_validation(lib):
     # output head with the fused loss: the same shape rules; z0, z1 and loss required; pred optional
     # but never aliasing a latent; workspace at least its own size (larger than the head's alone)
     fl = lib.mmdit_final_layer_loss_fwd
-    assert fl(C.byref(d), 64, 8, 7, 16, 16, 16, 16, 16, 16, 32, 48, 64, 80, 256, 1 << 30, None) == 1
-    assert fl(C.byref(d), 48, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 64, 80, 256, 1 << 30, None) == 2
-    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, None, 48, 64, 80, 256, 1 << 30, None) == 1
-    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 64, None, 256, 1 << 30, None) == 1
-    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 64, 82, 256, 1 << 30, None) == 1
-    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 32, 80, 256, 1 << 30, None) == 1
-    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 0x1004, 80, 256, 1 << 30, None) == 1
+    assert fl(C.byref(d), 64, 8, 7, 16, 16, 16, 16, 16, 16, 32, 48, 64, 80, None, 256, 1 << 30, None) == 1
+    assert fl(C.byref(d), 48, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 64, 80, None, 256, 1 << 30, None) == 2
+    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, None, 48, 64, 80, None, 256, 1 << 30, None) == 1
+    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 64, None, None, 256, 1 << 30, None) == 1
+    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 64, 82, None, 256, 1 << 30, None) == 1
+    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 32, 80, None, 256, 1 << 30, None) == 1
+    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 0x1004, 80, None, 256, 1 << 30, None) == 1
+    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, 64, 80, 0x1004, 256, 1 << 30, None) == 1
     need = L.mmdit_final_layer_loss_workspace_size(d, 64)
     assert need > L.mmdit_final_layer_workspace_size(d, 64)
-    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, None, 80, 256, need - 1, None) == 3
+    assert fl(C.byref(d), 64, 8, 8, 16, 16, 16, 16, 16, 16, 32, 48, None, 80, None, 256, need - 1, None) == 3
     # img_in with the noise fused: z0, z1, t required; z_t optional, never aliasing a latent
     fi = lib.mmdit_img_in_noise_fwd
     assert fi(1, 1, 12, 8, 8, 256, 16, 32, 48, 16, 16, 16, None, 256, 1 << 30, None) == 2

@@ -465,3 +465,44 @@ def test_fp8_tensorwise_block_small(B, S_i, S_t, D, H, F, single):
                     assert abs(amax[t] - ref) <= 2.0 ** -7 * ref, (name, lin, amax[t], ref)
                 assert scale[t] == np.float32(448.0) / np.float32(amax[t]), (name, lin)
     _check_norm_wise(y, y8, case.oracle(None), "FP8 tensorwise block")
+
+
+
+# ----------------------------------------------------------------------------- FP8 linear backward
+@pytest.mark.parametrize("recipe", ["e4m3", "hybrid"])
+@pytest.mark.parametrize("fp8_wgrad", [True, False])
+@pytest.mark.parametrize("M,N,K", [(300, 256, 384), (4608, 3072, 3072), (77, 48, 128)])
+def test_fp8_linear_backward_matches_oracle(recipe, fp8_wgrad, M, N, K):
+    """mmdit_fp8_linear_bwd against oracle.fp8_backward.fp8_linear_bwd ("FP8 training for Flux
+    models", §Configuration: fp8 "e4m3" / "hybrid", fp8_wgrad).  The forward casts come from the
+    library's bit-exact E4M3 cast at power-of-two scales, and dy's scale is a power of two too, so
+    both sides multiply the same codes: dx and dW agree to fp32 accumulation (2e-3 x RMS, the FP8
+    linear's bar), db to 1e-5.  The recorded amax of dy is max |dy| exactly."""
+    from oracle import fp8_backward as FB
+    rng = np.random.default_rng(M + N + K + (recipe == "hybrid"))
+    x = synth.bf16_round(rng.standard_normal((M, K)))
+    w = synth.bf16_round(rng.standard_normal((N, K)) * 0.02)
+    dy = synth.bf16_round(rng.standard_normal((M, N)) * 1e-3)
+    fmax = 448.0 if recipe == "e4m3" else 57344.0
+    sx, sw = _pow2_scale(np.abs(x).max()), _pow2_scale(np.abs(w).max())
+    sdy = 2.0 ** np.floor(np.log2(fmax / np.abs(dy).max()))
+    scales = torch.tensor([sx, sw, sdy], dtype=torch.float32, device="cuda")
+    amax = torch.zeros(3, device="cuda")
+    xq = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+    wq = torch.empty(N, K, dtype=torch.uint8, device="cuda")
+    L.mmdit_fp8_quantize_e4m3(dev(x), scales[0:1], amax[0:1], xq)
+    L.mmdit_fp8_quantize_e4m3(dev(w), scales[1:2], amax[1:2], wq)
+    dx = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    dw = torch.full((N, K), float("nan"), device="cuda")
+    db = torch.full((N,), float("nan"), device="cuda")
+    ws = L.mmdit_fp8_linear_bwd(dev(dy), xq, wq, scales[0:1], scales[1:2], scales[2:3], amax[2:3], dx, dw, db,
+                                x=dev(x), recipe=recipe, fp8_wgrad=fp8_wgrad)
+    torch.cuda.synchronize()
+    assert L.mmdit_workspace_status(ws) == 0
+    rdx, rdw, rdb = FB.fp8_linear_bwd(dy, x, w, sx, sw, sdy, recipe, fp8_wgrad)
+    assert amax[2].item() == np.float32(np.abs(dy).max())
+    assert_parity(host(dx), rdx, 2e-3, f"FP8 dgrad ({recipe})", out_bf16=True)
+    # without fp8_wgrad the weight gradient is the bf16 product dy^T x, held to the linear
+    # backward's bar
+    assert_parity(host(dw), rdw, 2e-3 if fp8_wgrad else 2e-2, f"wgrad ({recipe}, fp8_wgrad={fp8_wgrad})")
+    assert_parity(host(db), rdb, 1e-5, "db")
