@@ -783,6 +783,45 @@ def measure_parallel_block(st, L, torch, peak, reps=10):
             "achieved_tflops": round(flops / us / 1e6, 1), "frac": round(flops / us / 1e6 / peak, 4)}
 
 
+def measure_block_bwd(st, L, torch, peak, reps=3):
+    """The double block's backward (mmdit_double_block_bwd) at the step's shapes, every gradient
+    requested (both streams' fp32 weight gradients, dvec, dx): CUDA events around `reps` calls
+    after one warm-up.  Work counted: the backward's contractions, 2 x the block's GEMM FLOPs (dx
+    and dW of each linear) + 2.5 x its attention FLOPs (QK^T recomputed, dO V^T, P^T dO, dS K,
+    dS^T Q); the call also recomputes the forward (activation recomputation), which is not
+    counted, so the figure is conservative."""
+    wl = st.wl
+    B, D, F, H, S_i, S_t = wl.batch, wl.hidden, wl.mlp_hidden, wl.heads, wl.seq_img, wl.seq_txt
+    S = S_i + S_t
+    gen = torch.Generator(device=st.vec.device).manual_seed(7)
+    dy_i = (torch.randn(B, S_i, D, device=st.vec.device, generator=gen) * 1e-3).to(torch.bfloat16)
+    dy_t = (torch.randn(B, S_t, D, device=st.vec.device, generator=gen) * 1e-3).to(torch.bfloat16)
+    dx_i, dx_t = torch.empty_like(dy_i), torch.empty_like(dy_t)
+    dvec = torch.empty(B, D, device=st.vec.device)
+    grads = [{n: torch.empty(tuple(w[n].shape), device=st.vec.device) for n in L.STREAM_W_FIELDS}
+             for w in (st.w_dimg, st.w_dtxt)]
+    args = (st.dims, st.w_dimg, st.w_dtxt, st.vec, st.cos, st.sin, st.x_img, st.x_txt, dy_i, dy_t, dx_i, dx_t, dvec,
+            grads[0], grads[1])
+    ws = L.mmdit_double_block_bwd(*args)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        L.mmdit_double_block_bwd(*args, ws=ws)
+    b.record()
+    torch.cuda.synchronize()
+    if L.mmdit_workspace_status(ws) != 0:
+        raise RuntimeError("a kernel gave up a bounded wait in the block backward")
+    us = a.elapsed_time(b) * 1e3 / reps
+    gemm = 2 * B * S * D * (3 * D + D + 2 * F)
+    attn = 4 * B * S * S * 128 * H
+    flops = 2 * gemm + 2.5 * attn
+    del grads, ws
+    return {"op": "double block backward (all gradients, forward recomputed inside)", "tokens": S,
+            "avg_us": round(us, 2), "flops_counted": flops, "achieved_tflops": round(flops / us / 1e6, 1),
+            "frac": round(flops / us / 1e6 / peak, 4)}
+
+
 def measure_linear_bwd(L, torch, device, peak, M=4608, N=12288, K=3072, reps=5):
     """The backward of the block's fc1-shaped linear (mmdit_linear_bwd: dx and dW through the
     tensor-core GEMM on transposed operands, db): 4 M N K FLOPs per call, CUDA events around
@@ -1032,6 +1071,7 @@ def main():
         extras["hbm_sweeps"] = measure_hbm_sweeps(L, torch, device, hbm_peak)
         extras["single_block_parallel"] = measure_parallel_block(st, L, torch, bf16_peak)
         extras["linear_backward"] = measure_linear_bwd(L, torch, device, bf16_peak)
+        extras["double_block_backward"] = measure_block_bwd(st, L, torch, bf16_peak)
     if fp8:
         extras["fp8_peak"] = fp8_meas
 

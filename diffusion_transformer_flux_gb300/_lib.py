@@ -30,7 +30,8 @@ EXPORTED = [
     "mmdit_img_in_fwd", "mmdit_img_in_noise_fwd", "mmdit_final_layer_workspace_size",
     "mmdit_final_layer_fwd", "mmdit_final_layer_loss_workspace_size", "mmdit_final_layer_loss_fwd",
     "mmdit_ln_modulate_fwd", "mmdit_copy_rows",
-    "mmdit_attention_workspace_size", "mmdit_attention_fwd", "mmdit_double_block_workspace_size",
+    "mmdit_attention_workspace_size", "mmdit_attention_fwd", "mmdit_fp8_attention_workspace_size",
+    "mmdit_fp8_attention_fwd", "mmdit_double_block_workspace_size",
     "mmdit_double_block_fwd", "mmdit_single_block_workspace_size", "mmdit_single_block_fwd",
     "mmdit_block_workspace_offsets", "mmdit_fp8_quantize_e4m3", "mmdit_fp8_linear_workspace_size",
     "mmdit_fp8_linear_fwd", "mmdit_fp8_linear_bwd_workspace_size", "mmdit_fp8_linear_bwd",
@@ -150,6 +151,8 @@ _SIGS = {
     "mmdit_copy_rows": (C.c_int, [VP, I64, VP, I64, I64, I32, VP]),
     "mmdit_attention_workspace_size": (SZ, [I32, I32, I32]),
     "mmdit_attention_fwd": (C.c_int, [I32, I32, I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_fp8_attention_workspace_size": (SZ, [I32, I32, I32]),
+    "mmdit_fp8_attention_fwd": (C.c_int, [I32, I32, I32, I32, I32, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_double_block_workspace_size": (SZ, [PDIMS]),
     "mmdit_double_block_fwd": (C.c_int, [PDIMS, PW, PW, VP, VP, VP, VP, VP, VP, VP, PFP8, VP, SZ, VP]),
     "mmdit_single_block_workspace_size": (SZ, [PDIMS]),
@@ -648,4 +651,15 @@ def mmdit_fp8_linear_bwd(dy, x_q, w_q, scale_x, scale_w, scale_dy, amax_dy, dx, 
                                        _ptr(x_q), _ptr(w_q), _ptr(x), _ptr(scale_x), _ptr(scale_w),
                                        _ptr(scale_dy), _ptr(amax_dy), _ptr(dx), _ptr(dw), _ptr(db), _ptr(ws),
                                        ws.numel(), _stream(stream)))
+    return ws
+
+
+def mmdit_fp8_attention_fwd(q, k, v, scale_q, scale_k, scale_v, out, ws=None, stream=None):
+    """Joint attention on E4M3 operands (see include/mmdit.h); scales are device fp32 scalars."""
+    B, H, S, d = q.shape
+    if ws is None:
+        ws = workspace(load().mmdit_fp8_attention_workspace_size(B, H, S), q.device)
+    _check(load().mmdit_fp8_attention_fwd(act_of(out), B, H, S, d, _ptr(q), _ptr(k), _ptr(v), _ptr(scale_q),
+                                          _ptr(scale_k), _ptr(scale_v), _ptr(out), _ptr(ws), ws.numel(),
+                                          _stream(stream)))
     return ws

@@ -1878,6 +1878,54 @@ mmdit_status mmdit_fp8_linear_bwd(int32_t M, int32_t N, int32_t K, int32_t recip
   return MMDIT_OK;
 }
 
+size_t mmdit_fp8_attention_workspace_size(int32_t batch, int32_t heads, int32_t seq) {
+  if (batch < 1 || heads < 1 || seq < 1) return kStatusBytes;
+  const size_t bh = static_cast<size_t>(batch) * heads, sp = round_up(static_cast<size_t>(seq), 16);
+  Carver c;
+  c.take(bh * seq * 128);  // q8
+  c.take(bh * seq * 128);  // k8
+  c.take(bh * 128 * sp);   // vt8
+  c.take(2 * sizeof(float));
+  return c.off;
+}
+
+mmdit_status mmdit_fp8_attention_fwd(int32_t act, int32_t batch, int32_t heads, int32_t seq, int32_t head_dim,
+                                     const void* q, const void* k, const void* v, const float* scale_q,
+                                     const float* scale_k, const float* scale_v, void* out, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  if (act != MMDIT_F32 && act != MMDIT_BF16) return fail(MMDIT_ERR_INVALID_ARG, "bad act %d", act);
+  if (batch < 1 || heads < 1 || seq < 0) return fail(MMDIT_ERR_INVALID_ARG, "FP8 attention: bad shape");
+  if (head_dim != 128) return fail(MMDIT_ERR_UNSUPPORTED, "FP8 attention: head_dim must be 128");
+  if (static_cast<int64_t>(batch) * heads > 65535)
+    return fail(MMDIT_ERR_UNSUPPORTED, "FP8 attention: batch * heads must be <= 65535");
+  mmdit_status s = check_ptrs({q, k, v, out}, "FP8 attention");
+  if (s != MMDIT_OK) return s;
+  if (!scale_q || !scale_k || !scale_v) return fail(MMDIT_ERR_INVALID_ARG, "FP8 attention: NULL scale");
+  if ((s = check_workspace(workspace, workspace_bytes, mmdit_fp8_attention_workspace_size(batch, heads, seq))) !=
+      MMDIT_OK)
+    return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  if (seq == 0) return MMDIT_OK;
+  pdl_begin_call();
+  const size_t bh = static_cast<size_t>(batch) * heads;
+  Carver c;
+  AttnFp8Problem a;
+  a.act = act, a.batch = batch, a.heads = heads, a.seq = seq, a.seq_pad = static_cast<int>(round_up(seq, 16));
+  a.split = seq;
+  a.q = static_cast<const __nv_bfloat16*>(q), a.k = static_cast<const __nv_bfloat16*>(k);
+  a.v = static_cast<const __nv_bfloat16*>(v);
+  a.q8 = at<uint8_t>(workspace, c.take(bh * seq * 128));
+  a.k8 = at<uint8_t>(workspace, c.take(bh * seq * 128));
+  a.vt8 = at<uint8_t>(workspace, c.take(bh * 128 * a.seq_pad));
+  a.amax = at<float>(workspace, c.take(2 * sizeof(float)));
+  a.scale_q = scale_q, a.scale_k = scale_k, a.scale_v = scale_v;
+  a.out0 = out;
+  ProfScope ps_("fp8_attention", st);
+  MMDIT_CUDA(launch_attention_fp8(a, status_word(workspace), st), "FP8 joint attention");
+  return MMDIT_OK;
+}
+
 size_t mmdit_double_block_bwd_workspace_size(const mmdit_dims* d) {
   BwdPlan p;
   if (check_dims(d) != MMDIT_OK || !plan_block_bwd(d, false, &p)) return 0;

@@ -142,6 +142,22 @@ struct AttnProblem {
 };
 cudaError_t launch_attention(const AttnProblem& p, uint32_t* status, cudaStream_t stream);
 
+// attention_fp8.cu: the joint attention on E4M3 operands (fp8_dot_product_attention): the launcher
+// casts q, k (to q8, k8 [B, H, S, 128]) and v (to vt8 [B, H, 128, seq_pad], seq_pad a multiple of
+// 16) with the given device scales, recording their amax into amax[0..1] (q, k), then
+// O = E4M3(Pt 448) E4M3(v s_v) / (448 s_v) / rowsum(Pt), Pt = exp(S - rowmax), S from the casts.
+struct AttnFp8Problem {
+  int act = 1;  // output type: 0 fp32, 1 bf16
+  int batch = 0, heads = 0, seq = 0, seq_pad = 0, split = 0;
+  const __nv_bfloat16 *q = nullptr, *k = nullptr, *v = nullptr;  // [B, H, S, 128]
+  uint8_t *q8 = nullptr, *k8 = nullptr, *vt8 = nullptr;           // cast codes (workspace)
+  const float *scale_q = nullptr, *scale_k = nullptr, *scale_v = nullptr;
+  float* amax = nullptr;  // [2]
+  void* out0 = nullptr;
+  void* out1 = nullptr;
+};
+cudaError_t launch_attention_fp8(const AttnFp8Problem& p, uint32_t* status, cudaStream_t stream);
+
 // attention_bwd.cu: the joint attention's backward from the forward's log-sum-exp L and the
 // pre-pass's D = rowsum(dO * O): dV = P^T dO, dS = P (dO V^T - D) / sqrt(d), dK = dS^T Q, dQ = dS K,
 // P = exp2(q . k log2(e) / sqrt(d) - L).  dO (and so D and every output) carries the pre-pass's

@@ -335,6 +335,22 @@ mmdit_status mmdit_attention_fwd(int32_t act, int32_t batch, int32_t heads, int3
                                  void *out, void *workspace, size_t workspace_bytes,
                                  void *stream);
 
+/* Joint attention on E4M3 operands, the opt-in fp8_dot_product_attention of [FP8]
+ * §Configuration, FP8 model configuration (the blocks keep attention in bf16, its default):
+ *   S  = E4M3(q scale_q) E4M3(k scale_k)^T / (scale_q scale_k sqrt(d))
+ *   Pt = exp(S - rowmax S)  (fp32; the flash-style running maximum, so each tile's Pt <= 1)
+ *   out = E4M3(Pt 448) E4M3(v scale_v) / (448 scale_v) / rowsum(Pt)   (row sum of the fp32 Pt)
+ * Both products run on E4M3 tensor-core operands with fp32 accumulation.  q, k, v [B, H, S, d]
+ * bf16; scale_q, scale_k, scale_v device fp32 scalars (e.g. delayed scaling's 448 / amax);
+ * out [B, S, H*d] of type `act`.  d must be 128.
+ * workspace >= mmdit_fp8_attention_workspace_size(B, H, S) (the casts). */
+size_t mmdit_fp8_attention_workspace_size(int32_t batch, int32_t heads, int32_t seq);
+mmdit_status mmdit_fp8_attention_fwd(int32_t act, int32_t batch, int32_t heads, int32_t seq,
+                                     int32_t head_dim, const void *q, const void *k, const void *v,
+                                     const float *scale_q, const float *scale_k, const float *scale_v,
+                                     void *out, void *workspace, size_t workspace_bytes,
+                                     void *stream);
+
 /* ---------------------------------------------------------------------------------------
  * Double-stream (joint) block forward ([ARCH] §Model components, 3. MMDiT layer (double
  * block); [API] §Layer specifications, MMDiTLayer).  Per stream s in {img, txt}, each with its

