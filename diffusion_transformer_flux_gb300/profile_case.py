@@ -3,6 +3,10 @@
     python -m diffusion_transformer_flux_gb300.profile_case attention --batch 2 --seq 4608
     python -m diffusion_transformer_flux_gb300.profile_case double_block --seq-img 4096 --seq-txt 512
     python -m diffusion_transformer_flux_gb300.profile_case linear --m 4608 --n 12288 --k 3072
+    python -m diffusion_transformer_flux_gb300.profile_case double_block_bwd --seq-img 4096 --seq-txt 512
+    python -m diffusion_transformer_flux_gb300.profile_case fp8_attention --seq 4608
+    python -m diffusion_transformer_flux_gb300.profile_case head_loss --seq-img 4096
+    python -m diffusion_transformer_flux_gb300.profile_case modulation --jobs 4
 
 Inputs are drawn on the device (N(0,1) activations, N(0,0.02) weights); the case runs
 --iters times and exits 0 only if every kernel finished its waits.
@@ -29,7 +33,9 @@ def _stream_w(D, F, d=128):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["attention", "double_block", "single_block", "linear"])
+    ap.add_argument("case", choices=["attention", "double_block", "single_block", "linear", "double_block_bwd",
+                                     "fp8_attention", "head_loss", "modulation"])
+    ap.add_argument("--jobs", type=int, default=4)
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--seq", type=int, default=4608)
     ap.add_argument("--seq-img", type=int, default=4096)
@@ -44,7 +50,27 @@ def main():
     torch.manual_seed(0)
     L.load()
     wss = []
-    if a.case == "attention":
+    if a.case == "fp8_attention":
+        H = a.hidden // 128
+        q, k, v = (torch.randn(a.batch, H, a.seq, 128, device="cuda").to(torch.bfloat16) for _ in range(3))
+        scales = torch.full((3,), 32.0, device="cuda")
+        out = torch.empty(a.batch, a.seq, a.hidden, device="cuda", dtype=torch.bfloat16)
+        run = lambda: wss.append(L.mmdit_fp8_attention_fwd(q, k, v, scales[0:1], scales[1:2], scales[2:3], out))
+    elif a.case == "head_loss":
+        B, Si, D = a.batch, a.seq_img, a.hidden
+        hw = int(round(Si ** 0.5))
+        dims = L.make_dims(B, Si, 0, D, D // 128, a.mlp, L.MMDIT_BF16)
+        x, vec = _w(B, Si, D, std=1.0), _w(B, D, std=1.0)
+        z0, z1 = (torch.randn(B, 64, hw, hw, device="cuda") for _ in range(2))
+        loss = torch.zeros(1, device="cuda")
+        args = (dims, hw, hw, x, vec, _w(2 * D, D), _w(2 * D), _w(64, D), _w(64), z0, z1, loss)
+        run = lambda: wss.append(L.mmdit_final_layer_loss_fwd(*args))
+    elif a.case == "modulation":
+        D = a.hidden
+        vec = _w(a.batch, D, std=1.0)
+        jobs = [(_w(6 * D, D), _w(6 * D), torch.empty(a.batch, 6 * D, device="cuda")) for _ in range(a.jobs)]
+        run = lambda: L.mmdit_modulation_batched_fwd(vec, jobs)
+    elif a.case == "attention":
         H = a.hidden // 128
         q, k, v = (torch.randn(a.batch, H, a.seq, 128, device="cuda").to(torch.bfloat16) for _ in range(3))
         out = torch.empty(a.batch, a.seq, a.hidden, device="cuda", dtype=torch.bfloat16)
@@ -59,7 +85,17 @@ def main():
         dims = L.make_dims(B, Si, St, D, D // 128, F, L.MMDIT_BF16)
         vec = _w(B, D, std=1.0)
         cos, sin = torch.rand(B, S, 64, device="cuda"), torch.rand(B, S, 64, device="cuda")
-        if a.case == "double_block":
+        if a.case == "double_block_bwd":
+            wi, wt = _stream_w(D, F), _stream_w(D, F)
+            xi, xt = _w(B, Si, D, std=1.0), _w(B, St, D, std=1.0)
+            dyi, dyt = _w(B, Si, D, std=1e-3), _w(B, St, D, std=1e-3)
+            dxi, dxt = torch.empty_like(xi), torch.empty_like(xt)
+            dvec = torch.empty(B, D, device="cuda")
+            g = [{n: torch.empty(tuple(w[n].shape), device="cuda") for n in L.STREAM_W_FIELDS} for w in (wi, wt)]
+            ws = L.workspace(L.mmdit_double_block_bwd_workspace_size(dims))
+            run = lambda: wss.append(L.mmdit_double_block_bwd(dims, wi, wt, vec, cos, sin, xi, xt, dyi, dyt, dxi, dxt,
+                                                              dvec, g[0], g[1], ws=ws))
+        elif a.case == "double_block":
             wi, wt = _stream_w(D, F), _stream_w(D, F)
             xi, xt = _w(B, Si, D, std=1.0), _w(B, St, D, std=1.0)
             yi, yt = torch.empty_like(xi), torch.empty_like(xt)
