@@ -869,20 +869,35 @@ mmdit_status linear_bwd_body(int act, int M, int N, int K, const void* dy, const
   void* dyt = at(scratch, c.take(static_cast<size_t>(N) * Mp * e));
   void* xt = at(scratch, c.take(static_cast<size_t>(K) * Mp * e));
   float* part = at<float>(scratch, c.take(static_cast<size_t>(kColsumChunks) * N * 4));
+  // bf16 with K % 256 == 0: the tensor cores read W, dy and x as stored (MN-major operands);
+  // otherwise the operands are transposed into K-major copies first
+  const bool mn = act == 1 && K % 256 == 0 && N % 8 == 0;
   if (dx) {
-    // dx [M, K] = dy [M, N] W [N, K]: the GEMM's K-major operands are dy and W^T [K, N]
-    MMDIT_CUDA(launch_transpose_pad(act, w, N, K, N, wt, st), "W transpose");
+    // dx [M, K] = dy [M, N] W [N, K]: A = dy (K-major), B = W read as W^T's MN-major form
     GemmProblem g;
-    g.act = act, g.epi = kEpiBias, g.M = M, g.N = K, g.K = N, g.A = dy, g.W = wt, g.ep.out = dx;
+    g.act = act, g.epi = kEpiBias, g.M = M, g.N = K, g.K = N, g.A = dy, g.W = w, g.ep.out = dx;
+    if (mn) {
+      g.b_mn = 1;
+    } else {
+      MMDIT_CUDA(launch_transpose_pad(act, w, N, K, N, wt, st), "W transpose");
+      g.W = wt;
+    }
     MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "dx GEMM");
   }
   if (dw) {
-    // dW [N, K] = dy^T x, contracted over the M rows: operands dy^T [N, Mp] and x^T [K, Mp]
-    MMDIT_CUDA(launch_transpose_pad(act, dy, M, N, Mp, dyt, st), "dy transpose");
-    MMDIT_CUDA(launch_transpose_pad(act, x, M, K, Mp, xt, st), "x transpose");
+    // dW [N, K] = dy^T x, contracted over the M rows
     GemmProblem g;
-    g.act = act, g.epi = kEpiBias, g.M = N, g.N = K, g.K = Mp, g.A = dyt, g.W = xt, g.ep.out = dw;
+    g.act = act, g.epi = kEpiBias, g.M = N, g.N = K, g.ep.out = dw;
     g.ep.out_f32 = 1;
+    if (mn) {
+      // dy [M, N] and x [M, K] are dy^T's and x^T's MN-major forms; rows past M read as zeros
+      g.K = M, g.A = dy, g.W = x, g.a_mn = 1, g.b_mn = 1;
+    } else {
+      // K-major copies dy^T [N, Mp] and x^T [K, Mp], zero-padded to Mp
+      MMDIT_CUDA(launch_transpose_pad(act, dy, M, N, Mp, dyt, st), "dy transpose");
+      MMDIT_CUDA(launch_transpose_pad(act, x, M, K, Mp, xt, st), "x transpose");
+      g.K = Mp, g.A = dyt, g.W = xt;
+    }
     MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "dW GEMM");
   }
   if (db) MMDIT_CUDA(launch_colsum(act, dy, M, N, part, kColsumChunks, db, st), "db column sums");

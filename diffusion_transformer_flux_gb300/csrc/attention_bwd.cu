@@ -111,6 +111,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int k0 = blockIdx.x * kKeyTile;
   const int bh = blockIdx.y;
   const int n_q = (seq + kQryTile - 1) / kQryTile;
+  // The key tiles of one head start their walk over the query tiles at staggered offsets, so
+  // that their dQ additions do not land on the same rows at the same time.
+  const int q_first = static_cast<int>((static_cast<int64_t>(blockIdx.x) * n_q) / gridDim.x);
+  auto q_tile = [&](int i) { const int t = q_first + i; return (t >= n_q ? t - n_q : t) * kQryTile; };
 
   if (threadIdx.x == 0) {
     mbar_init(&sb->kv_full, 1);
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int issued = -1;
       for (int i = 0; i < n_q; ++i) {
         if (!wait(&sb->st_empty, (static_cast<uint32_t>(i) & 1u) ^ 1u)) break;
-        const int q0 = i * kQryTile;
+        const int q0 = q_tile(i);
         mbar_arrive_expect_tx(&sb->st_full, 2 * kQTileBytes + 2 * kTTileBytes + 2 * kQryTile * 4);
         tma_load_3d(smem + kOffQ, &tm_q, &sb->st_full, 0, q0, bh);
         tma_load_3d(smem + kOffQ + kQHalf, &tm_q, &sb->st_full, 64, q0, bh);
@@ -246,7 +250,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t key_byte = static_cast<uint32_t>(row & 63) * 2u;  // byte within the 128-byte line
     for (int i = 0; i < n_q; ++i) {
       const uint32_t ph = static_cast<uint32_t>(i) & 1u;
-      const int q0 = i * kQryTile;
+      const int q0 = q_tile(i);
       // the stage (L, D) was written by the bulk copies: observe its barrier here too
       bool w = wait(&sb->st_full, ph);
       if (w) w = wait(&sb->sp_full, ph);
@@ -322,7 +326,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_ld32_wait(t_dq + 32u, b);
       tc_fence_before();
       mbar_arrive(&sb->dq_empty);
-      const int q0 = i * kQryTile;
+      const int q0 = q_tile(i);
       float* base = dq + (static_cast<size_t>(bh) * seq + q0) * 128 + d;
 #pragma unroll 4
       for (int q = 0; q < 32; ++q)

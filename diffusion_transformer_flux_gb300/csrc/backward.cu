@@ -22,6 +22,8 @@ namespace {
 constexpr int kRowThreads = 128;   // LayerNorm backward: one block per row group, 8 elements per thread
 constexpr int kRowMaxChunks = 8;   // rows of up to 128 * 8 * 8 = 8192 elements
 constexpr int kBwdRowsPerBlock = 32;   // rows of one batch element per block (column sums)
+constexpr int kLnBwdRowsPerBlock = 8;  // LayerNorm backward: rows per block (more blocks in flight)
+constexpr int kColsumGroups = 32;      // column-sum finish: partial rows summed by 32 thread rows
 
 // The attention backward's gradient scale from amax(dO): 2^(8 - ceil(log2 amax)), 1 for 0 (headroom for dS = p (dP - D) / sqrt(d) in fp16).
 __device__ __forceinline__ float grad_scale_of(const float* amax) {
@@ -65,11 +67,11 @@ template <typename TX, typename TG, int NCT>
 __global__ void __launch_bounds__(kRowThreads) ln_modulate_bwd_kernel(LnBwdJob job, int dim, float eps) {
   pdl_wait();
   __shared__ float red[2 * (kRowThreads / 32)];
-  const int bpb = (job.rpb + kBwdRowsPerBlock - 1) / kBwdRowsPerBlock;
+  const int bpb = (job.rpb + kLnBwdRowsPerBlock - 1) / kLnBwdRowsPerBlock;
   const int b = blockIdx.x / bpb;
-  const int r0 = b * job.rpb + (blockIdx.x - b * bpb) * kBwdRowsPerBlock;
+  const int r0 = b * job.rpb + (blockIdx.x - b * bpb) * kLnBwdRowsPerBlock;
   const int r_end = (b + 1) * job.rpb;
-  const int r1 = r0 + kBwdRowsPerBlock < r_end ? r0 + kBwdRowsPerBlock : r_end;
+  const int r1 = r0 + kLnBwdRowsPerBlock < r_end ? r0 + kLnBwdRowsPerBlock : r_end;
   const float* sc = job.scale + b * job.mod_bstride;
   float dsc[NCT][8], dsh[NCT][8], opc[NCT][8];
 #pragma unroll
@@ -84,16 +86,23 @@ __global__ void __launch_bounds__(kRowThreads) ln_modulate_bwd_kernel(LnBwdJob j
       for (int e = 0; e < 8; ++e) opc[c][e] = 1.f + m[e];
     }
   }
-  for (int r = r0; r < r1; ++r) {
+  // x and dh of the next row are loaded while this row is reduced
+  Raw8<TX> rx[NCT];
+  Raw8<TG> rg[NCT];
+  auto load_row = [&](int r, Raw8<TX>(&ox)[NCT], Raw8<TG>(&og)[NCT]) {
     const TX* xr = static_cast<const TX*>(job.x) + static_cast<size_t>(r) * dim;
     const TG* gr = static_cast<const TG*>(job.dh) + static_cast<size_t>(r) * dim;
-    Raw8<TX> rx[NCT];
-    Raw8<TG> rg[NCT];
 #pragma unroll
     for (int c = 0; c < NCT; ++c) {
       const int k = (c * kRowThreads + threadIdx.x) * 8;
-      if (k < dim) rx[c].load(xr + k), rg[c].load(gr + k);
+      if (k < dim) ox[c].load(xr + k), og[c].load(gr + k);
     }
+  };
+  if (r0 < r1) load_row(r0, rx, rg);
+  for (int r = r0; r < r1; ++r) {
+    Raw8<TX> nx[NCT];
+    Raw8<TG> ng[NCT];
+    if (r + 1 < r1) load_row(r + 1, nx, ng);
     // mean and variance of x, two passes over the registers as the forward does
     float s = 0.f, unused = 0.f;
 #pragma unroll
@@ -155,6 +164,8 @@ __global__ void __launch_bounds__(kRowThreads) ln_modulate_bwd_kernel(LnBwdJob j
         store8(dxr + k, acc);
       }
     }
+#pragma unroll
+    for (int c = 0; c < NCT; ++c) rx[c] = nx[c], rg[c] = ng[c];
   }
   float* p = job.part + static_cast<size_t>(blockIdx.x) * 2 * dim;
 #pragma unroll
@@ -173,19 +184,32 @@ struct ColsumOut {
   int accumulate;
 };
 
-__global__ void batch_colsum_finish_kernel(const float* __restrict__ part, int bpb, int dim,
-                                           ColsumOut o) {
+// Block (32, kColsumGroups): thread (x, y) sums partials y, y + 32, ... of column 32 blockIdx.x + x
+// in order; thread row 0 then adds the 32 group sums in order (a fixed-order two-level sum).
+__global__ void __launch_bounds__(32 * kColsumGroups) batch_colsum_finish_kernel(const float* __restrict__ part,
+                                                                                 int bpb, int dim, ColsumOut o) {
   pdl_wait();
-  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  __shared__ float grp[kColsumGroups][33];
+  const int k = blockIdx.x * 32 + threadIdx.x;
   const int b = blockIdx.y;
-  if (k >= dim) return;
   for (int v = 0; v < o.nvec; ++v) {
     if (!o.out[v]) continue;  // a gradient the caller did not ask for
     float acc = 0.f;
-    for (int i = 0; i < bpb; ++i)
-      acc += part[(static_cast<size_t>(b) * bpb + i) * o.nvec * dim + static_cast<size_t>(v) * dim + k];
-    float* dst = o.out[v] + b * o.out_bstride + k;
-    *dst = o.accumulate ? *dst + acc : acc;
+    if (k < dim) {
+      const float* col = part + static_cast<size_t>(b) * bpb * o.nvec * dim + static_cast<size_t>(v) * dim + k;
+#pragma unroll 4
+      for (int i = threadIdx.y; i < bpb; i += kColsumGroups) acc += col[static_cast<size_t>(i) * o.nvec * dim];
+    }
+    grp[threadIdx.y][threadIdx.x] = acc;
+    __syncthreads();
+    if (threadIdx.y == 0 && k < dim) {
+      float t = 0.f;
+#pragma unroll 8
+      for (int g = 0; g < kColsumGroups; ++g) t += grp[g][threadIdx.x];
+      float* dst = o.out[v] + b * o.out_bstride + k;
+      *dst = o.accumulate ? *dst + t : t;
+    }
+    __syncthreads();
   }
 }
 
@@ -434,7 +458,8 @@ __global__ void untranspose_vt_kernel(const __half* __restrict__ vt, int seq, in
 // ----------------------------------------------------------------------------- modulation
 // m = SiLU(vec) W^T + b.  dW[n, k] = sum_b dm[b, n] sv[b, k] (fp32, written once), db[n] =
 // sum_b dm[b, n]; sv = SiLU(vec) as the forward used it (rounded to bf16 in bf16 mode).
-// One warp per row n, 8 columns per lane per step; sv in shared memory [batch, dim].
+// One warp per row n, 4 consecutive columns per lane per step (a warp covers 128 consecutive
+// columns: conflict-free shared reads, 512-byte stores); sv in shared memory [batch, dim].
 template <typename T>
 __global__ void __launch_bounds__(256) modulation_wgrad_kernel(const T* __restrict__ vec, const float* __restrict__ dm,
                                                                int batch, int rows, int dim,
@@ -458,14 +483,14 @@ __global__ void __launch_bounds__(256) modulation_wgrad_kernel(const T* __restri
       for (int bb = 0; bb < batch; ++bb) s += dmb[bb];
       db[n] = s;
     }
-    for (int k = lane * 8; dw && k < dim; k += 32 * 8) {
-      float o[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] = 0.f;
-      for (int bb = 0; bb < batch; ++bb)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = fmaf(dmb[bb], sv[bb * dim + k + e], o[e]);
-      store8(dw + static_cast<size_t>(n) * dim + k, o);
+    for (int k = lane * 4; dw && k < dim; k += 32 * 4) {
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int bb = 0; bb < batch; ++bb) {
+        const float4 v = *reinterpret_cast<const float4*>(sv + bb * dim + k);
+        o.x = fmaf(dmb[bb], v.x, o.x), o.y = fmaf(dmb[bb], v.y, o.y);
+        o.z = fmaf(dmb[bb], v.z, o.z), o.w = fmaf(dmb[bb], v.w, o.w);
+      }
+      *reinterpret_cast<float4*>(dw + static_cast<size_t>(n) * dim + k) = o;
     }
   }
 }
@@ -487,33 +512,52 @@ __global__ void __launch_bounds__(128) modulation_dvec_partial_kernel(const T* _
   for (int bb = 0; bb < 8; ++bb)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[bb][e] = 0.f;
-  for (int n = n0; n < n1; ++n) {
-    float wv[8];
-    load8(w + static_cast<size_t>(n) * dim + k, wv);
+  // rows in ascending order; four rows' loads are issued before their products
+  auto rows_from = [&](int n, int count) {
+    float wv[4][8];
 #pragma unroll
-    for (int bb = 0; bb < 8; ++bb) {
-      if (bb < batch) {
-        const float d = __ldg(dm + static_cast<size_t>(bb) * rows + n);
+    for (int u = 0; u < 4; ++u)
+      if (u < count) load8(w + static_cast<size_t>(n + u) * dim + k, wv[u]);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[bb][e] = fmaf(d, wv[e], acc[bb][e]);
+    for (int u = 0; u < 4; ++u) {
+      if (u >= count) break;
+#pragma unroll
+      for (int bb = 0; bb < 8; ++bb) {
+        if (bb < batch) {
+          const float d = __ldg(dm + static_cast<size_t>(bb) * rows + n + u);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[bb][e] = fmaf(d, wv[u][e], acc[bb][e]);
+        }
       }
     }
-  }
+  };
+  int n = n0;
+  for (; n + 4 <= n1; n += 4) rows_from(n, 4);
+  if (n < n1) rows_from(n, n1 - n);
 #pragma unroll
   for (int bb = 0; bb < 8; ++bb)
     if (bb < batch) store8(part + (static_cast<size_t>(blockIdx.y) * batch + bb) * dim + k, acc[bb]);
 }
 
+// Block (32, kColsumGroups) over 32 columns: the chunk partials in the same two-level fixed order
+// as batch_colsum_finish_kernel, then the SiLU derivative.
 template <typename T>
-__global__ void modulation_dvec_finish_kernel(const float* __restrict__ part, const T* __restrict__ vec,
-                                              int chunks, int batch, int dim, int accumulate,
-                                              float* __restrict__ dvec) {
+__global__ void __launch_bounds__(32 * kColsumGroups) modulation_dvec_finish_kernel(
+    const float* __restrict__ part, const T* __restrict__ vec, int chunks, int batch, int dim, int accumulate,
+    float* __restrict__ dvec) {
   pdl_wait();
-  const int k = blockIdx.x * blockDim.x + threadIdx.x;
+  __shared__ float grp[kColsumGroups][33];
+  const int k = blockIdx.x * 32 + threadIdx.x;
   const int bb = blockIdx.y;
-  if (k >= dim || bb >= batch) return;
+  float g = 0.f;
+  if (k < dim)
+    for (int i = threadIdx.y; i < chunks; i += kColsumGroups) g += part[(static_cast<size_t>(i) * batch + bb) * dim + k];
+  grp[threadIdx.y][threadIdx.x] = g;
+  __syncthreads();
+  if (threadIdx.y != 0 || k >= dim) return;
   float acc = 0.f;
-  for (int i = 0; i < chunks; ++i) acc += part[(static_cast<size_t>(i) * batch + bb) * dim + k];
+#pragma unroll 8
+  for (int i = 0; i < kColsumGroups; ++i) acc += grp[i][threadIdx.x];
   const float v = to_f32(vec[static_cast<size_t>(bb) * dim + k]);
   const float sg = 1.f / (1.f + expf(-v));
   const float d = acc * sg * (1.f + v * (1.f - sg));
@@ -538,7 +582,7 @@ __global__ void convert_kernel(const TI* __restrict__ in, int64_t n, TO* __restr
 
 // Bytes of the partial-sum buffer the LayerNorm-modulate backward needs.
 size_t ln_modulate_bwd_part_bytes(int batch, int rows_per_batch, int dim) {
-  const int bpb = (rows_per_batch + kBwdRowsPerBlock - 1) / kBwdRowsPerBlock;
+  const int bpb = (rows_per_batch + kLnBwdRowsPerBlock - 1) / kLnBwdRowsPerBlock;
   return static_cast<size_t>(batch) * bpb * 2 * dim * sizeof(float);
 }
 
@@ -551,7 +595,7 @@ cudaError_t launch_ln_modulate_bwd(int act, int x_f32, const void* x, const void
   if (batch == 0 || rows_per_batch == 0) return cudaSuccess;
   const int chunks = (dim + kRowThreads * 8 - 1) / (kRowThreads * 8);
   if (chunks > kRowMaxChunks || dim % 8 != 0) return cudaErrorInvalidValue;
-  const int bpb = (rows_per_batch + kBwdRowsPerBlock - 1) / kBwdRowsPerBlock;
+  const int bpb = (rows_per_batch + kLnBwdRowsPerBlock - 1) / kLnBwdRowsPerBlock;
   const LnBwdJob job{x, dh, scale, mod_bstride, dx, part, batch * rows_per_batch, rows_per_batch};
   const dim3 grid(batch * bpb);
   cudaError_t err = cudaSuccess;
@@ -582,7 +626,8 @@ cudaError_t launch_ln_modulate_bwd(int act, int x_f32, const void* x, const void
   o.out_bstride = mod_bstride;
   o.nvec = 2;
   o.accumulate = accumulate;
-  err = launch_pdl(batch_colsum_finish_kernel, dim3((dim + 255) / 256, batch), dim3(256), 0, stream, part, bpb, dim, o);
+  err = launch_pdl(batch_colsum_finish_kernel, dim3((dim + 31) / 32, batch), dim3(32, kColsumGroups), 0, stream, part,
+                   bpb, dim, o);
   if (err != cudaSuccess) return err;
   count_launch();
   return cudaSuccess;
@@ -617,7 +662,8 @@ cudaError_t launch_gated_residual_bwd(int act, const float* dy, const void* f, c
   o.out_bstride = gate_bstride;
   o.nvec = 1;
   o.accumulate = 0;
-  err = launch_pdl(batch_colsum_finish_kernel, dim3((dim + 255) / 256, batch), dim3(256), 0, stream, part, bpb, dim, o);
+  err = launch_pdl(batch_colsum_finish_kernel, dim3((dim + 31) / 32, batch), dim3(32, kColsumGroups), 0, stream, part,
+                   bpb, dim, o);
   if (err != cudaSuccess) return err;
   count_launch();
   return cudaSuccess;
@@ -664,7 +710,8 @@ cudaError_t launch_qk_norm_rope_bwd(int act, const QkBwdArgs& a, float* dg_q, fl
   o.nvec = 2;
   o.accumulate = 0;
   // the block partials are [grid, 2, 128]: one "batch" of `grid` blocks
-  err = launch_pdl(batch_colsum_finish_kernel, dim3(1, 1), dim3(128), 0, stream, a.part, grid, 128, o);
+  err = launch_pdl(batch_colsum_finish_kernel, dim3(128 / 32, 1), dim3(32, kColsumGroups), 0, stream, a.part, grid,
+                   128, o);
   if (err != cudaSuccess) return err;
   count_launch();
   return cudaSuccess;
@@ -749,12 +796,12 @@ cudaError_t launch_modulation_bwd(int act, const void* vec, const void* w, const
                        static_cast<const float*>(w), dm, batch, rows, dim, part);
     if (err != cudaSuccess) return err;
     count_launch();
-    const dim3 g2((dim + 255) / 256, batch);
+    const dim3 g2((dim + 31) / 32, batch), b2(32, kColsumGroups);
     if (act == 1)
-      err = launch_pdl(modulation_dvec_finish_kernel<__nv_bfloat16>, g2, dim3(256), 0, stream, part,
+      err = launch_pdl(modulation_dvec_finish_kernel<__nv_bfloat16>, g2, b2, 0, stream, part,
                        static_cast<const __nv_bfloat16*>(vec), chunks, batch, dim, accumulate, dvec);
     else
-      err = launch_pdl(modulation_dvec_finish_kernel<float>, g2, dim3(256), 0, stream, part,
+      err = launch_pdl(modulation_dvec_finish_kernel<float>, g2, b2, 0, stream, part,
                        static_cast<const float*>(vec), chunks, batch, dim, accumulate, dvec);
     if (err != cudaSuccess) return err;
     count_launch();

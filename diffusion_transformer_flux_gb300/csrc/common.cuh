@@ -193,6 +193,20 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand stored with the 128-byte swizzle: each
+// 128-byte line holds 64 consecutive M (or N) elements of one k, 8 lines make a 1024-byte atom,
+// atoms of the next 8 k follow at 1024 bytes (stride offset), and the next 64 M (or N) elements
+// start `mn_stride` bytes further (leading offset).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
 // Instruction descriptor: fp32 accumulator (bits 4-5 = 1), A/B formats (bits 7-9, 10-12),
 // both operands K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
 // Formats: kind::f16 -> 1 = bf16; kind::tf32 -> 2 = tf32; kind::f8f6f4 -> 0 = E4M3, 1 = E5M2.
@@ -203,6 +217,9 @@ __host__ __device__ constexpr uint32_t make_idesc(int M, int N) {
   return (1u << 4) | (fmt_a << 7) | (fmt << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
+// Bits 15 and 16 of the instruction descriptor: A (resp. B) read MN-major instead of K-major.
+constexpr uint32_t kIdescAMnMajor = 1u << 15;
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
 // kind::f16 with fp16 (format 0) A and B operands.
 __host__ __device__ constexpr uint32_t make_idesc_fp16(int M, int N) {
   return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);

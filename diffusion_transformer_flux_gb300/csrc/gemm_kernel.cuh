@@ -509,7 +509,7 @@ cudaError_t run_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream
   return cudaGetLastError();
 }
 
-template <int KIND, int BN, int EPI>
+template <int KIND, int BN, int EPI, int MAJ = 0>
 cudaError_t run_gemm_pair(const GemmProblem& p, uint32_t* status, cudaStream_t stream);
 
 // GEMMs that take the CTA-pair kernel (gemm_pair.cuh): the block linears' epilogues and plain
@@ -527,6 +527,16 @@ inline bool use_pair(const GemmProblem& p) {
 // Picks the tile width for N and the epilogue, then launches.
 template <int KIND>
 cudaError_t dispatch_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream) {
+  if (p.a_mn || p.b_mn) {
+    // transposed operands: the pair kernel's plain-bias products only
+    if constexpr (KIND == kKindF16) {
+      if (p.epi != kEpiBias || p.N % 256 != 0 || p.M1 > 0 || p.splits != 1) return cudaErrorInvalidValue;
+      if (p.a_mn && p.b_mn) return run_gemm_pair<KIND, 256, kEpiBias, 3>(p, status, stream);
+      if (p.b_mn) return run_gemm_pair<KIND, 256, kEpiBias, 2>(p, status, stream);
+      return run_gemm_pair<KIND, 256, kEpiBias, 1>(p, status, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
   if constexpr (KIND == kKindF16) {
     if (use_pair(p)) {
       switch (p.epi) {

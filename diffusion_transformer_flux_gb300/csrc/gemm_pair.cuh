@@ -16,6 +16,11 @@
 //            accumulator-empty barrier.
 // Every mbarrier wait is bounded (common.cuh); cluster barriers after set-up and before
 // teardown keep either CTA from leaving while the other may still address it.
+//
+// MAJ selects how the operands are stored (16-bit kinds): bit 0 set, A is held as A^T [K, M];
+// bit 1 set, W is held as W^T [K, N].  Such an operand is loaded as two 64-wide MN blocks of
+// 64 k lines each (the same 16 KB per CTA and stage) and read by the MMA through MN-major
+// descriptors, so a transposed product (a weight or input gradient) needs no transpose pass.
 #pragma once
 
 #include "gemm_kernel.cuh"
@@ -32,7 +37,7 @@ struct PairCfg {
   static constexpr int kSmemBytes = kStages * kStageBytes + 256 + 1024;
 };
 
-template <int KIND, int BN, int EPI>
+template <int KIND, int BN, int EPI, int MAJ = 0>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<EPI>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_b0,
                      const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b1,
@@ -43,7 +48,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<EPI>(),
   constexpr int kBK = 128 / KindTraits<KIND>::kEltBytes;    // elements per 128-byte K slice
   constexpr int kUmmaK = 32 / KindTraits<KIND>::kEltBytes;  // K of one tcgen05.mma
   constexpr int kKSteps = kBK / kUmmaK;
-  constexpr uint32_t kIdesc = make_idesc<KIND>(2 * kBM, BN);
+  constexpr uint32_t kIdesc = make_idesc<KIND>(2 * kBM, BN) | ((MAJ & 1) ? kIdescAMnMajor : 0u) |
+                              ((MAJ & 2) ? kIdescBMnMajor : 0u);
+  static_assert(MAJ == 0 || (KindTraits<KIND>::kEltBytes == 2 && BN == 256), "MN-major: 16-bit kinds, BN 256");
+  constexpr int kMnBlock = 128 / KindTraits<KIND>::kEltBytes;  // MN elements per 128-byte line
+  constexpr uint32_t kMnBoxBytes = static_cast<uint32_t>(kBK) * 128u;  // one MN block of kBK k lines
   constexpr int kEpiWarps = 4 * EpiGroups<EPI>::value;
 
   extern __shared__ uint8_t smem_raw[];
@@ -119,8 +128,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<EPI>(),
           uint8_t* sa = smem + stage * Cfg::kStageBytes;
           const uint32_t bar = full_leader + static_cast<uint32_t>(stage * sizeof(uint64_t));
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::kStageBytes);
-          tma_load_2d_pair(sa, ma, bar, kb * kBK, m0);
-          tma_load_2d_pair(sa + Cfg::kABytes, mw, bar, kb * kBK, nb * BN + static_cast<int>(rank) * (BN / 2));
+          const int n_base = nb * BN + static_cast<int>(rank) * (BN / 2);
+          if constexpr ((MAJ & 1) != 0) {
+            tma_load_2d_pair(sa, ma, bar, m0, kb * kBK);
+            tma_load_2d_pair(sa + kMnBoxBytes, ma, bar, m0 + kMnBlock, kb * kBK);
+          } else {
+            tma_load_2d_pair(sa, ma, bar, kb * kBK, m0);
+          }
+          if constexpr ((MAJ & 2) != 0) {
+            tma_load_2d_pair(sa + Cfg::kABytes, mw, bar, n_base, kb * kBK);
+            tma_load_2d_pair(sa + Cfg::kABytes + kMnBoxBytes, mw, bar, n_base + kMnBlock, kb * kBK);
+          } else {
+            tma_load_2d_pair(sa + Cfg::kABytes, mw, bar, kb * kBK, n_base);
+          }
           last_parity[stage] = static_cast<int>(phase);
           if (++stage == Cfg::kStages) stage = 0, phase ^= 1;
         }
@@ -152,10 +172,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<EPI>(),
           tc_fence_after();
           const uint32_t sa = smem_addr(smem + stage * Cfg::kStageBytes);
           const uint32_t sb = sa + Cfg::kABytes;
+          // K step k: 32 bytes into each 128-byte line (K-major), or kUmmaK lines further (MN-major)
 #pragma unroll
-          for (int k = 0; k < kKSteps; ++k)
-            tc_mma_pair<KIND>(d_tmem, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32),
-                              kIdesc, (kb != 0 || k != 0) ? 1u : 0u);
+          for (int k = 0; k < kKSteps; ++k) {
+            const uint64_t da = (MAJ & 1) ? sdesc_mnmajor_sw128(sa + k * kUmmaK * 128, kMnBoxBytes)
+                                          : sdesc_kmajor_sw128(sa + k * 32);
+            const uint64_t db = (MAJ & 2) ? sdesc_mnmajor_sw128(sb + k * kUmmaK * 128, kMnBoxBytes)
+                                          : sdesc_kmajor_sw128(sb + k * 32);
+            tc_mma_pair<KIND>(d_tmem, da, db, kIdesc, (kb != 0 || k != 0) ? 1u : 0u);
+          }
           tc_commit_pair_mc(&empty[stage], 0x3);
           if (++stage == Cfg::kStages) stage = 0, phase ^= 1;
         }
@@ -204,8 +229,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<EPI>(),
 }
 
 // Host side: 256 x BN pair tiles; N % BN == 0 and no split K.  The grid is as many pairs as can
-// be resident at once (every pair walks its share of the tile list).
-template <int KIND, int BN, int EPI>
+// be resident at once (every pair walks its share of the tile list).  MAJ as for the kernel.
+template <int KIND, int BN, int EPI, int MAJ>
 cudaError_t run_gemm_pair(const GemmProblem& p, uint32_t* status, cudaStream_t stream) {
   using Cfg = PairCfg<BN>;
   constexpr int kElt = KindTraits<KIND>::kEltBytes;
@@ -220,12 +245,27 @@ cudaError_t run_gemm_pair(const GemmProblem& p, uint32_t* status, cudaStream_t s
   const uint64_t da0[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.M)};
   const uint64_t db[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
   const uint64_t da1[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(two ? p.M1 : p.M)};
-  if (!encode_tmap(&ta0, dt, 2, p.A, da0, stride, box_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap(&tb0, dt, 2, p.W, db, stride, box_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap(&ta1, dt, 2, two ? p.A1 : p.A, da1, stride, box_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap(&tb1, dt, 2, two ? p.W1 : p.W, db, stride, box_b, CU_TENSOR_MAP_SWIZZLE_128B))
+  if constexpr (MAJ != 0) {
+    // transposed operands: [K, M] and [K, N] tensors read in (64 MN x kBK k) boxes
+    if (two || (p.a_mn && p.M % 8 != 0)) return cudaErrorInvalidValue;
+    const uint32_t box_mn[2] = {128u / kElt, static_cast<uint32_t>(kBK)};
+    const uint64_t dat[2] = {static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.K)};
+    const uint64_t dbt[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K)};
+    const uint64_t sat[1] = {static_cast<uint64_t>(p.M) * kElt};
+    const uint64_t sbt[1] = {static_cast<uint64_t>(p.N) * kElt};
+    const bool ok_a = (MAJ & 1) ? encode_tmap(&ta0, dt, 2, p.A, dat, sat, box_mn, CU_TENSOR_MAP_SWIZZLE_128B)
+                                : encode_tmap(&ta0, dt, 2, p.A, da0, stride, box_a, CU_TENSOR_MAP_SWIZZLE_128B);
+    const bool ok_b = (MAJ & 2) ? encode_tmap(&tb0, dt, 2, p.W, dbt, sbt, box_mn, CU_TENSOR_MAP_SWIZZLE_128B)
+                                : encode_tmap(&tb0, dt, 2, p.W, db, stride, box_b, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok_a || !ok_b) return cudaErrorInvalidValue;
+    ta1 = ta0, tb1 = tb0;
+  } else if (!encode_tmap(&ta0, dt, 2, p.A, da0, stride, box_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
+             !encode_tmap(&tb0, dt, 2, p.W, db, stride, box_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
+             !encode_tmap(&ta1, dt, 2, two ? p.A1 : p.A, da1, stride, box_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
+             !encode_tmap(&tb1, dt, 2, two ? p.W1 : p.W, db, stride, box_b, CU_TENSOR_MAP_SWIZZLE_128B)) {
     return cudaErrorInvalidValue;
-  auto kern = gemm_pair_kernel<KIND, BN, EPI>;
+  }
+  auto kern = gemm_pair_kernel<KIND, BN, EPI, MAJ>;
   static int configured_device = -1;
   static int max_pairs = 0;
   int dev = 0;

@@ -65,6 +65,9 @@ struct GemmProblem {
   const void* W = nullptr;  // [N, K]
   EpiArgs ep;
   int splits = 1;  // K split into this many ranges (kEpiPartial only), one work item each
+  // Operands stored MN-major (bf16, kEpiBias, N % 256 == 0, no second problem): with a_mn, A is
+  // held as A^T [K, M] (M contiguous, M % 8 == 0); with b_mn, W is held as W^T [K, N].
+  int a_mn = 0, b_mn = 0;
   // optional second problem with the same N, K and epilogue kind, run in the same launch
   int M1 = 0;
   const void* A1 = nullptr;  // [M1, K]
