@@ -910,7 +910,7 @@ struct BwdPlan {
   BlockPlan f;
   size_t h1[2], qkv_pre[2], a[2], u_pre[2], fo[2], ytmp[2];
   size_t dx1[2], df[2], du[2], dh[2], dO[2], dqkv[2], dm[2];
-  size_t lse, dsum, doh, dot, qt, kt, v, dq, dk, dv, amax;
+  size_t lse, dsum, doh, q16, k16, v, dq, dk, dv, amax;
   size_t part, lin;
   size_t total;
 };
@@ -933,8 +933,8 @@ bool plan_block_bwd(const mmdit_dims* d, bool single, BwdPlan* p) {
   }
   // L and D are read in 64-row tiles by bulk copies: 64 floats of slack past the end
   p->lse = c.take((B * H * Sp + 64) * 4), p->dsum = c.take((B * H * Sp + 64) * 4);
-  p->doh = c.take(B * H * S * 128 * 2), p->dot = c.take(B * H * 128 * Sp * 2);
-  p->qt = c.take(B * H * 128 * Sp * 2), p->kt = c.take(B * H * 128 * Sp * 2);
+  // the attention backward's fp16 operands, [B, H, S, 128] each
+  p->doh = c.take(B * H * S * 128 * 2), p->q16 = c.take(B * H * S * 128 * 2), p->k16 = c.take(B * H * S * 128 * 2);
   p->v = c.take(B * H * S * 128 * 2);
   p->dq = c.take(B * H * S * 128 * 4), p->dk = c.take(B * H * S * 128 * 4), p->dv = c.take(B * H * S * 128 * 4);
   p->amax = c.take(256);
@@ -1078,19 +1078,17 @@ mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, cons
     for (int i = 0; i < ns; ++i)
       MMDIT_CUDA(launch_attn_bwd_pre(at<__nv_bfloat16>(ws, p.o[i]), at<__nv_bfloat16>(ws, bp.dO[i]), B, rpb[i], S,
                                      p.S_pad, off[i], H, amax, at<float>(ws, bp.dsum),
-                                     at<__nv_bfloat16>(ws, bp.doh), st), "attention pre-pass");
-    MMDIT_CUDA(launch_transpose_v(at<__nv_bfloat16>(ws, p.k), bh, S, p.S_pad, at<__half>(ws, bp.kt), st), "K^T");
-    MMDIT_CUDA(launch_transpose_v(at<__nv_bfloat16>(ws, p.q), bh, S, p.S_pad, at<__half>(ws, bp.qt), st), "Q^T");
-    MMDIT_CUDA(launch_transpose_v(at<__nv_bfloat16>(ws, bp.doh), bh, S, p.S_pad, at<__half>(ws, bp.dot), st),
-               "dO^T");
-    MMDIT_CUDA(launch_untranspose_vt(at<__half>(ws, p.vt), bh, S, p.S_pad, at<__nv_bfloat16>(ws, bp.v), st), "V");
+                                     at<__half>(ws, bp.doh), st), "attention pre-pass");
+    MMDIT_CUDA(launch_qk_to_f16(at<__nv_bfloat16>(ws, p.q), at<__nv_bfloat16>(ws, p.k),
+                                static_cast<int64_t>(bh) * S * 128, at<__half>(ws, bp.q16), at<__half>(ws, bp.k16), st),
+               "Q, K to fp16");
+    MMDIT_CUDA(launch_untranspose_vt(at<__half>(ws, p.vt), bh, S, p.S_pad, at<__half>(ws, bp.v), st), "V");
   }
   {
     AttnBwdProblem a;
     a.batch = B, a.heads = H, a.seq = S, a.seq_pad = p.S_pad;
-    a.q = at<__nv_bfloat16>(ws, p.q), a.k = at<__nv_bfloat16>(ws, p.k), a.v = at<__nv_bfloat16>(ws, bp.v);
-    a.dout = at<__nv_bfloat16>(ws, bp.doh);
-    a.kt = at<__half>(ws, bp.kt), a.qt = at<__half>(ws, bp.qt), a.dout_t = at<__half>(ws, bp.dot);
+    a.q = at<__half>(ws, bp.q16), a.k = at<__half>(ws, bp.k16), a.v = at<__half>(ws, bp.v);
+    a.dout = at<__half>(ws, bp.doh);
     a.lse = at<float>(ws, bp.lse), a.dsum = at<float>(ws, bp.dsum);
     a.dq = at<float>(ws, bp.dq), a.dk = at<float>(ws, bp.dk), a.dv = at<float>(ws, bp.dv);
     ProfScope ps_("bwd.attention", st);

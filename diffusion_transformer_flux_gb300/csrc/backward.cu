@@ -409,7 +409,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const T* __restrict__ o, const T* __restrict__ dout,
                                                            int batch, int seq_s, int seq_joint, int seq_pad,
                                                            int seq_offset, int heads, const float* __restrict__ amax,
-                                                           float* __restrict__ Dsum, __nv_bfloat16* __restrict__ doh) {
+                                                           float* __restrict__ Dsum, __half* __restrict__ doh) {
   pdl_wait();
   const float g = grad_scale_of(amax);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -430,16 +430,15 @@ __global__ void __launch_bounds__(256) attn_bwd_pre_kernel(const T* __restrict__
     acc = warp_sum(acc);
     const size_t bh = static_cast<size_t>(b) * heads + h;
     if (lane == 0) Dsum[bh * seq_pad + seq_offset + s] = acc;
-    uint2 pk;
-    pk.x = pack_bf16x2(d4[0], d4[1]);
-    pk.y = pack_bf16x2(d4[2], d4[3]);
+    uint2 pk;  // the scaled dO in fp16 (the attention backward's operand)
+    pk.x = pack_half2(d4[0], d4[1]);
+    pk.y = pack_half2(d4[2], d4[3]);
     *reinterpret_cast<uint2*>(doh + (bh * seq_joint + seq_offset + s) * 128 + 4 * lane) = pk;
   }
 }
 
-// V [BH, S, 128] bf16 from V^T [BH, 128, S_pad] (fp16 holding bf16-rounded values: exact).
-__global__ void untranspose_vt_kernel(const __half* __restrict__ vt, int seq, int seq_pad,
-                                      __nv_bfloat16* __restrict__ v) {
+// V [BH, S, 128] fp16 from V^T [BH, 128, S_pad] fp16.
+__global__ void untranspose_vt_kernel(const __half* __restrict__ vt, int seq, int seq_pad, __half* __restrict__ v) {
   pdl_wait();
   __shared__ float tile[32][33];
   const size_t bh = blockIdx.z;
@@ -451,7 +450,23 @@ __global__ void untranspose_vt_kernel(const __half* __restrict__ vt, int seq, in
   __syncthreads();
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int s = s0 + i;
-    if (s < seq) v[(bh * seq + s) * 128 + j0 + threadIdx.x] = __float2bfloat16_rn(tile[threadIdx.x][i]);
+    if (s < seq) v[(bh * seq + s) * 128 + j0 + threadIdx.x] = __float2half_rn(tile[threadIdx.x][i]);
+  }
+}
+
+// q16 = q, k16 = k (bf16 -> fp16), 8 elements per thread.
+__global__ void qk_to_f16_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, int64_t n,
+                                 __half* __restrict__ q16, __half* __restrict__ k16) {
+  pdl_wait();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x * 8;
+  for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8; i < 2 * n; i += stride) {
+    const bool second = i >= n;
+    const int64_t j = second ? i - n : i;
+    float v[8];
+    load8((second ? k : q) + j, v);
+    uint4 o;
+    o.x = pack_half2(v[0], v[1]), o.y = pack_half2(v[2], v[3]), o.z = pack_half2(v[4], v[5]), o.w = pack_half2(v[6], v[7]);
+    *reinterpret_cast<uint4*>((second ? k16 : q16) + j) = o;
   }
 }
 
@@ -736,7 +751,7 @@ cudaError_t launch_grad_amax(const __nv_bfloat16* x, int64_t n, float* amax, boo
 
 cudaError_t launch_attn_bwd_pre(const __nv_bfloat16* o, const __nv_bfloat16* dout, int batch, int seq_s,
                                 int seq_joint, int seq_pad, int seq_offset, int heads, const float* amax,
-                                float* Dsum, __nv_bfloat16* doh, cudaStream_t stream) {
+                                float* Dsum, __half* doh, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(batch) * seq_s * heads;
   if (rows == 0) return cudaSuccess;
   const int grid = blocks_for(rows, 8, num_sms() * 8);
@@ -747,10 +762,20 @@ cudaError_t launch_attn_bwd_pre(const __nv_bfloat16* o, const __nv_bfloat16* dou
   return cudaSuccess;
 }
 
-cudaError_t launch_untranspose_vt(const __half* vt, int bh, int seq, int seq_pad, __nv_bfloat16* v,
-                                  cudaStream_t stream) {
+cudaError_t launch_untranspose_vt(const __half* vt, int bh, int seq, int seq_pad, __half* v, cudaStream_t stream) {
   const dim3 grid((seq + 31) / 32, 4, bh), block(32, 8);
   cudaError_t err = launch_pdl(untranspose_vt_kernel, grid, block, 0, stream, vt, seq, seq_pad, v);
+  if (err != cudaSuccess) return err;
+  count_launch();
+  return cudaSuccess;
+}
+
+cudaError_t launch_qk_to_f16(const __nv_bfloat16* q, const __nv_bfloat16* k, int64_t n, __half* q16, __half* k16,
+                             cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  if (n % 8 != 0) return cudaErrorInvalidValue;
+  const int grid = blocks_for(2 * n / 8, 256, num_sms() * 8);
+  cudaError_t err = launch_pdl(qk_to_f16_kernel, dim3(grid), dim3(256), 0, stream, q, k, n, q16, k16);
   if (err != cudaSuccess) return err;
   count_launch();
   return cudaSuccess;

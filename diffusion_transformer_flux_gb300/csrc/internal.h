@@ -167,8 +167,7 @@ cudaError_t launch_attention_fp8(const AttnFp8Problem& p, uint32_t* status, cuda
 // power-of-two gradient scale.
 struct AttnBwdProblem {
   int batch = 0, heads = 0, seq = 0, seq_pad = 0;
-  const __nv_bfloat16 *q = nullptr, *k = nullptr, *v = nullptr, *dout = nullptr;  // [B, H, S, 128]
-  const __half *kt = nullptr, *qt = nullptr, *dout_t = nullptr;  // [B, H, 128, S_pad] fp16
+  const __half *q = nullptr, *k = nullptr, *v = nullptr, *dout = nullptr;  // [B, H, S, 128] fp16
   const float *lse = nullptr, *dsum = nullptr;  // [B, H, S_pad] (+ 64 floats of slack)
   float *dq = nullptr, *dk = nullptr, *dv = nullptr;  // [B, H, S, 128] fp32; dq zeroed by the launcher
 };
@@ -213,14 +212,16 @@ int qk_norm_rope_bwd_blocks();
 cudaError_t launch_qk_norm_rope_bwd(int act, const QkBwdArgs& a, float* dg_q, float* dg_k, cudaStream_t stream);
 // amax[0] = max(amax[0], max |x|) (amax zeroed first when zero_first).
 cudaError_t launch_grad_amax(const __nv_bfloat16* x, int64_t n, float* amax, bool zero_first, cudaStream_t stream);
-// D[b, h, seq_offset + s] = g rowsum(dO O) and dOh = g dO head-major [B, H, S_joint, 128], with g
+// D[b, h, seq_offset + s] = g rowsum(dO O) and dOh = g dO head-major [B, H, S_joint, 128] (fp16), with g
 // the gradient scale of amax(dO).
 cudaError_t launch_attn_bwd_pre(const __nv_bfloat16* o, const __nv_bfloat16* dout, int batch, int seq_s,
                                 int seq_joint, int seq_pad, int seq_offset, int heads, const float* amax,
-                                float* Dsum, __nv_bfloat16* doh, cudaStream_t stream);
-// V [BH, S, 128] bf16 from V^T [BH, 128, S_pad] fp16 (holding bf16 values: exact).
-cudaError_t launch_untranspose_vt(const __half* vt, int bh, int seq, int seq_pad, __nv_bfloat16* v,
-                                  cudaStream_t stream);
+                                float* Dsum, __half* doh, cudaStream_t stream);
+// V [BH, S, 128] fp16 from V^T [BH, 128, S_pad] fp16.
+cudaError_t launch_untranspose_vt(const __half* vt, int bh, int seq, int seq_pad, __half* v, cudaStream_t stream);
+// q16 = q, k16 = k as fp16 (n elements each, n % 8 == 0; exact within fp16's range).
+cudaError_t launch_qk_to_f16(const __nv_bfloat16* q, const __nv_bfloat16* k, int64_t n, __half* q16, __half* k16,
+                             cudaStream_t stream);
 // m = SiLU(vec) W^T + b: dW [rows, dim] and db [rows] fp32 (written; either may be null) and dvec
 // [batch, dim] fp32 (= or += with accumulate) through part (modulation_dvec_chunks(rows) * batch *
 // dim floats).  batch <= 8.
