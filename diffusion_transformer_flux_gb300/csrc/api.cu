@@ -380,6 +380,12 @@ struct Streams {
   void* y[2] = {nullptr, nullptr};
   int rpb[2] = {0, 0};  // rows per batch element
   const float* mod[2] = {nullptr, nullptr};  // [B, 6D] modulation (precomputed or in the workspace)
+  // the backward's recomputation: where the linears' outputs before their norm, GELU or gate go
+  // (null in the forward)
+  void* pre_qkv[2] = {nullptr, nullptr};
+  void* pre_o[2] = {nullptr, nullptr};
+  void* pre_1[2] = {nullptr, nullptr};
+  void* pre_2[2] = {nullptr, nullptr};
 };
 
 // The FP8 state of one block call (f == nullptr when the linears are not FP8): where each
@@ -462,6 +468,7 @@ mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss,
     e.seq_offset = ss.s[i] == 0 ? 0 : p.Si;
     e.seq_joint = p.S, e.seq_pad = p.S_pad, e.heads = p.H, e.hidden = p.D;
     e.rms_eps = d->rms_eps, e.rope_interleaved = d->rope_interleaved ? 1 : 0;
+    e.pre = ss.pre_qkv[i];
     add_problem(g, i, p.B * ss.rpb[i], at(ws, p.h[ss.s[i]]), wmat, e);
   }
   ProfScope ps_(p.single ? "single.qkv" : "double.qkv", st);
@@ -507,6 +514,7 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
     e.bias = ss.w[i]->b_o, e.resid = ss.x[i], e.gate = mod + 2 * p.D,
     e.gate_bstride = static_cast<int64_t>(p.mod_chunks) * p.D;
     e.rows_per_batch = ss.rpb[i], e.out = at(ws, p.x1[ss.s[i]]), e.out_f32 = 1;
+    e.pre = ss.pre_o[i];
     dequant(e, i, 1);
     add_problem(g, i, p.B * ss.rpb[i], at(ws, f8.f ? p.o8[ss.s[i]] : p.o[ss.s[i]]), weight(i, 1), e);
   }
@@ -546,7 +554,7 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
   f1.act = mm, f1.epi = f8.f && !f8.current ? kEpiGeluF8 : kEpiGelu, f1.N = p.F, f1.K = p.D;
   for (int i = 0; i < ss.n; ++i) {
     EpiArgs e;
-    e.bias = ss.w[i]->b_1, e.gelu_tanh = d->gelu_tanh;
+    e.bias = ss.w[i]->b_1, e.gelu_tanh = d->gelu_tanh, e.pre = ss.pre_1[i];
     e.out = f8.current ? at(ws, p.stage[ss.s[i]]) : at(ws, p.u[ss.s[i]]);
     dequant(e, i, 2);
     if (f8.f && !f8.current) {
@@ -580,6 +588,7 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
     e.bias = ss.w[i]->b_2, e.resid = at(ws, p.x1[ss.s[i]]), e.resid_f32 = 1;
     e.gate = mod + (p.parallel ? 2 : 5) * p.D;
     e.gate_bstride = static_cast<int64_t>(p.mod_chunks) * p.D, e.rows_per_batch = ss.rpb[i], e.out = ss.y[i];
+    e.pre = ss.pre_2[i];
     dequant(e, i, 3);
     add_problem(f2, i, p.B * ss.rpb[i], at(ws, p.u[ss.s[i]]), weight(i, 3), e);
   }
@@ -859,8 +868,11 @@ size_t linear_bwd_scratch(size_t e, size_t M, size_t N, size_t K) {
 
 // dx = dy W [M, K] (activation type), dW = dy^T x [N, K] fp32, db = column sums of dy [N] fp32, each
 // skipped when its pointer is null; `scratch` holds linear_bwd_scratch bytes, `ws` the status word.
+// With gelu_pre ([M, K], the input of a GELU whose output is x), dx is multiplied by GELU'(gelu_pre):
+// the gradient of that GELU's input.
 mmdit_status linear_bwd_body(int act, int M, int N, int K, const void* dy, const void* x, const void* w, void* dx,
-                             float* dw, float* db, void* scratch, void* ws, cudaStream_t st) {
+                             float* dw, float* db, void* scratch, void* ws, cudaStream_t st,
+                             const void* gelu_pre = nullptr, int gelu_tanh = 0) {
   const size_t e = elt_bytes(act);
   const int Mp = static_cast<int>(round_up(static_cast<size_t>(M), 8));
   Carver c;
@@ -878,11 +890,14 @@ mmdit_status linear_bwd_body(int act, int M, int N, int K, const void* dy, const
     g.act = act, g.epi = kEpiBias, g.M = M, g.N = K, g.K = N, g.A = dy, g.W = w, g.ep.out = dx;
     if (mn) {
       g.b_mn = 1;
+      if (gelu_pre) g.epi = kEpiDGelu, g.ep.aux = gelu_pre, g.ep.gelu_tanh = gelu_tanh;
     } else {
       MMDIT_CUDA(launch_transpose_pad(act, w, N, K, N, wt, st), "W transpose");
       g.W = wt;
     }
     MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "dx GEMM");
+    if (gelu_pre && !mn)
+      MMDIT_CUDA(launch_gelu_bwd(act, dx, gelu_pre, static_cast<int64_t>(M) * K, gelu_tanh, dx, st), "GELU backward");
   }
   if (dw) {
     // dW [N, K] = dy^T x, contracted over the M rows
@@ -956,20 +971,13 @@ bool plan_block_bwd(const mmdit_dims* d, bool single, BwdPlan* p) {
   return true;
 }
 
-mmdit_status plain_linear(int act, int M, int N, int K, const void* x, const void* w, const void* b, void* y,
-                          void* ws, cudaStream_t st) {
-  GemmProblem g;
-  g.act = act, g.epi = kEpiBias, g.M = M, g.N = N, g.K = K, g.A = x, g.W = w, g.ep.bias = b, g.ep.out = y;
-  MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "recomputed linear");
-  return MMDIT_OK;
-}
-
 // The backward of a double block (ns = 2: image and text streams) or a single block (ns = 1, one
 // stream over the joint rows).  The forward is recomputed into the workspace first (activation
 // recomputation: the call needs only the block's inputs), keeping what the backward reads: the
 // attention branch's LayerNorm output h1, the QKV linear before its norm, the attention output
 // and its log-sum-exp, the output projection a, the fp32 residual x1, the MLP's LayerNorm output,
-// its pre-GELU u_pre, GELU output and fc2 output.  Then, per stream, the MLP branch and the
+// its pre-GELU u_pre, GELU output and fc2 output (the linears' pre-norm, pre-GELU and pre-gate
+// outputs are written by the fused GEMMs' epilogues alongside their usual outputs).  Then, per stream, the MLP branch and the
 // attention projection backward; the joint attention backward; per stream the QK-RMSNorm + RoPE,
 // QKV and LayerNorm backward and the modulation backward.
 mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, const mmdit_stream_w* const* W,
@@ -996,6 +1004,9 @@ mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, cons
     if (rpb[i] == 0) continue;
     ss.s[ss.n] = i, ss.w[ss.n] = W[i], ss.x[ss.n] = X[i], ss.y[ss.n] = at(ws, bp.ytmp[i]), ss.rpb[ss.n] = rpb[i];
     ss.mod[ss.n] = at<float>(ws, p.mod[i]);
+    // the linears' outputs before their norm, GELU or gate come out of the same GEMMs
+    ss.pre_qkv[ss.n] = at(ws, bp.qkv_pre[i]), ss.pre_o[ss.n] = at(ws, bp.a[i]);
+    ss.pre_1[ss.n] = at(ws, bp.u_pre[i]), ss.pre_2[ss.n] = at(ws, bp.fo[i]);
     ++ss.n;
   }
   Fp8 no_fp8;
@@ -1003,12 +1014,9 @@ mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, cons
   for (int i = 0; i < ns; ++i) {
     const size_t R = static_cast<size_t>(B) * rpb[i];
     if (R == 0) continue;
-    ProfScope ps_("bwd.recompute.qkv_pre", st);
+    ProfScope ps_("bwd.recompute.keep_h1", st);
     MMDIT_CUDA(cudaMemcpyAsync(at(ws, bp.h1[i]), at(ws, p.h[i]), R * D * e, cudaMemcpyDeviceToDevice, st), "keep h1");
     pdl_begin_call();  // the next kernel follows a copy
-    if ((s = plain_linear(act, static_cast<int>(R), 3 * D, D, at(ws, p.h[i]), W[i]->w_qkv, W[i]->b_qkv,
-                          at(ws, bp.qkv_pre[i]), ws, st)) != MMDIT_OK)
-      return s;
   }
   {
     AttnProblem a;
@@ -1019,19 +1027,8 @@ mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, cons
     ProfScope ps_("bwd.recompute.attention", st);
     MMDIT_CUDA(launch_attention(a, status_word(ws), st), "joint attention (with log-sum-exp)");
   }
-  if ((s = run_post(d, p, ss, no_fp8, ws, st)) != MMDIT_OK) return s;  // x1, the MLP's h (in h), u
-  for (int i = 0; i < ns; ++i) {
-    const int R = B * rpb[i];
-    if (R == 0) continue;
-    ProfScope ps_("bwd.recompute.linears", st);
-    if ((s = plain_linear(act, R, D, D, at(ws, p.o[i]), W[i]->w_o, W[i]->b_o, at(ws, bp.a[i]), ws, st)) != MMDIT_OK)
-      return s;
-    if ((s = plain_linear(act, R, F, D, at(ws, p.h[i]), W[i]->w_1, W[i]->b_1, at(ws, bp.u_pre[i]), ws, st)) !=
-        MMDIT_OK)
-      return s;
-    if ((s = plain_linear(act, R, D, F, at(ws, p.u[i]), W[i]->w_2, W[i]->b_2, at(ws, bp.fo[i]), ws, st)) != MMDIT_OK)
-      return s;
-  }
+  // x1, the MLP's h (in h), u, and the linears' pre-gate / pre-GELU outputs
+  if ((s = run_post(d, p, ss, no_fp8, ws, st)) != MMDIT_OK) return s;
   // ---------------- backward: MLP branch and the attention projection, per stream
   float* part = at<float>(ws, bp.part);
   void* lin = at(ws, bp.lin);
@@ -1047,11 +1044,10 @@ mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, cons
     MMDIT_CUDA(launch_convert(act, 1, DY[i], static_cast<int64_t>(R) * D, dx1, st), "dy to fp32");
     MMDIT_CUDA(launch_gated_residual_bwd(act, dx1, at(ws, bp.fo[i]), mod + 5 * D, bstr, B, rpb[i], D,
                                          at(ws, bp.df[i]), dm + 5 * D, part, st), "gate2 backward");
+    // fc2's input gradient times GELU'(u_pre): the gradient of fc1's output
     if ((s = linear_bwd_body(act, R, D, F, at(ws, bp.df[i]), at(ws, p.u[i]), W[i]->w_2, at(ws, bp.du[i]), g->w_2,
-                             g->b_2, lin, ws, st)) != MMDIT_OK)
+                             g->b_2, lin, ws, st, at(ws, bp.u_pre[i]), d->gelu_tanh)) != MMDIT_OK)
       return s;
-    MMDIT_CUDA(launch_gelu_bwd(act, at(ws, bp.du[i]), at(ws, bp.u_pre[i]), static_cast<int64_t>(R) * F,
-                               d->gelu_tanh, at(ws, bp.du[i]), st), "GELU backward");
     if ((s = linear_bwd_body(act, R, F, D, at(ws, bp.du[i]), at(ws, p.h[i]), W[i]->w_1, at(ws, bp.dh[i]), g->w_1,
                              g->b_1, lin, ws, st)) != MMDIT_OK)
       return s;

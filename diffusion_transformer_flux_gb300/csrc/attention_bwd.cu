@@ -10,7 +10,8 @@
 // its stored [token][d] layout: where a product needs it transposed, the tensor cores read it
 // MN-major, so no transposed copy is made.  Sixteen warps:
 //   warp 0       TMA: K, V of the key tile once; per query tile Q, dO (64 x 128) and L, D into
-//                one of two stages
+//                one of three stages (a stage is held from its tile's S^T product until its dV,
+//                dK products, which follow that tile's softmax, so three keep the loads ahead)
 //   warp 1       MMA issuer, for query tile i:   S^T = K Q_i^T, dP^T = V dO_i^T  (M 128 keys, N 64)
 //                and then, for tile i - 1:        dV += P^T dO, dK += dS^T Q      (N 128 = d, K 64)
 //                                                 dQ^T = K^T dS^T                 (M 128 = d, N 64)
@@ -20,8 +21,8 @@
 //   warps 12..15 dQ^T out of TMEM (one d row per thread), added into the fp32 dQ [B, H, S, 128]
 //                with coalesced atomic additions (lanes = consecutive d)
 // TMEM columns: dV [0,128), dK [128,256), S^T [256,320), dP^T [320,384), dQ^T [384,448).
-// Shared memory: K, V 32 KB each; two stages of Q, dO (16 KB each) with L, D; two P^T + dS^T
-// buffers of 32 KB.  About 195 KB.
+// Shared memory: K, V 32 KB each; three stages of Q, dO (16 KB each) and L, D; two P^T + dS^T
+// buffers of 32 KB.  About 227 KB.
 //
 // Precision: S^T and dP^T from fp16 operands holding the forward's bf16 values (exact within
 // fp16's range); P^T, dS^T in fp16 (10-bit mantissa: a CPU emulation of these tiles and
@@ -47,18 +48,20 @@ constexpr int kKVBlock = 128 * 128;            // 128 key lines of 64 fp16 (one 
 constexpr int kKVBytes = 2 * kKVBlock;         // 128 keys x 128 d
 constexpr int kQBlock = 64 * 128;              // 64 query lines of 64 fp16
 constexpr int kQBytes = 2 * kQBlock;           // 64 queries x 128 d
+constexpr int kStages = 3;
 constexpr int kStageTx = 2 * kQBytes + 2 * kQryTile * 4;  // Q, dO, L, D
-constexpr int kStageBytes = 33792;             // kStageTx rounded up to 1024
+constexpr int kStageBytes = 2 * kQBytes;       // Q then dO (L, D live in their own small region)
 constexpr int kPBytes = 128 * 128;             // 128 key lines of 64 fp16 queries
 // offsets in the 1024-aligned dynamic shared memory
 constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kKVBytes;
 constexpr int kOffStage = kOffV + kKVBytes;
-constexpr int kStQ = 0, kStDO = kQBytes, kStL = 2 * kQBytes, kStD = 2 * kQBytes + kQryTile * 4;
-constexpr int kOffPD = kOffStage + 2 * kStageBytes;  // two buffers, each P^T then dS^T (pbuf, dsbuf)
-constexpr int kOffBar = kOffPD + 2 * 2 * kPBytes;
+constexpr int kStQ = 0, kStDO = kQBytes;
+constexpr int kOffPD = kOffStage + kStages * kStageBytes;  // two buffers, each P^T then dS^T (pbuf, dsbuf)
+constexpr int kOffLD = kOffPD + 2 * 2 * kPBytes;           // per stage: L then D, 64 floats each
+constexpr int kOffBar = kOffLD + kStages * 2 * kQryTile * 4;
 constexpr int kBwdSmem = kOffBar + 256 + 1024;
-static_assert(kStageTx <= kStageBytes && kStageBytes % 1024 == 0, "stage layout");
+static_assert(kStageBytes % 1024 == 0 && kOffPD % 1024 == 0, "stage layout");
 static_assert(kBwdSmem <= 227 * 1024, "shared memory");
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr uint32_t kTmDV = 0, kTmDK = 128, kTmS = 256, kTmDP = 320, kTmDQ = 384;
@@ -69,9 +72,9 @@ constexpr float kScaleLog2 = 0.12751743074380043f;  // log2(e) / sqrt(128)
 constexpr float kInvSqrtD = 0.08838834764831845f;   // 1 / sqrt(128)
 
 struct BwdBarriers {
-  uint64_t kv_full;      // K, V landed
-  uint64_t st_full[2];   // the stage (Q, dO, L, D) landed
-  uint64_t st_empty[2];  // the stage's last readers (dV, dK) completed
+  uint64_t kv_full;            // K, V landed
+  uint64_t st_full[kStages];   // the stage (Q, dO, L, D) landed
+  uint64_t st_empty[kStages];  // the stage's last readers (dV, dK) completed
   uint64_t sp_full;      // S^T and dP^T in TMEM
   uint64_t sp_free;      // S^T and dP^T read out of TMEM (8 warp arrivals)
   uint64_t pd_full[2];   // P^T and dS^T in the shared buffer (256 arrivals)
@@ -106,6 +109,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   BwdBarriers* sb = reinterpret_cast<BwdBarriers*>(smem + kOffBar);
   volatile int* abort_flag = &sb->abort_flag;
   auto stage = [&](int s) { return smem + kOffStage + s * kStageBytes; };
+  auto ld_l = [&](int s) { return reinterpret_cast<float*>(smem + kOffLD + s * 2 * kQryTile * 4); };
+  auto ld_d = [&](int s) { return reinterpret_cast<float*>(smem + kOffLD + s * 2 * kQryTile * 4) + kQryTile; };
   auto pbuf = [&](int j) { return smem + kOffPD + j * 2 * kPBytes; };           // P^T [key][query]
   auto dsbuf = [&](int j) { return smem + kOffPD + j * 2 * kPBytes + kPBytes; };  // dS^T [key][query]
 
@@ -120,12 +125,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&sb->kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sb->st_full[s], 1);
-      mbar_init(&sb->st_empty[s], 1);
-      mbar_init(&sb->pd_full[s], kSoftmaxThreads);
-      mbar_init(&sb->pd_empty[s], 1);
-    }
+    for (int s = 0; s < kStages; ++s) mbar_init(&sb->st_full[s], 1), mbar_init(&sb->st_empty[s], 1);
+    for (int s = 0; s < 2; ++s) mbar_init(&sb->pd_full[s], kSoftmaxThreads), mbar_init(&sb->pd_empty[s], 1);
     mbar_init(&sb->sp_full, 1);
     mbar_init(&sb->sp_free, kSoftmaxThreads / 32);
     mbar_init(&sb->dq_full, 1);
@@ -159,10 +160,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_load_3d(smem + kOffK + kKVBlock, &tm_k, &sb->kv_full, 64, k0, bh);
       tma_load_3d(smem + kOffV, &tm_v, &sb->kv_full, 0, k0, bh);
       tma_load_3d(smem + kOffV + kKVBlock, &tm_v, &sb->kv_full, 64, k0, bh);
-      int issued0 = -1, issued1 = -1;  // the last tile issued into stage 0 and stage 1
+      int issued = 0;  // tiles whose copies were issued
       for (int i = 0; i < n_q; ++i) {
-        const int s = i & 1;
-        if (!wait(&sb->st_empty[s], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u)) break;
+        const int s = i % kStages;
+        if (!wait(&sb->st_empty[s], (static_cast<uint32_t>(i / kStages) & 1u) ^ 1u)) break;
         const int q0 = q_tile(i);
         uint8_t* st = stage(s);
         mbar_arrive_expect_tx(&sb->st_full[s], kStageTx);
@@ -170,16 +171,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(st + kStQ + kQBlock, &tm_q, &sb->st_full[s], 64, q0, bh);
         tma_load_3d(st + kStDO, &tm_do, &sb->st_full[s], 0, q0, bh);
         tma_load_3d(st + kStDO + kQBlock, &tm_do, &sb->st_full[s], 64, q0, bh);
-        bulk_load(st + kStL, lse + static_cast<size_t>(bh) * seq_pad + q0, kQryTile * 4, &sb->st_full[s]);
-        bulk_load(st + kStD, dsum + static_cast<size_t>(bh) * seq_pad + q0, kQryTile * 4, &sb->st_full[s]);
-        (s ? issued1 : issued0) = i;
+        bulk_load(ld_l(s), lse + static_cast<size_t>(bh) * seq_pad + q0, kQryTile * 4, &sb->st_full[s]);
+        bulk_load(ld_d(s), dsum + static_cast<size_t>(bh) * seq_pad + q0, kQryTile * 4, &sb->st_full[s]);
+        issued = i + 1;
       }
       if (*abort_flag) {
-        // give the copies already issued a bounded chance to land before the CTA exits
+        // give the copies already issued (the last one per stage) a bounded chance to land
         int never = 0;
         mbar_wait(&sb->kv_full, 0, &never, status, 0);
-        if (issued0 >= 0) mbar_wait(&sb->st_full[0], static_cast<uint32_t>(issued0 >> 1) & 1u, &never, status, 0);
-        if (issued1 >= 0) mbar_wait(&sb->st_full[1], static_cast<uint32_t>(issued1 >> 1) & 1u, &never, status, 0);
+        for (int t = issued - kStages > 0 ? issued - kStages : 0; t < issued; ++t)
+          mbar_wait(&sb->st_full[t % kStages], static_cast<uint32_t>(t / kStages) & 1u, &never, status, 0);
       }
     }
   } else if (warp == 1) {
@@ -190,12 +191,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       auto kmaj = [](uint32_t base, int k, uint32_t blk) {
         return sdesc_kmajor_sw128(base + static_cast<uint32_t>(k >> 2) * blk + static_cast<uint32_t>(k & 3) * 32u);
       };
-      // the backward products of query tile j (its P^T, dS^T in buffer j & 1, its Q, dO in stage j & 1)
+      // the backward products of query tile j (its P^T, dS^T in buffer j & 1, its Q, dO in stage j % 3)
       auto tail = [&](int j) -> bool {
         const int b = j & 1;
         if (!wait(&sb->pd_full[b], static_cast<uint32_t>(j >> 1) & 1u)) return false;
         tc_fence_after();
-        const uint32_t st = smem_addr(stage(b));
+        const uint32_t st = smem_addr(stage(j % kStages));
         const uint32_t sP = smem_addr(pbuf(b)), sDS = smem_addr(dsbuf(b));
         // dV += P^T dO_j, dK += dS^T Q_j: A [key][query] K-major; B = dO, Q read MN-major (N = d)
 #pragma unroll
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int k = 0; k < 4; ++k)
           tc_mma<kKindF16>(tmem + kTmDK, sdesc_kmajor_sw128(sDS + k * 32), sdesc_mnmajor_sw128(st + kStQ + k * 2048, kQBlock),
                            kIdescKV, (j > 0 || k > 0) ? 1u : 0u);
-        tc_commit(&sb->st_empty[b]);  // the stage may be refilled once these reads are done
+        tc_commit(&sb->st_empty[j % kStages]);  // the stage may be refilled once these reads are done
         if (j + 1 == n_q) tc_commit(&sb->kv_done);
         // dQ^T = K^T dS^T (M 128 = d, N 64 queries, K 128 keys): K and dS^T read MN-major
         if (j > 0 && !wait(&sb->dq_empty, static_cast<uint32_t>(j - 1) & 1u)) return false;
@@ -221,8 +222,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       };
       bool ok = wait(&sb->kv_full, 0);
       for (int i = 0; ok && i < n_q; ++i) {
-        const int s = i & 1;
-        if (!wait(&sb->st_full[s], static_cast<uint32_t>(i >> 1) & 1u)) break;
+        const int s = i % kStages;
+        if (!wait(&sb->st_full[s], static_cast<uint32_t>(i / kStages) & 1u)) break;
         // S^T, dP^T of the previous tile must have been read out of TMEM
         if (i > 0 && !wait(&sb->sp_free, static_cast<uint32_t>(i - 1) & 1u)) break;
         tc_fence_after();
@@ -255,10 +256,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t sw = static_cast<uint32_t>(row & 7);
     bool live = true;
     for (int i = 0; i < n_q; ++i) {
-      const int s = i & 1;
+      const int s = i & 1;  // P^T, dS^T buffer
       const int q0 = q_tile(i);
-      // the stage (L, D) was written by the bulk copies: observe its barrier here too
-      bool w = wait(&sb->st_full[s], static_cast<uint32_t>(i >> 1) & 1u);
+      // L, D were written by the bulk copies: observe the stage's barrier here too
+      bool w = wait(&sb->st_full[i % kStages], static_cast<uint32_t>(i / kStages) & 1u);
       if (w) w = wait(&sb->sp_full, static_cast<uint32_t>(i) & 1u);
       if (!__all_sync(0xffffffffu, w)) { live = false; break; }
       tc_fence_after();
@@ -272,8 +273,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // the buffer's previous tile (i - 2) must have been consumed by its dQ^T product
       w = i < 2 || wait(&sb->pd_empty[s], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u);
       if (!__all_sync(0xffffffffu, w)) { live = false; break; }
-      const float* sL = reinterpret_cast<const float*>(stage(s) + kStL);
-      const float* sD = reinterpret_cast<const float*>(stage(s) + kStD);
+      const float* sL = ld_l(i % kStages);
+      const float* sD = ld_d(i % kStages);
       uint32_t pk[16], dk2[16];
 #pragma unroll
       for (int c = 0; c < 16; ++c) {

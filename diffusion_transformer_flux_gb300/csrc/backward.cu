@@ -259,18 +259,7 @@ __global__ void gelu_bwd_kernel(const T* __restrict__ du, const T* __restrict__ 
     load8(du + i, d);
     load8(u_pre + i, u);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float gp;
-      if (tanh_form) {
-        const float c = 0.7978845608028654f;  // sqrt(2 / pi)
-        const float t = tanhf(c * (u[e] + 0.044715f * u[e] * u[e] * u[e]));
-        gp = 0.5f * (1.f + t) + 0.5f * u[e] * (1.f - t * t) * c * (1.f + 3.f * 0.044715f * u[e] * u[e]);
-      } else {
-        const float cdf = 0.5f * (1.f + erff(u[e] * 0.7071067811865476f));
-        gp = cdf + u[e] * expf(-0.5f * u[e] * u[e]) * 0.3989422804014327f;  // 1 / sqrt(2 pi)
-      }
-      o[e] = d[e] * gp;
-    }
+    for (int e = 0; e < 8; ++e) o[e] = d[e] * gelu_grad_f(u[e], tanh_form);
     store8(out + i, o);
   }
 }

@@ -278,6 +278,17 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// GELU'(u): Phi(u) + u phi(u) (erf form), or the derivative of the tanh form.
+__device__ __forceinline__ float gelu_grad_f(float u, int tanh_form) {
+  if (tanh_form) {
+    const float c = 0.7978845608028654f;  // sqrt(2 / pi)
+    const float t = tanhf(c * (u + 0.044715f * u * u * u));
+    return 0.5f * (1.f + t) + 0.5f * u * (1.f - t * t) * c * (1.f + 3.f * 0.044715f * u * u);
+  }
+  const float cdf = 0.5f * (1.f + erff(u * 0.7071067811865476f));
+  return cdf + u * expf(-0.5f * u * u) * 0.3989422804014327f;  // 1 / sqrt(2 pi)
+}
+
 __device__ __forceinline__ float fast_rcp(float x) {
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -23,7 +23,7 @@ constexpr int kBM = 128;
 // image embedding), one for the others.
 template <int EPI>
 struct EpiGroups {
-  static constexpr int value = (EPI == kEpiGelu || EPI == kEpiGeluF8 || EPI == kEpiBias) ? 2 : 1;
+  static constexpr int value = (EPI == kEpiGelu || EPI == kEpiGeluF8 || EPI == kEpiBias || EPI == kEpiDGelu) ? 2 : 1;
 };
 template <int EPI>
 constexpr int gemm_threads() {
@@ -150,6 +150,15 @@ __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, 
           for (int i = 0; i < 32; ++i) v[c * 32 + i] += bb[i];
         }
       }
+      if (ep.pre) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float t[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) t[i] = v[c * 32 + i];
+          store32(reinterpret_cast<T*>(ep.pre) + static_cast<size_t>(m) * N + nh + c * 32, t);
+        }
+      }
       const size_t bh = static_cast<size_t>(b) * ep.heads + head;
       if (which < 2) {
         float ss = 0.f;
@@ -231,6 +240,20 @@ __device__ __forceinline__ void gemm_epilogue(int group, uint32_t taddr, int m, 
         load32(reinterpret_cast<const T*>(ep.bias) + n, bb);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] += bb[i];
+      }
+      if constexpr (EPI == kEpiGelu || EPI == kEpiGateResid) {
+        if (ep.pre) store32(reinterpret_cast<T*>(ep.pre) + static_cast<size_t>(m) * N + n, v);
+      }
+      if constexpr (EPI == kEpiDGelu) {
+        float u[32];
+        load32(reinterpret_cast<const T*>(ep.aux) + static_cast<size_t>(m) * N + n, u);
+        if (ep.gelu_tanh) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(u[i], 1);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= gelu_grad_f(u[i], 0);
+        }
       }
       if constexpr (EPI == kEpiGelu || EPI == kEpiGeluF8) {
         // the variant is chosen once per chunk so the 32 evaluations interleave
@@ -530,7 +553,12 @@ cudaError_t dispatch_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t s
   if (p.a_mn || p.b_mn) {
     // transposed operands: the pair kernel's plain-bias products only
     if constexpr (KIND == kKindF16) {
-      if (p.epi != kEpiBias || p.N % 256 != 0 || p.M1 > 0 || p.splits != 1) return cudaErrorInvalidValue;
+      if ((p.epi != kEpiBias && p.epi != kEpiDGelu) || p.N % 256 != 0 || p.M1 > 0 || p.splits != 1)
+        return cudaErrorInvalidValue;
+      if (p.epi == kEpiDGelu) {
+        if (p.a_mn || !p.ep.aux) return cudaErrorInvalidValue;
+        return run_gemm_pair<KIND, 256, kEpiDGelu, 2>(p, status, stream);
+      }
       if (p.a_mn && p.b_mn) return run_gemm_pair<KIND, 256, kEpiBias, 3>(p, status, stream);
       if (p.b_mn) return run_gemm_pair<KIND, 256, kEpiBias, 2>(p, status, stream);
       return run_gemm_pair<KIND, 256, kEpiBias, 1>(p, status, stream);

@@ -18,7 +18,8 @@ enum EpiKind : int {
   kEpiQkv = 3,        // bias, per-head RMSNorm of q and k, RoPE, scatter to Q, K, Vt
   kEpiUnpatchify = 4, // pred[b, n, s] (fp32) = acc + bias[n], m = b * rows_per_batch + s
   kEpiPartial = 5,    // split-K: partial[split][m][n] (fp32) = acc over the split's K range
-  kEpiGeluF8 = 6      // out[m, n] (E4M3) = GELU(acc + bias[n]) * out_scale, amax recorded
+  kEpiGeluF8 = 6,     // out[m, n] (E4M3) = GELU(acc + bias[n]) * out_scale, amax recorded
+  kEpiDGelu = 7       // out[m, n] = (acc + bias[n]) * GELU'(aux[m, n]) (a GELU's input gradient)
 };
 
 struct EpiArgs {
@@ -31,6 +32,10 @@ struct EpiArgs {
   int64_t gate_bstride = 0;
   int rows_per_batch = 1;      // m -> (b = m / rows_per_batch, s = m % rows_per_batch)
   int gelu_tanh = 0;
+  // kEpiQkv, kEpiGelu, kEpiGateResid: when set, [M, N] (activation type) also receives the
+  // product plus bias before the epilogue's norm, activation or gate (what a backward reads)
+  void* pre = nullptr;
+  const void* aux = nullptr;   // kEpiDGelu: [M, N] activation type, the GELU's input
   // QKV scatter
   const void* g_q = nullptr;   // [128] activation type
   const void* g_k = nullptr;
