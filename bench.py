@@ -12,9 +12,8 @@ all through the C ABI of libmmdit.so, with inputs resident in HBM when the timed
 starts (``value``) or copied from pinned host memory inside it (``e2e``).  Other workloads:
 the same step at batch 2 with 4096 + 512 tokens (the metric's second point), the double block
 at batch 4 with 1024 + 512 tokens, the blocks at 16384 + 512 tokens with E4M3 linears, and the
-whole Flux 12B forward.  The blocks' AdaLN
-modulations (mmdit_modulation_fwd) run on a second stream, overlapped with the embeddings and
-the double block, and are joined before each block needs them.  The metric is the
+whole Flux 12B forward.  Every AdaLN modulation of the step (the blocks' and the output head's)
+is computed first, in one batched GEMV launch (mmdit_modulation_batched_fwd).  The metric is the
 dense-contraction throughput of the two blocks (2 * B * S * D * (3D + D + 2F) + 4 * B * S^2 *
 d * H floating-point operations per block) divided by the time of the whole step, reported
 in TFLOP/s and as a fraction of the measured bf16 tensor peak.
@@ -137,39 +136,23 @@ class HostWorkload:
         self.final = synth.final_layer_weights(rng_w, D, wl.channels, "bf16")
 
 
-class SideModulation:
-    """The blocks' AdaLN modulations computed on a second stream in one launch, overlapped with the
-    work the main stream does first (the RoPE tables and the embeddings): they depend only on vec
-    and the weights and are HBM-bound.  The blocks then read them through
-    the weight sets' `mod` entries.  Fork and join are CUDA events, so the step still captures
-    as one graph."""
+class BatchedModulation:
+    """Every AdaLN modulation of the step (the blocks' six-chunk modulations, the output head's shift
+    and scale) in one launch at the start of the step, on the step's stream: they depend only on vec
+    and the weights, and one launch streams the weights at close to the HBM rate.  (Run on a second
+    stream beside the RoPE tables and the embeddings, the GEMV's blocks hold every SM while those
+    short launches wait, and the pair took longer than the two in sequence.)  The blocks then read
+    them through the weight sets' `mod` entries."""
 
     def __init__(self, torch, L, vec, weight_sets, device):
         self.torch, self.L, self.vec = torch, L, vec
-        self.side = torch.cuda.Stream(device=device)
-        self.ev_start = torch.cuda.Event()
-        # [(name, w_mod, b_mod), ...] in the order the steps need them (the blocks' six-chunk
-        # modulations, the output head's shift and scale)
+        # [(name, w_mod, b_mod), ...] in the order the steps need them
         self.sets = weight_sets
         B = vec.shape[0]
         self.mods = {n: torch.empty(B, w.shape[0], device=device) for n, w, _ in weight_sets}
-        self.ready = {n: torch.cuda.Event() for n, _, _ in weight_sets}
 
-    def fork(self):
-        main = self.torch.cuda.current_stream()
-        self.ev_start.record(main)
-        self.side.wait_event(self.ev_start)
-        with self.torch.cuda.stream(self.side):
-            # every block's modulation in one launch (mmdit_modulation_batched_fwd): the weights
-            # stream at the HBM rate instead of one short launch per block
-            self.L.mmdit_modulation_batched_fwd(self.vec, [(w, b, self.mods[n]) for n, w, b in self.sets])
-            for n, _, _ in self.sets:
-                self.ready[n].record(self.side)
-
-    def join(self, *names):
-        main = self.torch.cuda.current_stream()
-        for n in names:
-            main.wait_event(self.ready[n])
+    def compute(self):
+        self.L.mmdit_modulation_batched_fwd(self.vec, [(w, b, self.mods[n]) for n, w, b in self.sets])
 
     def weights(self, name, w):
         return dict(w, mod=self.mods[name])
@@ -247,7 +230,7 @@ class DeviceStep:
         if hw.has_single:
             sets.append(("single", self.w_single["w_mod"], self.w_single["b_mod"]))
         sets.append(("head", self.final["w_ada"], self.final["b_ada"]))
-        self.side = SideModulation(torch, L, self.vec, sets, device)
+        self.mods = BatchedModulation(torch, L, self.vec, sets, device)
         n_blocks = 2 if hw.has_single else 1
         self.flops_blocks = n_blocks * block_flops(B, S, D, F, H)
         self.flops_dense = (self.flops_blocks + 2 * B * S_i * wl.channels * D
@@ -262,22 +245,20 @@ class DeviceStep:
 
     def step(self):
         """One pass of the hot path; every computation runs in libmmdit.so kernels."""
-        L, wl, side = self.L, self.wl, self.side
+        L, wl, side = self.L, self.wl, self.mods
         S_i = self.S_i
-        side.fork()  # the block modulations, on the side stream
+        side.compute()  # every modulation of the step, one launch
         L.rope3d_freqs(self.ids, AXES, THETA, self.cos, self.sin)
         # z_t = (1 - t) z0 + t z1 formed while patchifying, then projected
         L.mmdit_img_in_noise_fwd(self.z0, self.z1, self.t, self.img_in["w"], self.img_in["b"], self.x_img,
                                  ws=self.ws_img)
         if self.txt_in is not None:
             L.mmdit_linear_fwd(self.txt, self.txt_in["w"], self.txt_in["b"], self.x_txt, ws=self.ws_lin)
-        side.join("dimg", "dtxt")
         L.mmdit_double_block_fwd(self.dims, side.weights("dimg", self.w_dimg), side.weights("dtxt", self.w_dtxt),
                                  self.vec, self.cos, self.sin, self.x_img, self.x_txt,
                                  self.y_img, self.y_txt, ws=self.ws_block)
         head_in = self.y_img
         if self.w_single is not None:
-            side.join("single")
             if self.joint:
                 L.mmdit_single_block_fwd(self.dims, side.weights("single", self.w_single), self.vec, self.cos,
                                          self.sin, self.Y, self.Z, ws=self.ws_block)
@@ -291,7 +272,6 @@ class DeviceStep:
                 head_in = self.z_img
         # output head (its shift and scale from the batched modulation launch) with the
         # flow-matching loss fused onto its last kernel
-        side.join("head")
         L.mmdit_final_layer_loss_fwd(self.dims_final, wl.lat_h, wl.lat_w, head_in, self.vec,
                                      self.final["w_ada"], self.final["b_ada"], self.final["w_out"],
                                      self.final["b_out"], self.z0, self.z1, self.loss, pred=self.pred,
@@ -358,7 +338,7 @@ class Fp8BlockStep(DeviceStep):
                        L.mmdit_single_block_workspace_size(self.dims))
         self.ws_block = L.workspace(ws_block, device)
         self.S, self.S_i = S, S_i
-        self.side = SideModulation(torch, L, self.vec,
+        self.mods = BatchedModulation(torch, L, self.vec,
                                    [(n, w["w_mod"], w["b_mod"]) for n, w in (("dimg", self.w_dimg),
                                                                             ("dtxt", self.w_dtxt),
                                                                             ("single", self.w_single))], device)
@@ -376,14 +356,12 @@ class Fp8BlockStep(DeviceStep):
         return self.Z[:, :self.S_i]
 
     def step(self):
-        L, S_i, side = self.L, self.S_i, self.side
-        side.fork()
+        L, S_i, side = self.L, self.S_i, self.mods
+        side.compute()
         L.rope3d_freqs(self.ids, AXES, THETA, self.cos, self.sin)
-        side.join("dimg", "dtxt")
         L.mmdit_double_block_fwd(self.dims, side.weights("dimg", self.w_dimg), side.weights("dtxt", self.w_dtxt),
                                  self.vec, self.cos, self.sin, self.X[:, :S_i], self.X[:, S_i:],
                                  self.Y[:, :S_i], self.Y[:, S_i:], ws=self.ws_block, fp8=self.fp8_d)
-        side.join("single")
         L.mmdit_single_block_fwd(self.dims, side.weights("single", self.w_single), self.vec, self.cos,
                                  self.sin, self.Y, self.Z, ws=self.ws_block, fp8=self.fp8_s)
 
@@ -569,7 +547,9 @@ def kernel_work(label: str, wl):
     if label == "modulation.batched":  # every block stream's 6D x D modulation weights
         n_mod = (2 * wl.n_double + wl.n_single if "model" in wl.blocks
                  else 2 + (1 if "single" in wl.blocks else 0))
-        return "hbm", n_mod * (6.0 * D * D * 2 + B * 6 * D * 4) + B * D * 2, "B"
+        # the bf16 steps that end in the output head add its 2D x D shift-and-scale weights
+        head = 2.0 * D * D * 2 + B * 2 * D * 4 if ("model" not in wl.blocks and wl.dtype != "fp8") else 0.0
+        return "hbm", n_mod * (6.0 * D * D * 2 + B * 6 * D * 4) + head + B * D * 2, "B"
     if label == "modulation":  # one block stream's 6D x D weights (mmdit_modulation_fwd)
         return "hbm", 6.0 * D * D * 2 + B * 6 * D * 4 + B * D * 2, "B"
     if label == "rope3d_freqs":
@@ -816,16 +796,25 @@ def measure_block_bwd(st, L, torch, peak, reps=3):
     gemm = 2 * B * S * D * (3 * D + D + 2 * F)
     attn = 4 * B * S * S * 128 * H
     flops = 2 * gemm + 2.5 * attn
+    # one more call with the library's per-step events: the attention backward's own time
+    L.mmdit_profile_enable(True)
+    L.mmdit_double_block_bwd(*args, ws=ws)
+    steps = L.mmdit_profile_collect()
+    L.mmdit_profile_enable(False)
+    attn_us = 1e3 * sum(ms for n, ms in steps if n == "bwd.attention")
     del grads, ws
     return {"op": "double block backward (all gradients, forward recomputed inside)", "tokens": S,
             "avg_us": round(us, 2), "flops_counted": flops, "achieved_tflops": round(flops / us / 1e6, 1),
-            "frac": round(flops / us / 1e6 / peak, 4)}
+            "frac": round(flops / us / 1e6 / peak, 4),
+            "attention_backward": {"avg_us": round(attn_us, 2), "flops": 2.5 * attn,
+                                   "achieved_tflops": round(2.5 * attn / attn_us / 1e6, 1) if attn_us else None,
+                                   "frac": round(2.5 * attn / attn_us / 1e6 / peak, 4) if attn_us else None}}
 
 
 def measure_linear_bwd(L, torch, device, peak, M=4608, N=12288, K=3072, reps=5):
     """The backward of the block's fc1-shaped linear (mmdit_linear_bwd: dx and dW through the
-    tensor-core GEMM on transposed operands, db): 4 M N K FLOPs per call, CUDA events around
-    `reps` calls after one warm-up."""
+    tensor-core GEMM reading W, dy and x MN-major as stored, db): 4 M N K FLOPs per call, CUDA
+    events around `reps` calls after one warm-up."""
     dy = torch.randn(M, N, device=device).to(torch.bfloat16)
     x = torch.randn(M, K, device=device).to(torch.bfloat16)
     w = (torch.randn(N, K, device=device) * 0.02).to(torch.bfloat16)
@@ -1114,9 +1103,8 @@ def main():
                                 + "output head with the flow-matching loss fused on"
                                 + ("" if wl.batch == 1 else "; streams joined and split by strided "
                                    "copy-engine copies (mmdit_copy_rows)")),
-                       "streams": "one stream (the model's modulations run up front in one launch)"
-                                  if model else "the block modulations (mmdit_modulation_batched_fwd, one "
-                                  "launch) on a second stream, joined before each block",
+                       "streams": "one stream; every modulation of the step runs first, in one "
+                                  "launch (mmdit_modulation_batched_fwd)",
                        "flops_counted_per_step": st.flops_blocks,
                        "dense_flops_per_step_incl_embeds_and_head": st.flops_dense},
             "pct_of_bf16_peak": round(100 * value / world / bf16_peak, 2),

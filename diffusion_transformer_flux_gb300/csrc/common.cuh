@@ -392,7 +392,25 @@ __device__ __forceinline__ void load32(const float* p, float (&v)[32]) {
     v[4 * i] = u.x, v[4 * i + 1] = u.y, v[4 * i + 2] = u.z, v[4 * i + 3] = u.w;
   }
 }
+// 32 values of one row: 256-bit stores (whole 32-byte sectors, half the requests of 128-bit ones;
+// an epilogue thread writes its own row, so a warp's stores touch 32 rows at once) when the
+// address allows, 128-bit ones otherwise.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
 __device__ __forceinline__ void store32(__nv_bfloat16* p, const float (&v)[32]) {
+  if ((reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[16 * h + 2 * i], v[16 * h + 2 * i + 1]);
+      st_global_v8(p + 16 * h, w);
+    }
+    return;
+  }
   uint4* q = reinterpret_cast<uint4*>(p);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -405,6 +423,16 @@ __device__ __forceinline__ void store32(__nv_bfloat16* p, const float (&v)[32]) 
   }
 }
 __device__ __forceinline__ void store32(float* p, const float (&v)[32]) {
+  if ((reinterpret_cast<uintptr_t>(p) & 31u) == 0) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(v[8 * h + i]);
+      st_global_v8(p + 8 * h, w);
+    }
+    return;
+  }
   float4* q = reinterpret_cast<float4*>(p);
 #pragma unroll
   for (int i = 0; i < 8; ++i) q[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);

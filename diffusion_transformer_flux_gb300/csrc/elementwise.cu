@@ -23,13 +23,19 @@ struct RopeTable {
 
 __global__ void rope3d_kernel(const float* __restrict__ ids, int64_t n_tok, RopeTable tab,
                               float* __restrict__ cos_out, float* __restrict__ sin_out) {
+  // the per-pair table in shared memory: lanes read different pairs, which kernel-parameter
+  // reads would serialise
+  __shared__ float inv_freq[128];
+  __shared__ int axis[128];
+  for (int j = threadIdx.x; j < tab.pairs; j += blockDim.x) inv_freq[j] = tab.inv_freq[j], axis[j] = tab.axis[j];
+  __syncthreads();
   pdl_wait();  // the previous kernel's results are visible from here on
   const int64_t total = n_tok * tab.pairs;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t tok = i / tab.pairs;
     const int j = static_cast<int>(i - tok * tab.pairs);
-    const double ang = static_cast<double>(ids[tok * 3 + tab.axis[j]]) * tab.inv_freq[j];
+    const double ang = static_cast<double>(ids[tok * 3 + axis[j]]) * inv_freq[j];
     float s, c;
     sincosf(static_cast<float>(ang), &s, &c);
     cos_out[i] = c;
@@ -67,21 +73,6 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const void* __r
                                                                  int vec_f32) {
   pdl_wait();  // the previous kernel's results are visible from here on
   constexpr int batch = NB;  // batch rows handled by this launch (compile time: no idle lanes)
-  // [batch, dim] SiLU(vec) (or vec itself when silu == 0): fp32, or in bf16 mode the bf16
-  // operand it is there (stored as bf16, so each 16-byte weight load pairs with one 16-byte
-  // shared-memory load)
-  extern __shared__ float svec[];
-  __nv_bfloat16* svec_bf = reinterpret_cast<__nv_bfloat16*>(svec);
-  for (int i = threadIdx.x; i < batch * dim; i += blockDim.x) {
-    // vec is of the weights' type, or fp32 (an fp32 hidden layer feeding a bf16 linear)
-    const float v = vec_f32 ? static_cast<const float*>(vec)[i] : to_f32(static_cast<const T*>(vec)[i]);
-    const float sv = silu ? v / (1.f + expf(-v)) : v;
-    if constexpr (sizeof(T) == 2)
-      svec_bf[i] = __float2bfloat16_rn(sv);
-    else
-      svec[i] = sv;
-  }
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int warps = blockDim.x >> 5;
   const int total = jobs.start[jobs.n];
@@ -108,6 +99,29 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const void* __r
       if (k < dim) raw[c].load(wr + k);
     }
   };
+  // the first row's weights are requested before the block prepares SiLU(vec)
+  Raw8<T> ra[NC], rb[NC];
+  int g = blockIdx.x * warps + warp;
+  int ja = 0, jb = 0;
+  if (g < total) {
+    ja = job_of(g);
+    load_row(g, ja, ra);
+  }
+  // [batch, dim] SiLU(vec) (or vec itself when silu == 0): fp32, or in bf16 mode the bf16
+  // operand it is there (stored as bf16, so each 16-byte weight load pairs with one 16-byte
+  // shared-memory load)
+  extern __shared__ float svec[];
+  __nv_bfloat16* svec_bf = reinterpret_cast<__nv_bfloat16*>(svec);
+  for (int i = threadIdx.x; i < batch * dim; i += blockDim.x) {
+    // vec is of the weights' type, or fp32 (an fp32 hidden layer feeding a bf16 linear)
+    const float v = vec_f32 ? static_cast<const float*>(vec)[i] : to_f32(static_cast<const T*>(vec)[i]);
+    const float sv = silu ? v / (1.f + expf(-v)) : v;
+    if constexpr (sizeof(T) == 2)
+      svec_bf[i] = __float2bfloat16_rn(sv);
+    else
+      svec[i] = sv;
+  }
+  __syncthreads();
   auto reduce_row = [&](int g, int ji, const Raw8<T> (&raw)[NC]) {
     const ModJob& job = jobs.j[ji];
     const int r = g - jobs.start[ji];
@@ -157,13 +171,6 @@ __global__ void __launch_bounds__(kModThreads) modulation_kernel(const void* __r
       }
     }
   };
-  Raw8<T> ra[NC], rb[NC];
-  int g = blockIdx.x * warps + warp;
-  int ja = 0, jb = 0;
-  if (g < total) {
-    ja = job_of(g);
-    load_row(g, ja, ra);
-  }
   while (g < total) {
     const int g1 = g + stride;
     if (g1 < total) {
