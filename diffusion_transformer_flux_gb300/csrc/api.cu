@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <array>
 #include <initializer_list>
 #include <vector>
 
@@ -919,6 +920,53 @@ mmdit_status linear_bwd_body(int act, int M, int N, int K, const void* dy, const
   return MMDIT_OK;
 }
 
+// The linear backward of a block's two streams (same N and K; M[0] and M[1] rows): in bf16 with
+// MN-major operands, both streams' dx run in one GEMM launch and both dW in another (the text
+// stream's short contraction interleaved with the image stream's tiles, so its epilogue-heavy
+// tiles do not form a wave of their own); otherwise, or when the streams ask for different
+// outputs, one linear_bwd_body per stream.
+mmdit_status linear_bwd_streams(int act, int ns, const int* M, int N, int K, const void* const* dy,
+                                const void* const* x, const void* const* w, void* const* dx, float* const* dw,
+                                float* const* db, void* scratch, void* ws, cudaStream_t st,
+                                const void* const* gelu_pre = nullptr, int gelu_tanh = 0) {
+  const bool joint = ns == 2 && M[0] > 0 && M[1] > 0 && act == 1 && K % 256 == 0 && N % 8 == 0 &&
+                     (dx[0] == nullptr) == (dx[1] == nullptr) && (dw[0] == nullptr) == (dw[1] == nullptr) &&
+                     (gelu_pre == nullptr || (gelu_pre[0] == nullptr) == (gelu_pre[1] == nullptr));
+  if (!joint) {
+    for (int i = 0; i < ns; ++i) {
+      if (M[i] == 0) continue;
+      mmdit_status s = linear_bwd_body(act, M[i], N, K, dy[i], x[i], w[i], dx[i], dw[i], db[i], scratch, ws, st,
+                                       gelu_pre ? gelu_pre[i] : nullptr, gelu_tanh);
+      if (s != MMDIT_OK) return s;
+    }
+    return MMDIT_OK;
+  }
+  const bool dgelu = gelu_pre && gelu_pre[0];
+  if (dx[0]) {
+    GemmProblem g;
+    g.act = act, g.epi = dgelu ? kEpiDGelu : kEpiBias, g.N = K, g.K = N, g.b_mn = 1;
+    g.M = M[0], g.A = dy[0], g.W = w[0], g.ep.out = dx[0];
+    g.M1 = M[1], g.A1 = dy[1], g.W1 = w[1], g.ep1.out = dx[1];
+    if (dgelu) {
+      g.ep.aux = gelu_pre[0], g.ep1.aux = gelu_pre[1];
+      g.ep.gelu_tanh = g.ep1.gelu_tanh = gelu_tanh;
+    }
+    MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "dx GEMM (both streams)");
+  }
+  if (dw[0]) {
+    GemmProblem g;
+    g.act = act, g.epi = kEpiBias, g.N = K, g.a_mn = 1, g.b_mn = 1, g.interleave = 1;
+    g.M = N, g.K = M[0], g.A = dy[0], g.W = x[0], g.ep.out = dw[0], g.ep.out_f32 = 1;
+    g.M1 = N, g.K1 = M[1], g.A1 = dy[1], g.W1 = x[1], g.ep1.out = dw[1], g.ep1.out_f32 = 1;
+    MMDIT_CUDA(launch_gemm(g, status_word(ws), st), "dW GEMM (both streams)");
+  }
+  // (no transposed copies on this path: the column-sum partials take the scratch's start)
+  float* part = at<float>(scratch, 0);
+  for (int i = 0; i < 2; ++i)
+    if (db[i]) MMDIT_CUDA(launch_colsum(act, dy[i], M[i], N, part, kColsumChunks, db[i], st), "db column sums");
+  return MMDIT_OK;
+}
+
 // Workspace of a block backward: the forward's own slots first (the backward recomputes the
 // forward into them), then what the backward reads of the forward and its own gradients.
 struct BwdPlan {
@@ -1029,35 +1077,76 @@ mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, cons
   }
   // x1, the MLP's h (in h), u, and the linears' pre-gate / pre-GELU outputs
   if ((s = run_post(d, p, ss, no_fp8, ws, st)) != MMDIT_OK) return s;
-  // ---------------- backward: MLP branch and the attention projection, per stream
+  // ---------------- backward: MLP branch and the attention projection, both streams step by step
+  // (each linear's backward runs for both streams in shared launches)
   float* part = at<float>(ws, bp.part);
   void* lin = at(ws, bp.lin);
   const int64_t bstr = 6 * static_cast<int64_t>(D);
-  for (int i = 0; i < ns; ++i) {
-    const int R = B * rpb[i];
-    const mmdit_stream_grads* g = G[i] ? G[i] : &none;
-    float* dm = at<float>(ws, bp.dm[i]);
-    if (R == 0) continue;  // (the entry points reject streams without rows)
-    const float* mod = at<float>(ws, p.mod[i]);
-    float* dx1 = at<float>(ws, bp.dx1[i]);
+  int R[2] = {0, 0};
+  const mmdit_stream_grads* Gs[2] = {&none, &none};
+  for (int i = 0; i < ns; ++i) R[i] = B * rpb[i], Gs[i] = G[i] ? G[i] : &none;
+  auto ptrs = [&](auto f) {  // a per-stream pointer pair
+    using T = decltype(f(0));
+    std::array<T, 2> a{};
+    for (int i = 0; i < ns; ++i) a[i] = f(i);
+    return a;
+  };
+  {
     ProfScope ps_("bwd.mlp_and_out_proj", st);
-    MMDIT_CUDA(launch_convert(act, 1, DY[i], static_cast<int64_t>(R) * D, dx1, st), "dy to fp32");
-    MMDIT_CUDA(launch_gated_residual_bwd(act, dx1, at(ws, bp.fo[i]), mod + 5 * D, bstr, B, rpb[i], D,
-                                         at(ws, bp.df[i]), dm + 5 * D, part, st), "gate2 backward");
+    for (int i = 0; i < ns; ++i) {
+      if (R[i] == 0) continue;  // (the entry points reject streams without rows)
+      const float* mod = at<float>(ws, p.mod[i]);
+      float* dx1 = at<float>(ws, bp.dx1[i]);
+      MMDIT_CUDA(launch_convert(act, 1, DY[i], static_cast<int64_t>(R[i]) * D, dx1, st), "dy to fp32");
+      MMDIT_CUDA(launch_gated_residual_bwd(act, dx1, at(ws, bp.fo[i]), mod + 5 * D, bstr, B, rpb[i], D,
+                                           at(ws, bp.df[i]), at<float>(ws, bp.dm[i]) + 5 * D, part, st),
+                 "gate2 backward");
+    }
     // fc2's input gradient times GELU'(u_pre): the gradient of fc1's output
-    if ((s = linear_bwd_body(act, R, D, F, at(ws, bp.df[i]), at(ws, p.u[i]), W[i]->w_2, at(ws, bp.du[i]), g->w_2,
-                             g->b_2, lin, ws, st, at(ws, bp.u_pre[i]), d->gelu_tanh)) != MMDIT_OK)
-      return s;
-    if ((s = linear_bwd_body(act, R, F, D, at(ws, bp.du[i]), at(ws, p.h[i]), W[i]->w_1, at(ws, bp.dh[i]), g->w_1,
-                             g->b_1, lin, ws, st)) != MMDIT_OK)
-      return s;
-    MMDIT_CUDA(launch_ln_modulate_bwd(act, 1, at(ws, p.x1[i]), at(ws, bp.dh[i]), mod + 4 * D, bstr, B, rpb[i], D,
-                                      d->ln_eps, dx1, dm + 4 * D, dm + 3 * D, 0, part, st), "LN2 backward");
-    MMDIT_CUDA(launch_gated_residual_bwd(act, dx1, at(ws, bp.a[i]), mod + 2 * D, bstr, B, rpb[i], D,
-                                         at(ws, bp.df[i]), dm + 2 * D, part, st), "gate1 backward");
-    if ((s = linear_bwd_body(act, R, D, D, at(ws, bp.df[i]), at(ws, p.o[i]), W[i]->w_o, at(ws, bp.dO[i]), g->w_o,
-                             g->b_o, lin, ws, st)) != MMDIT_OK)
-      return s;
+    {
+      const auto dy = ptrs([&](int i) -> const void* { return at(ws, bp.df[i]); });
+      const auto xx = ptrs([&](int i) -> const void* { return at(ws, p.u[i]); });
+      const auto ww = ptrs([&](int i) -> const void* { return W[i]->w_2; });
+      const auto dx = ptrs([&](int i) -> void* { return at(ws, bp.du[i]); });
+      const auto dw = ptrs([&](int i) -> float* { return Gs[i]->w_2; });
+      const auto db = ptrs([&](int i) -> float* { return Gs[i]->b_2; });
+      const auto gp = ptrs([&](int i) -> const void* { return at(ws, bp.u_pre[i]); });
+      if ((s = linear_bwd_streams(act, ns, R, D, F, dy.data(), xx.data(), ww.data(), dx.data(), dw.data(), db.data(),
+                                  lin, ws, st, gp.data(), d->gelu_tanh)) != MMDIT_OK)
+        return s;
+    }
+    {
+      const auto dy = ptrs([&](int i) -> const void* { return at(ws, bp.du[i]); });
+      const auto xx = ptrs([&](int i) -> const void* { return at(ws, p.h[i]); });
+      const auto ww = ptrs([&](int i) -> const void* { return W[i]->w_1; });
+      const auto dx = ptrs([&](int i) -> void* { return at(ws, bp.dh[i]); });
+      const auto dw = ptrs([&](int i) -> float* { return Gs[i]->w_1; });
+      const auto db = ptrs([&](int i) -> float* { return Gs[i]->b_1; });
+      if ((s = linear_bwd_streams(act, ns, R, F, D, dy.data(), xx.data(), ww.data(), dx.data(), dw.data(), db.data(),
+                                  lin, ws, st)) != MMDIT_OK)
+        return s;
+    }
+    for (int i = 0; i < ns; ++i) {
+      if (R[i] == 0) continue;
+      const float* mod = at<float>(ws, p.mod[i]);
+      float* dx1 = at<float>(ws, bp.dx1[i]);
+      float* dm = at<float>(ws, bp.dm[i]);
+      MMDIT_CUDA(launch_ln_modulate_bwd(act, 1, at(ws, p.x1[i]), at(ws, bp.dh[i]), mod + 4 * D, bstr, B, rpb[i], D,
+                                        d->ln_eps, dx1, dm + 4 * D, dm + 3 * D, 0, part, st), "LN2 backward");
+      MMDIT_CUDA(launch_gated_residual_bwd(act, dx1, at(ws, bp.a[i]), mod + 2 * D, bstr, B, rpb[i], D,
+                                           at(ws, bp.df[i]), dm + 2 * D, part, st), "gate1 backward");
+    }
+    {
+      const auto dy = ptrs([&](int i) -> const void* { return at(ws, bp.df[i]); });
+      const auto xx = ptrs([&](int i) -> const void* { return at(ws, p.o[i]); });
+      const auto ww = ptrs([&](int i) -> const void* { return W[i]->w_o; });
+      const auto dx = ptrs([&](int i) -> void* { return at(ws, bp.dO[i]); });
+      const auto dw = ptrs([&](int i) -> float* { return Gs[i]->w_o; });
+      const auto db = ptrs([&](int i) -> float* { return Gs[i]->b_o; });
+      if ((s = linear_bwd_streams(act, ns, R, D, D, dy.data(), xx.data(), ww.data(), dx.data(), dw.data(), db.data(),
+                                  lin, ws, st)) != MMDIT_OK)
+        return s;
+    }
   }
   // ---------------- the joint attention backward
   const int bh = B * H;
@@ -1090,16 +1179,12 @@ mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, cons
     ProfScope ps_("bwd.attention", st);
     MMDIT_CUDA(launch_attention_bwd(a, status_word(ws), st), "attention backward");
   }
-  // ---------------- QK-RMSNorm + RoPE, QKV and LayerNorm backward, the modulation, per stream
-  bool dvec_written = false;
-  for (int i = 0; i < ns; ++i) {
-    const int R = B * rpb[i];
-    const mmdit_stream_grads* g = G[i] ? G[i] : &none;
-    float* dm = at<float>(ws, bp.dm[i]);
-    const float* mod = at<float>(ws, p.mod[i]);
-    float* dx1 = at<float>(ws, bp.dx1[i]);
+  // ---------------- QK-RMSNorm + RoPE, QKV (both streams' linear backward in shared launches) and
+  // LayerNorm backward, the modulation
+  {
     ProfScope ps_("bwd.qkv_and_ln1", st);
-    if (R > 0) {
+    for (int i = 0; i < ns; ++i) {
+      if (R[i] == 0) continue;
       QkBwdArgs q;
       q.qkv_pre = at(ws, bp.qkv_pre[i]), q.g_q = W[i]->g_q, q.g_k = W[i]->g_k;
       q.cos = rope_cos, q.sin = rope_sin;
@@ -1107,19 +1192,36 @@ mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, cons
       q.part = part, q.amax = amax;
       q.batch = B, q.seq_s = rpb[i], q.seq_joint = S, q.seq_offset = off[i], q.heads = H, q.hidden = D;
       q.interleaved = d->rope_interleaved ? 1 : 0, q.eps = d->rms_eps;
-      MMDIT_CUDA(launch_qk_norm_rope_bwd(act, q, g->g_q, g->g_k, st), "QK-RMSNorm + RoPE backward");
-      if ((s = linear_bwd_body(act, R, 3 * D, D, at(ws, bp.dqkv[i]), at(ws, bp.h1[i]), W[i]->w_qkv,
-                               at(ws, bp.dh[i]), g->w_qkv, g->b_qkv, lin, ws, st)) != MMDIT_OK)
-        return s;
-      MMDIT_CUDA(launch_ln_modulate_bwd(act, 0, X[i], at(ws, bp.dh[i]), mod + D, bstr, B, rpb[i], D, d->ln_eps,
-                                        dx1, dm + D, dm, 0, part, st),
-                 "LN1 backward");
+      MMDIT_CUDA(launch_qk_norm_rope_bwd(act, q, Gs[i]->g_q, Gs[i]->g_k, st), "QK-RMSNorm + RoPE backward");
     }
-    MMDIT_CUDA(launch_modulation_bwd(act, vec, W[i]->w_mod, dm, B, 6 * D, D, g->w_mod, g->b_mod, dvec,
-                                     dvec_written ? 1 : 0, part, st),
-               "modulation backward");
-    dvec_written = dvec_written || dvec != nullptr;
-    if (R > 0) MMDIT_CUDA(launch_convert(act, 0, dx1, static_cast<int64_t>(R) * D, DX[i], st), "dx to the activation type");
+    {
+      const auto dy = ptrs([&](int i) -> const void* { return at(ws, bp.dqkv[i]); });
+      const auto xx = ptrs([&](int i) -> const void* { return at(ws, bp.h1[i]); });
+      const auto ww = ptrs([&](int i) -> const void* { return W[i]->w_qkv; });
+      const auto dx = ptrs([&](int i) -> void* { return at(ws, bp.dh[i]); });
+      const auto dw = ptrs([&](int i) -> float* { return Gs[i]->w_qkv; });
+      const auto db = ptrs([&](int i) -> float* { return Gs[i]->b_qkv; });
+      if ((s = linear_bwd_streams(act, ns, R, 3 * D, D, dy.data(), xx.data(), ww.data(), dx.data(), dw.data(),
+                                  db.data(), lin, ws, st)) != MMDIT_OK)
+        return s;
+    }
+    bool dvec_written = false;
+    for (int i = 0; i < ns; ++i) {
+      const mmdit_stream_grads* g = Gs[i];
+      float* dm = at<float>(ws, bp.dm[i]);
+      const float* mod = at<float>(ws, p.mod[i]);
+      float* dx1 = at<float>(ws, bp.dx1[i]);
+      if (R[i] > 0)
+        MMDIT_CUDA(launch_ln_modulate_bwd(act, 0, X[i], at(ws, bp.dh[i]), mod + D, bstr, B, rpb[i], D, d->ln_eps,
+                                          dx1, dm + D, dm, 0, part, st),
+                   "LN1 backward");
+      MMDIT_CUDA(launch_modulation_bwd(act, vec, W[i]->w_mod, dm, B, 6 * D, D, g->w_mod, g->b_mod, dvec,
+                                       dvec_written ? 1 : 0, part, st),
+                 "modulation backward");
+      dvec_written = dvec_written || dvec != nullptr;
+      if (R[i] > 0)
+        MMDIT_CUDA(launch_convert(act, 0, dx1, static_cast<int64_t>(R[i]) * D, DX[i], st), "dx to the activation type");
+    }
   }
   return MMDIT_OK;
 }

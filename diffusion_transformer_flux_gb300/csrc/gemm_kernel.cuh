@@ -495,6 +495,7 @@ cudaError_t run_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t stream
   constexpr int kBK = 128 / kElt;
   const CUtensorMapDataType dt = KindTraits<KIND>::kMapType;
   const bool two = p.M1 > 0;
+  if (two && p.K1 > 0 && p.K1 != p.K) return cudaErrorInvalidValue;  // one K for both problems here
   CUtensorMap ta0, tb0, ta1, tb1;
   const uint64_t stride[1] = {static_cast<uint64_t>(p.K) * kElt};
   const uint32_t box_a[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kBM)};
@@ -553,8 +554,9 @@ cudaError_t dispatch_gemm(const GemmProblem& p, uint32_t* status, cudaStream_t s
   if (p.a_mn || p.b_mn) {
     // transposed operands: the pair kernel's plain-bias products only
     if constexpr (KIND == kKindF16) {
-      if ((p.epi != kEpiBias && p.epi != kEpiDGelu) || p.N % 256 != 0 || p.M1 > 0 || p.splits != 1)
+      if ((p.epi != kEpiBias && p.epi != kEpiDGelu) || p.N % 256 != 0 || p.splits != 1)
         return cudaErrorInvalidValue;
+      if (p.epi == kEpiDGelu && p.M1 > 0 && !p.ep1.aux) return cudaErrorInvalidValue;
       if (p.epi == kEpiDGelu) {
         if (p.a_mn || !p.ep.aux) return cudaErrorInvalidValue;
         return run_gemm_pair<KIND, 256, kEpiDGelu, 2>(p, status, stream);

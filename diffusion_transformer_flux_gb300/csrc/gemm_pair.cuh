@@ -41,7 +41,7 @@ template <int KIND, int BN, int EPI, int MAJ = 0>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<EPI>(), 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_b0,
                      const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b1,
-                     int M0, int M1, int N, int K, const __grid_constant__ EpiArgs ep0,
+                     int M0, int M1, int N, int K, int K1, int interleave, const __grid_constant__ EpiArgs ep0,
                      const __grid_constant__ EpiArgs ep1, uint32_t* status) {
   using Cfg = PairCfg<BN>;
   using TE = typename KindTraits<KIND>::TE;
@@ -69,16 +69,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<EPI>(),
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_kb = (K + kBK - 1) / kBK;
-  // Pair tiles: problem 0's (M fastest), then problem 1's; CTA r takes M block 2 mp + r.
+  const int num_kb0 = (K + kBK - 1) / kBK, num_kb1 = (K1 + kBK - 1) / kBK;
+  // Pair tiles: problem 0's (M fastest), then problem 1's (or, interleaved, alternating); CTA r
+  // takes M block 2 mp + r.
   const int num_n = N / BN;
   const int pm0 = (M0 + 2 * kBM - 1) / (2 * kBM), pm1 = (M1 + 2 * kBM - 1) / (2 * kBM);
   const int tiles0 = pm0 * num_n;
   const int tiles = tiles0 + pm1 * num_n;
   const int pair = blockIdx.x >> 1, pairs = gridDim.x >> 1;
   auto decode = [&](int tile, int& prob, int& m0, int& nb) {
-    prob = tile >= tiles0;
-    const int t = prob ? tile - tiles0 : tile;
+    // Interleaved (equal tile counts): every pair walks tile, tile + pairs, ...; the problem
+    // alternates along that walk, and each problem's tiles are numbered without gaps.
+    int t;
+    if (!interleave) {
+      prob = tile >= tiles0;
+      t = prob ? tile - tiles0 : tile;
+    } else if (pairs & 1) {
+      prob = tile & 1;
+      t = tile >> 1;
+    } else {
+      const int blk = tile / pairs, r = tile - blk * pairs;
+      prob = (r + blk) & 1;
+      t = blk * (pairs >> 1) + (r >> 1);
+    }
     const int pm = prob ? pm1 : pm0;
     m0 = (t % pm) * 2 * kBM + static_cast<int>(rank) * kBM;
     nb = t / pm;
@@ -120,6 +133,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<EPI>(),
         decode(tile, prob, m0, nb);
         const CUtensorMap* ma = prob ? &tm_a1 : &tm_a0;
         const CUtensorMap* mw = prob ? &tm_b1 : &tm_b0;
+        const int num_kb = prob ? num_kb1 : num_kb0;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait_cluster(&empty[stage], phase ^ 1, abort_flag, status, kErrGemmWait)) {
             ok = false;
@@ -164,6 +178,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(gemm_threads<EPI>(),
         if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1, abort_flag, status, kErrGemmWait)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        int prob, m0_unused, nb_unused;
+        decode(tile, prob, m0_unused, nb_unused);
+        const int num_kb = prob ? num_kb1 : num_kb0;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait_cluster(&full[stage], phase, abort_flag, status, kErrGemmWait)) {
             ok = false;
@@ -238,31 +255,46 @@ cudaError_t run_gemm_pair(const GemmProblem& p, uint32_t* status, cudaStream_t s
   if (p.N % BN != 0) return cudaErrorInvalidValue;
   const CUtensorMapDataType dt = KindTraits<KIND>::kMapType;
   const bool two = p.M1 > 0;
+  const int K1 = two && p.K1 > 0 ? p.K1 : p.K;  // the second problem's K
+  if (K1 < 1) return cudaErrorInvalidValue;
   CUtensorMap ta0, tb0, ta1, tb1;
   const uint64_t stride[1] = {static_cast<uint64_t>(p.K) * kElt};
+  const uint64_t stride1[1] = {static_cast<uint64_t>(K1) * kElt};
   const uint32_t box_a[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(kBM)};
   const uint32_t box_b[2] = {static_cast<uint32_t>(kBK), static_cast<uint32_t>(BN / 2)};
   const uint64_t da0[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.M)};
   const uint64_t db[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(p.N)};
-  const uint64_t da1[2] = {static_cast<uint64_t>(p.K), static_cast<uint64_t>(two ? p.M1 : p.M)};
+  const uint64_t da1[2] = {static_cast<uint64_t>(K1), static_cast<uint64_t>(two ? p.M1 : p.M)};
+  const uint64_t db1[2] = {static_cast<uint64_t>(K1), static_cast<uint64_t>(p.N)};
   if constexpr (MAJ != 0) {
     // transposed operands: [K, M] and [K, N] tensors read in (64 MN x kBK k) boxes
-    if (two || (p.a_mn && p.M % 8 != 0)) return cudaErrorInvalidValue;
+    if ((p.a_mn && (p.M % 8 != 0 || (two && p.M1 % 8 != 0)))) return cudaErrorInvalidValue;
     const uint32_t box_mn[2] = {128u / kElt, static_cast<uint32_t>(kBK)};
-    const uint64_t dat[2] = {static_cast<uint64_t>(p.M), static_cast<uint64_t>(p.K)};
-    const uint64_t dbt[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(p.K)};
-    const uint64_t sat[1] = {static_cast<uint64_t>(p.M) * kElt};
-    const uint64_t sbt[1] = {static_cast<uint64_t>(p.N) * kElt};
-    const bool ok_a = (MAJ & 1) ? encode_tmap(&ta0, dt, 2, p.A, dat, sat, box_mn, CU_TENSOR_MAP_SWIZZLE_128B)
-                                : encode_tmap(&ta0, dt, 2, p.A, da0, stride, box_a, CU_TENSOR_MAP_SWIZZLE_128B);
-    const bool ok_b = (MAJ & 2) ? encode_tmap(&tb0, dt, 2, p.W, dbt, sbt, box_mn, CU_TENSOR_MAP_SWIZZLE_128B)
-                                : encode_tmap(&tb0, dt, 2, p.W, db, stride, box_b, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (!ok_a || !ok_b) return cudaErrorInvalidValue;
-    ta1 = ta0, tb1 = tb0;
+    auto encode_pair = [&](CUtensorMap* ta, CUtensorMap* tb, const void* A, const void* W, int M, int K) {
+      const uint64_t dak[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+      const uint64_t dbk[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(p.N)};
+      const uint64_t sk[1] = {static_cast<uint64_t>(K) * kElt};
+      const uint64_t dat[2] = {static_cast<uint64_t>(M), static_cast<uint64_t>(K)};
+      const uint64_t dbt[2] = {static_cast<uint64_t>(p.N), static_cast<uint64_t>(K)};
+      const uint64_t sat[1] = {static_cast<uint64_t>(M) * kElt};
+      const uint64_t sbt[1] = {static_cast<uint64_t>(p.N) * kElt};
+      const bool ok_a = (MAJ & 1) ? encode_tmap(ta, dt, 2, A, dat, sat, box_mn, CU_TENSOR_MAP_SWIZZLE_128B)
+                                  : encode_tmap(ta, dt, 2, A, dak, sk, box_a, CU_TENSOR_MAP_SWIZZLE_128B);
+      const bool ok_b = (MAJ & 2) ? encode_tmap(tb, dt, 2, W, dbt, sbt, box_mn, CU_TENSOR_MAP_SWIZZLE_128B)
+                                  : encode_tmap(tb, dt, 2, W, dbk, sk, box_b, CU_TENSOR_MAP_SWIZZLE_128B);
+      return ok_a && ok_b;
+    };
+    if (!encode_pair(&ta0, &tb0, p.A, p.W, p.M, p.K)) return cudaErrorInvalidValue;
+    if (two) {
+      if (!encode_pair(&ta1, &tb1, p.A1, p.W1, p.M1, K1)) return cudaErrorInvalidValue;
+    } else {
+      ta1 = ta0, tb1 = tb0;
+    }
   } else if (!encode_tmap(&ta0, dt, 2, p.A, da0, stride, box_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
              !encode_tmap(&tb0, dt, 2, p.W, db, stride, box_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
-             !encode_tmap(&ta1, dt, 2, two ? p.A1 : p.A, da1, stride, box_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
-             !encode_tmap(&tb1, dt, 2, two ? p.W1 : p.W, db, stride, box_b, CU_TENSOR_MAP_SWIZZLE_128B)) {
+             !encode_tmap(&ta1, dt, 2, two ? p.A1 : p.A, da1, two ? stride1 : stride, box_a, CU_TENSOR_MAP_SWIZZLE_128B) ||
+             !encode_tmap(&tb1, dt, 2, two ? p.W1 : p.W, two ? db1 : db, two ? stride1 : stride, box_b,
+                          CU_TENSOR_MAP_SWIZZLE_128B)) {
     return cudaErrorInvalidValue;
   }
   auto kern = gemm_pair_kernel<KIND, BN, EPI, MAJ>;
@@ -291,12 +323,15 @@ cudaError_t run_gemm_pair(const GemmProblem& p, uint32_t* status, cudaStream_t s
     configured_device = dev;
   }
   const int num_n = p.N / BN;
-  const int tiles = ((p.M + 2 * kBM - 1) / (2 * kBM) + (two ? (p.M1 + 2 * kBM - 1) / (2 * kBM) : 0)) * num_n;
+  const int tiles0 = (p.M + 2 * kBM - 1) / (2 * kBM) * num_n;
+  const int tiles1 = two ? (p.M1 + 2 * kBM - 1) / (2 * kBM) * num_n : 0;
+  const int tiles = tiles0 + tiles1;
+  const int interleave = p.interleave && two && tiles0 == tiles1 ? 1 : 0;
   if (tiles == 0) return cudaSuccess;
   const int pairs = tiles < max_pairs ? tiles : max_pairs;
   {
     const cudaError_t e_ = launch_pdl(kern, dim3(2 * pairs), dim3(gemm_threads<EPI>()), Cfg::kSmemBytes, stream,
-                                        ta0, tb0, ta1, tb1, p.M, two ? p.M1 : 0, p.N, p.K, p.ep,
+                                        ta0, tb0, ta1, tb1, p.M, two ? p.M1 : 0, p.N, p.K, K1, interleave, p.ep,
                                         two ? p.ep1 : p.ep, status);
     if (e_ != cudaSuccess) return e_;
   }

@@ -73,8 +73,12 @@ struct GemmProblem {
   // Operands stored MN-major (bf16, kEpiBias, N % 256 == 0, no second problem): with a_mn, A is
   // held as A^T [K, M] (M contiguous, M % 8 == 0); with b_mn, W is held as W^T [K, N].
   int a_mn = 0, b_mn = 0;
-  // optional second problem with the same N, K and epilogue kind, run in the same launch
+  // optional second problem with the same N and epilogue kind, run in the same launch; its K is
+  // K1 (pair kernel only; 0: the same K).  With interleave (pair kernel, equal tile counts) the
+  // two problems' tiles alternate in the tile list instead of following one another.
   int M1 = 0;
+  int K1 = 0;
+  int interleave = 0;
   const void* A1 = nullptr;  // [M1, K]
   const void* W1 = nullptr;  // [N, K]
   EpiArgs ep1;
