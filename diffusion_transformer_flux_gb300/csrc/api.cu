@@ -52,7 +52,7 @@ EncodeTiledFn encode_fn() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-constexpr int kColsumChunks = 32;  // row chunks of the bias-gradient column sums
+constexpr int kColsumChunks = 128;  // row chunks of the bias-gradient column sums
 size_t elt_bytes(int act) { return act == MMDIT_BF16 ? 2 : 4; }
 
 // Sequential 256-byte-aligned carving of a workspace.

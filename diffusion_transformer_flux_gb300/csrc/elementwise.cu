@@ -653,27 +653,62 @@ __global__ void transpose_pad_kernel(const T* __restrict__ in, int R, int C, int
 }
 
 // Column sums of in [R, C] in a fixed order: chunk y of the rows into part[y, c], then the
-// chunks added in order.
-template <typename T>
+// chunks added in a fixed two-level order.  With C % 8 == 0 a thread sums 8 adjacent columns
+// from 16-byte (bf16) or 32-byte (fp32) loads, four rows in flight; otherwise one column.
+template <typename T, bool VEC>
 __global__ void colsum_partial_kernel(const T* __restrict__ in, int R, int C, float* __restrict__ part) {
   pdl_wait();  // the previous kernel's results are visible from here on
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  constexpr int W = VEC ? 8 : 1;
+  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * W;
   if (c >= C) return;
   const int per = (R + gridDim.y - 1) / gridDim.y;
   const int r0 = blockIdx.y * per;
   const int r1 = r0 + per < R ? r0 + per : R;
-  float acc = 0.f;
-  for (int r = r0; r < r1; ++r) acc += to_f32(in[static_cast<size_t>(r) * C + c]);
-  part[static_cast<size_t>(blockIdx.y) * C + c] = acc;
+  float acc[W];
+#pragma unroll
+  for (int e = 0; e < W; ++e) acc[e] = 0.f;
+  if constexpr (VEC) {
+    int r = r0;
+    for (; r + 4 <= r1; r += 4) {
+      float v[4][8];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) load8(in + static_cast<size_t>(r + u) * C + c, v[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += v[u][e];
+    }
+    for (; r < r1; ++r) {
+      float v[8];
+      load8(in + static_cast<size_t>(r) * C + c, v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] += v[e];
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) part[static_cast<size_t>(blockIdx.y) * C + c + e] = acc[e];
+  } else {
+    for (int r = r0; r < r1; ++r) acc[0] += to_f32(in[static_cast<size_t>(r) * C + c]);
+    part[static_cast<size_t>(blockIdx.y) * C + c] = acc[0];
+  }
 }
 
-__global__ void colsum_finish_kernel(const float* __restrict__ part, int chunks, int C, float* __restrict__ out) {
+// Block (32, 32) over 32 columns: thread (x, y) adds chunks y, y + 32, ... of its column in order,
+// thread row 0 then adds the 32 group sums in order.
+__global__ void __launch_bounds__(1024) colsum_finish_kernel(const float* __restrict__ part, int chunks, int C,
+                                                             float* __restrict__ out) {
   pdl_wait();  // the previous kernel's results are visible from here on
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= C) return;
+  __shared__ float grp[32][33];
+  const int c = blockIdx.x * 32 + threadIdx.x;
   float acc = 0.f;
-  for (int i = 0; i < chunks; ++i) acc += part[static_cast<size_t>(i) * C + c];
-  out[c] = acc;
+  if (c < C)
+    for (int i = threadIdx.y; i < chunks; i += 32) acc += part[static_cast<size_t>(i) * C + c];
+  grp[threadIdx.y][threadIdx.x] = acc;
+  __syncthreads();
+  if (threadIdx.y != 0 || c >= C) return;
+  float t = 0.f;
+#pragma unroll 8
+  for (int g = 0; g < 32; ++g) t += grp[g][threadIdx.x];
+  out[c] = t;
 }
 
 // ----------------------------------------------------------------------------- launchers
@@ -1040,22 +1075,24 @@ cudaError_t launch_colsum(int act, const void* in, int R, int C, float* part, in
                           cudaStream_t stream) {
   if (C <= 0) return cudaSuccess;
   if (chunks < 1) return cudaErrorInvalidValue;
-  const dim3 grid((C + 255) / 256, chunks);
-  if (act == 1) {
-    const cudaError_t e_ = launch_pdl(colsum_partial_kernel<__nv_bfloat16>, grid, dim3(256), 0, stream,
-                                      static_cast<const __nv_bfloat16*>(in), R, C, part);
-    if (e_ != cudaSuccess) return e_;
-  } else {
-    const cudaError_t e_ = launch_pdl(colsum_partial_kernel<float>, grid, dim3(256), 0, stream,
-                                      static_cast<const float*>(in), R, C, part);
-    if (e_ != cudaSuccess) return e_;
-  }
+  const size_t elt = act == 1 ? 2 : 4;
+  const bool vec = C % 8 == 0 && reinterpret_cast<uintptr_t>(in) % (8 * elt) == 0;
+  const dim3 grid(vec ? (C / 8 + 127) / 128 : (C + 127) / 128, chunks);
+  cudaError_t e_;
+  if (act == 1)
+    e_ = vec ? launch_pdl(colsum_partial_kernel<__nv_bfloat16, true>, grid, dim3(128), 0, stream,
+                          static_cast<const __nv_bfloat16*>(in), R, C, part)
+             : launch_pdl(colsum_partial_kernel<__nv_bfloat16, false>, grid, dim3(128), 0, stream,
+                          static_cast<const __nv_bfloat16*>(in), R, C, part);
+  else
+    e_ = vec ? launch_pdl(colsum_partial_kernel<float, true>, grid, dim3(128), 0, stream,
+                          static_cast<const float*>(in), R, C, part)
+             : launch_pdl(colsum_partial_kernel<float, false>, grid, dim3(128), 0, stream,
+                          static_cast<const float*>(in), R, C, part);
+  if (e_ != cudaSuccess) return e_;
   count_launch();
-  {
-    const cudaError_t e_ = launch_pdl(colsum_finish_kernel, dim3((C + 255) / 256), dim3(256), 0, stream, part,
-                                      chunks, C, out);
-    if (e_ != cudaSuccess) return e_;
-  }
+  e_ = launch_pdl(colsum_finish_kernel, dim3((C + 31) / 32), dim3(32, 32), 0, stream, part, chunks, C, out);
+  if (e_ != cudaSuccess) return e_;
   count_launch();
   return cudaGetLastError();
 }
