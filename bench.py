@@ -811,6 +811,59 @@ def measure_block_bwd(st, L, torch, peak, reps=3):
                                    "frac": round(2.5 * attn / attn_us / 1e6 / peak, 4) if attn_us else None}}
 
 
+def measure_block_train(st, L, torch, peak, reps=3):
+    """One double block's share of a training step at the step's shapes, two ways: the forward
+    (mmdit_double_block_fwd) then the one-call backward, which recomputes the forward; and the
+    training pair (mmdit_double_block_fwd_train, which keeps what the backward reads, then
+    mmdit_double_block_bwd_saved).  CUDA events around `reps` of each after one warm-up; the
+    work counted is the forward's contractions plus the backward's (2 x the GEMMs + 2.5 x the
+    attention), the same for both."""
+    wl = st.wl
+    B, D, F, H, S_i, S_t = wl.batch, wl.hidden, wl.mlp_hidden, wl.heads, wl.seq_img, wl.seq_txt
+    S = S_i + S_t
+    dev = st.vec.device
+    gen = torch.Generator(device=dev).manual_seed(8)
+    dy_i = (torch.randn(B, S_i, D, device=dev, generator=gen) * 1e-3).to(torch.bfloat16)
+    dy_t = (torch.randn(B, S_t, D, device=dev, generator=gen) * 1e-3).to(torch.bfloat16)
+    y_i, y_t = torch.empty_like(dy_i), torch.empty_like(dy_t)
+    dx_i, dx_t = torch.empty_like(dy_i), torch.empty_like(dy_t)
+    dvec = torch.empty(B, D, device=dev)
+    grads = [{n: torch.empty(tuple(w[n].shape), device=dev) for n in L.STREAM_W_FIELDS}
+             for w in (st.w_dimg, st.w_dtxt)]
+    common = (st.dims, st.w_dimg, st.w_dtxt, st.vec, st.cos, st.sin, st.x_img, st.x_txt)
+    ws_f = L.workspace(L.mmdit_double_block_workspace_size(st.dims), dev)
+    ws_b = L.workspace(L.mmdit_double_block_bwd_workspace_size(st.dims), dev)
+
+    def recompute():
+        L.mmdit_double_block_fwd(*common, y_i, y_t, ws=ws_f)
+        L.mmdit_double_block_bwd(*common, dy_i, dy_t, dx_i, dx_t, dvec, grads[0], grads[1], ws=ws_b)
+
+    def pair():
+        L.mmdit_double_block_fwd_train(*common, y_i, y_t, saved=ws_b)
+        L.mmdit_double_block_bwd_saved(*common, dy_i, dy_t, dx_i, dx_t, ws_b, dvec, grads[0], grads[1])
+
+    out = {}
+    for name, fn in (("forward + one-call backward", recompute), ("training pair", pair)):
+        fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        if L.mmdit_workspace_status(ws_b) != 0:
+            raise RuntimeError("a kernel gave up a bounded wait in the block training step")
+        out[name] = a.elapsed_time(b) * 1e3 / reps
+    gemm = 2 * B * S * D * (3 * D + D + 2 * F)
+    attn = 4 * B * S * S * 128 * H
+    flops = (gemm + attn) + (2 * gemm + 2.5 * attn)
+    del grads, ws_f, ws_b
+    return {"op": "double block forward + backward (all gradients)", "tokens": S, "flops_counted": flops,
+            **{k: {"avg_us": round(v, 2), "achieved_tflops": round(flops / v / 1e6, 1),
+                   "frac": round(flops / v / 1e6 / peak, 4)} for k, v in out.items()}}
+
+
 def measure_linear_bwd(L, torch, device, peak, M=4608, N=12288, K=3072, reps=5):
     """The backward of the block's fc1-shaped linear (mmdit_linear_bwd: dx and dW through the
     tensor-core GEMM reading W, dy and x MN-major as stored, db): 4 M N K FLOPs per call, CUDA
@@ -1061,6 +1114,7 @@ def main():
         extras["single_block_parallel"] = measure_parallel_block(st, L, torch, bf16_peak)
         extras["linear_backward"] = measure_linear_bwd(L, torch, device, bf16_peak)
         extras["double_block_backward"] = measure_block_bwd(st, L, torch, bf16_peak)
+        extras["double_block_training"] = measure_block_train(st, L, torch, bf16_peak)
     if fp8:
         extras["fp8_peak"] = fp8_meas
 

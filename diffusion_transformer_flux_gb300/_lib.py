@@ -37,7 +37,9 @@ EXPORTED = [
     "mmdit_fp8_linear_fwd", "mmdit_fp8_linear_bwd_workspace_size", "mmdit_fp8_linear_bwd",
     "mmdit_single_block_parallel_fwd", "mmdit_linear_bwd_workspace_size",
     "mmdit_linear_bwd", "mmdit_double_block_bwd_workspace_size", "mmdit_double_block_bwd",
-    "mmdit_single_block_bwd_workspace_size", "mmdit_single_block_bwd", "mmdit_modulation_batched_fwd", "mmdit_conditioning_workspace_size",
+    "mmdit_single_block_bwd_workspace_size", "mmdit_single_block_bwd", "mmdit_double_block_fwd_train",
+    "mmdit_double_block_bwd_saved", "mmdit_single_block_fwd_train", "mmdit_single_block_bwd_saved",
+    "mmdit_modulation_batched_fwd", "mmdit_conditioning_workspace_size",
     "mmdit_conditioning_fwd", "mmdit_flux_workspace_size", "mmdit_flux_forward",
 ]
 
@@ -172,6 +174,11 @@ _SIGS = {
                                          VP, SZ, VP]),
     "mmdit_single_block_bwd_workspace_size": (SZ, [PDIMS]),
     "mmdit_single_block_bwd": (C.c_int, [PDIMS, PW, VP, VP, VP, VP, VP, VP, VP, PGRADS, VP, SZ, VP]),
+    "mmdit_double_block_fwd_train": (C.c_int, [PDIMS, PW, PW, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_double_block_bwd_saved": (C.c_int, [PDIMS, PW, PW, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, PGRADS, PGRADS,
+                                               VP, SZ, VP]),
+    "mmdit_single_block_fwd_train": (C.c_int, [PDIMS, PW, VP, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_single_block_bwd_saved": (C.c_int, [PDIMS, PW, VP, VP, VP, VP, VP, VP, VP, PGRADS, VP, SZ, VP]),
     "mmdit_modulation_batched_fwd": (C.c_int, [I32, I32, I32, VP, I32, C.POINTER(GemvJob), VP]),
     "mmdit_conditioning_workspace_size": (SZ, [I32, I32, I32, I32]),
     "mmdit_conditioning_fwd": (C.c_int, [I32, I32, I32, I32, I32, PCOND, VP, VP, VP, VP, VP, SZ, VP]),
@@ -638,6 +645,51 @@ def mmdit_single_block_bwd(dims: Dims, w: dict, vec, cos, sin, x, dy, dx, dvec=N
                                          _ptr(dy), _ptr(dx), _ptr(dvec), C.byref(gg) if gg else None, _ptr(ws),
                                          ws.numel(), _stream(stream)))
     return ws
+
+
+def mmdit_double_block_fwd_train(dims: Dims, w_img: dict, w_txt: dict, vec, cos, sin, x_img, x_txt, y_img, y_txt,
+                                 saved=None, stream=None):
+    """The training pair's forward (see include/mmdit.h): the block outputs, and in `saved` (a
+    backward-sized workspace, returned) what mmdit_double_block_bwd_saved reads."""
+    if saved is None:
+        saved = workspace(mmdit_double_block_bwd_workspace_size(dims), x_img.device)
+    wi, wt = make_stream_w(w_img), make_stream_w(w_txt)
+    _check(load().mmdit_double_block_fwd_train(C.byref(dims), C.byref(wi), C.byref(wt), _ptr(vec), _ptr(cos), _ptr(sin),
+                                               _ptr(x_img), _ptr(x_txt), _ptr(y_img), _ptr(y_txt), _ptr(saved),
+                                               saved.numel(), _stream(stream)))
+    return saved
+
+
+def mmdit_double_block_bwd_saved(dims: Dims, w_img: dict, w_txt: dict, vec, cos, sin, x_img, x_txt, dy_img, dy_txt,
+                                 dx_img, dx_txt, saved, dvec=None, g_img=None, g_txt=None, stream=None):
+    """The training pair's backward: gradients from the state mmdit_double_block_fwd_train left."""
+    wi, wt = make_stream_w(w_img), make_stream_w(w_txt)
+    gi, gt = make_stream_grads(g_img), make_stream_grads(g_txt)
+    _check(load().mmdit_double_block_bwd_saved(C.byref(dims), C.byref(wi), C.byref(wt), _ptr(vec), _ptr(cos), _ptr(sin),
+                                               _ptr(x_img), _ptr(x_txt), _ptr(dy_img), _ptr(dy_txt), _ptr(dx_img),
+                                               _ptr(dx_txt), _ptr(dvec), C.byref(gi) if gi else None,
+                                               C.byref(gt) if gt else None, _ptr(saved), saved.numel(),
+                                               _stream(stream)))
+
+
+def mmdit_single_block_fwd_train(dims: Dims, w: dict, vec, cos, sin, x, y, saved=None, stream=None):
+    """The single block's training forward (see mmdit_double_block_fwd_train)."""
+    if saved is None:
+        saved = workspace(mmdit_single_block_bwd_workspace_size(dims), x.device)
+    sw = make_stream_w(w)
+    _check(load().mmdit_single_block_fwd_train(C.byref(dims), C.byref(sw), _ptr(vec), _ptr(cos), _ptr(sin), _ptr(x),
+                                               _ptr(y), _ptr(saved), saved.numel(), _stream(stream)))
+    return saved
+
+
+def mmdit_single_block_bwd_saved(dims: Dims, w: dict, vec, cos, sin, x, dy, dx, saved, dvec=None, g=None,
+                                 stream=None):
+    """The single block's training backward (see mmdit_double_block_bwd_saved)."""
+    sw = make_stream_w(w)
+    gg = make_stream_grads(g)
+    _check(load().mmdit_single_block_bwd_saved(C.byref(dims), C.byref(sw), _ptr(vec), _ptr(cos), _ptr(sin), _ptr(x),
+                                               _ptr(dy), _ptr(dx), _ptr(dvec), C.byref(gg) if gg else None,
+                                               _ptr(saved), saved.numel(), _stream(stream)))
 
 
 def mmdit_fp8_linear_bwd(dy, x_q, w_q, scale_x, scale_w, scale_dy, amax_dy, dx, dw=None, db=None, x=None,

@@ -1028,10 +1028,17 @@ bool plan_block_bwd(const mmdit_dims* d, bool single, BwdPlan* p) {
 // outputs are written by the fused GEMMs' epilogues alongside their usual outputs).  Then, per stream, the MLP branch and the
 // attention projection backward; the joint attention backward; per stream the QK-RMSNorm + RoPE,
 // QKV and LayerNorm backward and the modulation backward.
+//
+// `phases` selects the parts: kBwdForward (the recomputation, into the workspace; with Y the block's
+// outputs also go there) and kBwdGradients (everything after it, reading what the forward left in
+// the workspace).  The training pair mmdit_*_block_fwd_train / mmdit_*_block_bwd_saved runs them
+// in two calls around the caller's own work.
+constexpr int kBwdForward = 1, kBwdGradients = 2;
 mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, const mmdit_stream_w* const* W,
                             const void* vec, const float* rope_cos, const float* rope_sin, const void* const* X,
                             const void* const* DY, void* const* DX, float* dvec,
-                            const mmdit_stream_grads* const* G, void* ws, cudaStream_t st) {
+                            const mmdit_stream_grads* const* G, void* ws, cudaStream_t st,
+                            int phases = kBwdForward | kBwdGradients, void* const* Y = nullptr) {
   const BlockPlan& p = bp.f;
   const int act = d->act, B = p.B, D = p.D, F = p.F, H = p.H, S = p.S;
   const size_t e = p.elt;
@@ -1040,6 +1047,7 @@ mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, cons
   const mmdit_stream_grads none = {};
   mmdit_status s = MMDIT_OK;
   // ---------------- forward, keeping what the backward reads
+  if (phases & kBwdForward) {
   {
     ModulationJob jobs[2];
     for (int i = 0; i < ns; ++i) jobs[i] = {W[i]->w_mod, W[i]->b_mod, at<float>(ws, p.mod[i]), 6 * D};
@@ -1050,7 +1058,8 @@ mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, cons
   ss.n = 0;
   for (int i = 0; i < ns; ++i) {
     if (rpb[i] == 0) continue;
-    ss.s[ss.n] = i, ss.w[ss.n] = W[i], ss.x[ss.n] = X[i], ss.y[ss.n] = at(ws, bp.ytmp[i]), ss.rpb[ss.n] = rpb[i];
+    ss.s[ss.n] = i, ss.w[ss.n] = W[i], ss.x[ss.n] = X[i], ss.rpb[ss.n] = rpb[i];
+    ss.y[ss.n] = Y ? Y[i] : at(ws, bp.ytmp[i]);
     ss.mod[ss.n] = at<float>(ws, p.mod[i]);
     // the linears' outputs before their norm, GELU or gate come out of the same GEMMs
     ss.pre_qkv[ss.n] = at(ws, bp.qkv_pre[i]), ss.pre_o[ss.n] = at(ws, bp.a[i]);
@@ -1077,6 +1086,8 @@ mmdit_status block_bwd_body(const mmdit_dims* d, const BwdPlan& bp, int ns, cons
   }
   // x1, the MLP's h (in h), u, and the linears' pre-gate / pre-GELU outputs
   if ((s = run_post(d, p, ss, no_fp8, ws, st)) != MMDIT_OK) return s;
+  }
+  if (!(phases & kBwdGradients)) return MMDIT_OK;
   // ---------------- backward: MLP branch and the attention projection, both streams step by step
   // (each linear's backward runs for both streams in shared launches)
   float* part = at<float>(ws, bp.part);
@@ -2049,19 +2060,23 @@ size_t mmdit_single_block_bwd_workspace_size(const mmdit_dims* d) {
   return p.total;
 }
 
-mmdit_status mmdit_double_block_bwd(const mmdit_dims* d, const mmdit_stream_w* w_img, const mmdit_stream_w* w_txt,
-                                    const void* vec, const float* rope_cos, const float* rope_sin, const void* x_img,
-                                    const void* x_txt, const void* dy_img, const void* dy_txt, void* dx_img,
-                                    void* dx_txt, float* dvec, const mmdit_stream_grads* g_img,
-                                    const mmdit_stream_grads* g_txt, void* workspace, size_t workspace_bytes,
-                                    void* stream) {
+namespace {
+
+// The checks and set-up every double-block backward call shares; `dy`, `dx` may be NULL for the
+// forward half of the training pair.
+mmdit_status double_bwd_call(const mmdit_dims* d, const mmdit_stream_w* w_img, const mmdit_stream_w* w_txt,
+                             const void* vec, const float* rope_cos, const float* rope_sin, const void* x_img,
+                             const void* x_txt, const void* dy_img, const void* dy_txt, void* dx_img, void* dx_txt,
+                             float* dvec, const mmdit_stream_grads* g_img, const mmdit_stream_grads* g_txt,
+                             void* y_img, void* y_txt, void* workspace, size_t workspace_bytes, void* stream,
+                             int phases, const char* what) {
   mmdit_status s = check_block_bwd(d, false);
   if (s != MMDIT_OK) return s;
   if ((s = check_stream_w(w_img, "image weights")) != MMDIT_OK || (s = check_stream_w(w_txt, "text weights")) != MMDIT_OK)
     return s;
-  if ((s = check_ptrs({vec, rope_cos, rope_sin, x_img, x_txt, dy_img, dy_txt, dx_img, dx_txt},
-                      "double block backward")) != MMDIT_OK)
-    return s;
+  if ((s = check_ptrs({vec, rope_cos, rope_sin, x_img, x_txt}, what)) != MMDIT_OK) return s;
+  if ((phases & kBwdGradients) && (s = check_ptrs({dy_img, dy_txt, dx_img, dx_txt}, what)) != MMDIT_OK) return s;
+  if (!(phases & kBwdGradients) && (s = check_ptrs({y_img, y_txt}, what)) != MMDIT_OK) return s;
   if (dvec && !aligned16(dvec)) return fail(MMDIT_ERR_INVALID_ARG, "dvec is not 16-byte aligned");
   if ((s = check_grads(g_img, "image gradients")) != MMDIT_OK || (s = check_grads(g_txt, "text gradients")) != MMDIT_OK)
     return s;
@@ -2078,18 +2093,22 @@ mmdit_status mmdit_double_block_bwd(const mmdit_dims* d, const mmdit_stream_w* w
   const void* X[2] = {x_img, x_txt};
   const void* DY[2] = {dy_img, dy_txt};
   void* DX[2] = {dx_img, dx_txt};
+  void* Y[2] = {y_img, y_txt};
   const mmdit_stream_grads* G[2] = {g_img, g_txt};
-  return block_bwd_body(d, p, 2, W, vec, rope_cos, rope_sin, X, DY, DX, dvec, G, workspace, st);
+  return block_bwd_body(d, p, 2, W, vec, rope_cos, rope_sin, X, DY, DX, dvec, G, workspace, st, phases,
+                        (phases & kBwdGradients) ? nullptr : Y);
 }
 
-mmdit_status mmdit_single_block_bwd(const mmdit_dims* d, const mmdit_stream_w* w, const void* vec,
-                                    const float* rope_cos, const float* rope_sin, const void* x, const void* dy,
-                                    void* dx, float* dvec, const mmdit_stream_grads* g, void* workspace,
-                                    size_t workspace_bytes, void* stream) {
+mmdit_status single_bwd_call(const mmdit_dims* d, const mmdit_stream_w* w, const void* vec, const float* rope_cos,
+                             const float* rope_sin, const void* x, const void* dy, void* dx, float* dvec,
+                             const mmdit_stream_grads* g, void* y, void* workspace, size_t workspace_bytes,
+                             void* stream, int phases, const char* what) {
   mmdit_status s = check_block_bwd(d, true);
   if (s != MMDIT_OK) return s;
   if ((s = check_stream_w(w, "single block weights")) != MMDIT_OK) return s;
-  if ((s = check_ptrs({vec, rope_cos, rope_sin, x, dy, dx}, "single block backward")) != MMDIT_OK) return s;
+  if ((s = check_ptrs({vec, rope_cos, rope_sin, x}, what)) != MMDIT_OK) return s;
+  if ((phases & kBwdGradients) && (s = check_ptrs({dy, dx}, what)) != MMDIT_OK) return s;
+  if (!(phases & kBwdGradients) && (s = check_ptrs({y}, what)) != MMDIT_OK) return s;
   if (dvec && !aligned16(dvec)) return fail(MMDIT_ERR_INVALID_ARG, "dvec is not 16-byte aligned");
   if ((s = check_grads(g, "single block gradients")) != MMDIT_OK) return s;
   BwdPlan p;
@@ -2104,8 +2123,67 @@ mmdit_status mmdit_single_block_bwd(const mmdit_dims* d, const mmdit_stream_w* w
   const void* X[1] = {x};
   const void* DY[1] = {dy};
   void* DX[1] = {dx};
+  void* Y[1] = {y};
   const mmdit_stream_grads* G[1] = {g};
-  return block_bwd_body(d, p, 1, W, vec, rope_cos, rope_sin, X, DY, DX, dvec, G, workspace, st);
+  return block_bwd_body(d, p, 1, W, vec, rope_cos, rope_sin, X, DY, DX, dvec, G, workspace, st, phases,
+                        (phases & kBwdGradients) ? nullptr : Y);
+}
+
+}  // namespace
+
+mmdit_status mmdit_double_block_bwd(const mmdit_dims* d, const mmdit_stream_w* w_img, const mmdit_stream_w* w_txt,
+                                    const void* vec, const float* rope_cos, const float* rope_sin, const void* x_img,
+                                    const void* x_txt, const void* dy_img, const void* dy_txt, void* dx_img,
+                                    void* dx_txt, float* dvec, const mmdit_stream_grads* g_img,
+                                    const mmdit_stream_grads* g_txt, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+  return double_bwd_call(d, w_img, w_txt, vec, rope_cos, rope_sin, x_img, x_txt, dy_img, dy_txt, dx_img, dx_txt,
+                         dvec, g_img, g_txt, nullptr, nullptr, workspace, workspace_bytes, stream,
+                         kBwdForward | kBwdGradients, "double block backward");
+}
+
+mmdit_status mmdit_double_block_fwd_train(const mmdit_dims* d, const mmdit_stream_w* w_img,
+                                          const mmdit_stream_w* w_txt, const void* vec, const float* rope_cos,
+                                          const float* rope_sin, const void* x_img, const void* x_txt, void* y_img,
+                                          void* y_txt, void* saved, size_t saved_bytes, void* stream) {
+  return double_bwd_call(d, w_img, w_txt, vec, rope_cos, rope_sin, x_img, x_txt, nullptr, nullptr, nullptr, nullptr,
+                         nullptr, nullptr, nullptr, y_img, y_txt, saved, saved_bytes, stream, kBwdForward,
+                         "double block training forward");
+}
+
+mmdit_status mmdit_double_block_bwd_saved(const mmdit_dims* d, const mmdit_stream_w* w_img,
+                                          const mmdit_stream_w* w_txt, const void* vec, const float* rope_cos,
+                                          const float* rope_sin, const void* x_img, const void* x_txt,
+                                          const void* dy_img, const void* dy_txt, void* dx_img, void* dx_txt,
+                                          float* dvec, const mmdit_stream_grads* g_img,
+                                          const mmdit_stream_grads* g_txt, void* saved, size_t saved_bytes,
+                                          void* stream) {
+  return double_bwd_call(d, w_img, w_txt, vec, rope_cos, rope_sin, x_img, x_txt, dy_img, dy_txt, dx_img, dx_txt,
+                         dvec, g_img, g_txt, nullptr, nullptr, saved, saved_bytes, stream, kBwdGradients,
+                         "double block backward (saved forward)");
+}
+
+mmdit_status mmdit_single_block_bwd(const mmdit_dims* d, const mmdit_stream_w* w, const void* vec,
+                                    const float* rope_cos, const float* rope_sin, const void* x, const void* dy,
+                                    void* dx, float* dvec, const mmdit_stream_grads* g, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  return single_bwd_call(d, w, vec, rope_cos, rope_sin, x, dy, dx, dvec, g, nullptr, workspace, workspace_bytes,
+                         stream, kBwdForward | kBwdGradients, "single block backward");
+}
+
+mmdit_status mmdit_single_block_fwd_train(const mmdit_dims* d, const mmdit_stream_w* w, const void* vec,
+                                          const float* rope_cos, const float* rope_sin, const void* x, void* y,
+                                          void* saved, size_t saved_bytes, void* stream) {
+  return single_bwd_call(d, w, vec, rope_cos, rope_sin, x, nullptr, nullptr, nullptr, nullptr, y, saved, saved_bytes,
+                         stream, kBwdForward, "single block training forward");
+}
+
+mmdit_status mmdit_single_block_bwd_saved(const mmdit_dims* d, const mmdit_stream_w* w, const void* vec,
+                                          const float* rope_cos, const float* rope_sin, const void* x, const void* dy,
+                                          void* dx, float* dvec, const mmdit_stream_grads* g, void* saved,
+                                          size_t saved_bytes, void* stream) {
+  return single_bwd_call(d, w, vec, rope_cos, rope_sin, x, dy, dx, dvec, g, nullptr, saved, saved_bytes, stream,
+                         kBwdGradients, "single block backward (saved forward)");
 }
 
 mmdit_status mmdit_modulation_batched_fwd(int32_t act, int32_t batch, int32_t dim, const void* vec,

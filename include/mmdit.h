@@ -514,6 +514,38 @@ mmdit_status mmdit_single_block_bwd(const mmdit_dims *dims, const mmdit_stream_w
                                     void *dx, float *dvec, const mmdit_stream_grads *g,
                                     void *workspace, size_t workspace_bytes, void *stream);
 
+/* Training pair: the same backward split in two calls, so that a training step runs the forward
+ * once.  mmdit_*_block_fwd_train computes the block's outputs y (as mmdit_*_block_fwd would, from
+ * the same kernels) and leaves in `saved` (a buffer of mmdit_*_block_bwd_workspace_size bytes,
+ * owned by the caller) everything the backward reads; mmdit_*_block_bwd_saved then writes the
+ * gradients exactly as mmdit_*_block_bwd does, without recomputing the forward.  Between the two
+ * calls `saved` must not be touched, and the dims, weights, vec, RoPE tables and inputs x must be
+ * the same (the backward reads x again).  The backward consumes `saved`: a second backward needs
+ * a new forward.  Checks and supported shapes as for mmdit_*_block_bwd; y is of type `act` with
+ * the forward's layout. */
+mmdit_status mmdit_double_block_fwd_train(const mmdit_dims *dims, const mmdit_stream_w *w_img,
+                                          const mmdit_stream_w *w_txt, const void *vec,
+                                          const float *rope_cos, const float *rope_sin,
+                                          const void *x_img, const void *x_txt, void *y_img,
+                                          void *y_txt, void *saved, size_t saved_bytes, void *stream);
+mmdit_status mmdit_double_block_bwd_saved(const mmdit_dims *dims, const mmdit_stream_w *w_img,
+                                          const mmdit_stream_w *w_txt, const void *vec,
+                                          const float *rope_cos, const float *rope_sin,
+                                          const void *x_img, const void *x_txt, const void *dy_img,
+                                          const void *dy_txt, void *dx_img, void *dx_txt,
+                                          float *dvec, const mmdit_stream_grads *g_img,
+                                          const mmdit_stream_grads *g_txt, void *saved,
+                                          size_t saved_bytes, void *stream);
+mmdit_status mmdit_single_block_fwd_train(const mmdit_dims *dims, const mmdit_stream_w *w,
+                                          const void *vec, const float *rope_cos,
+                                          const float *rope_sin, const void *x, void *y, void *saved,
+                                          size_t saved_bytes, void *stream);
+mmdit_status mmdit_single_block_bwd_saved(const mmdit_dims *dims, const mmdit_stream_w *w,
+                                          const void *vec, const float *rope_cos,
+                                          const float *rope_sin, const void *x, const void *dy,
+                                          void *dx, float *dvec, const mmdit_stream_grads *g,
+                                          void *saved, size_t saved_bytes, void *stream);
+
 /* ---------------------------------------------------------------------------------------
  * Many modulations in one launch: the AdaLN modulation of mmdit_modulation_fwd for every job
  * in `jobs` (every block of a model, which all read the same vec), out_j[b, r] =

@@ -299,6 +299,35 @@ def test_block_backward_rejects_bad_arguments_before_any_cuda_call(lib):
     assert sb(C.byref(d), C.byref(w), 16, 16, 16, 16, 16, 16, None, None, 256, 16, None) == 3
 
 
+def test_training_pair_rejects_bad_arguments_before_any_cuda_call(lib):
+    # the split backward: same checks as the one-call backward; the forward half needs the
+    # outputs y, the backward half dy and dx, both a backward-sized `saved` buffer
+    d = _dims(seq_img=256, seq_txt=45, hidden=256, heads=2, mlp_hidden=1024)
+    need = L.mmdit_double_block_bwd_workspace_size(d)
+    w = L.StreamW(*([16] * 12), None)
+    ft, bs = lib.mmdit_double_block_fwd_train, lib.mmdit_double_block_bwd_saved
+    # fwd_train(dims, w_img, w_txt, vec, cos, sin, x_img, x_txt, y_img, y_txt, saved, bytes, stream)
+    assert ft(C.byref(d), C.byref(w), C.byref(w), 16, 16, 16, 16, 16, None, 16, 256, 1 << 40, None) == 1
+    assert "training forward" in L.last_error()
+    assert ft(C.byref(d), C.byref(w), C.byref(w), 16, 16, 16, 16, 16, 16, 16, 256, need - 1, None) == 3
+    f32 = _dims(seq_img=256, seq_txt=45, hidden=256, heads=2, mlp_hidden=1024, act=L.MMDIT_F32)
+    assert ft(C.byref(f32), C.byref(w), C.byref(w), 16, 16, 16, 16, 16, 16, 16, 256, 1 << 40, None) == 2
+    # bwd_saved(dims, w_img, w_txt, vec, cos, sin, x_img, x_txt, dy_img, dy_txt, dx_img, dx_txt, dvec,
+    #           g_img, g_txt, saved, bytes, stream)
+    assert bs(C.byref(d), C.byref(w), C.byref(w), 16, 16, 16, 16, 16, 16, 16, 16, None, None, None, None,
+              256, 1 << 40, None) == 1
+    assert "saved forward" in L.last_error()
+    assert bs(C.byref(d), C.byref(w), C.byref(w), 16, 16, 16, 16, 16, 16, 16, 16, 16, 0x1004, None, None,
+              256, 1 << 40, None) == 1
+    assert bs(C.byref(d), C.byref(w), C.byref(w), 16, 16, 16, 16, 16, 16, 16, 16, 16, None, None, None,
+              256, need - 1, None) == 3
+    sft, sbs = lib.mmdit_single_block_fwd_train, lib.mmdit_single_block_bwd_saved
+    assert sft(C.byref(d), C.byref(w), 16, 16, 16, 16, None, 256, 1 << 40, None) == 1
+    assert sbs(C.byref(d), C.byref(w), 16, 16, 16, 16, 16, None, None, None, 256, 1 << 40, None) == 1
+    assert sbs(C.byref(d), C.byref(w), 16, 16, 16, 16, 16, 16, None, None, 256,
+               L.mmdit_single_block_bwd_workspace_size(d) - 1, None) == 3
+
+
 def test_binding_refuses_host_tensors():
     # a host tensor's address would reach a kernel as if it were device memory
     import torch

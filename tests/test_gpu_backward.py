@@ -145,3 +145,70 @@ def test_backward_optional_outputs_and_repeat():
     rdx, _, rg = BW.single_block_backward(x, case.vec, case.cos, case.sin, case.w_img, case.H, host(dy))
     _check(host(g1["w_1"]), rg["w_1"], "w_1")
     _check(host(g1["b_mod"]), rg["b_mod"], "b_mod")
+
+
+def _close(a, b, what, rel=1e-5):
+    a, b = host(a), host(b)
+    scale = max(float(np.abs(b).max()), 1e-30)
+    err = float(np.abs(a - b).max())
+    assert err <= rel * scale, f"{what}: max diff {err:.3e} > {rel} x {scale:.3e}"
+
+
+def test_training_pair_matches_the_one_call_backward():
+    """mmdit_double_block_fwd_train gives the forward's outputs bit for bit, and
+    mmdit_double_block_bwd_saved the one-call backward's gradients (the same kernels on the same
+    values; only dQ's atomic accumulation order may move the last bits of the attention-side
+    gradients).  Likewise for the single block."""
+    B, S_i, S_t, D, H, F = 2, 256, 45, 256, 2, 1024
+    case = BlockCase(B, S_i, S_t, D, H, F, "bf16", seed=77, std=0.05, lat_hw=(16, 16))
+    rng = np.random.default_rng(78)
+    dy_i, dy_t = dev(_dy(case, rng, case.x_img.shape)), dev(_dy(case, rng, case.x_txt.shape))
+    cos, sin = _rope(case)
+    wi, wt = upload_weights(case.w_img, "bf16"), upload_weights(case.w_txt, "bf16")
+    xi, xt, vec = dev(case.x_img), dev(case.x_txt), dev(case.vec)
+    # reference: the forward, then the one-call backward
+    yi, yt = torch.empty_like(xi), torch.empty_like(xt)
+    L.mmdit_double_block_fwd(case.dims, wi, wt, vec, cos, sin, xi, xt, yi, yt)
+    ref_dx = torch.empty_like(xi), torch.empty_like(xt)
+    ref_dvec = torch.empty(B, D, device="cuda")
+    ref_g = _grads_like(case.w_img), _grads_like(case.w_txt)
+    L.mmdit_double_block_bwd(case.dims, wi, wt, vec, cos, sin, xi, xt, dy_i, dy_t, ref_dx[0], ref_dx[1], ref_dvec,
+                             ref_g[0], ref_g[1])
+    # the training pair
+    ti, tt = torch.full_like(xi, float("nan")), torch.full_like(xt, float("nan"))
+    saved = L.mmdit_double_block_fwd_train(case.dims, wi, wt, vec, cos, sin, xi, xt, ti, tt)
+    dx = torch.empty_like(xi), torch.empty_like(xt)
+    dvec = torch.empty(B, D, device="cuda")
+    g = _grads_like(case.w_img), _grads_like(case.w_txt)
+    L.mmdit_double_block_bwd_saved(case.dims, wi, wt, vec, cos, sin, xi, xt, dy_i, dy_t, dx[0], dx[1], saved, dvec,
+                                   g[0], g[1])
+    torch.cuda.synchronize()
+    assert L.mmdit_workspace_status(saved) == 0
+    assert torch.equal(ti, yi) and torch.equal(tt, yt)
+    for s in range(2):
+        # the MLP branch and the output projection come before the attention backward: bit-equal
+        for n in ("w_1", "b_1", "w_2", "b_2", "w_o", "b_o"):
+            assert torch.equal(g[s][n], ref_g[s][n]), n
+        for n in NAMES:
+            _close(g[s][n], ref_g[s][n], f"stream {s} {n}")
+        _close(dx[s].float(), ref_dx[s].float(), f"dx stream {s}", rel=1e-2)  # a bf16 rounding may flip
+    _close(dvec, ref_dvec, "dvec")
+    # single block
+    sc = BlockCase(1, 64, 16, 256, 2, 1024, "bf16", seed=79, std=0.05, lat_hw=(8, 8), single=True)
+    x = dev(sc.x_joint())
+    dy = dev(_dy(sc, rng, sc.x_joint().shape))
+    cos1, sin1 = _rope(sc)
+    w = upload_weights(sc.w_img, "bf16")
+    y = torch.empty_like(x)
+    L.mmdit_single_block_fwd(sc.dims, w, dev(sc.vec), cos1, sin1, x, y)
+    rdx, rg = torch.empty_like(x), _grads_like(sc.w_img)
+    L.mmdit_single_block_bwd(sc.dims, w, dev(sc.vec), cos1, sin1, x, dy, rdx, None, rg)
+    ty = torch.full_like(x, float("nan"))
+    saved1 = L.mmdit_single_block_fwd_train(sc.dims, w, dev(sc.vec), cos1, sin1, x, ty)
+    tdx, tg = torch.empty_like(x), _grads_like(sc.w_img)
+    L.mmdit_single_block_bwd_saved(sc.dims, w, dev(sc.vec), cos1, sin1, x, dy, tdx, saved1, None, tg)
+    torch.cuda.synchronize()
+    assert L.mmdit_workspace_status(saved1) == 0
+    assert torch.equal(ty, y)
+    for n in NAMES:
+        _close(tg[n], rg[n], f"single {n}")
