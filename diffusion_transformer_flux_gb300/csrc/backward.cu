@@ -98,11 +98,17 @@ __global__ void __launch_bounds__(kRowThreads) ln_modulate_bwd_kernel(LnBwdJob j
       if (k < dim) ox[c].load(xr + k), og[c].load(gr + k);
     }
   };
-  if (r0 < r1) load_row(r0, rx, rg);
+  // (rows of more than four chunks per thread load in place: a second set of registers would spill)
+  constexpr bool kPrefetch = NCT <= 4;
+  if (kPrefetch && r0 < r1) load_row(r0, rx, rg);
   for (int r = r0; r < r1; ++r) {
-    Raw8<TX> nx[NCT];
-    Raw8<TG> ng[NCT];
-    if (r + 1 < r1) load_row(r + 1, nx, ng);
+    Raw8<TX> nx[kPrefetch ? NCT : 1];
+    Raw8<TG> ng[kPrefetch ? NCT : 1];
+    if constexpr (kPrefetch) {
+      if (r + 1 < r1) load_row(r + 1, nx, ng);
+    } else {
+      load_row(r, rx, rg);
+    }
     // mean and variance of x, two passes over the registers as the forward does
     float s = 0.f, unused = 0.f;
 #pragma unroll
@@ -164,8 +170,10 @@ __global__ void __launch_bounds__(kRowThreads) ln_modulate_bwd_kernel(LnBwdJob j
         store8(dxr + k, acc);
       }
     }
+    if constexpr (kPrefetch) {
 #pragma unroll
-    for (int c = 0; c < NCT; ++c) rx[c] = nx[c], rg[c] = ng[c];
+      for (int c = 0; c < NCT; ++c) rx[c] = nx[c], rg[c] = ng[c];
+    }
   }
   float* p = job.part + static_cast<size_t>(blockIdx.x) * 2 * dim;
 #pragma unroll

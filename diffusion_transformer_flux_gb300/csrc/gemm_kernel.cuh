@@ -23,7 +23,8 @@ constexpr int kBM = 128;
 // image embedding), one for the others.
 template <int EPI>
 struct EpiGroups {
-  static constexpr int value = (EPI == kEpiGelu || EPI == kEpiGeluF8 || EPI == kEpiBias || EPI == kEpiDGelu) ? 2 : 1;
+  static constexpr int value =
+      (EPI == kEpiGelu || EPI == kEpiGeluF8 || EPI == kEpiBias || EPI == kEpiDGelu || EPI == kEpiGateResid) ? 2 : 1;
 };
 template <int EPI>
 constexpr int gemm_threads() {
