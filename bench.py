@@ -864,6 +864,29 @@ def measure_block_train(st, L, torch, peak, reps=3):
                    "frac": round(flops / v / 1e6 / peak, 4)} for k, v in out.items()}}
 
 
+def measure_blockwise_linear(L, torch, device, M=4608, N=12288, K=3072, reps=5):
+    """The blockwise FP8 linear (mmdit_fp8_blockwise_linear_fwd: per-tile E4M3 casts of x and W in
+    the call, then the slice-scaled GEMM) at the fc1 shape: 2 M N K FLOPs per call, CUDA events
+    around `reps` calls after one warm-up."""
+    x = torch.randn(M, K, device=device).to(torch.bfloat16)
+    w = (torch.randn(N, K, device=device) * 0.02).to(torch.bfloat16)
+    b = torch.zeros(N, device=device, dtype=torch.bfloat16)
+    y = torch.empty(M, N, device=device, dtype=torch.bfloat16)
+    ws = L.mmdit_fp8_blockwise_linear_fwd(x, w, b, y)
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        L.mmdit_fp8_blockwise_linear_fwd(x, w, b, y, ws=ws)
+    e.record()
+    torch.cuda.synchronize()
+    if L.mmdit_workspace_status(ws) != 0:
+        raise RuntimeError("a kernel gave up a bounded wait in the blockwise FP8 linear")
+    us = a.elapsed_time(e) * 1e3 / reps
+    return {"op": "blockwise FP8 linear (casts of x and W included)", "M": M, "N": N, "K": K,
+            "avg_us": round(us, 2), "achieved_tflops": round(2.0 * M * N * K / us / 1e6, 1)}
+
+
 def measure_linear_bwd(L, torch, device, peak, M=4608, N=12288, K=3072, reps=5):
     """The backward of the block's fc1-shaped linear (mmdit_linear_bwd: dx and dW through the
     tensor-core GEMM reading W, dy and x MN-major as stored, db): 4 M N K FLOPs per call, CUDA
@@ -1113,6 +1136,7 @@ def main():
         extras["hbm_sweeps"] = measure_hbm_sweeps(L, torch, device, hbm_peak)
         extras["single_block_parallel"] = measure_parallel_block(st, L, torch, bf16_peak)
         extras["linear_backward"] = measure_linear_bwd(L, torch, device, bf16_peak)
+        extras["blockwise_fp8_linear"] = measure_blockwise_linear(L, torch, device)
         extras["double_block_backward"] = measure_block_bwd(st, L, torch, bf16_peak)
         extras["double_block_training"] = measure_block_train(st, L, torch, bf16_peak)
     if fp8:

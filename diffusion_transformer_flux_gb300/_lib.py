@@ -35,6 +35,7 @@ EXPORTED = [
     "mmdit_double_block_fwd", "mmdit_single_block_workspace_size", "mmdit_single_block_fwd",
     "mmdit_block_workspace_offsets", "mmdit_fp8_quantize_e4m3", "mmdit_fp8_linear_workspace_size",
     "mmdit_fp8_linear_fwd", "mmdit_fp8_linear_bwd_workspace_size", "mmdit_fp8_linear_bwd",
+    "mmdit_fp8_blockwise_linear_workspace_size", "mmdit_fp8_blockwise_linear_fwd",
     "mmdit_single_block_parallel_fwd", "mmdit_linear_bwd_workspace_size",
     "mmdit_linear_bwd", "mmdit_double_block_bwd_workspace_size", "mmdit_double_block_bwd",
     "mmdit_single_block_bwd_workspace_size", "mmdit_single_block_bwd", "mmdit_double_block_fwd_train",
@@ -174,6 +175,8 @@ _SIGS = {
                                          VP, SZ, VP]),
     "mmdit_single_block_bwd_workspace_size": (SZ, [PDIMS]),
     "mmdit_single_block_bwd": (C.c_int, [PDIMS, PW, VP, VP, VP, VP, VP, VP, VP, PGRADS, VP, SZ, VP]),
+    "mmdit_fp8_blockwise_linear_workspace_size": (SZ, [I32, I32, I32]),
+    "mmdit_fp8_blockwise_linear_fwd": (C.c_int, [I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_double_block_fwd_train": (C.c_int, [PDIMS, PW, PW, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_double_block_bwd_saved": (C.c_int, [PDIMS, PW, PW, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, PGRADS, PGRADS,
                                                VP, SZ, VP]),
@@ -645,6 +648,22 @@ def mmdit_single_block_bwd(dims: Dims, w: dict, vec, cos, sin, x, dy, dx, dvec=N
                                          _ptr(dy), _ptr(dx), _ptr(dvec), C.byref(gg) if gg else None, _ptr(ws),
                                          ws.numel(), _stream(stream)))
     return ws
+
+
+def mmdit_fp8_blockwise_linear_fwd(x, w, b, y, ws=None, stream=None):
+    """y = x W^T + b under the blockwise FP8 recipe (see include/mmdit.h); x [M, K], w [N, K], y [M, N]
+    bf16.  Returns the workspace, whose layout the header states (codes and scales after the call)."""
+    M, K = x.shape[-2], x.shape[-1]
+    N = w.shape[0]
+    if ws is None:
+        ws = workspace(mmdit_fp8_blockwise_linear_workspace_size(M, N, K), x.device)
+    _check(load().mmdit_fp8_blockwise_linear_fwd(M, N, K, _ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(ws), ws.numel(),
+                                                 _stream(stream)))
+    return ws
+
+
+def mmdit_fp8_blockwise_linear_workspace_size(M, N, K) -> int:
+    return load().mmdit_fp8_blockwise_linear_workspace_size(M, N, K)
 
 
 def mmdit_double_block_fwd_train(dims: Dims, w_img: dict, w_txt: dict, vec, cos, sin, x_img, x_txt, y_img, y_txt,

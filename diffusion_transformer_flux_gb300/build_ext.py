@@ -22,8 +22,8 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]
-SOURCES = ["gemm_bf16.cu", "gemm_tf32.cu", "gemm_fp8.cu", "fp8.cu", "attention.cu", "attention_bwd.cu", "attention_fp8.cu",
-           "elementwise.cu", "backward.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["gemm_bf16.cu", "gemm_tf32.cu", "gemm_fp8.cu", "gemm_blockwise.cu", "fp8.cu", "attention.cu",
+           "attention_bwd.cu", "attention_fp8.cu", "elementwise.cu", "backward.cu", "api.cu", "noalloc.cu"]
 
 
 def _nvcc() -> str:

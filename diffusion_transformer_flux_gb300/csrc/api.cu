@@ -1798,6 +1798,35 @@ mmdit_status mmdit_fp8_linear_fwd(int32_t M, int32_t N, int32_t K, const void* x
   return MMDIT_OK;
 }
 
+size_t mmdit_fp8_blockwise_linear_workspace_size(int32_t M, int32_t N, int32_t K) {
+  if (M < 0 || N < 1 || K < 1) return kStatusBytes;
+  return kStatusBytes + blockwise_linear_scratch(M, N, K);
+}
+
+mmdit_status mmdit_fp8_blockwise_linear_fwd(int32_t M, int32_t N, int32_t K, const void* x, const void* w,
+                                            const void* b, void* y, void* workspace, size_t workspace_bytes,
+                                            void* stream) {
+  if (M < 0 || N < 1 || K < 1) return fail(MMDIT_ERR_INVALID_ARG, "bad blockwise FP8 linear shape");
+  if (N % 128 != 0 || K % 128 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "blockwise FP8 linear needs N %% 128 == 0 and K %% 128 == 0 (got %d, %d)", N, K);
+  if (M > 65535 * 128) return fail(MMDIT_ERR_UNSUPPORTED, "blockwise FP8 linear: M must be <= %d", 65535 * 128);
+  mmdit_status s = check_ptrs({x, w, y}, "blockwise FP8 linear");
+  if (s != MMDIT_OK) return s;
+  if (b && !aligned16(b)) return fail(MMDIT_ERR_INVALID_ARG, "blockwise FP8 linear: bias is not 16-byte aligned");
+  if ((s = check_workspace(workspace, workspace_bytes, mmdit_fp8_blockwise_linear_workspace_size(M, N, K))) != MMDIT_OK)
+    return s;
+  if (M == 0) return MMDIT_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
+  ProfScope ps_("fp8_blockwise_linear", st);
+  MMDIT_CUDA(launch_blockwise_linear(M, N, K, static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w),
+                                     static_cast<const __nv_bfloat16*>(b), static_cast<__nv_bfloat16*>(y),
+                                     at(workspace, kStatusBytes), status_word(workspace), st),
+             "blockwise FP8 linear");
+  return MMDIT_OK;
+}
+
 mmdit_status mmdit_single_block_parallel_fwd(const mmdit_dims* d, const mmdit_stream_w* w, const void* vec,
                                              const float* rope_cos, const float* rope_sin, const void* x,
                                              void* y, void* workspace, size_t workspace_bytes, void* stream) {

@@ -174,6 +174,14 @@ cudaError_t launch_attention_fp8(const AttnFp8Problem& p, uint32_t* status, cuda
 // pre-pass's D = rowsum(dO * O): dV = P^T dO, dS = P (dO V^T - D) / sqrt(d), dK = dS^T Q, dQ = dS K,
 // P = exp2(q . k log2(e) / sqrt(d) - L).  dO (and so D and every output) carries the pre-pass's
 // power-of-two gradient scale.
+// gemm_blockwise.cu: the blockwise FP8 linear y = x W^T + b (bf16 x, W, b, y): per-tile E4M3 casts
+// of x (1 x 128 tiles) and W (128 x 128 tiles) into `scratch` (blockwise_linear_scratch bytes),
+// then the GEMM that scales each 128-wide K slice's product.  N % 128 == 0, K % 128 == 0.
+size_t blockwise_linear_scratch(int M, int N, int K);
+cudaError_t launch_blockwise_linear(int M, int N, int K, const __nv_bfloat16* x, const __nv_bfloat16* w,
+                                    const __nv_bfloat16* bias, __nv_bfloat16* y, void* scratch, uint32_t* status,
+                                    cudaStream_t stream);
+
 struct AttnBwdProblem {
   int batch = 0, heads = 0, seq = 0, seq_pad = 0;
   const __half *q = nullptr, *k = nullptr, *v = nullptr, *dout = nullptr;  // [B, H, S, 128] fp16

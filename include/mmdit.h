@@ -420,6 +420,23 @@ mmdit_status mmdit_fp8_linear_fwd(int32_t M, int32_t N, int32_t K, const void *x
                                   const float *scale_x, const float *scale_w, const void *b,
                                   void *y, void *workspace, size_t workspace_bytes, void *stream);
 
+/* Blockwise FP8 linear ([FP8] §Configuration › FP8 model configuration, fp8_recipe "blockwise";
+ * the page names the recipe only).  y = x W^T + b with every tile cast to E4M3 under its own
+ * current scale s = 448 / amax(tile) (1 for a tile of zeros): x [M, K] in 1 x 128 tiles (one scale
+ * per row and 128-wide K slice), W [N, K] in 128 x 128 tiles; the product sums, over the 128-wide
+ * K slices j, Q_j(x) Q_j(W)^T / (s_x[m, j] s_w[n / 128, j]) in fp32 (tensor cores on the E4M3
+ * codes, each slice rescaled as it is accumulated), then adds b.
+ * x, W, b (NULL: none) and y are bf16, 16-byte aligned; N % 128 == 0, K % 128 == 0; M == 0 is a
+ * no-op.  The casts are float32: s = 448 / amax is the IEEE quotient, each element's product x s
+ * is rounded to float32 and then to E4M3 (nearest even, saturating).  The workspace (at least
+ * mmdit_fp8_blockwise_linear_workspace_size bytes) holds after its 256-byte status word, each
+ * part starting on a 256-byte boundary: the x codes [M, K], the W codes [N, K], s_x [K/128, M]
+ * and s_w [N/128, K/128] (fp32), readable after the call. */
+size_t mmdit_fp8_blockwise_linear_workspace_size(int32_t M, int32_t N, int32_t K);
+mmdit_status mmdit_fp8_blockwise_linear_fwd(int32_t M, int32_t N, int32_t K, const void *x, const void *w,
+                                            const void *b, void *y, void *workspace, size_t workspace_bytes,
+                                            void *stream);
+
 /* ---------------------------------------------------------------------------------------
  * Backward of the FP8 linear ([FP8] §Configuration, FP8 model configuration: fp8 "e4m3" or
  * "hybrid", fp8_wgrad; the chain rule of mmdit_fp8_linear_fwd), for a forward that ran on

@@ -299,6 +299,20 @@ def test_block_backward_rejects_bad_arguments_before_any_cuda_call(lib):
     assert sb(C.byref(d), C.byref(w), 16, 16, 16, 16, 16, 16, None, None, 256, 16, None) == 3
 
 
+def test_blockwise_fp8_linear_rejects_bad_arguments_before_any_cuda_call(lib):
+    need = L.mmdit_fp8_blockwise_linear_workspace_size(300, 256, 512)
+    # status word, codes of x and W, both scale arrays, each on a 256-byte boundary
+    assert need == 256 + 153600 + 131072 + 4864 + 256
+    f = lib.mmdit_fp8_blockwise_linear_fwd
+    assert f(300, 200, 512, 16, 16, None, 16, 256, 1 << 30, None) == 2      # N % 128
+    assert f(300, 256, 500, 16, 16, None, 16, 256, 1 << 30, None) == 2      # K % 128
+    assert f(-1, 256, 512, 16, 16, None, 16, 256, 1 << 30, None) == 1
+    assert f(300, 256, 512, None, 16, None, 16, 256, 1 << 30, None) == 1
+    assert "blockwise FP8 linear" in L.last_error()
+    assert f(300, 256, 512, 16, 16, 0x1008, 16, 256, 1 << 30, None) == 1   # bias alignment
+    assert f(300, 256, 512, 16, 16, None, 16, 256, need - 1, None) == 3
+
+
 def test_training_pair_rejects_bad_arguments_before_any_cuda_call(lib):
     # the split backward: same checks as the one-call backward; the forward half needs the
     # outputs y, the backward half dy and dx, both a backward-sized `saved` buffer

@@ -546,3 +546,84 @@ def test_fp8_attention_matches_oracle(B, H, S):
     else:
         assert m_gpu8 <= m_864, (m_gpu8, m_864)
         assert n_gpu8 <= n_864, (n_gpu8, n_864)
+
+
+# ----------------------------------------------------------------------------- blockwise recipe
+def _ru256(n):
+    return (n + 255) // 256 * 256
+
+
+def _blockwise_parts(ws, M, N, K):
+    """The codes and scales the call leaves in its workspace (layout stated in include/mmdit.h)."""
+    raw = ws.cpu().numpy().view(np.uint8)
+    off = 256
+    xq = raw[off:off + M * K].reshape(M, K)
+    off += _ru256(M * K)
+    wq = raw[off:off + N * K].reshape(N, K)
+    off += _ru256(N * K)
+    sx = raw[off:off + (K // 128) * M * 4].view(np.float32).reshape(K // 128, M)
+    off += _ru256((K // 128) * M * 4)
+    sw = raw[off:off + (N // 128) * (K // 128) * 4].view(np.float32).reshape(N // 128, K // 128)
+    return xq, wq, sx, sw
+
+
+def _f32_tile_cast(t):
+    """The stated float32 cast of one tile: s = 448 / amax (IEEE float32), codes of (x s) rounded to
+    float32 first, then to E4M3 (the oracle's encoder: nearest even, saturating)."""
+    t = np.asarray(t, np.float32)
+    amax = np.float32(np.abs(t).max())
+    s = np.float32(448.0) / amax if amax > 0 else np.float32(1.0)
+    return E.e4m3_encode((t * s).astype(np.float64)), s
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 256, 512), (1024, 3072, 3072)])
+def test_blockwise_fp8_linear(M, N, K):
+    """[FP8] §Configuration, fp8_recipe "blockwise" (oracle.fp8_recipes.blockwise_linear): the casts
+    are bit-exact against a float32 emulation of the stated arithmetic (codes and scales, with an
+    outlier, a tile of zeros and a ragged last row tile); the GEMM, fed the GPU's codes and scales,
+    agrees with their float64 product to fp32 accumulation and the bf16 output rounding; and the
+    whole linear sits far closer to the oracle's float64 recipe than that recipe sits to the exact
+    product (max norm, so a mistake in one tile's scale fails)."""
+    from oracle import fp8_recipes as R
+    rng = np.random.default_rng(M + N)
+    x = synth.bf16_round(rng.standard_normal((M, K)).astype(np.float32))
+    x[7, 200] = 300.0                            # an outlier owns its 1 x 128 tile's scale
+    w = synth.bf16_round((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    w[128:256, K - 128:] = 0.0                   # a tile of zeros: scale 1, codes 0
+    b = synth.bf16_round((rng.standard_normal(N) * 0.1).astype(np.float32))
+    y = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+    ws = L.mmdit_fp8_blockwise_linear_fwd(dev(x), dev(w), dev(b), y)
+    torch.cuda.synchronize()
+    assert L.mmdit_workspace_status(ws) == 0
+    xq, wq, sx, sw = _blockwise_parts(ws, M, N, K)
+    # casts, bit-exact
+    for m in range(0, M, max(1, M // 64)):
+        for j in range(K // 128):
+            codes, s = _f32_tile_cast(x[m, 128 * j:128 * (j + 1)])
+            assert sx[j, m] == s, (m, j)
+            assert np.array_equal(xq[m, 128 * j:128 * (j + 1)], codes), (m, j)
+    for i in range(N // 128):
+        for j in range(K // 128):
+            codes, s = _f32_tile_cast(w[128 * i:128 * (i + 1), 128 * j:128 * (j + 1)])
+            assert sw[i, j] == s, (i, j)
+            assert np.array_equal(wq[128 * i:128 * (i + 1), 128 * j:128 * (j + 1)], codes), (i, j)
+    assert sw[1, K // 128 - 1] == 1.0 and not wq[128:256, K - 128:].any()
+    # the GEMM from the GPU's own codes and scales, in float64
+    dec = np.array([E.e4m3_decode(c) for c in range(256)])
+    ref = np.zeros((M, N))
+    tile_row = np.arange(N) // 128
+    for j in range(K // 128):
+        sl = slice(128 * j, 128 * (j + 1))
+        ref += (dec[xq[:, sl]] @ dec[wq[:, sl]].T) / (sx[j][:, None].astype(np.float64) *
+                                                      sw[tile_row, j][None, :].astype(np.float64))
+    ref += b
+    got = host(y)
+    assert_parity(got, ref, 1e-3, f"blockwise GEMM {M}x{N}x{K}", out_bf16=True)
+    # the whole linear against the oracle's recipe and the exact product
+    y_or = R.blockwise_linear(x, w, b)
+    y_ex = x.astype(np.float64) @ w.astype(np.float64).T + b
+    rms = float(np.sqrt(np.mean(y_ex ** 2)))
+    d_gpu = float(np.abs(got - y_or).max()) / rms
+    d_fp8 = float(np.abs(y_or - y_ex).max()) / rms
+    print(f"[fp8 blockwise] {M}x{N}x{K}: max|GPU - recipe|/RMS {d_gpu:.3e}, max|recipe - exact|/RMS {d_fp8:.3e}")
+    assert d_gpu <= 0.25 * d_fp8
