@@ -80,6 +80,7 @@ AMAX_MAX = 1
 MMDIT_GEMM_NATIVE = 0
 MMDIT_GEMM_FP8_E4M3 = 1
 MMDIT_GEMM_FP8_TENSORWISE = 2
+MMDIT_GEMM_FP8_BLOCKWISE = 3
 FP8_LINEARS = ("qkv", "o", "fc1", "fc2")
 
 

@@ -201,11 +201,13 @@ struct BlockPlan {
   int mod_chunks = 6;     // modulation chunks per stream: 6, or 3 (shift, scale, gate) when parallel
   bool fp8;  // E4M3 linears: h, u hold E4M3 codes; o8 and wq hold the cast attention output
              // and weights
-  bool fp8_current = false;  // tensorwise (current) scaling: inputs staged in bf16 before their cast
+  bool fp8_current = false;  // tensorwise or blockwise (current) scaling: inputs staged in bf16 before their cast
+  bool fp8_blockwise = false;  // blockwise: per-tile scales (bw_sx, bw_sw), the blockwise GEMM
   int B, Si, St, S, S_pad, D, H, F;
   size_t elt;
   size_t mod[2], h[2], q, k, vt, o[2], x1[2], u[2];
   size_t o8[2], wq[2], stage[2];
+  size_t bw_sx[2], bw_sw[2];  // blockwise: the current input's s_x [K/128, rows]; the weights' s_w
   size_t total;
   // byte offsets of the four weights inside a stream's wq slot
   size_t wq_qkv() const { return 0; }
@@ -213,6 +215,12 @@ struct BlockPlan {
   size_t wq_1() const { return static_cast<size_t>(4) * D * D; }
   size_t wq_2() const { return static_cast<size_t>(4) * D * D + static_cast<size_t>(F) * D; }
   size_t wq_bytes() const { return static_cast<size_t>(4) * D * D + static_cast<size_t>(2) * F * D; }
+  // byte offsets of the four weights' s_w [N/128, K/128] inside a stream's bw_sw slot
+  size_t sw_qkv() const { return 0; }
+  size_t sw_o() const { return static_cast<size_t>(3 * D / 128) * (D / 128) * 4; }
+  size_t sw_1() const { return sw_o() + static_cast<size_t>(D / 128) * (D / 128) * 4; }
+  size_t sw_2() const { return sw_1() + static_cast<size_t>(F / 128) * (D / 128) * 4; }
+  size_t sw_bytes() const { return sw_2() + static_cast<size_t>(D / 128) * (F / 128) * 4; }
 };
 
 static bool plan_block(const mmdit_dims* d, bool single, BlockPlan* p) {
@@ -223,8 +231,10 @@ static bool plan_block(const mmdit_dims* d, bool single, BlockPlan* p) {
   p->S_pad = static_cast<int>(round_up(static_cast<size_t>(p->S), 8));
   p->D = d->hidden, p->H = d->heads, p->F = d->mlp_hidden;
   p->elt = elt_bytes(d->act);
-  p->fp8 = d->gemm == MMDIT_GEMM_FP8_E4M3 || d->gemm == MMDIT_GEMM_FP8_TENSORWISE;
-  p->fp8_current = d->gemm == MMDIT_GEMM_FP8_TENSORWISE;
+  p->fp8 = d->gemm == MMDIT_GEMM_FP8_E4M3 || d->gemm == MMDIT_GEMM_FP8_TENSORWISE ||
+           d->gemm == MMDIT_GEMM_FP8_BLOCKWISE;
+  p->fp8_blockwise = d->gemm == MMDIT_GEMM_FP8_BLOCKWISE;
+  p->fp8_current = d->gemm == MMDIT_GEMM_FP8_TENSORWISE || p->fp8_blockwise;
   const size_t mm_elt = p->fp8 ? 1 : p->elt;  // inputs of the QKV and fc1/fc2 linears
   Carver c;
   const size_t B = p->B, D = p->D, F = p->F, S = p->S;
@@ -245,6 +255,10 @@ static bool plan_block(const mmdit_dims* d, bool single, BlockPlan* p) {
   // tensorwise: a linear's bf16 input (LayerNorm-modulate output or GELU output) before its cast
   for (int s = 0; s < 2; ++s)
     p->stage[s] = p->fp8_current && s < ns ? c.take(rows[s] * (F > D ? F : D) * 2) : 0;
+  for (int s = 0; s < 2; ++s) {
+    p->bw_sx[s] = p->fp8_blockwise && s < ns ? c.take(rows[s] * ((F > D ? F : D) / 128) * 4) : 0;
+    p->bw_sw[s] = p->fp8_blockwise && s < ns ? c.take(p->sw_bytes()) : 0;
+  }
   p->total = c.off;
   return true;
 }
@@ -256,7 +270,8 @@ static mmdit_status check_dims(const mmdit_dims* d) {
                 d->seq_img, d->seq_txt);
   if (d->act != MMDIT_F32 && d->act != MMDIT_BF16)
     return fail(MMDIT_ERR_INVALID_ARG, "act must be MMDIT_F32 or MMDIT_BF16 (got %d)", d->act);
-  if (d->gemm != MMDIT_GEMM_NATIVE && d->gemm != MMDIT_GEMM_FP8_E4M3 && d->gemm != MMDIT_GEMM_FP8_TENSORWISE)
+  if (d->gemm != MMDIT_GEMM_NATIVE && d->gemm != MMDIT_GEMM_FP8_E4M3 && d->gemm != MMDIT_GEMM_FP8_TENSORWISE &&
+      d->gemm != MMDIT_GEMM_FP8_BLOCKWISE)
     return fail(MMDIT_ERR_INVALID_ARG, "unknown gemm mode %d", d->gemm);
   if (d->gemm != MMDIT_GEMM_NATIVE && d->act != MMDIT_BF16)
     return fail(MMDIT_ERR_UNSUPPORTED, "FP8 E4M3 linears need bf16 activations (act = MMDIT_BF16)");
@@ -315,6 +330,11 @@ inline int fp8_tensor(int slot, int g, int operand) { return kFp8TensorsPerStrea
 static mmdit_status check_fp8(const mmdit_dims* d, const mmdit_fp8_state* f, int n_needed) {
   if (d->gemm == MMDIT_GEMM_NATIVE) {
     if (f) return fail(MMDIT_ERR_INVALID_ARG, "fp8 state given but the gemm mode is native");
+    return MMDIT_OK;
+  }
+  if (d->gemm == MMDIT_GEMM_FP8_BLOCKWISE) {
+    // every scale is the call's own per-tile scale: there is no state to read or record
+    if (f) return fail(MMDIT_ERR_INVALID_ARG, "fp8 state given but the blockwise recipe keeps none");
     return MMDIT_OK;
   }
   if (!f) return fail(MMDIT_ERR_INVALID_ARG, "FP8 linears need an fp8 state (got NULL)");
@@ -393,8 +413,10 @@ struct Streams {
 // tensor's scale is read and where this call records its amax.
 struct Fp8 {
   const mmdit_fp8_state* f = nullptr;
-  bool current = false;  // tensorwise: every scale from the tensor's own amax in this call
+  bool current = false;  // tensorwise or blockwise: every scale from the tensor's own amax in this call
+  bool blockwise = false;  // per-tile scales in the plan's bw_sx / bw_sw slots; no state (f == nullptr)
   int n_tensors = 0;     // tensors this block records (16 double, 8 single)
+  bool on() const { return f != nullptr || blockwise; }  // the linears run on E4M3 codes
   const float* scale(int t) const { return f->scale + t; }
   float* amax(int t) const { return f->amax_history + static_cast<size_t>(t) * f->hist_len + f->pos; }
 };
@@ -431,16 +453,22 @@ mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss,
       void* out = f8.current ? at(ws, p.stage[ss.s[i]]) : at(ws, p.h[ss.s[i]]);
       jobs[i] = {ss.x[i], mod, mod + p.D, static_cast<int64_t>(p.mod_chunks) * p.D, out,
                  p.B * ss.rpb[i], ss.rpb[i]};
-      if (f8.f && !f8.current) {
+      if (f8.on() && !f8.current) {
         const int t = fp8_tensor(ss.s[i], 0, 0);
         jobs[i].q_scale = f8.scale(t), jobs[i].q_amax = f8.amax(t);
       }
     }
     MMDIT_CUDA(launch_ln_modulate2(d->act, d->act == MMDIT_F32, jobs, ss.n, p.D, d->ln_eps, st,
-                                   f8.f && !f8.current ? 1 : 0),
+                                   f8.on() && !f8.current ? 1 : 0),
                "LayerNorm-modulate (attention branch)");
   }
-  if (f8.current) {
+  if (f8.blockwise) {
+    ProfScope ps_(p.single ? "single.fp8_cast_h1" : "double.fp8_cast_h1", st);
+    for (int i = 0; i < ss.n; ++i)
+      MMDIT_CUDA(launch_blockwise_cast_act(at<__nv_bfloat16>(ws, p.stage[ss.s[i]]), p.B * ss.rpb[i], p.D,
+                                           at<uint8_t>(ws, p.h[ss.s[i]]), at<float>(ws, p.bw_sx[ss.s[i]]), st),
+                 "blockwise E4M3 cast of the QKV input");
+  } else if (f8.current) {
     ProfScope ps_(p.single ? "single.fp8_cast_h1" : "double.fp8_cast_h1", st);
     QuantJob q[2];
     for (int i = 0; i < ss.n; ++i) {
@@ -452,12 +480,15 @@ mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss,
     if (s != MMDIT_OK) return s;
   }
   GemmProblem g;
-  g.act = f8.f ? 2 : d->act, g.epi = kEpiQkv, g.N = 3 * p.D, g.K = p.D;
+  g.act = f8.on() ? 2 : d->act, g.epi = kEpiQkv, g.N = 3 * p.D, g.K = p.D;
   for (int i = 0; i < ss.n; ++i) {
     const mmdit_stream_w* w = ss.w[i];
     EpiArgs e;
     const void* wmat = w->w_qkv;
-    if (f8.f) {
+    if (f8.blockwise) {
+      e.bw_sx = at<float>(ws, p.bw_sx[ss.s[i]]), e.bw_sw = at<float>(ws, p.bw_sw[ss.s[i]] + p.sw_qkv());
+      wmat = at(ws, p.wq[ss.s[i]] + p.wq_qkv());
+    } else if (f8.f) {
       e.scale_a = f8.scale(fp8_tensor(ss.s[i], 0, 0)), e.scale_w = f8.scale(fp8_tensor(ss.s[i], 0, 1));
       wmat = at(ws, p.wq[ss.s[i]] + p.wq_qkv());
     }
@@ -480,18 +511,37 @@ mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss,
 mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss, const Fp8& f8,
                       void* ws, cudaStream_t st) {
   // the linears' operand type, and each stream's weight matrices as the GEMMs read them
-  const int mm = f8.f ? 2 : d->act;
+  const int mm = f8.on() ? 2 : d->act;
   auto weight = [&](int i, int g) -> const void* {
     const mmdit_stream_w* w = ss.w[i];
-    if (!f8.f) return g == 1 ? w->w_o : (g == 2 ? w->w_1 : w->w_2);
+    if (!f8.on()) return g == 1 ? w->w_o : (g == 2 ? w->w_1 : w->w_2);
     const size_t off = g == 1 ? p.wq_o() : (g == 2 ? p.wq_1() : p.wq_2());
     return at(ws, p.wq[ss.s[i]] + off);
   };
   auto dequant = [&](EpiArgs& e, int i, int g) {
+    if (f8.blockwise) {
+      const size_t off = g == 1 ? p.sw_o() : (g == 2 ? p.sw_1() : p.sw_2());
+      e.bw_sx = at<float>(ws, p.bw_sx[ss.s[i]]), e.bw_sw = at<float>(ws, p.bw_sw[ss.s[i]] + off);
+      return;
+    }
     if (!f8.f) return;
     e.scale_a = f8.scale(fp8_tensor(ss.s[i], g, 0)), e.scale_w = f8.scale(fp8_tensor(ss.s[i], g, 1));
   };
-  if (f8.f) {
+  // blockwise: a bf16 input cast per 1 x 128 tile, its scales into the stream's bw_sx slot
+  auto cast_blockwise = [&](int i, const void* src, size_t dst, int K, const char* what) -> mmdit_status {
+    MMDIT_CUDA(launch_blockwise_cast_act(static_cast<const __nv_bfloat16*>(src), p.B * ss.rpb[i], K,
+                                         at<uint8_t>(ws, dst), at<float>(ws, p.bw_sx[ss.s[i]]), st),
+               what);
+    return MMDIT_OK;
+  };
+  if (f8.blockwise) {
+    ProfScope ps_(p.single ? "single.fp8_cast_o" : "double.fp8_cast_o", st);
+    for (int i = 0; i < ss.n; ++i) {
+      mmdit_status s = cast_blockwise(i, at(ws, p.o[ss.s[i]]), p.o8[ss.s[i]], p.D,
+                                      "blockwise E4M3 cast of the attention output");
+      if (s != MMDIT_OK) return s;
+    }
+  } else if (f8.f) {
     // the attention output (bf16) cast to E4M3 for the output projection
     ProfScope ps_(p.single ? "single.fp8_cast_o" : "double.fp8_cast_o", st);
     QuantJob jobs[2];
@@ -517,7 +567,7 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
     e.rows_per_batch = ss.rpb[i], e.out = at(ws, p.x1[ss.s[i]]), e.out_f32 = 1;
     e.pre = ss.pre_o[i];
     dequant(e, i, 1);
-    add_problem(g, i, p.B * ss.rpb[i], at(ws, f8.f ? p.o8[ss.s[i]] : p.o[ss.s[i]]), weight(i, 1), e);
+    add_problem(g, i, p.B * ss.rpb[i], at(ws, f8.on() ? p.o8[ss.s[i]] : p.o[ss.s[i]]), weight(i, 1), e);
   }
   {
     ProfScope ps_(p.single ? "single.out" : "double.out", st);
@@ -532,15 +582,21 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
       void* out = f8.current ? at(ws, p.stage[ss.s[i]]) : at(ws, p.h[ss.s[i]]);
       jobs[i] = {at(ws, p.x1[ss.s[i]]), mod + 3 * p.D, mod + 4 * p.D, 6 * p.D, out,
                  p.B * ss.rpb[i], ss.rpb[i]};
-      if (f8.f && !f8.current) {
+      if (f8.on() && !f8.current) {
         const int t = fp8_tensor(ss.s[i], 2, 0);
         jobs[i].q_scale = f8.scale(t), jobs[i].q_amax = f8.amax(t);
       }
     }
-    MMDIT_CUDA(launch_ln_modulate2(d->act, 1, jobs, ss.n, p.D, d->ln_eps, st, f8.f && !f8.current ? 1 : 0),
+    MMDIT_CUDA(launch_ln_modulate2(d->act, 1, jobs, ss.n, p.D, d->ln_eps, st, f8.on() && !f8.current ? 1 : 0),
                "LayerNorm-modulate (MLP branch)");
   }
-  if (f8.current && !p.parallel) {
+  if (f8.blockwise && !p.parallel) {
+    ProfScope ps_(p.single ? "single.fp8_cast_h2" : "double.fp8_cast_h2", st);
+    for (int i = 0; i < ss.n; ++i) {
+      mmdit_status s = cast_blockwise(i, at(ws, p.stage[ss.s[i]]), p.h[ss.s[i]], p.D, "blockwise E4M3 cast of the fc1 input");
+      if (s != MMDIT_OK) return s;
+    }
+  } else if (f8.current && !p.parallel) {
     ProfScope ps_(p.single ? "single.fp8_cast_h2" : "double.fp8_cast_h2", st);
     QuantJob q[2];
     for (int i = 0; i < ss.n; ++i) {
@@ -552,13 +608,13 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
     if (s != MMDIT_OK) return s;
   }
   GemmProblem f1;
-  f1.act = mm, f1.epi = f8.f && !f8.current ? kEpiGeluF8 : kEpiGelu, f1.N = p.F, f1.K = p.D;
+  f1.act = mm, f1.epi = f8.on() && !f8.current ? kEpiGeluF8 : kEpiGelu, f1.N = p.F, f1.K = p.D;
   for (int i = 0; i < ss.n; ++i) {
     EpiArgs e;
     e.bias = ss.w[i]->b_1, e.gelu_tanh = d->gelu_tanh, e.pre = ss.pre_1[i];
     e.out = f8.current ? at(ws, p.stage[ss.s[i]]) : at(ws, p.u[ss.s[i]]);
     dequant(e, i, 2);
-    if (f8.f && !f8.current) {
+    if (f8.on() && !f8.current) {
       const int t = fp8_tensor(ss.s[i], 3, 0);  // GELU output = the input of fc2
       e.out_scale = f8.scale(t), e.out_amax = f8.amax(t);
     }
@@ -568,7 +624,13 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
     ProfScope ps_(p.single ? "single.fc1" : "double.fc1", st);
     MMDIT_CUDA(launch_gemm(f1, status_word(ws), st), "MLP fc1 + GELU");
   }
-  if (f8.current) {
+  if (f8.blockwise) {
+    ProfScope ps_(p.single ? "single.fp8_cast_u" : "double.fp8_cast_u", st);
+    for (int i = 0; i < ss.n; ++i) {
+      mmdit_status s = cast_blockwise(i, at(ws, p.stage[ss.s[i]]), p.u[ss.s[i]], p.F, "blockwise E4M3 cast of the fc2 input");
+      if (s != MMDIT_OK) return s;
+    }
+  } else if (f8.current) {
     ProfScope ps_(p.single ? "single.fp8_cast_u" : "double.fp8_cast_u", st);
     QuantJob q[2];
     for (int i = 0; i < ss.n; ++i) {
@@ -603,6 +665,23 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
 mmdit_status fp8_begin(const BlockPlan& p, const Streams& ss, const Fp8& f8, int n_tensors,
                        void* ws, cudaStream_t st) {
   ProfScope ps_(p.single ? "single.fp8_cast_w" : "double.fp8_cast_w", st);
+  if (f8.blockwise) {
+    // every weight cast per 128 x 128 tile, its scales into the stream's bw_sw slot
+    for (int i = 0; i < ss.n; ++i) {
+      const mmdit_stream_w* w = ss.w[i];
+      const int slot = ss.s[i];
+      const void* src[4] = {w->w_qkv, w->w_o, w->w_1, w->w_2};
+      const size_t off[4] = {p.wq_qkv(), p.wq_o(), p.wq_1(), p.wq_2()};
+      const size_t soff[4] = {p.sw_qkv(), p.sw_o(), p.sw_1(), p.sw_2()};
+      const int nn[4] = {3 * p.D, p.D, p.F, p.D}, kk[4] = {p.D, p.D, p.D, p.F};
+      for (int g = 0; g < 4; ++g)
+        MMDIT_CUDA(launch_blockwise_cast_weight(static_cast<const __nv_bfloat16*>(src[g]), nn[g], kk[g],
+                                                at<uint8_t>(ws, p.wq[slot] + off[g]),
+                                                at<float>(ws, p.bw_sw[slot] + soff[g]), st),
+                   "blockwise E4M3 cast of the weights");
+    }
+    return MMDIT_OK;
+  }
   MMDIT_CUDA(launch_amax_reset(f8.f->amax_history, f8.f->hist_len, n_tensors, f8.f->pos, st),
              "FP8 amax slot reset");
   QuantJob jobs[kQuantMaxJobs];
@@ -627,6 +706,7 @@ mmdit_status fp8_begin(const BlockPlan& p, const Streams& ss, const Fp8& f8, int
 
 // FP8 calls: the next call's scales from the recorded amax (most_recent or the history's max).
 mmdit_status fp8_end(const BlockPlan& p, const Fp8& f8, int n_tensors, cudaStream_t st) {
+  if (f8.blockwise) return MMDIT_OK;  // no state: every scale is this call's own
   ProfScope ps_(p.single ? "single.fp8_scale" : "double.fp8_scale", st);
   MMDIT_CUDA(launch_scale_update(f8.f->amax_history, f8.f->scale, f8.f->hist_len, n_tensors, f8.f->pos,
                                  f8.f->margin, f8.current ? 0 : f8.f->amax_compute_algo, st),
@@ -684,12 +764,12 @@ mmdit_status double_block_body(const mmdit_dims* d, const BlockPlan& p, const mm
   Fp8 f8;
   f8.f = fp8;
   const int n_tensors = 2 * kFp8TensorsPerStream;
-  f8.current = p.fp8_current, f8.n_tensors = n_tensors;
-  if (fp8 && (s = fp8_begin(p, ss, f8, n_tensors, workspace, st)) != MMDIT_OK) return s;
+  f8.current = p.fp8_current, f8.blockwise = p.fp8_blockwise, f8.n_tensors = n_tensors;
+  if (f8.on() && (s = fp8_begin(p, ss, f8, n_tensors, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, f8, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_post(d, p, ss, f8, workspace, st)) != MMDIT_OK) return s;
-  return fp8 ? fp8_end(p, f8, n_tensors, st) : MMDIT_OK;
+  return f8.on() ? fp8_end(p, f8, n_tensors, st) : MMDIT_OK;
 }
 
 mmdit_status single_block_body(const mmdit_dims* d, const BlockPlan& p, const mmdit_stream_w* w,
@@ -708,12 +788,12 @@ mmdit_status single_block_body(const mmdit_dims* d, const BlockPlan& p, const mm
   ss.mod[0] = w->mod ? w->mod : at<float>(workspace, p.mod[0]);
   Fp8 f8;
   f8.f = fp8;
-  f8.current = p.fp8_current, f8.n_tensors = kFp8TensorsPerStream;
-  if (fp8 && (s = fp8_begin(p, ss, f8, kFp8TensorsPerStream, workspace, st)) != MMDIT_OK) return s;
+  f8.current = p.fp8_current, f8.blockwise = p.fp8_blockwise, f8.n_tensors = kFp8TensorsPerStream;
+  if (f8.on() && (s = fp8_begin(p, ss, f8, kFp8TensorsPerStream, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, f8, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_post(d, p, ss, f8, workspace, st)) != MMDIT_OK) return s;
-  return fp8 ? fp8_end(p, f8, kFp8TensorsPerStream, st) : MMDIT_OK;
+  return f8.on() ? fp8_end(p, f8, kFp8TensorsPerStream, st) : MMDIT_OK;
 }
 
 // Output-head workspace: the head's modulation, its LayerNorm-modulate output, the split-K

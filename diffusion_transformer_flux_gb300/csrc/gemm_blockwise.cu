@@ -19,8 +19,7 @@
 // it by 1 / (s_x s_w) and add it to float32 registers, while the tensor cores fill the other buffer.
 // After the last slice the same warps add the bias and store bf16 rows.  Every wait is bounded
 // (common.cuh).
-#include "common.cuh"
-#include "internal.h"
+#include "gemm_kernel.cuh"
 
 namespace mmdit {
 namespace {
@@ -45,19 +44,33 @@ struct BwBarriers {
   int abort_flag;
 };
 
+// EPI: the epilogue applied to the promoted sums (kEpiBias, kEpiQkv, kEpiGelu, kEpiGateResid, as
+// for the other GEMMs).  Two problems of the same N and K (the image and text streams) share a
+// launch: blockIdx.x enumerates problem 0's row tiles, then problem 1's.  Per problem, ep.bw_sx
+// holds s_x [K/128, M] and ep.bw_sw s_w [N/128, K/128].
+template <int EPI>
 __global__ void __launch_bounds__(kBwThreads, 1)
-    gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                          const float* __restrict__ sx, const float* __restrict__ sw,
-                          const __nv_bfloat16* __restrict__ bias, __nv_bfloat16* __restrict__ y, int M, int N, int K,
-                          uint32_t* status) {
+    gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_b0,
+                          const __grid_constant__ CUtensorMap tm_a1, const __grid_constant__ CUtensorMap tm_b1,
+                          int M0, int M1, int N, int K, const __grid_constant__ EpiArgs ep0,
+                          const __grid_constant__ EpiArgs ep1, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   BwBarriers* sb = reinterpret_cast<BwBarriers*>(smem + kBwStages * kBwStageBytes);
   volatile int* abort_flag = &sb->abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kBwTile, nb = blockIdx.y, n0 = nb * kBwTile;
+  const int tiles0 = (M0 + kBwTile - 1) / kBwTile;
+  const int prob = static_cast<int>(blockIdx.x) >= tiles0;
+  const int M = prob ? M1 : M0;
+  const int m0 = (prob ? static_cast<int>(blockIdx.x) - tiles0 : static_cast<int>(blockIdx.x)) * kBwTile;
+  const int nb = blockIdx.y, n0 = nb * kBwTile;
   const int num_kb = K / kBwTile;
+  const CUtensorMap* tm_a = prob ? &tm_a1 : &tm_a0;
+  const CUtensorMap* tm_b = prob ? &tm_b1 : &tm_b0;
+  const EpiArgs& ep = prob ? ep1 : ep0;
+  const float* __restrict__ sx = ep.bw_sx;
+  const float* __restrict__ sw = ep.bw_sw;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kBwStages; ++s) mbar_init(&sb->full[s], 1), mbar_init(&sb->empty[s], 1);
@@ -81,16 +94,16 @@ __global__ void __launch_bounds__(kBwThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer
-      tma_prefetch_desc(&tm_a);
-      tma_prefetch_desc(&tm_b);
+      tma_prefetch_desc(tm_a);
+      tma_prefetch_desc(tm_b);
       int issued = 0;
       for (int kb = 0; kb < num_kb; ++kb) {
         const int s = kb % kBwStages;
         if (!wait(&sb->empty[s], (static_cast<uint32_t>(kb / kBwStages) & 1u) ^ 1u)) break;
         uint8_t* st = smem + s * kBwStageBytes;
         mbar_arrive_expect_tx(&sb->full[s], kBwStageBytes);
-        tma_load_2d(st, &tm_a, &sb->full[s], kb * kBwTile, m0);
-        tma_load_2d(st + kBwTile * kBwTile, &tm_b, &sb->full[s], kb * kBwTile, n0);
+        tma_load_2d(st, tm_a, &sb->full[s], kb * kBwTile, m0);
+        tma_load_2d(st + kBwTile * kBwTile, tm_b, &sb->full[s], kb * kBwTile, n0);
         issued = kb + 1;
       }
       if (*abort_flag) {
@@ -158,25 +171,26 @@ __global__ void __launch_bounds__(kBwThreads, 1)
         acc[32 + i] = fmaf(__uint_as_float(p1[i]), f, acc[32 + i]);
       }
     }
-    if (ok && row_ok) {
-      const int nc = n0 + g * 64;
+    // the promoted sums back into TMEM (buffer 0: every product has been read out of it), then
+    // the epilogue every GEMM shares reads them there
+    ok = ok && !*abort_flag;
+    if (ok) {
+      uint32_t w0[32], w1[32];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float v[32];
-        if (bias) {
-          float bb[32];
-          load32(bias + nc + 32 * h, bb);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = acc[32 * h + i] + bb[i];
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = acc[32 * h + i];
-        }
-        store32(y + static_cast<size_t>(m) * N + nc + 32 * h, v);
-      }
+      for (int i = 0; i < 32; ++i) w0[i] = __float_as_uint(acc[i]), w1[i] = __float_as_uint(acc[32 + i]);
+      const uint32_t t = tmem + static_cast<uint32_t>(g * 64) + lane_off;
+      tmem_st32(t, w0);
+      tmem_st32(t + 32u, w1);
+      tmem_st_wait();
+      tc_fence_before();
+    }
+    // the eight promotion warps (an epilogue group may read columns another group wrote)
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (ok && g < EpiGroups<EPI>::value) {
+      tc_fence_after();
+      gemm_epilogue<__nv_bfloat16, kBwTile, EPI, false>(g, tmem + lane_off, m, n0, M, N, ep);
     }
   }
-
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -239,12 +253,86 @@ __global__ void __launch_bounds__(256) blockwise_cast_weight_kernel(const __nv_b
   if (threadIdx.x == 0) s_out[blockIdx.x] = s;  // [N/128, K/128]: blockIdx.x = ti * tiles_k + tj
 }
 
+
+
+
+// The blockwise GEMM for a GemmProblem whose per-problem ep.bw_sx / ep.bw_sw are set: A, W (and
+// A1, W1) are E4M3 codes [M, K], [N, K]; N % 128 == 0, K % 128 == 0.
+template <int EPI>
+cudaError_t run_gemm_blockwise(const GemmProblem& p, uint32_t* status, cudaStream_t stream) {
+  const bool two = p.M1 > 0;
+  if (p.N % kBwTile != 0 || p.K % kBwTile != 0 || p.K < kBwTile || (two && p.K1 > 0 && p.K1 != p.K))
+    return cudaErrorInvalidValue;
+  if (!p.ep.bw_sx || !p.ep.bw_sw || (two && (!p.ep1.bw_sx || !p.ep1.bw_sw))) return cudaErrorInvalidValue;
+  const uint64_t k = static_cast<uint64_t>(p.K), n = static_cast<uint64_t>(p.N);
+  const uint64_t stride[1] = {k};
+  const uint32_t box[2] = {static_cast<uint32_t>(kBwTile), static_cast<uint32_t>(kBwTile)};
+  CUtensorMap ta0, tb0, ta1, tb1;
+  const uint64_t da0[2] = {k, static_cast<uint64_t>(p.M)}, db[2] = {k, n};
+  const uint64_t da1[2] = {k, static_cast<uint64_t>(two ? p.M1 : p.M)};
+  const auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (!encode_tmap(&ta0, U8, 2, p.A, da0, stride, box, SW) || !encode_tmap(&tb0, U8, 2, p.W, db, stride, box, SW) ||
+      !encode_tmap(&ta1, U8, 2, two ? p.A1 : p.A, da1, stride, box, SW) ||
+      !encode_tmap(&tb1, U8, 2, two ? p.W1 : p.W, db, stride, box, SW))
+    return cudaErrorInvalidValue;
+  static int configured = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured != dev) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_blockwise_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwSmem);
+    if (e != cudaSuccess) return e;
+    configured = dev;
+  }
+  const int tiles_m = (p.M + kBwTile - 1) / kBwTile + (two ? (p.M1 + kBwTile - 1) / kBwTile : 0);
+  if (tiles_m == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(tiles_m), static_cast<unsigned>(p.N / kBwTile));
+  cudaError_t e = launch_pdl(gemm_blockwise_kernel<EPI>, grid, dim3(kBwThreads), kBwSmem, stream, ta0, tb0, ta1, tb1,
+                             p.M, two ? p.M1 : 0, p.N, p.K, p.ep, two ? p.ep1 : p.ep, status);
+  if (e != cudaSuccess) return e;
+  count_launch();
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t blockwise_linear_scratch(int M, int N, int K) {
   const size_t m = static_cast<size_t>(M), n = static_cast<size_t>(N), k = static_cast<size_t>(K);
   return round256(m * k) + round256(n * k) + round256((k / kBwTile) * m * 4) +
          round256((n / kBwTile) * (k / kBwTile) * 4);
+}
+
+cudaError_t launch_blockwise_cast_act(const __nv_bfloat16* x, int M, int K, uint8_t* q, float* s, cudaStream_t stream) {
+  if (M == 0) return cudaSuccess;
+  if (M < 0 || K % kBwTile != 0) return cudaErrorInvalidValue;
+  const int64_t warps = static_cast<int64_t>(M) * (K / kBwTile);
+  int64_t blocks = (warps + 7) / 8;
+  if (blocks > num_sms() * 16) blocks = num_sms() * 16;
+  cudaError_t e = launch_pdl(blockwise_cast_act_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, x, M,
+                             K, q, s);
+  if (e != cudaSuccess) return e;
+  count_launch();
+  return cudaSuccess;
+}
+
+cudaError_t launch_blockwise_cast_weight(const __nv_bfloat16* w, int N, int K, uint8_t* q, float* s, cudaStream_t stream) {
+  if (N % kBwTile != 0 || K % kBwTile != 0) return cudaErrorInvalidValue;
+  const unsigned tiles = static_cast<unsigned>((N / kBwTile) * (K / kBwTile));
+  if (tiles == 0) return cudaSuccess;
+  cudaError_t e = launch_pdl(blockwise_cast_weight_kernel, dim3(tiles), dim3(256), 0, stream, w, N, K, q, s);
+  if (e != cudaSuccess) return e;
+  count_launch();
+  return cudaSuccess;
+}
+
+cudaError_t launch_gemm_blockwise(const GemmProblem& p, uint32_t* status, cudaStream_t stream) {
+  switch (p.epi) {
+    case kEpiBias: return run_gemm_blockwise<kEpiBias>(p, status, stream);
+    case kEpiQkv: return run_gemm_blockwise<kEpiQkv>(p, status, stream);
+    case kEpiGelu: return run_gemm_blockwise<kEpiGelu>(p, status, stream);
+    case kEpiGateResid: return run_gemm_blockwise<kEpiGateResid>(p, status, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_blockwise_linear(int M, int N, int K, const __nv_bfloat16* x, const __nv_bfloat16* w,
@@ -258,42 +346,13 @@ cudaError_t launch_blockwise_linear(int M, int N, int K, const __nv_bfloat16* x,
   uint8_t* wq = xq + round256(m * k);
   float* sx = reinterpret_cast<float*>(wq + round256(n * k));
   float* sw = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(sx) + round256((k / kBwTile) * m * 4));
-  cudaError_t e;
-  {
-    const int64_t warps = static_cast<int64_t>(M) * (K / kBwTile);
-    int64_t blocks = (warps + 7) / 8;
-    if (blocks > num_sms() * 16) blocks = num_sms() * 16;
-    e = launch_pdl(blockwise_cast_act_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, x, M, K, xq, sx);
-    if (e != cudaSuccess) return e;
-    count_launch();
-  }
-  {
-    const unsigned tiles = static_cast<unsigned>((N / kBwTile) * (K / kBwTile));
-    e = launch_pdl(blockwise_cast_weight_kernel, dim3(tiles), dim3(256), 0, stream, w, N, K, wq, sw);
-    if (e != cudaSuccess) return e;
-    count_launch();
-  }
-  CUtensorMap ta, tb;
-  const uint64_t da[2] = {k, m}, db[2] = {k, n};
-  const uint64_t stride[1] = {k};
-  const uint32_t box[2] = {static_cast<uint32_t>(kBwTile), static_cast<uint32_t>(kBwTile)};
-  if (!encode_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, xq, da, stride, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wq, db, stride, box, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
-  static int configured = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (configured != dev) {
-    e = cudaFuncSetAttribute(gemm_blockwise_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwSmem);
-    if (e != cudaSuccess) return e;
-    configured = dev;
-  }
-  const dim3 grid(static_cast<unsigned>((M + kBwTile - 1) / kBwTile), static_cast<unsigned>(N / kBwTile));
-  e = launch_pdl(gemm_blockwise_kernel, grid, dim3(kBwThreads), kBwSmem, stream, ta, tb,
-                 static_cast<const float*>(sx), static_cast<const float*>(sw), bias, y, M, N, K, status);
+  cudaError_t e = launch_blockwise_cast_act(x, M, K, xq, sx, stream);
   if (e != cudaSuccess) return e;
-  count_launch();
-  return cudaGetLastError();
+  if ((e = launch_blockwise_cast_weight(w, N, K, wq, sw, stream)) != cudaSuccess) return e;
+  GemmProblem g;
+  g.act = 2, g.epi = kEpiBias, g.M = M, g.N = N, g.K = K, g.A = xq, g.W = wq;
+  g.ep.bias = bias, g.ep.out = y, g.ep.bw_sx = sx, g.ep.bw_sw = sw;
+  return launch_gemm_blockwise(g, status, stream);
 }
 
 }  // namespace mmdit

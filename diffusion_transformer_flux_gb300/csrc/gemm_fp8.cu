@@ -7,6 +7,7 @@
 
 namespace mmdit {
 cudaError_t launch_gemm_fp8(const GemmProblem& p, uint32_t* status, cudaStream_t stream) {
+  if (p.ep.bw_sx) return launch_gemm_blockwise(p, status, stream);  // blockwise recipe: per-tile scales
   if (p.N % 128 != 0 || p.K % 16 != 0 || p.a_mn || p.b_mn) return cudaErrorInvalidValue;
   if (!p.ep.scale_a || !p.ep.scale_w || (p.M1 > 0 && (!p.ep1.scale_a || !p.ep1.scale_w)))
     return cudaErrorInvalidValue;

@@ -55,6 +55,10 @@ struct EpiArgs {
   // scales the operands were cast with
   const float* scale_a = nullptr;
   const float* scale_w = nullptr;
+  // blockwise FP8 (gemm_blockwise.cu): per-tile scales s_x [K/128, M] and s_w [N/128, K/128]; the
+  // GEMM divides each 128-wide K slice's product by them before the epilogue
+  const float* bw_sx = nullptr;
+  const float* bw_sw = nullptr;
   // kEpiGeluF8: `out` receives E4M3 codes of GELU(.) * out_scale[0]; out_amax[0] is raised to
   // the largest |GELU(.)| of the tile
   const float* out_scale = nullptr;
@@ -178,6 +182,13 @@ cudaError_t launch_attention_fp8(const AttnFp8Problem& p, uint32_t* status, cuda
 // of x (1 x 128 tiles) and W (128 x 128 tiles) into `scratch` (blockwise_linear_scratch bytes),
 // then the GEMM that scales each 128-wide K slice's product.  N % 128 == 0, K % 128 == 0.
 size_t blockwise_linear_scratch(int M, int N, int K);
+// The casts alone: x [M, K] -> codes q [M, K], scales s [K/128, M]; W [N, K] -> q [N, K], s [N/128, K/128].
+cudaError_t launch_blockwise_cast_act(const __nv_bfloat16* x, int M, int K, uint8_t* q, float* s, cudaStream_t stream);
+cudaError_t launch_blockwise_cast_weight(const __nv_bfloat16* w, int N, int K, uint8_t* q, float* s,
+                                         cudaStream_t stream);
+// The blockwise GEMM of a problem whose ep.bw_sx / ep.bw_sw (and ep1's) are set (E4M3 codes as A, W).
+struct GemmProblem;
+cudaError_t launch_gemm_blockwise(const GemmProblem& p, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_blockwise_linear(int M, int N, int K, const __nv_bfloat16* x, const __nv_bfloat16* w,
                                     const __nv_bfloat16* bias, __nv_bfloat16* y, void* scratch, uint32_t* status,
                                     cudaStream_t stream);

@@ -73,10 +73,17 @@ typedef enum mmdit_act_dtype { MMDIT_F32 = 0, MMDIT_BF16 = 1 } mmdit_act_dtype;
  * every input is first written in bf16, its amax taken, then cast (weights likewise at every
  * call).  The state's history column `pos` records those amax and `scale` ends holding the scales
  * used; amax_compute_algo is not read. */
+/* FP8_BLOCKWISE = the same four linears under the blockwise recipe ([FP8] §Configuration,
+ * fp8_recipe "blockwise"; the arithmetic of mmdit_fp8_blockwise_linear_fwd): each input, written
+ * in bf16, is cast per 1 x 128 tile of its rows and each weight per 128 x 128 tile, every tile
+ * with its own scale 448 / amax, and the GEMMs rescale each 128-wide K slice's product before
+ * their usual epilogues.  Nothing is kept between calls: the fp8 state argument must be NULL.
+ * Needs hidden % 128 == 0 and mlp_hidden % 128 == 0; not for the parallel single block. */
 typedef enum mmdit_gemm_mode {
   MMDIT_GEMM_NATIVE = 0,
   MMDIT_GEMM_FP8_E4M3 = 1,
-  MMDIT_GEMM_FP8_TENSORWISE = 2
+  MMDIT_GEMM_FP8_TENSORWISE = 2,
+  MMDIT_GEMM_FP8_BLOCKWISE = 3
 } mmdit_gemm_mode;
 
 /* Shapes and options of one block call ([API] §Configuration, FluxConfig). */

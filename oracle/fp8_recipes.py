@@ -125,6 +125,23 @@ def blockwise_quantize_weight(w, tile: int = BLOCKWISE_TILE):
     return q, s
 
 
+class BlockwiseScaling:
+    """The blockwise recipe as the block oracle's ``fp8`` object (``oracle.flux.block_linear`` calls
+    ``linear``): every linear is ``blockwise_linear`` of its input and weight, with no state.
+    ``act_cast``, if given, is applied to a linear's input first (the value it holds as a stored
+    activation tensor, as for ``TensorwiseScaling``)."""
+
+    def __init__(self, act_cast=None, tile: int = None):
+        self.act_cast = act_cast
+        self.tile = BLOCKWISE_TILE if tile is None else tile
+
+    def linear(self, name, x, w, b):
+        x = np.asarray(x, np.float64)
+        if self.act_cast is not None:
+            x = np.asarray(self.act_cast(x), np.float64)
+        return blockwise_linear(x, w, b, self.tile)
+
+
 def blockwise_linear(x, w, b, tile: int = BLOCKWISE_TILE):
     """y = sum over K slices j of Q_j(x) Q_j(W)^T / (s_x[row, j] s_w[tile row, j]) + b."""
     x = np.asarray(x, np.float64)

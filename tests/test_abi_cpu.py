@@ -93,6 +93,12 @@ def test_validation_errors_before_any_launch(lib):
     assert lib.mmdit_double_block_fwd(C.byref(fp8), C.byref(w), C.byref(w), None, None, None, None,
                                       None, None, None, None, None, 0, None) == 1
     assert "fp8 state" in L.last_error()
+    # the blockwise recipe keeps no state: one given is an error
+    bwd = _dims(gemm=L.MMDIT_GEMM_FP8_BLOCKWISE, act=1)
+    stb = L.Fp8State(0x1000, 0x2000, 1024, 16, 0, 0, 0)
+    assert lib.mmdit_double_block_fwd(C.byref(bwd), C.byref(w), C.byref(w), None, None, None, None,
+                                      None, None, None, C.byref(stb), None, 0, None) == 1
+    assert "blockwise" in L.last_error()
     # an FP8 state with too few tensors for a double block, or a position outside the history
     st8 = L.Fp8State(0x1000, 0x2000, 1024, 8, 0, 0, 0)
     assert lib.mmdit_double_block_fwd(C.byref(fp8), C.byref(w), C.byref(w), None, None, None, None,

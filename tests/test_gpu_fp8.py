@@ -627,3 +627,48 @@ def test_blockwise_fp8_linear(M, N, K):
     d_fp8 = float(np.abs(y_or - y_ex).max()) / rms
     print(f"[fp8 blockwise] {M}x{N}x{K}: max|GPU - recipe|/RMS {d_gpu:.3e}, max|recipe - exact|/RMS {d_fp8:.3e}")
     assert d_gpu <= 0.25 * d_fp8
+
+
+def _blockwise_block_run(case):
+    """One call of the block with gemm = MMDIT_GEMM_FP8_BLOCKWISE (no FP8 state)."""
+    dims = L.make_dims(case.B, case.S_i, case.S_t, case.D, case.H, case.F, L.MMDIT_BF16,
+                       rope_interleaved=case.interleaved, gelu_tanh=case.gelu_tanh,
+                       gemm=L.MMDIT_GEMM_FP8_BLOCKWISE)
+    ids = torch.from_numpy(case.ids).cuda()
+    cos = torch.empty(case.B, case.S, 64, device="cuda")
+    sin = torch.empty_like(cos)
+    L.rope3d_freqs(ids, (16, 56, 56), 10000.0, cos, sin)
+    wi = upload_weights(case.w_img, "bf16")
+    if case.single:
+        x = dev(case.x_joint())
+        y = torch.empty_like(x)
+        ws = L.mmdit_single_block_fwd(dims, wi, dev(case.vec), cos, sin, x, y)
+        outs = (y,)
+    else:
+        wt = upload_weights(case.w_txt, "bf16")
+        xi, xt = dev(case.x_img), dev(case.x_txt)
+        yi, yt = torch.empty_like(xi), torch.empty_like(xt)
+        ws = L.mmdit_double_block_fwd(dims, wi, wt, dev(case.vec), cos, sin, xi, xt, yi, yt)
+        outs = (yi, yt)
+    torch.cuda.synchronize()
+    assert L.mmdit_workspace_status(ws) == 0
+    return tuple(host(o) for o in outs)
+
+
+@pytest.mark.parametrize("B,S_i,S_t,D,H,F,single", SMALL)
+def test_fp8_blockwise_block_small(B, S_i, S_t, D, H, F, single):
+    """The blockwise recipe inside the blocks ("FP8 training for Flux models", §Configuration,
+    fp8_recipe "blockwise"): every linear's bf16 input cast per 1 x 128 tile and its weight per
+    128 x 128 tile, no state.  The block output under the FP8 bars against the exact blockwise
+    evaluation (oracle.fp8_recipes.BlockwiseScaling on bf16-stored inputs) and the float64 block."""
+    from oracle import fp8_recipes as R
+    case = BlockCase(B, S_i, S_t, D, H, F, "bf16", seed=51 + S_i + D, std=0.05, single=single)
+    y = _blockwise_block_run(case)
+    bw = R.BlockwiseScaling(act_cast=O.round_bf16)
+    args = dict(mm_cast=O.round_bf16, fp8=bw, interleaved=case.interleaved, gelu_tanh=case.gelu_tanh)
+    if single:
+        y8 = (O.single_block(case.x_joint(), case.vec, case.cos, case.sin, case.w_img, case.H, **args),)
+    else:
+        y8 = O.double_block(case.x_img, case.x_txt, case.vec, case.cos, case.sin, case.w_img, case.w_txt,
+                            case.H, **args)
+    _check_norm_wise(y, y8, case.oracle(None), "FP8 blockwise block")

@@ -302,3 +302,22 @@ def test_tensorwise_recipe_object_in_a_block_is_the_tensorwise_linear():
                           fp8=E4.DelayedScaling(dict(t1.scales)))
     for a, bb in zip(y_tw, y_dl):
         assert np.array_equal(a, bb)
+
+
+def test_blockwise_scaling_object_is_the_recipe_on_the_stored_input():
+    # the block oracle's fp8 object: blockwise_linear of the act_cast input, and exact wherever
+    # every tile is already on the E4M3 grid with its maximum at 448 (every scale 1, no rounding)
+    from oracle import flux as O
+    x = RNG.standard_normal((2, 5, 256))
+    w = RNG.standard_normal((256, 256)) * 0.02
+    b = RNG.standard_normal(256)
+    bw = R.BlockwiseScaling(act_cast=O.round_bf16)
+    np.testing.assert_array_equal(bw.linear("qkv", x, w, b), R.blockwise_linear(O.round_bf16(x), w, b))
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 448.0])
+    xg = RNG.choice(grid, size=(3, 256)) * RNG.choice([-1.0, 1.0], size=(3, 256))
+    xg[:, 0] = 448.0
+    xg[:, 128] = 448.0
+    wg = RNG.choice(grid, size=(128, 256))
+    wg[0, 0] = 448.0
+    wg[0, 128] = 448.0
+    np.testing.assert_array_equal(R.BlockwiseScaling().linear("o", xg, wg, None), xg @ wg.T)
