@@ -70,6 +70,10 @@ def parse_args():
                          "double + single block at 16384 + 512 tokens with E4M3 linears; "
                          f"{MODEL_WORKLOAD}: the whole Flux 12B forward (19 double + 38 single "
                          "blocks) at 1024 + 512 tokens through mmdit_flux_forward")
+    ap.add_argument("--fp8-recipe", choices=["delayed", "tensorwise", "blockwise"], default="delayed",
+                    help=f"the scaling recipe of the E4M3 linears in {FP8_WORKLOAD}: per-tensor delayed "
+                         "scaling (the FP8 page's default), per-tensor current scaling, or per-tile "
+                         "current scaling (1 x 128 inputs, 128 x 128 weights)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     return args
@@ -303,7 +307,7 @@ class Fp8BlockStep(DeviceStep):
     N(0, 1) at width D.  Each step records its amax into history column 0 (most_recent reads
     only the latest), so that a captured graph replays the same step."""
 
-    def __init__(self, wl, device):
+    def __init__(self, wl, device, recipe="delayed"):
         import torch
         from diffusion_transformer_flux_gb300 import _lib as L
         from diffusion_transformer_flux_gb300 import synth
@@ -333,7 +337,12 @@ class Fp8BlockStep(DeviceStep):
         self.scale_s = torch.ones(8, device=device)
         self.fp8_d = L.make_fp8_state(self.hist_d, self.scale_d, pos=0)
         self.fp8_s = L.make_fp8_state(self.hist_s, self.scale_s, pos=0)
-        self.dims = L.make_dims(B, S_i, S_t, D, H, F, L.MMDIT_BF16, gemm=L.MMDIT_GEMM_FP8_E4M3)
+        mode = {"delayed": L.MMDIT_GEMM_FP8_E4M3, "tensorwise": L.MMDIT_GEMM_FP8_TENSORWISE,
+                "blockwise": L.MMDIT_GEMM_FP8_BLOCKWISE}[recipe]
+        if recipe == "blockwise":  # per-tile scales of this call only: no state
+            self.fp8_d = self.fp8_s = None
+        self.recipe = recipe
+        self.dims = L.make_dims(B, S_i, S_t, D, H, F, L.MMDIT_BF16, gemm=mode)
         ws_block = max(L.mmdit_double_block_workspace_size(self.dims),
                        L.mmdit_single_block_workspace_size(self.dims))
         self.ws_block = L.workspace(ws_block, device)
@@ -994,7 +1003,8 @@ def main():
     fp8 = wl.dtype == "fp8"
     model = args.workload == MODEL_WORKLOAD
     hw = None if (fp8 or model) else HostWorkload(wl)
-    st = Fp8BlockStep(wl, device) if fp8 else ModelStep(wl, device) if model else DeviceStep(hw, device)
+    st = (Fp8BlockStep(wl, device, args.fp8_recipe) if fp8 else ModelStep(wl, device) if model
+          else DeviceStep(hw, device))
     peaks, peak_src = load_peaks()
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)  # > 129 MB of L2
@@ -1162,15 +1172,19 @@ def main():
             "dtype": "e4m3 linears, bf16 attention and activations" if fp8 else "bf16",
             "data": "synthetic (seeded PCG64; N(0,0.02) weights, N(0,1) activations, text embeddings "
                     "and latents; no dataset or trained weights)",
-            "config": {"workload": args.workload, "global_batch": world * wl.batch, "seq_len": S,
+            "config": {"workload": args.workload, **({"fp8_recipe": args.fp8_recipe} if fp8 else {}),
+                       "global_batch": world * wl.batch, "seq_len": S,
                        "tokens": f"{wl.seq_img} image + {wl.seq_txt} text", "hidden": wl.hidden,
                        "heads": wl.heads, "head_dim": 128, "mlp_hidden": wl.mlp_hidden,
                        "parallelism": f"{world} independent replica(s), no exchange",
                        "l2": "flushed before every timed step (256 MB write outside the events)",
                        "launch": "plain calls" if args.no_graph else
                                  "CUDA-graph replay of the step (e2e: plain calls)",
-                       "step": ("rope3d_freqs, double block, single block (E4M3 linears with "
-                                "delayed per-tensor scaling; weights cast at every call)") if fp8 else
+                       "step": ("rope3d_freqs, double block, single block (E4M3 linears; "
+                                + {"delayed": "delayed per-tensor scaling", "tensorwise": "current per-tensor scaling",
+                                   "blockwise": "current per-tile scaling, 1 x 128 inputs and 128 x 128 weights"}[
+                                    args.fp8_recipe]
+                                + "; weights cast at every call)") if fp8 else
                                ("rope3d_freqs, flow-matching noise, mmdit_flux_forward (conditioning, "
                                 "every block's modulation in one launch, img_in, txt_in, "
                                 f"{wl.n_double} double + {wl.n_single} single blocks, output head), "
