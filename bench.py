@@ -70,10 +70,11 @@ def parse_args():
                          "double + single block at 16384 + 512 tokens with E4M3 linears; "
                          f"{MODEL_WORKLOAD}: the whole Flux 12B forward (19 double + 38 single "
                          "blocks) at 1024 + 512 tokens through mmdit_flux_forward")
-    ap.add_argument("--fp8-recipe", choices=["delayed", "tensorwise", "blockwise"], default="delayed",
+    ap.add_argument("--fp8-recipe", choices=["delayed", "tensorwise", "blockwise", "mxfp8"], default="delayed",
                     help=f"the scaling recipe of the E4M3 linears in {FP8_WORKLOAD}: per-tensor delayed "
-                         "scaling (the FP8 page's default), per-tensor current scaling, or per-tile "
-                         "current scaling (1 x 128 inputs, 128 x 128 weights)")
+                         "scaling (the FP8 page's default), per-tensor current scaling, per-tile "
+                         "current scaling (1 x 128 inputs, 128 x 128 weights), or MXFP8 (a power-of-two "
+                         "scale per 32 elements along K; its products run on the bf16 tensor cores)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     return args
@@ -338,8 +339,8 @@ class Fp8BlockStep(DeviceStep):
         self.fp8_d = L.make_fp8_state(self.hist_d, self.scale_d, pos=0)
         self.fp8_s = L.make_fp8_state(self.hist_s, self.scale_s, pos=0)
         mode = {"delayed": L.MMDIT_GEMM_FP8_E4M3, "tensorwise": L.MMDIT_GEMM_FP8_TENSORWISE,
-                "blockwise": L.MMDIT_GEMM_FP8_BLOCKWISE}[recipe]
-        if recipe == "blockwise":  # per-tile scales of this call only: no state
+                "blockwise": L.MMDIT_GEMM_FP8_BLOCKWISE, "mxfp8": L.MMDIT_GEMM_FP8_MXFP8}[recipe]
+        if recipe in ("blockwise", "mxfp8"):  # per-tile or per-block scales of this call only: no state
             self.fp8_d = self.fp8_s = None
         self.recipe = recipe
         self.dims = L.make_dims(B, S_i, S_t, D, H, F, L.MMDIT_BF16, gemm=mode)
@@ -896,6 +897,29 @@ def measure_blockwise_linear(L, torch, device, M=4608, N=12288, K=3072, reps=5):
             "avg_us": round(us, 2), "achieved_tflops": round(2.0 * M * N * K / us / 1e6, 1)}
 
 
+def measure_mx_linear(L, torch, device, M=4608, N=12288, K=3072, reps=5):
+    """The MXFP8 linear (mmdit_fp8_mxfp8_linear_fwd: the MX casts of x and W in the call, then the
+    bf16 GEMM of their represented values) at the fc1 shape: 2 M N K FLOPs per call, CUDA events
+    around `reps` calls after one warm-up."""
+    x = torch.randn(M, K, device=device).to(torch.bfloat16)
+    w = (torch.randn(N, K, device=device) * 0.02).to(torch.bfloat16)
+    b = torch.zeros(N, device=device, dtype=torch.bfloat16)
+    y = torch.empty(M, N, device=device, dtype=torch.bfloat16)
+    ws = L.mmdit_fp8_mxfp8_linear_fwd(x, w, b, y)
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        L.mmdit_fp8_mxfp8_linear_fwd(x, w, b, y, ws=ws)
+    e.record()
+    torch.cuda.synchronize()
+    if L.mmdit_workspace_status(ws) != 0:
+        raise RuntimeError("a kernel gave up a bounded wait in the MXFP8 linear")
+    us = a.elapsed_time(e) * 1e3 / reps
+    return {"op": "MXFP8 linear (casts of x and W included; bf16 tensor cores)", "M": M, "N": N, "K": K,
+            "avg_us": round(us, 2), "achieved_tflops": round(2.0 * M * N * K / us / 1e6, 1)}
+
+
 def measure_linear_bwd(L, torch, device, peak, M=4608, N=12288, K=3072, reps=5):
     """The backward of the block's fc1-shaped linear (mmdit_linear_bwd: dx and dW through the
     tensor-core GEMM reading W, dy and x MN-major as stored, db): 4 M N K FLOPs per call, CUDA
@@ -1108,7 +1132,8 @@ def main():
 
     def peak_of(name):
         is_linear = name.split(".")[-1] in ("qkv", "out", "fc1", "fc2")
-        return fp8_peak if (fp8 and is_linear) else bf16_peak
+        # the MXFP8 recipe multiplies its represented values on the bf16 tensor cores
+        return fp8_peak if (fp8 and is_linear and args.fp8_recipe != "mxfp8") else bf16_peak
 
     per_kernel = []
     for name, (n, t) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
@@ -1147,6 +1172,7 @@ def main():
         extras["single_block_parallel"] = measure_parallel_block(st, L, torch, bf16_peak)
         extras["linear_backward"] = measure_linear_bwd(L, torch, device, bf16_peak)
         extras["blockwise_fp8_linear"] = measure_blockwise_linear(L, torch, device)
+        extras["mxfp8_linear"] = measure_mx_linear(L, torch, device)
         extras["double_block_backward"] = measure_block_bwd(st, L, torch, bf16_peak)
         extras["double_block_training"] = measure_block_train(st, L, torch, bf16_peak)
     if fp8:
@@ -1182,7 +1208,9 @@ def main():
                                  "CUDA-graph replay of the step (e2e: plain calls)",
                        "step": ("rope3d_freqs, double block, single block (E4M3 linears; "
                                 + {"delayed": "delayed per-tensor scaling", "tensorwise": "current per-tensor scaling",
-                                   "blockwise": "current per-tile scaling, 1 x 128 inputs and 128 x 128 weights"}[
+                                   "blockwise": "current per-tile scaling, 1 x 128 inputs and 128 x 128 weights",
+                                   "mxfp8": "MXFP8: E4M3 with a power-of-two scale per 32 elements along K, "
+                                            "products of the represented values on the bf16 tensor cores"}[
                                     args.fp8_recipe]
                                 + "; weights cast at every call)") if fp8 else
                                ("rope3d_freqs, flow-matching noise, mmdit_flux_forward (conditioning, "
@@ -1201,10 +1229,12 @@ def main():
                        "dense_flops_per_step_incl_embeds_and_head": st.flops_dense},
             "pct_of_bf16_peak": round(100 * value / world / bf16_peak, 2),
             **({"fp8_peak_tflops": fp8_peak, "fp8_peak_measured": fp8_measured,
+                # (none under MXFP8, whose linears run on the bf16 tensor cores)
                 "linears_pct_of_fp8_peak": round(100 * sum(r["achieved_tflops"] * r["avg_us"] for r in per_kernel
                                                            if r["bound"] == "tensor" and peak_of(r["kernel"]) == fp8_peak)
                                                  / max(1e-9, sum(r["avg_us"] for r in per_kernel if r["bound"] == "tensor"
-                                                                 and peak_of(r["kernel"]) == fp8_peak)) / fp8_peak, 2)}
+                                                                 and peak_of(r["kernel"]) == fp8_peak)) / fp8_peak, 2)
+                if args.fp8_recipe != "mxfp8" else None}
                if fp8 else {}),
             "tokens_per_s": round(world * wl.batch * S * args.steps / total_s, 1),
             "clocks": clocks,

@@ -36,6 +36,7 @@ EXPORTED = [
     "mmdit_block_workspace_offsets", "mmdit_fp8_quantize_e4m3", "mmdit_fp8_linear_workspace_size",
     "mmdit_fp8_linear_fwd", "mmdit_fp8_linear_bwd_workspace_size", "mmdit_fp8_linear_bwd",
     "mmdit_fp8_blockwise_linear_workspace_size", "mmdit_fp8_blockwise_linear_fwd",
+    "mmdit_fp8_mxfp8_linear_workspace_size", "mmdit_fp8_mxfp8_linear_fwd",
     "mmdit_single_block_parallel_fwd", "mmdit_linear_bwd_workspace_size",
     "mmdit_linear_bwd", "mmdit_double_block_bwd_workspace_size", "mmdit_double_block_bwd",
     "mmdit_single_block_bwd_workspace_size", "mmdit_single_block_bwd", "mmdit_double_block_fwd_train",
@@ -81,6 +82,7 @@ MMDIT_GEMM_NATIVE = 0
 MMDIT_GEMM_FP8_E4M3 = 1
 MMDIT_GEMM_FP8_TENSORWISE = 2
 MMDIT_GEMM_FP8_BLOCKWISE = 3
+MMDIT_GEMM_FP8_MXFP8 = 4
 FP8_LINEARS = ("qkv", "o", "fc1", "fc2")
 
 
@@ -178,6 +180,8 @@ _SIGS = {
     "mmdit_single_block_bwd": (C.c_int, [PDIMS, PW, VP, VP, VP, VP, VP, VP, VP, PGRADS, VP, SZ, VP]),
     "mmdit_fp8_blockwise_linear_workspace_size": (SZ, [I32, I32, I32]),
     "mmdit_fp8_blockwise_linear_fwd": (C.c_int, [I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
+    "mmdit_fp8_mxfp8_linear_workspace_size": (SZ, [I32, I32, I32]),
+    "mmdit_fp8_mxfp8_linear_fwd": (C.c_int, [I32, I32, I32, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_double_block_fwd_train": (C.c_int, [PDIMS, PW, PW, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
     "mmdit_double_block_bwd_saved": (C.c_int, [PDIMS, PW, PW, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, PGRADS, PGRADS,
                                                VP, SZ, VP]),
@@ -665,6 +669,22 @@ def mmdit_fp8_blockwise_linear_fwd(x, w, b, y, ws=None, stream=None):
 
 def mmdit_fp8_blockwise_linear_workspace_size(M, N, K) -> int:
     return load().mmdit_fp8_blockwise_linear_workspace_size(M, N, K)
+
+
+def mmdit_fp8_mxfp8_linear_fwd(x, w, b, y, ws=None, stream=None):
+    """y = x W^T + b under the MXFP8 recipe (see include/mmdit.h); x [M, K], w [N, K], y [M, N] bf16.
+    Returns the workspace, whose layout the header states (values, codes and scales after the call)."""
+    M, K = x.shape[-2], x.shape[-1]
+    N = w.shape[0]
+    if ws is None:
+        ws = workspace(mmdit_fp8_mxfp8_linear_workspace_size(M, N, K), x.device)
+    _check(load().mmdit_fp8_mxfp8_linear_fwd(M, N, K, _ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(ws), ws.numel(),
+                                             _stream(stream)))
+    return ws
+
+
+def mmdit_fp8_mxfp8_linear_workspace_size(M, N, K) -> int:
+    return load().mmdit_fp8_mxfp8_linear_workspace_size(M, N, K)
 
 
 def mmdit_double_block_fwd_train(dims: Dims, w_img: dict, w_txt: dict, vec, cos, sin, x_img, x_txt, y_img, y_txt,

@@ -23,7 +23,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]
 SOURCES = ["gemm_bf16.cu", "gemm_tf32.cu", "gemm_fp8.cu", "gemm_blockwise.cu", "fp8.cu", "attention.cu",
-           "attention_bwd.cu", "attention_fp8.cu", "elementwise.cu", "backward.cu", "api.cu", "noalloc.cu"]
+           "attention_bwd.cu", "attention_fp8.cu", "elementwise.cu", "backward.cu", "api.cu", "noalloc.cu",
+           "mxfp8.cu"]
 
 
 def _nvcc() -> str:

@@ -203,6 +203,7 @@ struct BlockPlan {
              // and weights
   bool fp8_current = false;  // tensorwise or blockwise (current) scaling: inputs staged in bf16 before their cast
   bool fp8_blockwise = false;  // blockwise: per-tile scales (bw_sx, bw_sw), the blockwise GEMM
+  bool fp8_mx = false;  // MXFP8: bf16 operands holding the MX-represented values; wq holds the weights' (bf16)
   int B, Si, St, S, S_pad, D, H, F;
   size_t elt;
   size_t mod[2], h[2], q, k, vt, o[2], x1[2], u[2];
@@ -235,6 +236,7 @@ static bool plan_block(const mmdit_dims* d, bool single, BlockPlan* p) {
            d->gemm == MMDIT_GEMM_FP8_BLOCKWISE;
   p->fp8_blockwise = d->gemm == MMDIT_GEMM_FP8_BLOCKWISE;
   p->fp8_current = d->gemm == MMDIT_GEMM_FP8_TENSORWISE || p->fp8_blockwise;
+  p->fp8_mx = d->gemm == MMDIT_GEMM_FP8_MXFP8;
   const size_t mm_elt = p->fp8 ? 1 : p->elt;  // inputs of the QKV and fc1/fc2 linears
   Carver c;
   const size_t B = p->B, D = p->D, F = p->F, S = p->S;
@@ -251,7 +253,9 @@ static bool plan_block(const mmdit_dims* d, bool single, BlockPlan* p) {
   for (int s = 0; s < 2; ++s) p->x1[s] = s < ns ? c.take(rows[s] * D * 4) : 0;
   for (int s = 0; s < 2; ++s) p->u[s] = s < ns ? c.take(rows[s] * F * mm_elt) : 0;
   for (int s = 0; s < 2; ++s) p->o8[s] = p->fp8 && s < ns ? c.take(rows[s] * D) : 0;
-  for (int s = 0; s < 2; ++s) p->wq[s] = p->fp8 && s < ns ? c.take(p->wq_bytes()) : 0;
+  // E4M3 weight codes, or (MXFP8) the weights' represented values in bf16
+  for (int s = 0; s < 2; ++s)
+    p->wq[s] = (p->fp8 || p->fp8_mx) && s < ns ? c.take(p->wq_bytes() * (p->fp8_mx ? 2 : 1)) : 0;
   // tensorwise: a linear's bf16 input (LayerNorm-modulate output or GELU output) before its cast
   for (int s = 0; s < 2; ++s)
     p->stage[s] = p->fp8_current && s < ns ? c.take(rows[s] * (F > D ? F : D) * 2) : 0;
@@ -271,7 +275,7 @@ static mmdit_status check_dims(const mmdit_dims* d) {
   if (d->act != MMDIT_F32 && d->act != MMDIT_BF16)
     return fail(MMDIT_ERR_INVALID_ARG, "act must be MMDIT_F32 or MMDIT_BF16 (got %d)", d->act);
   if (d->gemm != MMDIT_GEMM_NATIVE && d->gemm != MMDIT_GEMM_FP8_E4M3 && d->gemm != MMDIT_GEMM_FP8_TENSORWISE &&
-      d->gemm != MMDIT_GEMM_FP8_BLOCKWISE)
+      d->gemm != MMDIT_GEMM_FP8_BLOCKWISE && d->gemm != MMDIT_GEMM_FP8_MXFP8)
     return fail(MMDIT_ERR_INVALID_ARG, "unknown gemm mode %d", d->gemm);
   if (d->gemm != MMDIT_GEMM_NATIVE && d->act != MMDIT_BF16)
     return fail(MMDIT_ERR_UNSUPPORTED, "FP8 E4M3 linears need bf16 activations (act = MMDIT_BF16)");
@@ -332,9 +336,10 @@ static mmdit_status check_fp8(const mmdit_dims* d, const mmdit_fp8_state* f, int
     if (f) return fail(MMDIT_ERR_INVALID_ARG, "fp8 state given but the gemm mode is native");
     return MMDIT_OK;
   }
-  if (d->gemm == MMDIT_GEMM_FP8_BLOCKWISE) {
-    // every scale is the call's own per-tile scale: there is no state to read or record
-    if (f) return fail(MMDIT_ERR_INVALID_ARG, "fp8 state given but the blockwise recipe keeps none");
+  if (d->gemm == MMDIT_GEMM_FP8_BLOCKWISE || d->gemm == MMDIT_GEMM_FP8_MXFP8) {
+    // every scale is the call's own per-tile or per-block scale: there is no state to read or record
+    if (f) return fail(MMDIT_ERR_INVALID_ARG, "fp8 state given but the %s recipe keeps none",
+                       d->gemm == MMDIT_GEMM_FP8_MXFP8 ? "MXFP8" : "blockwise");
     return MMDIT_OK;
   }
   if (!f) return fail(MMDIT_ERR_INVALID_ARG, "FP8 linears need an fp8 state (got NULL)");
@@ -415,6 +420,7 @@ struct Fp8 {
   const mmdit_fp8_state* f = nullptr;
   bool current = false;  // tensorwise or blockwise: every scale from the tensor's own amax in this call
   bool blockwise = false;  // per-tile scales in the plan's bw_sx / bw_sw slots; no state (f == nullptr)
+  bool mx = false;  // MXFP8: every linear input and weight replaced by its MX-represented values (bf16)
   int n_tensors = 0;     // tensors this block records (16 double, 8 single)
   bool on() const { return f != nullptr || blockwise; }  // the linears run on E4M3 codes
   const float* scale(int t) const { return f->scale + t; }
@@ -432,6 +438,19 @@ mmdit_status fp8_cast_current(const Fp8& f8, const QuantJob* jobs, int n, cudaSt
                                  f8.f->margin, 0, st),
              what);
   MMDIT_CUDA(launch_quantize_e4m3(jobs, n, st), what);
+  return MMDIT_OK;
+}
+
+// MXFP8: replace each stream's bf16 tensor [rows, K] at plan offset `off` by its MX-represented
+// values, in place (one launch for the streams).
+mmdit_status mx_in_place(const BlockPlan& p, const Streams& ss, const size_t* off, int K, void* ws, cudaStream_t st,
+                         const char* what) {
+  MxJob jobs[2];
+  for (int i = 0; i < ss.n; ++i) {
+    __nv_bfloat16* t = at<__nv_bfloat16>(ws, off[ss.s[i]]);
+    jobs[i].src = t, jobs[i].deq = t, jobs[i].rows = static_cast<int64_t>(p.B) * ss.rpb[i], jobs[i].K = K;
+  }
+  MMDIT_CUDA(launch_mx_cast(jobs, ss.n, st), what);
   return MMDIT_OK;
 }
 
@@ -462,7 +481,11 @@ mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss,
                                    f8.on() && !f8.current ? 1 : 0),
                "LayerNorm-modulate (attention branch)");
   }
-  if (f8.blockwise) {
+  if (f8.mx) {
+    ProfScope ps_(p.single ? "single.fp8_cast_h1" : "double.fp8_cast_h1", st);
+    mmdit_status s = mx_in_place(p, ss, p.h, p.D, ws, st, "MXFP8 cast of the QKV input");
+    if (s != MMDIT_OK) return s;
+  } else if (f8.blockwise) {
     ProfScope ps_(p.single ? "single.fp8_cast_h1" : "double.fp8_cast_h1", st);
     for (int i = 0; i < ss.n; ++i)
       MMDIT_CUDA(launch_blockwise_cast_act(at<__nv_bfloat16>(ws, p.stage[ss.s[i]]), p.B * ss.rpb[i], p.D,
@@ -485,7 +508,9 @@ mmdit_status run_qkv(const mmdit_dims* d, const BlockPlan& p, const Streams& ss,
     const mmdit_stream_w* w = ss.w[i];
     EpiArgs e;
     const void* wmat = w->w_qkv;
-    if (f8.blockwise) {
+    if (f8.mx) {
+      wmat = at(ws, p.wq[ss.s[i]] + 2 * p.wq_qkv());
+    } else if (f8.blockwise) {
       e.bw_sx = at<float>(ws, p.bw_sx[ss.s[i]]), e.bw_sw = at<float>(ws, p.bw_sw[ss.s[i]] + p.sw_qkv());
       wmat = at(ws, p.wq[ss.s[i]] + p.wq_qkv());
     } else if (f8.f) {
@@ -514,9 +539,9 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
   const int mm = f8.on() ? 2 : d->act;
   auto weight = [&](int i, int g) -> const void* {
     const mmdit_stream_w* w = ss.w[i];
-    if (!f8.on()) return g == 1 ? w->w_o : (g == 2 ? w->w_1 : w->w_2);
+    if (!f8.on() && !f8.mx) return g == 1 ? w->w_o : (g == 2 ? w->w_1 : w->w_2);
     const size_t off = g == 1 ? p.wq_o() : (g == 2 ? p.wq_1() : p.wq_2());
-    return at(ws, p.wq[ss.s[i]] + off);
+    return at(ws, p.wq[ss.s[i]] + (f8.mx ? 2 : 1) * off);
   };
   auto dequant = [&](EpiArgs& e, int i, int g) {
     if (f8.blockwise) {
@@ -534,7 +559,11 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
                what);
     return MMDIT_OK;
   };
-  if (f8.blockwise) {
+  if (f8.mx) {
+    ProfScope ps_(p.single ? "single.fp8_cast_o" : "double.fp8_cast_o", st);
+    mmdit_status s = mx_in_place(p, ss, p.o, p.D, ws, st, "MXFP8 cast of the attention output");
+    if (s != MMDIT_OK) return s;
+  } else if (f8.blockwise) {
     ProfScope ps_(p.single ? "single.fp8_cast_o" : "double.fp8_cast_o", st);
     for (int i = 0; i < ss.n; ++i) {
       mmdit_status s = cast_blockwise(i, at(ws, p.o[ss.s[i]]), p.o8[ss.s[i]], p.D,
@@ -590,7 +619,11 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
     MMDIT_CUDA(launch_ln_modulate2(d->act, 1, jobs, ss.n, p.D, d->ln_eps, st, f8.on() && !f8.current ? 1 : 0),
                "LayerNorm-modulate (MLP branch)");
   }
-  if (f8.blockwise && !p.parallel) {
+  if (f8.mx && !p.parallel) {
+    ProfScope ps_(p.single ? "single.fp8_cast_h2" : "double.fp8_cast_h2", st);
+    mmdit_status s = mx_in_place(p, ss, p.h, p.D, ws, st, "MXFP8 cast of the fc1 input");
+    if (s != MMDIT_OK) return s;
+  } else if (f8.blockwise && !p.parallel) {
     ProfScope ps_(p.single ? "single.fp8_cast_h2" : "double.fp8_cast_h2", st);
     for (int i = 0; i < ss.n; ++i) {
       mmdit_status s = cast_blockwise(i, at(ws, p.stage[ss.s[i]]), p.h[ss.s[i]], p.D, "blockwise E4M3 cast of the fc1 input");
@@ -624,7 +657,11 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
     ProfScope ps_(p.single ? "single.fc1" : "double.fc1", st);
     MMDIT_CUDA(launch_gemm(f1, status_word(ws), st), "MLP fc1 + GELU");
   }
-  if (f8.blockwise) {
+  if (f8.mx) {
+    ProfScope ps_(p.single ? "single.fp8_cast_u" : "double.fp8_cast_u", st);
+    mmdit_status s = mx_in_place(p, ss, p.u, p.F, ws, st, "MXFP8 cast of the fc2 input");
+    if (s != MMDIT_OK) return s;
+  } else if (f8.blockwise) {
     ProfScope ps_(p.single ? "single.fp8_cast_u" : "double.fp8_cast_u", st);
     for (int i = 0; i < ss.n; ++i) {
       mmdit_status s = cast_blockwise(i, at(ws, p.stage[ss.s[i]]), p.u[ss.s[i]], p.F, "blockwise E4M3 cast of the fc2 input");
@@ -665,6 +702,24 @@ mmdit_status run_post(const mmdit_dims* d, const BlockPlan& p, const Streams& ss
 mmdit_status fp8_begin(const BlockPlan& p, const Streams& ss, const Fp8& f8, int n_tensors,
                        void* ws, cudaStream_t st) {
   ProfScope ps_(p.single ? "single.fp8_cast_w" : "double.fp8_cast_w", st);
+  if (f8.mx) {
+    // every weight's MX-represented values (bf16) into the stream's wq slot, one launch
+    MxJob jobs[kMxMaxJobs];
+    int n = 0;
+    for (int i = 0; i < ss.n; ++i) {
+      const mmdit_stream_w* w = ss.w[i];
+      const void* src[4] = {w->w_qkv, w->w_o, w->w_1, w->w_2};
+      const size_t off[4] = {p.wq_qkv(), p.wq_o(), p.wq_1(), p.wq_2()};
+      const int nn[4] = {3 * p.D, p.D, p.F, p.D}, kk[4] = {p.D, p.D, p.D, p.F};
+      for (int g = 0; g < 4; ++g, ++n) {
+        jobs[n].src = static_cast<const __nv_bfloat16*>(src[g]);
+        jobs[n].deq = at<__nv_bfloat16>(ws, p.wq[ss.s[i]] + 2 * off[g]);
+        jobs[n].rows = nn[g], jobs[n].K = kk[g];
+      }
+    }
+    MMDIT_CUDA(launch_mx_cast(jobs, n, st), "MXFP8 cast of the weights");
+    return MMDIT_OK;
+  }
   if (f8.blockwise) {
     // every weight cast per 128 x 128 tile, its scales into the stream's bw_sw slot
     for (int i = 0; i < ss.n; ++i) {
@@ -764,8 +819,8 @@ mmdit_status double_block_body(const mmdit_dims* d, const BlockPlan& p, const mm
   Fp8 f8;
   f8.f = fp8;
   const int n_tensors = 2 * kFp8TensorsPerStream;
-  f8.current = p.fp8_current, f8.blockwise = p.fp8_blockwise, f8.n_tensors = n_tensors;
-  if (f8.on() && (s = fp8_begin(p, ss, f8, n_tensors, workspace, st)) != MMDIT_OK) return s;
+  f8.current = p.fp8_current, f8.blockwise = p.fp8_blockwise, f8.mx = p.fp8_mx, f8.n_tensors = n_tensors;
+  if ((f8.on() || f8.mx) && (s = fp8_begin(p, ss, f8, n_tensors, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, f8, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_post(d, p, ss, f8, workspace, st)) != MMDIT_OK) return s;
@@ -788,8 +843,8 @@ mmdit_status single_block_body(const mmdit_dims* d, const BlockPlan& p, const mm
   ss.mod[0] = w->mod ? w->mod : at<float>(workspace, p.mod[0]);
   Fp8 f8;
   f8.f = fp8;
-  f8.current = p.fp8_current, f8.blockwise = p.fp8_blockwise, f8.n_tensors = kFp8TensorsPerStream;
-  if (f8.on() && (s = fp8_begin(p, ss, f8, kFp8TensorsPerStream, workspace, st)) != MMDIT_OK) return s;
+  f8.current = p.fp8_current, f8.blockwise = p.fp8_blockwise, f8.mx = p.fp8_mx, f8.n_tensors = kFp8TensorsPerStream;
+  if ((f8.on() || f8.mx) && (s = fp8_begin(p, ss, f8, kFp8TensorsPerStream, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_qkv(d, p, ss, rope_cos, rope_sin, f8, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_attention(p, d->act, workspace, st)) != MMDIT_OK) return s;
   if ((s = run_post(d, p, ss, f8, workspace, st)) != MMDIT_OK) return s;
@@ -1904,6 +1959,33 @@ mmdit_status mmdit_fp8_blockwise_linear_fwd(int32_t M, int32_t N, int32_t K, con
                                      static_cast<const __nv_bfloat16*>(b), static_cast<__nv_bfloat16*>(y),
                                      at(workspace, kStatusBytes), status_word(workspace), st),
              "blockwise FP8 linear");
+  return MMDIT_OK;
+}
+
+size_t mmdit_fp8_mxfp8_linear_workspace_size(int32_t M, int32_t N, int32_t K) {
+  if (M < 0 || N < 1 || K < 1) return kStatusBytes;
+  return kStatusBytes + mx_linear_scratch(M, N, K);
+}
+
+mmdit_status mmdit_fp8_mxfp8_linear_fwd(int32_t M, int32_t N, int32_t K, const void* x, const void* w, const void* b,
+                                        void* y, void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 0 || N < 1 || K < 1) return fail(MMDIT_ERR_INVALID_ARG, "bad MXFP8 linear shape");
+  if (N % 32 != 0 || K % 32 != 0)
+    return fail(MMDIT_ERR_UNSUPPORTED, "MXFP8 linear needs N %% 32 == 0 and K %% 32 == 0 (got %d, %d)", N, K);
+  mmdit_status s = check_ptrs({x, w, y}, "MXFP8 linear");
+  if (s != MMDIT_OK) return s;
+  if (b && !aligned16(b)) return fail(MMDIT_ERR_INVALID_ARG, "MXFP8 linear: bias is not 16-byte aligned");
+  if ((s = check_workspace(workspace, workspace_bytes, mmdit_fp8_mxfp8_linear_workspace_size(M, N, K))) != MMDIT_OK)
+    return s;
+  if (M == 0) return MMDIT_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MMDIT_CUDA(cudaMemsetAsync(workspace, 0, 4, st), "status clear");
+  pdl_begin_call();
+  ProfScope ps_("fp8_mxfp8_linear", st);
+  MMDIT_CUDA(launch_mx_linear(M, N, K, static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(w),
+                              static_cast<const __nv_bfloat16*>(b), static_cast<__nv_bfloat16*>(y),
+                              at(workspace, kStatusBytes), status_word(workspace), st),
+             "MXFP8 linear");
   return MMDIT_OK;
 }
 

@@ -193,6 +193,32 @@ cudaError_t launch_blockwise_linear(int M, int N, int K, const __nv_bfloat16* x,
                                     const __nv_bfloat16* bias, __nv_bfloat16* y, void* scratch, uint32_t* status,
                                     cudaStream_t stream);
 
+// mxfp8.cu: MXFP8 casts (E4M3 elements, one E8M0 scale per 32 consecutive elements along K).
+// Each job casts src [rows, K] (bf16, K % 32 == 0) and writes the represented values P * 2^e
+// as bf16 into deq (may be src itself), and, when not null, the E4M3 codes [rows, K] and the
+// E8M0 scale codes e + 127 [rows, K/32].
+struct MxJob {
+  const __nv_bfloat16* src = nullptr;
+  __nv_bfloat16* deq = nullptr;
+  uint8_t* codes = nullptr;
+  uint8_t* scales = nullptr;
+  int64_t rows = 0;
+  int K = 0;
+};
+constexpr int kMxMaxJobs = 8;
+struct MxJobs {
+  MxJob j[kMxMaxJobs];
+  int n = 0;
+};
+cudaError_t launch_mx_cast(const MxJob* jobs, int n, cudaStream_t stream);
+// The MXFP8 linear y = x W^T + b (bf16 x, W, b, y): the casts of x and W into `scratch`
+// (mx_linear_scratch bytes: x values, W values (bf16), x codes, W codes, x scales, W scales,
+// each part 256-byte aligned), then the bf16 GEMM of the represented values.  K % 32 == 0.
+size_t mx_linear_scratch(int M, int N, int K);
+cudaError_t launch_mx_linear(int M, int N, int K, const __nv_bfloat16* x, const __nv_bfloat16* w,
+                             const __nv_bfloat16* bias, __nv_bfloat16* y, void* scratch, uint32_t* status,
+                             cudaStream_t stream);
+
 struct AttnBwdProblem {
   int batch = 0, heads = 0, seq = 0, seq_pad = 0;
   const __half *q = nullptr, *k = nullptr, *v = nullptr, *dout = nullptr;  // [B, H, S, 128] fp16

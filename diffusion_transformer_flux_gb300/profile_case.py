@@ -8,6 +8,7 @@
     python -m diffusion_transformer_flux_gb300.profile_case head_loss --seq-img 4096
     python -m diffusion_transformer_flux_gb300.profile_case modulation --jobs 4
     python -m diffusion_transformer_flux_gb300.profile_case blockwise_linear --m 4608 --n 12288 --k 3072
+    python -m diffusion_transformer_flux_gb300.profile_case mxfp8_linear --m 4608 --n 12288 --k 3072
 
 Inputs are drawn on the device (N(0,1) activations, N(0,0.02) weights); the case runs
 --iters times and exits 0 only if every kernel finished its waits.
@@ -35,7 +36,8 @@ def _stream_w(D, F, d=128):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["attention", "double_block", "single_block", "linear", "double_block_bwd",
-                                     "fp8_attention", "head_loss", "modulation", "blockwise_linear"])
+                                     "fp8_attention", "head_loss", "modulation", "blockwise_linear",
+                                     "mxfp8_linear"])
     ap.add_argument("--jobs", type=int, default=4)
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--seq", type=int, default=4608)
@@ -84,6 +86,10 @@ def main():
         x, w, b = _w(a.m, a.k, std=1.0), _w(a.n, a.k), _w(a.n)
         y = torch.empty(a.m, a.n, device="cuda", dtype=torch.bfloat16)
         run = lambda: wss.append(L.mmdit_fp8_blockwise_linear_fwd(x, w, b, y))
+    elif a.case == "mxfp8_linear":
+        x, w, b = _w(a.m, a.k, std=1.0), _w(a.n, a.k), _w(a.n)
+        y = torch.empty(a.m, a.n, device="cuda", dtype=torch.bfloat16)
+        run = lambda: wss.append(L.mmdit_fp8_mxfp8_linear_fwd(x, w, b, y))
     else:
         B, Si, St, D, F = a.batch, a.seq_img, a.seq_txt, a.hidden, a.mlp
         S = Si + St

@@ -79,11 +79,18 @@ typedef enum mmdit_act_dtype { MMDIT_F32 = 0, MMDIT_BF16 = 1 } mmdit_act_dtype;
  * with its own scale 448 / amax, and the GEMMs rescale each 128-wide K slice's product before
  * their usual epilogues.  Nothing is kept between calls: the fp8 state argument must be NULL.
  * Needs hidden % 128 == 0 and mlp_hidden % 128 == 0; not for the parallel single block. */
+/* FP8_MXFP8 = the same four linears under the MXFP8 recipe ([FP8] §Configuration, fp8_recipe
+ * "mxfp8"; the arithmetic of mmdit_fp8_mxfp8_linear_fwd): each input, written in bf16, and each
+ * weight are cast per 32 consecutive elements along K to E4M3 with a shared power-of-two scale,
+ * and the linears multiply the values those casts represent (bf16 tensor cores, fp32 sums).
+ * Nothing is kept between calls: the fp8 state argument must be NULL.  Needs
+ * mlp_hidden % 128 == 0. */
 typedef enum mmdit_gemm_mode {
   MMDIT_GEMM_NATIVE = 0,
   MMDIT_GEMM_FP8_E4M3 = 1,
   MMDIT_GEMM_FP8_TENSORWISE = 2,
-  MMDIT_GEMM_FP8_BLOCKWISE = 3
+  MMDIT_GEMM_FP8_BLOCKWISE = 3,
+  MMDIT_GEMM_FP8_MXFP8 = 4
 } mmdit_gemm_mode;
 
 /* Shapes and options of one block call ([API] §Configuration, FluxConfig). */
@@ -443,6 +450,25 @@ size_t mmdit_fp8_blockwise_linear_workspace_size(int32_t M, int32_t N, int32_t K
 mmdit_status mmdit_fp8_blockwise_linear_fwd(int32_t M, int32_t N, int32_t K, const void *x, const void *w,
                                             const void *b, void *y, void *workspace, size_t workspace_bytes,
                                             void *stream);
+
+/* MXFP8 linear ([FP8] §Configuration › FP8 model configuration, fp8_recipe "mxfp8"; the page
+ * names the recipe only, read as the OCP Microscaling formats v1.0 MXFP8 with E4M3 elements).
+ * y = x W^T + b where x [M, K] and W [N, K] are each cast in blocks of 32 consecutive elements
+ * along K: a block with largest magnitude amax gets the shared exponent
+ * e = floor(log2 amax) - 8, clamped to [-127, 127] (-127 for a block of zeros), and each of its
+ * elements v is stored as the E4M3 code P = E4M3(v / 2^e) (nearest even, saturating at 448),
+ * standing for P * 2^e.  The product of those represented values accumulates in fp32 on the
+ * tensor cores (exactly formed bf16 products; exact for every block whose amax is at least
+ * 2^-116), then b is added.  x, W, b (NULL: none) and y are bf16, 16-byte aligned, finite;
+ * N % 32 == 0, K % 32 == 0; M == 0 is a no-op.  The workspace (at least
+ * mmdit_fp8_mxfp8_linear_workspace_size bytes) holds after its 256-byte status word, each part
+ * starting on a 256-byte boundary: the represented values of x [M, K] and of W [N, K] (bf16),
+ * the E4M3 codes of x [M, K] and of W [N, K], and the E8M0 scale codes e + 127 of x [M, K/32]
+ * and of W [N, K/32] (one byte each), readable after the call. */
+size_t mmdit_fp8_mxfp8_linear_workspace_size(int32_t M, int32_t N, int32_t K);
+mmdit_status mmdit_fp8_mxfp8_linear_fwd(int32_t M, int32_t N, int32_t K, const void *x, const void *w,
+                                        const void *b, void *y, void *workspace, size_t workspace_bytes,
+                                        void *stream);
 
 /* ---------------------------------------------------------------------------------------
  * Backward of the FP8 linear ([FP8] §Configuration, FP8 model configuration: fp8 "e4m3" or

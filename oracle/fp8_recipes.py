@@ -209,3 +209,20 @@ def mxfp8_linear(x, w, b, block: int = MX_BLOCK):
         scale = np.ldexp(1.0, ex[..., j][..., None] + ew[:, j])
         y += scale * (px[..., sl] @ pw[:, sl].T)
     return y if b is None else y + np.asarray(b, np.float64)
+
+
+class MxScaling:
+    """The MXFP8 recipe as the block oracle's ``fp8`` object (``oracle.flux.block_linear`` calls
+    ``linear``): every linear is ``mxfp8_linear`` of its input and weight, with no state.
+    ``act_cast``, if given, is applied to a linear's input first (the value it holds as a stored
+    activation tensor, as for ``TensorwiseScaling``)."""
+
+    def __init__(self, act_cast=None, block: int = None):
+        self.act_cast = act_cast
+        self.block = MX_BLOCK if block is None else block
+
+    def linear(self, name, x, w, b):
+        x = np.asarray(x, np.float64)
+        if self.act_cast is not None:
+            x = np.asarray(self.act_cast(x), np.float64)
+        return mxfp8_linear(x, w, b, self.block)

@@ -99,6 +99,15 @@ def test_validation_errors_before_any_launch(lib):
     assert lib.mmdit_double_block_fwd(C.byref(bwd), C.byref(w), C.byref(w), None, None, None, None,
                                       None, None, None, C.byref(stb), None, 0, None) == 1
     assert "blockwise" in L.last_error()
+    # nor does the MXFP8 recipe
+    mxd = _dims(gemm=L.MMDIT_GEMM_FP8_MXFP8, act=1)
+    assert lib.mmdit_double_block_fwd(C.byref(mxd), C.byref(w), C.byref(w), None, None, None, None,
+                                      None, None, None, C.byref(stb), None, 0, None) == 1
+    assert "MXFP8" in L.last_error()
+    # and the modes after it are unknown
+    assert lib.mmdit_double_block_fwd(C.byref(_dims(gemm=5, act=1)), C.byref(w), C.byref(w), None, None, None,
+                                      None, None, None, None, None, None, 0, None) == 1
+    assert "gemm mode" in L.last_error()
     # an FP8 state with too few tensors for a double block, or a position outside the history
     st8 = L.Fp8State(0x1000, 0x2000, 1024, 8, 0, 0, 0)
     assert lib.mmdit_double_block_fwd(C.byref(fp8), C.byref(w), C.byref(w), None, None, None, None,
@@ -317,6 +326,21 @@ def test_blockwise_fp8_linear_rejects_bad_arguments_before_any_cuda_call(lib):
     assert "blockwise FP8 linear" in L.last_error()
     assert f(300, 256, 512, 16, 16, 0x1008, 16, 256, 1 << 30, None) == 1   # bias alignment
     assert f(300, 256, 512, 16, 16, None, 16, 256, need - 1, None) == 3
+
+
+def test_mxfp8_linear_rejects_bad_arguments_before_any_cuda_call(lib):
+    need = L.mmdit_fp8_mxfp8_linear_workspace_size(300, 96, 512)
+    # status word; bf16 values of x and W; codes of x and W; E8M0 scales of x and W; each part on
+    # a 256-byte boundary
+    assert need == 256 + 307200 + 98304 + 153600 + 49152 + 4864 + 1536
+    f = lib.mmdit_fp8_mxfp8_linear_fwd
+    assert f(300, 80, 512, 16, 16, None, 16, 256, 1 << 30, None) == 2       # N % 32
+    assert f(300, 96, 500, 16, 16, None, 16, 256, 1 << 30, None) == 2       # K % 32
+    assert f(-1, 96, 512, 16, 16, None, 16, 256, 1 << 30, None) == 1
+    assert f(300, 96, 512, 16, None, None, 16, 256, 1 << 30, None) == 1
+    assert "MXFP8 linear" in L.last_error()
+    assert f(300, 96, 512, 16, 16, 0x1008, 16, 256, 1 << 30, None) == 1    # bias alignment
+    assert f(300, 96, 512, 16, 16, None, 16, 256, need - 1, None) == 3
 
 
 def test_training_pair_rejects_bad_arguments_before_any_cuda_call(lib):

@@ -629,11 +629,11 @@ def test_blockwise_fp8_linear(M, N, K):
     assert d_gpu <= 0.25 * d_fp8
 
 
-def _blockwise_block_run(case):
-    """One call of the block with gemm = MMDIT_GEMM_FP8_BLOCKWISE (no FP8 state)."""
+def _blockwise_block_run(case, gemm=L.MMDIT_GEMM_FP8_BLOCKWISE):
+    """One call of the block with a stateless recipe (gemm = MMDIT_GEMM_FP8_BLOCKWISE or
+    MMDIT_GEMM_FP8_MXFP8; no FP8 state)."""
     dims = L.make_dims(case.B, case.S_i, case.S_t, case.D, case.H, case.F, L.MMDIT_BF16,
-                       rope_interleaved=case.interleaved, gelu_tanh=case.gelu_tanh,
-                       gemm=L.MMDIT_GEMM_FP8_BLOCKWISE)
+                       rope_interleaved=case.interleaved, gelu_tanh=case.gelu_tanh, gemm=gemm)
     ids = torch.from_numpy(case.ids).cuda()
     cos = torch.empty(case.B, case.S, 64, device="cuda")
     sin = torch.empty_like(cos)
@@ -672,3 +672,91 @@ def test_fp8_blockwise_block_small(B, S_i, S_t, D, H, F, single):
         y8 = O.double_block(case.x_img, case.x_txt, case.vec, case.cos, case.sin, case.w_img, case.w_txt,
                             case.H, **args)
     _check_norm_wise(y, y8, case.oracle(None), "FP8 blockwise block")
+
+
+# ----------------------------------------------------------------------------- MXFP8 recipe
+def _mx_parts(ws, M, N, K):
+    """The represented values, codes and scale codes the call leaves in its workspace (layout
+    stated in include/mmdit.h)."""
+    raw = ws.cpu().numpy().view(np.uint8)
+
+    def bf16_at(off, n):
+        return (raw[off:off + 2 * n].view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+    off = 256
+    xd = bf16_at(off, M * K).reshape(M, K)
+    off += _ru256(2 * M * K)
+    wd = bf16_at(off, N * K).reshape(N, K)
+    off += _ru256(2 * N * K)
+    xq = raw[off:off + M * K].reshape(M, K)
+    off += _ru256(M * K)
+    wq = raw[off:off + N * K].reshape(N, K)
+    off += _ru256(N * K)
+    xs = raw[off:off + M * (K // 32)].reshape(M, K // 32)
+    off += _ru256(M * (K // 32))
+    wsc = raw[off:off + N * (K // 32)].reshape(N, K // 32)
+    return xd, wd, xq, wq, xs, wsc
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 96, 512), (1024, 3072, 3072)])
+def test_mxfp8_linear(M, N, K):
+    """[FP8] §Configuration, fp8_recipe "mxfp8" (oracle.fp8_recipes.mxfp8_quantize / mxfp8_linear,
+    the OCP MX v1.0 reading): the casts are bit-exact against the oracle's -- the E4M3 codes, the
+    E8M0 scale codes and the represented values P 2^e -- with an outlier, a quotient above 448
+    that saturates, a block of zeros and a block near 2^-100; the GEMM agrees with the float64
+    product of the GPU's represented values to fp32 accumulation and the bf16 output rounding;
+    and the whole linear sits far closer to the oracle's recipe than that recipe sits to the
+    exact product (max norm)."""
+    from oracle import fp8_recipes as R
+    rng = np.random.default_rng(M + 3 * N)
+    x = synth.bf16_round(rng.standard_normal((M, K)).astype(np.float32))
+    x[7, 200] = 300.0                               # an outlier owns its block's exponent
+    x[9, 96] = 480.0                                # e = 0 and 480 > 448: saturates
+    x[3, 64:96] = 0.0                               # a block of zeros: e = -127, codes 0
+    x[5, 32:64] = synth.bf16_round(x[5, 32:64] * np.float32(2.0 ** -100))
+    w = synth.bf16_round((rng.standard_normal((N, K)) * 0.02).astype(np.float32))
+    w[10, :32] = 0.0
+    b = synth.bf16_round((rng.standard_normal(N) * 0.1).astype(np.float32))
+    y = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+    ws = L.mmdit_fp8_mxfp8_linear_fwd(dev(x), dev(w), dev(b), y)
+    torch.cuda.synchronize()
+    assert L.mmdit_workspace_status(ws) == 0
+    xd, wd, xq, wq, xs, wsc = _mx_parts(ws, M, N, K)
+    dec = np.array([E.e4m3_decode(c) for c in range(256)])
+    for name, src, vals, codes, scales in (("x", x, xd, xq, xs), ("W", w, wd, wq, wsc)):
+        p, e = R.mxfp8_quantize(src.astype(np.float64))
+        assert np.array_equal(scales.astype(np.int64) - 127, e), name
+        assert np.array_equal(dec[codes], p), name
+        assert np.array_equal(vals.astype(np.float64), R.mxfp8_dequantize(p, e)), name
+    assert xs[3, 2] == 0 and not xq[3, 64:96].any() and dec[xq[9, 96]] == 448.0
+    # the GEMM from the GPU's represented values, in float64
+    got = host(y)
+    ref = xd.astype(np.float64) @ wd.astype(np.float64).T + b
+    assert_parity(got, ref, 1e-3, f"MXFP8 GEMM {M}x{N}x{K}", out_bf16=True)
+    # the whole linear against the oracle's recipe and the exact product
+    y_or = R.mxfp8_linear(x, w, b)
+    y_ex = x.astype(np.float64) @ w.astype(np.float64).T + b
+    rms = float(np.sqrt(np.mean(y_ex ** 2)))
+    d_gpu = float(np.abs(got - y_or).max()) / rms
+    d_fp8 = float(np.abs(y_or - y_ex).max()) / rms
+    print(f"[fp8 mxfp8] {M}x{N}x{K}: max|GPU - recipe|/RMS {d_gpu:.3e}, max|recipe - exact|/RMS {d_fp8:.3e}")
+    assert d_gpu <= 0.25 * d_fp8
+
+
+@pytest.mark.parametrize("B,S_i,S_t,D,H,F,single", SMALL)
+def test_fp8_mxfp8_block_small(B, S_i, S_t, D, H, F, single):
+    """The MXFP8 recipe inside the blocks ("FP8 training for Flux models", §Configuration,
+    fp8_recipe "mxfp8"): every linear's bf16 input and its weight cast per 32 elements along K,
+    no state.  The block output under the FP8 bars against the exact MXFP8 evaluation
+    (oracle.fp8_recipes.MxScaling on bf16-stored inputs) and the float64 block."""
+    from oracle import fp8_recipes as R
+    case = BlockCase(B, S_i, S_t, D, H, F, "bf16", seed=61 + S_i + D, std=0.05, single=single)
+    y = _blockwise_block_run(case, gemm=L.MMDIT_GEMM_FP8_MXFP8)
+    mx = R.MxScaling(act_cast=O.round_bf16)
+    args = dict(mm_cast=O.round_bf16, fp8=mx, interleaved=case.interleaved, gelu_tanh=case.gelu_tanh)
+    if single:
+        y8 = (O.single_block(case.x_joint(), case.vec, case.cos, case.sin, case.w_img, case.H, **args),)
+    else:
+        y8 = O.double_block(case.x_img, case.x_txt, case.vec, case.cos, case.sin, case.w_img, case.w_txt,
+                            case.H, **args)
+    _check_norm_wise(y, y8, case.oracle(None), "FP8 MXFP8 block")

@@ -321,3 +321,21 @@ def test_blockwise_scaling_object_is_the_recipe_on_the_stored_input():
     wg[0, 0] = 448.0
     wg[0, 128] = 448.0
     np.testing.assert_array_equal(R.BlockwiseScaling().linear("o", xg, wg, None), xg @ wg.T)
+
+
+def test_mx_scaling_object_is_the_recipe_on_the_stored_input():
+    # the block oracle's fp8 object: mxfp8_linear of the act_cast input, and exact wherever every
+    # 32-element block already holds E4M3 values whose maximum lies in [256, 448] (shared
+    # exponent 0: nothing is rescaled or rounded)
+    from oracle import flux as O
+    x = RNG.standard_normal((2, 5, 128))
+    w = RNG.standard_normal((64, 128)) * 0.02
+    b = RNG.standard_normal(64)
+    mx = R.MxScaling(act_cast=O.round_bf16)
+    np.testing.assert_array_equal(mx.linear("qkv", x, w, b), R.mxfp8_linear(O.round_bf16(x), w, b))
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 448.0])
+    xg = RNG.choice(grid, size=(3, 128)) * RNG.choice([-1.0, 1.0], size=(3, 128))
+    xg[:, ::32] = 448.0
+    wg = RNG.choice(grid, size=(64, 128))
+    wg[:, ::32] = 256.0
+    np.testing.assert_array_equal(R.MxScaling().linear("o", xg, wg, None), xg @ wg.T)
