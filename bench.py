@@ -518,8 +518,10 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- per-kernel roofline
-def kernel_work(label: str, wl):
-    """(bound, algorithmic amount per launch, unit) of one library step, from the workload shapes."""
+def kernel_work(label: str, wl, recipe: str = "delayed"):
+    """(bound, algorithmic amount per launch, unit) of one library step, from the workload shapes.
+    The FP8 casts move 3 B per element (bf16 in, E4M3 out) under the E4M3 recipes and 4 B under
+    MXFP8 (bf16 in, the represented values out in bf16)."""
     B, D, F, H = wl.batch, wl.hidden, wl.mlp_hidden, wl.heads
     S_i, S_t = wl.seq_img, wl.seq_txt
     S = S_i + S_t
@@ -544,11 +546,14 @@ def kernel_work(label: str, wl):
             return "hbm", r * D * 2 + r * D * e_mm, "B"
         if op == "ln2":
             return "hbm", r * D * 4 + r * D * e_mm, "B"
-        if op == "fp8_cast_w":  # every weight of the block's streams: bf16 in, E4M3 out
+        cast_b = 4.0 if recipe == "mxfp8" else 3.0
+        if op == "fp8_cast_w":  # every weight of the block's streams
             sets = 2 if parts[0] == "double" else 1
-            return "hbm", sets * 3.0 * (4 * D * D + 2 * F * D), "B"
-        if op == "fp8_cast_o":  # the attention output of every row: bf16 in, E4M3 out
-            return "hbm", 3.0 * B * S * D, "B"
+            return "hbm", sets * cast_b * (4 * D * D + 2 * F * D), "B"
+        if op in ("fp8_cast_o", "fp8_cast_h1", "fp8_cast_h2"):  # a D-wide input of every row
+            return "hbm", cast_b * B * S * D, "B"
+        if op == "fp8_cast_u":  # the fc2 input of every row
+            return "hbm", cast_b * B * S * F, "B"
         if op == "fp8_scale":
             return "latency", 0.0, ""
     n_lat = B * wl.channels * S_i
@@ -1137,7 +1142,7 @@ def main():
 
     per_kernel = []
     for name, (n, t) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
-        bound, amount, unit = kernel_work(name, wl)
+        bound, amount, unit = kernel_work(name, wl, args.fp8_recipe)
         avg_s = t / n / 1e3
         row = {"kernel": name, "launches": n, "avg_us": round(avg_s * 1e6, 2), "share": round(t / prof_total, 4),
                "bound": bound}
@@ -1149,7 +1154,7 @@ def main():
             row["frac"] = round(amount / avg_s / 1e9 / hbm_peak, 4)
         per_kernel.append(row)
     dom = per_kernel[0]
-    bound, amount, unit = kernel_work(dom["kernel"], wl)
+    bound, amount, unit = kernel_work(dom["kernel"], wl, args.fp8_recipe)
     dom_s = dom["avg_us"] / 1e6
     if bound == "tensor":
         ach, peak, runit = amount / dom_s / 1e12, peak_of(dom["kernel"]), "TFLOP/s"

@@ -31,6 +31,13 @@ def test_kernel_work_of_labelled_steps():
     assert (bound, unit) == ("hbm", "B")
     assert amount / 1e9 == pytest.approx(8.61, abs=0.01)  # 76 streams x 6D x D bf16 weights
     assert bench.kernel_work("no.such.step", wl)[0] == "unknown"
+    # the FP8 casts: bf16 in and E4M3 out (3 B per element), or under MXFP8 the represented values
+    # out in bf16 (4 B)
+    f8 = synth.WORKLOADS["flux12b_2048px_fp8"]
+    rows = f8.batch * (f8.seq_img + f8.seq_txt)
+    assert bench.kernel_work("single.fp8_cast_u", f8) == ("hbm", 3.0 * rows * f8.mlp_hidden, "B")
+    assert bench.kernel_work("double.fp8_cast_h1", f8, "mxfp8")[1] == 4.0 * rows * f8.hidden
+    assert bench.kernel_work("double.fp8_cast_w", f8, "mxfp8")[1] == 2 * 4.0 * (4 * 3072 ** 2 + 2 * 12288 * 3072)
 
 
 def test_committed_traffic_is_used_only_on_the_sources_it_was_taken_on(monkeypatch):
