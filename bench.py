@@ -220,6 +220,7 @@ class DeviceStep:
         # the prediction is written only when asked for (the step's result is the loss)
         self.pred = torch.empty_like(self.z0) if keep_pred else None
         self.dims = L.make_dims(B, S_i, S_t, D, H, F, L.MMDIT_BF16)
+        self.embed_stream = torch.cuda.Stream(device)
         self.dims_final = L.make_dims(B, S_i, 0, D, H, F, L.MMDIT_BF16)
         ws_block = max(L.mmdit_double_block_workspace_size(self.dims),
                        L.mmdit_single_block_workspace_size(self.dims))
@@ -253,12 +254,17 @@ class DeviceStep:
         L, wl, side = self.L, self.wl, self.mods
         S_i = self.S_i
         side.compute()  # every modulation of the step, one launch
+        # img_in on a second stream beside the RoPE tables and txt_in: neither fills the GPU alone
+        main = self.torch.cuda.current_stream()
+        self.embed_stream.wait_stream(main)
+        with self.torch.cuda.stream(self.embed_stream):
+            # z_t = (1 - t) z0 + t z1 formed while patchifying, then projected
+            L.mmdit_img_in_noise_fwd(self.z0, self.z1, self.t, self.img_in["w"], self.img_in["b"], self.x_img,
+                                     ws=self.ws_img)
         L.rope3d_freqs(self.ids, AXES, THETA, self.cos, self.sin)
-        # z_t = (1 - t) z0 + t z1 formed while patchifying, then projected
-        L.mmdit_img_in_noise_fwd(self.z0, self.z1, self.t, self.img_in["w"], self.img_in["b"], self.x_img,
-                                 ws=self.ws_img)
         if self.txt_in is not None:
             L.mmdit_linear_fwd(self.txt, self.txt_in["w"], self.txt_in["b"], self.x_txt, ws=self.ws_lin)
+        main.wait_stream(self.embed_stream)
         L.mmdit_double_block_fwd(self.dims, side.weights("dimg", self.w_dimg), side.weights("dtxt", self.w_dtxt),
                                  self.vec, self.cos, self.sin, self.x_img, self.x_txt,
                                  self.y_img, self.y_txt, ws=self.ws_block)
@@ -1228,7 +1234,11 @@ def main():
                                 + "output head with the flow-matching loss fused on"
                                 + ("" if wl.batch == 1 else "; streams joined and split by strided "
                                    "copy-engine copies (mmdit_copy_rows)")),
-                       "streams": "one stream; every modulation of the step runs first, in one "
+                       "streams": ("two streams: every modulation of the step first, in one launch "
+                                   "(mmdit_modulation_batched_fwd), then img_in on a second stream beside the "
+                                   "RoPE tables and txt_in, joined before the double block")
+                                  if type(st) is DeviceStep else
+                                  "one stream; every modulation of the step runs first, in one "
                                   "launch (mmdit_modulation_batched_fwd)",
                        "flops_counted_per_step": st.flops_blocks,
                        "dense_flops_per_step_incl_embeds_and_head": st.flops_dense},
