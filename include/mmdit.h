@@ -342,7 +342,11 @@ mmdit_status mmdit_copy_rows(void *dst, int64_t dst_stride, const void *src, int
  * Joint softmax attention ([ARCH] §Implementation details, Attention implementation (no mask)
  * and Joint Attention Trick).  out[b, s, h*d + j] = sum_t softmax_t(q_s . k_t / sqrt(d)) v_t[j]
  * for each (b, h), over all S keys.  q, k, v [B, H, S, d] bf16; out [B, S, H*d] of type
- * `act`.  d must be 128.  workspace >= mmdit_attention_workspace_size(B, H, S). */
+ * `act`.  d must be 128.  workspace >= mmdit_attention_workspace_size(B, H, S).
+ * Range: the PV product runs on fp16 operands (the probabilities and V, which fp16 holds exactly
+ * for every bf16 value with 2^-14 <= |v| <= 65504).  A |v| above 65504 overflows to an infinite
+ * output; a |v| below 2^-14 keeps fewer bits (an absolute error of at most 2^-25 per key weight).
+ * The blocks' V, written by their QKV epilogue, is read the same way. */
 size_t mmdit_attention_workspace_size(int32_t batch, int32_t heads, int32_t seq);
 mmdit_status mmdit_attention_fwd(int32_t act, int32_t batch, int32_t heads, int32_t seq,
                                  int32_t head_dim, const void *q, const void *k, const void *v,

@@ -153,6 +153,26 @@ def test_attention_matches_oracle(B, H, S, qscale, act):
     assert_parity(got, ref64, 5e-2, f"attention B={B} H={H} S={S} vs float64")
 
 
+@pytest.mark.parametrize("vscale", [6e4, 2.0 ** -10])
+def test_attention_v_at_the_ends_of_its_fp16_range(vscale):
+    """The PV product reads V in fp16 (the header states the range): V uniform in +-60000 (close to
+    fp16's largest finite 65504) and V near 2^-10 (above fp16's smallest normal) both meet the bar
+    against the oracle, which keeps V exact."""
+    B, H, S = 1, 2, 700
+    rng = np.random.default_rng(int(vscale) + 5)
+    q = synth.bf16_round(rng.standard_normal((B, H, S, 128)).astype(np.float32))
+    k = synth.bf16_round(rng.standard_normal((B, H, S, 128)).astype(np.float32))
+    v = synth.bf16_round((rng.uniform(-1.0, 1.0, (B, H, S, 128)) * vscale).astype(np.float32))
+    out = torch.empty(B, S, H * 128, device="cuda", dtype=torch.bfloat16)
+    ws = L.mmdit_attention_fwd(dev(q), dev(k), dev(v), out)
+    torch.cuda.synchronize()
+    assert L.mmdit_workspace_status(ws) == 0
+    got = host(out)
+    assert np.isfinite(got).all()
+    ref = O.attention(q, k, v, O.round_bf16).transpose(0, 2, 1, 3).reshape(B, S, H * 128)
+    assert_parity(got, ref, 2e-2, f"attention with |V| up to {vscale:g}", out_bf16=True)
+
+
 # ----------------------------------------------------------------------------- embeddings / head
 @pytest.mark.parametrize("act", ["bf16", "f32"])
 def test_img_in_matches_oracle(act):
