@@ -221,6 +221,7 @@ class DeviceStep:
         self.pred = torch.empty_like(self.z0) if keep_pred else None
         self.dims = L.make_dims(B, S_i, S_t, D, H, F, L.MMDIT_BF16)
         self.embed_stream = torch.cuda.Stream(device)
+        self.copy_stream = torch.cuda.Stream(device)
         self.dims_final = L.make_dims(B, S_i, 0, D, H, F, L.MMDIT_BF16)
         ws_block = max(L.mmdit_double_block_workspace_size(self.dims),
                        L.mmdit_single_block_workspace_size(self.dims))
@@ -249,13 +250,17 @@ class DeviceStep:
         self.L.mmdit_copy_rows(dst.data_ptr() + dst_off * e, dst.shape[1] * e, src.data_ptr() + src_off * e,
                                src.shape[1] * e, rows_per_sample * e, self.B)
 
-    def step(self):
-        """One pass of the hot path; every computation runs in libmmdit.so kernels."""
+    def step(self, before_embed=None):
+        """One pass of the hot path; every computation runs in libmmdit.so kernels.
+        `before_embed`, if given, runs on the host after the modulations are enqueued and before
+        anything that reads the other inputs (the end-to-end step waits there for its copies)."""
         L, wl, side = self.L, self.wl, self.mods
         S_i = self.S_i
         side.compute()  # every modulation of the step, one launch
-        # img_in on a second stream beside the RoPE tables and txt_in: neither fills the GPU alone
         main = self.torch.cuda.current_stream()
+        if before_embed is not None:
+            before_embed()
+        # img_in on a second stream beside the RoPE tables and txt_in: neither fills the GPU alone
         self.embed_stream.wait_stream(main)
         with self.torch.cuda.stream(self.embed_stream):
             # z_t = (1 - t) z0 + t z1 formed while patchifying, then projected
@@ -299,7 +304,29 @@ class DeviceStep:
 
     def step_from_host(self, pinned: dict, result_host):
         """The same step with this step's inputs copied from pinned host memory and the result
-        read back, all on the current stream."""
+        read back.  The copies run on a copy stream that starts after everything before the
+        step: vec first, on which the modulations (the step's first launch) wait alone, then the
+        rest, on which the embeddings wait; the loss comes back on the step's stream."""
+        torch = self.torch
+        main = torch.cuda.current_stream()
+        cs = self.copy_stream
+        cs.wait_stream(main)
+        with torch.cuda.stream(cs):
+            self.vec.copy_(pinned["vec"], non_blocking=True)
+            vec_in = torch.cuda.Event()
+            vec_in.record(cs)
+            for name, src in pinned.items():
+                if name != "vec":
+                    getattr(self, name).copy_(src, non_blocking=True)
+            all_in = torch.cuda.Event()
+            all_in.record(cs)
+        main.wait_event(vec_in)
+        self.step(before_embed=lambda: main.wait_event(all_in))
+        result_host.copy_(self.result(), non_blocking=True)
+
+    def copy_then_step(self, pinned: dict, result_host):
+        """The step with every input copied from pinned host memory first and the result read
+        back, all on the current stream."""
         for name, src in pinned.items():
             getattr(self, name).copy_(src, non_blocking=True)
         self.step()
@@ -363,6 +390,7 @@ class Fp8BlockStep(DeviceStep):
         self.flops_linears = 2 * 2 * B * S * D * (3 * D + D + 2 * F)
 
     input_names = ("X", "vec", "ids")
+    step_from_host = DeviceStep.copy_then_step
 
     def workspaces(self):
         return (self.ws_block,)
@@ -448,6 +476,7 @@ class ModelStep(DeviceStep):
                             + 2 * B * S_i * D * wl.channels)
 
     input_names = ("z0", "z1", "t", "txt", "y", "ids")
+    step_from_host = DeviceStep.copy_then_step
 
     def workspaces(self):
         return (self.ws_model, self.ws_flow)
@@ -1117,6 +1146,13 @@ def main():
         st.step_from_host(pinned, result_host)
     ms_e2e, _ = timed(lambda: st.step_from_host(pinned, result_host), args.steps)
     e2e_s = max_over_ranks(dist, sum(ms_e2e) / 1e3, device)
+    # the end-to-end step's result against a plain step of the same (now resident) inputs
+    torch.cuda.synchronize()
+    e2e_result = result_host.clone()
+    st.step()
+    torch.cuda.synchronize()
+    if not torch.equal(e2e_result, st.result().cpu()):
+        raise RuntimeError("the end-to-end step's result differs from the plain step's")
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
     d2h = result_host.numel() * result_host.element_size()
 
@@ -1255,7 +1291,13 @@ def main():
             "clocks": clocks,
             "e2e": {"value": round(whole_job_tflops(st.flops_blocks, args.steps, world, e2e_s), 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": round(e2e_s / args.steps * 1e3, 4)},
+                    "ms_per_step": round(e2e_s / args.steps * 1e3, 4),
+                    "copies": ("each step's inputs on a copy stream inside the timed region (vec first: "
+                               "the modulations wait for it alone, the embeddings for the rest); plain "
+                               "calls, no graph; the result checked bit-equal to a plain step's")
+                              if type(st) is DeviceStep else
+                              ("each step's inputs on the step's stream before the step; plain calls, "
+                               "no graph; the result checked bit-equal to a plain step's")},
             "gpu_launches": launches,
             "roofline": roofline,
             "per_kernel": per_kernel,
