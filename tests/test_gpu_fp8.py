@@ -760,3 +760,28 @@ def test_fp8_mxfp8_block_small(B, S_i, S_t, D, H, F, single):
         y8 = O.double_block(case.x_img, case.x_txt, case.vec, case.cos, case.sin, case.w_img, case.w_txt,
                             case.H, **args)
     _check_norm_wise(y, y8, case.oracle(None), "FP8 MXFP8 block")
+
+
+@pytest.mark.parametrize("recipe,single", [("mxfp8", False), ("blockwise", True)])
+def test_stateless_fp8_blocks_at_2048px_sampled_rows(recipe, single):
+    """The 12B block shapes at 2048 px (16384 image + 512 text tokens, batch 1) under the MXFP8
+    and blockwise recipes, in the launch configuration the benchmark times, on seeded rows.  Both
+    recipes scale activations within a row (1 x 32 or 1 x 128 blocks along K) and weights as a
+    whole, so the oracle evaluated on the sampled rows casts exactly what the GPU cast there."""
+    from oracle import fp8_recipes as R
+    case = BlockCase(1, 128 * 128, 512, 3072, 24, 12288, "bf16", seed=1014 + single, std=0.02,
+                     gain_jitter=0.0, lat_hw=(128, 128), single=single)
+    gemm = L.MMDIT_GEMM_FP8_MXFP8 if recipe == "mxfp8" else L.MMDIT_GEMM_FP8_BLOCKWISE
+    y = _blockwise_block_run(case, gemm=gemm)
+    rows = (_sample(case.S, 96, 7),) if single else (_sample(case.S_i, 64, 7), _sample(case.S_t, 32, 8))
+    obj = (R.MxScaling if recipe == "mxfp8" else R.BlockwiseScaling)(act_cast=O.round_bf16)
+    args = dict(mm_cast=O.round_bf16, fp8=obj, interleaved=case.interleaved, gelu_tanh=case.gelu_tanh)
+    if single:
+        y8 = (O.single_block_rows(case.x_joint(), case.vec, case.cos, case.sin, case.w_img, case.H, rows[0],
+                                  **args),)
+    else:
+        y8 = O.double_block_rows(case.x_img, case.x_txt, case.vec, case.cos, case.sin, case.w_img, case.w_txt,
+                                 case.H, rows[0], rows[1], **args)
+    y64 = case.oracle_rows(*rows, mm_cast=None)
+    got = [g[:, r] for g, r in zip(y, rows)]
+    _check_norm_wise(got, y8, y64, f"FP8 {recipe} block at 2048 px")
