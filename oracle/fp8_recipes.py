@@ -201,13 +201,12 @@ def mxfp8_dequantize(p, e, block: int = MX_BLOCK):
 
 
 def mxfp8_linear(x, w, b, block: int = MX_BLOCK):
-    """y = sum over K blocks j of 2^(e_x[row, j] + e_w[n, j]) * P_x,j P_w,j^T + b."""
+    """y = X_x W_x^T + b with X_x, W_x the values the two MXFP8 tensors stand for (P * 2^e), that
+    is the sum over K blocks j of 2^(e_x[row, j] + e_w[n, j]) * P_x,j P_w,j^T; every product is
+    exact in float64, so one product of the represented values gives the same sums."""
     px, ex = mxfp8_quantize(x, block)
     pw, ew = mxfp8_quantize(w, block)
-    y = np.zeros(px.shape[:-1] + (pw.shape[0],))
-    for j, sl in enumerate(_slices(px.shape[-1], block)):
-        scale = np.ldexp(1.0, ex[..., j][..., None] + ew[:, j])
-        y += scale * (px[..., sl] @ pw[:, sl].T)
+    y = mxfp8_dequantize(px, ex, block) @ mxfp8_dequantize(pw, ew, block).T
     return y if b is None else y + np.asarray(b, np.float64)
 
 
