@@ -79,8 +79,8 @@ MUTATIONS = [
      "p[..., sl] = e4m3_quantize(np.ldexp(part, -ej[..., None]))",
      "p[..., sl] = e4m3_quantize(np.ldexp(part, ej[..., None]))"),
     ("fp8_recipes.py", "MX linear takes the input's block exponent twice",
-     "scale = np.ldexp(1.0, ex[..., j][..., None] + ew[:, j])",
-     "scale = np.ldexp(1.0, 2 * ex[..., j][..., None] + 0 * ew[:, j])"),
+     "y = mxfp8_dequantize(px, ex, block) @ mxfp8_dequantize(pw, ew, block).T",
+     "y = mxfp8_dequantize(px, 2 * ex, block) @ mxfp8_dequantize(pw, 0 * ew, block).T"),
     ("fp8_recipes.py", "blockwise weight tiles one row high",
      "ns, ks = _slices(w.shape[0], tile), _slices(w.shape[1], tile)",
      "ns, ks = _slices(w.shape[0], 1), _slices(w.shape[1], tile)"),
